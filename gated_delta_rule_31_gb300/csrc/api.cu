@@ -1,0 +1,184 @@
+// api.cu - the C ABI (include/gdr.h): argument validation, workspace layout and launches.
+// Nothing here allocates device memory; every launch goes to the caller's stream.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "../../include/gdr.h"
+#include "chunk.h"
+#include "kernels.h"
+
+using namespace gdr;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool dim_ok(int d) { return d == 32 || d == 64 || d == 128; }
+
+gdr_status check_problem(const gdr_problem* p, bool decode) {
+    if (!p) return GDR_ERR_INVALID_ARG;
+    if (p->B < 0 || p->T < 0 || p->Hk <= 0 || p->Hv <= 0 || p->Dk <= 0 || p->Dv <= 0) return GDR_ERR_INVALID_ARG;
+    if (p->Hv % p->Hk != 0) return GDR_ERR_INVALID_ARG;
+    if (decode && p->T != 1) return GDR_ERR_INVALID_ARG;
+    if (p->dtype != GDR_F32 && p->dtype != GDR_BF16) return GDR_ERR_INVALID_ARG;
+    if (p->gate != GDR_GATE_SCALAR && p->gate != GDR_GATE_CHANNEL) return GDR_ERR_INVALID_ARG;
+    if (p->use_qk_l2norm != 0 && p->use_qk_l2norm != 1) return GDR_ERR_INVALID_ARG;
+    if (!isfinite(p->scale)) return GDR_ERR_INVALID_ARG;
+    if (!dim_ok(p->Dk) || !dim_ok(p->Dv)) return GDR_ERR_UNSUPPORTED;
+    if (p->B > 65535 || p->Hv > 65535) return GDR_ERR_UNSUPPORTED;  // grid y/z limits
+    return GDR_OK;
+}
+
+gdr_status check_ptrs(std::initializer_list<const void*> required, std::initializer_list<const void*> optional) {
+    for (const void* x : required)
+        if (!x) return GDR_ERR_INVALID_ARG;
+    for (const void* x : required)
+        if (!aligned16(x)) return GDR_ERR_INVALID_ARG;
+    for (const void* x : optional)
+        if (x && !aligned16(x)) return GDR_ERR_INVALID_ARG;
+    return GDR_OK;
+}
+
+// The chunked kernels are written for bf16 operands on the tensor cores, 128-wide heads
+// and the scalar gate.
+gdr_status check_chunked_support(const gdr_problem* p) {
+    if (p->dtype != GDR_BF16 || p->Dk != 128 || p->Dv != 128 || p->gate != GDR_GATE_SCALAR)
+        return GDR_ERR_UNSUPPORTED;
+    return GDR_OK;
+}
+
+RecurrentArgs recurrent_args(const gdr_problem* p, const void* q, const void* k, const void* v, const float* g,
+                             const float* beta, const float* h0, void* o, float* ht) {
+    RecurrentArgs a;
+    a.B = p->B; a.T = p->T; a.Hk = p->Hk; a.Hv = p->Hv; a.Dk = p->Dk; a.Dv = p->Dv;
+    a.channel = p->gate == GDR_GATE_CHANNEL;
+    a.use_norm = p->use_qk_l2norm;
+    a.bf16 = p->dtype == GDR_BF16;
+    a.scale = p->scale;
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.h0 = h0; a.o = o; a.ht = ht;
+    return a;
+}
+
+ChunkProblem chunk_problem(const gdr_problem* p) {
+    ChunkProblem c;
+    c.B = p->B; c.T = p->T; c.Hk = p->Hk; c.Hv = p->Hv;
+    c.NC = (p->T + kChunk - 1) / kChunk;
+    c.scale = p->scale;
+    c.use_norm = p->use_qk_l2norm;
+    return c;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* gdr_status_string(gdr_status s) {
+    switch (s) {
+        case GDR_OK: return "GDR_OK";
+        case GDR_ERR_INVALID_ARG: return "GDR_ERR_INVALID_ARG: invalid argument";
+        case GDR_ERR_UNSUPPORTED: return "GDR_ERR_UNSUPPORTED: combination not implemented";
+        case GDR_ERR_WORKSPACE: return "GDR_ERR_WORKSPACE: workspace too small";
+        case GDR_ERR_CUDA: return "GDR_ERR_CUDA: CUDA launch or runtime error";
+        case GDR_ERR_TIMEOUT: return "GDR_ERR_TIMEOUT: a bounded device wait expired";
+        default: return "unknown gdr_status";
+    }
+}
+
+size_t gdr_fwd_chunked_workspace(const gdr_problem* p) {
+    if (check_problem(p, false) != GDR_OK || check_chunked_support(p) != GDR_OK) return 0;
+    return chunk_fwd_workspace(chunk_problem(p));
+}
+
+size_t gdr_bwd_chunked_workspace(const gdr_problem* p) {
+    if (check_problem(p, false) != GDR_OK || check_chunked_support(p) != GDR_OK) return 0;
+    return chunk_bwd_workspace(chunk_problem(p));
+}
+
+gdr_status gdr_fwd_sequential(const gdr_problem* p, const void* q, const void* k, const void* v, const float* g,
+                              const float* beta, const float* h0, void* o, float* ht, gdr_stream_t stream) {
+    gdr_status s = check_problem(p, false);
+    if (s != GDR_OK) return s;
+    if ((s = check_ptrs({q, k, v, g, beta, o}, {h0, ht})) != GDR_OK) return s;
+    if (p->B == 0) return GDR_OK;
+    RecurrentArgs a = recurrent_args(p, q, k, v, g, beta, h0, o, ht);
+    return launch_recurrent(a, false, (cudaStream_t)stream) == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+}
+
+gdr_status gdr_decode_step(const gdr_problem* p, const void* q, const void* k, const void* v, const float* g,
+                           const float* beta, float* state, void* o, gdr_stream_t stream) {
+    gdr_status s = check_problem(p, true);
+    if (s != GDR_OK) return s;
+    if ((s = check_ptrs({q, k, v, g, beta, state, o}, {})) != GDR_OK) return s;
+    if (p->B == 0) return GDR_OK;
+    RecurrentArgs a = recurrent_args(p, q, k, v, g, beta, state, o, state);
+    return launch_recurrent(a, true, (cudaStream_t)stream) == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+}
+
+gdr_status gdr_fwd_chunked(const gdr_problem* p, const void* q, const void* k, const void* v, const float* g,
+                           const float* beta, const float* h0, void* o, float* ht, void* ws, size_t ws_bytes,
+                           gdr_stream_t stream) {
+    gdr_status s = check_problem(p, false);
+    if (s != GDR_OK) return s;
+    if ((s = check_ptrs({q, k, v, g, beta, o}, {h0, ht})) != GDR_OK) return s;
+    if ((s = check_chunked_support(p)) != GDR_OK) return s;
+    const size_t need = chunk_fwd_workspace(chunk_problem(p));
+    if (!ws || ws_bytes < need) return GDR_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return GDR_ERR_INVALID_ARG;
+    if (p->B == 0) return GDR_OK;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cudaMemsetAsync(ws, 0, 256, st) != cudaSuccess) return GDR_ERR_CUDA;
+    if (p->T == 0) {  // no token: ht = h0 (or zero)
+        if (!ht) return GDR_OK;
+        RecurrentArgs a = recurrent_args(p, q, k, v, g, beta, h0, o, ht);
+        return launch_recurrent(a, false, st) == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+    }
+    ChunkFwdArgs a;
+    a.p = chunk_problem(p);
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.h0 = h0; a.o = o; a.ht = ht;
+    a.ws = ws;
+    return launch_chunk_fwd(a, st) == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+}
+
+gdr_status gdr_bwd_chunked(const gdr_problem* p, const void* q, const void* k, const void* v, const float* g,
+                           const float* beta, const float* h0, const void* do_, const float* dht, float* dq,
+                           float* dk, float* dv, float* dg, float* dbeta, float* dh0, void* ws, size_t ws_bytes,
+                           gdr_stream_t stream) {
+    gdr_status s = check_problem(p, false);
+    if (s != GDR_OK) return s;
+    if ((s = check_ptrs({q, k, v, g, beta, do_, dq, dk, dv, dg, dbeta}, {h0, dht, dh0})) != GDR_OK) return s;
+    if ((s = check_chunked_support(p)) != GDR_OK) return s;
+    const size_t need = chunk_bwd_workspace(chunk_problem(p));
+    if (!ws || ws_bytes < need) return GDR_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return GDR_ERR_INVALID_ARG;
+    if (p->B == 0) return GDR_OK;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cudaMemsetAsync(ws, 0, 256, st) != cudaSuccess) return GDR_ERR_CUDA;
+    if (p->T == 0) {  // no token: dh0 = dht (or zero)
+        if (!dh0) return GDR_OK;
+        const size_t bytes = (size_t)p->B * p->Hv * p->Dv * p->Dk * sizeof(float);
+        cudaError_t e = dht ? cudaMemcpyAsync(dh0, dht, bytes, cudaMemcpyDeviceToDevice, st)
+                            : cudaMemsetAsync(dh0, 0, bytes, st);
+        return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+    }
+    ChunkBwdArgs a;
+    a.p = chunk_problem(p);
+    a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.h0 = h0; a.do_ = do_; a.dht = dht;
+    a.dq = dq; a.dk = dk; a.dv = dv; a.dg = dg; a.dbeta = dbeta; a.dh0 = dh0;
+    a.ws = ws;
+    return launch_chunk_bwd(a, st) == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+}
+
+gdr_status gdr_workspace_status(void* ws, size_t ws_bytes, gdr_stream_t stream) {
+    if (!ws || ws_bytes < 256) return GDR_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    int word[4] = {0, 0, 0, 0};
+    if (cudaMemcpyAsync(word, ws, sizeof(word), cudaMemcpyDeviceToHost, st) != cudaSuccess) return GDR_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return GDR_ERR_CUDA;
+    if (word[0] == 0) return GDR_OK;
+    if (cudaMemsetAsync(ws, 0, 256, st) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess)
+        return GDR_ERR_CUDA;
+    return word[0] == GDR_ERR_TIMEOUT ? GDR_ERR_TIMEOUT : GDR_ERR_CUDA;
+}
+
+}  // extern "C"

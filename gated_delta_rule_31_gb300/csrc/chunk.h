@@ -1,0 +1,123 @@
+// chunk.h - chunked (C = 64) gated delta rule on the tensor cores: launch interfaces and
+// the workspace layout shared by the forward and backward launches.
+//
+// Chunk algebra (derived from the recurrence; H = S^T is the Dk x Dv state, rows r of a
+// chunk are its tokens, gamma_r the in-chunk cumulative log-decay, E_rj = exp(gamma_r -
+// gamma_j), Gamma_r = exp(gamma_r), b_r = exp(gamma_C - gamma_r), k^ = rho_k k):
+//   A  = strict_lower(diag(beta) (E .* K^K^T)),   T = (I + A)^-1
+//   W  = T diag(beta Gamma) K^,   U~ = T diag(beta) V,   P = scale tril(E .* Q^K^T)
+//   U  = U~ - W H0;   O = scale diag(Gamma) Q^ H0 + P U;   H1 = Gamma_C H0 + K^T diag(b) U
+// Folding W into the per-chunk operators removes one dependent product from the scan:
+//   H1 = Gamma_C H0 + Mneg H0 + Kbar^T U~      with Mneg = -Kbar^T W, Kbar = diag(b) K^
+//   O  = Qc H0 + P U~                          with Qc = scale diag(Gamma) Q^ - P W
+//   dH0 = Gamma_C dH1 + Mneg^T dH1 + Qc^T dO   (the backward scan)
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace gdr {
+
+constexpr int kChunk = 64;
+constexpr int kD = 128;        // Dk = Dv handled by the tensor-core path
+constexpr int kSlice = 32;     // Dv columns of the state owned by one scan CTA
+constexpr int kSlices = kD / kSlice;
+
+// Per-(b, hv, chunk) record written by the prep kernel, as shared-memory images
+// (panelised SW128 tiles unless noted) so the scans fetch them with plain bulk copies.
+constexpr uint32_t REC_M = 0;            // Mneg  [128 d  x 128 d']  32 KB
+constexpr uint32_t REC_K = 32768;        // Kbar  [64 tok x 128 d]   16 KB
+constexpr uint32_t REC_Q = 49152;        // Qc    [64 tok x 128 d]   16 KB
+constexpr uint32_t REC_P = 65536;        // P     [64 tok x 64 tok]   8 KB
+constexpr uint32_t REC_U = 73728;        // U~    4 x [64 tok x 32] SW64 slices, 4 KB each
+constexpr uint32_t REC_BYTES = 90112;
+constexpr uint32_t STATE_IMG = 32768;    // one bf16 [128 d x 128 v] SW128 state image
+
+struct ChunkProblem {
+    int B, T, Hk, Hv, NC;
+    float scale;
+    int use_norm;
+};
+
+struct WsLayout {
+    size_t gam;      // float [B*Hv][ncpad]: Gamma_C per chunk
+    size_t rec;      // records [B*Hv][NC]
+    size_t hs;       // bwd: chunk-start states [B*Hv][NC] images
+    size_t dhs;      // bwd: chunk-end state gradients [B*Hv][NC] images
+    size_t total;
+    int ncpad;
+};
+
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline WsLayout ws_layout(const ChunkProblem& p, bool bwd) {
+    WsLayout w;
+    w.ncpad = (int)round_up((size_t)p.NC, 4);
+    size_t nh = (size_t)p.B * p.Hv;
+    w.gam = 256;
+    w.rec = round_up(w.gam + nh * w.ncpad * sizeof(float), 1024);
+    size_t end = w.rec + nh * p.NC * (size_t)REC_BYTES;
+    w.hs = w.dhs = 0;
+    if (bwd) {
+        w.hs = end;
+        w.dhs = w.hs + nh * p.NC * (size_t)STATE_IMG;
+        end = w.dhs + nh * p.NC * (size_t)STATE_IMG;
+    }
+    w.total = end;
+    return w;
+}
+inline size_t chunk_fwd_workspace(const ChunkProblem& p) { return ws_layout(p, false).total; }
+inline size_t chunk_bwd_workspace(const ChunkProblem& p) { return ws_layout(p, true).total; }
+
+struct ChunkFwdArgs {
+    ChunkProblem p;
+    const void *q, *k, *v;
+    const float *g, *beta, *h0;
+    void* o;
+    float* ht;
+    void* ws;
+};
+struct ChunkBwdArgs {
+    ChunkProblem p;
+    const void *q, *k, *v;
+    const float *g, *beta, *h0;
+    const void* do_;
+    const float* dht;
+    float *dq, *dk, *dv, *dg, *dbeta, *dh0;
+    void* ws;
+};
+
+cudaError_t launch_chunk_fwd(const ChunkFwdArgs& a, cudaStream_t s);
+cudaError_t launch_chunk_bwd(const ChunkBwdArgs& a, cudaStream_t s);
+
+// Pieces shared by the forward and backward launches (chunk_fwd.cu).
+struct PrepArgs {
+    ChunkProblem p;
+    const float *g, *beta;
+    float* gam;
+    uint8_t* rec;
+    int* status;
+    int ncpad;
+};
+cudaError_t launch_prep(const PrepArgs& a, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                        cudaStream_t s);
+
+enum ScanMode : int { SCAN_FWD_OUT = 0, SCAN_FWD_STATES = 1, SCAN_BWD = 2 };
+struct ScanArgs {
+    ChunkProblem p;
+    const float* gam;
+    const uint8_t* rec;
+    const float* hinit;   // h0 (forward) or dht (backward); may be null
+    void* o;              // forward output
+    float* hfinal;        // ht (forward) or dh0 (backward); may be null
+    uint8_t* states;      // per-chunk state images (SCAN_FWD_STATES / SCAN_BWD)
+    int* status;
+    int ncpad;
+};
+cudaError_t launch_scan(const ScanArgs& a, int mode, const CUtensorMap* mdo, cudaStream_t s);
+
+bool make_qkv_maps(const ChunkProblem& p, const void* q, const void* k, const void* v, CUtensorMap* mq,
+                   CUtensorMap* mk, CUtensorMap* mv);
+
+}  // namespace gdr

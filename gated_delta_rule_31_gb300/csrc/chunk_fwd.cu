@@ -1,0 +1,656 @@
+// chunk_fwd.cu - tensor-core chunked gated delta rule (chunks of 64 tokens, Dk = Dv = 128):
+//   prep_kernel : one CTA per (b, v-head, chunk), all chunks in parallel. Builds the
+//                 chunk's operators (UT/WY transform of the k k^T beta block, output and
+//                 state operators) on tcgen05 with TMEM accumulators and writes them as
+//                 ready-to-use shared-memory images.
+//   scan_kernel : one CTA per (b, v-head, 32-column slice of the state). Runs the chunks
+//                 in order (or in reverse for the backward) with the fp32 state slice in
+//                 registers; per chunk one dependent tensor-core product.
+// The algebra is stated in chunk.h. The chunked prefill and its backward are the
+// "chunked case" of "Adding VJP for gated delta net" (MLX PR #4565); the q/k L2 norm is
+// applied inside ("fold q/k L2-norm into the gated_delta_rule kernel", eps 1e-6) as an
+// fp32 factor on the raw bf16 operands, so normalised q/k are never rounded.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "chunk.h"
+#include "common.cuh"
+#include "tma_host.h"
+
+namespace gdr {
+
+// ================================================================== prep kernel
+// Shared memory (offsets from a 1024-aligned base).
+constexpr uint32_t PS_KQV = 0;                    // k rows 0-63 / q rows 64-127 of a 128-row tile
+                                                  // (panels at 0, 16K); v panels at 32K, 48K
+constexpr uint32_t PS_REC = 65536;                // record staging, REC_* layout (88 KB)
+constexpr uint32_t PS_TT = PS_REC + REC_BYTES;    // [Tw; Tu] 128 x 64 bf16, one panel (16 KB)
+constexpr uint32_t PS_AT = PS_TT + 16384;         // A, T fp32 [64][65] each; later Wbar, W images
+constexpr int LDA = 65;
+constexpr uint32_t PS_SCR = PS_AT + 2 * 64 * LDA * 4;   // solve scratch [3][16][17] fp32
+constexpr uint32_t PS_SMALL = PS_SCR + 3 * 16 * 17 * 4;  // gamma[64], beta[64], rho[128]
+constexpr uint32_t PS_BYTES = PS_SMALL + 1024;
+constexpr uint32_t PS_WBAR = PS_AT;               // [64 tok x 128 d] images (alias A/T)
+constexpr uint32_t PS_W = PS_AT + 16384;
+static_assert(PS_KQV % 1024 == 0 && PS_REC % 1024 == 0 && PS_TT % 1024 == 0 && PS_AT % 1024 == 0, "align");
+static_assert(PS_BYTES + 1024 <= 232448, "prep smem");
+
+__device__ __forceinline__ void unpack8(const uint4& u, float* x) {
+    x[0] = bf16lo(u.x); x[1] = bf16hi(u.x); x[2] = bf16lo(u.y); x[3] = bf16hi(u.y);
+    x[4] = bf16lo(u.z); x[5] = bf16hi(u.z); x[6] = bf16lo(u.w); x[7] = bf16hi(u.w);
+}
+__device__ __forceinline__ void st_chunk(uint32_t addr, const float* x, float s) {
+    st_shared_v4(addr, pack_bf16(s * x[0], s * x[1]), pack_bf16(s * x[2], s * x[3]), pack_bf16(s * x[4], s * x[5]),
+                 pack_bf16(s * x[6], s * x[7]));
+}
+
+__global__ void __launch_bounds__(256, 1)
+    prep_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                const __grid_constant__ CUtensorMap mv, PrepArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = align1024(smem_raw);
+    const uint32_t sb = smem_u32(sm);
+    __shared__ uint64_t bar_tma, bar_mma;
+    __shared__ uint32_t tmem_sh;
+    __shared__ int abort_sh;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = blockIdx.x, hv = blockIdx.y, b = blockIdx.z;
+    const ChunkProblem& P = a.p;
+    const int hk = hv / (P.Hv / P.Hk);
+    const int t0 = c * kChunk;
+    float* gam = reinterpret_cast<float*>(sm + PS_SMALL);  // in-chunk cumulative log-decay
+    float* bet = gam + 64;
+    float* rho = bet + 64;  // rows 0-63: k norm factors, 64-127: q norm factors
+    float* Am = reinterpret_cast<float*>(sm + PS_AT);
+    float* Tm = Am + 64 * LDA;
+    float* Xs = reinterpret_cast<float*>(sm + PS_SCR);
+
+    if (tid == 0) {
+        abort_sh = 0;
+        mbar_init(&bar_tma, 1);
+        mbar_init(&bar_mma, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&tmem_sh, 256);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = tmem_sh;
+    if (tid == 0) {
+        mbar_expect_tx(&bar_tma, 6 * 8192);
+        tma_load_4d(sm + PS_KQV + 0, &mk, 0, hk, t0, b, &bar_tma);
+        tma_load_4d(sm + PS_KQV + 16384, &mk, 64, hk, t0, b, &bar_tma);
+        tma_load_4d(sm + PS_KQV + 8192, &mq, 0, hk, t0, b, &bar_tma);
+        tma_load_4d(sm + PS_KQV + 24576, &mq, 64, hk, t0, b, &bar_tma);
+        tma_load_4d(sm + PS_KQV + 32768, &mv, 0, hv, t0, b, &bar_tma);
+        tma_load_4d(sm + PS_KQV + 49152, &mv, 64, hv, t0, b, &bar_tma);
+    }
+    // gates of the chunk; tokens past T act as g = 0, beta = 0 (state passes unchanged)
+    if (tid < 64) {
+        const int t = t0 + tid;
+        float gv = 0.f, bv = 0.f;
+        if (t < P.T) {
+            const size_t bt = ((size_t)b * P.T + t) * P.Hv + hv;
+            gv = a.g[bt];
+            bv = a.beta[bt];
+        }
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, gv, o);
+            if (lane >= o) gv += y;
+        }
+        gam[tid] = gv;
+        bet[tid] = bv;
+    }
+    __syncthreads();
+    if (tid >= 32 && tid < 64) gam[tid] += gam[31];
+    bool ok = mbar_wait(&bar_tma, 0, &abort_sh, a.status, 10);
+    if (__syncthreads_or(!ok)) goto teardown;
+
+    {  // L2 norm factors of the 64 keys (rows 0-63) and 64 queries (rows 64-127)
+        const int row = tid >> 1, half = tid & 1;
+        const uint32_t base = sb + PS_KQV + half * 16384 + row * 128;
+        float ss = 0.f;
+#pragma unroll
+        for (int ch = 0; ch < 8; ch++) {
+            float x[8];
+            unpack8(ld_shared_v4(base + ch * 16), x);
+#pragma unroll
+            for (int e = 0; e < 8; e++) ss += x[e] * x[e];
+        }
+        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+        if (half == 0) rho[row] = P.use_norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
+    }
+    __syncthreads();
+
+    // G = K K^T (rows 0-63) and Q K^T (rows 64-127) in one M=128 product, raw bf16 operands
+    if (tid == 0) {
+        tc_fence_after();
+        const uint32_t id = idesc_bf16(128, 64, 0, 0);
+        for (int k0 = 0; k0 < kD; k0 += 16)
+            mma_bf16(tm, desc_kmajor(sb + PS_KQV, 128, 0, k0), desc_kmajor(sb + PS_KQV, 128, 0, k0), id,
+                     k0 > 0);
+        mma_commit(&bar_mma);
+    }
+    ok = mbar_wait(&bar_mma, 0, &abort_sh, a.status, 11);
+    if (__syncthreads_or(!ok)) goto teardown;
+    tc_fence_after();
+    {  // A = strict_lower(beta_i rho_i rho_j E_ij G_ij) in fp32;  P = scale tril(rho rho E S) in bf16
+        const int lg = warp & 3, h = warp >> 2;
+        const int r = 32 * lg + lane;
+        float v[32];
+        tmem_ld32(tmem_at(tm, 32 * lg, 32 * h), v);
+        tmem_wait_ld();
+        if (r < 64) {
+            const int i = r;
+            const float gi = gam[i], ci = bet[i] * rho[i];
+#pragma unroll
+            for (int jj = 0; jj < 32; jj++) {
+                const int j = 32 * h + jj;
+                Am[i * LDA + j] = (j < i) ? ci * rho[j] * expf(gi - gam[j]) * v[jj] : 0.f;
+            }
+        } else {
+            const int i = r - 64;
+            const float gi = gam[i], ci = P.scale * rho[64 + i];
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                float x[8];
+#pragma unroll
+                for (int e = 0; e < 8; e++) {
+                    const int j = 32 * h + 8 * q + e;
+                    x[e] = (j <= i) ? ci * rho[j] * expf(gi - gam[j]) * v[8 * q + e] : 0.f;
+                }
+                st_chunk(sb + PS_REC + REC_P + sw128_chunk(i, 4 * h + q, 64), x, 1.f);
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+
+    // T = (I + A)^-1, unit lower triangular: 16x16 diagonal blocks by forward substitution,
+    // then the off-diagonal blocks T_IJ = -T_II sum_{J<=K<I} A_IK T_KJ by distance I-J.
+    for (int idx = tid; idx < 64 * 64; idx += 256) {
+        const int i = idx >> 6, j = idx & 63;
+        if ((i >> 4) < (j >> 4)) Tm[i * LDA + j] = 0.f;
+    }
+    if (tid < 64) {
+        const int I = tid >> 4, cc = tid & 15;
+        const float* Ab = Am + (16 * I) * LDA + 16 * I;
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 16; i++) {
+            float s = 0.f;
+#pragma unroll
+            for (int j = 0; j < i; j++) s += Ab[i * LDA + j] * x[j];
+            x[i] = (i < cc) ? 0.f : ((i == cc) ? 1.f : -s);
+        }
+#pragma unroll
+        for (int i = 0; i < 16; i++) Tm[(16 * I + i) * LDA + 16 * I + cc] = x[i];
+    }
+    __syncthreads();
+    for (int dlev = 1; dlev <= 3; dlev++) {
+        const int nb = 4 - dlev;
+        for (int o = tid; o < nb * 256; o += 256) {
+            const int blk = o >> 8, i = (o >> 4) & 15, cc = o & 15;
+            const int J = blk, I = blk + dlev;
+            float s = 0.f;
+            for (int K = J; K < I; K++) {
+                const float* ar = Am + (16 * I + i) * LDA + 16 * K;
+                const float* tc = Tm + (16 * K) * LDA + 16 * J + cc;
+#pragma unroll
+                for (int m = 0; m < 16; m++) s += ar[m] * tc[m * LDA];
+            }
+            Xs[(blk * 16 + i) * 17 + cc] = s;
+        }
+        __syncthreads();
+        for (int o = tid; o < nb * 256; o += 256) {
+            const int blk = o >> 8, i = (o >> 4) & 15, cc = o & 15;
+            const int J = blk, I = blk + dlev;
+            const float* tr = Tm + (16 * I + i) * LDA + 16 * I;
+            float s = 0.f;
+#pragma unroll
+            for (int m = 0; m < 16; m++) s += tr[m] * Xs[(blk * 16 + m) * 17 + cc];
+            Tm[(16 * I + i) * LDA + 16 * J + cc] = -s;
+        }
+        __syncthreads();
+    }
+    {  // [Tw; Tu] with Tw = T diag(beta Gamma rho_k), Tu = T diag(beta): K-major A operand
+        const int row = tid >> 1, half = tid & 1;
+        const int i = row & 63;
+        const bool isw = row < 64;
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; e++) {
+                const int j = 32 * half + 8 * q + e;
+                const float sj = isw ? bet[j] * expf(gam[j]) * rho[j] : bet[j];
+                x[e] = Tm[i * LDA + j] * sj;
+            }
+            st_chunk(sb + PS_TT + sw128_chunk(row, 4 * half + q, 128), x, 1.f);
+        }
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+
+    // W = Tw K and U~ = Tu V (M=64 each; B operands are the raw k / v tiles, MN-major)
+    if (tid == 0) {
+        tc_fence_after();
+        const uint32_t id = idesc_bf16(64, 128, 0, 1);
+        for (int k0 = 0; k0 < kChunk; k0 += 16) {
+            mma_bf16(tm + 128, desc_kmajor(sb + PS_TT, 128, 0, k0), desc_mnmajor(sb + PS_KQV, 128, 0, k0), id,
+                     k0 > 0);
+            mma_bf16(tm + 0, desc_kmajor(sb + PS_TT, 128, 64, k0),
+                     desc_mnmajor(sb + PS_KQV + 32768, 128, 0, k0), id, k0 > 0);
+        }
+        mma_commit(&bar_mma);
+    }
+    ok = mbar_wait(&bar_mma, 1, &abort_sh, a.status, 12);
+    if (__syncthreads_or(!ok)) goto teardown;
+    tc_fence_after();
+    {
+        const float gC = gam[63];
+        const int lg = warp & 3, h = warp >> 2;
+        const int i = 16 * lg + (lane & 15);  // M=64 accumulator rows: 16 per TMEM sub-partition
+        float w[64];
+        tmem_ld32(tmem_at(tm, 32 * lg, 128 + 64 * h), w);
+        tmem_ld32(tmem_at(tm, 32 * lg, 128 + 64 * h + 32), w + 32);
+        tmem_wait_ld();
+        if (lane < 16) {
+            const float sbar = expf(gC - gam[i]) * rho[i];
+#pragma unroll
+            for (int q = 0; q < 8; q++) {
+                st_chunk(sb + PS_W + sw128_chunk(i, 8 * h + q, 64), w + 8 * q, 1.f);
+                st_chunk(sb + PS_WBAR + sw128_chunk(i, 8 * h + q, 64), w + 8 * q, sbar);
+            }
+        }
+        float u[64];
+        tmem_ld32(tmem_at(tm, 32 * lg, 64 * h), u);
+        tmem_ld32(tmem_at(tm, 32 * lg, 64 * h + 32), u + 32);
+        tmem_wait_ld();
+        if (lane < 16) {
+#pragma unroll
+            for (int q = 0; q < 8; q++) {
+                const int col = 64 * h + 8 * q;
+                st_chunk(sb + PS_REC + REC_U + (col >> 5) * 4096 + sw64_chunk(i, q & 3), u + 8 * q, 1.f);
+            }
+        }
+        // Kbar = diag(exp(gamma_C - gamma) rho_k) K
+        for (int idx = tid; idx < 64 * 16; idx += 256) {
+            const int r = idx >> 4, j = idx & 15;
+            float x[8];
+            unpack8(ld_shared_v4(sb + PS_KQV + sw128_chunk(r, j, 128)), x);
+            st_chunk(sb + PS_REC + REC_K + sw128_chunk(r, j, 64), x, expf(gC - gam[r]) * rho[r]);
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+
+    // Mneg = -K^T Wbar (M=128: A = k tile read MN-major) and P W (M=64)
+    if (tid == 0) {
+        tc_fence_after();
+        const uint32_t idm = idesc_bf16(128, 128, 1, 1);
+        for (int k0 = 0; k0 < kChunk; k0 += 16)
+            mma_bf16(tm + 0, desc_mnmajor(sb + PS_KQV, 128, 0, k0), desc_mnmajor(sb + PS_WBAR, 64, 0, k0), idm,
+                     k0 > 0);
+        const uint32_t idp = idesc_bf16(64, 128, 0, 1);
+        for (int k0 = 0; k0 < kChunk; k0 += 16)
+            mma_bf16(tm + 128, desc_kmajor(sb + PS_REC + REC_P, 64, 0, k0), desc_mnmajor(sb + PS_W, 64, 0, k0),
+                     idp, k0 > 0);
+        mma_commit(&bar_mma);
+    }
+    ok = mbar_wait(&bar_mma, 0, &abort_sh, a.status, 13);
+    if (__syncthreads_or(!ok)) goto teardown;
+    tc_fence_after();
+    {
+        const int lg = warp & 3, h = warp >> 2;
+        {  // Mneg rows d = 32 lg + lane
+            const int d = 32 * lg + lane;
+            float m[64];
+            tmem_ld32(tmem_at(tm, 32 * lg, 64 * h), m);
+            tmem_ld32(tmem_at(tm, 32 * lg, 64 * h + 32), m + 32);
+            tmem_wait_ld();
+#pragma unroll
+            for (int q = 0; q < 8; q++) st_chunk(sb + PS_REC + REC_M + sw128_chunk(d, 8 * h + q, 128), m + 8 * q, -1.f);
+        }
+        {  // Qc = scale diag(Gamma rho_q) Q - P W, rows i = 16 lg + lane
+            const int i = 16 * lg + (lane & 15);
+            float pw[64];
+            tmem_ld32(tmem_at(tm, 32 * lg, 128 + 64 * h), pw);
+            tmem_ld32(tmem_at(tm, 32 * lg, 128 + 64 * h + 32), pw + 32);
+            tmem_wait_ld();
+            if (lane < 16) {
+                const float f = P.scale * expf(gam[i]) * rho[64 + i];
+#pragma unroll
+                for (int q = 0; q < 8; q++) {
+                    float x[8];
+                    unpack8(ld_shared_v4(sb + PS_KQV + sw128_chunk(64 + i, 8 * h + q, 128)), x);
+#pragma unroll
+                    for (int e = 0; e < 8; e++) x[e] = f * x[e] - pw[8 * q + e];
+                    st_chunk(sb + PS_REC + REC_Q + sw128_chunk(i, 8 * h + q, 64), x, 1.f);
+                }
+            }
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+        const size_t bh = (size_t)b * P.Hv + hv;
+        bulk_store(a.rec + (bh * P.NC + c) * REC_BYTES, sm + PS_REC, REC_BYTES);
+        bulk_commit();
+        a.gam[bh * a.ncpad + c] = expf(gam[63]);
+        bulk_wait_all();
+    }
+teardown:
+    tc_fence_before();
+    __syncthreads();
+    if (abort_sh && tid == 0) {  // let copies still in flight land before the CTA exits
+        uint32_t dummy = 0;
+        volatile int never = 0;
+        mbar_wait(&bar_tma, 0, &never, nullptr, 0);
+        (void)dummy;
+    }
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tm, 256);
+}
+
+cudaError_t launch_prep(const PrepArgs& a, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                        cudaStream_t s) {
+    const int smem = PS_BYTES + 1024;
+    cudaError_t e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(a.p.NC, a.p.Hv, a.p.B);
+    prep_kernel<<<grid, 256, smem, s>>>(mq, mk, mv, a);
+    return cudaGetLastError();
+}
+
+// ================================================================== scan kernel
+// Per stage (one chunk): Mneg 32 KB | Kbar or Qc^T source 16 KB | Qc 16 KB | P 8 KB | U~ / dO slice 4 KB.
+constexpr uint32_t ST_M = 0, ST_K = 32768, ST_Q = 49152, ST_P = 65536, ST_U = 73728;
+constexpr uint32_t STG = 78848;                  // 77 KB, 1024-aligned stages
+constexpr uint32_t SS_H = 2 * STG;               // two bf16 [128 x 32] SW64 state tiles (8 KB each)
+constexpr uint32_t SS_BYTES = SS_H + 16384;
+static_assert(SS_BYTES + 1024 <= 232448, "scan smem");
+
+__device__ __forceinline__ void write_state_tile(uint32_t tile, int d, const float* H) {
+#pragma unroll
+    for (int q = 0; q < 4; q++)
+        st_shared_v4(tile + sw64_chunk(d, q), pack_bf16(H[8 * q], H[8 * q + 1]), pack_bf16(H[8 * q + 2], H[8 * q + 3]),
+                     pack_bf16(H[8 * q + 4], H[8 * q + 5]), pack_bf16(H[8 * q + 6], H[8 * q + 7]));
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(192, 1) scan_kernel(const __grid_constant__ CUtensorMap mdo, ScanArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = align1024(smem_raw);
+    const uint32_t sb = smem_u32(sm);
+    __shared__ uint64_t full[2], empty[2], hready, sfull, ofull[2], drain;
+    __shared__ uint32_t tmem_sh;
+    __shared__ int abort_sh;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int j = blockIdx.x, hv = blockIdx.y, b = blockIdx.z;
+    const ChunkProblem& P = a.p;
+    const int NC = P.NC;
+    const size_t bh = (size_t)b * P.Hv + hv;
+    auto chunk_of = [&](int i) { return MODE == SCAN_BWD ? NC - 1 - i : i; };
+
+    if (tid == 0) {
+        abort_sh = 0;
+        for (int s = 0; s < 2; s++) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+            mbar_init(&ofull[s], 1);
+        }
+        mbar_init(&hready, 1);
+        mbar_init(&sfull, 1);
+        mbar_init(&drain, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&tmem_sh, 128);  // Ds[0..1] cols 0-63, Do[0..1] cols 64-127
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = tmem_sh;
+    int last_loaded = -1;
+
+    if (warp == 0) {
+        if (lane == 0) {  // producer: bulk copies of the chunk records (+ dO slice via TMA)
+            for (int i = 0; i < NC; i++) {
+                const int c = chunk_of(i), s = i & 1;
+                if (i >= 2 && !mbar_wait(&empty[s], ((i >> 1) + 1) & 1, &abort_sh, a.status, 20)) break;
+                uint8_t* st = sm + s * STG;
+                const uint8_t* rec = a.rec + (bh * NC + c) * REC_BYTES;
+                uint32_t bytes = 32768 + 4096 + 16384;
+                if (MODE == SCAN_FWD_OUT) bytes += 16384 + 8192;
+                mbar_expect_tx(&full[s], bytes);
+                bulk_load(st + ST_M, rec + REC_M, 32768, &full[s]);
+                if (MODE != SCAN_BWD) {
+                    bulk_load(st + ST_K, rec + REC_K, 16384, &full[s]);
+                    bulk_load(st + ST_U, rec + REC_U + j * 4096, 4096, &full[s]);
+                }
+                if (MODE == SCAN_FWD_OUT) {
+                    bulk_load(st + ST_Q, rec + REC_Q, 16384, &full[s]);
+                    bulk_load(st + ST_P, rec + REC_P, 8192, &full[s]);
+                }
+                if (MODE == SCAN_BWD) {
+                    bulk_load(st + ST_Q, rec + REC_Q, 16384, &full[s]);
+                    tma_load_4d(st + ST_U, &mdo, kSlice * j, hv, kChunk * c, b, &full[s]);
+                }
+                last_loaded = i;
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {  // MMA issuer
+            const uint32_t id_state = MODE == SCAN_BWD ? idesc_bf16(128, 32, 1, 1) : idesc_bf16(128, 32, 0, 1);
+            const uint32_t id_pre = idesc_bf16(128, 32, 1, 1);
+            const uint32_t id_out = idesc_bf16(64, 32, 0, 1);
+            auto issue_pre = [&](int i) {  // state-independent term into Ds[i & 1]
+                const uint32_t st = sb + (i & 1) * STG;
+                const uint32_t src = MODE == SCAN_BWD ? st + ST_Q : st + ST_K;  // Qc^T dO  or  Kbar^T U~
+                for (int k0 = 0; k0 < kChunk; k0 += 16)
+                    mma_bf16(tm + 32 * (i & 1), desc_mnmajor(src, 64, 0, k0), desc_mnmajor_sw64(st + ST_U, 64, k0),
+                             id_pre, k0 > 0);
+            };
+            for (int i = 0; i < NC; i++) {
+                const int s = i & 1;
+                const uint32_t st = sb + s * STG;
+                if (i == 0) {
+                    if (!mbar_wait(&full[0], 0, &abort_sh, a.status, 21)) break;
+                    tc_fence_after();
+                    issue_pre(0);
+                }
+                if (!mbar_wait(&hready, i & 1, &abort_sh, a.status, 22)) break;
+                tc_fence_after();
+                const uint32_t ht = sb + SS_H + (i & 1) * 8192;
+                for (int k0 = 0; k0 < kD; k0 += 16) {
+                    const uint64_t ad =
+                        MODE == SCAN_BWD ? desc_mnmajor(st + ST_M, 128, 0, k0) : desc_kmajor(st + ST_M, 128, 0, k0);
+                    mma_bf16(tm + 32 * s, ad, desc_mnmajor_sw64(ht, 128, k0), id_state, 1);
+                }
+                mma_commit(&sfull);
+                if (MODE == SCAN_FWD_OUT) {
+                    for (int k0 = 0; k0 < kD; k0 += 16)
+                        mma_bf16(tm + 64 + 32 * s, desc_kmajor(st + ST_Q, 64, 0, k0), desc_mnmajor_sw64(ht, 128, k0),
+                                 id_out, k0 > 0);
+                    for (int k0 = 0; k0 < kChunk; k0 += 16)
+                        mma_bf16(tm + 64 + 32 * s, desc_kmajor(st + ST_P, 64, 0, k0),
+                                 desc_mnmajor_sw64(st + ST_U, 64, k0), id_out, 1);
+                    mma_commit(&ofull[s]);
+                }
+                mma_commit(&empty[s]);
+                if (i + 1 < NC) {
+                    if (!mbar_wait(&full[s ^ 1], ((i + 1) >> 1) & 1, &abort_sh, a.status, 23)) break;
+                    tc_fence_after();
+                    issue_pre(i + 1);
+                }
+            }
+            // every product issued so far has completed before TMEM is released
+            mma_commit(&drain);
+            volatile int never = 0;
+            mbar_wait(&drain, 0, &never, nullptr, 0);
+        }
+    } else {  // epilogue: 4 warps, thread <-> TMEM lane d = state row (key channel)
+        const int et = tid - 64;
+        const int lg = warp & 3;
+        const int d = 32 * lg + lane;
+        float H[32];
+#pragma unroll
+        for (int n = 0; n < 32; n++)
+            H[n] = a.hinit ? a.hinit[(bh * kD + kSlice * j + n) * kD + d] : 0.f;
+        write_state_tile(sb + SS_H, d, H);
+        fence_proxy_async_smem();
+        bool bad = bar_sync_or(1, 128, false);
+        if (et == 0) mbar_arrive(&hready);
+        const float* gam = a.gam + bh * a.ncpad;
+        float gnext = gam[chunk_of(0)];
+        int i = 0;
+        for (; i < NC && !bad; i++) {
+            const int c = chunk_of(i), s = i & 1;
+            const float gC = gnext;
+            if (i + 1 < NC) gnext = gam[chunk_of(i + 1)];
+            if (MODE != SCAN_FWD_OUT) {  // state entering this step, as an SW128 [128 x 128] image
+                uint8_t* img = a.states + (bh * NC + c) * (size_t)STATE_IMG;
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    uint4 v = make_uint4(pack_bf16(H[8 * q], H[8 * q + 1]), pack_bf16(H[8 * q + 2], H[8 * q + 3]),
+                                         pack_bf16(H[8 * q + 4], H[8 * q + 5]), pack_bf16(H[8 * q + 6], H[8 * q + 7]));
+                    *reinterpret_cast<uint4*>(img + sw128_chunk(d, 4 * j + q, 128)) = v;
+                }
+            }
+            bool ok = __all_sync(0xffffffffu, mbar_wait(&sfull, i & 1, &abort_sh, a.status, 30));
+            tc_fence_after();
+            float D[32], O[32];
+            if (ok) tmem_ld32(tmem_at(tm, 32 * lg, 32 * s), D);
+            if (MODE == SCAN_FWD_OUT && i > 0 && ok) {
+                ok = __all_sync(0xffffffffu, mbar_wait(&ofull[(i - 1) & 1], ((i - 1) >> 1) & 1, &abort_sh, a.status, 31));
+                tc_fence_after();
+                if (ok) tmem_ld32(tmem_at(tm, 32 * lg, 64 + 32 * ((i - 1) & 1)), O);
+            }
+            tmem_wait_ld();
+#pragma unroll
+            for (int n = 0; n < 32; n++) H[n] = gC * H[n] + D[n];
+            if (i + 1 < NC) {
+                write_state_tile(sb + SS_H + ((i + 1) & 1) * 8192, d, H);
+                fence_proxy_async_smem();
+            }
+            tc_fence_before();
+            bad = bar_sync_or(1, 128, !ok || abort_sh);
+            if (bad) break;
+            if (i + 1 < NC && et == 0) mbar_arrive(&hready);
+            if (MODE == SCAN_FWD_OUT && i > 0 && lane < 16) {  // output rows of chunk c-1
+                const int r = 16 * lg + lane, t = kChunk * (c - 1) + r;
+                uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.o) +
+                                                      (((size_t)b * P.T + t) * P.Hv + hv) * kD + kSlice * j);
+#pragma unroll
+                for (int q = 0; q < 4; q++)
+                    dst[q] = make_uint4(pack_bf16(O[8 * q], O[8 * q + 1]), pack_bf16(O[8 * q + 2], O[8 * q + 3]),
+                                        pack_bf16(O[8 * q + 4], O[8 * q + 5]), pack_bf16(O[8 * q + 6], O[8 * q + 7]));
+            }
+        }
+        if (!bad && MODE == SCAN_FWD_OUT) {  // outputs of the last chunk
+            const int i_last = NC - 1;
+            bool ok = __all_sync(0xffffffffu, mbar_wait(&ofull[i_last & 1], (i_last >> 1) & 1, &abort_sh, a.status, 32));
+            tc_fence_after();
+            float O[32];
+            if (ok) tmem_ld32(tmem_at(tm, 32 * lg, 64 + 32 * (i_last & 1)), O);
+            tmem_wait_ld();
+            const int r = 16 * lg + lane, t = kChunk * i_last + r;
+            if (ok && lane < 16 && t < P.T) {
+                uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.o) +
+                                                      (((size_t)b * P.T + t) * P.Hv + hv) * kD + kSlice * j);
+#pragma unroll
+                for (int q = 0; q < 4; q++)
+                    dst[q] = make_uint4(pack_bf16(O[8 * q], O[8 * q + 1]), pack_bf16(O[8 * q + 2], O[8 * q + 3]),
+                                        pack_bf16(O[8 * q + 4], O[8 * q + 5]), pack_bf16(O[8 * q + 6], O[8 * q + 7]));
+            }
+            bad = !ok;
+        }
+        if (!bad && a.hfinal) {
+#pragma unroll
+            for (int n = 0; n < 32; n++) a.hfinal[(bh * kD + kSlice * j + n) * kD + d] = H[n];
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (abort_sh && tid == 0 && last_loaded >= 0) {  // copies still in flight must land first
+        volatile int never = 0;
+        for (int i = last_loaded > 0 ? last_loaded - 1 : 0; i <= last_loaded; i++)
+            mbar_wait(&full[i & 1], (i >> 1) & 1, &never, nullptr, 0);
+    }
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tm, 128);
+}
+
+cudaError_t launch_scan(const ScanArgs& a, int mode, const CUtensorMap* mdo, cudaStream_t s) {
+    const int smem = SS_BYTES + 1024;
+    dim3 grid(kSlices, a.p.Hv, a.p.B);
+    CUtensorMap dummy;
+    memset(&dummy, 0, sizeof(dummy));
+    const CUtensorMap& m = mdo ? *mdo : dummy;
+    cudaError_t e;
+    switch (mode) {
+        case SCAN_FWD_OUT:
+            e = cudaFuncSetAttribute(scan_kernel<SCAN_FWD_OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e != cudaSuccess) return e;
+            scan_kernel<SCAN_FWD_OUT><<<grid, 192, smem, s>>>(m, a);
+            break;
+        case SCAN_FWD_STATES:
+            e = cudaFuncSetAttribute(scan_kernel<SCAN_FWD_STATES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     smem);
+            if (e != cudaSuccess) return e;
+            scan_kernel<SCAN_FWD_STATES><<<grid, 192, smem, s>>>(m, a);
+            break;
+        default:
+            e = cudaFuncSetAttribute(scan_kernel<SCAN_BWD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e != cudaSuccess) return e;
+            scan_kernel<SCAN_BWD><<<grid, 192, smem, s>>>(m, a);
+            break;
+    }
+    return cudaGetLastError();
+}
+
+bool make_qkv_maps(const ChunkProblem& p, const void* q, const void* k, const void* v, CUtensorMap* mq,
+                   CUtensorMap* mk, CUtensorMap* mv) {
+    return make_map_4d_bf16(mq, q, kD, p.Hk, p.T, p.B, 64, kChunk, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           make_map_4d_bf16(mk, k, kD, p.Hk, p.T, p.B, 64, kChunk, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           make_map_4d_bf16(mv, v, kD, p.Hv, p.T, p.B, 64, kChunk, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+cudaError_t launch_chunk_fwd(const ChunkFwdArgs& a, cudaStream_t s) {
+    const WsLayout w = ws_layout(a.p, false);
+    uint8_t* ws = static_cast<uint8_t*>(a.ws);
+    CUtensorMap mq, mk, mv;
+    if (!make_qkv_maps(a.p, a.q, a.k, a.v, &mq, &mk, &mv)) return cudaErrorInvalidValue;
+    PrepArgs pa;
+    pa.p = a.p;
+    pa.g = a.g;
+    pa.beta = a.beta;
+    pa.gam = reinterpret_cast<float*>(ws + w.gam);
+    pa.rec = ws + w.rec;
+    pa.status = reinterpret_cast<int*>(ws);
+    pa.ncpad = w.ncpad;
+    cudaError_t e = launch_prep(pa, mq, mk, mv, s);
+    if (e != cudaSuccess) return e;
+    ScanArgs sa;
+    sa.p = a.p;
+    sa.gam = pa.gam;
+    sa.rec = pa.rec;
+    sa.hinit = a.h0;
+    sa.o = a.o;
+    sa.hfinal = a.ht;
+    sa.states = nullptr;
+    sa.status = pa.status;
+    sa.ncpad = w.ncpad;
+    return launch_scan(sa, SCAN_FWD_OUT, nullptr, s);
+}
+
+}  // namespace gdr

@@ -1,0 +1,279 @@
+// common.cuh - sm_103a device building blocks shared by the gated delta rule kernels:
+// mbarriers with bounded waits, TMA (tensor and plain bulk) copies, tcgen05 tensor-core
+// MMA with TMEM accumulators, shared-memory matrix descriptors and the swizzled tile
+// layouts the kernels write by hand.
+//
+// Tile convention used throughout: a "panelised SW128 tile" of R rows x C bf16 columns is
+// stored as C/64 panels; panel p holds columns [64p, 64p+64) of all R rows, one 128-byte
+// row each, with the 16-byte chunks of row r permuted by (chunk ^ (r & 7)) (the 128-byte
+// swizzle that TMA writes). Such a tile is a K-major MMA operand when the contraction
+// runs along its columns and an MN-major operand when it runs along its rows, so the
+// same bytes serve a product and its transpose. Narrow 32-column tiles use the 64-byte
+// swizzle (64-byte rows, chunk ^ ((r >> 1) & 3)).
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gdr {
+
+// ------------------------------------------------------------------ status word
+// First 256 bytes of a chunked workspace: word 0 = sticky error code (0 = ok),
+// word 1 = block id that gave up, word 2 = wait site.
+enum : int { DEV_OK = 0, DEV_TIMEOUT = 5 };
+constexpr long long kWaitCycles = 2000000000LL;  // ~1 s at GB300 clocks
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ------------------------------------------------------------------ mbarrier
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait on phase `parity`. Gives up after ~1 s or as soon as another thread of
+// the CTA has raised *abort; on expiry records DEV_TIMEOUT (and where) in the status
+// word and raises *abort. Returns false if the wait did not complete.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          int* status, int site) {
+    if (mbar_try_wait(bar, parity)) return true;
+    long long t0 = clock64();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (clock64() - t0 > kWaitCycles) {
+            *abort = 1;
+            if (status) {
+                if (atomicCAS(status, 0, DEV_TIMEOUT) == 0) {
+                    status[1] = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z);
+                    status[2] = site;
+                }
+            }
+            return false;
+        }
+    }
+}
+
+// ------------------------------------------------------------------ async-proxy fences
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ TMA copies
+// 4-D tiled tensor load into shared memory, completing on `bar` (tx bytes).
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            int c3, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+        : "memory");
+}
+// Plain bulk copy global -> shared (16-byte aligned addresses, size multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+// Plain bulk copy shared -> global, tracked by the issuing thread's bulk group.
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ tcgen05 / TMEM
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D[tmem] (+)= A[smem] * B[smem], bf16 inputs, fp32 accumulation; issued by one thread.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Arrive once on `bar` when every tcgen05 op issued so far by this thread has completed.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// 32 lanes x 32 consecutive fp32 columns: thread t of the warp gets lane (base + t).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+    uint32_t* r = reinterpret_cast<uint32_t*>(v);
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+    uint32_t* r = reinterpret_cast<uint32_t*>(v);
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15])
+        : "r"(taddr));
+}
+// TMEM address of (lane, column) relative to an allocation base.
+__device__ __forceinline__ uint32_t tmem_at(uint32_t base, uint32_t lane, uint32_t col) {
+    return base + (lane << 16) + col;
+}
+
+// Instruction descriptor, kind::f16 with bf16 A/B and fp32 D. a_mn / b_mn = 1 selects
+// an MN-major (transposed) operand.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(a_mn) << 15) | (uint32_t(b_mn) << 16) |
+           (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+}
+
+enum Swz : uint32_t { SWZ_NONE = 0, SWZ_128 = 2, SWZ_64 = 4, SWZ_32 = 6 };
+
+// Shared-memory matrix descriptor (start address, leading / stride byte offsets,
+// fixed version bits 46-47 = 1, swizzle mode in bits 61-63).
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t swz) {
+    return uint64_t((saddr & 0x3FFFFu) >> 4) | (uint64_t((lbo >> 4) & 0x3FFFu) << 16) |
+           (uint64_t((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (uint64_t(swz) << 61);
+}
+
+// Descriptors of a panelised SW128 tile (R rows, base 1024-aligned) for the 16-wide
+// contraction slice starting at k0.
+//  K-major: the contraction runs along the tile's columns; rows [r0, r0+M) are the
+//           operand's M (or N) rows (r0 % 8 == 0).
+__device__ __forceinline__ uint64_t desc_kmajor(uint32_t tile, int R, int r0, int k0) {
+    uint32_t a = tile + uint32_t(k0 >> 6) * uint32_t(R * 128) + uint32_t(r0 * 128) + uint32_t((k0 & 63) * 2);
+    return sdesc(a, 16, 1024, SWZ_128);
+}
+//  MN-major: the contraction runs along the tile's rows (k0 % 16 == 0); the operand's
+//           M (or N) index is the tile column, starting at panel c0/64.
+__device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int R, int c0, int k0) {
+    uint32_t a = tile + uint32_t(c0 >> 6) * uint32_t(R * 128) + uint32_t(k0 * 128);
+    return sdesc(a, uint32_t(R * 128), 1024, SWZ_128);
+}
+//  MN-major over a 32-column SW64 tile (64-byte rows): N = 32.
+__device__ __forceinline__ uint64_t desc_mnmajor_sw64(uint32_t tile, int R, int k0) {
+    return sdesc(tile + uint32_t(k0 * 64), uint32_t(R * 64), 512, SWZ_64);
+}
+
+// Byte offset of element (r, c) in a panelised SW128 bf16 tile with R rows.
+__host__ __device__ __forceinline__ uint32_t sw128_off(int r, int c, int R) {
+    return uint32_t(c >> 6) * uint32_t(R * 128) + uint32_t(r * 128) + ((uint32_t(((c & 63) >> 3) ^ (r & 7))) << 4) +
+           uint32_t((c & 7) * 2);
+}
+// Byte offset of the 16-byte chunk holding columns [8j, 8j+8) of row r.
+__host__ __device__ __forceinline__ uint32_t sw128_chunk(int r, int j, int R) {
+    return uint32_t(j >> 3) * uint32_t(R * 128) + uint32_t(r * 128) + (uint32_t((j & 7) ^ (r & 7)) << 4);
+}
+// Byte offset of element (r, c) in a 32-column SW64 bf16 tile.
+__host__ __device__ __forceinline__ uint32_t sw64_off(int r, int c) {
+    return uint32_t(r * 64) + (uint32_t(((c >> 3) & 3) ^ ((r >> 1) & 3)) << 4) + uint32_t((c & 7) * 2);
+}
+__host__ __device__ __forceinline__ uint32_t sw64_chunk(int r, int j) {
+    return uint32_t(r * 64) + (uint32_t((j & 3) ^ ((r >> 1) & 3)) << 4);
+}
+
+// ------------------------------------------------------------------ CTA-level helpers
+// Round a dynamic shared-memory pointer up to a 1024-byte boundary (swizzle atoms).
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+    const uint32_t s = smem_u32(p);
+    return p + ((1024u - (s & 1023u)) & 1023u);
+}
+// Named barrier over `n` threads that also ORs a predicate across them, so a group of
+// warps takes one uniform decision (used to stop together after a failed wait).
+__device__ __forceinline__ bool bar_sync_or(int id, int n, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "barrier.cta.red.or.pred p, %2, %3, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
+
+// ------------------------------------------------------------------ small helpers
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ float bf16lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+}  // namespace gdr

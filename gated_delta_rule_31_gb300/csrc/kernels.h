@@ -1,0 +1,21 @@
+// kernels.h - internal launch interfaces between the C ABI (api.cu) and the kernels.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace gdr {
+
+struct RecurrentArgs {
+    int B, T, Hk, Hv, Dk, Dv;
+    int channel, use_norm, bf16;
+    float scale;
+    const void *q, *k, *v;
+    const float *g, *beta, *h0;
+    void* o;
+    float* ht;
+};
+cudaError_t launch_recurrent(const RecurrentArgs& a, bool decode, cudaStream_t s);
+
+}  // namespace gdr

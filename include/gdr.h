@@ -1,0 +1,125 @@
+/*
+ * gdr.h - C ABI of the GB300 (sm_103a) gated delta rule library (libgdr.so).
+ *
+ * The operation (Gated DeltaNet recurrence). Per batch b and value head hv, with key
+ * head hk = hv / (Hv / Hk), a state S in R^{Dv x Dk} evolves over tokens t:
+ *
+ *     k^ = n(k_t),  q^ = n(q_t),   n(x) = x * (sum x^2 + 1e-6)^(-1/2)  (if use_qk_l2norm)
+ *     S_t = S_{t-1} diag(a_t) (I - beta_t k^ k^T) + beta_t v_t k^T,   a_t = exp(g_t)
+ *     o_t = scale * S_t q^
+ *
+ * a_t is one value per (b,t,hv) (scalar gate) or a vector over the Dk key channels
+ * (channel gate). Sources: "perf(gated_delta_net): fold q/k L2-norm into the
+ * gated_delta_rule kernel" (Megatron-LM PR #5396), What/Why: the kernel owns the q/k
+ * L2 norm of the last dimension with eps 1e-6; "Two-pass optimization for channelwise
+ * gated delta rule kernel" (ExecuTorch PR #21020), Summary: per-channel decay, decode
+ * in two state traversals with the decay folded into the prediction; "Adding VJP for
+ * gated delta net" (MLX PR #4565), description and Performance: a chunked and a
+ * sequential backward over B in {1,4,8}, T 8..4096, Hk=16, Hv=32, Dk=Dv=128.
+ *
+ * Layouts: dense row-major, innermost last.
+ *   q, k        [B, T, Hk, Dk]   dtype (fp32 or bf16)
+ *   v, o, do    [B, T, Hv, Dv]   dtype
+ *   g           [B, T, Hv] (scalar gate) or [B, T, Hv, Dk] (channel gate), fp32, log-decay
+ *   beta        [B, T, Hv]       fp32 (already in (0,1); the gradient is w.r.t. beta)
+ *   h0, ht, dht, dh0, state      [B, Hv, Dv, Dk] fp32 (row v of S is contiguous)
+ *   dq, dk      [B, T, Hk, Dk]   fp32 (summed over the value heads sharing a key head)
+ *   dv          [B, T, Hv, Dv]   fp32;  dg like g, dbeta like beta, fp32
+ * Decode uses the same layouts with the T axis removed.
+ *
+ * Ownership: every pointer is device memory owned by the caller (for example torch
+ * tensors). The library keeps no allocation between calls and allocates nothing in
+ * the compute calls; launches are asynchronous on the given stream and no call
+ * synchronises. Outputs may not alias inputs (except decode's in-place state).
+ *
+ * Errors: arguments are validated before anything is launched. A bad argument returns
+ * GDR_ERR_INVALID_ARG, a combination this build does not implement returns
+ * GDR_ERR_UNSUPPORTED, a short workspace GDR_ERR_WORKSPACE, all with nothing launched.
+ * A failed launch returns GDR_ERR_CUDA. The chunked kernels bound every wait; if a
+ * wait expires the kernel stops and records GDR_ERR_TIMEOUT in the workspace's
+ * status word, which gdr_workspace_status() reads back.
+ */
+#ifndef GDR_H_
+#define GDR_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* gdr_stream_t; /* same type as cudaStream_t; NULL = default stream */
+
+typedef enum {
+    GDR_OK = 0,
+    GDR_ERR_INVALID_ARG = 1, /* null required pointer, bad size, misaligned pointer, ... */
+    GDR_ERR_UNSUPPORTED = 2, /* valid, but not implemented by this build (see each call) */
+    GDR_ERR_WORKSPACE = 3,   /* ws_bytes smaller than the matching *_workspace() query */
+    GDR_ERR_CUDA = 4,        /* a CUDA launch or runtime call failed */
+    GDR_ERR_TIMEOUT = 5      /* a bounded device-side wait expired (read from the workspace) */
+} gdr_status;
+
+typedef enum { GDR_F32 = 0, GDR_BF16 = 1 } gdr_dtype;             /* of q, k, v, o, do */
+typedef enum { GDR_GATE_SCALAR = 0, GDR_GATE_CHANNEL = 1 } gdr_gate;
+
+typedef struct {
+    int B, T, Hk, Hv, Dk, Dv; /* Hv % Hk == 0; T >= 0 (T == 1 for decode) */
+    gdr_dtype dtype;
+    gdr_gate gate;
+    float scale;              /* applied to o = scale * S q^ (commonly Dk^-1/2) */
+    int use_qk_l2norm;        /* 1: normalise q and k inside, eps 1e-6; 0: use as given */
+} gdr_problem;
+
+/* Human-readable name of a status code (static storage). */
+const char* gdr_status_string(gdr_status s);
+
+/* Bytes of device workspace gdr_fwd_chunked / gdr_bwd_chunked need for this problem
+ * (0 if the problem is invalid). The workspace is scratch owned by the caller; its
+ * first 256 bytes hold the status word. */
+size_t gdr_fwd_chunked_workspace(const gdr_problem* p);
+size_t gdr_bwd_chunked_workspace(const gdr_problem* p);
+
+/* Chunked prefill forward (chunks of 64 tokens): o and, if ht != NULL, the final state.
+ * h0 may be NULL (zero initial state). Implemented for dtype BF16, Dk = Dv = 128,
+ * scalar gate; other combinations return GDR_ERR_UNSUPPORTED. Pointers 16-byte aligned.
+ * Work: per chunk a 64x64 unit-lower-triangular (UT/WY) transform of the k k^T beta
+ * block on the tensor cores, then one sequential scan over chunks per (b, hv, Dv slice)
+ * with the fp32 state held on chip. Clears and then sets the workspace status word. */
+gdr_status gdr_fwd_chunked(const gdr_problem* p, const void* q, const void* k, const void* v,
+                           const float* g, const float* beta, const float* h0, void* o, float* ht,
+                           void* ws, size_t ws_bytes, gdr_stream_t stream);
+
+/* Token-by-token forward (no workspace): o and, if ht != NULL, the final state. For every
+ * dtype, gate and Dk, Dv in {32, 64, 128}; the reference path for small problems and
+ * fp32 inputs. */
+gdr_status gdr_fwd_sequential(const gdr_problem* p, const void* q, const void* k, const void* v,
+                              const float* g, const float* beta, const float* h0, void* o,
+                              float* ht, gdr_stream_t stream);
+
+/* Chunked backward (VJP) of gdr_fwd_chunked for the loss <do, o> + <dht, ht>: writes dq, dk,
+ * dv, dg, dbeta and, if dh0 != NULL, dh0. h0 and dht may be NULL (zero). Recomputes the
+ * chunk-local terms and the chunk-start states instead of reading saved activations;
+ * the normalisation backward is done inside. Same support matrix as gdr_fwd_chunked.
+ * Deterministic: no floating-point atomics. */
+gdr_status gdr_bwd_chunked(const gdr_problem* p, const void* q, const void* k, const void* v,
+                           const float* g, const float* beta, const float* h0, const void* do_,
+                           const float* dht, float* dq, float* dk, float* dv, float* dg,
+                           float* dbeta, float* dh0, void* ws, size_t ws_bytes,
+                           gdr_stream_t stream);
+
+/* One decode step (p->T must be 1) on the state in place: per state row, one pass forms
+ * the prediction with the decay folded in, a second applies decay plus the rank-one
+ * update while accumulating the output, so the state is read once and written once.
+ * Layouts as above without the T axis. Every dtype, gate and Dk, Dv in {32, 64, 128}. */
+gdr_status gdr_decode_step(const gdr_problem* p, const void* q, const void* k, const void* v,
+                           const float* g, const float* beta, float* state, void* o,
+                           gdr_stream_t stream);
+
+/* Reads (synchronising on `stream`) and clears the workspace status word written by the
+ * chunked kernels: GDR_OK, or GDR_ERR_TIMEOUT if a bounded wait expired. */
+gdr_status gdr_workspace_status(void* ws, size_t ws_bytes, gdr_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GDR_H_ */

@@ -1,0 +1,115 @@
+"""Host-side checks of the C ABI: the library loads and exports every declared entry
+point, and argument validation returns the documented status codes with nothing
+launched (so these run without a GPU: invalid calls never reach the CUDA runtime)."""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+import gated_delta_rule_31_gb300 as gdr
+from gated_delta_rule_31_gb300 import Problem
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+OK, INVALID, UNSUPPORTED, WORKSPACE, CUDA, TIMEOUT = range(6)
+FAKE = ctypes.c_void_p(0x100000)      # never dereferenced: validation fails first
+MISALIGNED = ctypes.c_void_p(0x100004)
+
+
+@pytest.fixture(scope="module")
+def L():
+    gdr.build()
+    return gdr.lib()
+
+
+def declared_functions():
+    hdr = open(os.path.join(ROOT, "include", "gdr.h")).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[\w\*]+\s+\**(gdr_\w+)\s*\(", hdr, re.M)))
+
+
+def test_exports_every_declared_symbol(L):
+    names = declared_functions()
+    assert {"gdr_fwd_chunked", "gdr_bwd_chunked", "gdr_decode_step", "gdr_fwd_sequential"} <= set(names)
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_status_strings(L):
+    for code in range(6):
+        s = L.gdr_status_string(code).decode()
+        assert s.startswith("GDR_")
+    assert b"unknown" in L.gdr_status_string(99)
+
+
+def prob(**kw):
+    base = dict(B=1, T=64, Hk=2, Hv=4, Dk=128, Dv=128, dtype=1, gate=0, scale=0.088, use_qk_l2norm=1)
+    base.update(kw)
+    return Problem(*[base[f] for f, _ in Problem._fields_])
+
+
+def fwd_seq(L, p, ptrs=None):
+    ptrs = ptrs or [FAKE] * 8
+    return L.gdr_fwd_sequential(ctypes.byref(p) if p is not None else None, *ptrs, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Hv=3), INVALID), (dict(Hk=0), INVALID), (dict(T=-1), INVALID), (dict(B=-2), INVALID),
+    (dict(dtype=7), INVALID), (dict(gate=5), INVALID), (dict(use_qk_l2norm=2), INVALID),
+    (dict(scale=float("nan")), INVALID), (dict(Dk=96), UNSUPPORTED), (dict(Dv=256), UNSUPPORTED),
+    (dict(Dk=0), INVALID),
+])
+def test_problem_validation(L, kw, code):
+    assert fwd_seq(L, prob(**kw)) == code
+
+
+def test_null_and_misaligned_pointers(L):
+    assert fwd_seq(L, None) == INVALID
+    p = prob()
+    for i in range(6):  # q, k, v, g, beta (h0 optional), o
+        ptrs = [FAKE] * 8
+        idx = i if i < 5 else 6
+        ptrs[idx] = None
+        assert fwd_seq(L, p, ptrs) == INVALID, idx
+    ptrs = [FAKE] * 8
+    ptrs[5] = MISALIGNED  # optional h0, misaligned
+    assert fwd_seq(L, p, ptrs) == INVALID
+
+
+def test_decode_requires_single_token(L):
+    p = prob(T=2)
+    assert L.gdr_decode_step(ctypes.byref(p), *[FAKE] * 7, None) == INVALID
+    p = prob(T=1)
+    assert L.gdr_decode_step(ctypes.byref(p), *([FAKE] * 6 + [None]), None) == INVALID
+
+
+def test_chunked_support_matrix_and_workspace(L):
+    for kw in (dict(dtype=0), dict(gate=1), dict(Dk=64, Dv=64)):
+        p = prob(**kw)
+        assert L.gdr_fwd_chunked_workspace(ctypes.byref(p)) == 0
+        assert L.gdr_fwd_chunked(ctypes.byref(p), *[FAKE] * 8, FAKE, 1 << 30, None) == UNSUPPORTED
+        assert L.gdr_bwd_chunked(ctypes.byref(p), *[FAKE] * 14, FAKE, 1 << 30, None) == UNSUPPORTED
+    p = prob()
+    need = L.gdr_fwd_chunked_workspace(ctypes.byref(p))
+    need_b = L.gdr_bwd_chunked_workspace(ctypes.byref(p))
+    assert need > 0 and need_b > need
+    assert L.gdr_fwd_chunked(ctypes.byref(p), *[FAKE] * 8, FAKE, need - 1, None) == WORKSPACE
+    assert L.gdr_fwd_chunked(ctypes.byref(p), *[FAKE] * 8, None, need, None) == WORKSPACE
+    assert L.gdr_bwd_chunked(ctypes.byref(p), *[FAKE] * 14, FAKE, need_b - 1, None) == WORKSPACE
+    # dq (a required output) missing
+    ptrs = [FAKE] * 14
+    ptrs[8] = None
+    assert L.gdr_bwd_chunked(ctypes.byref(p), *ptrs, FAKE, need_b, None) == INVALID
+
+
+def test_workspace_grows_linearly_with_tokens(L):
+    a = L.gdr_fwd_chunked_workspace(ctypes.byref(prob(T=64)))
+    b = L.gdr_fwd_chunked_workspace(ctypes.byref(prob(T=128)))
+    c = L.gdr_fwd_chunked_workspace(ctypes.byref(prob(T=65)))
+    assert b > a and c == b  # a ragged chunk costs a whole chunk record
+
+
+def test_binding_rejects_cpu_tensors():
+    q = torch.zeros(1, 4, 1, 32)
+    with pytest.raises(ValueError):
+        gdr.fwd_sequential(q, q, torch.zeros(1, 4, 1, 32), torch.zeros(1, 4, 1), torch.zeros(1, 4, 1))

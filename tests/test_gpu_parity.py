@@ -1,0 +1,173 @@
+"""GPU parity: every CUDA entry point against the fp64 oracle on the same seeded inputs.
+
+Metric per output tensor: max|gpu - oracle| / max|oracle|; bounds 1e-4 for fp32 inputs
+and 2e-2 for bf16 inputs (fp32 state and accumulation). Shapes must match exactly.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gated_delta_rule_31_gb300 as gdr
+import oracle
+from gated_delta_rule_31_gb300.synth import DECODE, PREFILL, TINY_SEQ, Shape, make_decode_inputs, make_inputs
+from tests.util import BF16_TOL, F32_TOL, cuda_device, rel_err, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def run_oracle(x, norm=True, scale=None):
+    return oracle.forward(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"], scale=scale, use_qk_l2norm=norm)
+
+
+# ------------------------------------------------------------------ sequential forward
+def test_sequential_tiny_config():
+    """B=1, T=64, Hk=Hv=2, Dk=Dv=32, fp32, h0 = 0, in-kernel norm, scale Dk^-1/2."""
+    dev = cuda_device()
+    x = make_inputs(TINY_SEQ, dtype=torch.float32, seed=1000, h0_std=None)
+    d = to_dev(x, dev)
+    o, ht = gdr.fwd_sequential(d["q"], d["k"], d["v"], d["g"], d["beta"], None)
+    ro, rht = run_oracle(x)
+    assert tuple(o.shape) == (1, 64, 2, 32) and tuple(ht.shape) == (1, 2, 32, 32)
+    assert rel_err(o, ro) <= F32_TOL and rel_err(ht, rht) <= F32_TOL
+
+
+@pytest.mark.parametrize("D", [32, 64, 128])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("gate", ["scalar", "channel"])
+def test_sequential_matrix(D, dtype, gate):
+    dev = cuda_device()
+    for heads, T, norm, h0 in [((2, 4), 37, True, 0.02), ((1, 1), 1, False, None), ((2, 2), 9, True, None)]:
+        shape = Shape(2, T, heads[0], heads[1], D, D)
+        x = make_inputs(shape, dtype=dtype, seed=D + T, gate=gate, h0_std=h0)
+        d = to_dev(x, dev)
+        o, ht = gdr.fwd_sequential(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], use_qk_l2norm=norm)
+        ro, rht = run_oracle(x, norm)
+        tol = F32_TOL if dtype == torch.float32 else BF16_TOL
+        assert rel_err(o, ro) <= tol and rel_err(ht, rht) <= tol, (heads, T, norm)
+
+
+def test_sequential_no_final_state_and_empty():
+    dev = cuda_device()
+    x = make_inputs(Shape(1, 0, 1, 2, 64, 64), dtype=torch.float32, seed=3)
+    d = to_dev(x, dev)
+    o, ht = gdr.fwd_sequential(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"])
+    assert o.shape == (1, 0, 2, 64)
+    assert torch.equal(ht.cpu(), x["h0"])
+
+
+# ------------------------------------------------------------------ decode
+def test_decode_config_steps():
+    """B=32, Hk=16, Hv=32, Dk=Dv=128, channel gate, fp32: three consecutive steps."""
+    dev = cuda_device()
+    cfg = DECODE
+    x = make_decode_inputs(cfg["B"], cfg["Hk"], cfg["Hv"], cfg["Dk"], cfg["Dv"], steps=3, seed=1003)
+    st = x["state0"].to(dev).clone()
+    ref = x["state0"].double().numpy()
+    for t in range(3):
+        o = gdr.decode_step(x["q"][t].to(dev), x["k"][t].to(dev), x["v"][t].to(dev), x["g"][t].to(dev),
+                            x["beta"][t].to(dev), st)
+        ro, ref = oracle.decode_step(x["q"][t], x["k"][t], x["v"][t], x["g"][t], x["beta"][t], ref)
+        assert rel_err(o, ro) <= F32_TOL
+        assert rel_err(st, ref) <= F32_TOL
+
+
+@pytest.mark.parametrize("gate", ["scalar", "channel"])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_decode_steps_equal_sequential(gate, dtype):
+    """T decode steps equal one token-by-token forward over the T tokens."""
+    dev = cuda_device()
+    shape = Shape(3, 6, 2, 4, 64, 128)
+    x = make_inputs(shape, dtype=dtype, seed=11, gate=gate)
+    d = to_dev(x, dev)
+    o, ht = gdr.fwd_sequential(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"])
+    st = d["h0"].clone()
+    for t in range(6):
+        ot = gdr.decode_step(d["q"][:, t].contiguous(), d["k"][:, t].contiguous(), d["v"][:, t].contiguous(),
+                             d["g"][:, t].contiguous(), d["beta"][:, t].contiguous(), st)
+        assert rel_err(ot, o[:, t]) <= 1e-5
+    assert rel_err(st, ht) <= 1e-5
+
+
+# ------------------------------------------------------------------ chunked forward
+CHUNK_CASES = [
+    # (B, T, Hk, Hv, h0, norm, gate_scale)
+    (1, 1, 1, 1, True, True, 1.0),
+    (1, 7, 1, 2, False, True, 1.0),
+    (1, 63, 2, 2, True, True, 1.0),
+    (1, 64, 1, 1, True, True, 0.01),
+    (2, 65, 2, 4, True, True, 1.0),
+    (1, 129, 1, 2, True, False, 0.01),
+    (1, 300, 2, 4, False, True, 0.01),
+    (2, 512, 2, 4, True, True, 1.0),
+]
+
+
+@pytest.mark.parametrize("case", CHUNK_CASES, ids=[f"B{c[0]}T{c[1]}H{c[2]}x{c[3]}" for c in CHUNK_CASES])
+def test_chunked_forward_small(case):
+    dev = cuda_device()
+    B, T, Hk, Hv, h0, norm, gs = case
+    x = make_inputs(Shape(B, T, Hk, Hv, 128, 128), dtype=torch.bfloat16, seed=T * 7 + Hv,
+                    h0_std=0.02 if h0 else None, gate_scale=gs)
+    d = to_dev(x, dev)
+    ws = torch.empty(gdr.fwd_workspace_bytes(gdr._problem(d["q"], d["v"], d["g"], None, norm)),
+                     dtype=torch.uint8, device=dev)
+    o, ht = gdr.fwd_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], use_qk_l2norm=norm, workspace=ws)
+    assert gdr.workspace_status(ws) == 0
+    ro, rht = run_oracle(x, norm)
+    eo, eh = rel_err(o, ro), rel_err(ht, rht)
+    assert eo <= BF16_TOL and eh <= BF16_TOL, (eo, eh)
+
+
+def test_chunked_forward_prefill_config():
+    """B=1, T=4096, Hk=16, Hv=32, Dk=Dv=128, bf16, h0 ~ N(0, 0.02)."""
+    dev = cuda_device()
+    x = make_inputs(PREFILL, dtype=torch.bfloat16, seed=1001)
+    d = to_dev(x, dev)
+    o, ht = gdr.fwd_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"])
+    ro, rht = run_oracle(x)
+    assert tuple(o.shape) == (1, 4096, 32, 128)
+    assert rel_err(o, ro) <= BF16_TOL and rel_err(ht, rht) <= BF16_TOL
+
+
+def test_chunked_forward_prefill_mild_decay():
+    """Same shape with g scaled by 0.01, so the state carries information across the
+    whole sequence and errors in the chunk-to-chunk scan are not hidden by decay."""
+    dev = cuda_device()
+    x = make_inputs(PREFILL, dtype=torch.bfloat16, seed=1101, gate_scale=0.01)
+    d = to_dev(x, dev)
+    o, ht = gdr.fwd_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"])
+    ro, rht = run_oracle(x)
+    assert rel_err(o, ro) <= BF16_TOL and rel_err(ht, rht) <= BF16_TOL
+
+
+def test_chunked_equals_sequential_on_gpu():
+    dev = cuda_device()
+    x = make_inputs(Shape(1, 200, 2, 4, 128, 128), dtype=torch.bfloat16, seed=5, gate_scale=0.1)
+    d = to_dev(x, dev)
+    o1, h1 = gdr.fwd_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"])
+    o2, h2 = gdr.fwd_sequential(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"])
+    assert rel_err(o1, o2) <= BF16_TOL and rel_err(h1, h2) <= BF16_TOL
+
+
+def test_chunked_forward_is_deterministic_and_split_consistent():
+    dev = cuda_device()
+    x = make_inputs(Shape(1, 256, 1, 2, 128, 128), dtype=torch.bfloat16, seed=9, gate_scale=0.05)
+    d = to_dev(x, dev)
+    o1, h1 = gdr.fwd_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"])
+    o2, h2 = gdr.fwd_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"])
+    assert torch.equal(o1, o2) and torch.equal(h1, h2)
+    # prefill split at a chunk boundary: fwd(T1 + T2) == fwd(T2, h0 = fwd(T1).ht)
+    s = lambda t, a, b: t[:, a:b].contiguous()
+    oa, ha = gdr.fwd_chunked(s(d["q"], 0, 128), s(d["k"], 0, 128), s(d["v"], 0, 128), s(d["g"], 0, 128),
+                             s(d["beta"], 0, 128), d["h0"])
+    ob, hb = gdr.fwd_chunked(s(d["q"], 128, 256), s(d["k"], 128, 256), s(d["v"], 128, 256),
+                             s(d["g"], 128, 256), s(d["beta"], 128, 256), ha)
+    assert rel_err(torch.cat([oa, ob], 1), o1) <= 1e-2 and rel_err(hb, h1) <= 1e-2
+
+
+def test_chunked_empty_sequence():
+    dev = cuda_device()
+    x = make_inputs(Shape(1, 0, 1, 2, 128, 128), dtype=torch.bfloat16, seed=1)
+    d = to_dev(x, dev)
+    o, ht = gdr.fwd_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"])
+    assert o.shape == (1, 0, 2, 128) and torch.equal(ht.cpu(), x["h0"])

@@ -1,0 +1,388 @@
+#!/usr/bin/env python
+"""Benchmark of the gated delta rule hot path on GB300.
+
+Headline: the long-context training step (chunked forward + VJP) at B=1, T=32768, Hk=16,
+Hv=32, Dk=Dv=128, bf16 q/k/v with in-kernel L2 norm, fp32 gates/state, h0 = 0, dht = 0,
+do ~ N(0,1): tokens/s = B*T / step time, timed with CUDA events on the launch stream.
+Inputs (q, k 128 MiB each; v, do 256 MiB each) are larger than the 129 MB L2, so no flush
+is needed between steps. Also reported: the roofline of the dominant kernel (per-kernel
+times from the library's launch trace, recorded on the launch stream), the same step end
+to end with pinned-host inputs/outputs copied inside the timed region, the decode step's
+state bandwidth (B=32, channel gate, fp32, L2 flushed before every step), SM clocks
+sampled during the timed region, and the fp64 CPU oracle timed on a bounded sample.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mine|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDR fwd+bwd tokens/s at Hv=32,D=128 (% roofline); decode state GB/s vs HBM peak"
+B, T, HK, HV, D, C = 1, 32768, 16, 32, 128, 64
+UNITS = B * T * HV  # token x value-head units per step
+
+# Algorithmic work per (token x value head), D=128, C=64, as the kernels do it:
+# bytes = the user-visible tensors each kernel must read or write (no workspace);
+# flops = 2 x the multiply-adds of its tensor-core products.
+KERNEL_MODEL = {
+    "chunk_prep": (520, 114688),         # reads q,k (shared by 2 v-heads), v, g, beta
+    "chunk_scan_fwd": (256, 147456),     # writes o
+    "chunk_scan_states": (0, 98304),
+    "chunk_scan_bwd": (256, 98304),      # reads do
+    "chunk_grad": (1808, 331000),        # reads q,k,v,do,g,beta; writes dq,dk,dv,dg,dbeta
+}
+# Whole-step algorithmic roofline (forward + VJP): 655,360 flops and 2,584 bytes per unit.
+STEP_FLOPS, STEP_BYTES = 655360 * UNITS, 2584 * UNITS
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), tf=float(p["bf16_tflops"]),
+                    tf_sus=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), src="measured")
+    return dict(hbm=6800.0, tf=1900.0, tf_sus=1700.0, src="fallback")
+
+
+class Clocks:
+    """nvidia-smi sampler for the timed region (the exact child PID is stopped afterwards)."""
+
+    def __init__(self, index):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--id={index}", f"--query-gpu={q}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return None
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [l.strip().split(",") for l in self.f.read().splitlines() if l.strip()]
+        os.unlink(self.f.name)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                mx = float(r[2])
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.strip().lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return dict(sm_mhz=None, sm_max_mhz=mx, reasons=sorted(reasons), samples=0)
+        return dict(sm_mhz=statistics.median(sm), sm_max_mhz=mx, reasons=sorted(reasons), samples=len(sm))
+
+
+def oracle_sample(target_s=15.0, max_tokens=T):
+    """Time the fp64 oracle (forward + backward) on a prefix of the workload (all heads,
+    B=1), grown until one run takes about target_s seconds. Returns (tokens/s, tokens)."""
+    import oracle
+    from gated_delta_rule_31_gb300.synth import Shape, make_inputs
+
+    n = 64
+    while True:
+        x = make_inputs(Shape(B, n, HK, HV, D, D), seed=1004, grads=True, h0_std=None, dht_std=None)
+        t0 = time.perf_counter()
+        oracle.forward(x["q"], x["k"], x["v"], x["g"], x["beta"], None)
+        oracle.backward(x["q"], x["k"], x["v"], x["g"], x["beta"], None, x["do"], None)
+        dt = time.perf_counter() - t0
+        if dt >= target_s / 4 or n >= max_tokens:
+            if dt < target_s and n < max_tokens:
+                n2 = min(max_tokens, int(n * target_s / max(dt, 1e-3)))
+                x = make_inputs(Shape(B, n2, HK, HV, D, D), seed=1004, grads=True, h0_std=None, dht_std=None)
+                t0 = time.perf_counter()
+                oracle.forward(x["q"], x["k"], x["v"], x["g"], x["beta"], None)
+                oracle.backward(x["q"], x["k"], x["v"], x["g"], x["beta"], None, x["do"], None)
+                dt, n = time.perf_counter() - t0, n2
+            return n / dt, n
+        n *= 4
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: each step is one bounded sample of the workload."""
+    if rank != 0:
+        return
+    import oracle
+    from gated_delta_rule_31_gb300.synth import Shape, make_inputs
+
+    oracle.build()
+    n = args.ref_tokens
+    x = make_inputs(Shape(B, n, HK, HV, D, D), seed=1004, grads=True, h0_std=None, dht_std=None)
+
+    def step():
+        oracle.forward(x["q"], x["k"], x["v"], x["g"], x["beta"], None)
+        oracle.backward(x["q"], x["k"], x["v"], x["g"], x["beta"], None, x["do"], None)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = n / dt
+    sample = f"B=1, first {n} of {T} tokens of the workload, all {HV} value heads, forward + backward in fp64"
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }))
+
+
+def workload_config():
+    return {"workload": "long-context training step, chunked forward + VJP", "B": B, "T": T, "Hk": HK, "Hv": HV,
+            "Dk": D, "Dv": D, "chunk": C, "qkv": "bf16", "gates_state": "fp32", "use_qk_l2norm": True,
+            "h0": "zero", "dht": "zero", "l2": "inputs larger than L2 (q,k 128 MiB, v,do 256 MiB); no flush"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=40)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["mine", "reference"], default="mine")
+    ap.add_argument("--ref-tokens", type=int, default=512)
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    import gated_delta_rule_31_gb300 as gdr
+    from gated_delta_rule_31_gb300.synth import DECODE, LONG_TRAIN, make_decode_inputs, make_inputs
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    L = gdr.lib()  # fails loudly if the CUDA library is missing
+    peaks = load_peaks()
+
+    # ------------------------------------------------------------------ inputs (replica per rank)
+    x = make_inputs(LONG_TRAIN, dtype=torch.bfloat16, seed=1004 + rank, grads=True, h0_std=None, dht_std=None)
+    d = {k: (v.to(dev) if v is not None else None) for k, v in x.items()}
+    p = gdr.Problem(B, T, HK, HV, D, D, gdr.GDR_BF16, gdr.GDR_GATE_SCALAR, D ** -0.5, 1)
+    f32 = dict(dtype=torch.float32, device=dev)
+    out = dict(o=torch.empty(d["v"].shape, dtype=torch.bfloat16, device=dev),
+               dq=torch.empty(d["q"].shape, **f32), dk=torch.empty(d["k"].shape, **f32),
+               dv=torch.empty(d["v"].shape, **f32), dg=torch.empty(d["g"].shape, **f32),
+               dbeta=torch.empty(d["beta"].shape, **f32), dh0=torch.empty((B, HV, D, D), **f32))
+    nf, nb = gdr.fwd_workspace_bytes(p), gdr.bwd_workspace_bytes(p)
+    wsf = torch.empty(nf, dtype=torch.uint8, device=dev)
+    wsb = torch.empty(nb, dtype=torch.uint8, device=dev)
+    P = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None
+    pp = ctypes.byref(p)
+
+    def step(src, dst, stream):
+        rc = L.gdr_fwd_chunked(pp, P(src["q"]), P(src["k"]), P(src["v"]), P(src["g"]), P(src["beta"]), None,
+                               P(dst["o"]), None, P(wsf), nf, stream)
+        rc = rc or L.gdr_bwd_chunked(pp, P(src["q"]), P(src["k"]), P(src["v"]), P(src["g"]), P(src["beta"]),
+                                     None, P(src["do"]), None, P(dst["dq"]), P(dst["dk"]), P(dst["dv"]),
+                                     P(dst["dg"]), P(dst["dbeta"]), P(dst["dh0"]), P(wsb), nb, stream)
+        if rc:
+            raise gdr.GdrError(rc, L.gdr_status_string(rc).decode())
+
+    stream = torch.cuda.current_stream(dev)
+    sp = ctypes.c_void_p(stream.cuda_stream)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    for _ in range(args.warmup):
+        step(d, out, sp)
+    barrier()
+    assert gdr.workspace_status(wsf) == 0 and gdr.workspace_status(wsb) == 0
+
+    # ------------------------------------------------------------------ headline: device-resident
+    clk = Clocks(local)
+    time.sleep(0.3)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step(d, out, sp)
+    e1.record(stream)
+    barrier()
+    ms = e0.elapsed_time(e1) / args.steps
+    clocks = clk.stop()
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * B * T / (ms / 1e3)
+
+    # ------------------------------------------------------------------ per-kernel times (launch trace)
+    nt = min(args.steps, 10)
+    with gdr.trace() as tr:
+        for _ in range(nt):
+            step(d, out, sp)
+        torch.cuda.synchronize(dev)
+    kern = {}
+    for name, t in tr.records:
+        k = kern.setdefault(name, {"launches": 0, "ms_total": 0.0})
+        k["launches"] += 1
+        k["ms_total"] += t
+    tot = sum(k["ms_total"] for k in kern.values())
+    for k in kern.values():
+        k["share"] = k["ms_total"] / tot if tot else None
+        k["ms_mean"] = k["ms_total"] / k["launches"]
+    dom = max(kern, key=lambda n: kern[n]["ms_total"])
+    mb, mf = KERNEL_MODEL.get(dom, (0, 0))
+    t_launch = kern[dom]["ms_mean"] / 1e3
+    tb, tfl = mb * UNITS / (peaks["hbm"] * 1e9), mf * UNITS / (peaks["tf_sus"] * 1e12)
+    if tb >= tfl:
+        ach = mb * UNITS / t_launch / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": peaks["hbm"], "unit": "GB/s",
+                "frac": ach / peaks["hbm"], "traffic": None, "algorithmic_bytes": mb * UNITS,
+                "peak_source": peaks["src"] + " hbm_gbs"}
+    else:
+        ach = mf * UNITS / t_launch / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": peaks["tf_sus"], "unit": "TFLOP/s",
+                "frac": ach / peaks["tf_sus"], "traffic": None, "algorithmic_flops": mf * UNITS,
+                "peak_source": peaks["src"] + " bf16_tflops_sustained"}
+    t_star = max(STEP_FLOPS / (peaks["tf_sus"] * 1e12), STEP_BYTES / (peaks["hbm"] * 1e9))
+    launches_per_step = len(tr.records) / nt
+
+    # ------------------------------------------------------------------ end to end (pinned host buffers)
+    e2e = None
+    if not args.no_e2e:
+        hin = {k: v.pin_memory() for k, v in x.items() if v is not None}
+        hout = {k: torch.empty(v.shape, dtype=v.dtype, pin_memory=True) for k, v in out.items()}
+        din = {k: torch.empty_like(v, device=dev) for k, v in hin.items()}
+        h2d = sum(v.numel() * v.element_size() for v in hin.values())
+        d2h = sum(v.numel() * v.element_size() for v in hout.values())
+        ne = min(args.steps, 5)
+
+        def e2e_step():
+            for k in hin:
+                din[k].copy_(hin[k], non_blocking=True)
+            step(din, out, sp)
+            for k in hout:
+                hout[k].copy_(out[k], non_blocking=True)
+
+        e2e_step()
+        barrier()
+        e0.record(stream)
+        for _ in range(ne):
+            e2e_step()
+        e1.record(stream)
+        barrier()
+        ems = e0.elapsed_time(e1) / ne
+        e2e = {"value": world * B * T / (ems / 1e3), "unit": "tokens/s", "ms_per_step": ems,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        del hin, hout, din
+
+    # ------------------------------------------------------------------ decode (B=32, channel gate, fp32)
+    dec = None
+    if not args.no_decode:
+        Bd, Hkd, Hvd, Dd, S = DECODE["B"], DECODE["Hk"], DECODE["Hv"], DECODE["Dk"], DECODE["steps"]
+        xd = make_decode_inputs(Bd, Hkd, Hvd, Dd, Dd, steps=S, seed=1003)
+        dd = {k: v.to(dev) for k, v in xd.items()}
+        st = dd["state0"].clone()
+        od = torch.empty((Bd, Hvd, Dd), **f32)
+        pd = gdr.Problem(Bd, 1, Hkd, Hvd, Dd, Dd, gdr.GDR_F32, gdr.GDR_GATE_CHANNEL, Dd ** -0.5, 1)
+        flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+
+        def dstep(i):
+            rc = L.gdr_decode_step(ctypes.byref(pd), P(dd["q"][i]), P(dd["k"][i]), P(dd["v"][i]), P(dd["g"][i]),
+                                   P(dd["beta"][i]), P(st), P(od), sp)
+            if rc:
+                raise gdr.GdrError(rc, L.gdr_status_string(rc).decode())
+
+        for i in range(4):
+            dstep(i)
+        torch.cuda.synchronize(dev)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(S)]
+        for i in range(S):
+            flush.fill_(i & 255)  # 512 MiB write evicts the 64 MiB state from L2
+            evs[i][0].record(stream)
+            dstep(i)
+            evs[i][1].record(stream)
+        torch.cuda.synchronize(dev)
+        us = 1e3 * sum(a.elapsed_time(b) for a, b in evs) / S
+        state_bytes = 2 * Bd * Hvd * Dd * Dd * 4
+        vec_bytes = 4 * (2 * Bd * Hkd * Dd + 2 * Bd * Hvd * Dd + Bd * Hvd * Dd + Bd * Hvd)
+        gbs = (state_bytes + vec_bytes) / (us * 1e-6) / 1e9
+        # the same 256 steps back to back (state stays in L2 between steps: context only)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for i in range(S):
+            dstep(i)
+        g1.record(stream)
+        torch.cuda.synchronize(dev)
+        us_warm = 1e3 * g0.elapsed_time(g1) / S
+        dec = {"config": f"B={Bd}, Hk={Hkd}, Hv={Hvd}, Dk=Dv={Dd}, channel gate, fp32, {S} steps",
+               "us_per_step": us, "bytes_per_step": state_bytes + vec_bytes, "achieved_gbs": gbs,
+               "peak_gbs": peaks["hbm"], "frac": gbs / peaks["hbm"], "l2": "512 MiB flush before each step",
+               "us_per_step_back_to_back": us_warm}
+        del flush
+
+    # ------------------------------------------------------------------ CPU baseline (rank 0, N=1)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        import oracle
+
+        oracle.build()
+        v, n = oracle_sample()
+        cpu = {"value": v, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+               "sample": f"B=1, first {n} of {T} tokens of the workload, all {HV} value heads, fwd + bwd, fp64"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(),
+            "roofline": roof,
+            "step_roofline": {"t_star_ms": t_star * 1e3, "frac": t_star * 1e3 / ms,
+                              "note": "whole step vs max(flops/peak, bytes/peak) of the algorithm"},
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(round(launches_per_step * args.steps)),
+            "clocks": clocks, "kernels": kern, "decode": dec,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

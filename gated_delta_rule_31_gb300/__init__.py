@@ -22,7 +22,7 @@ from ._build import LIB as _LIB_PATH
 from ._build import build
 
 __all__ = ["build", "fwd_chunked", "bwd_chunked", "fwd_sequential", "decode_step", "GdrError",
-           "fwd_workspace_bytes", "bwd_workspace_bytes", "lib", "Problem", "workspace_status"]
+           "fwd_workspace_bytes", "bwd_workspace_bytes", "lib", "Problem", "workspace_status", "trace"]
 
 GDR_F32, GDR_BF16 = 0, 1
 GDR_GATE_SCALAR, GDR_GATE_CHANNEL = 0, 1
@@ -67,6 +67,11 @@ def lib():
         L.gdr_decode_step.restype = ctypes.c_int
         L.gdr_workspace_status.argtypes = [P, sz, st]
         L.gdr_workspace_status.restype = ctypes.c_int
+        L.gdr_trace_enable.argtypes = [ctypes.c_int]
+        L.gdr_trace_enable.restype = ctypes.c_int
+        L.gdr_trace_collect.argtypes = [ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float),
+                                        ctypes.c_int]
+        L.gdr_trace_collect.restype = ctypes.c_int
         _lib = L
     return _lib
 
@@ -217,3 +222,26 @@ def decode_step(q, k, v, g, beta, state, scale=None, use_qk_l2norm=True, out=Non
 def workspace_status(ws) -> int:
     """Reads and clears the status word of a chunked workspace (0 = ok, 5 = a wait expired)."""
     return int(lib().gdr_workspace_status(_ptr(ws), ctypes.c_size_t(ws.numel()), _stream(ws.device)))
+
+
+class trace:
+    """Context manager recording (kernel name, ms) for every library launch inside it:
+    ``with gdr.trace() as t: ...`` then ``t.records``."""
+
+    def __enter__(self):
+        lib().gdr_trace_collect(None, None, 0)
+        lib().gdr_trace_enable(1)
+        self.records = []
+        return self
+
+    def __exit__(self, *exc):
+        L = lib()
+        L.gdr_trace_enable(0)
+        n = L.gdr_trace_collect(None, None, 0) if exc[0] is not None else None
+        if n is None:
+            cap = 1 << 16
+            names = (ctypes.c_char_p * cap)()
+            ms = (ctypes.c_float * cap)()
+            n = L.gdr_trace_collect(names, ms, cap)
+            self.records = [(names[i].decode(), float(ms[i])) for i in range(min(n, cap))]
+        return False

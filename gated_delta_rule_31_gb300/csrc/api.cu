@@ -5,6 +5,8 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <vector>
+
 #include "../../include/gdr.h"
 #include "chunk.h"
 #include "kernels.h"
@@ -30,11 +32,15 @@ gdr_status check_problem(const gdr_problem* p, bool decode) {
     return GDR_OK;
 }
 
-gdr_status check_ptrs(std::initializer_list<const void*> required, std::initializer_list<const void*> optional) {
+// `required` pointers may be null only when the problem has no token (B * T == 0: empty
+// tensors have no storage); every non-null pointer must be 16-byte aligned.
+gdr_status check_ptrs(const gdr_problem* p, std::initializer_list<const void*> required,
+                      std::initializer_list<const void*> optional) {
+    const bool empty = p->B == 0 || p->T == 0;
     for (const void* x : required)
-        if (!x) return GDR_ERR_INVALID_ARG;
+        if (!x && !empty) return GDR_ERR_INVALID_ARG;
     for (const void* x : required)
-        if (!aligned16(x)) return GDR_ERR_INVALID_ARG;
+        if (x && !aligned16(x)) return GDR_ERR_INVALID_ARG;
     for (const void* x : optional)
         if (x && !aligned16(x)) return GDR_ERR_INVALID_ARG;
     return GDR_OK;
@@ -69,9 +75,65 @@ ChunkProblem chunk_problem(const gdr_problem* p) {
     return c;
 }
 
+struct TraceRec {
+    const char* name;
+    cudaEvent_t start, stop;
+};
+bool g_trace_on = false;
+std::vector<TraceRec> g_trace;
+std::vector<cudaEvent_t> g_event_pool;
+
+cudaEvent_t pooled_event() {
+    if (!g_event_pool.empty()) {
+        cudaEvent_t e = g_event_pool.back();
+        g_event_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+}
+
 }  // namespace
 
+namespace gdr {
+void trace_begin(const char* name, cudaStream_t s) {
+    if (!g_trace_on) return;
+    TraceRec r{name, pooled_event(), pooled_event()};
+    cudaEventRecord(r.start, s);
+    g_trace.push_back(r);
+}
+void trace_end(cudaStream_t s) {
+    if (!g_trace_on || g_trace.empty()) return;
+    cudaEventRecord(g_trace.back().stop, s);
+}
+}  // namespace gdr
+
 extern "C" {
+
+gdr_status gdr_trace_enable(int on) {
+    g_trace_on = on != 0;
+    return GDR_OK;
+}
+
+int gdr_trace_collect(const char** names, float* ms, int max) {
+    const int n = (int)g_trace.size();
+    for (int i = 0; i < n; i++) {
+        TraceRec& r = g_trace[i];
+        float t = 0.f;
+        if (cudaEventSynchronize(r.stop) != cudaSuccess || cudaEventElapsedTime(&t, r.start, r.stop) != cudaSuccess)
+            t = -1.f;
+        if (i < max) {
+            if (names) names[i] = r.name;
+            if (ms) ms[i] = t;
+        }
+        g_event_pool.push_back(r.start);
+        g_event_pool.push_back(r.stop);
+    }
+    g_trace.clear();
+    return n;
+}
+
 
 const char* gdr_status_string(gdr_status s) {
     switch (s) {
@@ -99,7 +161,7 @@ gdr_status gdr_fwd_sequential(const gdr_problem* p, const void* q, const void* k
                               const float* beta, const float* h0, void* o, float* ht, gdr_stream_t stream) {
     gdr_status s = check_problem(p, false);
     if (s != GDR_OK) return s;
-    if ((s = check_ptrs({q, k, v, g, beta, o}, {h0, ht})) != GDR_OK) return s;
+    if ((s = check_ptrs(p, {q, k, v, g, beta, o}, {h0, ht})) != GDR_OK) return s;
     if (p->B == 0) return GDR_OK;
     RecurrentArgs a = recurrent_args(p, q, k, v, g, beta, h0, o, ht);
     return launch_recurrent(a, false, (cudaStream_t)stream) == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
@@ -109,7 +171,7 @@ gdr_status gdr_decode_step(const gdr_problem* p, const void* q, const void* k, c
                            const float* beta, float* state, void* o, gdr_stream_t stream) {
     gdr_status s = check_problem(p, true);
     if (s != GDR_OK) return s;
-    if ((s = check_ptrs({q, k, v, g, beta, state, o}, {})) != GDR_OK) return s;
+    if ((s = check_ptrs(p, {q, k, v, g, beta, state, o}, {})) != GDR_OK) return s;
     if (p->B == 0) return GDR_OK;
     RecurrentArgs a = recurrent_args(p, q, k, v, g, beta, state, o, state);
     return launch_recurrent(a, true, (cudaStream_t)stream) == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
@@ -120,7 +182,7 @@ gdr_status gdr_fwd_chunked(const gdr_problem* p, const void* q, const void* k, c
                            gdr_stream_t stream) {
     gdr_status s = check_problem(p, false);
     if (s != GDR_OK) return s;
-    if ((s = check_ptrs({q, k, v, g, beta, o}, {h0, ht})) != GDR_OK) return s;
+    if ((s = check_ptrs(p, {q, k, v, g, beta, o}, {h0, ht})) != GDR_OK) return s;
     if ((s = check_chunked_support(p)) != GDR_OK) return s;
     const size_t need = chunk_fwd_workspace(chunk_problem(p));
     if (!ws || ws_bytes < need) return GDR_ERR_WORKSPACE;
@@ -146,7 +208,7 @@ gdr_status gdr_bwd_chunked(const gdr_problem* p, const void* q, const void* k, c
                            gdr_stream_t stream) {
     gdr_status s = check_problem(p, false);
     if (s != GDR_OK) return s;
-    if ((s = check_ptrs({q, k, v, g, beta, do_, dq, dk, dv, dg, dbeta}, {h0, dht, dh0})) != GDR_OK) return s;
+    if ((s = check_ptrs(p, {q, k, v, g, beta, do_, dq, dk, dv, dg, dbeta}, {h0, dht, dh0})) != GDR_OK) return s;
     if ((s = check_chunked_support(p)) != GDR_OK) return s;
     const size_t need = chunk_bwd_workspace(chunk_problem(p));
     if (!ws || ws_bytes < need) return GDR_ERR_WORKSPACE;

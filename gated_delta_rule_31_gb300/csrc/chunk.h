@@ -33,6 +33,8 @@ constexpr uint32_t REC_P = 65536;        // P     [64 tok x 64 tok]   8 KB
 constexpr uint32_t REC_U = 73728;        // U~    4 x [64 tok x 32] SW64 slices, 4 KB each
 constexpr uint32_t REC_BYTES = 90112;
 constexpr uint32_t STATE_IMG = 32768;    // one bf16 [128 d x 128 v] SW128 state image
+// Extra per-chunk record kept for the backward: T = (I + A)^-1 [64 x 64] and W [64 x 128].
+constexpr uint32_t REC2_T = 0, REC2_W = 8192, REC2_BYTES = 24576;
 
 struct ChunkProblem {
     int B, T, Hk, Hv, NC;
@@ -43,6 +45,7 @@ struct ChunkProblem {
 struct WsLayout {
     size_t gam;      // float [B*Hv][ncpad]: Gamma_C per chunk
     size_t rec;      // records [B*Hv][NC]
+    size_t rec2;     // bwd: T and W per chunk [B*Hv][NC]
     size_t hs;       // bwd: chunk-start states [B*Hv][NC] images
     size_t dhs;      // bwd: chunk-end state gradients [B*Hv][NC] images
     size_t total;
@@ -58,8 +61,10 @@ inline WsLayout ws_layout(const ChunkProblem& p, bool bwd) {
     w.gam = 256;
     w.rec = round_up(w.gam + nh * w.ncpad * sizeof(float), 1024);
     size_t end = w.rec + nh * p.NC * (size_t)REC_BYTES;
-    w.hs = w.dhs = 0;
+    w.rec2 = w.hs = w.dhs = 0;
     if (bwd) {
+        w.rec2 = end;
+        end = w.rec2 + nh * p.NC * (size_t)REC2_BYTES;
         w.hs = end;
         w.dhs = w.hs + nh * p.NC * (size_t)STATE_IMG;
         end = w.dhs + nh * p.NC * (size_t)STATE_IMG;
@@ -97,6 +102,7 @@ struct PrepArgs {
     const float *g, *beta;
     float* gam;
     uint8_t* rec;
+    uint8_t* rec2;  // null in the forward
     int* status;
     int ncpad;
 };

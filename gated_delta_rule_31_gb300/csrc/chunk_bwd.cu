@@ -1,10 +1,729 @@
-// chunk_bwd.cu - backward (VJP) of the chunked gated delta rule.
+// chunk_bwd.cu - backward (VJP) of the chunked gated delta rule, the "chunked case" of
+// "Adding VJP for gated delta net" (MLX PR #4565): dq, dk, dv, dg, dbeta and dh0 for the
+// loss <do, o> + <dht, ht>, through the in-kernel q/k L2 norm ("fold q/k L2-norm into the
+// gated_delta_rule kernel": the kernel owns the normalisation, so no normalised q/k is
+// ever stored). Launch sequence:
+//   prep (also keeps T and W per chunk)  ->  forward scan storing the chunk-start states
+//   ->  reverse scan storing the chunk-end state gradients (and dh0)  ->  grad_kernel.
+// grad_kernel: one CTA per (b, key head, chunk); it loops over the value heads that share
+// the key head, so dq and dk are summed over the group on chip (deterministic, no atomics).
+// Per value head, with H0 the chunk-start state, dH1 the chunk-end state gradient:
+//   U   = U~ - W H0                  dU  = P^T dO + Kbar dH1
+//   dP  = dO U^T  -> dS = scale E .* dP, Z = dP .* P      X = dO H0^T
+//   dQ^ += scale diag(Gamma) X + dS diag(rk) K            dK^ += (diag(rq) dS)^T Q
+//   Y   = U dH1^T -> dK^ += diag(b) Y, db = rk .* rowsum(K .* Y)
+//   dW  = -dU H0^T;  dT = dU V^T diag(beta) + dW K^T diag(beta Gamma rk)
+//   dV  = diag(beta) T^T dU;  T^T dW -> dK^ += diag(beta Gamma) T^T dW
+//   dA  = strict_lower(-T^T (dT T^T));  dK^ += N K with N_rj = rk_j (M_rj + M_jr), M = beta_r E .* dA
+//   dgamma from every Gamma, E, b, Gamma_C term;  dg = reverse cumsum of dgamma in the chunk
+//   dq = rq (dQ^ - q^ (q^ . dQ^)), likewise dk (after the group sum).
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
 
 #include "chunk.h"
+#include "common.cuh"
+#include "kernels.h"
+#include "tma_host.h"
 
 namespace gdr {
 
-cudaError_t launch_chunk_bwd(const ChunkBwdArgs&, cudaStream_t) { return cudaErrorNotSupported; }
+// shared memory (offsets from a 1024-aligned base)
+constexpr uint32_t G_KQ = 0;        // k rows 0-63, q rows 64-127 (panels 16 KB)      [whole CTA]
+constexpr uint32_t G_V = 32768;     // v [64 x 128]; later M fp32 [64][64]
+constexpr uint32_t G_DO = 49152;    // dO [64 x 128]; later dSq image [64 x 64]
+constexpr uint32_t G_H0 = 65536;    // H0 image [128 d x 128 v]; later dW image [64 x 128]
+constexpr uint32_t G_DH = 98304;    // dH1 image; later dT (+0), Yt (+8K), N (+16K) images
+constexpr uint32_t G_T = 131072;    // T image [64 x 64]
+constexpr uint32_t G_W = 139264;    // W image [64 x 128]; later U image
+constexpr uint32_t G_P = 155648;    // P image [64 x 64]; later dSk image
+constexpr uint32_t G_KB = 163840;   // Kbar image [64 x 128]; later dU image
+constexpr uint32_t G_GF = 180224;   // G = K K^T fp32 [64][64]                            [whole CTA]
+constexpr uint32_t G_ZS = 196608;   // fp32 [64][64] scratch (column sums)
+constexpr uint32_t G_SM = 212992;   // small arrays
+constexpr uint32_t G_BYTES = G_SM + 4096;
+static_assert(G_BYTES + 1024 <= 232448, "grad smem");
+
+// TMEM columns: dQ^ accumulator, dK^ accumulator (both M=64 x 128), two temporaries.
+constexpr uint32_t TM_DQ = 0, TM_DK = 128, TM_T1 = 256, TM_T2 = 384;
+
+struct GradArgs {
+    ChunkProblem p;
+    const float *g, *beta;
+    const uint8_t *rec, *rec2, *hs, *dhs;
+    const float* gam;  // Gamma_C per chunk (unused here: recomputed)
+    float *dq, *dk, *dv, *dg, *dbeta;
+    int* status;
+};
+
+__device__ __forceinline__ void unpack8b(const uint4& u, float* x) {
+    x[0] = bf16lo(u.x); x[1] = bf16hi(u.x); x[2] = bf16lo(u.y); x[3] = bf16hi(u.y);
+    x[4] = bf16lo(u.z); x[5] = bf16hi(u.z); x[6] = bf16lo(u.w); x[7] = bf16hi(u.w);
+}
+__device__ __forceinline__ void st_chunk8(uint32_t addr, const float* x, float s) {
+    st_shared_v4(addr, pack_bf16(s * x[0], s * x[1]), pack_bf16(s * x[2], s * x[3]), pack_bf16(s * x[4], s * x[5]),
+                 pack_bf16(s * x[6], s * x[7]));
+}
+// 64 consecutive fp32 columns of this warp's 32 TMEM lanes
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
+    tmem_ld32(taddr, v);
+    tmem_ld32(taddr + 32, v + 32);
+}
+
+__global__ void __launch_bounds__(256, 1)
+    grad_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo, GradArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = align1024(smem_raw);
+    const uint32_t sb = smem_u32(sm);
+    __shared__ uint64_t bar_ld, bar_mma;
+    __shared__ uint32_t tmem_sh;
+    __shared__ int abort_sh;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
+    const ChunkProblem& P = a.p;
+    const int G = P.Hv / P.Hk;
+    const int t0 = c * kChunk;
+    // M=64 accumulator mapping: row r in lanes 0-15 of sub-partition lg; h = column half
+    const int lg = warp & 3, h = warp >> 2;
+    const int r = 16 * lg + (lane & 15);
+    const bool act = lane < 16;
+    const bool rowvalid = act && (t0 + r < P.T);
+
+    float* GF = reinterpret_cast<float*>(sm + G_GF);
+    float* ZS = reinterpret_cast<float*>(sm + G_ZS);
+    float* MF = reinterpret_cast<float*>(sm + G_V);
+    float* rk = reinterpret_cast<float*>(sm + G_SM);  // [64]
+    float* rq = rk + 64;                                // [64]
+    float* gam = rq + 64;                               // [64]
+    float* bet = gam + 64;                              // [64]
+    float* dgp = bet + 64;                              // [2][64] dgamma partials by column half
+    float* dbp = dgp + 128;                             // [2][64] dbeta partials
+    float* sb3 = dbp + 128;                             // [2][64] b_r db_r partials
+    float* dgc = sb3 + 128;                             // [64] column-sum terms of dgamma
+    float* part = dgc + 64;                             // [2][64] norm-backward partial dots
+    float* red = part + 128;                            // [8] block reduction
+    float* hdh = red + 8;                               // <dH1, H0>
+
+    uint32_t ld_phase = 0, mma_phase = 0;
+    if (tid == 0) {
+        abort_sh = 0;
+        mbar_init(&bar_ld, 1);
+        mbar_init(&bar_mma, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&tmem_sh, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = tmem_sh;
+
+    auto wait_ld = [&](int site) -> bool {
+        bool ok = mbar_wait(&bar_ld, ld_phase, &abort_sh, a.status, site);
+        ld_phase ^= 1;
+        return !__syncthreads_or(!ok);
+    };
+    auto wait_mma = [&](int site) -> bool {
+        bool ok = mbar_wait(&bar_mma, mma_phase, &abort_sh, a.status, site);
+        mma_phase ^= 1;
+        ok = !__syncthreads_or(!ok);
+        tc_fence_after();
+        return ok;
+    };
+    auto sync_for_mma = [&]() {  // make generic smem writes / TMEM stores visible to the next MMAs
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncthreads();
+    };
+    auto mma = [&](uint32_t col, uint64_t ad, uint64_t bd, uint32_t id, bool acc) {
+        mma_bf16(tm + col, ad, bd, id, acc ? 1u : 0u);
+    };
+    const uint32_t id64x128_kk = idesc_bf16(64, 128, 0, 0), id64x128_km = idesc_bf16(64, 128, 0, 1),
+                   id64x128_mm = idesc_bf16(64, 128, 1, 1), id64x64_kk = idesc_bf16(64, 64, 0, 0),
+                   id64x64_mm = idesc_bf16(64, 64, 1, 1);
+
+    // ---------------------------------------------------------------- k, q of the chunk
+    if (tid == 0) {
+        mbar_expect_tx(&bar_ld, 4 * 8192);
+        tma_load_4d(sm + G_KQ + 0, &mk, 0, hk, t0, b, &bar_ld);
+        tma_load_4d(sm + G_KQ + 16384, &mk, 64, hk, t0, b, &bar_ld);
+        tma_load_4d(sm + G_KQ + 8192, &mq, 0, hk, t0, b, &bar_ld);
+        tma_load_4d(sm + G_KQ + 24576, &mq, 64, hk, t0, b, &bar_ld);
+    }
+    if (!wait_ld(40)) goto teardown;
+    {
+        const int row = tid >> 1, half = tid & 1;
+        const uint32_t base = sb + G_KQ + half * 16384 + row * 128;
+        float ss = 0.f;
+#pragma unroll
+        for (int ch = 0; ch < 8; ch++) {
+            float x[8];
+            unpack8b(ld_shared_v4(base + ch * 16), x);
+#pragma unroll
+            for (int e = 0; e < 8; e++) ss += x[e] * x[e];
+        }
+        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+        if (half == 0) {
+            const float f = P.use_norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
+            if (row < 64) rk[row] = f; else rq[row - 64] = f;
+        }
+    }
+    // G = K K^T into TMP1 (M=64, N=64)
+    if (tid == 0) {
+        tc_fence_after();
+        for (int k0 = 0; k0 < kD; k0 += 16)
+            mma(TM_T1, desc_kmajor(sb + G_KQ, 128, 0, k0), desc_kmajor(sb + G_KQ, 128, 0, k0), id64x64_kk, k0 > 0);
+        mma_commit(&bar_mma);
+    }
+    if (!wait_mma(41)) goto teardown;
+    {
+        float v[32];
+        tmem_ld32(tmem_at(tm, 32 * lg, TM_T1 + 32 * h), v);
+        tmem_wait_ld();
+        if (act) {
+#pragma unroll
+            for (int e = 0; e < 32; e++) GF[r * 64 + 32 * h + e] = v[e];
+        }
+        // zero the dQ^ / dK^ accumulators: warp covers its 32 lanes x 128 columns
+        float z[32];
+#pragma unroll
+        for (int e = 0; e < 32; e++) z[e] = 0.f;
+#pragma unroll
+        for (int q = 0; q < 4; q++) tmem_st32(tmem_at(tm, 32 * lg, 128 * h + 32 * q), z);
+        tmem_wait_st();
+    }
+    sync_for_mma();
+
+    for (int hv = hk * G; hv < (hk + 1) * G; hv++) {
+        const size_t bh = (size_t)b * P.Hv + hv;
+        const size_t idx = bh * P.NC + c;
+        const uint8_t* rec = a.rec + idx * REC_BYTES;
+        const uint8_t* rec2 = a.rec2 + idx * REC2_BYTES;
+        if (tid == 0) {
+            mbar_expect_tx(&bar_ld, 4 * 8192 + 2 * 32768 + 8192 + 16384 + 8192 + 16384);
+            tma_load_4d(sm + G_V + 0, &mv, 0, hv, t0, b, &bar_ld);
+            tma_load_4d(sm + G_V + 8192, &mv, 64, hv, t0, b, &bar_ld);
+            tma_load_4d(sm + G_DO + 0, &mdo, 0, hv, t0, b, &bar_ld);
+            tma_load_4d(sm + G_DO + 8192, &mdo, 64, hv, t0, b, &bar_ld);
+            bulk_load(sm + G_H0, a.hs + idx * STATE_IMG, 32768, &bar_ld);
+            bulk_load(sm + G_DH, a.dhs + idx * STATE_IMG, 32768, &bar_ld);
+            bulk_load(sm + G_T, rec2 + REC2_T, 8192, &bar_ld);
+            bulk_load(sm + G_W, rec2 + REC2_W, 16384, &bar_ld);
+            bulk_load(sm + G_P, rec + REC_P, 8192, &bar_ld);
+            bulk_load(sm + G_KB, rec + REC_K, 16384, &bar_ld);
+        }
+        if (tid < 64) {
+            const int t = t0 + tid;
+            float gv = 0.f, bv = 0.f;
+            if (t < P.T) {
+                const size_t bt = ((size_t)b * P.T + t) * P.Hv + hv;
+                gv = a.g[bt];
+                bv = a.beta[bt];
+            }
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, gv, o);
+                if (lane >= o) gv += y;
+            }
+            gam[tid] = gv;
+            bet[tid] = bv;
+            dgc[tid] = 0.f;
+        }
+        if (tid < 128) {
+            dgp[tid] = 0.f;
+            dbp[tid] = 0.f;
+            sb3[tid] = 0.f;
+        }
+        __syncthreads();
+        if (tid >= 32 && tid < 64) gam[tid] += gam[31];
+        if (!wait_ld(42)) goto teardown;
+        const float gC = gam[63];
+
+        // ------------------------------------------------------------ M1: W H0, dU
+        if (tid == 0) {
+            tc_fence_after();
+            for (int k0 = 0; k0 < kD; k0 += 16)
+                mma(TM_T1, desc_kmajor(sb + G_W, 64, 0, k0), desc_mnmajor(sb + G_H0, 128, 0, k0), id64x128_km,
+                    k0 > 0);
+            for (int k0 = 0; k0 < kChunk; k0 += 16)
+                mma(TM_T2, desc_mnmajor(sb + G_P, 64, 0, k0), desc_mnmajor(sb + G_DO, 64, 0, k0), id64x128_mm,
+                    k0 > 0);
+            for (int k0 = 0; k0 < kD; k0 += 16)
+                mma(TM_T2, desc_kmajor(sb + G_KB, 64, 0, k0), desc_mnmajor(sb + G_DH, 128, 0, k0), id64x128_km,
+                    true);
+            mma_commit(&bar_mma);
+        }
+        {  // <dH1, H0> over the two bf16 images (same layout, so elementwise)
+            float s = 0.f;
+            for (int i = tid; i < 2048; i += 256) {
+                float x[8], y[8];
+                unpack8b(ld_shared_v4(sb + G_H0 + i * 16), x);
+                unpack8b(ld_shared_v4(sb + G_DH + i * 16), y);
+#pragma unroll
+                for (int e = 0; e < 8; e++) s += x[e] * y[e];
+            }
+            s = warp_sum(s);
+            if (lane == 0) red[warp] = s;
+        }
+        if (!wait_mma(43)) goto teardown;
+        if (tid == 0) {
+            float s = 0.f;
+            for (int w = 0; w < 8; w++) s += red[w];
+            *hdh = s;
+        }
+        {  // U = U~ - W H0 -> U image (G_W);  dU -> dU image (G_KB)
+            float x[64];
+            tmem_ld64(tmem_at(tm, 32 * lg, TM_T1 + 64 * h), x);
+            tmem_wait_ld();
+            if (act) {
+#pragma unroll
+                for (int q = 0; q < 8; q++) {
+                    const int col = 64 * h + 8 * q;
+                    const uint4 u = *reinterpret_cast<const uint4*>(rec + REC_U + (col >> 5) * 4096 +
+                                                                    sw64_chunk(r, q & 3));
+                    float ut[8];
+                    unpack8b(u, ut);
+#pragma unroll
+                    for (int e = 0; e < 8; e++) ut[e] -= x[8 * q + e];
+                    st_chunk8(sb + G_W + sw128_chunk(r, 8 * h + q, 64), ut, 1.f);
+                }
+            }
+            tmem_ld64(tmem_at(tm, 32 * lg, TM_T2 + 64 * h), x);
+            tmem_wait_ld();
+            if (act) {
+#pragma unroll
+                for (int q = 0; q < 8; q++) st_chunk8(sb + G_KB + sw128_chunk(r, 8 * h + q, 64), x + 8 * q, 1.f);
+            }
+        }
+        sync_for_mma();
+
+        // ------------------------------------------------------------ M2: dP = dO U^T, X = dO H0^T
+        if (tid == 0) {
+            tc_fence_after();
+            for (int k0 = 0; k0 < kD; k0 += 16) {
+                mma(TM_T2, desc_kmajor(sb + G_DO, 64, 0, k0), desc_kmajor(sb + G_W, 64, 0, k0), id64x64_kk, k0 > 0);
+                mma(TM_T1, desc_kmajor(sb + G_DO, 64, 0, k0), desc_kmajor(sb + G_H0, 128, 0, k0), id64x128_kk,
+                    k0 > 0);
+            }
+            mma_commit(&bar_mma);
+        }
+        if (!wait_mma(44)) goto teardown;
+        {
+            const float gr = gam[r], Gr = expf(gr);
+            {  // X: dgamma_r += scale Gamma_r rq_r sum_d Q_rd X_rd; dQ^ += scale Gamma_r X_r
+                float x[64], dq[64];
+                tmem_ld64(tmem_at(tm, 32 * lg, TM_T1 + 64 * h), x);
+                tmem_ld64(tmem_at(tm, 32 * lg, TM_DQ + 64 * h), dq);
+                tmem_wait_ld();
+                const float f = P.scale * Gr;
+                float dot = 0.f;
+#pragma unroll
+                for (int q = 0; q < 8; q++) {
+                    float qq[8];
+                    unpack8b(ld_shared_v4(sb + G_KQ + sw128_chunk(64 + r, 8 * h + q, 128)), qq);
+#pragma unroll
+                    for (int e = 0; e < 8; e++) {
+                        dot += qq[e] * x[8 * q + e];
+                        dq[8 * q + e] += f * x[8 * q + e];
+                    }
+                }
+                tmem_st32(tmem_at(tm, 32 * lg, TM_DQ + 64 * h), dq);
+                tmem_st32(tmem_at(tm, 32 * lg, TM_DQ + 64 * h + 32), dq + 32);
+                if (act) dgp[h * 64 + r] += f * rq[r] * dot;
+            }
+            {  // dP: Z = dP .* P, dS = scale E .* dP; dSk = dS diag(rk) (G_P), dSq = diag(rq) dS (G_DO)
+                float v[32];
+                tmem_ld32(tmem_at(tm, 32 * lg, TM_T2 + 32 * h), v);
+                tmem_wait_ld();
+                if (act) {
+                    float pr[32];
+#pragma unroll
+                    for (int q = 0; q < 4; q++) unpack8b(ld_shared_v4(sb + G_P + sw128_chunk(r, 4 * h + q, 64)), pr + 8 * q);
+                    float zs = 0.f;
+                    float sk[32], sq[32];
+#pragma unroll
+                    for (int e = 0; e < 32; e++) {
+                        const int j = 32 * h + e;
+                        const float z = v[e] * pr[e];
+                        zs += z;
+                        ZS[r * 64 + j] = z;
+                        const float ds = (j <= r) ? P.scale * expf(gr - gam[j]) * v[e] : 0.f;
+                        sk[e] = ds * rk[j];
+                        sq[e] = ds * rq[r];
+                    }
+                    dgp[h * 64 + r] += zs;
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+                        st_chunk8(sb + G_P + sw128_chunk(r, 4 * h + q, 64), sk + 8 * q, 1.f);
+                        st_chunk8(sb + G_DO + sw128_chunk(r, 4 * h + q, 64), sq + 8 * q, 1.f);
+                    }
+                }
+            }
+            tmem_wait_st();
+        }
+        sync_for_mma();
+        if (tid < 64) {  // column sums of Z: dgamma_j -= sum_r Z_rj
+            float s = 0.f;
+            for (int i = 0; i < 64; i++) s += ZS[i * 64 + tid];
+            dgc[tid] -= s;
+        }
+
+        // ------------------------------------------------------------ M3
+        if (tid == 0) {
+            tc_fence_after();
+            for (int k0 = 0; k0 < kChunk; k0 += 16) {
+                // dQ^ += dSk K ;  dK^ += dSq^T Q
+                mma(TM_DQ, desc_kmajor(sb + G_P, 64, 0, k0), desc_mnmajor(sb + G_KQ, 128, 0, k0), id64x128_km, true);
+                mma(TM_DK, desc_mnmajor(sb + G_DO, 64, 0, k0), desc_mnmajor(sb + G_KQ, 128, 0, 64 + k0), id64x128_mm,
+                    true);
+            }
+            for (int k0 = 0; k0 < kD; k0 += 16) {
+                // Y = U dH1^T ;  dWn = dU H0^T
+                mma(TM_T1, desc_kmajor(sb + G_W, 64, 0, k0), desc_kmajor(sb + G_DH, 128, 0, k0), id64x128_kk, k0 > 0);
+                mma(TM_T2, desc_kmajor(sb + G_KB, 64, 0, k0), desc_kmajor(sb + G_H0, 128, 0, k0), id64x128_kk,
+                    k0 > 0);
+            }
+            mma_commit(&bar_mma);
+        }
+        if (!wait_mma(45)) goto teardown;
+        {
+            const float br = expf(gC - gam[r]);
+            {  // Y: db_r = rk_r sum_d K_rd Y_rd; dK^ += b_r Y_r
+                float y[64], dk[64];
+                tmem_ld64(tmem_at(tm, 32 * lg, TM_T1 + 64 * h), y);
+                tmem_ld64(tmem_at(tm, 32 * lg, TM_DK + 64 * h), dk);
+                tmem_wait_ld();
+                float dot = 0.f;
+#pragma unroll
+                for (int q = 0; q < 8; q++) {
+                    float kk[8];
+                    unpack8b(ld_shared_v4(sb + G_KQ + sw128_chunk(r, 8 * h + q, 128)), kk);
+#pragma unroll
+                    for (int e = 0; e < 8; e++) {
+                        dot += kk[e] * y[8 * q + e];
+                        dk[8 * q + e] += br * y[8 * q + e];
+                    }
+                }
+                tmem_st32(tmem_at(tm, 32 * lg, TM_DK + 64 * h), dk);
+                tmem_st32(tmem_at(tm, 32 * lg, TM_DK + 64 * h + 32), dk + 32);
+                if (act) sb3[h * 64 + r] = br * rk[r] * dot;
+            }
+            {  // dW = -dWn -> dW image (G_H0)
+                float x[64];
+                tmem_ld64(tmem_at(tm, 32 * lg, TM_T2 + 64 * h), x);
+                tmem_wait_ld();
+                if (act) {
+#pragma unroll
+                    for (int q = 0; q < 8; q++) st_chunk8(sb + G_H0 + sw128_chunk(r, 8 * h + q, 64), x + 8 * q, -1.f);
+                }
+            }
+            tmem_wait_st();
+        }
+        sync_for_mma();
+
+        // ------------------------------------------------------------ M4: dT parts, T^T dU
+        if (tid == 0) {
+            tc_fence_after();
+            for (int k0 = 0; k0 < kD; k0 += 16) {
+                mma(TM_T1, desc_kmajor(sb + G_KB, 64, 0, k0), desc_kmajor(sb + G_V, 64, 0, k0), id64x64_kk, k0 > 0);
+                mma(TM_T1 + 64, desc_kmajor(sb + G_H0, 64, 0, k0), desc_kmajor(sb + G_KQ, 128, 0, k0), id64x64_kk,
+                    k0 > 0);
+            }
+            for (int k0 = 0; k0 < kChunk; k0 += 16)
+                mma(TM_T2, desc_mnmajor(sb + G_T, 64, 0, k0), desc_mnmajor(sb + G_KB, 64, 0, k0), id64x128_mm, k0 > 0);
+            mma_commit(&bar_mma);
+        }
+        if (!wait_mma(46)) goto teardown;
+        {
+            {  // dT_rj = beta_j (dU V^T + Gamma_j rk_j dW K^T)_rj -> dT image (G_DH)
+                float d1[32], d2[32];
+                tmem_ld32(tmem_at(tm, 32 * lg, TM_T1 + 32 * h), d1);
+                tmem_ld32(tmem_at(tm, 32 * lg, TM_T1 + 64 + 32 * h), d2);
+                tmem_wait_ld();
+                if (act) {
+#pragma unroll
+                    for (int e = 0; e < 32; e++) {
+                        const int j = 32 * h + e;
+                        d1[e] = bet[j] * (d1[e] + expf(gam[j]) * rk[j] * d2[e]);
+                    }
+#pragma unroll
+                    for (int q = 0; q < 4; q++) st_chunk8(sb + G_DH + sw128_chunk(r, 4 * h + q, 64), d1 + 8 * q, 1.f);
+                }
+            }
+            {  // T^T dU: dv = beta T^T dU; dbeta_r += sum_v V_rv (T^T dU)_rv
+                float x[64];
+                tmem_ld64(tmem_at(tm, 32 * lg, TM_T2 + 64 * h), x);
+                tmem_wait_ld();
+                if (act) {
+                    float dot = 0.f;
+#pragma unroll
+                    for (int q = 0; q < 8; q++) {
+                        float vv[8];
+                        unpack8b(ld_shared_v4(sb + G_V + sw128_chunk(r, 8 * h + q, 64)), vv);
+#pragma unroll
+                        for (int e = 0; e < 8; e++) dot += vv[e] * x[8 * q + e];
+                    }
+                    dbp[h * 64 + r] += dot;
+                    if (rowvalid) {
+                        const float br = bet[r];
+                        float4* dst = reinterpret_cast<float4*>(a.dv + (((size_t)b * P.T + t0 + r) * P.Hv + hv) * kD +
+                                                                64 * h);
+#pragma unroll
+                        for (int q = 0; q < 16; q++)
+                            dst[q] = make_float4(br * x[4 * q], br * x[4 * q + 1], br * x[4 * q + 2], br * x[4 * q + 3]);
+                    }
+                }
+            }
+        }
+        sync_for_mma();
+
+        // ------------------------------------------------------------ M5: T^T dW, Yt = dT T^T
+        if (tid == 0) {
+            tc_fence_after();
+            for (int k0 = 0; k0 < kChunk; k0 += 16) {
+                mma(TM_T2, desc_mnmajor(sb + G_T, 64, 0, k0), desc_mnmajor(sb + G_H0, 64, 0, k0), id64x128_mm, k0 > 0);
+                mma(TM_T1, desc_kmajor(sb + G_DH, 64, 0, k0), desc_kmajor(sb + G_T, 64, 0, k0), id64x64_kk, k0 > 0);
+            }
+            mma_commit(&bar_mma);
+        }
+        if (!wait_mma(47)) goto teardown;
+        {
+            {  // T^T dW: dK^ += beta Gamma (T^T dW); dbeta, dgamma from k^ . (T^T dW)
+                float x[64], dk[64];
+                tmem_ld64(tmem_at(tm, 32 * lg, TM_T2 + 64 * h), x);
+                tmem_ld64(tmem_at(tm, 32 * lg, TM_DK + 64 * h), dk);
+                tmem_wait_ld();
+                const float Gr = expf(gam[r]), bgr = bet[r] * Gr;
+                float dot = 0.f;
+#pragma unroll
+                for (int q = 0; q < 8; q++) {
+                    float kk[8];
+                    unpack8b(ld_shared_v4(sb + G_KQ + sw128_chunk(r, 8 * h + q, 128)), kk);
+#pragma unroll
+                    for (int e = 0; e < 8; e++) {
+                        dot += kk[e] * x[8 * q + e];
+                        dk[8 * q + e] += bgr * x[8 * q + e];
+                    }
+                }
+                tmem_st32(tmem_at(tm, 32 * lg, TM_DK + 64 * h), dk);
+                tmem_st32(tmem_at(tm, 32 * lg, TM_DK + 64 * h + 32), dk + 32);
+                if (act) {
+                    dbp[h * 64 + r] += Gr * rk[r] * dot;
+                    dgp[h * 64 + r] += bgr * rk[r] * dot;
+                }
+            }
+            {  // Yt -> image (G_DH + 8K)
+                float v[32];
+                tmem_ld32(tmem_at(tm, 32 * lg, TM_T1 + 32 * h), v);
+                tmem_wait_ld();
+                if (act) {
+#pragma unroll
+                    for (int q = 0; q < 4; q++) st_chunk8(sb + G_DH + 8192 + sw128_chunk(r, 4 * h + q, 64), v + 8 * q, 1.f);
+                }
+            }
+            tmem_wait_st();
+        }
+        sync_for_mma();
+
+        // ------------------------------------------------------------ M6: T^T Yt
+        if (tid == 0) {
+            tc_fence_after();
+            for (int k0 = 0; k0 < kChunk; k0 += 16)
+                mma(TM_T1, desc_mnmajor(sb + G_T, 64, 0, k0), desc_mnmajor(sb + G_DH + 8192, 64, 0, k0), id64x64_mm,
+                    k0 > 0);
+            mma_commit(&bar_mma);
+        }
+        if (!wait_mma(48)) goto teardown;
+        {  // dA = strict_lower(-T^T Yt); terms of A_rj = beta_r rk_r rk_j E_rj G_rj
+            float v[32];
+            tmem_ld32(tmem_at(tm, 32 * lg, TM_T1 + 32 * h), v);
+            tmem_wait_ld();
+            if (act) {
+                const float gr = gam[r], br = bet[r], rkr = rk[r];
+                float db = 0.f, zs = 0.f;
+#pragma unroll
+                for (int e = 0; e < 32; e++) {
+                    const int j = 32 * h + e;
+                    float m = 0.f, z = 0.f;
+                    if (j < r) {
+                        const float dA = -v[e];
+                        const float E = expf(gr - gam[j]);
+                        const float kk = rkr * rk[j] * GF[r * 64 + j];
+                        db += dA * E * kk;
+                        z = dA * br * E * kk;
+                        m = dA * br * E;
+                    }
+                    zs += z;
+                    ZS[r * 64 + j] = z;
+                    MF[r * 64 + j] = m;
+                }
+                dbp[h * 64 + r] += db;
+                dgp[h * 64 + r] += zs;
+            }
+        }
+        __syncthreads();
+        if (tid < 64) {
+            float s = 0.f;
+            for (int i = 0; i < 64; i++) s += ZS[i * 64 + tid];
+            dgc[tid] -= s;
+        }
+        if (act) {  // N_rj = rk_j (M_rj + M_jr) -> image (G_DH + 16K)
+            float nrow[32];
+#pragma unroll
+            for (int e = 0; e < 32; e++) {
+                const int j = 32 * h + e;
+                nrow[e] = rk[j] * (MF[r * 64 + j] + MF[j * 64 + r]);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; q++) st_chunk8(sb + G_DH + 16384 + sw128_chunk(r, 4 * h + q, 64), nrow + 8 * q, 1.f);
+        }
+        sync_for_mma();
+
+        // ------------------------------------------------------------ M7: dK^ += N K
+        if (tid == 0) {
+            tc_fence_after();
+            for (int k0 = 0; k0 < kChunk; k0 += 16)
+                mma(TM_DK, desc_kmajor(sb + G_DH + 16384, 64, 0, k0), desc_mnmajor(sb + G_KQ, 128, 0, k0), id64x128_km,
+                    true);
+            mma_commit(&bar_mma);
+        }
+        // per-head scalars: dgamma -> dg (reverse cumsum), dbeta
+        if (tid < 64) {
+            float s3 = sb3[tid] + sb3[64 + tid];
+            float dgam = dgp[tid] + dgp[64 + tid] + dgc[tid] - s3;
+            ZS[tid] = dgam;  // ZS column sums are done; reuse as a 64-vector
+        }
+        __syncthreads();
+        if (tid == 0) {
+            float tot = 0.f;
+            for (int i = 0; i < 64; i++) tot += sb3[i] + sb3[64 + i];
+            ZS[63] += tot + expf(gC) * (*hdh);  // Gamma_C <dH1, H0>
+        }
+        __syncthreads();
+        if (tid < 64 && t0 + tid < P.T) {
+            float s = 0.f;
+            for (int i = tid; i < 64; i++) s += ZS[i];
+            const size_t bt = ((size_t)b * P.T + t0 + tid) * P.Hv + hv;
+            a.dg[bt] = s;
+            a.dbeta[bt] = dbp[tid] + dbp[64 + tid];
+        }
+        if (!wait_mma(49)) goto teardown;
+    }
+
+    // ---------------------------------------------------------------- dq, dk: norm backward
+    {
+        float x[64];
+#pragma unroll 1
+        for (int which = 0; which < 2; which++) {  // 0: q, 1: k
+            const float* rho = which == 0 ? rq : rk;
+            const int krow = which == 0 ? 64 + r : r;
+            tmem_ld64(tmem_at(tm, 32 * lg, (which == 0 ? TM_DQ : TM_DK) + 64 * h), x);
+            tmem_wait_ld();
+            float xx[64];
+            float dot = 0.f;
+#pragma unroll
+            for (int q = 0; q < 8; q++) {
+                unpack8b(ld_shared_v4(sb + G_KQ + sw128_chunk(krow, 8 * h + q, 128)), xx + 8 * q);
+#pragma unroll
+                for (int e = 0; e < 8; e++) dot += xx[8 * q + e] * x[8 * q + e];
+            }
+            if (act) part[h * 64 + r] = dot;
+            __syncthreads();
+            if (rowvalid) {
+                const float rr = rho[r];
+                const float full = part[r] + part[64 + r];
+                float* dst = (which == 0 ? a.dq : a.dk) + (((size_t)b * P.T + t0 + r) * P.Hk + hk) * kD + 64 * h;
+                float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+                for (int q = 0; q < 16; q++) {
+                    float o4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        const int i = 4 * q + e;
+                        o4[e] = P.use_norm ? rr * (x[i] - rr * xx[i] * rr * full) : x[i];
+                    }
+                    d4[q] = make_float4(o4[0], o4[1], o4[2], o4[3]);
+                }
+            }
+            __syncthreads();
+        }
+    }
+
+teardown:
+    tc_fence_before();
+    __syncthreads();
+    if (abort_sh && tid == 0) {  // let copies still in flight land before the CTA exits
+        volatile int never = 0;
+        mbar_wait(&bar_ld, ld_phase, &never, nullptr, 0);
+        mbar_wait(&bar_mma, mma_phase, &never, nullptr, 0);
+    }
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tm, 512);
+}
+
+cudaError_t launch_chunk_bwd(const ChunkBwdArgs& a, cudaStream_t s) {
+    const ChunkProblem& p = a.p;
+    const WsLayout w = ws_layout(p, true);
+    uint8_t* ws = static_cast<uint8_t*>(a.ws);
+    CUtensorMap mq, mk, mv, mdo32, mdo64;
+    if (!make_qkv_maps(p, a.q, a.k, a.v, &mq, &mk, &mv)) return cudaErrorInvalidValue;
+    if (!make_map_4d_bf16(&mdo32, a.do_, kD, p.Hv, p.T, p.B, kSlice, kChunk, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !make_map_4d_bf16(&mdo64, a.do_, kD, p.Hv, p.T, p.B, 64, kChunk, CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    int* status = reinterpret_cast<int*>(ws);
+    PrepArgs pa;
+    pa.p = p;
+    pa.g = a.g;
+    pa.beta = a.beta;
+    pa.gam = reinterpret_cast<float*>(ws + w.gam);
+    pa.rec = ws + w.rec;
+    pa.rec2 = ws + w.rec2;
+    pa.status = status;
+    pa.ncpad = w.ncpad;
+    cudaError_t e = launch_prep(pa, mq, mk, mv, s);
+    if (e != cudaSuccess) return e;
+    ScanArgs sa;
+    sa.p = p;
+    sa.gam = pa.gam;
+    sa.rec = pa.rec;
+    sa.hinit = a.h0;
+    sa.o = nullptr;
+    sa.hfinal = nullptr;
+    sa.states = ws + w.hs;
+    sa.status = status;
+    sa.ncpad = w.ncpad;
+    if ((e = launch_scan(sa, SCAN_FWD_STATES, nullptr, s)) != cudaSuccess) return e;
+    sa.hinit = a.dht;
+    sa.hfinal = a.dh0;
+    sa.states = ws + w.dhs;
+    if ((e = launch_scan(sa, SCAN_BWD, &mdo32, s)) != cudaSuccess) return e;
+    GradArgs ga;
+    ga.p = p;
+    ga.g = a.g;
+    ga.beta = a.beta;
+    ga.rec = pa.rec;
+    ga.rec2 = pa.rec2;
+    ga.hs = ws + w.hs;
+    ga.dhs = ws + w.dhs;
+    ga.gam = pa.gam;
+    ga.dq = a.dq;
+    ga.dk = a.dk;
+    ga.dv = a.dv;
+    ga.dg = a.dg;
+    ga.dbeta = a.dbeta;
+    ga.status = status;
+    const int smem = G_BYTES + 1024;
+    if ((e = cudaFuncSetAttribute(grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+        return e;
+    dim3 grid(p.NC, p.Hk, p.B);
+    trace_begin("chunk_grad", s);
+    grad_kernel<<<grid, 256, smem, s>>>(mq, mk, mv, mdo64, ga);
+    trace_end(s);
+    return cudaGetLastError();
+}
 
 }  // namespace gdr

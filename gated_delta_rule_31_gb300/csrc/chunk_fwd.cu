@@ -16,6 +16,7 @@
 
 #include "chunk.h"
 #include "common.cuh"
+#include "kernels.h"
 #include "tma_host.h"
 
 namespace gdr {
@@ -33,6 +34,7 @@ constexpr uint32_t PS_SMALL = PS_SCR + 3 * 16 * 17 * 4;  // gamma[64], beta[64],
 constexpr uint32_t PS_BYTES = PS_SMALL + 1024;
 constexpr uint32_t PS_WBAR = PS_AT;               // [64 tok x 128 d] images (alias A/T)
 constexpr uint32_t PS_W = PS_AT + 16384;
+constexpr uint32_t PS_TIMG = PS_KQV + 40960;     // T image [64 x 64] (rows 64-127 of v slot 0)
 static_assert(PS_KQV % 1024 == 0 && PS_REC % 1024 == 0 && PS_TT % 1024 == 0 && PS_AT % 1024 == 0, "align");
 static_assert(PS_BYTES + 1024 <= 232448, "prep smem");
 
@@ -222,6 +224,11 @@ __global__ void __launch_bounds__(256, 1)
         const int row = tid >> 1, half = tid & 1;
         const int i = row & 63;
         const bool isw = row < 64;
+        if (isw && a.rec2) {  // T itself for the backward, in the free half of a v slot
+#pragma unroll
+            for (int q = 0; q < 4; q++)
+                st_chunk(sb + PS_TIMG + sw128_chunk(i, 4 * half + q, 64), Tm + i * LDA + 32 * half + 8 * q, 1.f);
+        }
 #pragma unroll
         for (int q = 0; q < 4; q++) {
             float x[8];
@@ -344,6 +351,12 @@ __global__ void __launch_bounds__(256, 1)
         const size_t bh = (size_t)b * P.Hv + hv;
         bulk_store(a.rec + (bh * P.NC + c) * REC_BYTES, sm + PS_REC, REC_BYTES);
         bulk_commit();
+        if (a.rec2) {
+            uint8_t* r2 = a.rec2 + (bh * P.NC + c) * REC2_BYTES;
+            bulk_store(r2 + REC2_T, sm + PS_TIMG, 8192);
+            bulk_store(r2 + REC2_W, sm + PS_W, 16384);
+            bulk_commit();
+        }
         a.gam[bh * a.ncpad + c] = expf(gam[63]);
         bulk_wait_all();
     }
@@ -351,10 +364,8 @@ teardown:
     tc_fence_before();
     __syncthreads();
     if (abort_sh && tid == 0) {  // let copies still in flight land before the CTA exits
-        uint32_t dummy = 0;
         volatile int never = 0;
         mbar_wait(&bar_tma, 0, &never, nullptr, 0);
-        (void)dummy;
     }
     __syncthreads();
     if (warp == 0) tmem_dealloc(tm, 256);
@@ -366,7 +377,9 @@ cudaError_t launch_prep(const PrepArgs& a, const CUtensorMap& mq, const CUtensor
     cudaError_t e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     dim3 grid(a.p.NC, a.p.Hv, a.p.B);
+    trace_begin("chunk_prep", s);
     prep_kernel<<<grid, 256, smem, s>>>(mq, mk, mv, a);
+    trace_end(s);
     return cudaGetLastError();
 }
 
@@ -601,18 +614,24 @@ cudaError_t launch_scan(const ScanArgs& a, int mode, const CUtensorMap* mdo, cud
         case SCAN_FWD_OUT:
             e = cudaFuncSetAttribute(scan_kernel<SCAN_FWD_OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
             if (e != cudaSuccess) return e;
+            trace_begin("chunk_scan_fwd", s);
             scan_kernel<SCAN_FWD_OUT><<<grid, 192, smem, s>>>(m, a);
+            trace_end(s);
             break;
         case SCAN_FWD_STATES:
             e = cudaFuncSetAttribute(scan_kernel<SCAN_FWD_STATES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      smem);
             if (e != cudaSuccess) return e;
+            trace_begin("chunk_scan_states", s);
             scan_kernel<SCAN_FWD_STATES><<<grid, 192, smem, s>>>(m, a);
+            trace_end(s);
             break;
         default:
             e = cudaFuncSetAttribute(scan_kernel<SCAN_BWD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
             if (e != cudaSuccess) return e;
+            trace_begin("chunk_scan_bwd", s);
             scan_kernel<SCAN_BWD><<<grid, 192, smem, s>>>(m, a);
+            trace_end(s);
             break;
     }
     return cudaGetLastError();
@@ -636,6 +655,7 @@ cudaError_t launch_chunk_fwd(const ChunkFwdArgs& a, cudaStream_t s) {
     pa.beta = a.beta;
     pa.gam = reinterpret_cast<float*>(ws + w.gam);
     pa.rec = ws + w.rec;
+    pa.rec2 = nullptr;
     pa.status = reinterpret_cast<int*>(ws);
     pa.ncpad = w.ncpad;
     cudaError_t e = launch_prep(pa, mq, mk, mv, s);

@@ -18,4 +18,8 @@ struct RecurrentArgs {
 };
 cudaError_t launch_recurrent(const RecurrentArgs& a, bool decode, cudaStream_t s);
 
+// Launch tracing (api.cu): no-ops unless gdr_trace_enable(1) was called.
+void trace_begin(const char* name, cudaStream_t s);
+void trace_end(cudaStream_t s);
+
 }  // namespace gdr

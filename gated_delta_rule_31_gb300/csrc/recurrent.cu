@@ -159,7 +159,9 @@ __global__ void __launch_bounds__(WARPS * 32) recurrent_rows_kernel(RecurrentArg
 template <int DK, typename TIn, int ROWS, int WARPS>
 static cudaError_t launch_rows(const RecurrentArgs& a, cudaStream_t s) {
     dim3 grid((a.Dv + WARPS * ROWS - 1) / (WARPS * ROWS), a.Hv, a.B);
+    trace_begin(a.T == 1 ? "decode_step" : "recurrent_fwd", s);
     recurrent_rows_kernel<DK, TIn, ROWS, WARPS><<<grid, WARPS * 32, 0, s>>>(a);
+    trace_end(s);
     return cudaGetLastError();
 }
 

@@ -119,6 +119,15 @@ gdr_status gdr_decode_step(const gdr_problem* p, const void* q, const void* k, c
  * chunked kernels: GDR_OK, or GDR_ERR_TIMEOUT if a bounded wait expired. */
 gdr_status gdr_workspace_status(void* ws, size_t ws_bytes, gdr_stream_t stream);
 
+/* Launch tracing for profiling. While enabled, every kernel the library launches is
+ * bracketed by two CUDA events recorded on its own stream (host-side events only; no
+ * device memory). gdr_trace_collect() waits for the recorded events, writes up to `max`
+ * (kernel name, milliseconds) pairs in launch order, clears the list and returns the
+ * number of launches recorded since the last collect (which may exceed `max`). Names
+ * point to static strings. Not thread-safe: trace from one host thread at a time. */
+gdr_status gdr_trace_enable(int on);
+int gdr_trace_collect(const char** names, float* ms, int max);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,175 @@
+"""The chunked form of the gated delta rule in plain numpy fp64, written the way the CUDA
+kernels organise it (same per-chunk operators, same folding of the L2-norm factors and
+decays into raw q/k operands). It is not the oracle and does not feed any stored value:
+tests check it against the oracle (sequential recurrence) to ~1e-12, which pins the
+chunk algebra the kernels implement, forward and backward, independently of CUDA.
+
+Per chunk (rows r = tokens, chunk length C), with K, Q raw keys/queries, rk/rq their
+norm factors, gamma the in-chunk cumulative log-decay, Gamma = exp(gamma),
+b = exp(gamma_C - gamma), E_rj = exp(gamma_r - gamma_j):
+    A   = strict_lower(beta_r rk_r rk_j E_rj (K K^T)_rj),  T = (I + A)^-1
+    W   = T diag(beta Gamma rk) K,    U~ = T diag(beta) V
+    P   = scale * tril(rq_r rk_j E_rj (Q K^T)_rj)
+    Kbar = diag(b rk) K,  Mneg = -Kbar^T W,  Qc = scale diag(Gamma rq) Q - P W
+    H1 = Gamma_C H0 + Mneg H0 + Kbar^T U~,   O = Qc H0 + P U~
+Backward scan: dH0 = Gamma_C dH1 + Mneg^T dH1 + Qc^T dO.
+"""
+import numpy as np
+
+
+def _norm_factor(x, on):
+    if not on:
+        return np.ones(x.shape[:-1])
+    return 1.0 / np.sqrt(np.sum(x * x, axis=-1) + 1e-6)
+
+
+def chunk_ops(K, Q, V, g, beta, scale, rk, rq):
+    C = K.shape[0]
+    gam = np.cumsum(g)
+    Gam = np.exp(gam)
+    b = np.exp(gam[-1] - gam)
+    diff = gam[:, None] - gam[None, :]
+    low = np.tril(np.ones((C, C)), -1)
+    lowi = np.tril(np.ones((C, C)))
+    E = np.where(lowi > 0, np.exp(np.where(lowi > 0, diff, 0.0)), 0.0)
+    A = low * (beta * rk)[:, None] * rk[None, :] * E * (K @ K.T)
+    T = np.linalg.inv(np.eye(C) + A)
+    W = T @ ((beta * Gam * rk)[:, None] * K)
+    Ut = T @ (beta[:, None] * V)
+    P = scale * lowi * rq[:, None] * rk[None, :] * E * (Q @ K.T)
+    Kbar = (b * rk)[:, None] * K
+    Mneg = -Kbar.T @ W
+    Qc = scale * (Gam * rq)[:, None] * Q - P @ W
+    return dict(gam=gam, Gam=Gam, b=b, E=E, A=A, T=T, W=W, Ut=Ut, P=P, Kbar=Kbar, Mneg=Mneg, Qc=Qc)
+
+
+def _chunks(T, C):
+    return [(s, min(s + C, T)) for s in range(0, T, C)]
+
+
+def _pad(x, n):
+    if x.shape[0] == n:
+        return x
+    out = np.zeros((n,) + x.shape[1:])
+    out[: x.shape[0]] = x
+    return out
+
+
+def forward(q, k, v, g, beta, h0, scale, norm=True, C=64):
+    """Scalar gate. Shapes as the oracle; returns o, ht and the per-chunk start states."""
+    B, T, Hk, Dk = q.shape
+    Hv, Dv = v.shape[2:]
+    grp = Hv // Hk
+    o = np.zeros((B, T, Hv, Dv))
+    ht = np.zeros((B, Hv, Dv, Dk))
+    states = {}
+    for b_ in range(B):
+        for hv in range(Hv):
+            hk = hv // grp
+            H = np.zeros((Dk, Dv)) if h0 is None else h0[b_, hv].T.copy()
+            for ci, (s, e) in enumerate(_chunks(T, C)):
+                K = _pad(k[b_, s:e, hk], C)
+                Q = _pad(q[b_, s:e, hk], C)
+                V = _pad(v[b_, s:e, hv], C)
+                gg = _pad(g[b_, s:e, hv], C)
+                bb = _pad(beta[b_, s:e, hv], C)
+                ops = chunk_ops(K, Q, V, gg, bb, scale, _norm_factor(K, norm), _norm_factor(Q, norm))
+                states[(b_, hv, ci)] = H.copy()
+                O = ops["Qc"] @ H + ops["P"] @ ops["Ut"]
+                H = np.exp(ops["gam"][-1]) * H + ops["Mneg"] @ H + ops["Kbar"].T @ ops["Ut"]
+                o[b_, s:e, hv] = O[: e - s]
+            ht[b_, hv] = H.T
+    return o, ht, states
+
+
+def backward(q, k, v, g, beta, h0, do, dht, scale, norm=True, C=64):
+    """Gradients of <do, o> + <dht, ht> by chunks: recompute the chunk-start states, run the
+    reverse scan for the chunk-end state gradients, then chunk-local gradients."""
+    B, T, Hk, Dk = q.shape
+    Hv, Dv = v.shape[2:]
+    grp = Hv // Hk
+    _, _, states = forward(q, k, v, g, beta, h0, scale, norm, C)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    dg = np.zeros_like(g)
+    dbeta = np.zeros_like(beta)
+    dh0 = np.zeros((B, Hv, Dv, Dk))
+    chunks = _chunks(T, C)
+    for b_ in range(B):
+        for hk in range(Hk):
+            dQh = {ci: np.zeros((C, Dk)) for ci in range(len(chunks))}
+            dKh = {ci: np.zeros((C, Dk)) for ci in range(len(chunks))}
+            for hv in range(hk * grp, (hk + 1) * grp):
+                dH = np.zeros((Dk, Dv)) if dht is None else dht[b_, hv].T.copy()
+                for ci in reversed(range(len(chunks))):
+                    s, e = chunks[ci]
+                    K = _pad(k[b_, s:e, hk], C)
+                    Q = _pad(q[b_, s:e, hk], C)
+                    V = _pad(v[b_, s:e, hv], C)
+                    gg = _pad(g[b_, s:e, hv], C)
+                    bb = _pad(beta[b_, s:e, hv], C)
+                    dO = _pad(do[b_, s:e, hv], C)
+                    rk, rq = _norm_factor(K, norm), _norm_factor(Q, norm)
+                    ops = chunk_ops(K, Q, V, gg, bb, scale, rk, rq)
+                    H0 = states[(b_, hv, ci)]
+                    dH1 = dH
+                    g_, Gam, bv, E, A, Tm, W, Ut, P = (ops[n] for n in ("gam", "Gam", "b", "E", "A", "T", "W", "Ut", "P"))
+                    Kh, Qh = rk[:, None] * K, rq[:, None] * Q
+                    U = Ut - W @ H0
+                    dU = P.T @ dO + (bv * rk)[:, None] * (K @ dH1)
+                    dP = np.tril(dO @ U.T)
+                    dgam = np.zeros(C)
+                    # O = scale diag(Gamma) Q^ H0 + P U
+                    X = dO @ H0.T
+                    dQ = scale * Gam[:, None] * X
+                    dgam += scale * Gam * np.sum(Qh * X, axis=1)
+                    dS = scale * E * dP
+                    dQ += dS @ Kh
+                    dK = dS.T @ Qh
+                    Z = dP * P
+                    dgam += Z.sum(1) - Z.sum(0)
+                    # H1 = Gamma_C H0 + K^^T diag(b) U
+                    Y = U @ dH1.T
+                    dK += bv[:, None] * Y
+                    db = np.sum(Kh * Y, axis=1)
+                    dgam -= bv * db
+                    dgam[-1] += np.sum(bv * db) + np.exp(g_[-1]) * np.sum(dH1 * H0)
+                    # U = U~ - W H0, U~ = T diag(beta) V, W = T diag(beta Gamma) K^
+                    dW = -dU @ H0.T
+                    dT = dU @ (bb[:, None] * V).T + dW @ ((bb * Gam)[:, None] * Kh).T
+                    TdU = Tm.T @ dU
+                    TdW = Tm.T @ dW
+                    dV = bb[:, None] * TdU
+                    dbt = np.sum(V * TdU, axis=1) + Gam * np.sum(Kh * TdW, axis=1)
+                    dK += (bb * Gam)[:, None] * TdW
+                    dgam += bb * Gam * np.sum(Kh * TdW, axis=1)
+                    # T = (I + A)^-1, A = strict_lower(beta_r E k^_r . k^_j)
+                    dA = np.tril(-Tm.T @ dT @ Tm.T, -1)
+                    M = dA * bb[:, None] * E
+                    dbt += np.sum(dA * E * (Kh @ Kh.T), axis=1)
+                    Z = dA * A
+                    dgam += Z.sum(1) - Z.sum(0)
+                    dK += M @ Kh + M.T @ Kh
+                    # gamma = cumsum(g) within the chunk
+                    dgg = np.cumsum(dgam[::-1])[::-1]
+                    n = e - s
+                    dv[b_, s:e, hv] = dV[:n]
+                    dbeta[b_, s:e, hv] = dbt[:n]
+                    dg[b_, s:e, hv] = dgg[:n]
+                    dQh[ci] += dQ
+                    dKh[ci] += dK
+                    dH = np.exp(g_[-1]) * dH1 + ops["Mneg"].T @ dH1 + ops["Qc"].T @ dO
+                dh0[b_, hv] = dH.T
+            for ci, (s, e) in enumerate(chunks):
+                n = e - s
+                for name, X, Dst, raw in (("q", dQh[ci], dq, q), ("k", dKh[ci], dk, k)):
+                    x = raw[b_, s:e, hk]
+                    r = _norm_factor(x, norm)
+                    xh = r[:, None] * x
+                    Xn = X[:n]
+                    if norm:
+                        Dst[b_, s:e, hk] = r[:, None] * (Xn - xh * np.sum(xh * Xn, axis=1, keepdims=True))
+                    else:
+                        Dst[b_, s:e, hk] = Xn
+    return dict(dq=dq, dk=dk, dv=dv, dg=dg, dbeta=dbeta, dh0=dh0)

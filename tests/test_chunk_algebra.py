@@ -1,0 +1,28 @@
+"""The chunk algebra the CUDA kernels implement (tests/chunk_algebra.py, numpy fp64)
+equals the sequential oracle to rounding, forward and backward, including ragged last
+chunks, GQA sharing, no-norm, zero initial state and several chunk lengths."""
+import numpy as np
+import pytest
+
+import oracle
+from tests import chunk_algebra as ca
+from tests.test_oracle_pins import rand_inputs
+
+
+@pytest.mark.parametrize("C,T,Hk,Hv,norm,h0", [(4, 11, 1, 2, True, True), (8, 16, 2, 4, True, False),
+                                              (64, 70, 1, 1, True, True), (5, 5, 1, 2, False, True),
+                                              (16, 3, 1, 1, True, True)])
+def test_chunk_forward_and_backward_equal_oracle(C, T, Hk, Hv, norm, h0):
+    q, k, v, g, beta, hh = rand_inputs(B=2, T=T, Hk=Hk, Hv=Hv, Dk=6, Dv=5, seed=C + T, h0=h0)
+    r = np.random.default_rng(7)
+    do = r.standard_normal(v.shape)
+    dht = r.standard_normal((2, Hv, 5, 6))
+    scale = 0.7
+    o, ht = oracle.forward(q, k, v, g, beta, hh, scale=scale, use_qk_l2norm=norm)
+    o2, ht2, _ = ca.forward(q, k, v, g, beta, hh, scale, norm, C)
+    assert np.max(np.abs(o - o2)) < 1e-11 and np.max(np.abs(ht - ht2)) < 1e-11
+    ref = oracle.backward(q, k, v, g, beta, hh, do, dht, scale=scale, use_qk_l2norm=norm)
+    got = ca.backward(q, k, v, g, beta, hh, do, dht, scale, norm, C)
+    for name in ("dq", "dk", "dv", "dg", "dbeta", "dh0"):
+        err = np.max(np.abs(ref[name] - got[name])) / max(1.0, np.max(np.abs(ref[name])))
+        assert err < 1e-10, (name, err)

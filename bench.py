@@ -46,6 +46,13 @@ KERNEL_MODEL = {
 STEP_FLOPS, STEP_BYTES = 655360 * UNITS, 2584 * UNITS
 
 
+def set_tokens(n):
+    global T, UNITS, STEP_FLOPS, STEP_BYTES
+    T = n
+    UNITS = B * T * HV
+    STEP_FLOPS, STEP_BYTES = 655360 * UNITS, 2584 * UNITS
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -161,7 +168,8 @@ def run_reference(args, rank, world):
 def workload_config():
     return {"workload": "long-context training step, chunked forward + VJP", "B": B, "T": T, "Hk": HK, "Hv": HV,
             "Dk": D, "Dv": D, "chunk": C, "qkv": "bf16", "gates_state": "fp32", "use_qk_l2norm": True,
-            "h0": "zero", "dht": "zero", "l2": "inputs larger than L2 (q,k 128 MiB, v,do 256 MiB); no flush"}
+            "h0": "zero", "dht": "zero",
+            "l2": f"inputs larger than L2 (q,k {T * HK * D * 2 >> 20} MiB, v,do {T * HV * D * 2 >> 20} MiB); no flush"}
 
 
 def main():
@@ -171,11 +179,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["mine", "reference"], default="mine")
     ap.add_argument("--ref-tokens", type=int, default=512)
+    ap.add_argument("--tokens", type=int, default=T, help="sequence length (smaller only for profiling runs)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    set_tokens(args.tokens)
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -198,7 +208,8 @@ def main():
     peaks = load_peaks()
 
     # ------------------------------------------------------------------ inputs (replica per rank)
-    x = make_inputs(LONG_TRAIN, dtype=torch.bfloat16, seed=1004 + rank, grads=True, h0_std=None, dht_std=None)
+    shape = LONG_TRAIN if T == LONG_TRAIN.T else LONG_TRAIN.__class__(B, T, HK, HV, D, D)
+    x = make_inputs(shape, dtype=torch.bfloat16, seed=1004 + rank, grads=True, h0_std=None, dht_std=None)
     d = {k: (v.to(dev) if v is not None else None) for k, v in x.items()}
     p = gdr.Problem(B, T, HK, HV, D, D, gdr.GDR_BF16, gdr.GDR_GATE_SCALAR, D ** -0.5, 1)
     f32 = dict(dtype=torch.float32, device=dev)

@@ -119,6 +119,27 @@ gdr_status gdr_decode_step(const gdr_problem* p, const void* q, const void* k, c
  * chunked kernels: GDR_OK, or GDR_ERR_TIMEOUT if a bounded wait expired. */
 gdr_status gdr_workspace_status(void* ws, size_t ws_bytes, gdr_stream_t stream);
 
+/* Bytes of the scratch array built into the library for gdr_fwd_chunked_noalloc. */
+#define GDR_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/* gdr_fwd_chunked without a workspace argument, for callers that cannot allocate device
+ * memory: for example a host application whose device memory is entirely owned by
+ * another allocator, or a deployment that forbids device allocation once it has started.
+ * (The pages on the gated delta rule have no counterpart to this call.) Instead of a
+ * caller workspace it uses a scratch array of GDR_NOALLOC_SCRATCH_BYTES (64 MiB) that the
+ * library keeps on every GPU where it is loaded, for the life of the process. It allocates
+ * nothing. Problems whose gdr_fwd_chunked_workspace() exceeds that size return
+ * GDR_ERR_WORKSPACE with nothing launched (about 740 chunk records: for example B=1, Hv=32,
+ * T <= 1472). Inputs, outputs and the support matrix are those of gdr_fwd_chunked.
+ * The first call on a device looks up the scratch address on that device (so make the
+ * first call on each device before any stream capture). All calls share the one array and
+ * it keeps the last call's contents (the call clears the status word it needs at zero):
+ * calls that can overlap on the GPU (different streams, or different host threads) race
+ * on it, so serialise them. */
+gdr_status gdr_fwd_chunked_noalloc(const gdr_problem* p, const void* q, const void* k, const void* v,
+                                   const float* g, const float* beta, const float* h0, void* o, float* ht,
+                                   gdr_stream_t stream);
+
 /* Launch tracing for profiling. While enabled, every kernel the library launches is
  * bracketed by two CUDA events recorded on its own stream (host-side events only; no
  * device memory). gdr_trace_collect() waits for the recorded events, writes up to `max`

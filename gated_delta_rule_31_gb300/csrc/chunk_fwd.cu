@@ -22,32 +22,37 @@
 namespace gdr {
 
 // ================================================================== prep kernel
-// Shared memory (offsets from a 1024-aligned base).
-constexpr uint32_t PS_KQV = 0;                    // k rows 0-63 / q rows 64-127 of a 128-row tile
-                                                  // (panels at 0, 16K); v panels at 32K, 48K
-constexpr uint32_t PS_REC = 65536;                // record staging, REC_* layout (88 KB)
-constexpr uint32_t PS_TT = PS_REC + REC_BYTES;    // [Tw; Tu] 128 x 64 bf16, one panel (16 KB)
-constexpr uint32_t PS_AT = PS_TT + 16384;         // A, T fp32 [64][65] each; later Wbar, W images
+// Shared memory (offsets from a 1024-aligned base), ~97 KB so two CTAs share an SM:
+// the record images go straight from registers to global memory, nothing is staged.
+constexpr uint32_t PS_KQ = 0;        // k rows 0-63 / q rows 64-127 of a 128-row tile (panels 16 KB)
+constexpr uint32_t PS_V = 32768;     // v [64 tok x 128] (panels 8 KB)
 constexpr int LDA = 65;
-constexpr uint32_t PS_SCR = PS_AT + 2 * 64 * LDA * 4;   // solve scratch [3][16][17] fp32
-constexpr uint32_t PS_SMALL = PS_SCR + 3 * 16 * 17 * 4;  // gamma[64], beta[64], rho[128]
-constexpr uint32_t PS_BYTES = PS_SMALL + 1024;
-constexpr uint32_t PS_WBAR = PS_AT;               // [64 tok x 128 d] images (alias A/T)
-constexpr uint32_t PS_W = PS_AT + 16384;
-constexpr uint32_t PS_TIMG = PS_KQV + 40960;     // T image [64 x 64] (rows 64-127 of v slot 0)
-static_assert(PS_KQV % 1024 == 0 && PS_REC % 1024 == 0 && PS_TT % 1024 == 0 && PS_AT % 1024 == 0, "align");
-static_assert(PS_BYTES + 1024 <= 232448, "prep smem");
+constexpr uint32_t PS_A = 49152;     // A fp32 [64][65]; then [Tw; Tu] 128 x 64 bf16; then Wbar image
+constexpr uint32_t PS_T = 66560;     // T fp32 [64][65]; then W image [64 x 128]
+constexpr uint32_t PS_P = 83968;     // P image [64 x 64]
+constexpr uint32_t PS_SCR = 92160;   // solve scratch [3][16][17] fp32
+constexpr uint32_t PS_SMALL = PS_SCR + 3 * 16 * 17 * 4;  // per-token factors (8 x 64 fp32)
+constexpr uint32_t PS_BYTES = PS_SMALL + 2048;
+constexpr uint32_t PS_TT = PS_A, PS_WBAR = PS_A, PS_W = PS_T;
+static_assert(PS_A % 1024 == 0 && PS_T % 1024 == 0 && PS_P % 1024 == 0, "align");
+static_assert(PS_A + 64 * LDA * 4 <= PS_T && PS_T + 64 * LDA * 4 <= PS_P, "fp32 tiles");
+static_assert(2 * (PS_BYTES + 1024) <= 228 * 1024, "two prep CTAs per SM");
 
 __device__ __forceinline__ void unpack8(const uint4& u, float* x) {
     x[0] = bf16lo(u.x); x[1] = bf16hi(u.x); x[2] = bf16lo(u.y); x[3] = bf16hi(u.y);
     x[4] = bf16lo(u.z); x[5] = bf16hi(u.z); x[6] = bf16lo(u.w); x[7] = bf16hi(u.w);
 }
-__device__ __forceinline__ void st_chunk(uint32_t addr, const float* x, float s) {
-    st_shared_v4(addr, pack_bf16(s * x[0], s * x[1]), pack_bf16(s * x[2], s * x[3]), pack_bf16(s * x[4], s * x[5]),
-                 pack_bf16(s * x[6], s * x[7]));
+__device__ __forceinline__ uint4 pack8(const float* x, float s) {
+    return make_uint4(pack_bf16(s * x[0], s * x[1]), pack_bf16(s * x[2], s * x[3]), pack_bf16(s * x[4], s * x[5]),
+                      pack_bf16(s * x[6], s * x[7]));
 }
+__device__ __forceinline__ void st_chunk(uint32_t addr, const float* x, float s) {
+    const uint4 u = pack8(x, s);
+    st_shared_v4(addr, u.x, u.y, u.z, u.w);
+}
+__device__ __forceinline__ void st_global16(uint8_t* p, const uint4& u) { *reinterpret_cast<uint4*>(p) = u; }
 
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(256, 2)
     prep_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                 const __grid_constant__ CUtensorMap mv, PrepArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -61,11 +66,17 @@ __global__ void __launch_bounds__(256, 1)
     const ChunkProblem& P = a.p;
     const int hk = hv / (P.Hv / P.Hk);
     const int t0 = c * kChunk;
+    const size_t bh = (size_t)b * P.Hv + hv;
+    uint8_t* rec = a.rec + (bh * P.NC + c) * REC_BYTES;
+    uint8_t* rec2 = a.rec2 ? a.rec2 + (bh * P.NC + c) * REC2_BYTES : nullptr;
     float* gam = reinterpret_cast<float*>(sm + PS_SMALL);  // in-chunk cumulative log-decay
     float* bet = gam + 64;
-    float* rho = bet + 64;  // rows 0-63: k norm factors, 64-127: q norm factors
-    float* Am = reinterpret_cast<float*>(sm + PS_AT);
-    float* Tm = Am + 64 * LDA;
+    float* rho = bet + 64;   // [128] rows 0-63: k norm factors, 64-127: q norm factors
+    float* fw = rho + 128;   // beta Gamma rho_k     (columns of Tw)
+    float* fb = fw + 64;     // exp(gamma_C - gamma) rho_k   (rows of Kbar, Wbar)
+    float* fq = fb + 64;     // scale Gamma rho_q     (rows of Qc)
+    float* Am = reinterpret_cast<float*>(sm + PS_A);
+    float* Tm = reinterpret_cast<float*>(sm + PS_T);
     float* Xs = reinterpret_cast<float*>(sm + PS_SCR);
 
     if (tid == 0) {
@@ -84,12 +95,12 @@ __global__ void __launch_bounds__(256, 1)
     const uint32_t tm = tmem_sh;
     if (tid == 0) {
         mbar_expect_tx(&bar_tma, 6 * 8192);
-        tma_load_4d(sm + PS_KQV + 0, &mk, 0, hk, t0, b, &bar_tma);
-        tma_load_4d(sm + PS_KQV + 16384, &mk, 64, hk, t0, b, &bar_tma);
-        tma_load_4d(sm + PS_KQV + 8192, &mq, 0, hk, t0, b, &bar_tma);
-        tma_load_4d(sm + PS_KQV + 24576, &mq, 64, hk, t0, b, &bar_tma);
-        tma_load_4d(sm + PS_KQV + 32768, &mv, 0, hv, t0, b, &bar_tma);
-        tma_load_4d(sm + PS_KQV + 49152, &mv, 64, hv, t0, b, &bar_tma);
+        tma_load_4d(sm + PS_KQ + 0, &mk, 0, hk, t0, b, &bar_tma);
+        tma_load_4d(sm + PS_KQ + 16384, &mk, 64, hk, t0, b, &bar_tma);
+        tma_load_4d(sm + PS_KQ + 8192, &mq, 0, hk, t0, b, &bar_tma);
+        tma_load_4d(sm + PS_KQ + 24576, &mq, 64, hk, t0, b, &bar_tma);
+        tma_load_4d(sm + PS_V + 0, &mv, 0, hv, t0, b, &bar_tma);
+        tma_load_4d(sm + PS_V + 8192, &mv, 64, hv, t0, b, &bar_tma);
     }
     // gates of the chunk; tokens past T act as g = 0, beta = 0 (state passes unchanged)
     if (tid < 64) {
@@ -115,7 +126,7 @@ __global__ void __launch_bounds__(256, 1)
 
     {  // L2 norm factors of the 64 keys (rows 0-63) and 64 queries (rows 64-127)
         const int row = tid >> 1, half = tid & 1;
-        const uint32_t base = sb + PS_KQV + half * 16384 + row * 128;
+        const uint32_t base = sb + PS_KQ + half * 16384 + row * 128;
         float ss = 0.f;
 #pragma unroll
         for (int ch = 0; ch < 8; ch++) {
@@ -128,14 +139,19 @@ __global__ void __launch_bounds__(256, 1)
         if (half == 0) rho[row] = P.use_norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
     }
     __syncthreads();
+    if (tid < 64) {
+        const float G = expf(gam[tid]);
+        fw[tid] = bet[tid] * G * rho[tid];
+        fb[tid] = expf(gam[63] - gam[tid]) * rho[tid];
+        fq[tid] = P.scale * G * rho[64 + tid];
+    }
 
     // G = K K^T (rows 0-63) and Q K^T (rows 64-127) in one M=128 product, raw bf16 operands
     if (tid == 0) {
         tc_fence_after();
         const uint32_t id = idesc_bf16(128, 64, 0, 0);
         for (int k0 = 0; k0 < kD; k0 += 16)
-            mma_bf16(tm, desc_kmajor(sb + PS_KQV, 128, 0, k0), desc_kmajor(sb + PS_KQV, 128, 0, k0), id,
-                     k0 > 0);
+            mma_bf16(tm, desc_kmajor(sb + PS_KQ, 128, 0, k0), desc_kmajor(sb + PS_KQ, 128, 0, k0), id, k0 > 0);
         mma_commit(&bar_mma);
     }
     ok = mbar_wait(&bar_mma, 0, &abort_sh, a.status, 11);
@@ -153,7 +169,7 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
             for (int jj = 0; jj < 32; jj++) {
                 const int j = 32 * h + jj;
-                Am[i * LDA + j] = (j < i) ? ci * rho[j] * expf(gi - gam[j]) * v[jj] : 0.f;
+                Am[i * LDA + j] = (j < i) ? ci * rho[j] * __expf(gi - gam[j]) * v[jj] : 0.f;
             }
         } else {
             const int i = r - 64;
@@ -164,9 +180,12 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
                 for (int e = 0; e < 8; e++) {
                     const int j = 32 * h + 8 * q + e;
-                    x[e] = (j <= i) ? ci * rho[j] * expf(gi - gam[j]) * v[8 * q + e] : 0.f;
+                    x[e] = (j <= i) ? ci * rho[j] * __expf(gi - gam[j]) * v[8 * q + e] : 0.f;
                 }
-                st_chunk(sb + PS_REC + REC_P + sw128_chunk(i, 4 * h + q, 64), x, 1.f);
+                const uint4 u = pack8(x, 1.f);
+                const uint32_t off = sw128_chunk(i, 4 * h + q, 64);
+                st_shared_v4(sb + PS_P + off, u.x, u.y, u.z, u.w);
+                st_global16(rec + REC_P + off, u);
             }
         }
     }
@@ -220,25 +239,22 @@ __global__ void __launch_bounds__(256, 1)
         }
         __syncthreads();
     }
-    {  // [Tw; Tu] with Tw = T diag(beta Gamma rho_k), Tu = T diag(beta): K-major A operand
+    {  // [Tw; Tu] with Tw = T diag(beta Gamma rho_k), Tu = T diag(beta): K-major A operand (over A)
         const int row = tid >> 1, half = tid & 1;
         const int i = row & 63;
         const bool isw = row < 64;
-        if (isw && a.rec2) {  // T itself for the backward, in the free half of a v slot
-#pragma unroll
-            for (int q = 0; q < 4; q++)
-                st_chunk(sb + PS_TIMG + sw128_chunk(i, 4 * half + q, 64), Tm + i * LDA + 32 * half + 8 * q, 1.f);
-        }
+        const float* trow = Tm + i * LDA + 32 * half;
 #pragma unroll
         for (int q = 0; q < 4; q++) {
             float x[8];
 #pragma unroll
             for (int e = 0; e < 8; e++) {
                 const int j = 32 * half + 8 * q + e;
-                const float sj = isw ? bet[j] * expf(gam[j]) * rho[j] : bet[j];
-                x[e] = Tm[i * LDA + j] * sj;
+                x[e] = trow[8 * q + e] * (isw ? fw[j] : bet[j]);
             }
             st_chunk(sb + PS_TT + sw128_chunk(row, 4 * half + q, 128), x, 1.f);
+            if (isw && rec2)  // T itself for the backward
+                st_global16(rec2 + REC2_T + sw128_chunk(i, 4 * half + q, 64), pack8(trow + 8 * q, 1.f));
         }
     }
     fence_proxy_async_smem();
@@ -249,10 +265,9 @@ __global__ void __launch_bounds__(256, 1)
         tc_fence_after();
         const uint32_t id = idesc_bf16(64, 128, 0, 1);
         for (int k0 = 0; k0 < kChunk; k0 += 16) {
-            mma_bf16(tm + 128, desc_kmajor(sb + PS_TT, 128, 0, k0), desc_mnmajor(sb + PS_KQV, 128, 0, k0), id,
+            mma_bf16(tm + 128, desc_kmajor(sb + PS_TT, 128, 0, k0), desc_mnmajor(sb + PS_KQ, 128, 0, k0), id,
                      k0 > 0);
-            mma_bf16(tm + 0, desc_kmajor(sb + PS_TT, 128, 64, k0),
-                     desc_mnmajor(sb + PS_KQV + 32768, 128, 0, k0), id, k0 > 0);
+            mma_bf16(tm + 0, desc_kmajor(sb + PS_TT, 128, 64, k0), desc_mnmajor(sb + PS_V, 64, 0, k0), id, k0 > 0);
         }
         mma_commit(&bar_mma);
     }
@@ -260,38 +275,44 @@ __global__ void __launch_bounds__(256, 1)
     if (__syncthreads_or(!ok)) goto teardown;
     tc_fence_after();
     {
-        const float gC = gam[63];
         const int lg = warp & 3, h = warp >> 2;
         const int i = 16 * lg + (lane & 15);  // M=64 accumulator rows: 16 per TMEM sub-partition
-        float w[64];
-        tmem_ld32(tmem_at(tm, 32 * lg, 128 + 64 * h), w);
-        tmem_ld32(tmem_at(tm, 32 * lg, 128 + 64 * h + 32), w + 32);
-        tmem_wait_ld();
-        if (lane < 16) {
-            const float sbar = expf(gC - gam[i]) * rho[i];
+        {
+            float w[64];
+            tmem_ld32(tmem_at(tm, 32 * lg, 128 + 64 * h), w);
+            tmem_ld32(tmem_at(tm, 32 * lg, 128 + 64 * h + 32), w + 32);
+            tmem_wait_ld();
+            if (lane < 16) {
+                const float sbar = fb[i];
 #pragma unroll
-            for (int q = 0; q < 8; q++) {
-                st_chunk(sb + PS_W + sw128_chunk(i, 8 * h + q, 64), w + 8 * q, 1.f);
-                st_chunk(sb + PS_WBAR + sw128_chunk(i, 8 * h + q, 64), w + 8 * q, sbar);
+                for (int q = 0; q < 8; q++) {
+                    const uint4 u = pack8(w + 8 * q, 1.f);
+                    const uint32_t off = sw128_chunk(i, 8 * h + q, 64);
+                    st_shared_v4(sb + PS_W + off, u.x, u.y, u.z, u.w);
+                    if (rec2) st_global16(rec2 + REC2_W + off, u);
+                    st_chunk(sb + PS_WBAR + off, w + 8 * q, sbar);
+                }
             }
         }
-        float u[64];
-        tmem_ld32(tmem_at(tm, 32 * lg, 64 * h), u);
-        tmem_ld32(tmem_at(tm, 32 * lg, 64 * h + 32), u + 32);
-        tmem_wait_ld();
-        if (lane < 16) {
+        {
+            float u[64];
+            tmem_ld32(tmem_at(tm, 32 * lg, 64 * h), u);
+            tmem_ld32(tmem_at(tm, 32 * lg, 64 * h + 32), u + 32);
+            tmem_wait_ld();
+            if (lane < 16) {
 #pragma unroll
-            for (int q = 0; q < 8; q++) {
-                const int col = 64 * h + 8 * q;
-                st_chunk(sb + PS_REC + REC_U + (col >> 5) * 4096 + sw64_chunk(i, q & 3), u + 8 * q, 1.f);
+                for (int q = 0; q < 8; q++) {
+                    const int col = 64 * h + 8 * q;
+                    st_global16(rec + REC_U + (col >> 5) * 4096 + sw64_chunk(i, q & 3), pack8(u + 8 * q, 1.f));
+                }
             }
         }
-        // Kbar = diag(exp(gamma_C - gamma) rho_k) K
+        // Kbar = diag(exp(gamma_C - gamma) rho_k) K, straight to the record
         for (int idx = tid; idx < 64 * 16; idx += 256) {
             const int r = idx >> 4, j = idx & 15;
             float x[8];
-            unpack8(ld_shared_v4(sb + PS_KQV + sw128_chunk(r, j, 128)), x);
-            st_chunk(sb + PS_REC + REC_K + sw128_chunk(r, j, 64), x, expf(gC - gam[r]) * rho[r]);
+            unpack8(ld_shared_v4(sb + PS_KQ + sw128_chunk(r, j, 128)), x);
+            st_global16(rec + REC_K + sw128_chunk(r, j, 64), pack8(x, fb[r]));
         }
     }
     fence_proxy_async_smem();
@@ -303,12 +324,11 @@ __global__ void __launch_bounds__(256, 1)
         tc_fence_after();
         const uint32_t idm = idesc_bf16(128, 128, 1, 1);
         for (int k0 = 0; k0 < kChunk; k0 += 16)
-            mma_bf16(tm + 0, desc_mnmajor(sb + PS_KQV, 128, 0, k0), desc_mnmajor(sb + PS_WBAR, 64, 0, k0), idm,
+            mma_bf16(tm + 0, desc_mnmajor(sb + PS_KQ, 128, 0, k0), desc_mnmajor(sb + PS_WBAR, 64, 0, k0), idm,
                      k0 > 0);
         const uint32_t idp = idesc_bf16(64, 128, 0, 1);
         for (int k0 = 0; k0 < kChunk; k0 += 16)
-            mma_bf16(tm + 128, desc_kmajor(sb + PS_REC + REC_P, 64, 0, k0), desc_mnmajor(sb + PS_W, 64, 0, k0),
-                     idp, k0 > 0);
+            mma_bf16(tm + 128, desc_kmajor(sb + PS_P, 64, 0, k0), desc_mnmajor(sb + PS_W, 64, 0, k0), idp, k0 > 0);
         mma_commit(&bar_mma);
     }
     ok = mbar_wait(&bar_mma, 0, &abort_sh, a.status, 13);
@@ -323,7 +343,7 @@ __global__ void __launch_bounds__(256, 1)
             tmem_ld32(tmem_at(tm, 32 * lg, 64 * h + 32), m + 32);
             tmem_wait_ld();
 #pragma unroll
-            for (int q = 0; q < 8; q++) st_chunk(sb + PS_REC + REC_M + sw128_chunk(d, 8 * h + q, 128), m + 8 * q, -1.f);
+            for (int q = 0; q < 8; q++) st_global16(rec + REC_M + sw128_chunk(d, 8 * h + q, 128), pack8(m + 8 * q, -1.f));
         }
         {  // Qc = scale diag(Gamma rho_q) Q - P W, rows i = 16 lg + lane
             const int i = 16 * lg + (lane & 15);
@@ -332,34 +352,19 @@ __global__ void __launch_bounds__(256, 1)
             tmem_ld32(tmem_at(tm, 32 * lg, 128 + 64 * h + 32), pw + 32);
             tmem_wait_ld();
             if (lane < 16) {
-                const float f = P.scale * expf(gam[i]) * rho[64 + i];
+                const float f = fq[i];
 #pragma unroll
                 for (int q = 0; q < 8; q++) {
                     float x[8];
-                    unpack8(ld_shared_v4(sb + PS_KQV + sw128_chunk(64 + i, 8 * h + q, 128)), x);
+                    unpack8(ld_shared_v4(sb + PS_KQ + sw128_chunk(64 + i, 8 * h + q, 128)), x);
 #pragma unroll
                     for (int e = 0; e < 8; e++) x[e] = f * x[e] - pw[8 * q + e];
-                    st_chunk(sb + PS_REC + REC_Q + sw128_chunk(i, 8 * h + q, 64), x, 1.f);
+                    st_global16(rec + REC_Q + sw128_chunk(i, 8 * h + q, 64), pack8(x, 1.f));
                 }
             }
         }
     }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-        const size_t bh = (size_t)b * P.Hv + hv;
-        bulk_store(a.rec + (bh * P.NC + c) * REC_BYTES, sm + PS_REC, REC_BYTES);
-        bulk_commit();
-        if (a.rec2) {
-            uint8_t* r2 = a.rec2 + (bh * P.NC + c) * REC2_BYTES;
-            bulk_store(r2 + REC2_T, sm + PS_TIMG, 8192);
-            bulk_store(r2 + REC2_W, sm + PS_W, 16384);
-            bulk_commit();
-        }
-        a.gam[bh * a.ncpad + c] = expf(gam[63]);
-        bulk_wait_all();
-    }
+    if (tid == 0) a.gam[bh * a.ncpad + c] = expf(gam[63]);
 teardown:
     tc_fence_before();
     __syncthreads();

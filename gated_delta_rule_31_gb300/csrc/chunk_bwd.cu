@@ -42,7 +42,9 @@ constexpr uint32_t G_KB = 163840;   // Kbar image [64 x 128]; later dU image
 constexpr uint32_t G_GF = 180224;   // G = K K^T fp32 [64][64]                            [whole CTA]
 constexpr uint32_t G_ZS = 196608;   // fp32 [64][64] scratch (column sums)
 constexpr uint32_t G_SM = 212992;   // small arrays
-constexpr uint32_t G_BYTES = G_SM + 4096;
+constexpr uint32_t G_SM_FLOATS = 64 * 4 + 256 * 4 + 64 + 16 + 4;  // see the carve-up in grad_kernel
+constexpr uint32_t G_BYTES = G_SM + 6144;
+static_assert(G_SM_FLOATS * 4 <= 6144, "small arrays");
 static_assert(G_BYTES + 1024 <= 232448, "grad smem");
 
 // TMEM columns: dQ^ accumulator, dK^ accumulator (both M=64 x 128), two temporaries.
@@ -71,7 +73,11 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
     tmem_ld32(taddr + 32, v + 32);
 }
 
-__global__ void __launch_bounds__(256, 1)
+// 16 warps: warp w reads TMEM lane group (w & 3) (M=64 accumulator rows 16*(w&3) .. +15 in
+// lanes 0-15) and column quarter (w >> 2) of every product.
+constexpr int GRAD_THREADS = 512;
+
+__global__ void __launch_bounds__(GRAD_THREADS, 1)
     grad_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                 const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo, GradArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -85,11 +91,11 @@ __global__ void __launch_bounds__(256, 1)
     const ChunkProblem& P = a.p;
     const int G = P.Hv / P.Hk;
     const int t0 = c * kChunk;
-    // M=64 accumulator mapping: row r in lanes 0-15 of sub-partition lg; h = column half
-    const int lg = warp & 3, h = warp >> 2;
+    const int lg = warp & 3, qt = warp >> 2;
     const int r = 16 * lg + (lane & 15);
     const bool act = lane < 16;
     const bool rowvalid = act && (t0 + r < P.T);
+    const int c32 = 32 * qt, c16 = 16 * qt;  // this thread's columns of N=128 / N=64 products
 
     float* GF = reinterpret_cast<float*>(sm + G_GF);
     float* ZS = reinterpret_cast<float*>(sm + G_ZS);
@@ -98,13 +104,13 @@ __global__ void __launch_bounds__(256, 1)
     float* rq = rk + 64;                                // [64]
     float* gam = rq + 64;                               // [64]
     float* bet = gam + 64;                              // [64]
-    float* dgp = bet + 64;                              // [2][64] dgamma partials by column half
-    float* dbp = dgp + 128;                             // [2][64] dbeta partials
-    float* sb3 = dbp + 128;                             // [2][64] b_r db_r partials
-    float* dgc = sb3 + 128;                             // [64] column-sum terms of dgamma
-    float* part = dgc + 64;                             // [2][64] norm-backward partial dots
-    float* red = part + 128;                            // [8] block reduction
-    float* hdh = red + 8;                               // <dH1, H0>
+    float* dgp = bet + 64;                              // [4][64] dgamma partials by column quarter
+    float* dbp = dgp + 256;                             // [4][64] dbeta partials
+    float* sb3 = dbp + 256;                             // [4][64] b_r db_r partials
+    float* part = sb3 + 256;                            // [4][64] norm-backward partial dots
+    float* dgc = part + 256;                            // [64] column-sum terms of dgamma
+    float* red = dgc + 64;                              // [16] block reduction
+    float* hdh = red + 16;                              // <dH1, H0>
 
     uint32_t ld_phase = 0, mma_phase = 0;
     if (tid == 0) {
@@ -121,6 +127,7 @@ __global__ void __launch_bounds__(256, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tm = tmem_sh;
+    const uint32_t tl = tmem_at(tm, 32 * lg, 0);  // this warp's TMEM lane base
 
     auto wait_ld = [&](int site) -> bool {
         bool ok = mbar_wait(&bar_ld, ld_phase, &abort_sh, a.status, site);
@@ -142,6 +149,10 @@ __global__ void __launch_bounds__(256, 1)
     auto mma = [&](uint32_t col, uint64_t ad, uint64_t bd, uint32_t id, bool acc) {
         mma_bf16(tm + col, ad, bd, id, acc ? 1u : 0u);
     };
+    // 8 bf16 of row `row` of a panelised tile, logical chunk j
+    auto ldrow8 = [&](uint32_t tile, int row, int j, int R, float* x) {
+        unpack8b(ld_shared_v4(sb + tile + sw128_chunk(row, j, R)), x);
+    };
     const uint32_t id64x128_kk = idesc_bf16(64, 128, 0, 0), id64x128_km = idesc_bf16(64, 128, 0, 1),
                    id64x128_mm = idesc_bf16(64, 128, 1, 1), id64x64_kk = idesc_bf16(64, 64, 0, 0),
                    id64x64_mm = idesc_bf16(64, 64, 1, 1);
@@ -155,19 +166,19 @@ __global__ void __launch_bounds__(256, 1)
         tma_load_4d(sm + G_KQ + 24576, &mq, 64, hk, t0, b, &bar_ld);
     }
     if (!wait_ld(40)) goto teardown;
-    {
-        const int row = tid >> 1, half = tid & 1;
-        const uint32_t base = sb + G_KQ + half * 16384 + row * 128;
+    {  // norm factors: 4 threads per row, 32 elements each
+        const int row = tid >> 2, pp = tid & 3;
         float ss = 0.f;
 #pragma unroll
-        for (int ch = 0; ch < 8; ch++) {
+        for (int q = 0; q < 4; q++) {
             float x[8];
-            unpack8b(ld_shared_v4(base + ch * 16), x);
+            ldrow8(G_KQ, row, 4 * pp + q, 128, x);
 #pragma unroll
             for (int e = 0; e < 8; e++) ss += x[e] * x[e];
         }
         ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-        if (half == 0) {
+        ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+        if (pp == 0) {
             const float f = P.use_norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
             if (row < 64) rk[row] = f; else rq[row - 64] = f;
         }
@@ -181,19 +192,18 @@ __global__ void __launch_bounds__(256, 1)
     }
     if (!wait_mma(41)) goto teardown;
     {
-        float v[32];
-        tmem_ld32(tmem_at(tm, 32 * lg, TM_T1 + 32 * h), v);
+        float v[16];
+        tmem_ld16(tl + TM_T1 + c16, v);
         tmem_wait_ld();
         if (act) {
 #pragma unroll
-            for (int e = 0; e < 32; e++) GF[r * 64 + 32 * h + e] = v[e];
+            for (int e = 0; e < 16; e++) GF[r * 64 + c16 + e] = v[e];
         }
-        // zero the dQ^ / dK^ accumulators: warp covers its 32 lanes x 128 columns
         float z[32];
 #pragma unroll
         for (int e = 0; e < 32; e++) z[e] = 0.f;
-#pragma unroll
-        for (int q = 0; q < 4; q++) tmem_st32(tmem_at(tm, 32 * lg, 128 * h + 32 * q), z);
+        tmem_st32(tl + 64 * qt, z);  // zero dQ^ / dK^: 16 warps x 32 lanes x 64 columns
+        tmem_st32(tl + 64 * qt + 32, z);
         tmem_wait_st();
     }
     sync_for_mma();
@@ -233,7 +243,7 @@ __global__ void __launch_bounds__(256, 1)
             bet[tid] = bv;
             dgc[tid] = 0.f;
         }
-        if (tid < 128) {
+        if (tid < 256) {
             dgp[tid] = 0.f;
             dbp[tid] = 0.f;
             sb3[tid] = 0.f;
@@ -259,7 +269,8 @@ __global__ void __launch_bounds__(256, 1)
         }
         {  // <dH1, H0> over the two bf16 images (same layout, so elementwise)
             float s = 0.f;
-            for (int i = tid; i < 2048; i += 256) {
+#pragma unroll
+            for (int i = tid; i < 2048; i += GRAD_THREADS) {
                 float x[8], y[8];
                 unpack8b(ld_shared_v4(sb + G_H0 + i * 16), x);
                 unpack8b(ld_shared_v4(sb + G_DH + i * 16), y);
@@ -272,31 +283,28 @@ __global__ void __launch_bounds__(256, 1)
         if (!wait_mma(43)) goto teardown;
         if (tid == 0) {
             float s = 0.f;
-            for (int w = 0; w < 8; w++) s += red[w];
+            for (int w = 0; w < 16; w++) s += red[w];
             *hdh = s;
         }
         {  // U = U~ - W H0 -> U image (G_W);  dU -> dU image (G_KB)
-            float x[64];
-            tmem_ld64(tmem_at(tm, 32 * lg, TM_T1 + 64 * h), x);
+            float x[32];
+            tmem_ld32(tl + TM_T1 + c32, x);
             tmem_wait_ld();
             if (act) {
 #pragma unroll
-                for (int q = 0; q < 8; q++) {
-                    const int col = 64 * h + 8 * q;
-                    const uint4 u = *reinterpret_cast<const uint4*>(rec + REC_U + (col >> 5) * 4096 +
-                                                                    sw64_chunk(r, q & 3));
+                for (int q = 0; q < 4; q++) {  // columns c32.. are exactly U~ slice qt
                     float ut[8];
-                    unpack8b(u, ut);
+                    unpack8b(*reinterpret_cast<const uint4*>(rec + REC_U + qt * 4096 + sw64_chunk(r, q)), ut);
 #pragma unroll
                     for (int e = 0; e < 8; e++) ut[e] -= x[8 * q + e];
-                    st_chunk8(sb + G_W + sw128_chunk(r, 8 * h + q, 64), ut, 1.f);
+                    st_chunk8(sb + G_W + sw128_chunk(r, 4 * qt + q, 64), ut, 1.f);
                 }
             }
-            tmem_ld64(tmem_at(tm, 32 * lg, TM_T2 + 64 * h), x);
+            tmem_ld32(tl + TM_T2 + c32, x);
             tmem_wait_ld();
             if (act) {
 #pragma unroll
-                for (int q = 0; q < 8; q++) st_chunk8(sb + G_KB + sw128_chunk(r, 8 * h + q, 64), x + 8 * q, 1.f);
+                for (int q = 0; q < 4; q++) st_chunk8(sb + G_KB + sw128_chunk(r, 4 * qt + q, 64), x + 8 * q, 1.f);
             }
         }
         sync_for_mma();
@@ -315,51 +323,50 @@ __global__ void __launch_bounds__(256, 1)
         {
             const float gr = gam[r], Gr = expf(gr);
             {  // X: dgamma_r += scale Gamma_r rq_r sum_d Q_rd X_rd; dQ^ += scale Gamma_r X_r
-                float x[64], dq[64];
-                tmem_ld64(tmem_at(tm, 32 * lg, TM_T1 + 64 * h), x);
-                tmem_ld64(tmem_at(tm, 32 * lg, TM_DQ + 64 * h), dq);
+                float x[32], dq[32];
+                tmem_ld32(tl + TM_T1 + c32, x);
+                tmem_ld32(tl + TM_DQ + c32, dq);
                 tmem_wait_ld();
                 const float f = P.scale * Gr;
                 float dot = 0.f;
 #pragma unroll
-                for (int q = 0; q < 8; q++) {
+                for (int q = 0; q < 4; q++) {
                     float qq[8];
-                    unpack8b(ld_shared_v4(sb + G_KQ + sw128_chunk(64 + r, 8 * h + q, 128)), qq);
+                    ldrow8(G_KQ, 64 + r, 4 * qt + q, 128, qq);
 #pragma unroll
                     for (int e = 0; e < 8; e++) {
                         dot += qq[e] * x[8 * q + e];
                         dq[8 * q + e] += f * x[8 * q + e];
                     }
                 }
-                tmem_st32(tmem_at(tm, 32 * lg, TM_DQ + 64 * h), dq);
-                tmem_st32(tmem_at(tm, 32 * lg, TM_DQ + 64 * h + 32), dq + 32);
-                if (act) dgp[h * 64 + r] += f * rq[r] * dot;
+                tmem_st32(tl + TM_DQ + c32, dq);
+                if (act) dgp[qt * 64 + r] += f * rq[r] * dot;
             }
             {  // dP: Z = dP .* P, dS = scale E .* dP; dSk = dS diag(rk) (G_P), dSq = diag(rq) dS (G_DO)
-                float v[32];
-                tmem_ld32(tmem_at(tm, 32 * lg, TM_T2 + 32 * h), v);
+                float v[16];
+                tmem_ld16(tl + TM_T2 + c16, v);
                 tmem_wait_ld();
                 if (act) {
-                    float pr[32];
+                    float pr[16];
 #pragma unroll
-                    for (int q = 0; q < 4; q++) unpack8b(ld_shared_v4(sb + G_P + sw128_chunk(r, 4 * h + q, 64)), pr + 8 * q);
+                    for (int q = 0; q < 2; q++) ldrow8(G_P, r, 2 * qt + q, 64, pr + 8 * q);
                     float zs = 0.f;
-                    float sk[32], sq[32];
+                    float sk[16], sq[16];
 #pragma unroll
-                    for (int e = 0; e < 32; e++) {
-                        const int j = 32 * h + e;
+                    for (int e = 0; e < 16; e++) {
+                        const int j = c16 + e;
                         const float z = v[e] * pr[e];
                         zs += z;
                         ZS[r * 64 + j] = z;
-                        const float ds = (j <= r) ? P.scale * expf(gr - gam[j]) * v[e] : 0.f;
+                        const float ds = (j <= r) ? P.scale * __expf(gr - gam[j]) * v[e] : 0.f;
                         sk[e] = ds * rk[j];
                         sq[e] = ds * rq[r];
                     }
-                    dgp[h * 64 + r] += zs;
+                    dgp[qt * 64 + r] += zs;
 #pragma unroll
-                    for (int q = 0; q < 4; q++) {
-                        st_chunk8(sb + G_P + sw128_chunk(r, 4 * h + q, 64), sk + 8 * q, 1.f);
-                        st_chunk8(sb + G_DO + sw128_chunk(r, 4 * h + q, 64), sq + 8 * q, 1.f);
+                    for (int q = 0; q < 2; q++) {
+                        st_chunk8(sb + G_P + sw128_chunk(r, 2 * qt + q, 64), sk + 8 * q, 1.f);
+                        st_chunk8(sb + G_DO + sw128_chunk(r, 2 * qt + q, 64), sq + 8 * q, 1.f);
                     }
                 }
             }
@@ -391,34 +398,33 @@ __global__ void __launch_bounds__(256, 1)
         }
         if (!wait_mma(45)) goto teardown;
         {
-            const float br = expf(gC - gam[r]);
+            const float br = __expf(gC - gam[r]);
             {  // Y: db_r = rk_r sum_d K_rd Y_rd; dK^ += b_r Y_r
-                float y[64], dk[64];
-                tmem_ld64(tmem_at(tm, 32 * lg, TM_T1 + 64 * h), y);
-                tmem_ld64(tmem_at(tm, 32 * lg, TM_DK + 64 * h), dk);
+                float y[32], dk[32];
+                tmem_ld32(tl + TM_T1 + c32, y);
+                tmem_ld32(tl + TM_DK + c32, dk);
                 tmem_wait_ld();
                 float dot = 0.f;
 #pragma unroll
-                for (int q = 0; q < 8; q++) {
+                for (int q = 0; q < 4; q++) {
                     float kk[8];
-                    unpack8b(ld_shared_v4(sb + G_KQ + sw128_chunk(r, 8 * h + q, 128)), kk);
+                    ldrow8(G_KQ, r, 4 * qt + q, 128, kk);
 #pragma unroll
                     for (int e = 0; e < 8; e++) {
                         dot += kk[e] * y[8 * q + e];
                         dk[8 * q + e] += br * y[8 * q + e];
                     }
                 }
-                tmem_st32(tmem_at(tm, 32 * lg, TM_DK + 64 * h), dk);
-                tmem_st32(tmem_at(tm, 32 * lg, TM_DK + 64 * h + 32), dk + 32);
-                if (act) sb3[h * 64 + r] = br * rk[r] * dot;
+                tmem_st32(tl + TM_DK + c32, dk);
+                if (act) sb3[qt * 64 + r] = br * rk[r] * dot;
             }
             {  // dW = -dWn -> dW image (G_H0)
-                float x[64];
-                tmem_ld64(tmem_at(tm, 32 * lg, TM_T2 + 64 * h), x);
+                float x[32];
+                tmem_ld32(tl + TM_T2 + c32, x);
                 tmem_wait_ld();
                 if (act) {
 #pragma unroll
-                    for (int q = 0; q < 8; q++) st_chunk8(sb + G_H0 + sw128_chunk(r, 8 * h + q, 64), x + 8 * q, -1.f);
+                    for (int q = 0; q < 4; q++) st_chunk8(sb + G_H0 + sw128_chunk(r, 4 * qt + q, 64), x + 8 * q, -1.f);
                 }
             }
             tmem_wait_st();
@@ -440,41 +446,41 @@ __global__ void __launch_bounds__(256, 1)
         if (!wait_mma(46)) goto teardown;
         {
             {  // dT_rj = beta_j (dU V^T + Gamma_j rk_j dW K^T)_rj -> dT image (G_DH)
-                float d1[32], d2[32];
-                tmem_ld32(tmem_at(tm, 32 * lg, TM_T1 + 32 * h), d1);
-                tmem_ld32(tmem_at(tm, 32 * lg, TM_T1 + 64 + 32 * h), d2);
+                float d1[16], d2[16];
+                tmem_ld16(tl + TM_T1 + c16, d1);
+                tmem_ld16(tl + TM_T1 + 64 + c16, d2);
                 tmem_wait_ld();
                 if (act) {
 #pragma unroll
-                    for (int e = 0; e < 32; e++) {
-                        const int j = 32 * h + e;
-                        d1[e] = bet[j] * (d1[e] + expf(gam[j]) * rk[j] * d2[e]);
+                    for (int e = 0; e < 16; e++) {
+                        const int j = c16 + e;
+                        d1[e] = bet[j] * (d1[e] + __expf(gam[j]) * rk[j] * d2[e]);
                     }
 #pragma unroll
-                    for (int q = 0; q < 4; q++) st_chunk8(sb + G_DH + sw128_chunk(r, 4 * h + q, 64), d1 + 8 * q, 1.f);
+                    for (int q = 0; q < 2; q++) st_chunk8(sb + G_DH + sw128_chunk(r, 2 * qt + q, 64), d1 + 8 * q, 1.f);
                 }
             }
             {  // T^T dU: dv = beta T^T dU; dbeta_r += sum_v V_rv (T^T dU)_rv
-                float x[64];
-                tmem_ld64(tmem_at(tm, 32 * lg, TM_T2 + 64 * h), x);
+                float x[32];
+                tmem_ld32(tl + TM_T2 + c32, x);
                 tmem_wait_ld();
                 if (act) {
                     float dot = 0.f;
 #pragma unroll
-                    for (int q = 0; q < 8; q++) {
+                    for (int q = 0; q < 4; q++) {
                         float vv[8];
-                        unpack8b(ld_shared_v4(sb + G_V + sw128_chunk(r, 8 * h + q, 64)), vv);
+                        ldrow8(G_V, r, 4 * qt + q, 64, vv);
 #pragma unroll
                         for (int e = 0; e < 8; e++) dot += vv[e] * x[8 * q + e];
                     }
-                    dbp[h * 64 + r] += dot;
+                    dbp[qt * 64 + r] += dot;
                     if (rowvalid) {
-                        const float br = bet[r];
+                        const float bb = bet[r];
                         float4* dst = reinterpret_cast<float4*>(a.dv + (((size_t)b * P.T + t0 + r) * P.Hv + hv) * kD +
-                                                                64 * h);
+                                                                c32);
 #pragma unroll
-                        for (int q = 0; q < 16; q++)
-                            dst[q] = make_float4(br * x[4 * q], br * x[4 * q + 1], br * x[4 * q + 2], br * x[4 * q + 3]);
+                        for (int q = 0; q < 8; q++)
+                            dst[q] = make_float4(bb * x[4 * q], bb * x[4 * q + 1], bb * x[4 * q + 2], bb * x[4 * q + 3]);
                     }
                 }
             }
@@ -493,36 +499,36 @@ __global__ void __launch_bounds__(256, 1)
         if (!wait_mma(47)) goto teardown;
         {
             {  // T^T dW: dK^ += beta Gamma (T^T dW); dbeta, dgamma from k^ . (T^T dW)
-                float x[64], dk[64];
-                tmem_ld64(tmem_at(tm, 32 * lg, TM_T2 + 64 * h), x);
-                tmem_ld64(tmem_at(tm, 32 * lg, TM_DK + 64 * h), dk);
+                float x[32], dk[32];
+                tmem_ld32(tl + TM_T2 + c32, x);
+                tmem_ld32(tl + TM_DK + c32, dk);
                 tmem_wait_ld();
-                const float Gr = expf(gam[r]), bgr = bet[r] * Gr;
+                const float Gr = __expf(gam[r]), bgr = bet[r] * Gr;
                 float dot = 0.f;
 #pragma unroll
-                for (int q = 0; q < 8; q++) {
+                for (int q = 0; q < 4; q++) {
                     float kk[8];
-                    unpack8b(ld_shared_v4(sb + G_KQ + sw128_chunk(r, 8 * h + q, 128)), kk);
+                    ldrow8(G_KQ, r, 4 * qt + q, 128, kk);
 #pragma unroll
                     for (int e = 0; e < 8; e++) {
                         dot += kk[e] * x[8 * q + e];
                         dk[8 * q + e] += bgr * x[8 * q + e];
                     }
                 }
-                tmem_st32(tmem_at(tm, 32 * lg, TM_DK + 64 * h), dk);
-                tmem_st32(tmem_at(tm, 32 * lg, TM_DK + 64 * h + 32), dk + 32);
+                tmem_st32(tl + TM_DK + c32, dk);
                 if (act) {
-                    dbp[h * 64 + r] += Gr * rk[r] * dot;
-                    dgp[h * 64 + r] += bgr * rk[r] * dot;
+                    dbp[qt * 64 + r] += Gr * rk[r] * dot;
+                    dgp[qt * 64 + r] += bgr * rk[r] * dot;
                 }
             }
             {  // Yt -> image (G_DH + 8K)
-                float v[32];
-                tmem_ld32(tmem_at(tm, 32 * lg, TM_T1 + 32 * h), v);
+                float v[16];
+                tmem_ld16(tl + TM_T1 + c16, v);
                 tmem_wait_ld();
                 if (act) {
 #pragma unroll
-                    for (int q = 0; q < 4; q++) st_chunk8(sb + G_DH + 8192 + sw128_chunk(r, 4 * h + q, 64), v + 8 * q, 1.f);
+                    for (int q = 0; q < 2; q++)
+                        st_chunk8(sb + G_DH + 8192 + sw128_chunk(r, 2 * qt + q, 64), v + 8 * q, 1.f);
                 }
             }
             tmem_wait_st();
@@ -539,19 +545,19 @@ __global__ void __launch_bounds__(256, 1)
         }
         if (!wait_mma(48)) goto teardown;
         {  // dA = strict_lower(-T^T Yt); terms of A_rj = beta_r rk_r rk_j E_rj G_rj
-            float v[32];
-            tmem_ld32(tmem_at(tm, 32 * lg, TM_T1 + 32 * h), v);
+            float v[16];
+            tmem_ld16(tl + TM_T1 + c16, v);
             tmem_wait_ld();
             if (act) {
                 const float gr = gam[r], br = bet[r], rkr = rk[r];
                 float db = 0.f, zs = 0.f;
 #pragma unroll
-                for (int e = 0; e < 32; e++) {
-                    const int j = 32 * h + e;
+                for (int e = 0; e < 16; e++) {
+                    const int j = c16 + e;
                     float m = 0.f, z = 0.f;
                     if (j < r) {
                         const float dA = -v[e];
-                        const float E = expf(gr - gam[j]);
+                        const float E = __expf(gr - gam[j]);
                         const float kk = rkr * rk[j] * GF[r * 64 + j];
                         db += dA * E * kk;
                         z = dA * br * E * kk;
@@ -561,8 +567,8 @@ __global__ void __launch_bounds__(256, 1)
                     ZS[r * 64 + j] = z;
                     MF[r * 64 + j] = m;
                 }
-                dbp[h * 64 + r] += db;
-                dgp[h * 64 + r] += zs;
+                dbp[qt * 64 + r] += db;
+                dgp[qt * 64 + r] += zs;
             }
         }
         __syncthreads();
@@ -572,14 +578,14 @@ __global__ void __launch_bounds__(256, 1)
             dgc[tid] -= s;
         }
         if (act) {  // N_rj = rk_j (M_rj + M_jr) -> image (G_DH + 16K)
-            float nrow[32];
+            float nrow[16];
 #pragma unroll
-            for (int e = 0; e < 32; e++) {
-                const int j = 32 * h + e;
+            for (int e = 0; e < 16; e++) {
+                const int j = c16 + e;
                 nrow[e] = rk[j] * (MF[r * 64 + j] + MF[j * 64 + r]);
             }
 #pragma unroll
-            for (int q = 0; q < 4; q++) st_chunk8(sb + G_DH + 16384 + sw128_chunk(r, 4 * h + q, 64), nrow + 8 * q, 1.f);
+            for (int q = 0; q < 2; q++) st_chunk8(sb + G_DH + 16384 + sw128_chunk(r, 2 * qt + q, 64), nrow + 8 * q, 1.f);
         }
         sync_for_mma();
 
@@ -593,14 +599,18 @@ __global__ void __launch_bounds__(256, 1)
         }
         // per-head scalars: dgamma -> dg (reverse cumsum), dbeta
         if (tid < 64) {
-            float s3 = sb3[tid] + sb3[64 + tid];
-            float dgam = dgp[tid] + dgp[64 + tid] + dgc[tid] - s3;
-            ZS[tid] = dgam;  // ZS column sums are done; reuse as a 64-vector
+            float s3 = 0.f, dg = dgc[tid];
+#pragma unroll
+            for (int k = 0; k < 4; k++) {
+                s3 += sb3[k * 64 + tid];
+                dg += dgp[k * 64 + tid];
+            }
+            ZS[tid] = dg - s3;  // ZS column sums are done; reuse as a 64-vector
         }
         __syncthreads();
         if (tid == 0) {
             float tot = 0.f;
-            for (int i = 0; i < 64; i++) tot += sb3[i] + sb3[64 + i];
+            for (int i = 0; i < 256; i++) tot += sb3[i];
             ZS[63] += tot + expf(gC) * (*hdh);  // Gamma_C <dH1, H0>
         }
         __syncthreads();
@@ -609,37 +619,36 @@ __global__ void __launch_bounds__(256, 1)
             for (int i = tid; i < 64; i++) s += ZS[i];
             const size_t bt = ((size_t)b * P.T + t0 + tid) * P.Hv + hv;
             a.dg[bt] = s;
-            a.dbeta[bt] = dbp[tid] + dbp[64 + tid];
+            a.dbeta[bt] = dbp[tid] + dbp[64 + tid] + dbp[128 + tid] + dbp[192 + tid];
         }
         if (!wait_mma(49)) goto teardown;
     }
 
     // ---------------------------------------------------------------- dq, dk: norm backward
     {
-        float x[64];
+        float x[32], xx[32];
 #pragma unroll 1
         for (int which = 0; which < 2; which++) {  // 0: q, 1: k
             const float* rho = which == 0 ? rq : rk;
             const int krow = which == 0 ? 64 + r : r;
-            tmem_ld64(tmem_at(tm, 32 * lg, (which == 0 ? TM_DQ : TM_DK) + 64 * h), x);
+            tmem_ld32(tl + (which == 0 ? TM_DQ : TM_DK) + c32, x);
             tmem_wait_ld();
-            float xx[64];
             float dot = 0.f;
 #pragma unroll
-            for (int q = 0; q < 8; q++) {
-                unpack8b(ld_shared_v4(sb + G_KQ + sw128_chunk(krow, 8 * h + q, 128)), xx + 8 * q);
+            for (int q = 0; q < 4; q++) {
+                ldrow8(G_KQ, krow, 4 * qt + q, 128, xx + 8 * q);
 #pragma unroll
                 for (int e = 0; e < 8; e++) dot += xx[8 * q + e] * x[8 * q + e];
             }
-            if (act) part[h * 64 + r] = dot;
+            if (act) part[qt * 64 + r] = dot;
             __syncthreads();
             if (rowvalid) {
                 const float rr = rho[r];
-                const float full = part[r] + part[64 + r];
-                float* dst = (which == 0 ? a.dq : a.dk) + (((size_t)b * P.T + t0 + r) * P.Hk + hk) * kD + 64 * h;
+                const float full = part[r] + part[64 + r] + part[128 + r] + part[192 + r];
+                float* dst = (which == 0 ? a.dq : a.dk) + (((size_t)b * P.T + t0 + r) * P.Hk + hk) * kD + c32;
                 float4* d4 = reinterpret_cast<float4*>(dst);
 #pragma unroll
-                for (int q = 0; q < 16; q++) {
+                for (int q = 0; q < 8; q++) {
                     float o4[4];
 #pragma unroll
                     for (int e = 0; e < 4; e++) {
@@ -721,7 +730,7 @@ cudaError_t launch_chunk_bwd(const ChunkBwdArgs& a, cudaStream_t s) {
         return e;
     dim3 grid(p.NC, p.Hk, p.B);
     trace_begin("chunk_grad", s);
-    grad_kernel<<<grid, 256, smem, s>>>(mq, mk, mv, mdo64, ga);
+    grad_kernel<<<grid, GRAD_THREADS, smem, s>>>(mq, mk, mv, mdo64, ga);
     trace_end(s);
     return cudaGetLastError();
 }

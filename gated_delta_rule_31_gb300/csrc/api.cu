@@ -7,7 +7,7 @@
 
 #include <vector>
 
-#include "../../include/gdr.h"
+#include "gdr.h"
 #include "chunk.h"
 #include "kernels.h"
 

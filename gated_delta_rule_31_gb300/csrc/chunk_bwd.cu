@@ -67,6 +67,9 @@ __device__ __forceinline__ void st_chunk8(uint32_t addr, const float* x, float s
     st_shared_v4(addr, pack_bf16(s * x[0], s * x[1]), pack_bf16(s * x[2], s * x[3]), pack_bf16(s * x[4], s * x[5]),
                  pack_bf16(s * x[6], s * x[7]));
 }
+// fp32 [64][64] scratch element (r, j), columns XOR-swizzled by the row so that a warp
+// touching one column across rows (or one row across columns) hits distinct banks
+__device__ __forceinline__ int fsw(int r, int j) { return r * 64 + (j ^ (r & 31)); }
 // 64 consecutive fp32 columns of this warp's 32 TMEM lanes
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
     tmem_ld32(taddr, v);
@@ -197,7 +200,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
         tmem_wait_ld();
         if (act) {
 #pragma unroll
-            for (int e = 0; e < 16; e++) GF[r * 64 + c16 + e] = v[e];
+            for (int e = 0; e < 16; e++) GF[fsw(r, c16 + e)] = v[e];
         }
         float z[32];
 #pragma unroll
@@ -357,7 +360,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
                         const int j = c16 + e;
                         const float z = v[e] * pr[e];
                         zs += z;
-                        ZS[r * 64 + j] = z;
+                        ZS[fsw(r, j)] = z;
                         const float ds = (j <= r) ? P.scale * __expf(gr - gam[j]) * v[e] : 0.f;
                         sk[e] = ds * rk[j];
                         sq[e] = ds * rq[r];
@@ -375,7 +378,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
         sync_for_mma();
         if (tid < 64) {  // column sums of Z: dgamma_j -= sum_r Z_rj
             float s = 0.f;
-            for (int i = 0; i < 64; i++) s += ZS[i * 64 + tid];
+            for (int i = 0; i < 64; i++) s += ZS[fsw(i, tid)];
             dgc[tid] -= s;
         }
 
@@ -558,14 +561,14 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
                     if (j < r) {
                         const float dA = -v[e];
                         const float E = __expf(gr - gam[j]);
-                        const float kk = rkr * rk[j] * GF[r * 64 + j];
+                        const float kk = rkr * rk[j] * GF[fsw(r, j)];
                         db += dA * E * kk;
                         z = dA * br * E * kk;
                         m = dA * br * E;
                     }
                     zs += z;
-                    ZS[r * 64 + j] = z;
-                    MF[r * 64 + j] = m;
+                    ZS[fsw(r, j)] = z;
+                    MF[fsw(r, j)] = m;
                 }
                 dbp[qt * 64 + r] += db;
                 dgp[qt * 64 + r] += zs;
@@ -574,7 +577,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
         __syncthreads();
         if (tid < 64) {
             float s = 0.f;
-            for (int i = 0; i < 64; i++) s += ZS[i * 64 + tid];
+            for (int i = 0; i < 64; i++) s += ZS[fsw(i, tid)];
             dgc[tid] -= s;
         }
         if (act) {  // N_rj = rk_j (M_rj + M_jr) -> image (G_DH + 16K)
@@ -582,7 +585,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
 #pragma unroll
             for (int e = 0; e < 16; e++) {
                 const int j = c16 + e;
-                nrow[e] = rk[j] * (MF[r * 64 + j] + MF[j * 64 + r]);
+                nrow[e] = rk[j] * (MF[fsw(r, j)] + MF[fsw(j, r)]);
             }
 #pragma unroll
             for (int q = 0; q < 2; q++) st_chunk8(sb + G_DH + 16384 + sw128_chunk(r, 2 * qt + q, 64), nrow + 8 * q, 1.f);

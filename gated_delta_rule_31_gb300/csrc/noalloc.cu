@@ -11,7 +11,7 @@
 
 #include <mutex>
 
-#include "../../include/gdr.h"
+#include "gdr.h"
 
 namespace {
 

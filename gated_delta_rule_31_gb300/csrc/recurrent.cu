@@ -156,10 +156,127 @@ __global__ void __launch_bounds__(WARPS * 32) recurrent_rows_kernel(RecurrentArg
     }
 }
 
+// Decode: one CTA of 4 warps per (b, hv); warp w streams state rows [w*Dv/4, (w+1)*Dv/4) in
+// groups of 4 rows, loading group g+1 while it reduces and writes group g, so each lane
+// keeps four to eight 128-bit loads in flight for the whole CTA life. With one wave of
+// CTAs (B*Hv of them) the grid has no tail.
+template <int DK, typename TIn>
+__global__ void __launch_bounds__(128) decode_kernel(RecurrentArgs a) {
+    constexpr int EL = DK / 32;
+    constexpr int G = 4;  // rows per group
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int hv = blockIdx.x, b = blockIdx.y;
+    const int hk = hv / (a.Hv / a.Hk);
+    const int rows_per_warp = a.Dv / 4;
+    const int ngroups = rows_per_warp / G;
+    const int r0 = warp * rows_per_warp;
+    const int c0 = lane * EL;
+    const size_t bh = (size_t)b * a.Hv + hv;
+    const float* Sin = a.h0 + bh * (size_t)a.Dv * DK;
+    float* Sout = a.ht + bh * (size_t)a.Dv * DK;
+
+    float cur[G][EL], nxt[G][EL];
+#pragma unroll
+    for (int i = 0; i < G; i++) ld_row<EL>(Sin + (size_t)(r0 + i) * DK + c0, cur[i]);
+
+    const TIn* q = reinterpret_cast<const TIn*>(a.q);
+    const TIn* k = reinterpret_cast<const TIn*>(a.k);
+    const TIn* v = reinterpret_cast<const TIn*>(a.v);
+    TIn* o = reinterpret_cast<TIn*>(a.o);
+    const size_t qk_off = ((size_t)b * a.Hk + hk) * DK + c0;
+    float kh[EL], qh[EL], dec[EL];
+    float sk = 0.f, sq = 0.f;
+#pragma unroll
+    for (int e = 0; e < EL; e++) {
+        kh[e] = to_f(k[qk_off + e]);
+        qh[e] = to_f(q[qk_off + e]);
+        sk += kh[e] * kh[e];
+        sq += qh[e] * qh[e];
+    }
+    if (a.use_norm) {
+        sk = warp_sum(sk);
+        sq = warp_sum(sq);
+        const float rk = 1.0f / sqrtf(sk + 1e-6f), rq = 1.0f / sqrtf(sq + 1e-6f);
+#pragma unroll
+        for (int e = 0; e < EL; e++) {
+            kh[e] *= rk;
+            qh[e] *= rq;
+        }
+    }
+    if (a.channel) {
+#pragma unroll
+        for (int e = 0; e < EL; e++) dec[e] = expf(a.g[bh * DK + c0 + e]);
+    } else {
+        const float sg = expf(a.g[bh]);
+#pragma unroll
+        for (int e = 0; e < EL; e++) dec[e] = sg;
+    }
+    float ak[EL];
+#pragma unroll
+    for (int e = 0; e < EL; e++) ak[e] = dec[e] * kh[e];
+    const float beta = a.beta[bh];
+    const size_t vo = bh * (size_t)a.Dv;
+
+    for (int gi = 0; gi < ngroups; gi++) {
+        const int rg = r0 + gi * G;
+        if (gi + 1 < ngroups) {
+#pragma unroll
+            for (int i = 0; i < G; i++) ld_row<EL>(Sin + (size_t)(rg + G + i) * DK + c0, nxt[i]);
+        }
+        // pass 1: prediction with the decay folded in
+        float p[G];
+#pragma unroll
+        for (int i = 0; i < G; i++) {
+            float acc = 0.f;
+#pragma unroll
+            for (int e = 0; e < EL; e++) acc += cur[i][e] * ak[e];
+            p[i] = acc;
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+            for (int i = 0; i < G; i++) p[i] += __shfl_xor_sync(0xffffffffu, p[i], off);
+        // pass 2: decay + rank-one update, output accumulated on the fly
+        float out[G];
+#pragma unroll
+        for (int i = 0; i < G; i++) {
+            const float d = beta * (to_f(v[vo + rg + i]) - p[i]);
+            float acc = 0.f;
+#pragma unroll
+            for (int e = 0; e < EL; e++) {
+                cur[i][e] = dec[e] * cur[i][e] + d * kh[e];
+                acc += cur[i][e] * qh[e];
+            }
+            out[i] = acc;
+            st_row<EL>(Sout + (size_t)(rg + i) * DK + c0, cur[i]);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+            for (int i = 0; i < G; i++) out[i] += __shfl_xor_sync(0xffffffffu, out[i], off);
+#pragma unroll
+        for (int i = 0; i < G; i++)
+            if (lane == i) o[vo + rg + i] = from_f<TIn>(a.scale * out[i]);
+#pragma unroll
+        for (int i = 0; i < G; i++)
+#pragma unroll
+            for (int e = 0; e < EL; e++) cur[i][e] = nxt[i][e];
+    }
+}
+
+template <int DK, typename TIn>
+static cudaError_t launch_decode(const RecurrentArgs& a, cudaStream_t s) {
+    dim3 grid(a.Hv, a.B);
+    trace_begin("decode_step", s);
+    decode_kernel<DK, TIn><<<grid, 128, 0, s>>>(a);
+    trace_end(s);
+    return cudaGetLastError();
+}
+
 template <int DK, typename TIn, int ROWS, int WARPS>
 static cudaError_t launch_rows(const RecurrentArgs& a, cudaStream_t s) {
     dim3 grid((a.Dv + WARPS * ROWS - 1) / (WARPS * ROWS), a.Hv, a.B);
-    trace_begin(a.T == 1 ? "decode_step" : "recurrent_fwd", s);
+    trace_begin("recurrent_fwd", s);
     recurrent_rows_kernel<DK, TIn, ROWS, WARPS><<<grid, WARPS * 32, 0, s>>>(a);
     trace_end(s);
     return cudaGetLastError();
@@ -175,13 +292,20 @@ static cudaError_t launch_dk(const RecurrentArgs& a, cudaStream_t s) {
     }
 }
 
-cudaError_t launch_recurrent(const RecurrentArgs& a, bool decode, cudaStream_t s) {
-    // Decode is bound by the state's HBM traffic: 4 rows per warp keep four 128-bit loads
-    // in flight per lane. The multi-token path is latency bound: 2 rows per warp.
-    if (a.bf16) {
-        return decode ? launch_dk<__nv_bfloat16, 4, 8>(a, s) : launch_dk<__nv_bfloat16, 2, 4>(a, s);
+// The multi-token path is latency bound: 2 rows per warp, small blocks.
+template <typename TIn>
+static cudaError_t launch_decode_dk(const RecurrentArgs& a, cudaStream_t s) {
+    switch (a.Dk) {
+        case 32: return launch_decode<32, TIn>(a, s);
+        case 64: return launch_decode<64, TIn>(a, s);
+        case 128: return launch_decode<128, TIn>(a, s);
+        default: return cudaErrorInvalidValue;
     }
-    return decode ? launch_dk<float, 4, 8>(a, s) : launch_dk<float, 2, 4>(a, s);
+}
+
+cudaError_t launch_recurrent(const RecurrentArgs& a, bool decode, cudaStream_t s) {
+    if (decode) return a.bf16 ? launch_decode_dk<__nv_bfloat16>(a, s) : launch_decode_dk<float>(a, s);
+    return a.bf16 ? launch_dk<__nv_bfloat16, 2, 4>(a, s) : launch_dk<float, 2, 4>(a, s);
 }
 
 }  // namespace gdr

@@ -42,9 +42,9 @@ constexpr uint32_t G_KB = 163840;   // Kbar image [64 x 128]; later dU image
 constexpr uint32_t G_GF = 180224;   // G = K K^T fp32 [64][64]                            [whole CTA]
 constexpr uint32_t G_ZS = 196608;   // fp32 [64][64] scratch (column sums)
 constexpr uint32_t G_SM = 212992;   // small arrays
-constexpr uint32_t G_SM_FLOATS = 64 * 4 + 256 * 4 + 64 + 16 + 4;  // see the carve-up in grad_kernel
-constexpr uint32_t G_BYTES = G_SM + 6144;
-static_assert(G_SM_FLOATS * 4 <= 6144, "small arrays");
+constexpr uint32_t G_SM_FLOATS = 64 * 4 + 256 * 4 + 64 + 272 + 4;  // see the carve-up in grad_kernel
+constexpr uint32_t G_BYTES = G_SM + 7168;
+static_assert(G_SM_FLOATS * 4 <= 7168, "small arrays");
 static_assert(G_BYTES + 1024 <= 232448, "grad smem");
 
 // TMEM columns: dQ^ accumulator, dK^ accumulator (both M=64 x 128), two temporaries.
@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
     const uint32_t sb = smem_u32(sm);
-    __shared__ uint64_t bar_ld, bar_mma;
+    __shared__ uint64_t bar_ld, bar_mma, bar_h;
     __shared__ uint32_t tmem_sh;
     __shared__ int abort_sh;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -112,14 +112,15 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
     float* sb3 = dbp + 256;                             // [4][64] b_r db_r partials
     float* part = sb3 + 256;                            // [4][64] norm-backward partial dots
     float* dgc = part + 256;                            // [64] column-sum terms of dgamma
-    float* red = dgc + 64;                              // [16] block reduction
-    float* hdh = red + 16;                              // <dH1, H0>
+    float* red = dgc + 64;                              // [16 + 256] reductions
+    float* hdh = red + 272;                             // <dH1, H0>
 
-    uint32_t ld_phase = 0, mma_phase = 0;
+    uint32_t ld_phase = 0, mma_phase = 0, h_phase = 0;
     if (tid == 0) {
         abort_sh = 0;
         mbar_init(&bar_ld, 1);
         mbar_init(&bar_mma, 1);
+        mbar_init(&bar_h, 1);
         fence_barrier_init();
     }
     if (warp == 0) {
@@ -160,6 +161,45 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
                    id64x128_mm = idesc_bf16(64, 128, 1, 1), id64x64_kk = idesc_bf16(64, 64, 0, 0),
                    id64x64_mm = idesc_bf16(64, 64, 1, 1);
 
+    // Inputs of value head hv, issued in pieces as their buffers free up (thread 0 only):
+    // piece 0: P, W, dO   1: Kbar   2: H0   3: T   4: v   5: dH1 (the arrival)
+    auto load_piece = [&](int hv, int piece) {
+        const size_t bh = (size_t)b * P.Hv + hv;
+        const size_t idx = bh * P.NC + c;
+        const uint8_t* rec = a.rec + idx * REC_BYTES;
+        const uint8_t* rec2 = a.rec2 + idx * REC2_BYTES;
+        switch (piece) {
+            case 0:
+                mbar_add_tx(&bar_h, 8192 + 16384 + 2 * 8192);
+                bulk_load(sm + G_P, rec + REC_P, 8192, &bar_h);
+                bulk_load(sm + G_W, rec2 + REC2_W, 16384, &bar_h);
+                tma_load_4d(sm + G_DO + 0, &mdo, 0, hv, t0, b, &bar_h);
+                tma_load_4d(sm + G_DO + 8192, &mdo, 64, hv, t0, b, &bar_h);
+                break;
+            case 1:
+                mbar_add_tx(&bar_h, 16384);
+                bulk_load(sm + G_KB, rec + REC_K, 16384, &bar_h);
+                break;
+            case 2:
+                mbar_add_tx(&bar_h, 32768);
+                bulk_load(sm + G_H0, a.hs + idx * STATE_IMG, 32768, &bar_h);
+                break;
+            case 3:
+                mbar_add_tx(&bar_h, 8192);
+                bulk_load(sm + G_T, rec2 + REC2_T, 8192, &bar_h);
+                break;
+            case 4:
+                mbar_add_tx(&bar_h, 2 * 8192);
+                tma_load_4d(sm + G_V + 0, &mv, 0, hv, t0, b, &bar_h);
+                tma_load_4d(sm + G_V + 8192, &mv, 64, hv, t0, b, &bar_h);
+                break;
+            default:
+                mbar_expect_tx(&bar_h, 32768);  // arrives: the head's phase completes when all landed
+                bulk_load(sm + G_DH, a.dhs + idx * STATE_IMG, 32768, &bar_h);
+                break;
+        }
+    };
+
     // ---------------------------------------------------------------- k, q of the chunk
     if (tid == 0) {
         mbar_expect_tx(&bar_ld, 4 * 8192);
@@ -167,6 +207,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
         tma_load_4d(sm + G_KQ + 16384, &mk, 64, hk, t0, b, &bar_ld);
         tma_load_4d(sm + G_KQ + 8192, &mq, 0, hk, t0, b, &bar_ld);
         tma_load_4d(sm + G_KQ + 24576, &mq, 64, hk, t0, b, &bar_ld);
+        for (int piece = 0; piece < 6; piece++) load_piece(hk * G, piece);  // first value head
     }
     if (!wait_ld(40)) goto teardown;
     {  // norm factors: 4 threads per row, 32 elements each
@@ -215,20 +256,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
         const size_t bh = (size_t)b * P.Hv + hv;
         const size_t idx = bh * P.NC + c;
         const uint8_t* rec = a.rec + idx * REC_BYTES;
-        const uint8_t* rec2 = a.rec2 + idx * REC2_BYTES;
-        if (tid == 0) {
-            mbar_expect_tx(&bar_ld, 4 * 8192 + 2 * 32768 + 8192 + 16384 + 8192 + 16384);
-            tma_load_4d(sm + G_V + 0, &mv, 0, hv, t0, b, &bar_ld);
-            tma_load_4d(sm + G_V + 8192, &mv, 64, hv, t0, b, &bar_ld);
-            tma_load_4d(sm + G_DO + 0, &mdo, 0, hv, t0, b, &bar_ld);
-            tma_load_4d(sm + G_DO + 8192, &mdo, 64, hv, t0, b, &bar_ld);
-            bulk_load(sm + G_H0, a.hs + idx * STATE_IMG, 32768, &bar_ld);
-            bulk_load(sm + G_DH, a.dhs + idx * STATE_IMG, 32768, &bar_ld);
-            bulk_load(sm + G_T, rec2 + REC2_T, 8192, &bar_ld);
-            bulk_load(sm + G_W, rec2 + REC2_W, 16384, &bar_ld);
-            bulk_load(sm + G_P, rec + REC_P, 8192, &bar_ld);
-            bulk_load(sm + G_KB, rec + REC_K, 16384, &bar_ld);
-        }
+        const bool more = hv + 1 < (hk + 1) * G;  // prefetch the next value head's inputs
         if (tid < 64) {
             const int t = t0 + tid;
             float gv = 0.f, bv = 0.f;
@@ -253,7 +281,11 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
         }
         __syncthreads();
         if (tid >= 32 && tid < 64) gam[tid] += gam[31];
-        if (!wait_ld(42)) goto teardown;
+        {
+            bool okh = mbar_wait(&bar_h, h_phase, &abort_sh, a.status, 42);
+            h_phase ^= 1;
+            if (__syncthreads_or(!okh)) goto teardown;
+        }
         const float gC = gam[63];
 
         // ------------------------------------------------------------ M1: W H0, dU
@@ -376,11 +408,15 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
             tmem_wait_st();
         }
         sync_for_mma();
-        if (tid < 64) {  // column sums of Z: dgamma_j -= sum_r Z_rj
+        if (tid < 256) {  // column sums of Z: dgamma_j -= sum_r Z_rj (4 threads per column)
+            const int j = tid & 63, part4 = tid >> 6;
             float s = 0.f;
-            for (int i = 0; i < 64; i++) s += ZS[fsw(i, tid)];
-            dgc[tid] -= s;
+#pragma unroll
+            for (int i = 16 * part4; i < 16 * part4 + 16; i++) s += ZS[fsw(i, j)];
+            red[16 + tid] = s;
         }
+        __syncthreads();
+        if (tid < 64) dgc[tid] -= red[16 + tid] + red[80 + tid] + red[144 + tid] + red[208 + tid];
 
         // ------------------------------------------------------------ M3
         if (tid == 0) {
@@ -400,6 +436,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
             mma_commit(&bar_mma);
         }
         if (!wait_mma(45)) goto teardown;
+        if (more && tid == 0) load_piece(hv + 1, 0);
         {
             const float br = __expf(gC - gam[r]);
             {  // Y: db_r = rk_r sum_d K_rd Y_rd; dK^ += b_r Y_r
@@ -447,6 +484,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
             mma_commit(&bar_mma);
         }
         if (!wait_mma(46)) goto teardown;
+        if (more && tid == 0) load_piece(hv + 1, 1);
         {
             {  // dT_rj = beta_j (dU V^T + Gamma_j rk_j dW K^T)_rj -> dT image (G_DH)
                 float d1[16], d2[16];
@@ -500,6 +538,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
             mma_commit(&bar_mma);
         }
         if (!wait_mma(47)) goto teardown;
+        if (more && tid == 0) load_piece(hv + 1, 2);
         {
             {  // T^T dW: dK^ += beta Gamma (T^T dW); dbeta, dgamma from k^ . (T^T dW)
                 float x[32], dk[32];
@@ -547,6 +586,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
             mma_commit(&bar_mma);
         }
         if (!wait_mma(48)) goto teardown;
+        if (more && tid == 0) load_piece(hv + 1, 3);
         {  // dA = strict_lower(-T^T Yt); terms of A_rj = beta_r rk_r rk_j E_rj G_rj
             float v[16];
             tmem_ld16(tl + TM_T1 + c16, v);
@@ -575,10 +615,12 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
             }
         }
         __syncthreads();
-        if (tid < 64) {
+        if (tid < 256) {
+            const int j = tid & 63, part4 = tid >> 6;
             float s = 0.f;
-            for (int i = 0; i < 64; i++) s += ZS[fsw(i, tid)];
-            dgc[tid] -= s;
+#pragma unroll
+            for (int i = 16 * part4; i < 16 * part4 + 16; i++) s += ZS[fsw(i, j)];
+            red[16 + tid] = s;
         }
         if (act) {  // N_rj = rk_j (M_rj + M_jr) -> image (G_DH + 16K)
             float nrow[16];
@@ -599,32 +641,42 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
                 mma(TM_DK, desc_kmajor(sb + G_DH + 16384, 64, 0, k0), desc_mnmajor(sb + G_KQ, 128, 0, k0), id64x128_km,
                     true);
             mma_commit(&bar_mma);
+            if (more) load_piece(hv + 1, 4);  // v: its buffer held M, read before the sync above
         }
-        // per-head scalars: dgamma -> dg (reverse cumsum), dbeta
-        if (tid < 64) {
-            float s3 = 0.f, dg = dgc[tid];
+        // per-head scalars: dgamma -> dg (reverse cumsum within the chunk), dbeta
+        if (tid < 64) {  // two warps; row r = tid
+            float s3 = 0.f, dgr = dgc[tid] - (red[16 + tid] + red[80 + tid] + red[144 + tid] + red[208 + tid]);
 #pragma unroll
             for (int k = 0; k < 4; k++) {
                 s3 += sb3[k * 64 + tid];
-                dg += dgp[k * 64 + tid];
+                dgr += dgp[k * 64 + tid];
             }
-            ZS[tid] = dg - s3;  // ZS column sums are done; reuse as a 64-vector
+            dgr -= s3;
+            const float tot3 = warp_sum(s3);  // per warp; the two halves meet through red[]
+            if (lane == 0) red[warp] = tot3;
+            // suffix sum within the warp
+            float suf = dgr;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float y = __shfl_down_sync(0xffffffffu, suf, o);
+                if (lane + o < 32) suf += y;
+            }
+            ZS[tid] = suf;
         }
         __syncthreads();
-        if (tid == 0) {
-            float tot = 0.f;
-            for (int i = 0; i < 256; i++) tot += sb3[i];
-            ZS[63] += tot + expf(gC) * (*hdh);  // Gamma_C <dH1, H0>
-        }
-        __syncthreads();
-        if (tid < 64 && t0 + tid < P.T) {
-            float s = 0.f;
-            for (int i = tid; i < 64; i++) s += ZS[i];
-            const size_t bt = ((size_t)b * P.T + t0 + tid) * P.Hv + hv;
-            a.dg[bt] = s;
-            a.dbeta[bt] = dbp[tid] + dbp[64 + tid] + dbp[128 + tid] + dbp[192 + tid];
+        if (tid < 64) {
+            // rows 0-31 also get the suffix of rows 32-63; every row gets the gamma_C terms
+            // (they sit on the last row, which every suffix includes)
+            const float last = red[0] + red[1] + expf(gC) * (*hdh);  // sum b db + Gamma_C <dH1,H0>
+            float s = ZS[tid] + last + (tid < 32 ? ZS[32] : 0.f);
+            if (t0 + tid < P.T) {
+                const size_t bt = ((size_t)b * P.T + t0 + tid) * P.Hv + hv;
+                a.dg[bt] = s;
+                a.dbeta[bt] = dbp[tid] + dbp[64 + tid] + dbp[128 + tid] + dbp[192 + tid];
+            }
         }
         if (!wait_mma(49)) goto teardown;
+        if (more && tid == 0) load_piece(hv + 1, 5);
     }
 
     // ---------------------------------------------------------------- dq, dk: norm backward

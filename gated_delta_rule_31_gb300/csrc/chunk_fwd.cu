@@ -389,12 +389,21 @@ cudaError_t launch_prep(const PrepArgs& a, const CUtensorMap& mq, const CUtensor
 }
 
 // ================================================================== scan kernel
-// Per stage (one chunk): Mneg 32 KB | Kbar or Qc^T source 16 KB | Qc 16 KB | P 8 KB | U~ / dO slice 4 KB.
-constexpr uint32_t ST_M = 0, ST_K = 32768, ST_Q = 49152, ST_P = 65536, ST_U = 73728;
-constexpr uint32_t STG = 78848;                  // 77 KB, 1024-aligned stages
-constexpr uint32_t SS_H = 2 * STG;               // two bf16 [128 x 32] SW64 state tiles (8 KB each)
-constexpr uint32_t SS_BYTES = SS_H + 16384;
-static_assert(SS_BYTES + 1024 <= 232448, "scan smem");
+// One ring stage per chunk. Forward with outputs (2 stages): Mneg 32 KB | Kbar 16 KB | Qc 16 KB |
+// P 8 KB | U~ slice 4 KB. States / backward (3 stages): Mneg 32 KB | Kbar or Qc 16 KB | U~ or dO
+// slice 4 KB. The third stage lets the next chunk's operators arrive a step earlier.
+template <int MODE>
+struct ScanLayout {
+    static constexpr int NS = MODE == SCAN_FWD_OUT ? 2 : 3;
+    static constexpr uint32_t ST_M = 0, ST_K = 32768;  // ST_K: Kbar (forward) or Qc (backward)
+    static constexpr uint32_t ST_Q = 49152, ST_P = 65536;  // forward outputs only
+    static constexpr uint32_t ST_U = MODE == SCAN_FWD_OUT ? 73728 : 49152;
+    static constexpr uint32_t STG = MODE == SCAN_FWD_OUT ? 78848 : 53248;
+    static constexpr uint32_t SS_H = NS * STG;  // two bf16 [128 x 32] SW64 state tiles (8 KB each)
+    static constexpr uint32_t BYTES = SS_H + 16384;
+    static_assert(BYTES + 1024 <= 232448, "scan smem");
+    static_assert(STG % 1024 == 0, "stage alignment");
+};
 
 __device__ __forceinline__ void write_state_tile(uint32_t tile, int d, const float* H) {
 #pragma unroll
@@ -405,10 +414,14 @@ __device__ __forceinline__ void write_state_tile(uint32_t tile, int d, const flo
 
 template <int MODE>
 __global__ void __launch_bounds__(192, 1) scan_kernel(const __grid_constant__ CUtensorMap mdo, ScanArgs a) {
+    using LY = ScanLayout<MODE>;
+    constexpr int NS = LY::NS;
+    constexpr uint32_t ST_M = LY::ST_M, ST_K = LY::ST_K, ST_Q = LY::ST_Q, ST_P = LY::ST_P, ST_U = LY::ST_U;
+    constexpr uint32_t STG = LY::STG, SS_H = LY::SS_H;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
     const uint32_t sb = smem_u32(sm);
-    __shared__ uint64_t full[2], empty[2], hready, sfull, ofull[2], drain;
+    __shared__ uint64_t full[3], empty[3], hready, sfull, ofull[2], drain;
     __shared__ uint32_t tmem_sh;
     __shared__ int abort_sh;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -420,11 +433,12 @@ __global__ void __launch_bounds__(192, 1) scan_kernel(const __grid_constant__ CU
 
     if (tid == 0) {
         abort_sh = 0;
-        for (int s = 0; s < 2; s++) {
+        for (int s = 0; s < NS; s++) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
-            mbar_init(&ofull[s], 1);
         }
+        mbar_init(&ofull[0], 1);
+        mbar_init(&ofull[1], 1);
         mbar_init(&hready, 1);
         mbar_init(&sfull, 1);
         mbar_init(&drain, 1);
@@ -443,8 +457,8 @@ __global__ void __launch_bounds__(192, 1) scan_kernel(const __grid_constant__ CU
     if (warp == 0) {
         if (lane == 0) {  // producer: bulk copies of the chunk records (+ dO slice via TMA)
             for (int i = 0; i < NC; i++) {
-                const int c = chunk_of(i), s = i & 1;
-                if (i >= 2 && !mbar_wait(&empty[s], ((i >> 1) + 1) & 1, &abort_sh, a.status, 20)) break;
+                const int c = chunk_of(i), s = i % NS;
+                if (i >= NS && !mbar_wait(&empty[s], ((i / NS) + 1) & 1, &abort_sh, a.status, 20)) break;
                 uint8_t* st = sm + s * STG;
                 const uint8_t* rec = a.rec + (bh * NC + c) * REC_BYTES;
                 uint32_t bytes = 32768 + 4096 + 16384;
@@ -460,7 +474,7 @@ __global__ void __launch_bounds__(192, 1) scan_kernel(const __grid_constant__ CU
                     bulk_load(st + ST_P, rec + REC_P, 8192, &full[s]);
                 }
                 if (MODE == SCAN_BWD) {
-                    bulk_load(st + ST_Q, rec + REC_Q, 16384, &full[s]);
+                    bulk_load(st + ST_K, rec + REC_Q, 16384, &full[s]);
                     tma_load_4d(st + ST_U, &mdo, kSlice * j, hv, kChunk * c, b, &full[s]);
                 }
                 last_loaded = i;
@@ -472,14 +486,14 @@ __global__ void __launch_bounds__(192, 1) scan_kernel(const __grid_constant__ CU
             const uint32_t id_pre = idesc_bf16(128, 32, 1, 1);
             const uint32_t id_out = idesc_bf16(64, 32, 0, 1);
             auto issue_pre = [&](int i) {  // state-independent term into Ds[i & 1]
-                const uint32_t st = sb + (i & 1) * STG;
-                const uint32_t src = MODE == SCAN_BWD ? st + ST_Q : st + ST_K;  // Qc^T dO  or  Kbar^T U~
+                const uint32_t st = sb + (i % NS) * STG;
+                const uint32_t src = st + ST_K;  // Qc^T dO (backward)  or  Kbar^T U~ (forward)
                 for (int k0 = 0; k0 < kChunk; k0 += 16)
                     mma_bf16(tm + 32 * (i & 1), desc_mnmajor(src, 64, 0, k0), desc_mnmajor_sw64(st + ST_U, 64, k0),
                              id_pre, k0 > 0);
             };
             for (int i = 0; i < NC; i++) {
-                const int s = i & 1;
+                const int s = i % NS, sd = i & 1;  // ring stage, double-buffer index
                 const uint32_t st = sb + s * STG;
                 if (i == 0) {
                     if (!mbar_wait(&full[0], 0, &abort_sh, a.status, 21)) break;
@@ -492,21 +506,21 @@ __global__ void __launch_bounds__(192, 1) scan_kernel(const __grid_constant__ CU
                 for (int k0 = 0; k0 < kD; k0 += 16) {
                     const uint64_t ad =
                         MODE == SCAN_BWD ? desc_mnmajor(st + ST_M, 128, 0, k0) : desc_kmajor(st + ST_M, 128, 0, k0);
-                    mma_bf16(tm + 32 * s, ad, desc_mnmajor_sw64(ht, 128, k0), id_state, 1);
+                    mma_bf16(tm + 32 * sd, ad, desc_mnmajor_sw64(ht, 128, k0), id_state, 1);
                 }
                 mma_commit(&sfull);
                 if (MODE == SCAN_FWD_OUT) {
                     for (int k0 = 0; k0 < kD; k0 += 16)
-                        mma_bf16(tm + 64 + 32 * s, desc_kmajor(st + ST_Q, 64, 0, k0), desc_mnmajor_sw64(ht, 128, k0),
+                        mma_bf16(tm + 64 + 32 * sd, desc_kmajor(st + ST_Q, 64, 0, k0), desc_mnmajor_sw64(ht, 128, k0),
                                  id_out, k0 > 0);
                     for (int k0 = 0; k0 < kChunk; k0 += 16)
-                        mma_bf16(tm + 64 + 32 * s, desc_kmajor(st + ST_P, 64, 0, k0),
+                        mma_bf16(tm + 64 + 32 * sd, desc_kmajor(st + ST_P, 64, 0, k0),
                                  desc_mnmajor_sw64(st + ST_U, 64, k0), id_out, 1);
-                    mma_commit(&ofull[s]);
+                    mma_commit(&ofull[sd]);
                 }
                 mma_commit(&empty[s]);
                 if (i + 1 < NC) {
-                    if (!mbar_wait(&full[s ^ 1], ((i + 1) >> 1) & 1, &abort_sh, a.status, 23)) break;
+                    if (!mbar_wait(&full[(i + 1) % NS], ((i + 1) / NS) & 1, &abort_sh, a.status, 23)) break;
                     tc_fence_after();
                     issue_pre(i + 1);
                 }
@@ -601,15 +615,15 @@ __global__ void __launch_bounds__(192, 1) scan_kernel(const __grid_constant__ CU
     __syncthreads();
     if (abort_sh && tid == 0 && last_loaded >= 0) {  // copies still in flight must land first
         volatile int never = 0;
-        for (int i = last_loaded > 0 ? last_loaded - 1 : 0; i <= last_loaded; i++)
-            mbar_wait(&full[i & 1], (i >> 1) & 1, &never, nullptr, 0);
+        for (int i = last_loaded >= NS - 1 ? last_loaded - (NS - 1) : 0; i <= last_loaded; i++)
+            mbar_wait(&full[i % NS], (i / NS) & 1, &never, nullptr, 0);
     }
     __syncthreads();
     if (warp == 0) tmem_dealloc(tm, 128);
 }
 
 cudaError_t launch_scan(const ScanArgs& a, int mode, const CUtensorMap* mdo, cudaStream_t s) {
-    const int smem = SS_BYTES + 1024;
+    const int smem = (mode == SCAN_FWD_OUT ? ScanLayout<SCAN_FWD_OUT>::BYTES : ScanLayout<SCAN_BWD>::BYTES) + 1024;
     dim3 grid(kSlices, a.p.Hv, a.p.B);
     CUtensorMap dummy;
     memset(&dummy, 0, sizeof(dummy));

@@ -30,8 +30,8 @@ constexpr int LDA = 65;
 constexpr uint32_t PS_A = 49152;     // A fp32 [64][65]; then [Tw; Tu] 128 x 64 bf16; then Wbar image
 constexpr uint32_t PS_T = 66560;     // T fp32 [64][65]; then W image [64 x 128]
 constexpr uint32_t PS_P = 83968;     // P image [64 x 64]
-constexpr uint32_t PS_SCR = 92160;   // solve scratch [3][16][17] fp32
-constexpr uint32_t PS_SMALL = PS_SCR + 3 * 16 * 17 * 4;  // per-token factors (8 x 64 fp32)
+constexpr uint32_t PS_SCR = 92160;   // solve scratch: Y_IK blocks [6][16][17] fp32
+constexpr uint32_t PS_SMALL = PS_SCR + 6 * 16 * 17 * 4;  // per-token factors (8 x 64 fp32)
 constexpr uint32_t PS_BYTES = PS_SMALL + 2048;
 constexpr uint32_t PS_TT = PS_A, PS_WBAR = PS_A, PS_W = PS_T;
 static_assert(PS_A % 1024 == 0 && PS_T % 1024 == 0 && PS_P % 1024 == 0, "align");
@@ -124,6 +124,15 @@ __global__ void __launch_bounds__(256, 2)
     bool ok = mbar_wait(&bar_tma, 0, &abort_sh, a.status, 10);
     if (__syncthreads_or(!ok)) goto teardown;
 
+    // G = K K^T (rows 0-63) and Q K^T (rows 64-127) in one M=128 product on the raw bf16
+    // operands; the norm factors are applied in the epilogue, so they are computed meanwhile
+    if (tid == 0) {
+        tc_fence_after();
+        const uint32_t id = idesc_bf16(128, 64, 0, 0);
+        for (int k0 = 0; k0 < kD; k0 += 16)
+            mma_bf16(tm, desc_kmajor(sb + PS_KQ, 128, 0, k0), desc_kmajor(sb + PS_KQ, 128, 0, k0), id, k0 > 0);
+        mma_commit(&bar_mma);
+    }
     {  // L2 norm factors of the 64 keys (rows 0-63) and 64 queries (rows 64-127)
         const int row = tid >> 1, half = tid & 1;
         const uint32_t base = sb + PS_KQ + half * 16384 + row * 128;
@@ -146,14 +155,6 @@ __global__ void __launch_bounds__(256, 2)
         fq[tid] = P.scale * G * rho[64 + tid];
     }
 
-    // G = K K^T (rows 0-63) and Q K^T (rows 64-127) in one M=128 product, raw bf16 operands
-    if (tid == 0) {
-        tc_fence_after();
-        const uint32_t id = idesc_bf16(128, 64, 0, 0);
-        for (int k0 = 0; k0 < kD; k0 += 16)
-            mma_bf16(tm, desc_kmajor(sb + PS_KQ, 128, 0, k0), desc_kmajor(sb + PS_KQ, 128, 0, k0), id, k0 > 0);
-        mma_commit(&bar_mma);
-    }
     ok = mbar_wait(&bar_mma, 0, &abort_sh, a.status, 11);
     if (__syncthreads_or(!ok)) goto teardown;
     tc_fence_after();
@@ -192,49 +193,59 @@ __global__ void __launch_bounds__(256, 2)
     tc_fence_before();
     __syncthreads();
 
-    // T = (I + A)^-1, unit lower triangular: 16x16 diagonal blocks by forward substitution,
-    // then the off-diagonal blocks T_IJ = -T_II sum_{J<=K<I} A_IK T_KJ by distance I-J.
+    // T = (I + A)^-1 (unit lower triangular) by 16x16 blocks. Phase 1 (160 threads, one
+    // column each): forward substitution with L_II = I + A_II gives the diagonal inverses T_II
+    // (right-hand side e_c) and Y_IK = T_II A_IK for I > K (right-hand side column c of A_IK).
+    // Then T_IJ = -sum_{J<=K<I} Y_IK T_KJ by block distance I-J = 1, 2, 3.
     for (int idx = tid; idx < 64 * 64; idx += 256) {
         const int i = idx >> 6, j = idx & 63;
         if ((i >> 4) < (j >> 4)) Tm[i * LDA + j] = 0.f;
     }
-    if (tid < 64) {
-        const int I = tid >> 4, cc = tid & 15;
+    if (tid < 160) {
+        int I, K, cc;
+        const bool diag = tid < 64;
+        if (diag) {
+            I = tid >> 4;
+            K = I;
+            cc = tid & 15;
+        } else {
+            const int pidx = (tid - 64) >> 4;  // pairs (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
+            cc = (tid - 64) & 15;
+            I = pidx == 0 ? 1 : (pidx < 3 ? 2 : 3);
+            K = pidx - I * (I - 1) / 2;
+        }
         const float* Ab = Am + (16 * I) * LDA + 16 * I;
-        float x[16];
+        const float* Bc = Am + (16 * I) * LDA + 16 * K + cc;
+        float y[16];
 #pragma unroll
         for (int i = 0; i < 16; i++) {
-            float s = 0.f;
+            float s = diag ? (i == cc ? 1.f : 0.f) : Bc[i * LDA];
 #pragma unroll
-            for (int j = 0; j < i; j++) s += Ab[i * LDA + j] * x[j];
-            x[i] = (i < cc) ? 0.f : ((i == cc) ? 1.f : -s);
+            for (int j = 0; j < i; j++) s -= Ab[i * LDA + j] * y[j];
+            y[i] = s;
         }
+        if (diag) {
 #pragma unroll
-        for (int i = 0; i < 16; i++) Tm[(16 * I + i) * LDA + 16 * I + cc] = x[i];
+            for (int i = 0; i < 16; i++) Tm[(16 * I + i) * LDA + 16 * I + cc] = y[i];
+        } else {
+            float* yp = Xs + ((tid - 64) >> 4) * (16 * 17);
+#pragma unroll
+            for (int i = 0; i < 16; i++) yp[i * 17 + cc] = y[i];
+        }
     }
     __syncthreads();
     for (int dlev = 1; dlev <= 3; dlev++) {
         const int nb = 4 - dlev;
         for (int o = tid; o < nb * 256; o += 256) {
-            const int blk = o >> 8, i = (o >> 4) & 15, cc = o & 15;
-            const int J = blk, I = blk + dlev;
+            const int J = o >> 8, i = (o >> 4) & 15, cc = o & 15;
+            const int I = J + dlev;
             float s = 0.f;
             for (int K = J; K < I; K++) {
-                const float* ar = Am + (16 * I + i) * LDA + 16 * K;
+                const float* yr = Xs + (I * (I - 1) / 2 + K) * (16 * 17) + i * 17;
                 const float* tc = Tm + (16 * K) * LDA + 16 * J + cc;
 #pragma unroll
-                for (int m = 0; m < 16; m++) s += ar[m] * tc[m * LDA];
+                for (int m = 0; m < 16; m++) s += yr[m] * tc[m * LDA];
             }
-            Xs[(blk * 16 + i) * 17 + cc] = s;
-        }
-        __syncthreads();
-        for (int o = tid; o < nb * 256; o += 256) {
-            const int blk = o >> 8, i = (o >> 4) & 15, cc = o & 15;
-            const int J = blk, I = blk + dlev;
-            const float* tr = Tm + (16 * I + i) * LDA + 16 * I;
-            float s = 0.f;
-#pragma unroll
-            for (int m = 0; m < 16; m++) s += tr[m] * Xs[(blk * 16 + m) * 17 + cc];
             Tm[(16 * I + i) * LDA + 16 * J + cc] = -s;
         }
         __syncthreads();

@@ -160,10 +160,13 @@ __global__ void __launch_bounds__(WARPS * 32) recurrent_rows_kernel(RecurrentArg
 // groups of 4 rows, loading group g+1 while it reduces and writes group g, so each lane
 // keeps four to eight 128-bit loads in flight for the whole CTA life. With one wave of
 // CTAs (B*Hv of them) the grid has no tail.
+#ifndef GDR_DECODE_GROUP
+#define GDR_DECODE_GROUP 4
+#endif
 template <int DK, typename TIn>
 __global__ void __launch_bounds__(128) decode_kernel(RecurrentArgs a) {
     constexpr int EL = DK / 32;
-    constexpr int G = 4;  // rows per group
+    constexpr int G = GDR_DECODE_GROUP;  // rows per group
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int hv = blockIdx.x, b = blockIdx.y;
     const int hk = hv / (a.Hv / a.Hk);

@@ -65,6 +65,14 @@ def lib():
         L.gdr_bwd_chunked.restype = ctypes.c_int
         L.gdr_decode_step.argtypes = [PP] + [P] * 7 + [st]
         L.gdr_decode_step.restype = ctypes.c_int
+        L.gdr_chunk_states_bytes.argtypes = [PP]
+        L.gdr_chunk_states_bytes.restype = sz
+        L.gdr_bwd_chunked_states_workspace.argtypes = [PP]
+        L.gdr_bwd_chunked_states_workspace.restype = sz
+        L.gdr_fwd_chunked_states.argtypes = [PP] + [P] * 8 + [P, sz, P, sz, st]
+        L.gdr_fwd_chunked_states.restype = ctypes.c_int
+        L.gdr_bwd_chunked_states.argtypes = [PP] + [P] * 5 + [P, sz] + [P] * 8 + [P, sz, st]
+        L.gdr_bwd_chunked_states.restype = ctypes.c_int
         L.gdr_workspace_status.argtypes = [P, sz, st]
         L.gdr_workspace_status.restype = ctypes.c_int
         L.gdr_trace_enable.argtypes = [ctypes.c_int]
@@ -169,8 +177,10 @@ def fwd_sequential(q, k, v, g, beta, h0=None, scale=None, use_qk_l2norm=True, ou
 
 
 def fwd_chunked(q, k, v, g, beta, h0=None, scale=None, use_qk_l2norm=True, output_final_state=True,
-                workspace=None):
-    """Chunked prefill forward on the tensor cores (gdr_fwd_chunked). Returns (o, ht or None)."""
+                workspace=None, save_states=False):
+    """Chunked prefill forward on the tensor cores (gdr_fwd_chunked). Returns (o, ht or None),
+    or (o, ht, states) with save_states=True (gdr_fwd_chunked_states: the chunk-start states
+    kept for bwd_chunked(..., states=states))."""
     _check_inputs(q, k, v, g, beta, h0)
     p = _problem(q, v, g, scale, use_qk_l2norm)
     o = torch.empty(v.shape, dtype=v.dtype, device=v.device)
@@ -179,14 +189,24 @@ def fwd_chunked(q, k, v, g, beta, h0=None, scale=None, use_qk_l2norm=True, outpu
     if nbytes == 0:
         _check(2)  # unsupported combination
     ws = _workspace(nbytes, q.device, workspace)
-    _check(lib().gdr_fwd_chunked(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
-                                 _ptr(o), _ptr(ht), _ptr(ws), ctypes.c_size_t(nbytes), _stream(q.device)))
-    return o, ht
+    if not save_states:
+        _check(lib().gdr_fwd_chunked(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
+                                     _ptr(o), _ptr(ht), _ptr(ws), ctypes.c_size_t(nbytes), _stream(q.device)))
+        return o, ht
+    sb = int(lib().gdr_chunk_states_bytes(ctypes.byref(p)))
+    states = torch.empty(max(sb, 256), dtype=torch.uint8, device=q.device)
+    _check(lib().gdr_fwd_chunked_states(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
+                                        _ptr(o), _ptr(ht), _ptr(states), ctypes.c_size_t(sb), _ptr(ws),
+                                        ctypes.c_size_t(nbytes), _stream(q.device)))
+    return o, ht, states
 
 
-def bwd_chunked(q, k, v, g, beta, h0, do, dht=None, scale=None, use_qk_l2norm=True, workspace=None):
+def bwd_chunked(q, k, v, g, beta, h0, do, dht=None, scale=None, use_qk_l2norm=True, workspace=None,
+                states=None):
     """Chunked backward (gdr_bwd_chunked) of <do,o> + <dht,ht>. Returns a dict of fp32
-    gradients dq, dk, dv, dg, dbeta, dh0."""
+    gradients dq, dk, dv, dg, dbeta, dh0. With `states` from fwd_chunked(save_states=True)
+    on the same inputs, gdr_bwd_chunked_states reads them instead of re-running the
+    forward scan (h0 is then unused)."""
     _check_inputs(q, k, v, g, beta, h0)
     _need(do, "do", dtype=v.dtype, device=v.device, shape=v.shape)
     p = _problem(q, v, g, scale, use_qk_l2norm)
@@ -196,14 +216,26 @@ def bwd_chunked(q, k, v, g, beta, h0, do, dht=None, scale=None, use_qk_l2norm=Tr
     out = dict(dq=torch.empty(q.shape, **f32), dk=torch.empty(k.shape, **f32), dv=torch.empty(v.shape, **f32),
                dg=torch.empty(g.shape, **f32), dbeta=torch.empty(beta.shape, **f32),
                dh0=torch.empty((p.B, p.Hv, p.Dv, p.Dk), **f32))
-    nbytes = bwd_workspace_bytes(p)
+    if states is None:
+        nbytes = bwd_workspace_bytes(p)
+        if nbytes == 0:
+            _check(2)
+        ws = _workspace(nbytes, q.device, workspace)
+        _check(lib().gdr_bwd_chunked(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
+                                     _ptr(do), _ptr(dht), _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]),
+                                     _ptr(out["dg"]), _ptr(out["dbeta"]), _ptr(out["dh0"]), _ptr(ws),
+                                     ctypes.c_size_t(nbytes), _stream(q.device)))
+        return out
+    _need(states, "states", dtype=torch.uint8, device=q.device)
+    nbytes = int(lib().gdr_bwd_chunked_states_workspace(ctypes.byref(p)))
     if nbytes == 0:
         _check(2)
     ws = _workspace(nbytes, q.device, workspace)
-    _check(lib().gdr_bwd_chunked(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
-                                 _ptr(do), _ptr(dht), _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]),
-                                 _ptr(out["dg"]), _ptr(out["dbeta"]), _ptr(out["dh0"]), _ptr(ws),
-                                 ctypes.c_size_t(nbytes), _stream(q.device)))
+    _check(lib().gdr_bwd_chunked_states(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                        _ptr(states), ctypes.c_size_t(states.numel()), _ptr(do), _ptr(dht),
+                                        _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dg"]),
+                                        _ptr(out["dbeta"]), _ptr(out["dh0"]), _ptr(ws), ctypes.c_size_t(nbytes),
+                                        _stream(q.device)))
     return out
 
 

@@ -54,7 +54,8 @@ struct WsLayout {
 
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-inline WsLayout ws_layout(const ChunkProblem& p, bool bwd) {
+// bwd_states: a backward that reads saved chunk-start states (no states region of its own).
+inline WsLayout ws_layout(const ChunkProblem& p, bool bwd, bool bwd_states = false) {
     WsLayout w;
     w.ncpad = (int)round_up((size_t)p.NC, 4);
     size_t nh = (size_t)p.B * p.Hv;
@@ -66,7 +67,8 @@ inline WsLayout ws_layout(const ChunkProblem& p, bool bwd) {
         w.rec2 = end;
         end = w.rec2 + nh * p.NC * (size_t)REC2_BYTES;
         w.hs = end;
-        w.dhs = w.hs + nh * p.NC * (size_t)STATE_IMG;
+        if (!bwd_states) end += nh * p.NC * (size_t)STATE_IMG;
+        w.dhs = end;
         end = w.dhs + nh * p.NC * (size_t)STATE_IMG;
     }
     w.total = end;
@@ -74,6 +76,8 @@ inline WsLayout ws_layout(const ChunkProblem& p, bool bwd) {
 }
 inline size_t chunk_fwd_workspace(const ChunkProblem& p) { return ws_layout(p, false).total; }
 inline size_t chunk_bwd_workspace(const ChunkProblem& p) { return ws_layout(p, true).total; }
+inline size_t chunk_bwd_states_workspace(const ChunkProblem& p) { return ws_layout(p, true, true).total; }
+inline size_t chunk_states_bytes(const ChunkProblem& p) { return (size_t)p.B * p.Hv * p.NC * STATE_IMG; }
 
 struct ChunkFwdArgs {
     ChunkProblem p;
@@ -81,6 +85,7 @@ struct ChunkFwdArgs {
     const float *g, *beta, *h0;
     void* o;
     float* ht;
+    void* states;  // optional: chunk-start states kept for the backward
     void* ws;
 };
 struct ChunkBwdArgs {
@@ -90,6 +95,7 @@ struct ChunkBwdArgs {
     const void* do_;
     const float* dht;
     float *dq, *dk, *dv, *dg, *dbeta, *dh0;
+    const void* states;  // optional: chunk-start states saved by the forward
     void* ws;
 };
 

@@ -731,7 +731,8 @@ teardown:
 
 cudaError_t launch_chunk_bwd(const ChunkBwdArgs& a, cudaStream_t s) {
     const ChunkProblem& p = a.p;
-    const WsLayout w = ws_layout(p, true);
+    const bool saved = a.states != nullptr;
+    const WsLayout w = ws_layout(p, true, saved);
     uint8_t* ws = static_cast<uint8_t*>(a.ws);
     CUtensorMap mq, mk, mv, mdo32, mdo64;
     if (!make_qkv_maps(p, a.q, a.k, a.v, &mq, &mk, &mv)) return cudaErrorInvalidValue;
@@ -760,7 +761,8 @@ cudaError_t launch_chunk_bwd(const ChunkBwdArgs& a, cudaStream_t s) {
     sa.states = ws + w.hs;
     sa.status = status;
     sa.ncpad = w.ncpad;
-    if ((e = launch_scan(sa, SCAN_FWD_STATES, nullptr, s)) != cudaSuccess) return e;
+    const uint8_t* hs = saved ? static_cast<const uint8_t*>(a.states) : ws + w.hs;
+    if (!saved && (e = launch_scan(sa, SCAN_FWD_STATES, nullptr, s)) != cudaSuccess) return e;
     sa.hinit = a.dht;
     sa.hfinal = a.dh0;
     sa.states = ws + w.dhs;
@@ -771,7 +773,7 @@ cudaError_t launch_chunk_bwd(const ChunkBwdArgs& a, cudaStream_t s) {
     ga.beta = a.beta;
     ga.rec = pa.rec;
     ga.rec2 = pa.rec2;
-    ga.hs = ws + w.hs;
+    ga.hs = hs;
     ga.dhs = ws + w.dhs;
     ga.gam = pa.gam;
     ga.dq = a.dq;

@@ -560,7 +560,7 @@ __global__ void __launch_bounds__(192, 1) scan_kernel(const __grid_constant__ CU
             const int c = chunk_of(i), s = i & 1;
             const float gC = gnext;
             if (i + 1 < NC) gnext = gam[chunk_of(i + 1)];
-            if (MODE != SCAN_FWD_OUT) {  // state entering this step, as an SW128 [128 x 128] image
+            if (MODE != SCAN_FWD_OUT || a.states) {  // state entering this step, SW128 [128 x 128] image
                 uint8_t* img = a.states + (bh * NC + c) * (size_t)STATE_IMG;
 #pragma unroll
                 for (int q = 0; q < 4; q++) {
@@ -697,7 +697,7 @@ cudaError_t launch_chunk_fwd(const ChunkFwdArgs& a, cudaStream_t s) {
     sa.hinit = a.h0;
     sa.o = a.o;
     sa.hfinal = a.ht;
-    sa.states = nullptr;
+    sa.states = static_cast<uint8_t*>(a.states);
     sa.status = pa.status;
     sa.ncpad = w.ncpad;
     return launch_scan(sa, SCAN_FWD_OUT, nullptr, s);

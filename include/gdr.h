@@ -107,6 +107,28 @@ gdr_status gdr_bwd_chunked(const gdr_problem* p, const void* q, const void* k, c
                            float* dbeta, float* dh0, void* ws, size_t ws_bytes,
                            gdr_stream_t stream);
 
+/* Saved-state handoff from the forward to the backward. The forward can keep the state
+ * entering every chunk (bf16, opaque layout, gdr_chunk_states_bytes() bytes:
+ * B*Hv*ceil(T/64)*32 KB, caller-owned, 256-byte aligned); the backward then reads them
+ * instead of re-running the forward scan. Chunk-local operators are still recomputed by
+ * the backward. Same support matrix as gdr_fwd_chunked; 0 if the problem is invalid. */
+size_t gdr_chunk_states_bytes(const gdr_problem* p);
+size_t gdr_bwd_chunked_states_workspace(const gdr_problem* p);
+
+/* gdr_fwd_chunked that also writes the chunk-start states into `states`. */
+gdr_status gdr_fwd_chunked_states(const gdr_problem* p, const void* q, const void* k, const void* v,
+                                  const float* g, const float* beta, const float* h0, void* o, float* ht,
+                                  void* states, size_t states_bytes, void* ws, size_t ws_bytes,
+                                  gdr_stream_t stream);
+
+/* gdr_bwd_chunked for the same inputs, reading the chunk-start states written by
+ * gdr_fwd_chunked_states (h0 is then not needed). Workspace:
+ * gdr_bwd_chunked_states_workspace() bytes. */
+gdr_status gdr_bwd_chunked_states(const gdr_problem* p, const void* q, const void* k, const void* v,
+                                  const float* g, const float* beta, const void* states, size_t states_bytes,
+                                  const void* do_, const float* dht, float* dq, float* dk, float* dv, float* dg,
+                                  float* dbeta, float* dh0, void* ws, size_t ws_bytes, gdr_stream_t stream);
+
 /* One decode step (p->T must be 1) on the state in place: per state row, one pass forms
  * the prediction with the decay folded in, a second applies decay plus the rank-one
  * update while accumulating the output, so the state is read once and written once.

@@ -20,7 +20,7 @@ MISALIGNED = ctypes.c_void_p(0x100004)
 @pytest.fixture(scope="module")
 def L():
     gdr.build()
-    return gdr.lib()
+    return gdr.lib()  # the binding declares argtypes for every entry point
 
 
 def declared_functions():
@@ -113,3 +113,22 @@ def test_binding_rejects_cpu_tensors():
     q = torch.zeros(1, 4, 1, 32)
     with pytest.raises(ValueError):
         gdr.fwd_sequential(q, q, torch.zeros(1, 4, 1, 32), torch.zeros(1, 4, 1), torch.zeros(1, 4, 1))
+
+
+def test_saved_state_handoff_validation(L):
+    p = prob()
+    sb = L.gdr_chunk_states_bytes(ctypes.byref(p))
+    wsb = L.gdr_bwd_chunked_states_workspace(ctypes.byref(p))
+    assert sb == 1 * 4 * 1 * 32768  # B * Hv * chunks * one 128 x 128 bf16 image
+    assert 0 < wsb < L.gdr_bwd_chunked_workspace(ctypes.byref(p))
+    need_f = L.gdr_fwd_chunked_workspace(ctypes.byref(p))
+    assert L.gdr_fwd_chunked_states(ctypes.byref(p), *[FAKE] * 8, FAKE, sb - 1, FAKE, need_f, None) == WORKSPACE
+    assert L.gdr_fwd_chunked_states(ctypes.byref(p), *[FAKE] * 8, None, sb, FAKE, need_f, None) == WORKSPACE
+    assert L.gdr_fwd_chunked_states(ctypes.byref(p), *[FAKE] * 8, MISALIGNED, sb, FAKE, need_f, None) == INVALID
+    args = [FAKE] * 5 + [FAKE, sb] + [FAKE] * 8
+    assert L.gdr_bwd_chunked_states(ctypes.byref(p), *args, FAKE, wsb - 1, None) == WORKSPACE
+    args = [FAKE] * 5 + [FAKE, sb - 16] + [FAKE] * 8
+    assert L.gdr_bwd_chunked_states(ctypes.byref(p), *args, FAKE, wsb, None) == WORKSPACE
+    q = prob(dtype=0)
+    assert L.gdr_chunk_states_bytes(ctypes.byref(q)) == 0
+    assert L.gdr_fwd_chunked_states(ctypes.byref(q), *[FAKE] * 8, FAKE, sb, FAKE, need_f, None) == UNSUPPORTED

@@ -126,3 +126,21 @@ def test_backward_empty_sequence():
     x = make_inputs(Shape(1, 0, 1, 2, 128, 128), dtype=torch.bfloat16, seed=1, grads=True)
     gr = gpu_bwd(x, dev)
     assert torch.equal(gr["dh0"].cpu(), x["dht"])
+
+
+@pytest.mark.parametrize("shape", [Shape(1, 300, 2, 4, 128, 128), Shape(2, 129, 1, 2, 128, 128)])
+def test_saved_state_handoff_matches_recompute(shape):
+    """The forward can keep its chunk-start states for the backward: same outputs bit for bit,
+    and the backward that reads them equals the one that re-runs the forward scan bit for bit
+    (and therefore the oracle)."""
+    dev = cuda_device()
+    x = make_inputs(shape, dtype=torch.bfloat16, seed=shape.T, grads=True, gate_scale=0.1)
+    d = to_dev(x, dev)
+    o1, h1 = gdr.fwd_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"])
+    o2, h2, states = gdr.fwd_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], save_states=True)
+    assert torch.equal(o1, o2) and torch.equal(h1, h2)
+    ga = gdr.bwd_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], d["do"], d["dht"])
+    gb = gdr.bwd_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], None, d["do"], d["dht"], states=states)
+    for n in NAMES:
+        assert torch.equal(ga[n], gb[n]), n
+    check(gb, x)

@@ -3,7 +3,10 @@
 
 Headline: the long-context training step (chunked forward + VJP) at B=1, T=32768, Hk=16,
 Hv=32, Dk=Dv=128, bf16 q/k/v with in-kernel L2 norm, fp32 gates/state, h0 = 0, dht = 0,
-do ~ N(0,1): tokens/s = B*T / step time, timed with CUDA events on the launch stream.
+do ~ N(0,1): tokens/s = B*T / step time, timed with CUDA events on the launch stream. The
+forward keeps its chunk-start states (bf16, 32 KiB per chunk and value head) for the
+backward, as a training framework keeps activations; the step that keeps nothing and
+re-runs the forward scan in the backward is timed beside it.
 Inputs (q, k 128 MiB each; v, do 256 MiB each) are larger than the 129 MB L2, so no flush
 is needed between steps. Also reported: the roofline of the dominant kernel (per-kernel
 times from the library's launch trace, recorded on the launch stream), the same step end
@@ -218,19 +221,33 @@ def main():
                dv=torch.empty(d["v"].shape, **f32), dg=torch.empty(d["g"].shape, **f32),
                dbeta=torch.empty(d["beta"].shape, **f32), dh0=torch.empty((B, HV, D, D), **f32))
     nf, nb = gdr.fwd_workspace_bytes(p), gdr.bwd_workspace_bytes(p)
+    nbs, nst = int(L.gdr_bwd_chunked_states_workspace(ctypes.byref(p))), int(L.gdr_chunk_states_bytes(ctypes.byref(p)))
     wsf = torch.empty(nf, dtype=torch.uint8, device=dev)
-    wsb = torch.empty(nb, dtype=torch.uint8, device=dev)
+    wsb = torch.empty(max(nb, nbs), dtype=torch.uint8, device=dev)
+    states = torch.empty(nst, dtype=torch.uint8, device=dev)
     P = lambda t: ctypes.c_void_p(t.data_ptr()) if t is not None else None
     pp = ctypes.byref(p)
 
-    def step(src, dst, stream):
-        rc = L.gdr_fwd_chunked(pp, P(src["q"]), P(src["k"]), P(src["v"]), P(src["g"]), P(src["beta"]), None,
-                               P(dst["o"]), None, P(wsf), nf, stream)
-        rc = rc or L.gdr_bwd_chunked(pp, P(src["q"]), P(src["k"]), P(src["v"]), P(src["g"]), P(src["beta"]),
-                                     None, P(src["do"]), None, P(dst["dq"]), P(dst["dk"]), P(dst["dv"]),
-                                     P(dst["dg"]), P(dst["dbeta"]), P(dst["dh0"]), P(wsb), nb, stream)
+    def raise_on(rc):
         if rc:
             raise gdr.GdrError(rc, L.gdr_status_string(rc).decode())
+
+    def step(src, dst, stream):
+        """One training step: the forward keeps its chunk-start states, the backward reads them."""
+        raise_on(L.gdr_fwd_chunked_states(pp, P(src["q"]), P(src["k"]), P(src["v"]), P(src["g"]), P(src["beta"]),
+                                          None, P(dst["o"]), None, P(states), nst, P(wsf), nf, stream))
+        raise_on(L.gdr_bwd_chunked_states(pp, P(src["q"]), P(src["k"]), P(src["v"]), P(src["g"]), P(src["beta"]),
+                                          P(states), nst, P(src["do"]), None, P(dst["dq"]), P(dst["dk"]),
+                                          P(dst["dv"]), P(dst["dg"]), P(dst["dbeta"]), P(dst["dh0"]), P(wsb), nbs,
+                                          stream))
+
+    def step_recompute(src, dst, stream):
+        """The same step with nothing kept: the backward re-runs the forward states scan."""
+        raise_on(L.gdr_fwd_chunked(pp, P(src["q"]), P(src["k"]), P(src["v"]), P(src["g"]), P(src["beta"]), None,
+                                   P(dst["o"]), None, P(wsf), nf, stream))
+        raise_on(L.gdr_bwd_chunked(pp, P(src["q"]), P(src["k"]), P(src["v"]), P(src["g"]), P(src["beta"]), None,
+                                   P(src["do"]), None, P(dst["dq"]), P(dst["dk"]), P(dst["dv"]), P(dst["dg"]),
+                                   P(dst["dbeta"]), P(dst["dh0"]), P(wsb), nb, stream))
 
     stream = torch.cuda.current_stream(dev)
     sp = ctypes.c_void_p(stream.cuda_stream)
@@ -262,6 +279,17 @@ def main():
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
     value = world * B * T / (ms / 1e3)
+
+    # the full-recompute variant of the same step (context, not the headline)
+    for _ in range(2):
+        step_recompute(d, out, sp)
+    barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step_recompute(d, out, sp)
+    e1.record(stream)
+    barrier()
+    ms_rc = e0.elapsed_time(e1) / args.steps
 
     # ------------------------------------------------------------------ per-kernel times (launch trace)
     nt = min(args.steps, 10)
@@ -336,10 +364,8 @@ def main():
         flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
 
         def dstep(i):
-            rc = L.gdr_decode_step(ctypes.byref(pd), P(dd["q"][i]), P(dd["k"][i]), P(dd["v"][i]), P(dd["g"][i]),
-                                   P(dd["beta"][i]), P(st), P(od), sp)
-            if rc:
-                raise gdr.GdrError(rc, L.gdr_status_string(rc).decode())
+            raise_on(L.gdr_decode_step(ctypes.byref(pd), P(dd["q"][i]), P(dd["k"][i]), P(dd["v"][i]),
+                                       P(dd["g"][i]), P(dd["beta"][i]), P(st), P(od), sp))
 
         for i in range(4):
             dstep(i)
@@ -387,6 +413,8 @@ def main():
             "roofline": roof,
             "step_roofline": {"t_star_ms": t_star * 1e3, "frac": t_star * 1e3 / ms,
                               "note": "whole step vs max(flops/peak, bytes/peak) of the algorithm"},
+            "step_recompute": {"ms_per_step": ms_rc, "tokens_per_s": world * B * T / (ms_rc / 1e3),
+                               "note": "forward keeps no states; backward re-runs the forward states scan"},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(round(launches_per_step * args.steps)),
             "clocks": clocks, "kernels": kern, "decode": dec,
         }

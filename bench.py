@@ -11,7 +11,8 @@ Inputs (q, k 128 MiB each; v, do 256 MiB each) are larger than the 129 MB L2, so
 is needed between steps. Also reported: the roofline of the dominant kernel (per-kernel
 times from the library's launch trace, recorded on the launch stream), the same step end
 to end with pinned-host inputs/outputs copied inside the timed region, the decode step's
-state bandwidth (B=32, channel gate, fp32, L2 flushed before every step), SM clocks
+state bandwidth (B=32, channel gate, fp32, L2 flushed before every step), the short-prefill
+crossover of the sequential and chunked forwards (T = 1..256 continuing a B=32 state), SM clocks
 sampled during the timed region, and the fp64 CPU oracle timed on a bounded sample.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mine|reference]
@@ -34,6 +35,7 @@ sys.path.insert(0, ROOT)
 METRIC = "GDR fwd+bwd tokens/s at Hv=32,D=128 (% roofline); decode state GB/s vs HBM peak"
 B, T, HK, HV, D, C = 1, 32768, 16, 32, 128, 64
 UNITS = B * T * HV  # token x value-head units per step
+PREFILL_T = (1, 2, 4, 8, 16, 32, 64, 128, 256)  # short prefills continuing a B=32 decode state
 
 # Algorithmic work per (token x value head), D=128, C=64, as the kernels do it:
 # bytes = the user-visible tensors each kernel must read or write (no workspace);
@@ -186,6 +188,7 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the short-prefill crossover table")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     set_tokens(args.tokens)
@@ -395,6 +398,44 @@ def main():
                "us_per_step_back_to_back": us_warm}
         del flush
 
+    # ------------------------------------------------------------------ short prefill: sequential vs chunked
+    pre = None
+    if not args.no_prefill:
+        from gated_delta_rule_31_gb300.synth import Shape
+
+        flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+        rows = []
+        for Tp in PREFILL_T:
+            xs = make_inputs(Shape(32, Tp, 16, 32, D, D), dtype=torch.bfloat16, seed=1003, gate="scalar")
+            ds = {k: v.to(dev) for k, v in xs.items() if v is not None}
+            ps = gdr.Problem(32, Tp, 16, 32, D, D, gdr.GDR_BF16, gdr.GDR_GATE_SCALAR, D ** -0.5, 1)
+            os_ = torch.empty(ds["v"].shape, dtype=torch.bfloat16, device=dev)
+            hts = torch.empty(ds["h0"].shape, **f32)
+            nws = gdr.fwd_workspace_bytes(ps)
+            wss = torch.empty(nws, dtype=torch.uint8, device=dev)
+            args_in = [P(ds[n]) for n in ("q", "k", "v", "g", "beta", "h0")] + [P(os_), P(hts)]
+            calls = {"sequential": lambda: raise_on(L.gdr_fwd_sequential(ctypes.byref(ps), *args_in, sp)),
+                     "chunked": lambda: raise_on(L.gdr_fwd_chunked(ctypes.byref(ps), *args_in, P(wss), nws, sp))}
+            row = {"T": Tp}
+            for name, fn in calls.items():
+                for _ in range(3):
+                    fn()
+                reps = 10
+                ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+                for a_, b_ in ev:
+                    flush.fill_(1)
+                    a_.record(stream)
+                    fn()
+                    b_.record(stream)
+                torch.cuda.synchronize(dev)
+                row[name + "_us"] = 1e3 * statistics.median(a_.elapsed_time(b_) for a_, b_ in ev)
+            rows.append(row)
+            del ds, os_, hts, wss
+        cross = next((r["T"] for r in rows if r["chunked_us"] < r["sequential_us"]), None)
+        pre = {"config": "B=32, Hk=16, Hv=32, Dk=Dv=128, bf16, scalar gate, h0 ~ N(0,0.02), L2 flushed, median of 10",
+               "rows": rows, "chunked_faster_from_T": cross}
+        del flush
+
     # ------------------------------------------------------------------ CPU baseline (rank 0, N=1)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -416,7 +457,7 @@ def main():
             "step_recompute": {"ms_per_step": ms_rc, "tokens_per_s": world * B * T / (ms_rc / 1e3),
                                "note": "forward keeps no states; backward re-runs the forward states scan"},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(round(launches_per_step * args.steps)),
-            "clocks": clocks, "kernels": kern, "decode": dec,
+            "clocks": clocks, "kernels": kern, "decode": dec, "short_prefill": pre,
         }
         print(json.dumps(line))
     if world > 1:

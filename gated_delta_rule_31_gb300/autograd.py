@@ -1,0 +1,58 @@
+"""torch.autograd integration of the chunked gated delta rule.
+
+``gated_delta_rule(q, k, v, g, beta, h0=None, scale=None, use_qk_l2norm=True)`` returns
+``(o, ht)`` and is differentiable in q, k, v, g, beta and h0. Its forward runs
+``gdr_fwd_chunked_states`` when any input needs a gradient (the chunk-start states are
+kept for the backward, 32 KB per chunk and value head) and ``gdr_fwd_chunked`` otherwise;
+its backward runs ``gdr_bwd_chunked_states``. With ``use_qk_l2norm`` the kernels own the
+q/k L2 normalisation (eps 1e-6), so no normalised copy of q or k is ever materialised or
+kept for the backward — the point of "fold q/k L2-norm into the gated_delta_rule kernel"
+(Megatron-LM PR #5396, "What" / "Why"). The VJP is the chunked backward of "Adding VJP for
+gated delta net" (MLX PR #4565).
+
+Supported as the chunked kernels are: bf16 q/k/v, Dk = Dv = 128, scalar gate g [B,T,Hv];
+other problems raise ``GdrError`` (GDR_ERR_UNSUPPORTED). The only torch operations here
+are argument marshalling: a zero ``do`` when the output is unused, contiguity, and casting
+the fp32 gradients of q/k/v to their bf16 dtype.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import bwd_chunked, fwd_chunked
+
+__all__ = ["gated_delta_rule", "GatedDeltaRuleFunction"]
+
+
+class GatedDeltaRuleFunction(torch.autograd.Function):
+    @staticmethod
+    def forward(ctx, q, k, v, g, beta, h0, scale, use_qk_l2norm):
+        ctx.scale, ctx.norm, ctx.has_h0 = scale, bool(use_qk_l2norm), h0 is not None
+        if any(ctx.needs_input_grad[:6]):
+            o, ht, states = fwd_chunked(q, k, v, g, beta, h0, scale=scale, use_qk_l2norm=use_qk_l2norm,
+                                        save_states=True)
+            ctx.save_for_backward(q, k, v, g, beta, states)
+        else:
+            o, ht = fwd_chunked(q, k, v, g, beta, h0, scale=scale, use_qk_l2norm=use_qk_l2norm)
+        return o, ht
+
+    @staticmethod
+    @torch.autograd.function.once_differentiable
+    def backward(ctx, do, dht):
+        q, k, v, g, beta, states = ctx.saved_tensors
+        do = torch.zeros_like(v) if do is None else do.to(v.dtype).contiguous()
+        dht = None if dht is None else dht.to(torch.float32).contiguous()
+        gr = bwd_chunked(q, k, v, g, beta, None, do, dht, scale=ctx.scale, use_qk_l2norm=ctx.norm,
+                         states=states)
+        return (gr["dq"].to(q.dtype), gr["dk"].to(k.dtype), gr["dv"].to(v.dtype), gr["dg"], gr["dbeta"],
+                gr["dh0"] if ctx.has_h0 else None, None, None)
+
+
+def gated_delta_rule(q, k, v, g, beta, h0=None, scale=None, use_qk_l2norm=True):
+    """Differentiable chunked gated delta rule: (o [B,T,Hv,Dv] bf16, ht [B,Hv,Dv,Dk] fp32).
+
+    q, k [B,T,Hk,Dk] bf16; v [B,T,Hv,Dv] bf16; g [B,T,Hv] fp32 log-decay; beta [B,T,Hv]
+    fp32; h0 [B,Hv,Dv,Dk] fp32 or None (zero). scale defaults to Dk^-1/2."""
+    if scale is None:
+        scale = q.shape[-1] ** -0.5
+    return GatedDeltaRuleFunction.apply(q, k, v, g, beta, h0, float(scale), bool(use_qk_l2norm))

@@ -132,3 +132,13 @@ def test_saved_state_handoff_validation(L):
     q = prob(dtype=0)
     assert L.gdr_chunk_states_bytes(ctypes.byref(q)) == 0
     assert L.gdr_fwd_chunked_states(ctypes.byref(q), *[FAKE] * 8, FAKE, sb, FAKE, need_f, None) == UNSUPPORTED
+
+
+def test_autograd_function_has_no_cpu_path():
+    from gated_delta_rule_31_gb300.autograd import gated_delta_rule
+
+    q = torch.randn(1, 8, 1, 128, dtype=torch.bfloat16, requires_grad=True)
+    v = torch.randn(1, 8, 2, 128, dtype=torch.bfloat16, requires_grad=True)
+    g, beta = torch.zeros(1, 8, 2), torch.full((1, 8, 2), 0.5)
+    with pytest.raises(ValueError, match="CUDA"):
+        gated_delta_rule(q, q, v, g, beta)

@@ -173,3 +173,34 @@ def test_chunked_empty_sequence():
     d = to_dev(x, dev)
     o, ht = gdr.fwd_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"])
     assert o.shape == (1, 0, 2, 128) and torch.equal(ht.cpu(), x["h0"])
+
+
+# ------------------------------------------------------------------ short prefill (multi-token decode)
+SHORT_T = [2, 4, 16, 64]
+
+
+@pytest.mark.parametrize("T", SHORT_T)
+def test_short_prefill_at_decode_sizes(T):
+    """Representative short prefills continuing a decode state (B=32, Hk=16, Hv=32, D=128,
+    h0 ~ N(0,0.02)): the sequential kernel (channel gate, fp32 and scalar gate, bf16) and the
+    chunked kernel (bf16, scalar gate), checked on two sampled (batch, key head) groups."""
+    dev = cuda_device()
+    shape = Shape(32, T, 16, 32, 128, 128)
+
+    def sliced(x, b, hk):
+        return {n: (None if t is None else t[b:b + 1, :, hk:hk + 1] if n in ("q", "k") else
+                    t[b:b + 1, hk * 2:(hk + 1) * 2] if n == "h0" else t[b:b + 1, :, hk * 2:(hk + 1) * 2])
+                for n, t in x.items()}
+
+    for dtype, gate, paths in ((torch.float32, "channel", ("seq",)), (torch.bfloat16, "scalar", ("seq", "chunk"))):
+        x = make_inputs(shape, dtype=dtype, seed=1003 + T, gate=gate)
+        d = to_dev(x, dev)
+        tol = F32_TOL if dtype == torch.float32 else BF16_TOL
+        for path in paths:
+            fn = gdr.fwd_sequential if path == "seq" else gdr.fwd_chunked
+            o, ht = fn(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"])
+            o, ht = o.cpu(), ht.cpu()
+            for b, hk in ((0, 0), (31, 15)):
+                ro, rht = run_oracle(sliced(x, b, hk))
+                assert rel_err(o[b:b + 1, :, 2 * hk:2 * hk + 2], ro) <= tol, (path, dtype, b, hk)
+                assert rel_err(ht[b:b + 1, 2 * hk:2 * hk + 2], rht) <= tol, (path, dtype, b, hk)

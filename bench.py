@@ -244,6 +244,19 @@ def main():
                                           P(dst["dv"]), P(dst["dg"]), P(dst["dbeta"]), P(dst["dh0"]), P(wsb), nbs,
                                           stream))
 
+    nsv = int(L.gdr_chunk_saved_bytes(ctypes.byref(p)))
+    nbsv = int(L.gdr_bwd_chunked_saved_workspace(ctypes.byref(p)))
+
+    def step_saved(src, dst, stream, saved, wsv):
+        """Optional variant: the forward keeps its chunk operators too and the backward skips prep
+        (not the headline: the chunk-local terms are stored instead of recomputed)."""
+        raise_on(L.gdr_fwd_chunked_saved(pp, P(src["q"]), P(src["k"]), P(src["v"]), P(src["g"]), P(src["beta"]),
+                                         None, P(dst["o"]), None, P(saved), nsv, P(wsf), 256, stream))
+        raise_on(L.gdr_bwd_chunked_saved(pp, P(src["q"]), P(src["k"]), P(src["v"]), P(src["g"]), P(src["beta"]),
+                                         P(saved), nsv, P(src["do"]), None, P(dst["dq"]), P(dst["dk"]),
+                                         P(dst["dv"]), P(dst["dg"]), P(dst["dbeta"]), P(dst["dh0"]), P(wsv), nbsv,
+                                         stream))
+
     def step_recompute(src, dst, stream):
         """The same step with nothing kept: the backward re-runs the forward states scan."""
         raise_on(L.gdr_fwd_chunked(pp, P(src["q"]), P(src["k"]), P(src["v"]), P(src["g"]), P(src["beta"]), None,
@@ -293,6 +306,20 @@ def main():
     e1.record(stream)
     barrier()
     ms_rc = e0.elapsed_time(e1) / args.steps
+
+    # the saved-operator variant (context: 2.4 GB kept between forward and backward at T=32768)
+    saved_buf = torch.empty(nsv, dtype=torch.uint8, device=dev)
+    wsv = torch.empty(nbsv, dtype=torch.uint8, device=dev)
+    for _ in range(2):
+        step_saved(d, out, sp, saved_buf, wsv)
+    barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step_saved(d, out, sp, saved_buf, wsv)
+    e1.record(stream)
+    barrier()
+    ms_sv = e0.elapsed_time(e1) / args.steps
+    del saved_buf, wsv
 
     # ------------------------------------------------------------------ per-kernel times (launch trace)
     nt = min(args.steps, 10)
@@ -456,6 +483,10 @@ def main():
                               "note": "whole step vs max(flops/peak, bytes/peak) of the algorithm"},
             "step_recompute": {"ms_per_step": ms_rc, "tokens_per_s": world * B * T / (ms_rc / 1e3),
                                "note": "forward keeps no states; backward re-runs the forward states scan"},
+            "step_saved_operators": {"ms_per_step": ms_sv, "tokens_per_s": world * B * T / (ms_sv / 1e3),
+                                     "saved_bytes": nsv,
+                                     "note": "optional: forward also keeps the chunk operators, backward runs no "
+                                             "prep (chunk-local terms stored, not recomputed)"},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(round(launches_per_step * args.steps)),
             "clocks": clocks, "kernels": kern, "decode": dec, "short_prefill": pre,
         }

@@ -73,6 +73,13 @@ def lib():
         L.gdr_fwd_chunked_states.restype = ctypes.c_int
         L.gdr_bwd_chunked_states.argtypes = [PP] + [P] * 5 + [P, sz] + [P] * 8 + [P, sz, st]
         L.gdr_bwd_chunked_states.restype = ctypes.c_int
+        for name in ("gdr_chunk_saved_bytes", "gdr_fwd_chunked_saved_workspace", "gdr_bwd_chunked_saved_workspace"):
+            getattr(L, name).argtypes = [PP]
+            getattr(L, name).restype = sz
+        L.gdr_fwd_chunked_saved.argtypes = [PP] + [P] * 8 + [P, sz, P, sz, st]
+        L.gdr_fwd_chunked_saved.restype = ctypes.c_int
+        L.gdr_bwd_chunked_saved.argtypes = [PP] + [P] * 5 + [P, sz] + [P] * 8 + [P, sz, st]
+        L.gdr_bwd_chunked_saved.restype = ctypes.c_int
         L.gdr_workspace_status.argtypes = [P, sz, st]
         L.gdr_workspace_status.restype = ctypes.c_int
         L.gdr_trace_enable.argtypes = [ctypes.c_int]
@@ -177,14 +184,27 @@ def fwd_sequential(q, k, v, g, beta, h0=None, scale=None, use_qk_l2norm=True, ou
 
 
 def fwd_chunked(q, k, v, g, beta, h0=None, scale=None, use_qk_l2norm=True, output_final_state=True,
-                workspace=None, save_states=False):
+                workspace=None, save_states=False, save_all=False):
     """Chunked prefill forward on the tensor cores (gdr_fwd_chunked). Returns (o, ht or None),
     or (o, ht, states) with save_states=True (gdr_fwd_chunked_states: the chunk-start states
-    kept for bwd_chunked(..., states=states))."""
+    kept for bwd_chunked(..., states=states)), or (o, ht, saved) with save_all=True
+    (gdr_fwd_chunked_saved: states and chunk operators kept for bwd_chunked(..., saved=saved))."""
     _check_inputs(q, k, v, g, beta, h0)
     p = _problem(q, v, g, scale, use_qk_l2norm)
     o = torch.empty(v.shape, dtype=v.dtype, device=v.device)
     ht = torch.empty((p.B, p.Hv, p.Dv, p.Dk), dtype=torch.float32, device=v.device) if output_final_state else None
+    if save_all:
+        L = lib()
+        nbytes = int(L.gdr_fwd_chunked_saved_workspace(ctypes.byref(p)))
+        if nbytes == 0:
+            _check(2)
+        ws = _workspace(nbytes, q.device, workspace)
+        sb = int(L.gdr_chunk_saved_bytes(ctypes.byref(p)))
+        saved = torch.empty(max(sb, 256), dtype=torch.uint8, device=q.device)
+        _check(L.gdr_fwd_chunked_saved(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
+                                       _ptr(o), _ptr(ht), _ptr(saved), ctypes.c_size_t(sb), _ptr(ws),
+                                       ctypes.c_size_t(nbytes), _stream(q.device)))
+        return o, ht, saved
     nbytes = fwd_workspace_bytes(p)
     if nbytes == 0:
         _check(2)  # unsupported combination
@@ -202,11 +222,12 @@ def fwd_chunked(q, k, v, g, beta, h0=None, scale=None, use_qk_l2norm=True, outpu
 
 
 def bwd_chunked(q, k, v, g, beta, h0, do, dht=None, scale=None, use_qk_l2norm=True, workspace=None,
-                states=None):
+                states=None, saved=None):
     """Chunked backward (gdr_bwd_chunked) of <do,o> + <dht,ht>. Returns a dict of fp32
     gradients dq, dk, dv, dg, dbeta, dh0. With `states` from fwd_chunked(save_states=True)
     on the same inputs, gdr_bwd_chunked_states reads them instead of re-running the
-    forward scan (h0 is then unused)."""
+    forward scan; with `saved` from fwd_chunked(save_all=True), gdr_bwd_chunked_saved runs
+    neither prep nor the forward scan (h0 is unused in both cases)."""
     _check_inputs(q, k, v, g, beta, h0)
     _need(do, "do", dtype=v.dtype, device=v.device, shape=v.shape)
     p = _problem(q, v, g, scale, use_qk_l2norm)
@@ -216,6 +237,19 @@ def bwd_chunked(q, k, v, g, beta, h0, do, dht=None, scale=None, use_qk_l2norm=Tr
     out = dict(dq=torch.empty(q.shape, **f32), dk=torch.empty(k.shape, **f32), dv=torch.empty(v.shape, **f32),
                dg=torch.empty(g.shape, **f32), dbeta=torch.empty(beta.shape, **f32),
                dh0=torch.empty((p.B, p.Hv, p.Dv, p.Dk), **f32))
+    if saved is not None:
+        _need(saved, "saved", dtype=torch.uint8, device=q.device)
+        L = lib()
+        nbytes = int(L.gdr_bwd_chunked_saved_workspace(ctypes.byref(p)))
+        if nbytes == 0:
+            _check(2)
+        ws = _workspace(nbytes, q.device, workspace)
+        _check(L.gdr_bwd_chunked_saved(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                       _ptr(saved), ctypes.c_size_t(saved.numel()), _ptr(do), _ptr(dht),
+                                       _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dg"]),
+                                       _ptr(out["dbeta"]), _ptr(out["dh0"]), _ptr(ws), ctypes.c_size_t(nbytes),
+                                       _stream(q.device)))
+        return out
     if states is None:
         nbytes = bwd_workspace_bytes(p)
         if nbytes == 0:

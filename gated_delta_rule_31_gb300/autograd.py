@@ -3,8 +3,9 @@
 ``gated_delta_rule(q, k, v, g, beta, h0=None, scale=None, use_qk_l2norm=True)`` returns
 ``(o, ht)`` and is differentiable in q, k, v, g, beta and h0. Its forward runs
 ``gdr_fwd_chunked_states`` when any input needs a gradient (the chunk-start states are
-kept for the backward, 32 KB per chunk and value head) and ``gdr_fwd_chunked`` otherwise;
-its backward runs ``gdr_bwd_chunked_states``. With ``use_qk_l2norm`` the kernels own the
+kept for the backward, 32 KB per chunk and value head; ``gdr_fwd_chunked_saved`` with
+``keep_operators=True``) and ``gdr_fwd_chunked`` otherwise; its backward runs the matching
+``gdr_bwd_chunked_states`` / ``gdr_bwd_chunked_saved``. With ``use_qk_l2norm`` the kernels own the
 q/k L2 normalisation (eps 1e-6), so no normalised copy of q or k is ever materialised or
 kept for the backward — the point of "fold q/k L2-norm into the gated_delta_rule kernel"
 (Megatron-LM PR #5396, "What" / "Why"). The VJP is the chunked backward of "Adding VJP for
@@ -26,12 +27,13 @@ __all__ = ["gated_delta_rule", "GatedDeltaRuleFunction"]
 
 class GatedDeltaRuleFunction(torch.autograd.Function):
     @staticmethod
-    def forward(ctx, q, k, v, g, beta, h0, scale, use_qk_l2norm):
+    def forward(ctx, q, k, v, g, beta, h0, scale, use_qk_l2norm, keep_operators):
         ctx.scale, ctx.norm, ctx.has_h0 = scale, bool(use_qk_l2norm), h0 is not None
+        ctx.keep_operators = bool(keep_operators)
         if any(ctx.needs_input_grad[:6]):
-            o, ht, states = fwd_chunked(q, k, v, g, beta, h0, scale=scale, use_qk_l2norm=use_qk_l2norm,
-                                        save_states=True)
-            ctx.save_for_backward(q, k, v, g, beta, states)
+            o, ht, kept = fwd_chunked(q, k, v, g, beta, h0, scale=scale, use_qk_l2norm=use_qk_l2norm,
+                                      save_states=not keep_operators, save_all=keep_operators)
+            ctx.save_for_backward(q, k, v, g, beta, kept)
         else:
             o, ht = fwd_chunked(q, k, v, g, beta, h0, scale=scale, use_qk_l2norm=use_qk_l2norm)
         return o, ht
@@ -39,20 +41,24 @@ class GatedDeltaRuleFunction(torch.autograd.Function):
     @staticmethod
     @torch.autograd.function.once_differentiable
     def backward(ctx, do, dht):
-        q, k, v, g, beta, states = ctx.saved_tensors
+        q, k, v, g, beta, kept = ctx.saved_tensors
         do = torch.zeros_like(v) if do is None else do.to(v.dtype).contiguous()
         dht = None if dht is None else dht.to(torch.float32).contiguous()
-        gr = bwd_chunked(q, k, v, g, beta, None, do, dht, scale=ctx.scale, use_qk_l2norm=ctx.norm,
-                         states=states)
+        handoff = {"saved": kept} if ctx.keep_operators else {"states": kept}
+        gr = bwd_chunked(q, k, v, g, beta, None, do, dht, scale=ctx.scale, use_qk_l2norm=ctx.norm, **handoff)
         return (gr["dq"].to(q.dtype), gr["dk"].to(k.dtype), gr["dv"].to(v.dtype), gr["dg"], gr["dbeta"],
-                gr["dh0"] if ctx.has_h0 else None, None, None)
+                gr["dh0"] if ctx.has_h0 else None, None, None, None)
 
 
-def gated_delta_rule(q, k, v, g, beta, h0=None, scale=None, use_qk_l2norm=True):
+def gated_delta_rule(q, k, v, g, beta, h0=None, scale=None, use_qk_l2norm=True, keep_operators=False):
     """Differentiable chunked gated delta rule: (o [B,T,Hv,Dv] bf16, ht [B,Hv,Dv,Dk] fp32).
 
     q, k [B,T,Hk,Dk] bf16; v [B,T,Hv,Dv] bf16; g [B,T,Hv] fp32 log-decay; beta [B,T,Hv]
-    fp32; h0 [B,Hv,Dv,Dk] fp32 or None (zero). scale defaults to Dk^-1/2."""
+    fp32; h0 [B,Hv,Dv,Dk] fp32 or None (zero). scale defaults to Dk^-1/2. The forward keeps
+    the chunk-start states (32 KB per chunk and value head) for the backward; with
+    keep_operators=True it keeps the chunk operators too (144 KB per chunk and value head)
+    and the backward then skips all recomputation. Both give bitwise the same results."""
     if scale is None:
         scale = q.shape[-1] ** -0.5
-    return GatedDeltaRuleFunction.apply(q, k, v, g, beta, h0, float(scale), bool(use_qk_l2norm))
+    return GatedDeltaRuleFunction.apply(q, k, v, g, beta, h0, float(scale), bool(use_qk_l2norm),
+                                        bool(keep_operators))

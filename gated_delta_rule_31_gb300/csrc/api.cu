@@ -189,7 +189,7 @@ size_t gdr_bwd_chunked_states_workspace(const gdr_problem* p) {
 
 static gdr_status fwd_chunked_impl(const gdr_problem* p, const void* q, const void* k, const void* v,
                                    const float* g, const float* beta, const float* h0, void* o, float* ht,
-                                   void* states, void* ws, size_t ws_bytes, gdr_stream_t stream);
+                                   void* states, void* saved, void* ws, size_t ws_bytes, gdr_stream_t stream);
 
 gdr_status gdr_fwd_chunked_states(const gdr_problem* p, const void* q, const void* k, const void* v,
                                   const float* g, const float* beta, const float* h0, void* o, float* ht,
@@ -201,23 +201,50 @@ gdr_status gdr_fwd_chunked_states(const gdr_problem* p, const void* q, const voi
     const size_t need = chunk_states_bytes(chunk_problem(p));
     if (need && (!states || states_bytes < need)) return GDR_ERR_WORKSPACE;
     if (states && (reinterpret_cast<uintptr_t>(states) & 255u) != 0) return GDR_ERR_INVALID_ARG;
-    return fwd_chunked_impl(p, q, k, v, g, beta, h0, o, ht, states, ws, ws_bytes, stream);
+    return fwd_chunked_impl(p, q, k, v, g, beta, h0, o, ht, states, nullptr, ws, ws_bytes, stream);
 }
 
 gdr_status gdr_fwd_chunked(const gdr_problem* p, const void* q, const void* k, const void* v, const float* g,
                            const float* beta, const float* h0, void* o, float* ht, void* ws, size_t ws_bytes,
                            gdr_stream_t stream) {
-    return fwd_chunked_impl(p, q, k, v, g, beta, h0, o, ht, nullptr, ws, ws_bytes, stream);
+    return fwd_chunked_impl(p, q, k, v, g, beta, h0, o, ht, nullptr, nullptr, ws, ws_bytes, stream);
+}
+
+size_t gdr_chunk_saved_bytes(const gdr_problem* p) {
+    if (check_problem(p, false) != GDR_OK || check_chunked_support(p) != GDR_OK) return 0;
+    return chunk_saved_bytes(chunk_problem(p));
+}
+
+size_t gdr_fwd_chunked_saved_workspace(const gdr_problem* p) {
+    if (check_problem(p, false) != GDR_OK || check_chunked_support(p) != GDR_OK) return 0;
+    return kSavedFwdWorkspace;
+}
+
+size_t gdr_bwd_chunked_saved_workspace(const gdr_problem* p) {
+    if (check_problem(p, false) != GDR_OK || check_chunked_support(p) != GDR_OK) return 0;
+    return chunk_bwd_saved_workspace(chunk_problem(p));
+}
+
+gdr_status gdr_fwd_chunked_saved(const gdr_problem* p, const void* q, const void* k, const void* v,
+                                 const float* g, const float* beta, const float* h0, void* o, float* ht,
+                                 void* saved, size_t saved_bytes, void* ws, size_t ws_bytes, gdr_stream_t stream) {
+    gdr_status s = check_problem(p, false);
+    if (s != GDR_OK) return s;
+    if ((s = check_chunked_support(p)) != GDR_OK) return s;
+    const size_t need = chunk_saved_bytes(chunk_problem(p));
+    if (need && (!saved || saved_bytes < need)) return GDR_ERR_WORKSPACE;
+    if (saved && (reinterpret_cast<uintptr_t>(saved) & 255u) != 0) return GDR_ERR_INVALID_ARG;
+    return fwd_chunked_impl(p, q, k, v, g, beta, h0, o, ht, nullptr, saved, ws, ws_bytes, stream);
 }
 
 static gdr_status fwd_chunked_impl(const gdr_problem* p, const void* q, const void* k, const void* v,
                                    const float* g, const float* beta, const float* h0, void* o, float* ht,
-                                   void* states, void* ws, size_t ws_bytes, gdr_stream_t stream) {
+                                   void* states, void* saved, void* ws, size_t ws_bytes, gdr_stream_t stream) {
     gdr_status s = check_problem(p, false);
     if (s != GDR_OK) return s;
     if ((s = check_ptrs(p, {q, k, v, g, beta, o}, {h0, ht})) != GDR_OK) return s;
     if ((s = check_chunked_support(p)) != GDR_OK) return s;
-    const size_t need = chunk_fwd_workspace(chunk_problem(p));
+    const size_t need = saved ? kSavedFwdWorkspace : chunk_fwd_workspace(chunk_problem(p));
     if (!ws || ws_bytes < need) return GDR_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return GDR_ERR_INVALID_ARG;
     if (p->B == 0) return GDR_OK;
@@ -232,21 +259,23 @@ static gdr_status fwd_chunked_impl(const gdr_problem* p, const void* q, const vo
     a.p = chunk_problem(p);
     a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.h0 = h0; a.o = o; a.ht = ht;
     a.states = states;
+    a.saved = saved;
     a.ws = ws;
     return launch_chunk_fwd(a, st) == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
 }
 
 static gdr_status bwd_chunked_impl(const gdr_problem* p, const void* q, const void* k, const void* v,
                                    const float* g, const float* beta, const float* h0, const void* states,
-                                   const void* do_, const float* dht, float* dq, float* dk, float* dv, float* dg,
-                                   float* dbeta, float* dh0, void* ws, size_t ws_bytes, gdr_stream_t stream);
+                                   const void* saved, const void* do_, const float* dht, float* dq, float* dk,
+                                   float* dv, float* dg, float* dbeta, float* dh0, void* ws, size_t ws_bytes,
+                                   gdr_stream_t stream);
 
 gdr_status gdr_bwd_chunked(const gdr_problem* p, const void* q, const void* k, const void* v, const float* g,
                            const float* beta, const float* h0, const void* do_, const float* dht, float* dq,
                            float* dk, float* dv, float* dg, float* dbeta, float* dh0, void* ws, size_t ws_bytes,
                            gdr_stream_t stream) {
-    return bwd_chunked_impl(p, q, k, v, g, beta, h0, nullptr, do_, dht, dq, dk, dv, dg, dbeta, dh0, ws, ws_bytes,
-                            stream);
+    return bwd_chunked_impl(p, q, k, v, g, beta, h0, nullptr, nullptr, do_, dht, dq, dk, dv, dg, dbeta, dh0, ws,
+                            ws_bytes, stream);
 }
 
 gdr_status gdr_bwd_chunked_states(const gdr_problem* p, const void* q, const void* k, const void* v,
@@ -259,20 +288,37 @@ gdr_status gdr_bwd_chunked_states(const gdr_problem* p, const void* q, const voi
     const size_t need = chunk_states_bytes(chunk_problem(p));
     if (need && (!states || states_bytes < need)) return GDR_ERR_WORKSPACE;
     if (states && (reinterpret_cast<uintptr_t>(states) & 255u) != 0) return GDR_ERR_INVALID_ARG;
-    return bwd_chunked_impl(p, q, k, v, g, beta, nullptr, states, do_, dht, dq, dk, dv, dg, dbeta,
+    return bwd_chunked_impl(p, q, k, v, g, beta, nullptr, states, nullptr, do_, dht, dq, dk, dv, dg, dbeta,
                             dh0, ws, ws_bytes, stream);
+}
+
+gdr_status gdr_bwd_chunked_saved(const gdr_problem* p, const void* q, const void* k, const void* v,
+                                 const float* g, const float* beta, const void* saved, size_t saved_bytes,
+                                 const void* do_, const float* dht, float* dq, float* dk, float* dv, float* dg,
+                                 float* dbeta, float* dh0, void* ws, size_t ws_bytes, gdr_stream_t stream) {
+    gdr_status s = check_problem(p, false);
+    if (s != GDR_OK) return s;
+    if ((s = check_chunked_support(p)) != GDR_OK) return s;
+    const size_t need = chunk_saved_bytes(chunk_problem(p));
+    if (need && (!saved || saved_bytes < need)) return GDR_ERR_WORKSPACE;
+    if (saved && (reinterpret_cast<uintptr_t>(saved) & 255u) != 0) return GDR_ERR_INVALID_ARG;
+    return bwd_chunked_impl(p, q, k, v, g, beta, nullptr, nullptr, saved, do_, dht, dq, dk, dv, dg, dbeta, dh0,
+                            ws, ws_bytes, stream);
 }
 
 static gdr_status bwd_chunked_impl(const gdr_problem* p, const void* q, const void* k, const void* v,
                                    const float* g, const float* beta, const float* h0, const void* states,
-                                   const void* do_, const float* dht, float* dq, float* dk, float* dv, float* dg,
-                                   float* dbeta, float* dh0, void* ws, size_t ws_bytes, gdr_stream_t stream) {
+                                   const void* saved, const void* do_, const float* dht, float* dq, float* dk,
+                                   float* dv, float* dg, float* dbeta, float* dh0, void* ws, size_t ws_bytes,
+                                   gdr_stream_t stream) {
     gdr_status s = check_problem(p, false);
     if (s != GDR_OK) return s;
     if ((s = check_ptrs(p, {q, k, v, g, beta, do_, dq, dk, dv, dg, dbeta}, {h0, dht, dh0})) != GDR_OK) return s;
     if ((s = check_chunked_support(p)) != GDR_OK) return s;
     const ChunkProblem cp = chunk_problem(p);
-    const size_t need = states ? chunk_bwd_states_workspace(cp) : chunk_bwd_workspace(cp);
+    const size_t need = saved    ? chunk_bwd_saved_workspace(cp)
+                        : states ? chunk_bwd_states_workspace(cp)
+                                 : chunk_bwd_workspace(cp);
     if (!ws || ws_bytes < need) return GDR_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return GDR_ERR_INVALID_ARG;
     if (p->B == 0) return GDR_OK;
@@ -290,6 +336,7 @@ static gdr_status bwd_chunked_impl(const gdr_problem* p, const void* q, const vo
     a.q = q; a.k = k; a.v = v; a.g = g; a.beta = beta; a.h0 = h0; a.do_ = do_; a.dht = dht;
     a.dq = dq; a.dk = dk; a.dv = dv; a.dg = dg; a.dbeta = dbeta; a.dh0 = dh0;
     a.states = states;
+    a.saved = saved;
     a.ws = ws;
     return launch_chunk_bwd(a, st) == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
 }

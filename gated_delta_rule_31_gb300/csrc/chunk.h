@@ -79,6 +79,32 @@ inline size_t chunk_bwd_workspace(const ChunkProblem& p) { return ws_layout(p, t
 inline size_t chunk_bwd_states_workspace(const ChunkProblem& p) { return ws_layout(p, true, true).total; }
 inline size_t chunk_states_bytes(const ChunkProblem& p) { return (size_t)p.B * p.Hv * p.NC * STATE_IMG; }
 
+// Everything the forward can keep for the backward (the caller's "saved" buffer): Gamma_C per
+// chunk, the operator records, T and W per chunk, and the chunk-start state images. With it
+// the backward runs neither prep nor the forward states scan. Its own workspace then holds
+// the status word and the chunk-end state gradients.
+struct SavedLayout {
+    size_t gam, rec, rec2, hs, total;
+    int ncpad;
+};
+inline SavedLayout saved_layout(const ChunkProblem& p) {
+    SavedLayout l;
+    l.ncpad = (int)round_up((size_t)p.NC, 4);
+    const size_t nh = (size_t)p.B * p.Hv;
+    l.gam = 0;
+    l.rec = round_up(nh * l.ncpad * sizeof(float), 1024);
+    l.rec2 = l.rec + nh * p.NC * (size_t)REC_BYTES;
+    l.hs = l.rec2 + nh * p.NC * (size_t)REC2_BYTES;
+    l.total = l.hs + nh * p.NC * (size_t)STATE_IMG;
+    return l;
+}
+inline size_t chunk_saved_bytes(const ChunkProblem& p) { return saved_layout(p).total; }
+constexpr size_t kSavedFwdWorkspace = 256;  // status word only
+constexpr size_t kSavedBwdDhs = 1024;       // offset of the state gradients in the backward workspace
+inline size_t chunk_bwd_saved_workspace(const ChunkProblem& p) {
+    return kSavedBwdDhs + (size_t)p.B * p.Hv * p.NC * STATE_IMG;
+}
+
 struct ChunkFwdArgs {
     ChunkProblem p;
     const void *q, *k, *v;
@@ -86,6 +112,7 @@ struct ChunkFwdArgs {
     void* o;
     float* ht;
     void* states;  // optional: chunk-start states kept for the backward
+    void* saved;   // optional: the whole saved buffer (saved_layout); then ws is the status word only
     void* ws;
 };
 struct ChunkBwdArgs {
@@ -96,6 +123,7 @@ struct ChunkBwdArgs {
     const float* dht;
     float *dq, *dk, *dv, *dg, *dbeta, *dh0;
     const void* states;  // optional: chunk-start states saved by the forward
+    const void* saved;   // optional: the forward's saved buffer (saved_layout)
     void* ws;
 };
 

@@ -732,7 +732,9 @@ teardown:
 cudaError_t launch_chunk_bwd(const ChunkBwdArgs& a, cudaStream_t s) {
     const ChunkProblem& p = a.p;
     const bool saved = a.states != nullptr;
+    const uint8_t* keep = static_cast<const uint8_t*>(a.saved);
     const WsLayout w = ws_layout(p, true, saved);
+    const SavedLayout l = saved_layout(p);
     uint8_t* ws = static_cast<uint8_t*>(a.ws);
     CUtensorMap mq, mk, mv, mdo32, mdo64;
     if (!make_qkv_maps(p, a.q, a.k, a.v, &mq, &mk, &mv)) return cudaErrorInvalidValue;
@@ -740,17 +742,25 @@ cudaError_t launch_chunk_bwd(const ChunkBwdArgs& a, cudaStream_t s) {
         !make_map_4d_bf16(&mdo64, a.do_, kD, p.Hv, p.T, p.B, 64, kChunk, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     int* status = reinterpret_cast<int*>(ws);
+    cudaError_t e = cudaSuccess;
     PrepArgs pa;
     pa.p = p;
     pa.g = a.g;
     pa.beta = a.beta;
-    pa.gam = reinterpret_cast<float*>(ws + w.gam);
-    pa.rec = ws + w.rec;
-    pa.rec2 = ws + w.rec2;
     pa.status = status;
-    pa.ncpad = w.ncpad;
-    cudaError_t e = launch_prep(pa, mq, mk, mv, s);
-    if (e != cudaSuccess) return e;
+    if (keep) {  // the forward kept its operators: no prep, no forward scan
+        pa.gam = reinterpret_cast<float*>(const_cast<uint8_t*>(keep + l.gam));
+        pa.rec = const_cast<uint8_t*>(keep + l.rec);
+        pa.rec2 = const_cast<uint8_t*>(keep + l.rec2);
+        pa.ncpad = l.ncpad;
+    } else {
+        pa.gam = reinterpret_cast<float*>(ws + w.gam);
+        pa.rec = ws + w.rec;
+        pa.rec2 = ws + w.rec2;
+        pa.ncpad = w.ncpad;
+        if ((e = launch_prep(pa, mq, mk, mv, s)) != cudaSuccess) return e;
+    }
+    uint8_t* dhs = keep ? ws + kSavedBwdDhs : ws + w.dhs;
     ScanArgs sa;
     sa.p = p;
     sa.gam = pa.gam;
@@ -760,12 +770,12 @@ cudaError_t launch_chunk_bwd(const ChunkBwdArgs& a, cudaStream_t s) {
     sa.hfinal = nullptr;
     sa.states = ws + w.hs;
     sa.status = status;
-    sa.ncpad = w.ncpad;
-    const uint8_t* hs = saved ? static_cast<const uint8_t*>(a.states) : ws + w.hs;
-    if (!saved && (e = launch_scan(sa, SCAN_FWD_STATES, nullptr, s)) != cudaSuccess) return e;
+    sa.ncpad = pa.ncpad;
+    const uint8_t* hs = keep ? keep + l.hs : saved ? static_cast<const uint8_t*>(a.states) : ws + w.hs;
+    if (!keep && !saved && (e = launch_scan(sa, SCAN_FWD_STATES, nullptr, s)) != cudaSuccess) return e;
     sa.hinit = a.dht;
     sa.hfinal = a.dh0;
-    sa.states = ws + w.dhs;
+    sa.states = dhs;
     if ((e = launch_scan(sa, SCAN_BWD, &mdo32, s)) != cudaSuccess) return e;
     GradArgs ga;
     ga.p = p;
@@ -774,7 +784,7 @@ cudaError_t launch_chunk_bwd(const ChunkBwdArgs& a, cudaStream_t s) {
     ga.rec = pa.rec;
     ga.rec2 = pa.rec2;
     ga.hs = hs;
-    ga.dhs = ws + w.dhs;
+    ga.dhs = dhs;
     ga.gam = pa.gam;
     ga.dq = a.dq;
     ga.dk = a.dk;

@@ -677,17 +677,19 @@ bool make_qkv_maps(const ChunkProblem& p, const void* q, const void* k, const vo
 cudaError_t launch_chunk_fwd(const ChunkFwdArgs& a, cudaStream_t s) {
     const WsLayout w = ws_layout(a.p, false);
     uint8_t* ws = static_cast<uint8_t*>(a.ws);
+    uint8_t* keep = static_cast<uint8_t*>(a.saved);
+    const SavedLayout l = saved_layout(a.p);
     CUtensorMap mq, mk, mv;
     if (!make_qkv_maps(a.p, a.q, a.k, a.v, &mq, &mk, &mv)) return cudaErrorInvalidValue;
     PrepArgs pa;
     pa.p = a.p;
     pa.g = a.g;
     pa.beta = a.beta;
-    pa.gam = reinterpret_cast<float*>(ws + w.gam);
-    pa.rec = ws + w.rec;
-    pa.rec2 = nullptr;
+    pa.gam = reinterpret_cast<float*>(keep ? keep + l.gam : ws + w.gam);
+    pa.rec = keep ? keep + l.rec : ws + w.rec;
+    pa.rec2 = keep ? keep + l.rec2 : nullptr;
     pa.status = reinterpret_cast<int*>(ws);
-    pa.ncpad = w.ncpad;
+    pa.ncpad = keep ? l.ncpad : w.ncpad;
     cudaError_t e = launch_prep(pa, mq, mk, mv, s);
     if (e != cudaSuccess) return e;
     ScanArgs sa;
@@ -697,9 +699,9 @@ cudaError_t launch_chunk_fwd(const ChunkFwdArgs& a, cudaStream_t s) {
     sa.hinit = a.h0;
     sa.o = a.o;
     sa.hfinal = a.ht;
-    sa.states = static_cast<uint8_t*>(a.states);
+    sa.states = keep ? keep + l.hs : static_cast<uint8_t*>(a.states);
     sa.status = pa.status;
-    sa.ncpad = w.ncpad;
+    sa.ncpad = pa.ncpad;
     return launch_scan(sa, SCAN_FWD_OUT, nullptr, s);
 }
 

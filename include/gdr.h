@@ -129,6 +129,36 @@ gdr_status gdr_bwd_chunked_states(const gdr_problem* p, const void* q, const voi
                                   const void* do_, const float* dht, float* dq, float* dk, float* dv, float* dg,
                                   float* dbeta, float* dh0, void* ws, size_t ws_bytes, gdr_stream_t stream);
 
+/* Saved-operator handoff: the forward keeps everything the backward would recompute — the
+ * per-chunk decay, the chunk operator records (88 KB), the UT inverse T and W (24 KB) and the
+ * chunk-start states (32 KB), i.e. 144 KB per (b, hv, chunk) plus a small header, in one
+ * caller-owned, 256-byte-aligned buffer of gdr_chunk_saved_bytes() bytes (opaque layout;
+ * 2.4 GB at B=1, T=32768, Hv=32). The backward then runs only the reverse scan and the
+ * chunk-local gradient kernel. This trades memory for the backward's recomputation, which
+ * the chunked VJP of "Adding VJP for gated delta net" (MLX PR #4565) performs; results are
+ * bitwise identical to gdr_fwd_chunked / gdr_bwd_chunked. The buffer must not be modified
+ * between the two calls, and the backward must get the same q, k, v, g, beta and problem.
+ * Workspaces: gdr_fwd_chunked_saved_workspace() (the status word only) and
+ * gdr_bwd_chunked_saved_workspace(). Same support matrix as gdr_fwd_chunked; the size
+ * queries return 0 for an invalid or unsupported problem. Errors as gdr_fwd_chunked, plus
+ * GDR_ERR_WORKSPACE if `saved` is NULL or smaller than required. */
+size_t gdr_chunk_saved_bytes(const gdr_problem* p);
+size_t gdr_fwd_chunked_saved_workspace(const gdr_problem* p);
+size_t gdr_bwd_chunked_saved_workspace(const gdr_problem* p);
+
+/* gdr_fwd_chunked that also fills `saved`. */
+gdr_status gdr_fwd_chunked_saved(const gdr_problem* p, const void* q, const void* k, const void* v,
+                                 const float* g, const float* beta, const float* h0, void* o, float* ht,
+                                 void* saved, size_t saved_bytes, void* ws, size_t ws_bytes,
+                                 gdr_stream_t stream);
+
+/* gdr_bwd_chunked for the same inputs, reading `saved` from gdr_fwd_chunked_saved (h0 is
+ * then not needed; dh0 is still written if non-NULL). */
+gdr_status gdr_bwd_chunked_saved(const gdr_problem* p, const void* q, const void* k, const void* v,
+                                 const float* g, const float* beta, const void* saved, size_t saved_bytes,
+                                 const void* do_, const float* dht, float* dq, float* dk, float* dv, float* dg,
+                                 float* dbeta, float* dh0, void* ws, size_t ws_bytes, gdr_stream_t stream);
+
 /* One decode step (p->T must be 1) on the state in place: per state row, one pass forms
  * the prediction with the decay folded in, a second applies decay plus the rank-one
  * update while accumulating the output, so the state is read once and written once.

@@ -142,3 +142,24 @@ def test_autograd_function_has_no_cpu_path():
     g, beta = torch.zeros(1, 8, 2), torch.full((1, 8, 2), 0.5)
     with pytest.raises(ValueError, match="CUDA"):
         gated_delta_rule(q, q, v, g, beta)
+
+
+def test_saved_operator_handoff_validation(L):
+    p = prob()
+    sb = L.gdr_chunk_saved_bytes(ctypes.byref(p))
+    # header (per-chunk decay, padded) + (88 KB record + 24 KB T/W + 32 KB state) per (b, hv, chunk)
+    assert sb == 1024 + 4 * 1 * (90112 + 24576 + 32768)
+    fw = L.gdr_fwd_chunked_saved_workspace(ctypes.byref(p))
+    bw = L.gdr_bwd_chunked_saved_workspace(ctypes.byref(p))
+    assert fw == 256 and bw == 1024 + 4 * 32768
+    assert L.gdr_fwd_chunked_saved(ctypes.byref(p), *[FAKE] * 8, FAKE, sb - 1, FAKE, fw, None) == WORKSPACE
+    assert L.gdr_fwd_chunked_saved(ctypes.byref(p), *[FAKE] * 8, None, sb, FAKE, fw, None) == WORKSPACE
+    assert L.gdr_fwd_chunked_saved(ctypes.byref(p), *[FAKE] * 8, FAKE, sb, FAKE, fw - 1, None) == WORKSPACE
+    assert L.gdr_fwd_chunked_saved(ctypes.byref(p), *[FAKE] * 8, MISALIGNED, sb, FAKE, fw, None) == INVALID
+    args = [FAKE] * 5 + [FAKE, sb] + [FAKE] * 8
+    assert L.gdr_bwd_chunked_saved(ctypes.byref(p), *args, FAKE, bw - 1, None) == WORKSPACE
+    args = [FAKE] * 5 + [FAKE, sb - 16] + [FAKE] * 8
+    assert L.gdr_bwd_chunked_saved(ctypes.byref(p), *args, FAKE, bw, None) == WORKSPACE
+    q = prob(dtype=0)
+    assert L.gdr_chunk_saved_bytes(ctypes.byref(q)) == 0
+    assert L.gdr_fwd_chunked_saved(ctypes.byref(q), *[FAKE] * 8, FAKE, sb, FAKE, fw, None) == UNSUPPORTED

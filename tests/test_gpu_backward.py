@@ -144,3 +144,31 @@ def test_saved_state_handoff_matches_recompute(shape):
     for n in NAMES:
         assert torch.equal(ga[n], gb[n]), n
     check(gb, x)
+
+
+@pytest.mark.parametrize("shape", [Shape(1, 300, 2, 4, 128, 128), Shape(2, 129, 1, 2, 128, 128),
+                                   Shape(1, 64, 1, 1, 128, 128)])
+def test_saved_operator_handoff_matches_recompute(shape):
+    """The forward can keep every chunk operator and state for the backward: outputs and all
+    gradients are bitwise those of the recompute path (and therefore match the oracle)."""
+    dev = cuda_device()
+    x = make_inputs(shape, dtype=torch.bfloat16, seed=shape.T + 7, grads=True, gate_scale=0.1)
+    d = to_dev(x, dev)
+    o1, h1 = gdr.fwd_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"])
+    o2, h2, saved = gdr.fwd_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], save_all=True)
+    assert torch.equal(o1, o2) and torch.equal(h1, h2)
+    ga = gdr.bwd_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], d["do"], d["dht"])
+    gb = gdr.bwd_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], None, d["do"], d["dht"], saved=saved)
+    for n in NAMES:
+        assert torch.equal(ga[n], gb[n]), n
+    check(gb, x)
+
+
+def test_saved_operator_handoff_empty_sequence():
+    dev = cuda_device()
+    x = make_inputs(Shape(1, 0, 1, 2, 128, 128), dtype=torch.bfloat16, seed=1, grads=True)
+    d = to_dev(x, dev)
+    o, ht, saved = gdr.fwd_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], save_all=True)
+    assert torch.equal(ht.cpu(), x["h0"])
+    gr = gdr.bwd_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], None, d["do"], d["dht"], saved=saved)
+    assert torch.equal(gr["dh0"].cpu(), x["dht"])

@@ -74,6 +74,19 @@ def test_autograd_equals_direct_calls():
         assert torch.equal(gr[n], ref[n]), n
 
 
+def test_keep_operators_is_bitwise_identical():
+    dev = cuda_device()
+    x = make_inputs(Shape(1, 150, 2, 4, 128, 128), dtype=torch.bfloat16, seed=31, grads=True)
+    res = []
+    for keep in (False, True):
+        t = leaves(x, dev)
+        o, ht = gated_delta_rule(t["q"], t["k"], t["v"], t["g"], t["beta"], t["h0"], keep_operators=keep)
+        ((o.float() * x["do"].to(dev).float()).sum() + (ht * x["dht"].to(dev)).sum()).backward()
+        res.append([o.detach(), ht.detach()] + [t[n].grad for n in INPUTS])
+    for a, b in zip(*res):
+        assert torch.equal(a, b)
+
+
 def test_unused_outputs_and_no_grad():
     dev = cuda_device()
     x = make_inputs(Shape(1, 70, 1, 2, 128, 128), dtype=torch.bfloat16, seed=23, grads=True, h0_std=None)

@@ -138,9 +138,9 @@ __global__ void __launch_bounds__(256, 2)
         const uint32_t base = sb + PS_KQ + half * 16384 + row * 128;
         float ss = 0.f;
 #pragma unroll
-        for (int ch = 0; ch < 8; ch++) {
-            float x[8];
-            unpack8(ld_shared_v4(base + ch * 16), x);
+        for (int ch = 0; ch < 8; ch++) {  // physical chunk order rotated per thread: a quarter warp
+            float x[8];                   // (4 rows x 2 halves) then reads 8 distinct bank groups
+            unpack8(ld_shared_v4(base + ((ch + 2 * row + half) & 7) * 16), x);
 #pragma unroll
             for (int e = 0; e < 8; e++) ss += x[e] * x[e];
         }
@@ -197,10 +197,6 @@ __global__ void __launch_bounds__(256, 2)
     // column each): forward substitution with L_II = I + A_II gives the diagonal inverses T_II
     // (right-hand side e_c) and Y_IK = T_II A_IK for I > K (right-hand side column c of A_IK).
     // Then T_IJ = -sum_{J<=K<I} Y_IK T_KJ by block distance I-J = 1, 2, 3.
-    for (int idx = tid; idx < 64 * 64; idx += 256) {
-        const int i = idx >> 6, j = idx & 63;
-        if ((i >> 4) < (j >> 4)) Tm[i * LDA + j] = 0.f;
-    }
     if (tid < 160) {
         int I, K, cc;
         const bool diag = tid < 64;
@@ -250,35 +246,38 @@ __global__ void __launch_bounds__(256, 2)
         }
         __syncthreads();
     }
-    {  // [Tw; Tu] with Tw = T diag(beta Gamma rho_k), Tu = T diag(beta): K-major A operand (over A)
+    {  // [Tw; Tu] with Tw = T diag(beta Gamma rho_k), Tu = T diag(beta): K-major A operand (over A).
+       // T's blocks above the block diagonal are zero and never stored: masked here.
         const int row = tid >> 1, half = tid & 1;
         const int i = row & 63;
         const bool isw = row < 64;
         const float* trow = Tm + i * LDA + 32 * half;
 #pragma unroll
         for (int q = 0; q < 4; q++) {
-            float x[8];
+            float t[8], x[8];
 #pragma unroll
             for (int e = 0; e < 8; e++) {
                 const int j = 32 * half + 8 * q + e;
-                x[e] = trow[8 * q + e] * (isw ? fw[j] : bet[j]);
+                t[e] = (j >> 4) <= (i >> 4) ? trow[8 * q + e] : 0.f;
+                x[e] = t[e] * (isw ? fw[j] : bet[j]);
             }
             st_chunk(sb + PS_TT + sw128_chunk(row, 4 * half + q, 128), x, 1.f);
             if (isw && rec2)  // T itself for the backward
-                st_global16(rec2 + REC2_T + sw128_chunk(i, 4 * half + q, 64), pack8(trow + 8 * q, 1.f));
+                st_global16(rec2 + REC2_T + sw128_chunk(i, 4 * half + q, 64), pack8(t, 1.f));
         }
     }
     fence_proxy_async_smem();
     __syncthreads();
 
-    // W = Tw K and U~ = Tu V (M=64 each; B operands are the raw k / v tiles, MN-major)
+    // W = Tw K and U~ = Tu V as two M=128 products of [Tw; Tu] (rows 0-63 of the first and
+    // rows 64-127 of the second are the wanted ones; an M=64 product would take as long and
+    // leave half of every warp idle in the epilogue). B operands: raw k / v tiles, MN-major.
     if (tid == 0) {
         tc_fence_after();
-        const uint32_t id = idesc_bf16(64, 128, 0, 1);
+        const uint32_t id = idesc_bf16(128, 128, 0, 1);
         for (int k0 = 0; k0 < kChunk; k0 += 16) {
-            mma_bf16(tm + 128, desc_kmajor(sb + PS_TT, 128, 0, k0), desc_mnmajor(sb + PS_KQ, 128, 0, k0), id,
-                     k0 > 0);
-            mma_bf16(tm + 0, desc_kmajor(sb + PS_TT, 128, 64, k0), desc_mnmajor(sb + PS_V, 64, 0, k0), id, k0 > 0);
+            mma_bf16(tm + 0, desc_kmajor(sb + PS_TT, 128, 0, k0), desc_mnmajor(sb + PS_KQ, 128, 0, k0), id, k0 > 0);
+            mma_bf16(tm + 128, desc_kmajor(sb + PS_TT, 128, 0, k0), desc_mnmajor(sb + PS_V, 64, 0, k0), id, k0 > 0);
         }
         mma_commit(&bar_mma);
     }
@@ -287,35 +286,31 @@ __global__ void __launch_bounds__(256, 2)
     tc_fence_after();
     {
         const int lg = warp & 3, h = warp >> 2;
-        const int i = 16 * lg + (lane & 15);  // M=64 accumulator rows: 16 per TMEM sub-partition
-        {
+        if (lg < 2) {  // W rows i = 32 lg + lane (first product, columns 64 h ..)
+            const int i = 32 * lg + lane;
             float w[64];
-            tmem_ld32(tmem_at(tm, 32 * lg, 128 + 64 * h), w);
-            tmem_ld32(tmem_at(tm, 32 * lg, 128 + 64 * h + 32), w + 32);
+            tmem_ld32(tmem_at(tm, 32 * lg, 64 * h), w);
+            tmem_ld32(tmem_at(tm, 32 * lg, 64 * h + 32), w + 32);
             tmem_wait_ld();
-            if (lane < 16) {
-                const float sbar = fb[i];
+            const float sbar = fb[i];
 #pragma unroll
-                for (int q = 0; q < 8; q++) {
-                    const uint4 u = pack8(w + 8 * q, 1.f);
-                    const uint32_t off = sw128_chunk(i, 8 * h + q, 64);
-                    st_shared_v4(sb + PS_W + off, u.x, u.y, u.z, u.w);
-                    if (rec2) st_global16(rec2 + REC2_W + off, u);
-                    st_chunk(sb + PS_WBAR + off, w + 8 * q, sbar);
-                }
+            for (int q = 0; q < 8; q++) {
+                const uint4 u = pack8(w + 8 * q, 1.f);
+                const uint32_t off = sw128_chunk(i, 8 * h + q, 64);
+                st_shared_v4(sb + PS_W + off, u.x, u.y, u.z, u.w);
+                if (rec2) st_global16(rec2 + REC2_W + off, u);
+                st_chunk(sb + PS_WBAR + off, w + 8 * q, sbar);
             }
-        }
-        {
+        } else {  // U~ rows i = 32 lg + lane - 64 (second product)
+            const int i = 32 * lg + lane - 64;
             float u[64];
-            tmem_ld32(tmem_at(tm, 32 * lg, 64 * h), u);
-            tmem_ld32(tmem_at(tm, 32 * lg, 64 * h + 32), u + 32);
+            tmem_ld32(tmem_at(tm, 32 * lg, 128 + 64 * h), u);
+            tmem_ld32(tmem_at(tm, 32 * lg, 128 + 64 * h + 32), u + 32);
             tmem_wait_ld();
-            if (lane < 16) {
 #pragma unroll
-                for (int q = 0; q < 8; q++) {
-                    const int col = 64 * h + 8 * q;
-                    st_global16(rec + REC_U + (col >> 5) * 4096 + sw64_chunk(i, q & 3), pack8(u + 8 * q, 1.f));
-                }
+            for (int q = 0; q < 8; q++) {
+                const int col = 64 * h + 8 * q;
+                st_global16(rec + REC_U + (col >> 5) * 4096 + sw64_chunk(i, q & 3), pack8(u + 8 * q, 1.f));
             }
         }
         // Kbar = diag(exp(gamma_C - gamma) rho_k) K, straight to the record

@@ -164,26 +164,31 @@ __global__ void __launch_bounds__(256, 2)
         float v[32];
         tmem_ld32(tmem_at(tm, 32 * lg, 32 * h), v);
         tmem_wait_ld();
-        if (r < 64) {
-            const int i = r;
-            const float gi = gam[i], ci = bet[i] * rho[i];
+        // All loads first, then all stores: stores into the same shared memory in between
+        // would keep the compiler from overlapping the loads (it cannot rule out aliasing).
+        const bool arow = r < 64;  // warp-uniform
+        const int i = r & 63;
+        const int lim = arow ? i : i + 1;  // A: j < i (strict), P: j <= i
+        const float gi = gam[i], ci = arow ? bet[i] * rho[i] : P.scale * rho[64 + i];
+        const float4* g4 = reinterpret_cast<const float4*>(gam + 32 * h);
+        const float4* r4 = reinterpret_cast<const float4*>(rho + 32 * h);
 #pragma unroll
-            for (int jj = 0; jj < 32; jj++) {
-                const int j = 32 * h + jj;
-                Am[i * LDA + j] = (j < i) ? ci * rho[j] * __expf(gi - gam[j]) * v[jj] : 0.f;
+        for (int q = 0; q < 8; q++) {
+            const float4 gg = g4[q], rr = r4[q];
+            const float gj[4] = {gg.x, gg.y, gg.z, gg.w}, rj[4] = {rr.x, rr.y, rr.z, rr.w};
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                const int jj = 4 * q + e;
+                v[jj] = (32 * h + jj < lim) ? ci * rj[e] * __expf(gi - gj[e]) * v[jj] : 0.f;
             }
+        }
+        if (arow) {
+#pragma unroll
+            for (int jj = 0; jj < 32; jj++) Am[i * LDA + 32 * h + jj] = v[jj];
         } else {
-            const int i = r - 64;
-            const float gi = gam[i], ci = P.scale * rho[64 + i];
 #pragma unroll
             for (int q = 0; q < 4; q++) {
-                float x[8];
-#pragma unroll
-                for (int e = 0; e < 8; e++) {
-                    const int j = 32 * h + 8 * q + e;
-                    x[e] = (j <= i) ? ci * rho[j] * __expf(gi - gam[j]) * v[8 * q + e] : 0.f;
-                }
-                const uint4 u = pack8(x, 1.f);
+                const uint4 u = pack8(v + 8 * q, 1.f);
                 const uint32_t off = sw128_chunk(i, 4 * h + q, 64);
                 st_shared_v4(sb + PS_P + off, u.x, u.y, u.z, u.w);
                 st_global16(rec + REC_P + off, u);
@@ -230,20 +235,25 @@ __global__ void __launch_bounds__(256, 2)
         }
     }
     __syncthreads();
-    for (int dlev = 1; dlev <= 3; dlev++) {
+    for (int dlev = 1; dlev <= 3; dlev++) {  // item J of a level: block (J + dlev, J); all sums before any store
         const int nb = 4 - dlev;
-        for (int o = tid; o < nb * 256; o += 256) {
-            const int J = o >> 8, i = (o >> 4) & 15, cc = o & 15;
-            const int I = J + dlev;
-            float s = 0.f;
-            for (int K = J; K < I; K++) {
-                const float* yr = Xs + (I * (I - 1) / 2 + K) * (16 * 17) + i * 17;
-                const float* tc = Tm + (16 * K) * LDA + 16 * J + cc;
+        const int i = (tid >> 4) & 15, cc = tid & 15;
+        float s[3] = {0.f, 0.f, 0.f};
 #pragma unroll
-                for (int m = 0; m < 16; m++) s += yr[m] * tc[m * LDA];
+        for (int J = 0; J < 3; J++) {
+            if (J < nb) {
+                const int I = J + dlev;
+                for (int K = J; K < I; K++) {
+                    const float* yr = Xs + (I * (I - 1) / 2 + K) * (16 * 17) + i * 17;
+                    const float* tc = Tm + (16 * K) * LDA + 16 * J + cc;
+#pragma unroll
+                    for (int m = 0; m < 16; m++) s[J] += yr[m] * tc[m * LDA];
+                }
             }
-            Tm[(16 * I + i) * LDA + 16 * J + cc] = -s;
         }
+#pragma unroll
+        for (int J = 0; J < 3; J++)
+            if (J < nb) Tm[(16 * (J + dlev) + i) * LDA + 16 * J + cc] = -s[J];
         __syncthreads();
     }
     {  // [Tw; Tu] with Tw = T diag(beta Gamma rho_k), Tu = T diag(beta): K-major A operand (over A).
@@ -252,18 +262,19 @@ __global__ void __launch_bounds__(256, 2)
         const int i = row & 63;
         const bool isw = row < 64;
         const float* trow = Tm + i * LDA + 32 * half;
+        const float* fac = (isw ? fw : bet) + 32 * half;
+        float t[32], x[32];
+#pragma unroll
+        for (int jj = 0; jj < 32; jj++) {  // all loads first (see the A/P epilogue)
+            const int j = 32 * half + jj;
+            t[jj] = (j >> 4) <= (i >> 4) ? trow[jj] : 0.f;
+            x[jj] = t[jj] * fac[jj];
+        }
 #pragma unroll
         for (int q = 0; q < 4; q++) {
-            float t[8], x[8];
-#pragma unroll
-            for (int e = 0; e < 8; e++) {
-                const int j = 32 * half + 8 * q + e;
-                t[e] = (j >> 4) <= (i >> 4) ? trow[8 * q + e] : 0.f;
-                x[e] = t[e] * (isw ? fw[j] : bet[j]);
-            }
-            st_chunk(sb + PS_TT + sw128_chunk(row, 4 * half + q, 128), x, 1.f);
+            st_chunk(sb + PS_TT + sw128_chunk(row, 4 * half + q, 128), x + 8 * q, 1.f);
             if (isw && rec2)  // T itself for the backward
-                st_global16(rec2 + REC2_T + sw128_chunk(i, 4 * half + q, 64), pack8(t, 1.f));
+                st_global16(rec2 + REC2_T + sw128_chunk(i, 4 * half + q, 64), pack8(t + 8 * q, 1.f));
         }
     }
     fence_proxy_async_smem();
@@ -314,11 +325,20 @@ __global__ void __launch_bounds__(256, 2)
             }
         }
         // Kbar = diag(exp(gamma_C - gamma) rho_k) K, straight to the record
-        for (int idx = tid; idx < 64 * 16; idx += 256) {
-            const int r = idx >> 4, j = idx & 15;
-            float x[8];
-            unpack8(ld_shared_v4(sb + PS_KQ + sw128_chunk(r, j, 128)), x);
-            st_global16(rec + REC_K + sw128_chunk(r, j, 64), pack8(x, fb[r]));
+        {
+            uint4 kv[4];
+#pragma unroll
+            for (int n = 0; n < 4; n++) {
+                const int idx = tid + 256 * n, r = idx >> 4, j = idx & 15;
+                kv[n] = ld_shared_v4(sb + PS_KQ + sw128_chunk(r, j, 128));
+            }
+#pragma unroll
+            for (int n = 0; n < 4; n++) {
+                const int idx = tid + 256 * n, r = idx >> 4, j = idx & 15;
+                float x[8];
+                unpack8(kv[n], x);
+                st_global16(rec + REC_K + sw128_chunk(r, j, 64), pack8(x, fb[r]));
+            }
         }
     }
     fence_proxy_async_smem();
@@ -359,10 +379,13 @@ __global__ void __launch_bounds__(256, 2)
             tmem_wait_ld();
             if (lane < 16) {
                 const float f = fq[i];
+                uint4 qv[8];
+#pragma unroll
+                for (int q = 0; q < 8; q++) qv[q] = ld_shared_v4(sb + PS_KQ + sw128_chunk(64 + i, 8 * h + q, 128));
 #pragma unroll
                 for (int q = 0; q < 8; q++) {
                     float x[8];
-                    unpack8(ld_shared_v4(sb + PS_KQ + sw128_chunk(64 + i, 8 * h + q, 128)), x);
+                    unpack8(qv[q], x);
 #pragma unroll
                     for (int e = 0; e < 8; e++) x[e] = f * x[e] - pw[8 * q + e];
                     st_global16(rec + REC_Q + sw128_chunk(i, 8 * h + q, 64), pack8(x, 1.f));

@@ -315,6 +315,11 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
             s = warp_sum(s);
             if (lane == 0) red[warp] = s;
         }
+        uint4 utv[4];  // U~ slice qt (columns c32..) from the record, fetched while M1 runs
+        if (act) {
+#pragma unroll
+            for (int q = 0; q < 4; q++) utv[q] = *reinterpret_cast<const uint4*>(rec + REC_U + qt * 4096 + sw64_chunk(r, q));
+        }
         if (!wait_mma(43)) goto teardown;
         if (tid == 0) {
             float s = 0.f;
@@ -327,9 +332,9 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
             tmem_wait_ld();
             if (act) {
 #pragma unroll
-                for (int q = 0; q < 4; q++) {  // columns c32.. are exactly U~ slice qt
+                for (int q = 0; q < 4; q++) {
                     float ut[8];
-                    unpack8b(*reinterpret_cast<const uint4*>(rec + REC_U + qt * 4096 + sw64_chunk(r, q)), ut);
+                    unpack8b(utv[q], ut);
 #pragma unroll
                     for (int e = 0; e < 8; e++) ut[e] -= x[8 * q + e];
                     st_chunk8(sb + G_W + sw128_chunk(r, 4 * qt + q, 64), ut, 1.f);

@@ -1,6 +1,8 @@
 // chunk_fwd.cu - tensor-core chunked gated delta rule (chunks of 64 tokens, Dk = Dv = 128):
-//   prep_kernel : one CTA per (b, v-head, chunk), all chunks in parallel. Builds the
-//                 chunk's operators (UT/WY transform of the k k^T beta block, output and
+//   prep_kernel : persistent, two CTAs per SM; a CTA takes (b, key head, chunk) groups in
+//                 turn and, for each, the value heads sharing that key head one after the
+//                 other (k, q and their norms loaded once per group; the next head's v is
+//                 fetched while the current head finishes). Builds each chunk's operators (UT/WY transform of the k k^T beta block, output and
 //                 state operators) on tcgen05 with TMEM accumulators and writes them as
 //                 ready-to-use shared-memory images.
 //   scan_kernel : one CTA per (b, v-head, 32-column slice of the state). Runs the chunks
@@ -58,17 +60,13 @@ __global__ void __launch_bounds__(256, 2)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
     const uint32_t sb = smem_u32(sm);
-    __shared__ uint64_t bar_tma, bar_mma;
+    __shared__ uint64_t bar_kq, bar_v, bar_mma;
     __shared__ uint32_t tmem_sh;
     __shared__ int abort_sh;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int c = blockIdx.x, hv = blockIdx.y, b = blockIdx.z;
     const ChunkProblem& P = a.p;
-    const int hk = hv / (P.Hv / P.Hk);
-    const int t0 = c * kChunk;
-    const size_t bh = (size_t)b * P.Hv + hv;
-    uint8_t* rec = a.rec + (bh * P.NC + c) * REC_BYTES;
-    uint8_t* rec2 = a.rec2 ? a.rec2 + (bh * P.NC + c) * REC2_BYTES : nullptr;
+    const int G = P.Hv / P.Hk;
+    const int ngroups = P.B * P.Hk * P.NC;  // (b, key head, chunk); its G value heads run in turn
     float* gam = reinterpret_cast<float*>(sm + PS_SMALL);  // in-chunk cumulative log-decay
     float* bet = gam + 64;
     float* rho = bet + 64;   // [128] rows 0-63: k norm factors, 64-127: q norm factors
@@ -78,10 +76,31 @@ __global__ void __launch_bounds__(256, 2)
     float* Am = reinterpret_cast<float*>(sm + PS_A);
     float* Tm = reinterpret_cast<float*>(sm + PS_T);
     float* Xs = reinterpret_cast<float*>(sm + PS_SCR);
+    uint32_t kq_ph = 0, v_ph = 0, mph = 0;  // mbarrier phases
+    bool kq_pend = false, v_pend = false;   // copies issued and not yet waited for (thread 0)
+    bool ok = true;
+    // group g -> (b, hk, c); value head hv = hk * G + hh
+    auto issue_kq = [&](int g) {
+        const int c = g % P.NC, hk = (g / P.NC) % P.Hk, b = g / (P.NC * P.Hk);
+        mbar_expect_tx(&bar_kq, 4 * 8192);
+        tma_load_4d(sm + PS_KQ + 0, &mk, 0, hk, c * kChunk, b, &bar_kq);
+        tma_load_4d(sm + PS_KQ + 16384, &mk, 64, hk, c * kChunk, b, &bar_kq);
+        tma_load_4d(sm + PS_KQ + 8192, &mq, 0, hk, c * kChunk, b, &bar_kq);
+        tma_load_4d(sm + PS_KQ + 24576, &mq, 64, hk, c * kChunk, b, &bar_kq);
+        kq_pend = true;
+    };
+    auto issue_v = [&](int g, int hh) {
+        const int c = g % P.NC, hk = (g / P.NC) % P.Hk, b = g / (P.NC * P.Hk);
+        mbar_expect_tx(&bar_v, 2 * 8192);
+        tma_load_4d(sm + PS_V + 0, &mv, 0, hk * G + hh, c * kChunk, b, &bar_v);
+        tma_load_4d(sm + PS_V + 8192, &mv, 64, hk * G + hh, c * kChunk, b, &bar_v);
+        v_pend = true;
+    };
 
     if (tid == 0) {
         abort_sh = 0;
-        mbar_init(&bar_tma, 1);
+        mbar_init(&bar_kq, 1);
+        mbar_init(&bar_v, 1);
         mbar_init(&bar_mma, 1);
         fence_barrier_init();
     }
@@ -93,14 +112,34 @@ __global__ void __launch_bounds__(256, 2)
     __syncthreads();
     tc_fence_after();
     const uint32_t tm = tmem_sh;
+    if (tid == 0 && (int)blockIdx.x < ngroups) {
+        issue_kq(blockIdx.x);
+        issue_v(blockIdx.x, 0);
+    }
+
+    for (int grp = blockIdx.x; grp < ngroups; grp += gridDim.x) {
+    const int c = grp % P.NC, hk = (grp / P.NC) % P.Hk, b = grp / (P.NC * P.Hk);
+    const int t0 = c * kChunk;
+    const int next = grp + (int)gridDim.x;
+    ok = mbar_wait(&bar_kq, kq_ph, &abort_sh, a.status, 10);
+    kq_ph ^= 1;
+    if (tid == 0) kq_pend = false;
+    if (__syncthreads_or(!ok)) goto teardown;
+
+    for (int hh = 0; hh < G; hh++) {
+    const int hv = hk * G + hh;
+    const size_t bh = (size_t)b * P.Hv + hv;
+    uint8_t* rec = a.rec + (bh * P.NC + c) * REC_BYTES;
+    uint8_t* rec2 = a.rec2 ? a.rec2 + (bh * P.NC + c) * REC2_BYTES : nullptr;
+
+    // G = K K^T (rows 0-63) and Q K^T (rows 64-127) in one M=128 product on the raw bf16
+    // operands; the norm factors are applied in the epilogue, so they are computed meanwhile
     if (tid == 0) {
-        mbar_expect_tx(&bar_tma, 6 * 8192);
-        tma_load_4d(sm + PS_KQ + 0, &mk, 0, hk, t0, b, &bar_tma);
-        tma_load_4d(sm + PS_KQ + 16384, &mk, 64, hk, t0, b, &bar_tma);
-        tma_load_4d(sm + PS_KQ + 8192, &mq, 0, hk, t0, b, &bar_tma);
-        tma_load_4d(sm + PS_KQ + 24576, &mq, 64, hk, t0, b, &bar_tma);
-        tma_load_4d(sm + PS_V + 0, &mv, 0, hv, t0, b, &bar_tma);
-        tma_load_4d(sm + PS_V + 8192, &mv, 64, hv, t0, b, &bar_tma);
+        tc_fence_after();
+        const uint32_t id = idesc_bf16(128, 64, 0, 0);
+        for (int k0 = 0; k0 < kD; k0 += 16)
+            mma_bf16(tm, desc_kmajor(sb + PS_KQ, 128, 0, k0), desc_kmajor(sb + PS_KQ, 128, 0, k0), id, k0 > 0);
+        mma_commit(&bar_mma);
     }
     // gates of the chunk; tokens past T act as g = 0, beta = 0 (state passes unchanged)
     if (tid < 64) {
@@ -119,21 +158,7 @@ __global__ void __launch_bounds__(256, 2)
         gam[tid] = gv;
         bet[tid] = bv;
     }
-    __syncthreads();
-    if (tid >= 32 && tid < 64) gam[tid] += gam[31];
-    bool ok = mbar_wait(&bar_tma, 0, &abort_sh, a.status, 10);
-    if (__syncthreads_or(!ok)) goto teardown;
-
-    // G = K K^T (rows 0-63) and Q K^T (rows 64-127) in one M=128 product on the raw bf16
-    // operands; the norm factors are applied in the epilogue, so they are computed meanwhile
-    if (tid == 0) {
-        tc_fence_after();
-        const uint32_t id = idesc_bf16(128, 64, 0, 0);
-        for (int k0 = 0; k0 < kD; k0 += 16)
-            mma_bf16(tm, desc_kmajor(sb + PS_KQ, 128, 0, k0), desc_kmajor(sb + PS_KQ, 128, 0, k0), id, k0 > 0);
-        mma_commit(&bar_mma);
-    }
-    {  // L2 norm factors of the 64 keys (rows 0-63) and 64 queries (rows 64-127)
+    if (hh == 0) {  // L2 norm factors of the 64 keys (rows 0-63) and 64 queries (rows 64-127)
         const int row = tid >> 1, half = tid & 1;
         const uint32_t base = sb + PS_KQ + half * 16384 + row * 128;
         float ss = 0.f;
@@ -148,6 +173,8 @@ __global__ void __launch_bounds__(256, 2)
         if (half == 0) rho[row] = P.use_norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
     }
     __syncthreads();
+    if (tid >= 32 && tid < 64) gam[tid] += gam[31];
+    __syncthreads();
     if (tid < 64) {
         const float G = expf(gam[tid]);
         fw[tid] = bet[tid] * G * rho[tid];
@@ -155,7 +182,8 @@ __global__ void __launch_bounds__(256, 2)
         fq[tid] = P.scale * G * rho[64 + tid];
     }
 
-    ok = mbar_wait(&bar_mma, 0, &abort_sh, a.status, 11);
+    ok = mbar_wait(&bar_mma, mph, &abort_sh, a.status, 11);
+    mph ^= 1;
     if (__syncthreads_or(!ok)) goto teardown;
     tc_fence_after();
     {  // A = strict_lower(beta_i rho_i rho_j E_ij G_ij) in fp32;  P = scale tril(rho rho E S) in bf16
@@ -284,16 +312,28 @@ __global__ void __launch_bounds__(256, 2)
     // rows 64-127 of the second are the wanted ones; an M=64 product would take as long and
     // leave half of every warp idle in the epilogue). B operands: raw k / v tiles, MN-major.
     if (tid == 0) {
-        tc_fence_after();
-        const uint32_t id = idesc_bf16(128, 128, 0, 1);
-        for (int k0 = 0; k0 < kChunk; k0 += 16) {
-            mma_bf16(tm + 0, desc_kmajor(sb + PS_TT, 128, 0, k0), desc_mnmajor(sb + PS_KQ, 128, 0, k0), id, k0 > 0);
-            mma_bf16(tm + 128, desc_kmajor(sb + PS_TT, 128, 0, k0), desc_mnmajor(sb + PS_V, 64, 0, k0), id, k0 > 0);
+        // v of this value head (prefetched while the previous head was finishing)
+        if (mbar_wait(&bar_v, v_ph, &abort_sh, a.status, 14)) {
+            v_pend = false;
+            tc_fence_after();
+            const uint32_t id = idesc_bf16(128, 128, 0, 1);
+            for (int k0 = 0; k0 < kChunk; k0 += 16) {
+                mma_bf16(tm + 0, desc_kmajor(sb + PS_TT, 128, 0, k0), desc_mnmajor(sb + PS_KQ, 128, 0, k0), id,
+                         k0 > 0);
+                mma_bf16(tm + 128, desc_kmajor(sb + PS_TT, 128, 0, k0), desc_mnmajor(sb + PS_V, 64, 0, k0), id,
+                         k0 > 0);
+            }
+            mma_commit(&bar_mma);
+            v_ph ^= 1;
         }
-        mma_commit(&bar_mma);
     }
-    ok = mbar_wait(&bar_mma, 1, &abort_sh, a.status, 12);
+    ok = mbar_wait(&bar_mma, mph, &abort_sh, a.status, 12);
+    mph ^= 1;
     if (__syncthreads_or(!ok)) goto teardown;
+    if (tid == 0) {  // v is consumed: fetch the next value head's (or the next group's first)
+        if (hh + 1 < G) issue_v(grp, hh + 1);
+        else if (next < ngroups) issue_v(next, 0);
+    }
     tc_fence_after();
     {
         const int lg = warp & 3, h = warp >> 2;
@@ -357,7 +397,8 @@ __global__ void __launch_bounds__(256, 2)
             mma_bf16(tm + 128, desc_kmajor(sb + PS_P, 64, 0, k0), desc_mnmajor(sb + PS_W, 64, 0, k0), idp, k0 > 0);
         mma_commit(&bar_mma);
     }
-    ok = mbar_wait(&bar_mma, 0, &abort_sh, a.status, 13);
+    ok = mbar_wait(&bar_mma, mph, &abort_sh, a.status, 13);
+    mph ^= 1;
     if (__syncthreads_or(!ok)) goto teardown;
     tc_fence_after();
     {
@@ -394,12 +435,19 @@ __global__ void __launch_bounds__(256, 2)
         }
     }
     if (tid == 0) a.gam[bh * a.ncpad + c] = expf(gam[63]);
+    tc_fence_before();
+    __syncthreads();  // every buffer of this value head is free again
+    tc_fence_after();
+    }  // value heads of the group
+    if (tid == 0 && next < ngroups) issue_kq(next);  // k, q are no longer read
+    }  // groups
 teardown:
     tc_fence_before();
     __syncthreads();
     if (abort_sh && tid == 0) {  // let copies still in flight land before the CTA exits
         volatile int never = 0;
-        mbar_wait(&bar_tma, 0, &never, nullptr, 0);
+        if (kq_pend) mbar_wait(&bar_kq, kq_ph, &never, nullptr, 0);
+        if (v_pend) mbar_wait(&bar_v, v_ph, &never, nullptr, 0);
     }
     __syncthreads();
     if (warp == 0) tmem_dealloc(tm, 256);
@@ -410,7 +458,14 @@ cudaError_t launch_prep(const PrepArgs& a, const CUtensorMap& mq, const CUtensor
     const int smem = PS_BYTES + 1024;
     cudaError_t e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    dim3 grid(a.p.NC, a.p.Hv, a.p.B);
+    static int nsm = 0;  // 2 CTAs fit an SM (smem, TMEM, registers): a persistent grid of 2 per SM
+    if (nsm == 0) {
+        int dev = 0;
+        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+        if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    }
+    const int ngroups = a.p.B * a.p.Hk * a.p.NC;
+    dim3 grid(ngroups < 2 * nsm ? ngroups : 2 * nsm);
     trace_begin("chunk_prep", s);
     prep_kernel<<<grid, 256, smem, s>>>(mq, mk, mv, a);
     trace_end(s);

@@ -2,9 +2,10 @@
 //   prep_kernel : persistent, two CTAs per SM; a CTA takes (b, key head, chunk) groups in
 //                 turn and, for each, the value heads sharing that key head one after the
 //                 other (k, q and their norms loaded once per group; the next head's v is
-//                 fetched while the current head finishes). Builds each chunk's operators (UT/WY transform of the k k^T beta block, output and
-//                 state operators) on tcgen05 with TMEM accumulators and writes them as
-//                 ready-to-use shared-memory images.
+//                 fetched while the current head finishes). Builds each chunk's operators
+//                 (UT/WY transform of the k k^T beta block, output and state operators) on
+//                 tcgen05 with TMEM accumulators and writes them as ready-to-use
+//                 shared-memory images.
 //   scan_kernel : one CTA per (b, v-head, 32-column slice of the state). Runs the chunks
 //                 in order (or in reverse for the backward) with the fp32 state slice in
 //                 registers; per chunk one dependent tensor-core product.
@@ -118,328 +119,332 @@ __global__ void __launch_bounds__(256, 2)
     }
 
     for (int grp = blockIdx.x; grp < ngroups; grp += gridDim.x) {
-    const int c = grp % P.NC, hk = (grp / P.NC) % P.Hk, b = grp / (P.NC * P.Hk);
-    const int t0 = c * kChunk;
-    const int next = grp + (int)gridDim.x;
-    ok = mbar_wait(&bar_kq, kq_ph, &abort_sh, a.status, 10);
-    kq_ph ^= 1;
-    if (tid == 0) kq_pend = false;
-    if (__syncthreads_or(!ok)) goto teardown;
+        const int c = grp % P.NC, hk = (grp / P.NC) % P.Hk, b = grp / (P.NC * P.Hk);
+        const int t0 = c * kChunk;
+        const int next = grp + (int)gridDim.x;
+        ok = mbar_wait(&bar_kq, kq_ph, &abort_sh, a.status, 10);
+        kq_ph ^= 1;
+        if (tid == 0) kq_pend = false;
+        if (__syncthreads_or(!ok)) goto teardown;
 
-    for (int hh = 0; hh < G; hh++) {
-    const int hv = hk * G + hh;
-    const size_t bh = (size_t)b * P.Hv + hv;
-    uint8_t* rec = a.rec + (bh * P.NC + c) * REC_BYTES;
-    uint8_t* rec2 = a.rec2 ? a.rec2 + (bh * P.NC + c) * REC2_BYTES : nullptr;
+        for (int hh = 0; hh < G; hh++) {
+            const int hv = hk * G + hh;
+            const size_t bh = (size_t)b * P.Hv + hv;
+            uint8_t* rec = a.rec + (bh * P.NC + c) * REC_BYTES;
+            uint8_t* rec2 = a.rec2 ? a.rec2 + (bh * P.NC + c) * REC2_BYTES : nullptr;
 
-    // G = K K^T (rows 0-63) and Q K^T (rows 64-127) in one M=128 product on the raw bf16
-    // operands; the norm factors are applied in the epilogue, so they are computed meanwhile
-    if (tid == 0) {
-        tc_fence_after();
-        const uint32_t id = idesc_bf16(128, 64, 0, 0);
-        for (int k0 = 0; k0 < kD; k0 += 16)
-            mma_bf16(tm, desc_kmajor(sb + PS_KQ, 128, 0, k0), desc_kmajor(sb + PS_KQ, 128, 0, k0), id, k0 > 0);
-        mma_commit(&bar_mma);
-    }
-    // gates of the chunk; tokens past T act as g = 0, beta = 0 (state passes unchanged)
-    if (tid < 64) {
-        const int t = t0 + tid;
-        float gv = 0.f, bv = 0.f;
-        if (t < P.T) {
-            const size_t bt = ((size_t)b * P.T + t) * P.Hv + hv;
-            gv = a.g[bt];
-            bv = a.beta[bt];
-        }
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, gv, o);
-            if (lane >= o) gv += y;
-        }
-        gam[tid] = gv;
-        bet[tid] = bv;
-    }
-    if (hh == 0) {  // L2 norm factors of the 64 keys (rows 0-63) and 64 queries (rows 64-127)
-        const int row = tid >> 1, half = tid & 1;
-        const uint32_t base = sb + PS_KQ + half * 16384 + row * 128;
-        float ss = 0.f;
-#pragma unroll
-        for (int ch = 0; ch < 8; ch++) {  // physical chunk order rotated per thread: a quarter warp
-            float x[8];                   // (4 rows x 2 halves) then reads 8 distinct bank groups
-            unpack8(ld_shared_v4(base + ((ch + 2 * row + half) & 7) * 16), x);
-#pragma unroll
-            for (int e = 0; e < 8; e++) ss += x[e] * x[e];
-        }
-        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-        if (half == 0) rho[row] = P.use_norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
-    }
-    __syncthreads();
-    if (tid >= 32 && tid < 64) gam[tid] += gam[31];
-    __syncthreads();
-    if (tid < 64) {
-        const float G = expf(gam[tid]);
-        fw[tid] = bet[tid] * G * rho[tid];
-        fb[tid] = expf(gam[63] - gam[tid]) * rho[tid];
-        fq[tid] = P.scale * G * rho[64 + tid];
-    }
-
-    ok = mbar_wait(&bar_mma, mph, &abort_sh, a.status, 11);
-    mph ^= 1;
-    if (__syncthreads_or(!ok)) goto teardown;
-    tc_fence_after();
-    {  // A = strict_lower(beta_i rho_i rho_j E_ij G_ij) in fp32;  P = scale tril(rho rho E S) in bf16
-        const int lg = warp & 3, h = warp >> 2;
-        const int r = 32 * lg + lane;
-        float v[32];
-        tmem_ld32(tmem_at(tm, 32 * lg, 32 * h), v);
-        tmem_wait_ld();
-        // All loads first, then all stores: stores into the same shared memory in between
-        // would keep the compiler from overlapping the loads (it cannot rule out aliasing).
-        const bool arow = r < 64;  // warp-uniform
-        const int i = r & 63;
-        const int lim = arow ? i : i + 1;  // A: j < i (strict), P: j <= i
-        const float gi = gam[i], ci = arow ? bet[i] * rho[i] : P.scale * rho[64 + i];
-        const float4* g4 = reinterpret_cast<const float4*>(gam + 32 * h);
-        const float4* r4 = reinterpret_cast<const float4*>(rho + 32 * h);
-#pragma unroll
-        for (int q = 0; q < 8; q++) {
-            const float4 gg = g4[q], rr = r4[q];
-            const float gj[4] = {gg.x, gg.y, gg.z, gg.w}, rj[4] = {rr.x, rr.y, rr.z, rr.w};
-#pragma unroll
-            for (int e = 0; e < 4; e++) {
-                const int jj = 4 * q + e;
-                v[jj] = (32 * h + jj < lim) ? ci * rj[e] * __expf(gi - gj[e]) * v[jj] : 0.f;
+            // G = K K^T (rows 0-63) and Q K^T (rows 64-127) in one M=128 product on the raw bf16
+            // operands; the norm factors are applied in the epilogue, so they are computed meanwhile
+            if (tid == 0) {
+                tc_fence_after();
+                const uint32_t id = idesc_bf16(128, 64, 0, 0);
+                for (int k0 = 0; k0 < kD; k0 += 16)
+                    mma_bf16(tm, desc_kmajor(sb + PS_KQ, 128, 0, k0), desc_kmajor(sb + PS_KQ, 128, 0, k0), id, k0 > 0);
+                mma_commit(&bar_mma);
             }
-        }
-        if (arow) {
-#pragma unroll
-            for (int jj = 0; jj < 32; jj++) Am[i * LDA + 32 * h + jj] = v[jj];
-        } else {
-#pragma unroll
-            for (int q = 0; q < 4; q++) {
-                const uint4 u = pack8(v + 8 * q, 1.f);
-                const uint32_t off = sw128_chunk(i, 4 * h + q, 64);
-                st_shared_v4(sb + PS_P + off, u.x, u.y, u.z, u.w);
-                st_global16(rec + REC_P + off, u);
-            }
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
-
-    // T = (I + A)^-1 (unit lower triangular) by 16x16 blocks. Phase 1 (160 threads, one
-    // column each): forward substitution with L_II = I + A_II gives the diagonal inverses T_II
-    // (right-hand side e_c) and Y_IK = T_II A_IK for I > K (right-hand side column c of A_IK).
-    // Then T_IJ = -sum_{J<=K<I} Y_IK T_KJ by block distance I-J = 1, 2, 3.
-    if (tid < 160) {
-        int I, K, cc;
-        const bool diag = tid < 64;
-        if (diag) {
-            I = tid >> 4;
-            K = I;
-            cc = tid & 15;
-        } else {
-            const int pidx = (tid - 64) >> 4;  // pairs (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
-            cc = (tid - 64) & 15;
-            I = pidx == 0 ? 1 : (pidx < 3 ? 2 : 3);
-            K = pidx - I * (I - 1) / 2;
-        }
-        const float* Ab = Am + (16 * I) * LDA + 16 * I;
-        const float* Bc = Am + (16 * I) * LDA + 16 * K + cc;
-        float y[16];
-#pragma unroll
-        for (int i = 0; i < 16; i++) {
-            float s = diag ? (i == cc ? 1.f : 0.f) : Bc[i * LDA];
-#pragma unroll
-            for (int j = 0; j < i; j++) s -= Ab[i * LDA + j] * y[j];
-            y[i] = s;
-        }
-        if (diag) {
-#pragma unroll
-            for (int i = 0; i < 16; i++) Tm[(16 * I + i) * LDA + 16 * I + cc] = y[i];
-        } else {
-            float* yp = Xs + ((tid - 64) >> 4) * (16 * 17);
-#pragma unroll
-            for (int i = 0; i < 16; i++) yp[i * 17 + cc] = y[i];
-        }
-    }
-    __syncthreads();
-    for (int dlev = 1; dlev <= 3; dlev++) {  // item J of a level: block (J + dlev, J); all sums before any store
-        const int nb = 4 - dlev;
-        const int i = (tid >> 4) & 15, cc = tid & 15;
-        float s[3] = {0.f, 0.f, 0.f};
-#pragma unroll
-        for (int J = 0; J < 3; J++) {
-            if (J < nb) {
-                const int I = J + dlev;
-                for (int K = J; K < I; K++) {
-                    const float* yr = Xs + (I * (I - 1) / 2 + K) * (16 * 17) + i * 17;
-                    const float* tc = Tm + (16 * K) * LDA + 16 * J + cc;
-#pragma unroll
-                    for (int m = 0; m < 16; m++) s[J] += yr[m] * tc[m * LDA];
+            // gates of the chunk; tokens past T act as g = 0, beta = 0 (state passes unchanged)
+            if (tid < 64) {
+                const int t = t0 + tid;
+                float gv = 0.f, bv = 0.f;
+                if (t < P.T) {
+                    const size_t bt = ((size_t)b * P.T + t) * P.Hv + hv;
+                    gv = a.g[bt];
+                    bv = a.beta[bt];
                 }
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, gv, o);
+                    if (lane >= o) gv += y;
+                }
+                gam[tid] = gv;
+                bet[tid] = bv;
             }
-        }
+            if (hh == 0) {  // L2 norm factors of the 64 keys (rows 0-63) and 64 queries (rows 64-127)
+                const int row = tid >> 1, half = tid & 1;
+                const uint32_t base = sb + PS_KQ + half * 16384 + row * 128;
+                float ss = 0.f;
 #pragma unroll
-        for (int J = 0; J < 3; J++)
-            if (J < nb) Tm[(16 * (J + dlev) + i) * LDA + 16 * J + cc] = -s[J];
-        __syncthreads();
-    }
-    {  // [Tw; Tu] with Tw = T diag(beta Gamma rho_k), Tu = T diag(beta): K-major A operand (over A).
-       // T's blocks above the block diagonal are zero and never stored: masked here.
-        const int row = tid >> 1, half = tid & 1;
-        const int i = row & 63;
-        const bool isw = row < 64;
-        const float* trow = Tm + i * LDA + 32 * half;
-        const float* fac = (isw ? fw : bet) + 32 * half;
-        float t[32], x[32];
+                for (int ch = 0; ch < 8; ch++) {  // physical chunk order rotated per thread: a quarter warp
+                    float x[8];                   // (4 rows x 2 halves) then reads 8 distinct bank groups
+                    unpack8(ld_shared_v4(base + ((ch + 2 * row + half) & 7) * 16), x);
 #pragma unroll
-        for (int jj = 0; jj < 32; jj++) {  // all loads first (see the A/P epilogue)
-            const int j = 32 * half + jj;
-            t[jj] = (j >> 4) <= (i >> 4) ? trow[jj] : 0.f;
-            x[jj] = t[jj] * fac[jj];
-        }
-#pragma unroll
-        for (int q = 0; q < 4; q++) {
-            st_chunk(sb + PS_TT + sw128_chunk(row, 4 * half + q, 128), x + 8 * q, 1.f);
-            if (isw && rec2)  // T itself for the backward
-                st_global16(rec2 + REC2_T + sw128_chunk(i, 4 * half + q, 64), pack8(t + 8 * q, 1.f));
-        }
-    }
-    fence_proxy_async_smem();
-    __syncthreads();
+                    for (int e = 0; e < 8; e++) ss += x[e] * x[e];
+                }
+                ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+                if (half == 0) rho[row] = P.use_norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
+            }
+            __syncthreads();
+            if (tid >= 32 && tid < 64) gam[tid] += gam[31];
+            __syncthreads();
+            if (tid < 64) {
+                const float G = expf(gam[tid]);
+                fw[tid] = bet[tid] * G * rho[tid];
+                fb[tid] = expf(gam[63] - gam[tid]) * rho[tid];
+                fq[tid] = P.scale * G * rho[64 + tid];
+            }
 
-    // W = Tw K and U~ = Tu V as two M=128 products of [Tw; Tu] (rows 0-63 of the first and
-    // rows 64-127 of the second are the wanted ones; an M=64 product would take as long and
-    // leave half of every warp idle in the epilogue). B operands: raw k / v tiles, MN-major.
-    if (tid == 0) {
-        // v of this value head (prefetched while the previous head was finishing)
-        if (mbar_wait(&bar_v, v_ph, &abort_sh, a.status, 14)) {
-            v_pend = false;
+            ok = mbar_wait(&bar_mma, mph, &abort_sh, a.status, 11);
+            mph ^= 1;
+            if (__syncthreads_or(!ok)) goto teardown;
             tc_fence_after();
-            const uint32_t id = idesc_bf16(128, 128, 0, 1);
-            for (int k0 = 0; k0 < kChunk; k0 += 16) {
-                mma_bf16(tm + 0, desc_kmajor(sb + PS_TT, 128, 0, k0), desc_mnmajor(sb + PS_KQ, 128, 0, k0), id,
-                         k0 > 0);
-                mma_bf16(tm + 128, desc_kmajor(sb + PS_TT, 128, 0, k0), desc_mnmajor(sb + PS_V, 64, 0, k0), id,
-                         k0 > 0);
-            }
-            mma_commit(&bar_mma);
-            v_ph ^= 1;
-        }
-    }
-    ok = mbar_wait(&bar_mma, mph, &abort_sh, a.status, 12);
-    mph ^= 1;
-    if (__syncthreads_or(!ok)) goto teardown;
-    if (tid == 0) {  // v is consumed: fetch the next value head's (or the next group's first)
-        if (hh + 1 < G) issue_v(grp, hh + 1);
-        else if (next < ngroups) issue_v(next, 0);
-    }
-    tc_fence_after();
-    {
-        const int lg = warp & 3, h = warp >> 2;
-        if (lg < 2) {  // W rows i = 32 lg + lane (first product, columns 64 h ..)
-            const int i = 32 * lg + lane;
-            float w[64];
-            tmem_ld32(tmem_at(tm, 32 * lg, 64 * h), w);
-            tmem_ld32(tmem_at(tm, 32 * lg, 64 * h + 32), w + 32);
-            tmem_wait_ld();
-            const float sbar = fb[i];
-#pragma unroll
-            for (int q = 0; q < 8; q++) {
-                const uint4 u = pack8(w + 8 * q, 1.f);
-                const uint32_t off = sw128_chunk(i, 8 * h + q, 64);
-                st_shared_v4(sb + PS_W + off, u.x, u.y, u.z, u.w);
-                if (rec2) st_global16(rec2 + REC2_W + off, u);
-                st_chunk(sb + PS_WBAR + off, w + 8 * q, sbar);
-            }
-        } else {  // U~ rows i = 32 lg + lane - 64 (second product)
-            const int i = 32 * lg + lane - 64;
-            float u[64];
-            tmem_ld32(tmem_at(tm, 32 * lg, 128 + 64 * h), u);
-            tmem_ld32(tmem_at(tm, 32 * lg, 128 + 64 * h + 32), u + 32);
-            tmem_wait_ld();
-#pragma unroll
-            for (int q = 0; q < 8; q++) {
-                const int col = 64 * h + 8 * q;
-                st_global16(rec + REC_U + (col >> 5) * 4096 + sw64_chunk(i, q & 3), pack8(u + 8 * q, 1.f));
-            }
-        }
-        // Kbar = diag(exp(gamma_C - gamma) rho_k) K, straight to the record
-        {
-            uint4 kv[4];
-#pragma unroll
-            for (int n = 0; n < 4; n++) {
-                const int idx = tid + 256 * n, r = idx >> 4, j = idx & 15;
-                kv[n] = ld_shared_v4(sb + PS_KQ + sw128_chunk(r, j, 128));
-            }
-#pragma unroll
-            for (int n = 0; n < 4; n++) {
-                const int idx = tid + 256 * n, r = idx >> 4, j = idx & 15;
-                float x[8];
-                unpack8(kv[n], x);
-                st_global16(rec + REC_K + sw128_chunk(r, j, 64), pack8(x, fb[r]));
-            }
-        }
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-
-    // Mneg = -K^T Wbar (M=128: A = k tile read MN-major) and P W (M=64)
-    if (tid == 0) {
-        tc_fence_after();
-        const uint32_t idm = idesc_bf16(128, 128, 1, 1);
-        for (int k0 = 0; k0 < kChunk; k0 += 16)
-            mma_bf16(tm + 0, desc_mnmajor(sb + PS_KQ, 128, 0, k0), desc_mnmajor(sb + PS_WBAR, 64, 0, k0), idm,
-                     k0 > 0);
-        const uint32_t idp = idesc_bf16(64, 128, 0, 1);
-        for (int k0 = 0; k0 < kChunk; k0 += 16)
-            mma_bf16(tm + 128, desc_kmajor(sb + PS_P, 64, 0, k0), desc_mnmajor(sb + PS_W, 64, 0, k0), idp, k0 > 0);
-        mma_commit(&bar_mma);
-    }
-    ok = mbar_wait(&bar_mma, mph, &abort_sh, a.status, 13);
-    mph ^= 1;
-    if (__syncthreads_or(!ok)) goto teardown;
-    tc_fence_after();
-    {
-        const int lg = warp & 3, h = warp >> 2;
-        {  // Mneg rows d = 32 lg + lane
-            const int d = 32 * lg + lane;
-            float m[64];
-            tmem_ld32(tmem_at(tm, 32 * lg, 64 * h), m);
-            tmem_ld32(tmem_at(tm, 32 * lg, 64 * h + 32), m + 32);
-            tmem_wait_ld();
-#pragma unroll
-            for (int q = 0; q < 8; q++) st_global16(rec + REC_M + sw128_chunk(d, 8 * h + q, 128), pack8(m + 8 * q, -1.f));
-        }
-        {  // Qc = scale diag(Gamma rho_q) Q - P W, rows i = 16 lg + lane
-            const int i = 16 * lg + (lane & 15);
-            float pw[64];
-            tmem_ld32(tmem_at(tm, 32 * lg, 128 + 64 * h), pw);
-            tmem_ld32(tmem_at(tm, 32 * lg, 128 + 64 * h + 32), pw + 32);
-            tmem_wait_ld();
-            if (lane < 16) {
-                const float f = fq[i];
-                uint4 qv[8];
-#pragma unroll
-                for (int q = 0; q < 8; q++) qv[q] = ld_shared_v4(sb + PS_KQ + sw128_chunk(64 + i, 8 * h + q, 128));
+            {  // A = strict_lower(beta_i rho_i rho_j E_ij G_ij) in fp32;  P = scale tril(rho rho E S) in bf16
+                const int lg = warp & 3, h = warp >> 2;
+                const int r = 32 * lg + lane;
+                float v[32];
+                tmem_ld32(tmem_at(tm, 32 * lg, 32 * h), v);
+                tmem_wait_ld();
+                // All loads first, then all stores: stores into the same shared memory in between
+                // would keep the compiler from overlapping the loads (it cannot rule out aliasing).
+                const bool arow = r < 64;  // warp-uniform
+                const int i = r & 63;
+                const int lim = arow ? i : i + 1;  // A: j < i (strict), P: j <= i
+                const float gi = gam[i], ci = arow ? bet[i] * rho[i] : P.scale * rho[64 + i];
+                const float4* g4 = reinterpret_cast<const float4*>(gam + 32 * h);
+                const float4* r4 = reinterpret_cast<const float4*>(rho + 32 * h);
 #pragma unroll
                 for (int q = 0; q < 8; q++) {
-                    float x[8];
-                    unpack8(qv[q], x);
+                    const float4 gg = g4[q], rr = r4[q];
+                    const float gj[4] = {gg.x, gg.y, gg.z, gg.w}, rj[4] = {rr.x, rr.y, rr.z, rr.w};
 #pragma unroll
-                    for (int e = 0; e < 8; e++) x[e] = f * x[e] - pw[8 * q + e];
-                    st_global16(rec + REC_Q + sw128_chunk(i, 8 * h + q, 64), pack8(x, 1.f));
+                    for (int e = 0; e < 4; e++) {
+                        const int jj = 4 * q + e;
+                        v[jj] = (32 * h + jj < lim) ? ci * rj[e] * __expf(gi - gj[e]) * v[jj] : 0.f;
+                    }
+                }
+                if (arow) {
+#pragma unroll
+                    for (int jj = 0; jj < 32; jj++) Am[i * LDA + 32 * h + jj] = v[jj];
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+                        const uint4 u = pack8(v + 8 * q, 1.f);
+                        const uint32_t off = sw128_chunk(i, 4 * h + q, 64);
+                        st_shared_v4(sb + PS_P + off, u.x, u.y, u.z, u.w);
+                        st_global16(rec + REC_P + off, u);
+                    }
                 }
             }
-        }
-    }
-    if (tid == 0) a.gam[bh * a.ncpad + c] = expf(gam[63]);
-    tc_fence_before();
-    __syncthreads();  // every buffer of this value head is free again
-    tc_fence_after();
-    }  // value heads of the group
-    if (tid == 0 && next < ngroups) issue_kq(next);  // k, q are no longer read
+            tc_fence_before();
+            __syncthreads();
+
+            // T = (I + A)^-1 (unit lower triangular) by 16x16 blocks. Phase 1 (160 threads, one
+            // column each): forward substitution with L_II = I + A_II gives the diagonal inverses T_II
+            // (right-hand side e_c) and Y_IK = T_II A_IK for I > K (right-hand side column c of A_IK).
+            // Then T_IJ = -sum_{J<=K<I} Y_IK T_KJ by block distance I-J = 1, 2, 3.
+            if (tid < 160) {
+                int I, K, cc;
+                const bool diag = tid < 64;
+                if (diag) {
+                    I = tid >> 4;
+                    K = I;
+                    cc = tid & 15;
+                } else {
+                    const int pidx = (tid - 64) >> 4;  // pairs (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
+                    cc = (tid - 64) & 15;
+                    I = pidx == 0 ? 1 : (pidx < 3 ? 2 : 3);
+                    K = pidx - I * (I - 1) / 2;
+                }
+                const float* Ab = Am + (16 * I) * LDA + 16 * I;
+                const float* Bc = Am + (16 * I) * LDA + 16 * K + cc;
+                float y[16];
+#pragma unroll
+                for (int i = 0; i < 16; i++) {
+                    float s = diag ? (i == cc ? 1.f : 0.f) : Bc[i * LDA];
+#pragma unroll
+                    for (int j = 0; j < i; j++) s -= Ab[i * LDA + j] * y[j];
+                    y[i] = s;
+                }
+                if (diag) {
+#pragma unroll
+                    for (int i = 0; i < 16; i++) Tm[(16 * I + i) * LDA + 16 * I + cc] = y[i];
+                } else {
+                    float* yp = Xs + ((tid - 64) >> 4) * (16 * 17);
+#pragma unroll
+                    for (int i = 0; i < 16; i++) yp[i * 17 + cc] = y[i];
+                }
+            }
+            __syncthreads();
+            // item J of a level is block (J + dlev, J); all sums are formed before any store
+            for (int dlev = 1; dlev <= 3; dlev++) {
+                const int nb = 4 - dlev;
+                const int i = (tid >> 4) & 15, cc = tid & 15;
+                float s[3] = {0.f, 0.f, 0.f};
+#pragma unroll
+                for (int J = 0; J < 3; J++) {
+                    if (J < nb) {
+                        const int I = J + dlev;
+                        for (int K = J; K < I; K++) {
+                            const float* yr = Xs + (I * (I - 1) / 2 + K) * (16 * 17) + i * 17;
+                            const float* tc = Tm + (16 * K) * LDA + 16 * J + cc;
+#pragma unroll
+                            for (int m = 0; m < 16; m++) s[J] += yr[m] * tc[m * LDA];
+                        }
+                    }
+                }
+#pragma unroll
+                for (int J = 0; J < 3; J++)
+                    if (J < nb) Tm[(16 * (J + dlev) + i) * LDA + 16 * J + cc] = -s[J];
+                __syncthreads();
+            }
+            {  // [Tw; Tu] with Tw = T diag(beta Gamma rho_k), Tu = T diag(beta): K-major A operand (over A).
+               // T's blocks above the block diagonal are zero and never stored: masked here.
+                const int row = tid >> 1, half = tid & 1;
+                const int i = row & 63;
+                const bool isw = row < 64;
+                const float* trow = Tm + i * LDA + 32 * half;
+                const float* fac = (isw ? fw : bet) + 32 * half;
+                float t[32], x[32];
+#pragma unroll
+                for (int jj = 0; jj < 32; jj++) {  // all loads first (see the A/P epilogue)
+                    const int j = 32 * half + jj;
+                    t[jj] = (j >> 4) <= (i >> 4) ? trow[jj] : 0.f;
+                    x[jj] = t[jj] * fac[jj];
+                }
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    st_chunk(sb + PS_TT + sw128_chunk(row, 4 * half + q, 128), x + 8 * q, 1.f);
+                    if (isw && rec2)  // T itself for the backward
+                        st_global16(rec2 + REC2_T + sw128_chunk(i, 4 * half + q, 64), pack8(t + 8 * q, 1.f));
+                }
+            }
+            fence_proxy_async_smem();
+            __syncthreads();
+
+            // W = Tw K and U~ = Tu V as two M=128 products of [Tw; Tu] (rows 0-63 of the first and
+            // rows 64-127 of the second are the wanted ones; an M=64 product would take as long and
+            // leave half of every warp idle in the epilogue). B operands: raw k / v tiles, MN-major.
+            if (tid == 0) {
+                // v of this value head (prefetched while the previous head was finishing)
+                if (mbar_wait(&bar_v, v_ph, &abort_sh, a.status, 14)) {
+                    v_pend = false;
+                    tc_fence_after();
+                    const uint32_t id = idesc_bf16(128, 128, 0, 1);
+                    for (int k0 = 0; k0 < kChunk; k0 += 16) {
+                        mma_bf16(tm + 0, desc_kmajor(sb + PS_TT, 128, 0, k0), desc_mnmajor(sb + PS_KQ, 128, 0, k0), id,
+                                 k0 > 0);
+                        mma_bf16(tm + 128, desc_kmajor(sb + PS_TT, 128, 0, k0), desc_mnmajor(sb + PS_V, 64, 0, k0), id,
+                                 k0 > 0);
+                    }
+                    mma_commit(&bar_mma);
+                    v_ph ^= 1;
+                }
+            }
+            ok = mbar_wait(&bar_mma, mph, &abort_sh, a.status, 12);
+            mph ^= 1;
+            if (__syncthreads_or(!ok)) goto teardown;
+            if (tid == 0) {  // v is consumed: fetch the next value head's (or the next group's first)
+                if (hh + 1 < G) issue_v(grp, hh + 1);
+                else if (next < ngroups) issue_v(next, 0);
+            }
+            tc_fence_after();
+            {
+                const int lg = warp & 3, h = warp >> 2;
+                if (lg < 2) {  // W rows i = 32 lg + lane (first product, columns 64 h ..)
+                    const int i = 32 * lg + lane;
+                    float w[64];
+                    tmem_ld32(tmem_at(tm, 32 * lg, 64 * h), w);
+                    tmem_ld32(tmem_at(tm, 32 * lg, 64 * h + 32), w + 32);
+                    tmem_wait_ld();
+                    const float sbar = fb[i];
+#pragma unroll
+                    for (int q = 0; q < 8; q++) {
+                        const uint4 u = pack8(w + 8 * q, 1.f);
+                        const uint32_t off = sw128_chunk(i, 8 * h + q, 64);
+                        st_shared_v4(sb + PS_W + off, u.x, u.y, u.z, u.w);
+                        if (rec2) st_global16(rec2 + REC2_W + off, u);
+                        st_chunk(sb + PS_WBAR + off, w + 8 * q, sbar);
+                    }
+                } else {  // U~ rows i = 32 lg + lane - 64 (second product)
+                    const int i = 32 * lg + lane - 64;
+                    float u[64];
+                    tmem_ld32(tmem_at(tm, 32 * lg, 128 + 64 * h), u);
+                    tmem_ld32(tmem_at(tm, 32 * lg, 128 + 64 * h + 32), u + 32);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int q = 0; q < 8; q++) {
+                        const int col = 64 * h + 8 * q;
+                        st_global16(rec + REC_U + (col >> 5) * 4096 + sw64_chunk(i, q & 3), pack8(u + 8 * q, 1.f));
+                    }
+                }
+                // Kbar = diag(exp(gamma_C - gamma) rho_k) K, straight to the record
+                {
+                    uint4 kv[4];
+#pragma unroll
+                    for (int n = 0; n < 4; n++) {
+                        const int idx = tid + 256 * n, r = idx >> 4, j = idx & 15;
+                        kv[n] = ld_shared_v4(sb + PS_KQ + sw128_chunk(r, j, 128));
+                    }
+#pragma unroll
+                    for (int n = 0; n < 4; n++) {
+                        const int idx = tid + 256 * n, r = idx >> 4, j = idx & 15;
+                        float x[8];
+                        unpack8(kv[n], x);
+                        st_global16(rec + REC_K + sw128_chunk(r, j, 64), pack8(x, fb[r]));
+                    }
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncthreads();
+
+            // Mneg = -K^T Wbar (M=128: A = k tile read MN-major) and P W (M=64)
+            if (tid == 0) {
+                tc_fence_after();
+                const uint32_t idm = idesc_bf16(128, 128, 1, 1);
+                for (int k0 = 0; k0 < kChunk; k0 += 16)
+                    mma_bf16(tm + 0, desc_mnmajor(sb + PS_KQ, 128, 0, k0), desc_mnmajor(sb + PS_WBAR, 64, 0, k0), idm,
+                             k0 > 0);
+                const uint32_t idp = idesc_bf16(64, 128, 0, 1);
+                for (int k0 = 0; k0 < kChunk; k0 += 16)
+                    mma_bf16(tm + 128, desc_kmajor(sb + PS_P, 64, 0, k0), desc_mnmajor(sb + PS_W, 64, 0, k0), idp,
+                             k0 > 0);
+                mma_commit(&bar_mma);
+            }
+            ok = mbar_wait(&bar_mma, mph, &abort_sh, a.status, 13);
+            mph ^= 1;
+            if (__syncthreads_or(!ok)) goto teardown;
+            tc_fence_after();
+            {
+                const int lg = warp & 3, h = warp >> 2;
+                {  // Mneg rows d = 32 lg + lane
+                    const int d = 32 * lg + lane;
+                    float m[64];
+                    tmem_ld32(tmem_at(tm, 32 * lg, 64 * h), m);
+                    tmem_ld32(tmem_at(tm, 32 * lg, 64 * h + 32), m + 32);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int q = 0; q < 8; q++)
+                        st_global16(rec + REC_M + sw128_chunk(d, 8 * h + q, 128), pack8(m + 8 * q, -1.f));
+                }
+                {  // Qc = scale diag(Gamma rho_q) Q - P W, rows i = 16 lg + lane
+                    const int i = 16 * lg + (lane & 15);
+                    float pw[64];
+                    tmem_ld32(tmem_at(tm, 32 * lg, 128 + 64 * h), pw);
+                    tmem_ld32(tmem_at(tm, 32 * lg, 128 + 64 * h + 32), pw + 32);
+                    tmem_wait_ld();
+                    if (lane < 16) {
+                        const float f = fq[i];
+                        uint4 qv[8];
+#pragma unroll
+                        for (int q = 0; q < 8; q++)
+                            qv[q] = ld_shared_v4(sb + PS_KQ + sw128_chunk(64 + i, 8 * h + q, 128));
+#pragma unroll
+                        for (int q = 0; q < 8; q++) {
+                            float x[8];
+                            unpack8(qv[q], x);
+#pragma unroll
+                            for (int e = 0; e < 8; e++) x[e] = f * x[e] - pw[8 * q + e];
+                            st_global16(rec + REC_Q + sw128_chunk(i, 8 * h + q, 64), pack8(x, 1.f));
+                        }
+                    }
+                }
+            }
+            if (tid == 0) a.gam[bh * a.ncpad + c] = expf(gam[63]);
+            tc_fence_before();
+            __syncthreads();  // every buffer of this value head is free again
+            tc_fence_after();
+        }  // value heads of the group
+        if (tid == 0 && next < ngroups) issue_kq(next);  // k, q are no longer read
     }  // groups
 teardown:
     tc_fence_before();

@@ -48,9 +48,10 @@ gdr_status check_ptrs(const gdr_problem* p, std::initializer_list<const void*> r
 
 // The chunked kernels are written for bf16 operands on the tensor cores, 128-wide heads
 // and the scalar gate.
-gdr_status check_chunked_support(const gdr_problem* p) {
-    if (p->dtype != GDR_BF16 || p->Dk != 128 || p->Dv != 128 || p->gate != GDR_GATE_SCALAR)
-        return GDR_ERR_UNSUPPORTED;
+// The tensor-core chunked path: bf16, Dk = Dv = 128; the per-channel gate in the forward only.
+gdr_status check_chunked_support(const gdr_problem* p, bool channel_ok = false) {
+    if (p->dtype != GDR_BF16 || p->Dk != 128 || p->Dv != 128) return GDR_ERR_UNSUPPORTED;
+    if (p->gate != GDR_GATE_SCALAR && !(channel_ok && p->gate == GDR_GATE_CHANNEL)) return GDR_ERR_UNSUPPORTED;
     return GDR_OK;
 }
 
@@ -72,6 +73,7 @@ ChunkProblem chunk_problem(const gdr_problem* p) {
     c.NC = (p->T + kChunk - 1) / kChunk;
     c.scale = p->scale;
     c.use_norm = p->use_qk_l2norm;
+    c.channel = p->gate == GDR_GATE_CHANNEL;
     return c;
 }
 
@@ -148,7 +150,7 @@ const char* gdr_status_string(gdr_status s) {
 }
 
 size_t gdr_fwd_chunked_workspace(const gdr_problem* p) {
-    if (check_problem(p, false) != GDR_OK || check_chunked_support(p) != GDR_OK) return 0;
+    if (check_problem(p, false) != GDR_OK || check_chunked_support(p, true) != GDR_OK) return 0;
     return chunk_fwd_workspace(chunk_problem(p));
 }
 
@@ -243,7 +245,7 @@ static gdr_status fwd_chunked_impl(const gdr_problem* p, const void* q, const vo
     gdr_status s = check_problem(p, false);
     if (s != GDR_OK) return s;
     if ((s = check_ptrs(p, {q, k, v, g, beta, o}, {h0, ht})) != GDR_OK) return s;
-    if ((s = check_chunked_support(p)) != GDR_OK) return s;
+    if ((s = check_chunked_support(p, !states && !saved)) != GDR_OK) return s;
     const size_t need = saved ? kSavedFwdWorkspace : chunk_fwd_workspace(chunk_problem(p));
     if (!ws || ws_bytes < need) return GDR_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return GDR_ERR_INVALID_ARG;

@@ -40,10 +40,11 @@ struct ChunkProblem {
     int B, T, Hk, Hv, NC;
     float scale;
     int use_norm;
+    int channel;  // per-channel gate g [B,T,Hv,Dk] (forward only); else one gate per head
 };
 
 struct WsLayout {
-    size_t gam;      // float [B*Hv][ncpad]: Gamma_C per chunk
+    size_t gam;      // float [B*Hv][ncpad]: Gamma_C per chunk ([B*Hv][NC][Dk] per channel)
     size_t rec;      // records [B*Hv][NC]
     size_t rec2;     // bwd: T and W per chunk [B*Hv][NC]
     size_t hs;       // bwd: chunk-start states [B*Hv][NC] images
@@ -60,7 +61,8 @@ inline WsLayout ws_layout(const ChunkProblem& p, bool bwd, bool bwd_states = fal
     w.ncpad = (int)round_up((size_t)p.NC, 4);
     size_t nh = (size_t)p.B * p.Hv;
     w.gam = 256;
-    w.rec = round_up(w.gam + nh * w.ncpad * sizeof(float), 1024);
+    const size_t ngam = p.channel ? (size_t)p.NC * kD : (size_t)w.ncpad;
+    w.rec = round_up(w.gam + nh * ngam * sizeof(float), 1024);
     size_t end = w.rec + nh * p.NC * (size_t)REC_BYTES;
     w.rec2 = w.hs = w.dhs = 0;
     if (bwd) {
@@ -142,6 +144,9 @@ struct PrepArgs {
 };
 cudaError_t launch_prep(const PrepArgs& a, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                         cudaStream_t s);
+// Per-channel gate (chunk_fwd_ch.cu): same record, Gamma_C as [B*Hv][NC][Dk].
+cudaError_t launch_prep_ch(const PrepArgs& a, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                           cudaStream_t s);
 
 enum ScanMode : int { SCAN_FWD_OUT = 0, SCAN_FWD_STATES = 1, SCAN_BWD = 2 };
 struct ScanArgs {

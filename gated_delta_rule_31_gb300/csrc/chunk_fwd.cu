@@ -18,6 +18,7 @@
 #include <stdint.h>
 
 #include "chunk.h"
+#include "chunk_dev.cuh"
 #include "common.cuh"
 #include "kernels.h"
 #include "tma_host.h"
@@ -29,7 +30,6 @@ namespace gdr {
 // the record images go straight from registers to global memory, nothing is staged.
 constexpr uint32_t PS_KQ = 0;        // k rows 0-63 / q rows 64-127 of a 128-row tile (panels 16 KB)
 constexpr uint32_t PS_V = 32768;     // v [64 tok x 128] (panels 8 KB)
-constexpr int LDA = 65;
 constexpr uint32_t PS_A = 49152;     // A fp32 [64][65]; then [Tw; Tu] 128 x 64 bf16; then Wbar image
 constexpr uint32_t PS_T = 66560;     // T fp32 [64][65]; then W image [64 x 128]
 constexpr uint32_t PS_P = 83968;     // P image [64 x 64]
@@ -40,20 +40,6 @@ constexpr uint32_t PS_TT = PS_A, PS_WBAR = PS_A, PS_W = PS_T;
 static_assert(PS_A % 1024 == 0 && PS_T % 1024 == 0 && PS_P % 1024 == 0, "align");
 static_assert(PS_A + 64 * LDA * 4 <= PS_T && PS_T + 64 * LDA * 4 <= PS_P, "fp32 tiles");
 static_assert(2 * (PS_BYTES + 1024) <= 228 * 1024, "two prep CTAs per SM");
-
-__device__ __forceinline__ void unpack8(const uint4& u, float* x) {
-    x[0] = bf16lo(u.x); x[1] = bf16hi(u.x); x[2] = bf16lo(u.y); x[3] = bf16hi(u.y);
-    x[4] = bf16lo(u.z); x[5] = bf16hi(u.z); x[6] = bf16lo(u.w); x[7] = bf16hi(u.w);
-}
-__device__ __forceinline__ uint4 pack8(const float* x, float s) {
-    return make_uint4(pack_bf16(s * x[0], s * x[1]), pack_bf16(s * x[2], s * x[3]), pack_bf16(s * x[4], s * x[5]),
-                      pack_bf16(s * x[6], s * x[7]));
-}
-__device__ __forceinline__ void st_chunk(uint32_t addr, const float* x, float s) {
-    const uint4 u = pack8(x, s);
-    st_shared_v4(addr, u.x, u.y, u.z, u.w);
-}
-__device__ __forceinline__ void st_global16(uint8_t* p, const uint4& u) { *reinterpret_cast<uint4*>(p) = u; }
 
 __global__ void __launch_bounds__(256, 2)
     prep_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
@@ -227,65 +213,7 @@ __global__ void __launch_bounds__(256, 2)
             tc_fence_before();
             __syncthreads();
 
-            // T = (I + A)^-1 (unit lower triangular) by 16x16 blocks. Phase 1 (160 threads, one
-            // column each): forward substitution with L_II = I + A_II gives the diagonal inverses T_II
-            // (right-hand side e_c) and Y_IK = T_II A_IK for I > K (right-hand side column c of A_IK).
-            // Then T_IJ = -sum_{J<=K<I} Y_IK T_KJ by block distance I-J = 1, 2, 3.
-            if (tid < 160) {
-                int I, K, cc;
-                const bool diag = tid < 64;
-                if (diag) {
-                    I = tid >> 4;
-                    K = I;
-                    cc = tid & 15;
-                } else {
-                    const int pidx = (tid - 64) >> 4;  // pairs (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
-                    cc = (tid - 64) & 15;
-                    I = pidx == 0 ? 1 : (pidx < 3 ? 2 : 3);
-                    K = pidx - I * (I - 1) / 2;
-                }
-                const float* Ab = Am + (16 * I) * LDA + 16 * I;
-                const float* Bc = Am + (16 * I) * LDA + 16 * K + cc;
-                float y[16];
-#pragma unroll
-                for (int i = 0; i < 16; i++) {
-                    float s = diag ? (i == cc ? 1.f : 0.f) : Bc[i * LDA];
-#pragma unroll
-                    for (int j = 0; j < i; j++) s -= Ab[i * LDA + j] * y[j];
-                    y[i] = s;
-                }
-                if (diag) {
-#pragma unroll
-                    for (int i = 0; i < 16; i++) Tm[(16 * I + i) * LDA + 16 * I + cc] = y[i];
-                } else {
-                    float* yp = Xs + ((tid - 64) >> 4) * (16 * 17);
-#pragma unroll
-                    for (int i = 0; i < 16; i++) yp[i * 17 + cc] = y[i];
-                }
-            }
-            __syncthreads();
-            // item J of a level is block (J + dlev, J); all sums are formed before any store
-            for (int dlev = 1; dlev <= 3; dlev++) {
-                const int nb = 4 - dlev;
-                const int i = (tid >> 4) & 15, cc = tid & 15;
-                float s[3] = {0.f, 0.f, 0.f};
-#pragma unroll
-                for (int J = 0; J < 3; J++) {
-                    if (J < nb) {
-                        const int I = J + dlev;
-                        for (int K = J; K < I; K++) {
-                            const float* yr = Xs + (I * (I - 1) / 2 + K) * (16 * 17) + i * 17;
-                            const float* tc = Tm + (16 * K) * LDA + 16 * J + cc;
-#pragma unroll
-                            for (int m = 0; m < 16; m++) s[J] += yr[m] * tc[m * LDA];
-                        }
-                    }
-                }
-#pragma unroll
-                for (int J = 0; J < 3; J++)
-                    if (J < nb) Tm[(16 * (J + dlev) + i) * LDA + 16 * J + cc] = -s[J];
-                __syncthreads();
-            }
+            ut_solve(Am, Tm, Xs, tid);  // T = (I + A)^-1
             {  // [Tw; Tu] with Tw = T diag(beta Gamma rho_k), Tu = T diag(beta): K-major A operand (over A).
                // T's blocks above the block diagonal are zero and never stored: masked here.
                 const int row = tid >> 1, half = tid & 1;
@@ -631,13 +559,15 @@ __global__ void __launch_bounds__(192, 1) scan_kernel(const __grid_constant__ CU
         fence_proxy_async_smem();
         bool bad = bar_sync_or(1, 128, false);
         if (et == 0) mbar_arrive(&hready);
-        const float* gam = a.gam + bh * a.ncpad;
-        float gnext = gam[chunk_of(0)];
+        // Gamma_C of each chunk: one per head, or one per key channel (this thread's row d)
+        const float* gam = P.channel ? a.gam + bh * NC * kD + d : a.gam + bh * a.ncpad;
+        const int gstride = P.channel ? kD : 1;
+        float gnext = gam[chunk_of(0) * gstride];
         int i = 0;
         for (; i < NC && !bad; i++) {
             const int c = chunk_of(i), s = i & 1;
             const float gC = gnext;
-            if (i + 1 < NC) gnext = gam[chunk_of(i + 1)];
+            if (i + 1 < NC) gnext = gam[chunk_of(i + 1) * gstride];
             if (MODE != SCAN_FWD_OUT || a.states) {  // state entering this step, SW128 [128 x 128] image
                 uint8_t* img = a.states + (bh * NC + c) * (size_t)STATE_IMG;
 #pragma unroll
@@ -768,7 +698,7 @@ cudaError_t launch_chunk_fwd(const ChunkFwdArgs& a, cudaStream_t s) {
     pa.rec2 = keep ? keep + l.rec2 : nullptr;
     pa.status = reinterpret_cast<int*>(ws);
     pa.ncpad = keep ? l.ncpad : w.ncpad;
-    cudaError_t e = launch_prep(pa, mq, mk, mv, s);
+    cudaError_t e = a.p.channel ? launch_prep_ch(pa, mq, mk, mv, s) : launch_prep(pa, mq, mk, mv, s);
     if (e != cudaSuccess) return e;
     ScanArgs sa;
     sa.p = a.p;

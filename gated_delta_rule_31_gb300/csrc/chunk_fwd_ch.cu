@@ -1,0 +1,361 @@
+// chunk_fwd_ch.cu - chunk operators of the gated delta rule with a per-channel gate (one decay
+// per key channel, g [B,T,Hv,Dk]): the channelwise variant described in "Two-pass optimization
+// for channelwise gated delta rule kernel" (ExecuTorch PR #21020, Summary), here in the chunked
+// form of "Adding VJP for gated delta net" (MLX PR #4565). One CTA per (b, v-head, chunk).
+//
+// With a_t = exp(g_t) in R^Dk, Gamma_r = prod_{t<=r} a_t and E_rj = prod_{j<t<=r} a_t (per
+// channel), the chunk algebra of chunk.h holds with every decay taken channel by channel:
+//   A_rj = beta_r sum_d k^_rd k^_jd E_rj,d (j < r),   P_rj = scale sum_d q^_rd k^_jd E_rj,d (j <= r)
+//   W = T diag(beta) (K^ .* Gamma),   U~ = T diag(beta) V,   Kbar = K^ .* (Gamma_C / Gamma_r)
+//   Mneg = -Kbar^T W,   Qc = scale Q^ .* Gamma - P W,   H1 = diag(Gamma_C) H0 + Mneg H0 + Kbar^T U~
+// so the record has the scalar-gate layout and the scan only scales state row d by Gamma_C,d.
+// Decays are formed as products of per-token factors a_t <= 1 (never as exp of a difference
+// of cumulative sums), so no factor can overflow however strong the decay. A and P are
+// accumulated on the CUDA cores (the decay sits inside the contraction); the WY products,
+// Mneg and P W run on tcgen05 from scaled bf16 operand images.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "chunk.h"
+#include "chunk_dev.cuh"
+#include "common.cuh"
+#include "kernels.h"
+#include "tma_host.h"
+
+namespace gdr {
+
+// Shared memory (offsets from a 1024-aligned base), ~195 KB: one CTA per SM.
+constexpr uint32_t CS_KQ = 0;         // k rows 0-63 / q rows 64-127 (TMA, panels 16 KB)
+constexpr uint32_t CS_V = 32768;      // v [64 x 128] (panels 8 KB)
+constexpr uint32_t CS_AL = 49152;     // a_t = exp(g_t) fp32 [64][128]; later prod_{t>r} a_t
+constexpr uint32_t CS_GP = 81920;     // Gamma_r = prod_{t<=r} a_t fp32 [64][128]
+constexpr uint32_t CS_A = 114688;     // A fp32 [64][LDA]; then the [Tw; Tu] image
+constexpr uint32_t CS_T = 132096;     // T fp32 [64][LDA]; then the W image [64 x 128]
+constexpr uint32_t CS_P = 149504;     // P image [64 x 64]
+constexpr uint32_t CS_KG = 157696;    // K .* Gamma image [64 x 128]
+constexpr uint32_t CS_KB = 174080;    // Kbar image [64 x 128]
+constexpr uint32_t CS_SCR = 190464;   // solve scratch [6][16][17] fp32
+constexpr uint32_t CS_SMALL = CS_SCR + 6 * 16 * 17 * 4;  // bet[64], rho[128]
+constexpr uint32_t CS_BYTES = CS_SMALL + 1024;
+static_assert(CS_A % 1024 == 0 && CS_T % 1024 == 0 && CS_P % 1024 == 0 && CS_KG % 1024 == 0 &&
+                  CS_KB % 1024 == 0, "operand images need 1024-byte alignment");
+static_assert(CS_A + 64 * LDA * 4 <= CS_T && CS_T + 64 * LDA * 4 <= CS_P, "fp32 tiles");
+static_assert(CS_BYTES + 1024 <= 232448, "prep_ch smem");
+
+__global__ void __launch_bounds__(256, 1)
+    prep_ch_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
+                   const __grid_constant__ CUtensorMap mv, PrepArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = align1024(smem_raw);
+    const uint32_t sb = smem_u32(sm);
+    __shared__ uint64_t bar_tma, bar_mma;
+    __shared__ uint32_t tmem_sh;
+    __shared__ int abort_sh;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = blockIdx.x, hv = blockIdx.y, b = blockIdx.z;
+    const ChunkProblem& P = a.p;
+    const int hk = hv / (P.Hv / P.Hk);
+    const int t0 = c * kChunk;
+    const size_t bh = (size_t)b * P.Hv + hv;
+    uint8_t* rec = a.rec + (bh * P.NC + c) * REC_BYTES;
+    float* al = reinterpret_cast<float*>(sm + CS_AL);
+    float* gp = reinterpret_cast<float*>(sm + CS_GP);
+    float* Am = reinterpret_cast<float*>(sm + CS_A);
+    float* Tm = reinterpret_cast<float*>(sm + CS_T);
+    float* Xs = reinterpret_cast<float*>(sm + CS_SCR);
+    float* bet = reinterpret_cast<float*>(sm + CS_SMALL);
+    float* rho = bet + 64;  // [128] rows 0-63: k norm factors, 64-127: q norm factors
+    bool ok;
+
+    if (tid == 0) {
+        abort_sh = 0;
+        mbar_init(&bar_tma, 1);
+        mbar_init(&bar_mma, 1);
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&tmem_sh, 256);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = tmem_sh;
+    if (tid == 0) {
+        mbar_expect_tx(&bar_tma, 6 * 8192);
+        tma_load_4d(sm + CS_KQ + 0, &mk, 0, hk, t0, b, &bar_tma);
+        tma_load_4d(sm + CS_KQ + 16384, &mk, 64, hk, t0, b, &bar_tma);
+        tma_load_4d(sm + CS_KQ + 8192, &mq, 0, hk, t0, b, &bar_tma);
+        tma_load_4d(sm + CS_KQ + 24576, &mq, 64, hk, t0, b, &bar_tma);
+        tma_load_4d(sm + CS_V + 0, &mv, 0, hv, t0, b, &bar_tma);
+        tma_load_4d(sm + CS_V + 8192, &mv, 64, hv, t0, b, &bar_tma);
+    }
+    {  // a_t = exp(g_t) per channel (tokens past T: g = 0, beta = 0: the state passes unchanged)
+        const int t = tid >> 2, q4 = tid & 3;
+        const bool valid = t0 + t < P.T;
+        const float4* src = reinterpret_cast<const float4*>(a.g + (((size_t)b * P.T + t0 + t) * P.Hv + hv) * kD + 32 * q4);
+        float4* dst = reinterpret_cast<float4*>(al + t * kD + 32 * q4);
+        float4 gv[8];
+#pragma unroll
+        for (int n = 0; n < 8; n++) gv[n] = valid ? src[n] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int n = 0; n < 8; n++) dst[n] = make_float4(__expf(gv[n].x), __expf(gv[n].y), __expf(gv[n].z), __expf(gv[n].w));
+        if (tid < 64) bet[tid] = (t0 + tid < P.T) ? a.beta[((size_t)b * P.T + t0 + tid) * P.Hv + hv] : 0.f;
+    }
+    ok = mbar_wait(&bar_tma, 0, &abort_sh, a.status, 15);
+    if (__syncthreads_or(!ok)) goto teardown;
+    if (tid < 128) {  // Gamma_r, channel d = tid: running product over the chunk's tokens
+        float p = 1.f;
+        for (int t = 0; t < kChunk; t++) {
+            p *= al[t * kD + tid];
+            gp[t * kD + tid] = p;
+        }
+    } else {  // L2 norm factors: row tid-128 of the [k; q] tile (read order rotated by the row)
+        const int row = tid - 128;
+        float ss = 0.f;
+#pragma unroll
+        for (int ch = 0; ch < 16; ch++) {
+            const int j = (ch + row) & 15;
+            float x[8];
+            unpack8(ld_shared_v4(sb + CS_KQ + sw128_chunk(row, j, 128)), x);
+#pragma unroll
+            for (int e = 0; e < 8; e++) ss += x[e] * x[e];
+        }
+        rho[row] = P.use_norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
+    }
+    {  // P image starts at zero (its upper triangle is never written)
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+        st_shared_v4(sb + CS_P + tid * 32, z.x, z.y, z.z, z.w);
+        st_shared_v4(sb + CS_P + tid * 32 + 16, z.x, z.y, z.z, z.w);
+    }
+    __syncthreads();
+
+    // A and P on the CUDA cores. Lane = (j group jsel = lane >> 3, channel group cg = lane & 7,
+    // 16 channels each); a thread owns column j1 = 4 warp + jsel and then j2 = 63 - j1, walking
+    // rows r = j .. 63 with the running decay E_rj of its channels (65 steps for every thread,
+    // so control flow stays uniform for the shuffles that sum the 8 channel groups).
+    {
+        const int jsel = lane >> 3, cg = lane & 7;
+        const int j1 = 4 * warp + jsel, j2 = 63 - j1;
+        const int n1 = kChunk - j1;  // steps spent on j1
+        float kj[16], e[16];
+        auto load_row16 = [&](int row, float* x) {  // 16 bf16 of row `row` of the [k; q] tile, channels 16 cg..
+            unpack8(ld_shared_v4(sb + CS_KQ + sw128_chunk(row, 2 * cg, 128)), x);
+            unpack8(ld_shared_v4(sb + CS_KQ + sw128_chunk(row, 2 * cg + 1, 128)), x + 8);
+        };
+        for (int s = 0; s <= kChunk; s++) {
+            const bool first = s < n1;
+            const int j = first ? j1 : j2;
+            const int r = first ? j1 + s : j2 + (s - n1);
+            if (s == 0 || s == n1) {  // start of a column: its k row, decay 1
+                load_row16(j, kj);
+#pragma unroll
+                for (int x = 0; x < 16; x++) e[x] = 1.f;
+            } else {  // E_rj = E_(r-1)j * a_r   (float4 order rotated so 8 lanes hit 8 bank groups)
+#pragma unroll
+                for (int c4 = 0; c4 < 4; c4++) {
+                    const int cc = (c4 + (cg >> 1)) & 3;
+                    const float4 f = *reinterpret_cast<const float4*>(al + r * kD + 16 * cg + 4 * cc);
+                    e[4 * cc] *= f.x; e[4 * cc + 1] *= f.y; e[4 * cc + 2] *= f.z; e[4 * cc + 3] *= f.w;
+                }
+            }
+            float kr[16], qr[16];
+            load_row16(r, kr);
+            load_row16(64 + r, qr);
+            float pa = 0.f, pp = 0.f;
+#pragma unroll
+            for (int x = 0; x < 16; x++) {
+                const float w = kj[x] * e[x];
+                pa += kr[x] * w;
+                pp += qr[x] * w;
+            }
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) {
+                pa += __shfl_xor_sync(0xffffffffu, pa, o);
+                pp += __shfl_xor_sync(0xffffffffu, pp, o);
+            }
+            if (cg == 0) {
+                if (r > j) Am[r * LDA + j] = bet[r] * rho[r] * rho[j] * pa;
+                const __nv_bfloat16 pv = __float2bfloat16_rn(P.scale * rho[64 + r] * rho[j] * pp);
+                *reinterpret_cast<__nv_bfloat16*>(sm + CS_P + sw128_off(r, j, 64)) = pv;
+            }
+        }
+    }
+    __syncthreads();
+    if (tid < 128) {  // prod_{t>r} a_t, channel d = tid, in place of a_t (read before written)
+        float p = 1.f;
+        for (int t = kChunk - 1; t >= 0; t--) {
+            const float at = al[t * kD + tid];
+            al[t * kD + tid] = p;
+            p *= at;
+        }
+        a.gam[(bh * P.NC + c) * kD + tid] = gp[(kChunk - 1) * kD + tid];  // Gamma_C per channel
+    }
+    {  // P to the record
+        const uint4 u = ld_shared_v4(sb + CS_P + tid * 32), w = ld_shared_v4(sb + CS_P + tid * 32 + 16);
+        st_global16(rec + REC_P + tid * 32, u);
+        st_global16(rec + REC_P + tid * 32 + 16, w);
+    }
+    ut_solve(Am, Tm, Xs, tid);  // T = (I + A)^-1 (ends with a barrier; suffix products done)
+    {  // [Tw; Tu]: Tw = T diag(beta rho_k), Tu = T diag(beta) (K-major A operand, over A)
+        const int row = tid >> 1, half = tid & 1;
+        const int i = row & 63;
+        const bool isw = row < 64;
+        const float* trow = Tm + i * LDA + 32 * half;
+        float x[32];
+#pragma unroll
+        for (int jj = 0; jj < 32; jj++) {
+            const int j = 32 * half + jj;
+            const float t = (j >> 4) <= (i >> 4) ? trow[jj] : 0.f;
+            x[jj] = t * bet[j] * (isw ? rho[j] : 1.f);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; q++) st_chunk(sb + CS_A + sw128_chunk(row, 4 * half + q, 128), x + 8 * q, 1.f);
+    }
+    {  // K .* Gamma and Kbar = diag(rho_k) K .* prod_{t>r} a_t, row r = tid >> 2, 32 channels each
+        const int r = tid >> 2, q4 = tid & 3;
+        const float rk = rho[r];
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const int j = 4 * q4 + q;  // 8-channel chunk of the row
+            float x[8], yg[8], yb[8];
+            unpack8(ld_shared_v4(sb + CS_KQ + sw128_chunk(r, j, 128)), x);
+            const float4* g4 = reinterpret_cast<const float4*>(gp + r * kD + 8 * j);
+            const float4* b4 = reinterpret_cast<const float4*>(al + r * kD + 8 * j);
+            const float4 g0 = g4[0], g1 = g4[1], b0 = b4[0], b1 = b4[1];
+            const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+            const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+            for (int e = 0; e < 8; e++) {
+                yg[e] = x[e] * gg[e];
+                yb[e] = rk * x[e] * bb[e];
+            }
+            const uint32_t off = sw128_chunk(r, j, 64);
+            st_chunk(sb + CS_KG + off, yg, 1.f);
+            const uint4 ub = pack8(yb, 1.f);
+            st_shared_v4(sb + CS_KB + off, ub.x, ub.y, ub.z, ub.w);
+            st_global16(rec + REC_K + off, ub);
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+
+    // W = Tw (K .* Gamma) and U~ = Tu V as two M=128 products of [Tw; Tu] (rows 0-63 of the
+    // first, rows 64-127 of the second are the wanted ones); B operands MN-major
+    if (tid == 0) {
+        tc_fence_after();
+        const uint32_t id = idesc_bf16(128, 128, 0, 1);
+        for (int k0 = 0; k0 < kChunk; k0 += 16) {
+            mma_bf16(tm + 0, desc_kmajor(sb + CS_A, 128, 0, k0), desc_mnmajor(sb + CS_KG, 64, 0, k0), id, k0 > 0);
+            mma_bf16(tm + 128, desc_kmajor(sb + CS_A, 128, 0, k0), desc_mnmajor(sb + CS_V, 64, 0, k0), id, k0 > 0);
+        }
+        mma_commit(&bar_mma);
+    }
+    ok = mbar_wait(&bar_mma, 0, &abort_sh, a.status, 16);
+    if (__syncthreads_or(!ok)) goto teardown;
+    tc_fence_after();
+    {
+        const int lg = warp & 3, h = warp >> 2;
+        if (lg < 2) {  // W rows i = 32 lg + lane -> W image (over T)
+            const int i = 32 * lg + lane;
+            float w[64];
+            tmem_ld32(tmem_at(tm, 32 * lg, 64 * h), w);
+            tmem_ld32(tmem_at(tm, 32 * lg, 64 * h + 32), w + 32);
+            tmem_wait_ld();
+#pragma unroll
+            for (int q = 0; q < 8; q++) st_chunk(sb + CS_T + sw128_chunk(i, 8 * h + q, 64), w + 8 * q, 1.f);
+        } else {  // U~ rows i = 32 lg + lane - 64 -> record slices
+            const int i = 32 * lg + lane - 64;
+            float u[64];
+            tmem_ld32(tmem_at(tm, 32 * lg, 128 + 64 * h), u);
+            tmem_ld32(tmem_at(tm, 32 * lg, 128 + 64 * h + 32), u + 32);
+            tmem_wait_ld();
+#pragma unroll
+            for (int q = 0; q < 8; q++) {
+                const int col = 64 * h + 8 * q;
+                st_global16(rec + REC_U + (col >> 5) * 4096 + sw64_chunk(i, q & 3), pack8(u + 8 * q, 1.f));
+            }
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+
+    // Mneg = -Kbar^T W (M=128: A = Kbar image read MN-major) and P W (M=64)
+    if (tid == 0) {
+        tc_fence_after();
+        const uint32_t idm = idesc_bf16(128, 128, 1, 1);
+        for (int k0 = 0; k0 < kChunk; k0 += 16)
+            mma_bf16(tm + 0, desc_mnmajor(sb + CS_KB, 64, 0, k0), desc_mnmajor(sb + CS_T, 64, 0, k0), idm, k0 > 0);
+        const uint32_t idp = idesc_bf16(64, 128, 0, 1);
+        for (int k0 = 0; k0 < kChunk; k0 += 16)
+            mma_bf16(tm + 128, desc_kmajor(sb + CS_P, 64, 0, k0), desc_mnmajor(sb + CS_T, 64, 0, k0), idp, k0 > 0);
+        mma_commit(&bar_mma);
+    }
+    ok = mbar_wait(&bar_mma, 1, &abort_sh, a.status, 17);
+    if (__syncthreads_or(!ok)) goto teardown;
+    tc_fence_after();
+    {
+        const int lg = warp & 3, h = warp >> 2;
+        {  // Mneg rows d = 32 lg + lane
+            const int d = 32 * lg + lane;
+            float m[64];
+            tmem_ld32(tmem_at(tm, 32 * lg, 64 * h), m);
+            tmem_ld32(tmem_at(tm, 32 * lg, 64 * h + 32), m + 32);
+            tmem_wait_ld();
+#pragma unroll
+            for (int q = 0; q < 8; q++)
+                st_global16(rec + REC_M + sw128_chunk(d, 8 * h + q, 128), pack8(m + 8 * q, -1.f));
+        }
+        {  // Qc = scale diag(rho_q) Q .* Gamma - P W, rows i = 16 lg + lane (M=64 layout)
+            const int i = 16 * lg + (lane & 15);
+            float pw[64];
+            tmem_ld32(tmem_at(tm, 32 * lg, 128 + 64 * h), pw);
+            tmem_ld32(tmem_at(tm, 32 * lg, 128 + 64 * h + 32), pw + 32);
+            tmem_wait_ld();
+            if (lane < 16) {
+                const float f = P.scale * rho[64 + i];
+                uint4 qv[8];
+#pragma unroll
+                for (int q = 0; q < 8; q++)
+                    qv[q] = ld_shared_v4(sb + CS_KQ + sw128_chunk(64 + i, 8 * h + q, 128));
+#pragma unroll
+                for (int q = 0; q < 8; q++) {
+                    float x[8];
+                    unpack8(qv[q], x);
+                    const float4* g4 = reinterpret_cast<const float4*>(gp + i * kD + 64 * h + 8 * q);
+                    const float4 g0 = g4[0], g1 = g4[1];
+                    const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+                    for (int e = 0; e < 8; e++) x[e] = f * x[e] * gg[e] - pw[8 * q + e];
+                    st_global16(rec + REC_Q + sw128_chunk(i, 8 * h + q, 64), pack8(x, 1.f));
+                }
+            }
+        }
+    }
+teardown:
+    tc_fence_before();
+    __syncthreads();
+    if (abort_sh && tid == 0) {  // let copies still in flight land before the CTA exits
+        volatile int never = 0;
+        mbar_wait(&bar_tma, 0, &never, nullptr, 0);
+    }
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tm, 256);
+}
+
+cudaError_t launch_prep_ch(const PrepArgs& a, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                           cudaStream_t s) {
+    const int smem = CS_BYTES + 1024;
+    cudaError_t e = cudaFuncSetAttribute(prep_ch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    dim3 grid(a.p.NC, a.p.Hv, a.p.B);
+    trace_begin("chunk_prep_channel", s);
+    prep_ch_kernel<<<grid, 256, smem, s>>>(mq, mk, mv, a);
+    trace_end(s);
+    return cudaGetLastError();
+}
+
+}  // namespace gdr

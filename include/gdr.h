@@ -80,8 +80,10 @@ size_t gdr_fwd_chunked_workspace(const gdr_problem* p);
 size_t gdr_bwd_chunked_workspace(const gdr_problem* p);
 
 /* Chunked prefill forward (chunks of 64 tokens): o and, if ht != NULL, the final state.
- * h0 may be NULL (zero initial state). Implemented for dtype BF16, Dk = Dv = 128,
- * scalar gate; other combinations return GDR_ERR_UNSUPPORTED. Pointers 16-byte aligned.
+ * h0 may be NULL (zero initial state). Implemented for dtype BF16, Dk = Dv = 128, with the
+ * scalar gate or the per-channel gate (g [B,T,Hv,Dk], the channelwise variant of
+ * "Two-pass optimization for channelwise gated delta rule kernel", ExecuTorch PR #21020);
+ * other combinations return GDR_ERR_UNSUPPORTED. Pointers 16-byte aligned.
  * Work: per chunk a 64x64 unit-lower-triangular (UT/WY) transform of the k k^T beta
  * block on the tensor cores, then one sequential scan over chunks per (b, hv, Dv slice)
  * with the fp32 state held on chip. Clears and then sets the workspace status word. */
@@ -99,7 +101,8 @@ gdr_status gdr_fwd_sequential(const gdr_problem* p, const void* q, const void* k
 /* Chunked backward (VJP) of gdr_fwd_chunked for the loss <do, o> + <dht, ht>: writes dq, dk,
  * dv, dg, dbeta and, if dh0 != NULL, dh0. h0 and dht may be NULL (zero). Recomputes the
  * chunk-local terms and the chunk-start states instead of reading saved activations;
- * the normalisation backward is done inside. Same support matrix as gdr_fwd_chunked.
+ * the normalisation backward is done inside. Same support matrix as gdr_fwd_chunked, except
+ * that the per-channel gate is forward only (GDR_ERR_UNSUPPORTED here).
  * Deterministic: no floating-point atomics. */
 gdr_status gdr_bwd_chunked(const gdr_problem* p, const void* q, const void* k, const void* v,
                            const float* g, const float* beta, const float* h0, const void* do_,
@@ -111,7 +114,7 @@ gdr_status gdr_bwd_chunked(const gdr_problem* p, const void* q, const void* k, c
  * entering every chunk (bf16, opaque layout, gdr_chunk_states_bytes() bytes:
  * B*Hv*ceil(T/64)*32 KB, caller-owned, 256-byte aligned); the backward then reads them
  * instead of re-running the forward scan. Chunk-local operators are still recomputed by
- * the backward. Same support matrix as gdr_fwd_chunked; 0 if the problem is invalid. */
+ * the backward. Same support matrix as gdr_bwd_chunked; 0 if the problem is invalid. */
 size_t gdr_chunk_states_bytes(const gdr_problem* p);
 size_t gdr_bwd_chunked_states_workspace(const gdr_problem* p);
 
@@ -139,7 +142,7 @@ gdr_status gdr_bwd_chunked_states(const gdr_problem* p, const void* q, const voi
  * bitwise identical to gdr_fwd_chunked / gdr_bwd_chunked. The buffer must not be modified
  * between the two calls, and the backward must get the same q, k, v, g, beta and problem.
  * Workspaces: gdr_fwd_chunked_saved_workspace() (the status word only) and
- * gdr_bwd_chunked_saved_workspace(). Same support matrix as gdr_fwd_chunked; the size
+ * gdr_bwd_chunked_saved_workspace(). Same support matrix as gdr_bwd_chunked; the size
  * queries return 0 for an invalid or unsupported problem. Errors as gdr_fwd_chunked, plus
  * GDR_ERR_WORKSPACE if `saved` is NULL or smaller than required. */
 size_t gdr_chunk_saved_bytes(const gdr_problem* p);

@@ -84,11 +84,19 @@ def test_decode_requires_single_token(L):
 
 
 def test_chunked_support_matrix_and_workspace(L):
-    for kw in (dict(dtype=0), dict(gate=1), dict(Dk=64, Dv=64)):
+    for kw in (dict(dtype=0), dict(Dk=64, Dv=64)):
         p = prob(**kw)
         assert L.gdr_fwd_chunked_workspace(ctypes.byref(p)) == 0
         assert L.gdr_fwd_chunked(ctypes.byref(p), *[FAKE] * 8, FAKE, 1 << 30, None) == UNSUPPORTED
         assert L.gdr_bwd_chunked(ctypes.byref(p), *[FAKE] * 14, FAKE, 1 << 30, None) == UNSUPPORTED
+    # per-channel gate: chunked forward only (Gamma_C kept per key channel: a larger workspace)
+    pc = prob(gate=1)
+    assert L.gdr_fwd_chunked_workspace(ctypes.byref(pc)) > L.gdr_fwd_chunked_workspace(ctypes.byref(prob()))
+    assert L.gdr_bwd_chunked_workspace(ctypes.byref(pc)) == 0
+    assert L.gdr_bwd_chunked(ctypes.byref(pc), *[FAKE] * 14, FAKE, 1 << 30, None) == UNSUPPORTED
+    assert L.gdr_chunk_states_bytes(ctypes.byref(pc)) == 0 and L.gdr_chunk_saved_bytes(ctypes.byref(pc)) == 0
+    assert L.gdr_fwd_chunked_states(ctypes.byref(pc), *[FAKE] * 8, FAKE, 1 << 30, FAKE, 1 << 30, None) == UNSUPPORTED
+    assert L.gdr_fwd_chunked_saved(ctypes.byref(pc), *[FAKE] * 8, FAKE, 1 << 30, FAKE, 1 << 30, None) == UNSUPPORTED
     p = prob()
     need = L.gdr_fwd_chunked_workspace(ctypes.byref(p))
     need_b = L.gdr_bwd_chunked_workspace(ctypes.byref(p))

@@ -12,7 +12,8 @@ is needed between steps. Also reported: the roofline of the dominant kernel (per
 times from the library's launch trace, recorded on the launch stream), the same step end
 to end with pinned-host inputs/outputs copied inside the timed region, the decode step's
 state bandwidth (B=32, channel gate, fp32, L2 flushed before every step), the short-prefill
-crossover of the sequential and chunked forwards (T = 1..256 continuing a B=32 state), SM clocks
+crossover of the sequential and chunked forwards (T = 1..256 continuing a B=32 state), the
+per-channel-gate chunked prefill (T=4096) beside the scalar-gate one and the sequential kernel, SM clocks
 sampled during the timed region, and the fp64 CPU oracle timed on a bounded sample.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mine|reference]
@@ -189,6 +190,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the short-prefill crossover table")
+    ap.add_argument("--no-channel", action="store_true", help="skip the per-channel gate prefill timing")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     set_tokens(args.tokens)
@@ -463,6 +465,48 @@ def main():
                "rows": rows, "chunked_faster_from_T": cross}
         del flush
 
+    # ------------------------------------------------------------------ per-channel gate prefill
+    chan = None
+    if not args.no_channel:
+        from gated_delta_rule_31_gb300.synth import PREFILL
+
+        flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)
+        res = {}
+        for gate in ("channel", "scalar"):
+            xc = make_inputs(PREFILL, dtype=torch.bfloat16, seed=1001, gate=gate)
+            dc = {k: v.to(dev) for k, v in xc.items() if v is not None}
+            pc = gdr.Problem(PREFILL.B, PREFILL.T, PREFILL.Hk, PREFILL.Hv, D, D, gdr.GDR_BF16,
+                             gdr.GDR_GATE_CHANNEL if gate == "channel" else gdr.GDR_GATE_SCALAR, D ** -0.5, 1)
+            oc = torch.empty(dc["v"].shape, dtype=torch.bfloat16, device=dev)
+            hc = torch.empty(dc["h0"].shape, **f32)
+            nwc = gdr.fwd_workspace_bytes(pc)
+            wsc = torch.empty(nwc, dtype=torch.uint8, device=dev)
+            ins = [P(dc[n]) for n in ("q", "k", "v", "g", "beta", "h0")] + [P(oc), P(hc)]
+            calls = {"chunked": lambda: raise_on(L.gdr_fwd_chunked(ctypes.byref(pc), *ins, P(wsc), nwc, sp))}
+            if gate == "channel":
+                calls["sequential"] = lambda: raise_on(L.gdr_fwd_sequential(ctypes.byref(pc), *ins, sp))
+            for name, fn in calls.items():
+                for _ in range(3):
+                    fn()
+                ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(5)]
+                for a_, b_ in ev:
+                    flush.fill_(2)
+                    a_.record(stream)
+                    fn()
+                    b_.record(stream)
+                torch.cuda.synchronize(dev)
+                res[f"{gate}_{name}_us"] = 1e3 * statistics.median(a_.elapsed_time(b_) for a_, b_ in ev)
+            if gate == "channel":
+                with gdr.trace() as trc:
+                    calls["chunked"]()
+                    torch.cuda.synchronize(dev)
+                res["channel_kernels_us"] = {n: round(1e3 * t, 1) for n, t in trc.records}
+            del dc, oc, hc, wsc
+        toks = PREFILL.B * PREFILL.T
+        chan = {"config": "B=1, T=4096, Hk=16, Hv=32, Dk=Dv=128, bf16, h0 ~ N(0,0.02), L2 flushed, median of 5",
+                "tokens_per_s_channel_chunked": toks / (res["channel_chunked_us"] * 1e-6), **res}
+        del flush
+
     # ------------------------------------------------------------------ CPU baseline (rank 0, N=1)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -488,7 +532,7 @@ def main():
                                      "note": "optional: forward also keeps the chunk operators, backward runs no "
                                              "prep (chunk-local terms stored, not recomputed)"},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(round(launches_per_step * args.steps)),
-            "clocks": clocks, "kernels": kern, "decode": dec, "short_prefill": pre,
+            "clocks": clocks, "kernels": kern, "decode": dec, "short_prefill": pre, "channel_prefill": chan,
         }
         print(json.dumps(line))
     if world > 1:

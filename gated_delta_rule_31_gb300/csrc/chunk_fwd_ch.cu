@@ -94,13 +94,15 @@ __global__ void __launch_bounds__(256, 1)
     {  // a_t = exp(g_t) per channel (tokens past T: g = 0, beta = 0: the state passes unchanged)
         const int t = tid >> 2, q4 = tid & 3;
         const bool valid = t0 + t < P.T;
-        const float4* src = reinterpret_cast<const float4*>(a.g + (((size_t)b * P.T + t0 + t) * P.Hv + hv) * kD + 32 * q4);
+        const float4* src =
+            reinterpret_cast<const float4*>(a.g + (((size_t)b * P.T + t0 + t) * P.Hv + hv) * kD + 32 * q4);
         float4* dst = reinterpret_cast<float4*>(al + t * kD + 32 * q4);
         float4 gv[8];
 #pragma unroll
         for (int n = 0; n < 8; n++) gv[n] = valid ? src[n] : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int n = 0; n < 8; n++) dst[n] = make_float4(__expf(gv[n].x), __expf(gv[n].y), __expf(gv[n].z), __expf(gv[n].w));
+        for (int n = 0; n < 8; n++)
+            dst[n] = make_float4(__expf(gv[n].x), __expf(gv[n].y), __expf(gv[n].z), __expf(gv[n].w));
         if (tid < 64) bet[tid] = (t0 + tid < P.T) ? a.beta[((size_t)b * P.T + t0 + tid) * P.Hv + hv] : 0.f;
     }
     ok = mbar_wait(&bar_tma, 0, &abort_sh, a.status, 15);
@@ -131,18 +133,28 @@ __global__ void __launch_bounds__(256, 1)
     }
     __syncthreads();
 
-    // A and P on the CUDA cores. Lane = (j group jsel = lane >> 3, channel group cg = lane & 7,
-    // 16 channels each); a thread owns column j1 = 4 warp + jsel and then j2 = 63 - j1, walking
-    // rows r = j .. 63 with the running decay E_rj of its channels (65 steps for every thread,
-    // so control flow stays uniform for the shuffles that sum the 8 channel groups).
+    // A and P on the CUDA cores. Lane = (j group jsel = lane >> 3, channel group cg = lane & 7);
+    // channel group cg owns channels 32 m + 4 cg + x (m, x < 4), so the 8 lanes of a group read
+    // 8 consecutive 16-byte words of a row (no bank conflict) with compile-time register
+    // indices. A thread owns column j1 = 4 warp + jsel and then j2 = 63 - j1, walking rows
+    // r = j .. 63 with the running decay E_rj of its channels (65 steps for every thread, so
+    // control flow stays uniform for the shuffles that sum the 8 channel groups).
     {
         const int jsel = lane >> 3, cg = lane & 7;
         const int j1 = 4 * warp + jsel, j2 = 63 - j1;
         const int n1 = kChunk - j1;  // steps spent on j1
         float kj[16], e[16];
-        auto load_row16 = [&](int row, float* x) {  // 16 bf16 of row `row` of the [k; q] tile, channels 16 cg..
-            unpack8(ld_shared_v4(sb + CS_KQ + sw128_chunk(row, 2 * cg, 128)), x);
-            unpack8(ld_shared_v4(sb + CS_KQ + sw128_chunk(row, 2 * cg + 1, 128)), x + 8);
+        // 16 channels of row `row` of the [k; q] tile: 4 bf16 (8 bytes) per m
+        auto load_row16 = [&](int row, float* x) {
+#pragma unroll
+            for (int m = 0; m < 4; m++) {
+                const uint32_t off = CS_KQ + sw128_chunk(row, 4 * m + (cg >> 1), 128) + 8 * (cg & 1);
+                const uint2 u = *reinterpret_cast<const uint2*>(sm + off);
+                x[4 * m] = bf16lo(u.x);
+                x[4 * m + 1] = bf16hi(u.x);
+                x[4 * m + 2] = bf16lo(u.y);
+                x[4 * m + 3] = bf16hi(u.y);
+            }
         };
         for (int s = 0; s <= kChunk; s++) {
             const bool first = s < n1;
@@ -152,12 +164,11 @@ __global__ void __launch_bounds__(256, 1)
                 load_row16(j, kj);
 #pragma unroll
                 for (int x = 0; x < 16; x++) e[x] = 1.f;
-            } else {  // E_rj = E_(r-1)j * a_r   (float4 order rotated so 8 lanes hit 8 bank groups)
+            } else {  // E_rj = E_(r-1)j * a_r
 #pragma unroll
-                for (int c4 = 0; c4 < 4; c4++) {
-                    const int cc = (c4 + (cg >> 1)) & 3;
-                    const float4 f = *reinterpret_cast<const float4*>(al + r * kD + 16 * cg + 4 * cc);
-                    e[4 * cc] *= f.x; e[4 * cc + 1] *= f.y; e[4 * cc + 2] *= f.z; e[4 * cc + 3] *= f.w;
+                for (int m = 0; m < 4; m++) {
+                    const float4 f = *reinterpret_cast<const float4*>(al + r * kD + 32 * m + 4 * cg);
+                    e[4 * m] *= f.x; e[4 * m + 1] *= f.y; e[4 * m + 2] *= f.z; e[4 * m + 3] *= f.w;
                 }
             }
             float kr[16], qr[16];

@@ -21,7 +21,7 @@ import torch
 from ._build import LIB as _LIB_PATH
 from ._build import build
 
-__all__ = ["build", "fwd_chunked", "bwd_chunked", "fwd_sequential", "decode_step", "GdrError",
+__all__ = ["build", "fwd_chunked", "bwd_chunked", "fwd_sequential", "bwd_sequential", "decode_step", "GdrError",
            "fwd_workspace_bytes", "bwd_workspace_bytes", "lib", "Problem", "workspace_status", "trace"]
 
 GDR_F32, GDR_BF16 = 0, 1
@@ -62,6 +62,10 @@ def lib():
         L.gdr_fwd_sequential.argtypes = [PP] + [P] * 8 + [st]
         L.gdr_fwd_sequential.restype = ctypes.c_int
         L.gdr_bwd_chunked.argtypes = [PP] + [P] * 14 + [P, sz, st]
+        L.gdr_bwd_sequential_workspace.argtypes = [PP]
+        L.gdr_bwd_sequential_workspace.restype = sz
+        L.gdr_bwd_sequential.argtypes = [PP] + [P] * 14 + [P, sz, st]
+        L.gdr_bwd_sequential.restype = ctypes.c_int
         L.gdr_bwd_chunked.restype = ctypes.c_int
         L.gdr_decode_step.argtypes = [PP] + [P] * 7 + [st]
         L.gdr_decode_step.restype = ctypes.c_int
@@ -270,6 +274,29 @@ def bwd_chunked(q, k, v, g, beta, h0, do, dht=None, scale=None, use_qk_l2norm=Tr
                                         _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dg"]),
                                         _ptr(out["dbeta"]), _ptr(out["dh0"]), _ptr(ws), ctypes.c_size_t(nbytes),
                                         _stream(q.device)))
+    return out
+
+
+def bwd_sequential(q, k, v, g, beta, h0, do, dht=None, scale=None, use_qk_l2norm=True, workspace=None):
+    """Sequential VJP (gdr_bwd_sequential) of <do,o> + <dht,ht>: every dtype, gate and head
+    size. Returns a dict of fp32 gradients dq, dk, dv, dg, dbeta, dh0 (dg has g's shape)."""
+    _check_inputs(q, k, v, g, beta, h0)
+    _need(do, "do", dtype=v.dtype, device=v.device, shape=v.shape)
+    p = _problem(q, v, g, scale, use_qk_l2norm)
+    if dht is not None:
+        _need(dht, "dht", dtype=torch.float32, device=v.device, shape=(p.B, p.Hv, p.Dv, p.Dk))
+    f32 = dict(dtype=torch.float32, device=v.device)
+    out = dict(dq=torch.empty(q.shape, **f32), dk=torch.empty(k.shape, **f32), dv=torch.empty(v.shape, **f32),
+               dg=torch.empty(g.shape, **f32), dbeta=torch.empty(beta.shape, **f32),
+               dh0=torch.empty((p.B, p.Hv, p.Dv, p.Dk), **f32))
+    nbytes = int(lib().gdr_bwd_sequential_workspace(ctypes.byref(p)))
+    if nbytes == 0:
+        _check(1)
+    ws = _workspace(nbytes, q.device, workspace)
+    _check(lib().gdr_bwd_sequential(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
+                                    _ptr(do), _ptr(dht), _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]),
+                                    _ptr(out["dg"]), _ptr(out["dbeta"]), _ptr(out["dh0"]), _ptr(ws),
+                                    ctypes.c_size_t(nbytes), _stream(q.device)))
     return out
 
 

@@ -11,8 +11,10 @@ kept for the backward — the point of "fold q/k L2-norm into the gated_delta_ru
 (Megatron-LM PR #5396, "What" / "Why"). The VJP is the chunked backward of "Adding VJP for
 gated delta net" (MLX PR #4565).
 
-Supported as the chunked kernels are: bf16 q/k/v, Dk = Dv = 128, scalar gate g [B,T,Hv];
-other problems raise ``GdrError`` (GDR_ERR_UNSUPPORTED). The only torch operations here
+bf16 q/k/v with Dk = Dv = 128 run the chunked forward (scalar or per-channel gate) and, for the
+scalar gate, the chunked VJP; every other problem (fp32, other head sizes, the per-channel
+gate's backward) uses the token-by-token kernels (gdr_fwd_sequential / gdr_bwd_sequential),
+keeping h0 for the backward. The only torch operations here
 are argument marshalling: a zero ``do`` when the output is unused, contiguity, and casting
 the fp32 gradients of q/k/v to their bf16 dtype.
 """
@@ -20,22 +22,33 @@ from __future__ import annotations
 
 import torch
 
-from . import bwd_chunked, fwd_chunked
+from . import bwd_chunked, bwd_sequential, fwd_chunked, fwd_sequential
 
 __all__ = ["gated_delta_rule", "GatedDeltaRuleFunction"]
+
+
+def _chunked_ok(q, v):
+    return q.dtype == torch.bfloat16 and q.shape[-1] == 128 and v.shape[-1] == 128
 
 
 class GatedDeltaRuleFunction(torch.autograd.Function):
     @staticmethod
     def forward(ctx, q, k, v, g, beta, h0, scale, use_qk_l2norm, keep_operators):
         ctx.scale, ctx.norm, ctx.has_h0 = scale, bool(use_qk_l2norm), h0 is not None
-        ctx.keep_operators = bool(keep_operators)
-        if any(ctx.needs_input_grad[:6]):
-            o, ht, kept = fwd_chunked(q, k, v, g, beta, h0, scale=scale, use_qk_l2norm=use_qk_l2norm,
-                                      save_states=not keep_operators, save_all=keep_operators)
+        fwd_chunk = _chunked_ok(q, v)
+        # the chunked VJP covers the scalar gate; otherwise the sequential VJP runs
+        ctx.bwd_chunk = fwd_chunk and g.dim() == 3
+        ctx.keep_operators = bool(keep_operators) and ctx.bwd_chunk
+        kw = dict(scale=scale, use_qk_l2norm=use_qk_l2norm)
+        fwd = fwd_chunked if fwd_chunk else fwd_sequential
+        if any(ctx.needs_input_grad[:6]) and ctx.bwd_chunk:
+            o, ht, kept = fwd_chunked(q, k, v, g, beta, h0, save_states=not ctx.keep_operators,
+                                      save_all=ctx.keep_operators, **kw)
             ctx.save_for_backward(q, k, v, g, beta, kept)
         else:
-            o, ht = fwd_chunked(q, k, v, g, beta, h0, scale=scale, use_qk_l2norm=use_qk_l2norm)
+            o, ht = fwd(q, k, v, g, beta, h0, **kw)
+            if any(ctx.needs_input_grad[:6]):
+                ctx.save_for_backward(q, k, v, g, beta, h0)
         return o, ht
 
     @staticmethod
@@ -44,8 +57,12 @@ class GatedDeltaRuleFunction(torch.autograd.Function):
         q, k, v, g, beta, kept = ctx.saved_tensors
         do = torch.zeros_like(v) if do is None else do.to(v.dtype).contiguous()
         dht = None if dht is None else dht.to(torch.float32).contiguous()
-        handoff = {"saved": kept} if ctx.keep_operators else {"states": kept}
-        gr = bwd_chunked(q, k, v, g, beta, None, do, dht, scale=ctx.scale, use_qk_l2norm=ctx.norm, **handoff)
+        kw = dict(scale=ctx.scale, use_qk_l2norm=ctx.norm)
+        if ctx.bwd_chunk:
+            handoff = {"saved": kept} if ctx.keep_operators else {"states": kept}
+            gr = bwd_chunked(q, k, v, g, beta, None, do, dht, **handoff, **kw)
+        else:  # kept is h0 here
+            gr = bwd_sequential(q, k, v, g, beta, kept, do, dht, **kw)
         return (gr["dq"].to(q.dtype), gr["dk"].to(k.dtype), gr["dv"].to(v.dtype), gr["dg"], gr["dbeta"],
                 gr["dh0"] if ctx.has_h0 else None, None, None, None)
 

@@ -343,6 +343,41 @@ static gdr_status bwd_chunked_impl(const gdr_problem* p, const void* q, const vo
     return launch_chunk_bwd(a, st) == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
 }
 
+size_t gdr_bwd_sequential_workspace(const gdr_problem* p) {
+    if (check_problem(p, false) != GDR_OK) return 0;
+    return seq_bwd_workspace(p->B, p->T, p->Hv, p->Dk, p->Dv);
+}
+
+gdr_status gdr_bwd_sequential(const gdr_problem* p, const void* q, const void* k, const void* v, const float* g,
+                              const float* beta, const float* h0, const void* do_, const float* dht, float* dq,
+                              float* dk, float* dv, float* dg, float* dbeta, float* dh0, void* ws, size_t ws_bytes,
+                              gdr_stream_t stream) {
+    gdr_status s = check_problem(p, false);
+    if (s != GDR_OK) return s;
+    if ((s = check_ptrs(p, {q, k, v, g, beta, do_, dq, dk, dv, dg, dbeta}, {h0, dht, dh0})) != GDR_OK) return s;
+    const size_t need = seq_bwd_workspace(p->B, p->T, p->Hv, p->Dk, p->Dv);
+    if (!ws || ws_bytes < need) return GDR_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return GDR_ERR_INVALID_ARG;
+    if (p->B == 0) return GDR_OK;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (p->T == 0) {  // no token: dh0 = dht (or zero)
+        if (!dh0) return GDR_OK;
+        const size_t bytes = (size_t)p->B * p->Hv * p->Dv * p->Dk * sizeof(float);
+        cudaError_t e = dht ? cudaMemcpyAsync(dh0, dht, bytes, cudaMemcpyDeviceToDevice, st)
+                            : cudaMemsetAsync(dh0, 0, bytes, st);
+        return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+    }
+    SeqBwdArgs a;
+    a.B = p->B; a.T = p->T; a.Hk = p->Hk; a.Hv = p->Hv; a.Dk = p->Dk; a.Dv = p->Dv;
+    a.channel = p->gate == GDR_GATE_CHANNEL;
+    a.use_norm = p->use_qk_l2norm;
+    a.bf16 = p->dtype == GDR_BF16;
+    a.scale = p->scale;
+    a.q = q; a.k = k; a.v = v; a.do_ = do_; a.g = g; a.beta = beta; a.h0 = h0; a.dht = dht;
+    a.dq = dq; a.dk = dk; a.dv = dv; a.dg = dg; a.dbeta = dbeta; a.dh0 = dh0;
+    return launch_seq_bwd(a, ws, st) == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+}
+
 gdr_status gdr_workspace_status(void* ws, size_t ws_bytes, gdr_stream_t stream) {
     if (!ws || ws_bytes < 256) return GDR_ERR_INVALID_ARG;
     cudaStream_t st = (cudaStream_t)stream;

@@ -18,6 +18,19 @@ struct RecurrentArgs {
 };
 cudaError_t launch_recurrent(const RecurrentArgs& a, bool decode, cudaStream_t s);
 
+// Sequential VJP (recurrent_bwd.cu).
+struct SeqBwdArgs {
+    int B, T, Hk, Hv, Dk, Dv;
+    int channel, use_norm, bf16;
+    float scale;
+    const void *q, *k, *v, *do_;
+    const float *g, *beta, *h0, *dht;
+    float *dq, *dk, *dv, *dg, *dbeta, *dh0;
+    float *ckpt, *segs, *dqh, *dkh, *dah;  // workspace pieces, set by launch_seq_bwd
+};
+size_t seq_bwd_workspace(int B, int T, int Hv, int Dk, int Dv);
+cudaError_t launch_seq_bwd(SeqBwdArgs a, void* ws, cudaStream_t s);
+
 // Launch tracing (api.cu): no-ops unless gdr_trace_enable(1) was called.
 void trace_begin(const char* name, cudaStream_t s);
 void trace_end(cudaStream_t s);

@@ -110,6 +110,21 @@ gdr_status gdr_bwd_chunked(const gdr_problem* p, const void* q, const void* k, c
                            float* dbeta, float* dh0, void* ws, size_t ws_bytes,
                            gdr_stream_t stream);
 
+/* Sequential (token-by-token) VJP of gdr_fwd_sequential for the loss <do, o> + <dht, ht>:
+ * the "sequential case" of "Adding VJP for gated delta net" (MLX PR #4565). Every dtype, gate
+ * (scalar or per channel) and Dk, Dv in {32, 64, 128}; the reference backward for problems
+ * the chunked VJP does not cover (fp32, other head sizes, the per-channel gate). Arguments,
+ * layouts and outputs as gdr_bwd_chunked (gradients fp32; dg has g's shape). The forward is
+ * re-run with a checkpoint every 64 tokens (B*Hv*ceil(T/64) fp32 states in the workspace)
+ * and each 64-token segment is recomputed in reverse. Deterministic (fixed-order sums, no
+ * atomics). Workspace: gdr_bwd_sequential_workspace() bytes, 256-byte aligned. */
+size_t gdr_bwd_sequential_workspace(const gdr_problem* p);
+gdr_status gdr_bwd_sequential(const gdr_problem* p, const void* q, const void* k, const void* v,
+                              const float* g, const float* beta, const float* h0, const void* do_,
+                              const float* dht, float* dq, float* dk, float* dv, float* dg,
+                              float* dbeta, float* dh0, void* ws, size_t ws_bytes,
+                              gdr_stream_t stream);
+
 /* Saved-state handoff from the forward to the backward. The forward can keep the state
  * entering every chunk (bf16, opaque layout, gdr_chunk_states_bytes() bytes:
  * B*Hv*ceil(T/64)*32 KB, caller-owned, 256-byte aligned); the backward then reads them

@@ -171,3 +171,19 @@ def test_saved_operator_handoff_validation(L):
     q = prob(dtype=0)
     assert L.gdr_chunk_saved_bytes(ctypes.byref(q)) == 0
     assert L.gdr_fwd_chunked_saved(ctypes.byref(q), *[FAKE] * 8, FAKE, sb, FAKE, fw, None) == UNSUPPORTED
+
+
+def test_sequential_backward_validation(L):
+    p = prob(dtype=0, gate=1, Dk=64, Dv=64)  # fp32, per-channel gate, D=64: all supported here
+    need = L.gdr_bwd_sequential_workspace(ctypes.byref(p))
+    assert need > 0
+    assert L.gdr_bwd_sequential(ctypes.byref(p), *[FAKE] * 14, FAKE, need - 1, None) == WORKSPACE
+    ptrs = [FAKE] * 14
+    ptrs[5] = None  # h0 optional
+    ptrs[7] = None  # dht optional
+    ptrs[13] = None  # dh0 optional
+    assert L.gdr_bwd_sequential(ctypes.byref(p), *ptrs, FAKE, need - 1, None) == WORKSPACE
+    ptrs = [FAKE] * 14
+    ptrs[6] = None  # do required
+    assert L.gdr_bwd_sequential(ctypes.byref(p), *ptrs, FAKE, need, None) == INVALID
+    assert L.gdr_bwd_sequential_workspace(ctypes.byref(prob(Dk=96))) == 0

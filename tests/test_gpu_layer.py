@@ -99,3 +99,21 @@ def test_unused_outputs_and_no_grad():
     with torch.no_grad():
         o3, _ = gated_delta_rule(t["q"], t["k"], t["v"], t["g"], t["beta"], None)
     assert torch.equal(o3, o.detach())
+
+
+@pytest.mark.parametrize("dtype,D,gate,tol", [(torch.bfloat16, 128, "channel", BF16_TOL),
+                                              (torch.float32, 64, "scalar", 1e-4),
+                                              (torch.float32, 32, "channel", 1e-4)],
+                         ids=["bf16-D128-channel", "fp32-D64-scalar", "fp32-D32-channel"])
+def test_autograd_outside_the_chunked_vjp(dtype, D, gate, tol):
+    """Problems the chunked VJP does not cover run the sequential kernels under autograd."""
+    dev = cuda_device()
+    x = make_inputs(Shape(1, 100, 1, 2, D, D), dtype=dtype, seed=41, gate=gate, grads=True, gate_scale=0.3)
+    t = leaves(x, dev)
+    o, ht = gated_delta_rule(t["q"], t["k"], t["v"], t["g"], t["beta"], t["h0"])
+    ((o.float() * x["do"].to(dev).float()).sum() + (ht * x["dht"].to(dev)).sum()).backward()
+    ro, rht = oracle.forward(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"])
+    ref = oracle.backward(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"], x["do"], x["dht"])
+    assert rel_err(o.detach(), ro) <= tol and rel_err(ht.detach(), rht) <= tol
+    errs = {n: rel_err(t[n].grad, ref["d" + n]) for n in INPUTS}
+    assert all(e <= tol for e in errs.values()), errs

@@ -13,7 +13,8 @@ times from the library's launch trace, recorded on the launch stream), the same 
 to end with pinned-host inputs/outputs copied inside the timed region, the decode step's
 state bandwidth (B=32, channel gate, fp32, L2 flushed before every step), the short-prefill
 crossover of the sequential and chunked forwards (T = 1..256 continuing a B=32 state), the
-per-channel-gate chunked prefill (T=4096) beside the scalar-gate one and the sequential kernel, SM clocks
+per-channel-gate chunked prefill (T=4096) beside the scalar-gate one and the sequential kernel, the
+chunked vs sequential VJP over the pages' B x T grid, SM clocks
 sampled during the timed region, and the fp64 CPU oracle timed on a bounded sample.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mine|reference]
@@ -191,6 +192,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the short-prefill crossover table")
     ap.add_argument("--no-channel", action="store_true", help="skip the per-channel gate prefill timing")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the chunked vs sequential VJP sweep")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     set_tokens(args.tokens)
@@ -485,6 +487,13 @@ def main():
             calls = {"chunked": lambda: raise_on(L.gdr_fwd_chunked(ctypes.byref(pc), *ins, P(wsc), nwc, sp))}
             if gate == "channel":
                 calls["sequential"] = lambda: raise_on(L.gdr_fwd_sequential(ctypes.byref(pc), *ins, sp))
+                # its backward (the sequential VJP: the chunked VJP covers the scalar gate)
+                dco = torch.randn(dc["v"].shape, device=dev).to(torch.bfloat16)
+                gout = [torch.empty(dc[n].shape, **f32) for n in ("q", "k", "v", "g", "beta", "h0")]
+                nbw = int(L.gdr_bwd_sequential_workspace(ctypes.byref(pc)))
+                wbw = torch.empty(nbw, dtype=torch.uint8, device=dev)
+                bins = [P(dc[n]) for n in ("q", "k", "v", "g", "beta", "h0")] + [P(dco), None] + [P(t) for t in gout]
+                calls["bwd_sequential"] = lambda: raise_on(L.gdr_bwd_sequential(ctypes.byref(pc), *bins, P(wbw), nbw, sp))
             for name, fn in calls.items():
                 for _ in range(3):
                     fn()
@@ -506,6 +515,43 @@ def main():
         chan = {"config": "B=1, T=4096, Hk=16, Hv=32, Dk=Dv=128, bf16, h0 ~ N(0,0.02), L2 flushed, median of 5",
                 "tokens_per_s_channel_chunked": toks / (res["channel_chunked_us"] * 1e-6), **res}
         del flush
+
+    # ------------------------------------------------------------------ VJP sweep: chunked vs sequential
+    sweep = None
+    if not args.no_sweep:
+        from gated_delta_rule_31_gb300.synth import VJP_SWEEP
+
+        rows = []
+        for sh in VJP_SWEEP:
+            xs = make_inputs(sh, dtype=torch.bfloat16, seed=1200, grads=True)
+            ds = {k: v.to(dev) for k, v in xs.items() if v is not None}
+            ps = gdr.Problem(sh.B, sh.T, sh.Hk, sh.Hv, D, D, gdr.GDR_BF16, gdr.GDR_GATE_SCALAR, D ** -0.5, 1)
+            outs = [torch.empty(ds[n].shape, **f32) for n in ("q", "k", "v", "g", "beta", "h0")]
+            ins = [P(ds[n]) for n in ("q", "k", "v", "g", "beta", "h0", "do", "dht")] + [P(t) for t in outs]
+            ncw, nsw = gdr.bwd_workspace_bytes(ps), int(L.gdr_bwd_sequential_workspace(ctypes.byref(ps)))
+            wcw = torch.empty(ncw, dtype=torch.uint8, device=dev)
+            wsw = torch.empty(nsw, dtype=torch.uint8, device=dev)
+            calls = {"chunked": lambda: raise_on(L.gdr_bwd_chunked(ctypes.byref(ps), *ins, P(wcw), ncw, sp)),
+                     "sequential": lambda: raise_on(L.gdr_bwd_sequential(ctypes.byref(ps), *ins, P(wsw), nsw, sp))}
+            row = {"B": sh.B, "T": sh.T}
+            for name, fn in calls.items():
+                fn()
+                torch.cuda.synchronize(dev)
+                reps = 5 if name == "chunked" else 2
+                g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                g0.record(stream)
+                for _ in range(reps):
+                    fn()
+                g1.record(stream)
+                torch.cuda.synchronize(dev)
+                row[name + "_us"] = 1e3 * g0.elapsed_time(g1) / reps
+            row["speedup"] = row["sequential_us"] / row["chunked_us"]
+            rows.append(row)
+            del ds, outs, wcw, wsw
+        sweep = {"config": "backward (VJP) of <do,o> + <dht,ht>, Hk=16, Hv=32, D=128, bf16, scalar gate, "
+                           "do ~ N(0,1), dht ~ N(0,0.01); back-to-back launches",
+                 "rows": rows,
+                 "pages": "chunked VJP 1.4x-6.3x faster than the sequential one on Apple silicon (MLX), same grid"}
 
     # ------------------------------------------------------------------ CPU baseline (rank 0, N=1)
     cpu = None
@@ -532,7 +578,7 @@ def main():
                                      "note": "optional: forward also keeps the chunk operators, backward runs no "
                                              "prep (chunk-local terms stored, not recomputed)"},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(round(launches_per_step * args.steps)),
-            "clocks": clocks, "kernels": kern, "decode": dec, "short_prefill": pre, "channel_prefill": chan,
+            "clocks": clocks, "kernels": kern, "decode": dec, "short_prefill": pre, "channel_prefill": chan, "vjp_sweep": sweep,
         }
         print(json.dumps(line))
     if world > 1:

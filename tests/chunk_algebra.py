@@ -173,3 +173,60 @@ def backward(q, k, v, g, beta, h0, do, dht, scale, norm=True, C=64):
                     else:
                         Dst[b_, s:e, hk] = Xn
     return dict(dq=dq, dk=dk, dv=dv, dg=dg, dbeta=dbeta, dh0=dh0)
+
+
+def chunk_ops_channel(K, Q, V, g, beta, scale, rk, rq):
+    """Per-channel gate g [C, Dk], written as the per-channel kernel forms it: every decay is a
+    product of per-token factors a_t = exp(g_t) <= 1 (E_rj = prod_{j<t<=r} a_t per channel,
+    Gamma_r = prod_{t<=r} a_t, Kbar's factor prod_{t>r} a_t), never an exp of a difference."""
+    C, Dk = K.shape
+    a = np.exp(g)
+    Gam = np.cumprod(a, axis=0)                                   # [C, Dk]
+    suf = np.ones_like(a)                                         # prod_{t>r} a_t
+    for r in range(C - 2, -1, -1):
+        suf[r] = suf[r + 1] * a[r + 1]
+    E = np.zeros((C, C, Dk))                                      # E[r, j, :] for j <= r
+    for j in range(C):
+        e = np.ones(Dk)
+        for r in range(j, C):
+            if r > j:
+                e = e * a[r]
+            E[r, j] = e
+    Kh, Qh = rk[:, None] * K, rq[:, None] * Q
+    A = np.zeros((C, C))
+    P = np.zeros((C, C))
+    for r in range(C):
+        for j in range(r + 1):
+            if j < r:
+                A[r, j] = beta[r] * np.sum(Kh[r] * Kh[j] * E[r, j])
+            P[r, j] = scale * np.sum(Qh[r] * Kh[j] * E[r, j])
+    T = np.linalg.inv(np.eye(C) + A)
+    W = T @ (beta[:, None] * (Kh * Gam))
+    Ut = T @ (beta[:, None] * V)
+    Kbar = Kh * suf
+    Mneg = -Kbar.T @ W
+    Qc = scale * Qh * Gam - P @ W
+    return dict(GamC=Gam[-1], W=W, Ut=Ut, P=P, Kbar=Kbar, Mneg=Mneg, Qc=Qc)
+
+
+def forward_channel(q, k, v, g, beta, h0, scale, norm=True, C=64):
+    """Per-channel gate: o, ht with H1 = diag(Gamma_C) H0 + Mneg H0 + Kbar^T U~ per chunk."""
+    B, T, Hk, Dk = q.shape
+    Hv, Dv = v.shape[2:]
+    grp = Hv // Hk
+    o = np.zeros((B, T, Hv, Dv))
+    ht = np.zeros((B, Hv, Dv, Dk))
+    for b_ in range(B):
+        for hv in range(Hv):
+            hk = hv // grp
+            H = np.zeros((Dk, Dv)) if h0 is None else h0[b_, hv].T.copy()
+            for s, e in _chunks(T, C):
+                K = _pad(k[b_, s:e, hk], C)
+                Q = _pad(q[b_, s:e, hk], C)
+                ops = chunk_ops_channel(K, Q, _pad(v[b_, s:e, hv], C), _pad(g[b_, s:e, hv], C),
+                                        _pad(beta[b_, s:e, hv], C), scale, _norm_factor(K, norm), _norm_factor(Q, norm))
+                O = ops["Qc"] @ H + ops["P"] @ ops["Ut"]
+                H = ops["GamC"][:, None] * H + ops["Mneg"] @ H + ops["Kbar"].T @ ops["Ut"]
+                o[b_, s:e, hv] = O[: e - s]
+            ht[b_, hv] = H.T
+    return o, ht

@@ -26,3 +26,17 @@ def test_chunk_forward_and_backward_equal_oracle(C, T, Hk, Hv, norm, h0):
     for name in ("dq", "dk", "dv", "dg", "dbeta", "dh0"):
         err = np.max(np.abs(ref[name] - got[name])) / max(1.0, np.max(np.abs(ref[name])))
         assert err < 1e-10, (name, err)
+
+
+@pytest.mark.parametrize("C,T,Hk,Hv,norm,h0,gs", [(4, 11, 1, 2, True, True, 1.0), (8, 16, 2, 4, True, False, 1.0),
+                                                  (5, 5, 1, 2, False, True, 1.0), (16, 21, 1, 1, True, True, 8.0)])
+def test_channel_chunk_forward_equals_oracle(C, T, Hk, Hv, norm, h0, gs):
+    """The per-channel chunk algebra (decays as products of per-token factors, diag(Gamma_C)
+    in the state update) equals the sequential oracle; gs = 8 makes per-token factors as small
+    as e^-40, where a factorised form exp(gamma_r) exp(-gamma_j) would overflow."""
+    q, k, v, g, beta, hh = rand_inputs(B=2, T=T, Hk=Hk, Hv=Hv, Dk=6, Dv=5, channel=True, seed=3 * C + T, h0=h0,
+                                       gate_scale=gs)
+    o, ht = oracle.forward(q, k, v, g, beta, hh, scale=0.7, use_qk_l2norm=norm)
+    o2, ht2 = ca.forward_channel(q, k, v, g, beta, hh, 0.7, norm, C)
+    assert np.max(np.abs(o - o2)) < 1e-11 * max(1.0, np.max(np.abs(o)))
+    assert np.max(np.abs(ht - ht2)) < 1e-11 * max(1.0, np.max(np.abs(ht)))

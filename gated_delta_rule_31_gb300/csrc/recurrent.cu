@@ -82,15 +82,34 @@ __global__ void __launch_bounds__(WARPS * 32) recurrent_rows_kernel(RecurrentArg
     const TIn* v = reinterpret_cast<const TIn*>(a.v);
     TIn* o = reinterpret_cast<TIn*>(a.o);
 
-    for (int t = 0; t < a.T; t++) {
+    // the raw inputs of token t + 1 are loaded while token t is processed
+    struct Raw {
+        float k[EL], q[EL], g[EL], beta, v[ROWS];
+    };
+    auto load_raw = [&](int t, Raw& x) {
         const size_t qk_off = (((size_t)b * a.T + t) * a.Hk + hk) * DK + c0;
+        const size_t bt = ((size_t)b * a.T + t) * a.Hv + hv;
+#pragma unroll
+        for (int e = 0; e < EL; e++) {
+            x.k[e] = to_f(k[qk_off + e]);
+            x.q[e] = to_f(q[qk_off + e]);
+            x.g[e] = a.channel ? a.g[bt * DK + c0 + e] : (e == 0 ? a.g[bt] : 0.f);
+        }
+        x.beta = a.beta[bt];
+#pragma unroll
+        for (int i = 0; i < ROWS; i++) x.v[i] = (r0 + i < a.Dv) ? to_f(v[bt * (size_t)a.Dv + r0 + i]) : 0.f;
+    };
+    Raw cur, nxt;
+    if (a.T > 0) load_raw(0, cur);
+    for (int t = 0; t < a.T; t++) {
+        if (t + 1 < a.T) load_raw(t + 1, nxt);
         const size_t bt = ((size_t)b * a.T + t) * a.Hv + hv;
         float kh[EL], qh[EL], dec[EL];
         float sk = 0.f, sq = 0.f;
 #pragma unroll
         for (int e = 0; e < EL; e++) {
-            kh[e] = to_f(k[qk_off + e]);
-            qh[e] = to_f(q[qk_off + e]);
+            kh[e] = cur.k[e];
+            qh[e] = cur.q[e];
             sk += kh[e] * kh[e];
             sq += qh[e] * qh[e];
         }
@@ -106,13 +125,13 @@ __global__ void __launch_bounds__(WARPS * 32) recurrent_rows_kernel(RecurrentArg
         }
         if (a.channel) {
 #pragma unroll
-            for (int e = 0; e < EL; e++) dec[e] = expf(a.g[bt * DK + c0 + e]);
+            for (int e = 0; e < EL; e++) dec[e] = expf(cur.g[e]);
         } else {
-            const float s = expf(a.g[bt]);
+            const float s = expf(cur.g[0]);
 #pragma unroll
             for (int e = 0; e < EL; e++) dec[e] = s;
         }
-        const float beta = a.beta[bt];
+        const float beta = cur.beta;
         const size_t vo = bt * (size_t)a.Dv + r0;
         // pass 1: prediction with the decay folded in
         float p[ROWS];
@@ -131,8 +150,7 @@ __global__ void __launch_bounds__(WARPS * 32) recurrent_rows_kernel(RecurrentArg
         float out[ROWS];
 #pragma unroll
         for (int i = 0; i < ROWS; i++) {
-            const float vi = (r0 + i < a.Dv) ? to_f(v[vo + i]) : 0.f;
-            const float d = beta * (vi - p[i]);
+            const float d = beta * (cur.v[i] - p[i]);
             float acc = 0.f;
 #pragma unroll
             for (int e = 0; e < EL; e++) {
@@ -148,6 +166,7 @@ __global__ void __launch_bounds__(WARPS * 32) recurrent_rows_kernel(RecurrentArg
 #pragma unroll
         for (int i = 0; i < ROWS; i++)
             if (lane == i && r0 + i < a.Dv) o[vo + i] = from_f<TIn>(a.scale * out[i]);
+        cur = nxt;
     }
     if (a.ht) {
 #pragma unroll
@@ -295,7 +314,6 @@ static cudaError_t launch_dk(const RecurrentArgs& a, cudaStream_t s) {
     }
 }
 
-// The multi-token path is latency bound: 2 rows per warp, small blocks.
 template <typename TIn>
 static cudaError_t launch_decode_dk(const RecurrentArgs& a, cudaStream_t s) {
     switch (a.Dk) {
@@ -308,6 +326,11 @@ static cudaError_t launch_decode_dk(const RecurrentArgs& a, cudaStream_t s) {
 
 cudaError_t launch_recurrent(const RecurrentArgs& a, bool decode, cudaStream_t s) {
     if (decode) return a.bf16 ? launch_decode_dk<__nv_bfloat16>(a, s) : launch_decode_dk<float>(a, s);
+    // Few rows in flight (small B * Hv): 2 rows per warp, the most warps. Many rows: 8 rows per
+    // warp, so the grid stays near one wave and each warp overlaps 8 rows' reductions.
+    const long long rows = (long long)a.B * a.Hv * a.Dv;
+    if (rows > 16384)
+        return a.bf16 ? launch_dk<__nv_bfloat16, 8, 4>(a, s) : launch_dk<float, 8, 4>(a, s);
     return a.bf16 ? launch_dk<__nv_bfloat16, 2, 4>(a, s) : launch_dk<float, 2, 4>(a, s);
 }
 

@@ -36,21 +36,39 @@ struct TokenIn {  // this lane's columns of the token's key-side vectors
     float beta, ga;  // ga: the scalar gate's a (channel gate: unused)
 };
 
-// Loads k^, q^ (normalised when asked), a = exp(g) and beta of token t.
+// Raw inputs of token t (this lane's columns of k, q, g; beta): loaded one token ahead.
+template <int DK>
+struct TokenRaw {
+    float k[DK / 32], q[DK / 32], g[DK / 32], beta;
+};
 template <int DK, typename TIn>
-__device__ __forceinline__ void load_token(const SeqBwdArgs& A, int b, int hk, int hv, int t, int lane,
-                                           TokenIn<DK, TIn>& x, bool need_q) {
+__device__ __forceinline__ void load_raw(const SeqBwdArgs& A, int b, int hk, int hv, int t, int lane,
+                                         TokenRaw<DK>& r, bool need_q) {
     constexpr int CPL = DK / 32;
     const TIn* kp = static_cast<const TIn*>(A.k) + (((size_t)b * A.T + t) * A.Hk + hk) * DK;
     const TIn* qp = static_cast<const TIn*>(A.q) + (((size_t)b * A.T + t) * A.Hk + hk) * DK;
     const size_t bt = ((size_t)b * A.T + t) * A.Hv + hv;
+#pragma unroll
+    for (int c = 0; c < CPL; c++) {
+        r.k[c] = ldf(kp + lane + 32 * c);
+        r.q[c] = need_q ? ldf(qp + lane + 32 * c) : 0.f;
+        r.g[c] = A.channel ? A.g[bt * DK + lane + 32 * c] : (c == 0 ? A.g[bt] : 0.f);
+    }
+    r.beta = A.beta[bt];
+}
+
+// k^, q^ (normalised when asked), a = exp(g) and beta of a token from its raw inputs.
+template <int DK, typename TIn>
+__device__ __forceinline__ void load_token(const SeqBwdArgs& A, const TokenRaw<DK>& r, TokenIn<DK, TIn>& x,
+                                           bool need_q) {
+    constexpr int CPL = DK / 32;
     float sk = 0.f, sq = 0.f;
 #pragma unroll
     for (int c = 0; c < CPL; c++) {
-        x.k[c] = ldf(kp + lane + 32 * c);
+        x.k[c] = r.k[c];
         sk += x.k[c] * x.k[c];
         if (need_q) {
-            x.q[c] = ldf(qp + lane + 32 * c);
+            x.q[c] = r.q[c];
             sq += x.q[c] * x.q[c];
         }
     }
@@ -65,18 +83,17 @@ __device__ __forceinline__ void load_token(const SeqBwdArgs& A, int b, int hk, i
         }
     }
     if (A.channel) {
-        const float* gp = A.g + bt * DK;
 #pragma unroll
-        for (int c = 0; c < CPL; c++) x.a[c] = expf(gp[lane + 32 * c]);
+        for (int c = 0; c < CPL; c++) x.a[c] = expf(r.g[c]);
         x.ga = 0.f;
     } else {
-        x.ga = expf(A.g[bt]);
+        x.ga = expf(r.g[0]);
 #pragma unroll
         for (int c = 0; c < CPL; c++) x.a[c] = x.ga;
     }
 #pragma unroll
     for (int c = 0; c < CPL; c++) x.ak[c] = x.a[c] * x.k[c];
-    x.beta = A.beta[bt];
+    x.beta = r.beta;
 }
 
 template <int DK, typename TIn>
@@ -122,10 +139,14 @@ __global__ void __launch_bounds__(512) seq_bwd_kernel(SeqBwdArgs A) {
     };
 
     // ---- forward pass: checkpoint the state entering every segment
+    TokenRaw<DK> cur, nxt;
+    load_raw<DK, TIn>(A, b, hk, hv, 0, lane, cur, false);
     for (int t = 0; t < T; t++) {
+        if (t + 1 < T) load_raw<DK, TIn>(A, b, hk, hv, t + 1, lane, nxt, false);
         TokenIn<DK, TIn> x;
-        load_token<DK, TIn>(A, b, hk, hv, t, lane, x, false);
+        load_token<DK, TIn>(A, cur, x, false);
         step(x, t, (t % kSeg) == 0 ? ckpt + (size_t)(t / kSeg) * plane : nullptr);
+        cur = nxt;
     }
 
     // ---- reverse pass
@@ -142,14 +163,19 @@ __global__ void __launch_bounds__(512) seq_bwd_kernel(SeqBwdArgs A) {
 #pragma unroll
             for (int c = 0; c < CPL; c++)
                 S[r][c] = ckpt[(size_t)sg * plane + (size_t)(row0 + r) * DK + lane + 32 * c];
+        load_raw<DK, TIn>(A, b, hk, hv, t0, lane, cur, false);
         for (int t = t0; t < t1; t++) {
+            if (t + 1 < t1) load_raw<DK, TIn>(A, b, hk, hv, t + 1, lane, nxt, false);
             TokenIn<DK, TIn> x;
-            load_token<DK, TIn>(A, b, hk, hv, t, lane, x, false);
+            load_token<DK, TIn>(A, cur, x, false);
             step(x, t, segs + (size_t)(t - t0) * plane);
+            cur = nxt;
         }
+        load_raw<DK, TIn>(A, b, hk, hv, t1 - 1, lane, cur, true);
         for (int t = t1 - 1; t >= t0; t--) {
+            if (t - 1 >= t0) load_raw<DK, TIn>(A, b, hk, hv, t - 1, lane, nxt, true);
             TokenIn<DK, TIn> x;
-            load_token<DK, TIn>(A, b, hk, hv, t, lane, x, true);
+            load_token<DK, TIn>(A, cur, x, true);
             const float* Sp_all = segs + (size_t)(t - t0) * plane;
             float dq[CPL], dk[CPL], da[CPL], dbeta = 0.f;
 #pragma unroll
@@ -214,6 +240,7 @@ __global__ void __launch_bounds__(512) seq_bwd_kernel(SeqBwdArgs A) {
                 for (int w = 0; w < nw; w++) s += rr[w * NRED + 3 * DK];
                 A.dbeta[bt] = s;
             }
+            cur = nxt;
         }
     }
 #pragma unroll

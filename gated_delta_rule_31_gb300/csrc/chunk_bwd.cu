@@ -318,7 +318,8 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
         uint4 utv[4];  // U~ slice qt (columns c32..) from the record, fetched while M1 runs
         if (act) {
 #pragma unroll
-            for (int q = 0; q < 4; q++) utv[q] = *reinterpret_cast<const uint4*>(rec + REC_U + qt * 4096 + sw64_chunk(r, q));
+            for (int q = 0; q < 4; q++)
+                utv[q] = *reinterpret_cast<const uint4*>(rec + REC_U + qt * 4096 + sw64_chunk(r, q));
         }
         if (!wait_mma(43)) goto teardown;
         if (tid == 0) {
@@ -526,7 +527,8 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
                                                                 c32);
 #pragma unroll
                         for (int q = 0; q < 8; q++)
-                            dst[q] = make_float4(bb * x[4 * q], bb * x[4 * q + 1], bb * x[4 * q + 2], bb * x[4 * q + 3]);
+                            dst[q] = make_float4(bb * x[4 * q], bb * x[4 * q + 1], bb * x[4 * q + 2],
+                                                 bb * x[4 * q + 3]);
                     }
                 }
             }
@@ -635,7 +637,8 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
                 nrow[e] = rk[j] * (MF[fsw(r, j)] + MF[fsw(j, r)]);
             }
 #pragma unroll
-            for (int q = 0; q < 2; q++) st_chunk8(sb + G_DH + 16384 + sw128_chunk(r, 2 * qt + q, 64), nrow + 8 * q, 1.f);
+            for (int q = 0; q < 2; q++)
+                st_chunk8(sb + G_DH + 16384 + sw128_chunk(r, 2 * qt + q, 64), nrow + 8 * q, 1.f);
         }
         sync_for_mma();
 

@@ -8,7 +8,11 @@
 
 namespace gdr {
 
-constexpr int LDA = 65;  // row stride (floats) of the fp32 [64 x 64] A / T tiles in shared memory
+// Row stride (floats) of the fp32 [64 x 64] A / T tiles in shared memory: rows start on 16-byte
+// boundaries, so rows and 4-column strips move as float4.
+constexpr int LDA = 68;
+constexpr int LDY = 20;  // row stride of the [16 x 16] Y blocks of the solve scratch (float4 rows)
+constexpr int SOLVE_SCRATCH_BYTES = 6 * 16 * LDY * 4;
 
 __device__ __forceinline__ void unpack8(const uint4& u, float* x) {
     x[0] = bf16lo(u.x); x[1] = bf16hi(u.x); x[2] = bf16lo(u.y); x[3] = bf16hi(u.y);
@@ -27,9 +31,11 @@ __device__ __forceinline__ void st_global16(uint8_t* p, const uint4& u) { *reint
 // T = (I + A)^-1 for the strictly lower triangular fp32 A [64 x 64] (row stride LDA), by 16 x 16
 // blocks. Phase 1 (160 threads, one column each): forward substitution with L_II = I + A_II
 // gives the diagonal inverses T_II (right-hand side e_c) and Y_IK = T_II A_IK for I > K
-// (right-hand side column c of A_IK). Then T_IJ = -sum_{J<=K<I} Y_IK T_KJ by block distance
-// I - J = 1, 2, 3. Called by all 256 threads of the CTA; ends with a CTA barrier. T's blocks
-// above the block diagonal are not written (they are zero). Xs: [6][16][17] fp32 scratch.
+// (right-hand side column c of A_IK); rows of L_II are read as float4. Then, by block distance
+// I - J = 1, 2, 3, T_IJ = -sum_{J<=K<I} Y_IK T_KJ with one thread per (block, row, 4-column
+// strip), reading Y rows and T strips as float4. Called by all 256 threads of the CTA; ends
+// with a CTA barrier. T's blocks above the block diagonal are not written (they are zero).
+// Xs: [6][16][LDY] fp32 scratch.
 __device__ __forceinline__ void ut_solve(const float* Am, float* Tm, float* Xs, int tid) {
     if (tid < 160) {
         int I, K, cc;
@@ -49,41 +55,52 @@ __device__ __forceinline__ void ut_solve(const float* Am, float* Tm, float* Xs, 
         float y[16];
 #pragma unroll
         for (int i = 0; i < 16; i++) {
+            float l[16];
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                if (4 * q < i) {
+                    const float4 f = *reinterpret_cast<const float4*>(Ab + i * LDA + 4 * q);
+                    l[4 * q] = f.x; l[4 * q + 1] = f.y; l[4 * q + 2] = f.z; l[4 * q + 3] = f.w;
+                }
+            }
             float s = diag ? (i == cc ? 1.f : 0.f) : Bc[i * LDA];
 #pragma unroll
-            for (int j = 0; j < i; j++) s -= Ab[i * LDA + j] * y[j];
+            for (int j = 0; j < i; j++) s -= l[j] * y[j];
             y[i] = s;
         }
         if (diag) {
 #pragma unroll
             for (int i = 0; i < 16; i++) Tm[(16 * I + i) * LDA + 16 * I + cc] = y[i];
         } else {
-            float* yp = Xs + ((tid - 64) >> 4) * (16 * 17);
+            float* yp = Xs + ((tid - 64) >> 4) * (16 * LDY);
 #pragma unroll
-            for (int i = 0; i < 16; i++) yp[i * 17 + cc] = y[i];
+            for (int i = 0; i < 16; i++) yp[i * LDY + cc] = y[i];
         }
     }
     __syncthreads();
-    // item J of a level is block (J + dlev, J); all sums are formed before any store
     for (int dlev = 1; dlev <= 3; dlev++) {
-        const int nb = 4 - dlev;
-        const int i = (tid >> 4) & 15, cc = tid & 15;
-        float s[3] = {0.f, 0.f, 0.f};
+        const int J = tid >> 6, i = (tid >> 2) & 15, c4 = tid & 3;  // block (J + dlev, J), row i, cols 4 c4..
+        if (J < 4 - dlev) {
+            const int I = J + dlev;
+            float s[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int K = J; K < I; K++) {
+                const float* yr = Xs + (I * (I - 1) / 2 + K) * (16 * LDY) + i * LDY;
+                float y[16];
 #pragma unroll
-        for (int J = 0; J < 3; J++) {
-            if (J < nb) {
-                const int I = J + dlev;
-                for (int K = J; K < I; K++) {
-                    const float* yr = Xs + (I * (I - 1) / 2 + K) * (16 * 17) + i * 17;
-                    const float* tc = Tm + (16 * K) * LDA + 16 * J + cc;
+                for (int q = 0; q < 4; q++) {
+                    const float4 f = *reinterpret_cast<const float4*>(yr + 4 * q);
+                    y[4 * q] = f.x; y[4 * q + 1] = f.y; y[4 * q + 2] = f.z; y[4 * q + 3] = f.w;
+                }
+                const float* tc = Tm + (16 * K) * LDA + 16 * J + 4 * c4;
 #pragma unroll
-                    for (int m = 0; m < 16; m++) s[J] += yr[m] * tc[m * LDA];
+                for (int m = 0; m < 16; m++) {
+                    const float4 t = *reinterpret_cast<const float4*>(tc + m * LDA);
+                    s[0] += y[m] * t.x; s[1] += y[m] * t.y; s[2] += y[m] * t.z; s[3] += y[m] * t.w;
                 }
             }
+            *reinterpret_cast<float4*>(Tm + (16 * I + i) * LDA + 16 * J + 4 * c4) =
+                make_float4(-s[0], -s[1], -s[2], -s[3]);
         }
-#pragma unroll
-        for (int J = 0; J < 3; J++)
-            if (J < nb) Tm[(16 * (J + dlev) + i) * LDA + 16 * J + cc] = -s[J];
         __syncthreads();
     }
 }

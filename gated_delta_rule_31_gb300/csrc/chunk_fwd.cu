@@ -30,11 +30,11 @@ namespace gdr {
 // the record images go straight from registers to global memory, nothing is staged.
 constexpr uint32_t PS_KQ = 0;        // k rows 0-63 / q rows 64-127 of a 128-row tile (panels 16 KB)
 constexpr uint32_t PS_V = 32768;     // v [64 tok x 128] (panels 8 KB)
-constexpr uint32_t PS_A = 49152;     // A fp32 [64][65]; then [Tw; Tu] 128 x 64 bf16; then Wbar image
-constexpr uint32_t PS_T = 66560;     // T fp32 [64][65]; then W image [64 x 128]
+constexpr uint32_t PS_A = 49152;     // A fp32 [64][LDA]; then [Tw; Tu] 128 x 64 bf16; then Wbar image
+constexpr uint32_t PS_T = 66560;     // T fp32 [64][LDA]; then W image [64 x 128]
 constexpr uint32_t PS_P = 83968;     // P image [64 x 64]
-constexpr uint32_t PS_SCR = 92160;   // solve scratch: Y_IK blocks [6][16][17] fp32
-constexpr uint32_t PS_SMALL = PS_SCR + 6 * 16 * 17 * 4;  // per-token factors (8 x 64 fp32)
+constexpr uint32_t PS_SCR = 92160;   // solve scratch: Y_IK blocks [6][16][LDY] fp32
+constexpr uint32_t PS_SMALL = PS_SCR + SOLVE_SCRATCH_BYTES;  // per-token factors (8 x 64 fp32)
 constexpr uint32_t PS_BYTES = PS_SMALL + 2048;
 constexpr uint32_t PS_TT = PS_A, PS_WBAR = PS_A, PS_W = PS_T;
 static_assert(PS_A % 1024 == 0 && PS_T % 1024 == 0 && PS_P % 1024 == 0, "align");
@@ -199,7 +199,9 @@ __global__ void __launch_bounds__(256, 2)
                 }
                 if (arow) {
 #pragma unroll
-                    for (int jj = 0; jj < 32; jj++) Am[i * LDA + 32 * h + jj] = v[jj];
+                    for (int q = 0; q < 8; q++)
+                        *reinterpret_cast<float4*>(Am + i * LDA + 32 * h + 4 * q) =
+                            make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
                 } else {
 #pragma unroll
                     for (int q = 0; q < 4; q++) {
@@ -223,10 +225,16 @@ __global__ void __launch_bounds__(256, 2)
                 const float* fac = (isw ? fw : bet) + 32 * half;
                 float t[32], x[32];
 #pragma unroll
-                for (int jj = 0; jj < 32; jj++) {  // all loads first (see the A/P epilogue)
-                    const int j = 32 * half + jj;
-                    t[jj] = (j >> 4) <= (i >> 4) ? trow[jj] : 0.f;
-                    x[jj] = t[jj] * fac[jj];
+                for (int q = 0; q < 8; q++) {  // all loads first (see the A/P epilogue)
+                    const float4 f = *reinterpret_cast<const float4*>(trow + 4 * q);
+                    const float4 w = *reinterpret_cast<const float4*>(fac + 4 * q);
+                    const float tv[4] = {f.x, f.y, f.z, f.w}, wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int e = 0; e < 4; e++) {
+                        const int j = 32 * half + 4 * q + e;
+                        t[4 * q + e] = (j >> 4) <= (i >> 4) ? tv[e] : 0.f;
+                        x[4 * q + e] = t[4 * q + e] * wv[e];
+                    }
                 }
 #pragma unroll
                 for (int q = 0; q < 4; q++) {
@@ -582,7 +590,8 @@ __global__ void __launch_bounds__(192, 1) scan_kernel(const __grid_constant__ CU
             float D[32], O[32];
             if (ok) tmem_ld32(tmem_at(tm, 32 * lg, 32 * s), D);
             if (MODE == SCAN_FWD_OUT && i > 0 && ok) {
-                ok = __all_sync(0xffffffffu, mbar_wait(&ofull[(i - 1) & 1], ((i - 1) >> 1) & 1, &abort_sh, a.status, 31));
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(&ofull[(i - 1) & 1], ((i - 1) >> 1) & 1, &abort_sh, a.status, 31));
                 tc_fence_after();
                 if (ok) tmem_ld32(tmem_at(tm, 32 * lg, 64 + 32 * ((i - 1) & 1)), O);
             }
@@ -609,7 +618,8 @@ __global__ void __launch_bounds__(192, 1) scan_kernel(const __grid_constant__ CU
         }
         if (!bad && MODE == SCAN_FWD_OUT) {  // outputs of the last chunk
             const int i_last = NC - 1;
-            bool ok = __all_sync(0xffffffffu, mbar_wait(&ofull[i_last & 1], (i_last >> 1) & 1, &abort_sh, a.status, 32));
+            bool ok = __all_sync(0xffffffffu,
+                                 mbar_wait(&ofull[i_last & 1], (i_last >> 1) & 1, &abort_sh, a.status, 32));
             tc_fence_after();
             float O[32];
             if (ok) tmem_ld32(tmem_at(tm, 32 * lg, 64 + 32 * (i_last & 1)), O);

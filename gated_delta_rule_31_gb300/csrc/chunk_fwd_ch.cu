@@ -35,8 +35,8 @@ constexpr uint32_t CS_T = 132096;     // T fp32 [64][LDA]; then the W image [64 
 constexpr uint32_t CS_P = 149504;     // P image [64 x 64]
 constexpr uint32_t CS_KG = 157696;    // K .* Gamma image [64 x 128]
 constexpr uint32_t CS_KB = 174080;    // Kbar image [64 x 128]
-constexpr uint32_t CS_SCR = 190464;   // solve scratch [6][16][17] fp32
-constexpr uint32_t CS_SMALL = CS_SCR + 6 * 16 * 17 * 4;  // bet[64], rho[128]
+constexpr uint32_t CS_SCR = 190464;   // solve scratch [6][16][LDY] fp32
+constexpr uint32_t CS_SMALL = CS_SCR + SOLVE_SCRATCH_BYTES;  // bet[64], rho[128]
 constexpr uint32_t CS_BYTES = CS_SMALL + 1024;
 static_assert(CS_A % 1024 == 0 && CS_T % 1024 == 0 && CS_P % 1024 == 0 && CS_KG % 1024 == 0 &&
                   CS_KB % 1024 == 0, "operand images need 1024-byte alignment");
@@ -216,10 +216,15 @@ __global__ void __launch_bounds__(256, 1)
         const float* trow = Tm + i * LDA + 32 * half;
         float x[32];
 #pragma unroll
-        for (int jj = 0; jj < 32; jj++) {
-            const int j = 32 * half + jj;
-            const float t = (j >> 4) <= (i >> 4) ? trow[jj] : 0.f;
-            x[jj] = t * bet[j] * (isw ? rho[j] : 1.f);
+        for (int q = 0; q < 8; q++) {
+            const float4 f = *reinterpret_cast<const float4*>(trow + 4 * q);
+            const float tv[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                const int j = 32 * half + 4 * q + e;
+                const float t = (j >> 4) <= (i >> 4) ? tv[e] : 0.f;
+                x[4 * q + e] = t * bet[j] * (isw ? rho[j] : 1.f);
+            }
         }
 #pragma unroll
         for (int q = 0; q < 4; q++) st_chunk(sb + CS_A + sw128_chunk(row, 4 * half + q, 128), x + 8 * q, 1.f);

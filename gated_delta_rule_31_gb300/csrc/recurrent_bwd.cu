@@ -311,7 +311,8 @@ cudaError_t launch_seq_bwd_t(const SeqBwdArgs& a, cudaStream_t s) {
     const int threads = a.Dv / kRows * 32;
     const int nw = threads / 32;
     const size_t smem = 2 * (size_t)nw * (3 * DK + 1) * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(seq_bwd_kernel<DK, TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(seq_bwd_kernel<DK, TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     trace_begin("seq_bwd", s);
     seq_bwd_kernel<DK, TIn><<<a.B * a.Hv, threads, smem, s>>>(a);

@@ -90,18 +90,21 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
     __shared__ uint32_t tmem_sh;
     __shared__ int abort_sh;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int c = blockIdx.x, hk = blockIdx.y, b = blockIdx.z;
     const ChunkProblem& P = a.p;
     const int G = P.Hv / P.Hk;
-    const int t0 = c * kChunk;
+    const int ntiles = P.B * P.Hk * P.NC;  // (b, key head, chunk), chunk fastest
     const int lg = warp & 3, qt = warp >> 2;
     const int r = 16 * lg + (lane & 15);
     const bool act = lane < 16;
-    const bool rowvalid = act && (t0 + r < P.T);
+    int c = 0, hk = 0, b = 0, t0 = 0;  // the current tile
+    bool rowvalid = false;
     const int c32 = 32 * qt, c16 = 16 * qt;  // this thread's columns of N=128 / N=64 products
 
-    float* GF = reinterpret_cast<float*>(sm + G_GF);
-    float* ZS = reinterpret_cast<float*>(sm + G_ZS);
+    // k/q and the GF / ZS scratch swap their two 32 KB regions from tile to tile, so the next
+    // tile's k/q can land while this tile's norm backward still reads its own
+    uint32_t kq = G_KQ, gfz = G_GF;
+    float* GF = reinterpret_cast<float*>(sm + gfz);
+    float* ZS = reinterpret_cast<float*>(sm + gfz + 16384);
     float* MF = reinterpret_cast<float*>(sm + G_V);
     float* rk = reinterpret_cast<float*>(sm + G_SM);  // [64]
     float* rq = rk + 64;                                // [64]
@@ -116,6 +119,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
     float* hdh = red + 272;                             // <dH1, H0>
 
     uint32_t ld_phase = 0, mma_phase = 0, h_phase = 0;
+    bool pend_ld = false, pend_h = false;  // copies issued and not yet waited for (thread 0)
     if (tid == 0) {
         abort_sh = 0;
         mbar_init(&bar_ld, 1);
@@ -136,6 +140,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
     auto wait_ld = [&](int site) -> bool {
         bool ok = mbar_wait(&bar_ld, ld_phase, &abort_sh, a.status, site);
         ld_phase ^= 1;
+        if (ok) pend_ld = false;
         return !__syncthreads_or(!ok);
     };
     auto wait_mma = [&](int site) -> bool {
@@ -163,9 +168,10 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
 
     // Inputs of value head hv, issued in pieces as their buffers free up (thread 0 only):
     // piece 0: P, W, dO   1: Kbar   2: H0   3: T   4: v   5: dH1 (the arrival)
-    auto load_piece = [&](int hv, int piece) {
-        const size_t bh = (size_t)b * P.Hv + hv;
-        const size_t idx = bh * P.NC + c;
+    auto load_piece = [&](int bb, int cc, int hv, int piece) {
+        const size_t bh = (size_t)bb * P.Hv + hv;
+        const size_t idx = bh * P.NC + cc;
+        const int tt = cc * kChunk;
         const uint8_t* rec = a.rec + idx * REC_BYTES;
         const uint8_t* rec2 = a.rec2 + idx * REC2_BYTES;
         switch (piece) {
@@ -173,8 +179,8 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
                 mbar_add_tx(&bar_h, 8192 + 16384 + 2 * 8192);
                 bulk_load(sm + G_P, rec + REC_P, 8192, &bar_h);
                 bulk_load(sm + G_W, rec2 + REC2_W, 16384, &bar_h);
-                tma_load_4d(sm + G_DO + 0, &mdo, 0, hv, t0, b, &bar_h);
-                tma_load_4d(sm + G_DO + 8192, &mdo, 64, hv, t0, b, &bar_h);
+                tma_load_4d(sm + G_DO + 0, &mdo, 0, hv, tt, bb, &bar_h);
+                tma_load_4d(sm + G_DO + 8192, &mdo, 64, hv, tt, bb, &bar_h);
                 break;
             case 1:
                 mbar_add_tx(&bar_h, 16384);
@@ -190,25 +196,40 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
                 break;
             case 4:
                 mbar_add_tx(&bar_h, 2 * 8192);
-                tma_load_4d(sm + G_V + 0, &mv, 0, hv, t0, b, &bar_h);
-                tma_load_4d(sm + G_V + 8192, &mv, 64, hv, t0, b, &bar_h);
+                tma_load_4d(sm + G_V + 0, &mv, 0, hv, tt, bb, &bar_h);
+                tma_load_4d(sm + G_V + 8192, &mv, 64, hv, tt, bb, &bar_h);
                 break;
             default:
                 mbar_expect_tx(&bar_h, 32768);  // arrives: the head's phase completes when all landed
                 bulk_load(sm + G_DH, a.dhs + idx * STATE_IMG, 32768, &bar_h);
+                pend_h = true;
                 break;
         }
     };
 
-    // ---------------------------------------------------------------- k, q of the chunk
-    if (tid == 0) {
+    auto issue_kq = [&](int bb, int cc, int hh, uint32_t dst) {  // k, q of a tile (thread 0)
         mbar_expect_tx(&bar_ld, 4 * 8192);
-        tma_load_4d(sm + G_KQ + 0, &mk, 0, hk, t0, b, &bar_ld);
-        tma_load_4d(sm + G_KQ + 16384, &mk, 64, hk, t0, b, &bar_ld);
-        tma_load_4d(sm + G_KQ + 8192, &mq, 0, hk, t0, b, &bar_ld);
-        tma_load_4d(sm + G_KQ + 24576, &mq, 64, hk, t0, b, &bar_ld);
-        for (int piece = 0; piece < 6; piece++) load_piece(hk * G, piece);  // first value head
+        tma_load_4d(sm + dst + 0, &mk, 0, hh, cc * kChunk, bb, &bar_ld);
+        tma_load_4d(sm + dst + 16384, &mk, 64, hh, cc * kChunk, bb, &bar_ld);
+        tma_load_4d(sm + dst + 8192, &mq, 0, hh, cc * kChunk, bb, &bar_ld);
+        tma_load_4d(sm + dst + 24576, &mq, 64, hh, cc * kChunk, bb, &bar_ld);
+        pend_ld = true;
+    };
+    // ---------------------------------------------------------------- persistent loop over tiles
+    if (tid == 0 && (int)blockIdx.x < ntiles) {
+        const int t = blockIdx.x;
+        const int cc = t % P.NC, hh = (t / P.NC) % P.Hk, bb = t / (P.NC * P.Hk);
+        issue_kq(bb, cc, hh, kq);
+        for (int piece = 0; piece < 6; piece++) load_piece(bb, cc, hh * G, piece);  // first value head
     }
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    c = tile % P.NC;
+    hk = (tile / P.NC) % P.Hk;
+    b = tile / (P.NC * P.Hk);
+    t0 = c * kChunk;
+    rowvalid = act && (t0 + r < P.T);
+    const int ntile = tile + (int)gridDim.x;  // the next tile of this CTA
+    const int nc = ntile % P.NC, nhk = (ntile / P.NC) % P.Hk, nb = ntile / (P.NC * P.Hk);
     if (!wait_ld(40)) goto teardown;
     {  // norm factors: 4 threads per row, 32 elements each
         const int row = tid >> 2, pp = tid & 3;
@@ -216,7 +237,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
 #pragma unroll
         for (int q = 0; q < 4; q++) {
             float x[8];
-            ldrow8(G_KQ, row, 4 * pp + q, 128, x);
+            ldrow8(kq, row, 4 * pp + q, 128, x);
 #pragma unroll
             for (int e = 0; e < 8; e++) ss += x[e] * x[e];
         }
@@ -231,7 +252,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
     if (tid == 0) {
         tc_fence_after();
         for (int k0 = 0; k0 < kD; k0 += 16)
-            mma(TM_T1, desc_kmajor(sb + G_KQ, 128, 0, k0), desc_kmajor(sb + G_KQ, 128, 0, k0), id64x64_kk, k0 > 0);
+            mma(TM_T1, desc_kmajor(sb + kq, 128, 0, k0), desc_kmajor(sb + kq, 128, 0, k0), id64x64_kk, k0 > 0);
         mma_commit(&bar_mma);
     }
     if (!wait_mma(41)) goto teardown;
@@ -256,7 +277,14 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
         const size_t bh = (size_t)b * P.Hv + hv;
         const size_t idx = bh * P.NC + c;
         const uint8_t* rec = a.rec + idx * REC_BYTES;
-        const bool more = hv + 1 < (hk + 1) * G;  // prefetch the next value head's inputs
+        // the next value head's inputs (the next tile's first head after the last one), fetched
+        // piece by piece as their buffers free up
+        const bool last_head = hv + 1 == (hk + 1) * G;
+        const bool more = !last_head || ntile < ntiles;
+        auto prefetch = [&](int piece) {
+            if (!last_head) load_piece(b, c, hv + 1, piece);
+            else load_piece(nb, nc, nhk * G, piece);
+        };
         if (tid < 64) {
             const int t = t0 + tid;
             float gv = 0.f, bv = 0.f;
@@ -284,6 +312,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
         {
             bool okh = mbar_wait(&bar_h, h_phase, &abort_sh, a.status, 42);
             h_phase ^= 1;
+            if (okh) pend_h = false;
             if (__syncthreads_or(!okh)) goto teardown;
         }
         const float gC = gam[63];
@@ -373,7 +402,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
 #pragma unroll
                 for (int q = 0; q < 4; q++) {
                     float qq[8];
-                    ldrow8(G_KQ, 64 + r, 4 * qt + q, 128, qq);
+                    ldrow8(kq, 64 + r, 4 * qt + q, 128, qq);
 #pragma unroll
                     for (int e = 0; e < 8; e++) {
                         dot += qq[e] * x[8 * q + e];
@@ -429,8 +458,8 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
             tc_fence_after();
             for (int k0 = 0; k0 < kChunk; k0 += 16) {
                 // dQ^ += dSk K ;  dK^ += dSq^T Q
-                mma(TM_DQ, desc_kmajor(sb + G_P, 64, 0, k0), desc_mnmajor(sb + G_KQ, 128, 0, k0), id64x128_km, true);
-                mma(TM_DK, desc_mnmajor(sb + G_DO, 64, 0, k0), desc_mnmajor(sb + G_KQ, 128, 0, 64 + k0), id64x128_mm,
+                mma(TM_DQ, desc_kmajor(sb + G_P, 64, 0, k0), desc_mnmajor(sb + kq, 128, 0, k0), id64x128_km, true);
+                mma(TM_DK, desc_mnmajor(sb + G_DO, 64, 0, k0), desc_mnmajor(sb + kq, 128, 0, 64 + k0), id64x128_mm,
                     true);
             }
             for (int k0 = 0; k0 < kD; k0 += 16) {
@@ -442,7 +471,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
             mma_commit(&bar_mma);
         }
         if (!wait_mma(45)) goto teardown;
-        if (more && tid == 0) load_piece(hv + 1, 0);
+        if (more && tid == 0) prefetch(0);
         {
             const float br = __expf(gC - gam[r]);
             {  // Y: db_r = rk_r sum_d K_rd Y_rd; dK^ += b_r Y_r
@@ -454,7 +483,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
 #pragma unroll
                 for (int q = 0; q < 4; q++) {
                     float kk[8];
-                    ldrow8(G_KQ, r, 4 * qt + q, 128, kk);
+                    ldrow8(kq, r, 4 * qt + q, 128, kk);
 #pragma unroll
                     for (int e = 0; e < 8; e++) {
                         dot += kk[e] * y[8 * q + e];
@@ -482,7 +511,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
             tc_fence_after();
             for (int k0 = 0; k0 < kD; k0 += 16) {
                 mma(TM_T1, desc_kmajor(sb + G_KB, 64, 0, k0), desc_kmajor(sb + G_V, 64, 0, k0), id64x64_kk, k0 > 0);
-                mma(TM_T1 + 64, desc_kmajor(sb + G_H0, 64, 0, k0), desc_kmajor(sb + G_KQ, 128, 0, k0), id64x64_kk,
+                mma(TM_T1 + 64, desc_kmajor(sb + G_H0, 64, 0, k0), desc_kmajor(sb + kq, 128, 0, k0), id64x64_kk,
                     k0 > 0);
             }
             for (int k0 = 0; k0 < kChunk; k0 += 16)
@@ -490,7 +519,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
             mma_commit(&bar_mma);
         }
         if (!wait_mma(46)) goto teardown;
-        if (more && tid == 0) load_piece(hv + 1, 1);
+        if (more && tid == 0) prefetch(1);
         {
             {  // dT_rj = beta_j (dU V^T + Gamma_j rk_j dW K^T)_rj -> dT image (G_DH)
                 float d1[16], d2[16];
@@ -545,7 +574,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
             mma_commit(&bar_mma);
         }
         if (!wait_mma(47)) goto teardown;
-        if (more && tid == 0) load_piece(hv + 1, 2);
+        if (more && tid == 0) prefetch(2);
         {
             {  // T^T dW: dK^ += beta Gamma (T^T dW); dbeta, dgamma from k^ . (T^T dW)
                 float x[32], dk[32];
@@ -557,7 +586,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
 #pragma unroll
                 for (int q = 0; q < 4; q++) {
                     float kk[8];
-                    ldrow8(G_KQ, r, 4 * qt + q, 128, kk);
+                    ldrow8(kq, r, 4 * qt + q, 128, kk);
 #pragma unroll
                     for (int e = 0; e < 8; e++) {
                         dot += kk[e] * x[8 * q + e];
@@ -593,7 +622,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
             mma_commit(&bar_mma);
         }
         if (!wait_mma(48)) goto teardown;
-        if (more && tid == 0) load_piece(hv + 1, 3);
+        if (more && tid == 0) prefetch(3);
         {  // dA = strict_lower(-T^T Yt); terms of A_rj = beta_r rk_r rk_j E_rj G_rj
             float v[16];
             tmem_ld16(tl + TM_T1 + c16, v);
@@ -646,10 +675,10 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
         if (tid == 0) {
             tc_fence_after();
             for (int k0 = 0; k0 < kChunk; k0 += 16)
-                mma(TM_DK, desc_kmajor(sb + G_DH + 16384, 64, 0, k0), desc_mnmajor(sb + G_KQ, 128, 0, k0), id64x128_km,
+                mma(TM_DK, desc_kmajor(sb + G_DH + 16384, 64, 0, k0), desc_mnmajor(sb + kq, 128, 0, k0), id64x128_km,
                     true);
             mma_commit(&bar_mma);
-            if (more) load_piece(hv + 1, 4);  // v: its buffer held M, read before the sync above
+            if (more) prefetch(4);  // v: its buffer held M, read before the sync above
         }
         // per-head scalars: dgamma -> dg (reverse cumsum within the chunk), dbeta
         if (tid < 64) {  // two warps; row r = tid
@@ -684,7 +713,8 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
             }
         }
         if (!wait_mma(49)) goto teardown;
-        if (more && tid == 0) load_piece(hv + 1, 5);
+        if (more && tid == 0) prefetch(5);
+        if (last_head && tid == 0 && ntile < ntiles) issue_kq(nb, nc, nhk, gfz);  // GF / ZS are free now
     }
 
     // ---------------------------------------------------------------- dq, dk: norm backward
@@ -699,7 +729,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
             float dot = 0.f;
 #pragma unroll
             for (int q = 0; q < 4; q++) {
-                ldrow8(G_KQ, krow, 4 * qt + q, 128, xx + 8 * q);
+                ldrow8(kq, krow, 4 * qt + q, 128, xx + 8 * q);
 #pragma unroll
                 for (int e = 0; e < 8; e++) dot += xx[8 * q + e] * x[8 * q + e];
             }
@@ -721,16 +751,26 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
                     d4[q] = make_float4(o4[0], o4[1], o4[2], o4[3]);
                 }
             }
+            tc_fence_before();
             __syncthreads();
         }
     }
+    {  // swap the k/q and scratch regions for the next tile
+        const uint32_t t = kq;
+        kq = gfz;
+        gfz = t;
+        GF = reinterpret_cast<float*>(sm + gfz);
+        ZS = reinterpret_cast<float*>(sm + gfz + 16384);
+    }
+    }  // tiles
 
 teardown:
     tc_fence_before();
     __syncthreads();
     if (abort_sh && tid == 0) {  // let copies still in flight land before the CTA exits
         volatile int never = 0;
-        mbar_wait(&bar_ld, ld_phase, &never, nullptr, 0);
+        if (pend_ld) mbar_wait(&bar_ld, ld_phase, &never, nullptr, 0);
+        if (pend_h) mbar_wait(&bar_h, h_phase, &never, nullptr, 0);
         mbar_wait(&bar_mma, mma_phase, &never, nullptr, 0);
     }
     __syncthreads();
@@ -803,7 +843,14 @@ cudaError_t launch_chunk_bwd(const ChunkBwdArgs& a, cudaStream_t s) {
     const int smem = G_BYTES + 1024;
     if ((e = cudaFuncSetAttribute(grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
         return e;
-    dim3 grid(p.NC, p.Hk, p.B);
+    static int nsm = 0;  // one 222 KB CTA per SM: a persistent grid of one per SM
+    if (nsm == 0) {
+        int dev = 0;
+        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+        if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    }
+    const int ntiles = p.B * p.Hk * p.NC;
+    dim3 grid(ntiles < nsm ? ntiles : nsm);
     trace_begin("chunk_grad", s);
     grad_kernel<<<grid, GRAD_THREADS, smem, s>>>(mq, mk, mv, mdo64, ga);
     trace_end(s);

@@ -172,3 +172,18 @@ def test_saved_operator_handoff_empty_sequence():
     assert torch.equal(ht.cpu(), x["h0"])
     gr = gdr.bwd_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], None, d["do"], d["dht"], saved=saved)
     assert torch.equal(gr["dh0"].cpu(), x["dht"])
+
+
+@pytest.mark.parametrize("shape", [Shape(1, 200, 1, 4, 128, 128), Shape(3, 100, 2, 16, 128, 128),
+                                   Shape(1, 130, 1, 8, 128, 128)], ids=["G4", "B3-G8", "G8-ragged"])
+def test_wider_head_groups(shape):
+    """Value-head groups of 4, 8 and 16 per key head (the persistent prep and grad kernels loop
+    over a group's heads and fetch the next one while finishing the current one), an odd batch
+    count and ragged last chunks: forward and backward against the oracle."""
+    dev = cuda_device()
+    x = make_inputs(shape, dtype=torch.bfloat16, seed=shape.Hv + shape.T, grads=True, gate_scale=0.2)
+    d = to_dev(x, dev)
+    o, ht = gdr.fwd_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"])
+    ro, rht = oracle.forward(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"])
+    assert rel_err(o, ro) <= BF16_TOL and rel_err(ht, rht) <= BF16_TOL
+    check(gpu_bwd(x, dev), x)

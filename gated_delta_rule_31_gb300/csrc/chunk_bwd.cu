@@ -70,6 +70,15 @@ __device__ __forceinline__ void st_chunk8(uint32_t addr, const float* x, float s
 // fp32 [64][64] scratch element (r, j), columns XOR-swizzled by the row so that a warp
 // touching one column across rows (or one row across columns) hits distinct banks
 __device__ __forceinline__ int fsw(int r, int j) { return r * 64 + (j ^ (r & 31)); }
+// An M=64 accumulator row lives in lane l < 16 of its warp; lanes l and l + 16 split its 16
+// columns: lane l keeps columns 0-7, lane l + 16 takes 8-15 (returned in w[0..7]).
+__device__ __forceinline__ void split16(const float* v, float* w, int lane) {
+#pragma unroll
+    for (int e = 0; e < 8; e++) {
+        const float hi = __shfl_sync(0xffffffffu, v[8 + e], lane & 15);
+        w[e] = (lane >> 4) ? hi : v[e];
+    }
+}
 // 64 consecutive fp32 columns of this warp's 32 TMEM lanes
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
     tmem_ld32(taddr, v);
@@ -413,32 +422,29 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
                 if (act) dgp[qt * 64 + r] += f * rq[r] * dot;
             }
             {  // dP: Z = dP .* P, dS = scale E .* dP; dSk = dS diag(rk) (G_P), dSq = diag(rq) dS (G_DO)
-                float v[16];
+                float v[16], w[8];
                 tmem_ld16(tl + TM_T2 + c16, v);
                 tmem_wait_ld();
-                if (act) {
-                    float pr[16];
+                split16(v, w, lane);
+                const int jc = 2 * qt + (lane >> 4);  // this lane's 8-column chunk of the row
+                float pr[8];
+                ldrow8(G_P, r, jc, 64, pr);
+                float zs = 0.f;
+                float sk[8], sq[8];
 #pragma unroll
-                    for (int q = 0; q < 2; q++) ldrow8(G_P, r, 2 * qt + q, 64, pr + 8 * q);
-                    float zs = 0.f;
-                    float sk[16], sq[16];
-#pragma unroll
-                    for (int e = 0; e < 16; e++) {
-                        const int j = c16 + e;
-                        const float z = v[e] * pr[e];
-                        zs += z;
-                        ZS[fsw(r, j)] = z;
-                        const float ds = (j <= r) ? P.scale * __expf(gr - gam[j]) * v[e] : 0.f;
-                        sk[e] = ds * rk[j];
-                        sq[e] = ds * rq[r];
-                    }
-                    dgp[qt * 64 + r] += zs;
-#pragma unroll
-                    for (int q = 0; q < 2; q++) {
-                        st_chunk8(sb + G_P + sw128_chunk(r, 2 * qt + q, 64), sk + 8 * q, 1.f);
-                        st_chunk8(sb + G_DO + sw128_chunk(r, 2 * qt + q, 64), sq + 8 * q, 1.f);
-                    }
+                for (int e = 0; e < 8; e++) {
+                    const int j = 8 * jc + e;
+                    const float z = w[e] * pr[e];
+                    zs += z;
+                    ZS[fsw(r, j)] = z;
+                    const float ds = (j <= r) ? P.scale * __expf(gr - gam[j]) * w[e] : 0.f;
+                    sk[e] = ds * rk[j];
+                    sq[e] = ds * rq[r];
                 }
+                zs += __shfl_xor_sync(0xffffffffu, zs, 16);
+                if (act) dgp[qt * 64 + r] += zs;
+                st_chunk8(sb + G_P + sw128_chunk(r, jc, 64), sk, 1.f);
+                st_chunk8(sb + G_DO + sw128_chunk(r, jc, 64), sq, 1.f);
             }
             tmem_wait_st();
         }
@@ -624,18 +630,20 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
         if (!wait_mma(48)) goto teardown;
         if (more && tid == 0) prefetch(3);
         {  // dA = strict_lower(-T^T Yt); terms of A_rj = beta_r rk_r rk_j E_rj G_rj
-            float v[16];
+            float v[16], w[8];
             tmem_ld16(tl + TM_T1 + c16, v);
             tmem_wait_ld();
-            if (act) {
+            split16(v, w, lane);
+            {
+                const int jc = 2 * qt + (lane >> 4);
                 const float gr = gam[r], br = bet[r], rkr = rk[r];
                 float db = 0.f, zs = 0.f;
 #pragma unroll
-                for (int e = 0; e < 16; e++) {
-                    const int j = c16 + e;
+                for (int e = 0; e < 8; e++) {
+                    const int j = 8 * jc + e;
                     float m = 0.f, z = 0.f;
                     if (j < r) {
-                        const float dA = -v[e];
+                        const float dA = -w[e];
                         const float E = __expf(gr - gam[j]);
                         const float kk = rkr * rk[j] * GF[fsw(r, j)];
                         db += dA * E * kk;
@@ -646,8 +654,12 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
                     ZS[fsw(r, j)] = z;
                     MF[fsw(r, j)] = m;
                 }
-                dbp[qt * 64 + r] += db;
-                dgp[qt * 64 + r] += zs;
+                db += __shfl_xor_sync(0xffffffffu, db, 16);
+                zs += __shfl_xor_sync(0xffffffffu, zs, 16);
+                if (act) {
+                    dbp[qt * 64 + r] += db;
+                    dgp[qt * 64 + r] += zs;
+                }
             }
         }
         __syncthreads();
@@ -658,16 +670,15 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
             for (int i = 16 * part4; i < 16 * part4 + 16; i++) s += ZS[fsw(i, j)];
             red[16 + tid] = s;
         }
-        if (act) {  // N_rj = rk_j (M_rj + M_jr) -> image (G_DH + 16K)
-            float nrow[16];
+        {  // N_rj = rk_j (M_rj + M_jr) -> image (G_DH + 16K); 8 columns per lane
+            const int jc = 2 * qt + (lane >> 4);
+            float nrow[8];
 #pragma unroll
-            for (int e = 0; e < 16; e++) {
-                const int j = c16 + e;
+            for (int e = 0; e < 8; e++) {
+                const int j = 8 * jc + e;
                 nrow[e] = rk[j] * (MF[fsw(r, j)] + MF[fsw(j, r)]);
             }
-#pragma unroll
-            for (int q = 0; q < 2; q++)
-                st_chunk8(sb + G_DH + 16384 + sw128_chunk(r, 2 * qt + q, 64), nrow + 8 * q, 1.f);
+            st_chunk8(sb + G_DH + 16384 + sw128_chunk(r, jc, 64), nrow, 1.f);
         }
         sync_for_mma();
 

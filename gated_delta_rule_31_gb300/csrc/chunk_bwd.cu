@@ -79,6 +79,14 @@ __device__ __forceinline__ void split16(const float* v, float* w, int lane) {
         w[e] = (lane >> 4) ? hi : v[e];
     }
 }
+// The same for 32 columns: lane l keeps 0-15, lane l + 16 takes 16-31 (returned in w[0..15]).
+__device__ __forceinline__ void split32(const float* v, float* w, int lane) {
+#pragma unroll
+    for (int e = 0; e < 16; e++) {
+        const float hi = __shfl_sync(0xffffffffu, v[16 + e], lane & 15);
+        w[e] = (lane >> 4) ? hi : v[e];
+    }
+}
 // 64 consecutive fp32 columns of this warp's 32 TMEM lanes
 __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
     tmem_ld32(taddr, v);
@@ -353,12 +361,10 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
             s = warp_sum(s);
             if (lane == 0) red[warp] = s;
         }
-        uint4 utv[4];  // U~ slice qt (columns c32..) from the record, fetched while M1 runs
-        if (act) {
+        uint4 utv[2];  // this lane's half of U~ slice qt (columns c32 + 16 h ..), fetched while M1 runs
 #pragma unroll
-            for (int q = 0; q < 4; q++)
-                utv[q] = *reinterpret_cast<const uint4*>(rec + REC_U + qt * 4096 + sw64_chunk(r, q));
-        }
+        for (int q = 0; q < 2; q++)
+            utv[q] = *reinterpret_cast<const uint4*>(rec + REC_U + qt * 4096 + sw64_chunk(r, 2 * (lane >> 4) + q));
         if (!wait_mma(43)) goto teardown;
         if (tid == 0) {
             float s = 0.f;
@@ -366,25 +372,24 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
             *hdh = s;
         }
         {  // U = U~ - W H0 -> U image (G_W);  dU -> dU image (G_KB)
-            float x[32];
+            float x[32], w[16];
+            const int q0 = 4 * qt + 2 * (lane >> 4);  // this lane's two 8-column chunks
             tmem_ld32(tl + TM_T1 + c32, x);
             tmem_wait_ld();
-            if (act) {
+            split32(x, w, lane);
 #pragma unroll
-                for (int q = 0; q < 4; q++) {
-                    float ut[8];
-                    unpack8b(utv[q], ut);
+            for (int q = 0; q < 2; q++) {
+                float ut[8];
+                unpack8b(utv[q], ut);
 #pragma unroll
-                    for (int e = 0; e < 8; e++) ut[e] -= x[8 * q + e];
-                    st_chunk8(sb + G_W + sw128_chunk(r, 4 * qt + q, 64), ut, 1.f);
-                }
+                for (int e = 0; e < 8; e++) ut[e] -= w[8 * q + e];
+                st_chunk8(sb + G_W + sw128_chunk(r, q0 + q, 64), ut, 1.f);
             }
             tmem_ld32(tl + TM_T2 + c32, x);
             tmem_wait_ld();
-            if (act) {
+            split32(x, w, lane);
 #pragma unroll
-                for (int q = 0; q < 4; q++) st_chunk8(sb + G_KB + sw128_chunk(r, 4 * qt + q, 64), x + 8 * q, 1.f);
-            }
+            for (int q = 0; q < 2; q++) st_chunk8(sb + G_KB + sw128_chunk(r, q0 + q, 64), w + 8 * q, 1.f);
         }
         sync_for_mma();
 
@@ -528,43 +533,43 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
         if (more && tid == 0) prefetch(1);
         {
             {  // dT_rj = beta_j (dU V^T + Gamma_j rk_j dW K^T)_rj -> dT image (G_DH)
-                float d1[16], d2[16];
+                float d1[16], d2[16], w1[8], w2[8];
                 tmem_ld16(tl + TM_T1 + c16, d1);
                 tmem_ld16(tl + TM_T1 + 64 + c16, d2);
                 tmem_wait_ld();
-                if (act) {
+                split16(d1, w1, lane);
+                split16(d2, w2, lane);
+                const int jc = 2 * qt + (lane >> 4);
 #pragma unroll
-                    for (int e = 0; e < 16; e++) {
-                        const int j = c16 + e;
-                        d1[e] = bet[j] * (d1[e] + __expf(gam[j]) * rk[j] * d2[e]);
-                    }
-#pragma unroll
-                    for (int q = 0; q < 2; q++) st_chunk8(sb + G_DH + sw128_chunk(r, 2 * qt + q, 64), d1 + 8 * q, 1.f);
+                for (int e = 0; e < 8; e++) {
+                    const int j = 8 * jc + e;
+                    w1[e] = bet[j] * (w1[e] + __expf(gam[j]) * rk[j] * w2[e]);
                 }
+                st_chunk8(sb + G_DH + sw128_chunk(r, jc, 64), w1, 1.f);
             }
             {  // T^T dU: dv = beta T^T dU; dbeta_r += sum_v V_rv (T^T dU)_rv
-                float x[32];
+                float x[32], w[16];
                 tmem_ld32(tl + TM_T2 + c32, x);
                 tmem_wait_ld();
-                if (act) {
-                    float dot = 0.f;
+                split32(x, w, lane);
+                const int hf = lane >> 4;  // this lane's 16 columns: c32 + 16 hf ..
+                float dot = 0.f;
 #pragma unroll
-                    for (int q = 0; q < 4; q++) {
-                        float vv[8];
-                        ldrow8(G_V, r, 4 * qt + q, 64, vv);
+                for (int q = 0; q < 2; q++) {
+                    float vv[8];
+                    ldrow8(G_V, r, 4 * qt + 2 * hf + q, 64, vv);
 #pragma unroll
-                        for (int e = 0; e < 8; e++) dot += vv[e] * x[8 * q + e];
-                    }
-                    dbp[qt * 64 + r] += dot;
-                    if (rowvalid) {
-                        const float bb = bet[r];
-                        float4* dst = reinterpret_cast<float4*>(a.dv + (((size_t)b * P.T + t0 + r) * P.Hv + hv) * kD +
-                                                                c32);
+                    for (int e = 0; e < 8; e++) dot += vv[e] * w[8 * q + e];
+                }
+                dot += __shfl_xor_sync(0xffffffffu, dot, 16);
+                if (act) dbp[qt * 64 + r] += dot;
+                if (t0 + r < P.T) {
+                    const float bb = bet[r];
+                    float4* dst = reinterpret_cast<float4*>(a.dv + (((size_t)b * P.T + t0 + r) * P.Hv + hv) * kD +
+                                                            c32 + 16 * hf);
 #pragma unroll
-                        for (int q = 0; q < 8; q++)
-                            dst[q] = make_float4(bb * x[4 * q], bb * x[4 * q + 1], bb * x[4 * q + 2],
-                                                 bb * x[4 * q + 3]);
-                    }
+                    for (int q = 0; q < 4; q++)
+                        dst[q] = make_float4(bb * w[4 * q], bb * w[4 * q + 1], bb * w[4 * q + 2], bb * w[4 * q + 3]);
                 }
             }
         }

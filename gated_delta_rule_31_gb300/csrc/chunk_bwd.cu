@@ -42,7 +42,7 @@ constexpr uint32_t G_KB = 163840;   // Kbar image [64 x 128]; later dU image
 constexpr uint32_t G_GF = 180224;   // G = K K^T fp32 [64][64]                            [whole CTA]
 constexpr uint32_t G_ZS = 196608;   // fp32 [64][64] scratch (column sums)
 constexpr uint32_t G_SM = 212992;   // small arrays
-constexpr uint32_t G_SM_FLOATS = 64 * 4 + 256 * 4 + 64 + 272 + 4;  // see the carve-up in grad_kernel
+constexpr uint32_t G_SM_FLOATS = 64 * 4 + 256 * 4 + 64 + 272 + 4 + 128;  // see the carve-up in grad_kernel
 constexpr uint32_t G_BYTES = G_SM + 7168;
 static_assert(G_SM_FLOATS * 4 <= 7168, "small arrays");
 static_assert(G_BYTES + 1024 <= 232448, "grad smem");
@@ -134,6 +134,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
     float* dgc = part + 256;                            // [64] column-sum terms of dgamma
     float* red = dgc + 64;                              // [16 + 256] reductions
     float* hdh = red + 272;                             // <dH1, H0>
+    float* gst = hdh + 4;                               // [2][64] the next value head's g, beta (cp.async)
 
     uint32_t ld_phase = 0, mma_phase = 0, h_phase = 0;
     bool pend_ld = false, pend_h = false;  // copies issued and not yet waited for (thread 0)
@@ -232,7 +233,21 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
         tma_load_4d(sm + dst + 24576, &mq, 64, hh, cc * kChunk, bb, &bar_ld);
         pend_ld = true;
     };
+    auto stage_gb = [&](int bb, int cc, int hv) {  // g, beta of a head's chunk into gst (threads < 64)
+        if (tid < 64) {
+            const int t = cc * kChunk + tid;
+            const bool valid = t < P.T;
+            const size_t bt = valid ? ((size_t)bb * P.T + t) * P.Hv + hv : 0;
+            cp_async4(gst + tid, a.g + bt, valid);
+            cp_async4(gst + 64 + tid, a.beta + bt, valid);
+            cp_async_commit();
+        }
+    };
     // ---------------------------------------------------------------- persistent loop over tiles
+    if ((int)blockIdx.x < ntiles) {
+        const int t = blockIdx.x;
+        stage_gb(t / (P.NC * P.Hk), t % P.NC, ((t / P.NC) % P.Hk) * G);
+    }
     if (tid == 0 && (int)blockIdx.x < ntiles) {
         const int t = blockIdx.x;
         const int cc = t % P.NC, hh = (t / P.NC) % P.Hk, bb = t / (P.NC * P.Hk);
@@ -302,14 +317,9 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
             if (!last_head) load_piece(b, c, hv + 1, piece);
             else load_piece(nb, nc, nhk * G, piece);
         };
-        if (tid < 64) {
-            const int t = t0 + tid;
-            float gv = 0.f, bv = 0.f;
-            if (t < P.T) {
-                const size_t bt = ((size_t)b * P.T + t) * P.Hv + hv;
-                gv = a.g[bt];
-                bv = a.beta[bt];
-            }
+        if (tid < 64) {  // gates of this head, staged during the previous one (thread tid: token tid)
+            cp_async_wait_all();
+            float gv = gst[tid], bv = gst[64 + tid];
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const float y = __shfl_up_sync(0xffffffffu, gv, o);
@@ -326,6 +336,10 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
         }
         __syncthreads();
         if (tid >= 32 && tid < 64) gam[tid] += gam[31];
+        if (more) {  // the next head's gates into gst (read by the same threads above)
+            if (!last_head) stage_gb(b, c, hv + 1);
+            else stage_gb(nb, nc, nhk * G);
+        }
         {
             bool okh = mbar_wait(&bar_h, h_phase, &abort_sh, a.status, 42);
             h_phase ^= 1;
@@ -781,6 +795,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
     }  // tiles
 
 teardown:
+    cp_async_wait_all();  // staged gates still in flight
     tc_fence_before();
     __syncthreads();
     if (abort_sh && tid == 0) {  // let copies still in flight land before the CTA exits

@@ -277,29 +277,32 @@ __global__ void __launch_bounds__(256, 2)
                 const int lg = warp & 3, h = warp >> 2;
                 if (lg < 2) {  // W rows i = 32 lg + lane (first product, columns 64 h ..)
                     const int i = 32 * lg + lane;
-                    float w[64];
-                    tmem_ld32(tmem_at(tm, 32 * lg, 64 * h), w);
-                    tmem_ld32(tmem_at(tm, 32 * lg, 64 * h + 32), w + 32);
-                    tmem_wait_ld();
                     const float sbar = fb[i];
+#pragma unroll 1
+                    for (int hh2 = 0; hh2 < 2; hh2++) {  // 32 columns at a time (register budget)
+                        float w[32];
+                        tmem_ld32(tmem_at(tm, 32 * lg, 64 * h + 32 * hh2), w);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int q = 0; q < 8; q++) {
-                        const uint4 u = pack8(w + 8 * q, 1.f);
-                        const uint32_t off = sw128_chunk(i, 8 * h + q, 64);
-                        st_shared_v4(sb + PS_W + off, u.x, u.y, u.z, u.w);
-                        if (rec2) st_global16(rec2 + REC2_W + off, u);
-                        st_chunk(sb + PS_WBAR + off, w + 8 * q, sbar);
+                        for (int q = 0; q < 4; q++) {
+                            const uint4 u = pack8(w + 8 * q, 1.f);
+                            const uint32_t off = sw128_chunk(i, 8 * h + 4 * hh2 + q, 64);
+                            st_shared_v4(sb + PS_W + off, u.x, u.y, u.z, u.w);
+                            if (rec2) st_global16(rec2 + REC2_W + off, u);
+                            st_chunk(sb + PS_WBAR + off, w + 8 * q, sbar);
+                        }
                     }
                 } else {  // U~ rows i = 32 lg + lane - 64 (second product)
                     const int i = 32 * lg + lane - 64;
-                    float u[64];
-                    tmem_ld32(tmem_at(tm, 32 * lg, 128 + 64 * h), u);
-                    tmem_ld32(tmem_at(tm, 32 * lg, 128 + 64 * h + 32), u + 32);
-                    tmem_wait_ld();
+#pragma unroll 1
+                    for (int hh2 = 0; hh2 < 2; hh2++) {
+                        float u[32];
+                        tmem_ld32(tmem_at(tm, 32 * lg, 128 + 64 * h + 32 * hh2), u);
+                        tmem_wait_ld();
+                        const int col = 64 * h + 32 * hh2;  // one 32-column U~ slice
 #pragma unroll
-                    for (int q = 0; q < 8; q++) {
-                        const int col = 64 * h + 8 * q;
-                        st_global16(rec + REC_U + (col >> 5) * 4096 + sw64_chunk(i, q & 3), pack8(u + 8 * q, 1.f));
+                        for (int q = 0; q < 4; q++)
+                            st_global16(rec + REC_U + (col >> 5) * 4096 + sw64_chunk(i, q), pack8(u + 8 * q, 1.f));
                     }
                 }
                 // Kbar = diag(exp(gamma_C - gamma) rho_k) K, straight to the record
@@ -344,34 +347,44 @@ __global__ void __launch_bounds__(256, 2)
                 const int lg = warp & 3, h = warp >> 2;
                 {  // Mneg rows d = 32 lg + lane
                     const int d = 32 * lg + lane;
-                    float m[64];
-                    tmem_ld32(tmem_at(tm, 32 * lg, 64 * h), m);
-                    tmem_ld32(tmem_at(tm, 32 * lg, 64 * h + 32), m + 32);
-                    tmem_wait_ld();
+#pragma unroll 1
+                    for (int hh2 = 0; hh2 < 2; hh2++) {
+                        float m[32];
+                        tmem_ld32(tmem_at(tm, 32 * lg, 64 * h + 32 * hh2), m);
+                        tmem_wait_ld();
 #pragma unroll
-                    for (int q = 0; q < 8; q++)
-                        st_global16(rec + REC_M + sw128_chunk(d, 8 * h + q, 128), pack8(m + 8 * q, -1.f));
+                        for (int q = 0; q < 4; q++)
+                            st_global16(rec + REC_M + sw128_chunk(d, 8 * h + 4 * hh2 + q, 128), pack8(m + 8 * q, -1.f));
+                    }
                 }
                 {  // Qc = scale diag(Gamma rho_q) Q - P W, rows i = 16 lg + lane
+                    // M=64 rows live in lanes 0-15; lane l + 16 takes columns 32-63 of lane l's row
                     const int i = 16 * lg + (lane & 15);
-                    float pw[64];
-                    tmem_ld32(tmem_at(tm, 32 * lg, 128 + 64 * h), pw);
-                    tmem_ld32(tmem_at(tm, 32 * lg, 128 + 64 * h + 32), pw + 32);
-                    tmem_wait_ld();
-                    if (lane < 16) {
-                        const float f = fq[i];
-                        uint4 qv[8];
+                    const int hf = lane >> 4;
+                    float pw[32];
+                    {
+                        float lo[32];
+                        tmem_ld32(tmem_at(tm, 32 * lg, 128 + 64 * h), lo);
+                        tmem_ld32(tmem_at(tm, 32 * lg, 128 + 64 * h + 32), pw);
+                        tmem_wait_ld();
 #pragma unroll
-                        for (int q = 0; q < 8; q++)
-                            qv[q] = ld_shared_v4(sb + PS_KQ + sw128_chunk(64 + i, 8 * h + q, 128));
-#pragma unroll
-                        for (int q = 0; q < 8; q++) {
-                            float x[8];
-                            unpack8(qv[q], x);
-#pragma unroll
-                            for (int e = 0; e < 8; e++) x[e] = f * x[e] - pw[8 * q + e];
-                            st_global16(rec + REC_Q + sw128_chunk(i, 8 * h + q, 64), pack8(x, 1.f));
+                        for (int e = 0; e < 32; e++) {
+                            const float hi = __shfl_sync(0xffffffffu, pw[e], lane & 15);
+                            pw[e] = hf ? hi : lo[e];
                         }
+                    }
+                    const float f = fq[i];
+                    uint4 qv[4];
+#pragma unroll
+                    for (int q = 0; q < 4; q++)
+                        qv[q] = ld_shared_v4(sb + PS_KQ + sw128_chunk(64 + i, 8 * h + 4 * hf + q, 128));
+#pragma unroll
+                    for (int q = 0; q < 4; q++) {
+                        float x[8];
+                        unpack8(qv[q], x);
+#pragma unroll
+                        for (int e = 0; e < 8; e++) x[e] = f * x[e] - pw[8 * q + e];
+                        st_global16(rec + REC_Q + sw128_chunk(i, 8 * h + 4 * hf + q, 64), pack8(x, 1.f));
                     }
                 }
             }

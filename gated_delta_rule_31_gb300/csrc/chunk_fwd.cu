@@ -35,7 +35,8 @@ constexpr uint32_t PS_T = 66560;     // T fp32 [64][LDA]; then W image [64 x 128
 constexpr uint32_t PS_P = 83968;     // P image [64 x 64]
 constexpr uint32_t PS_SCR = 92160;   // solve scratch: Y_IK blocks [6][16][LDY] fp32
 constexpr uint32_t PS_SMALL = PS_SCR + SOLVE_SCRATCH_BYTES;  // per-token factors (8 x 64 fp32)
-constexpr uint32_t PS_BYTES = PS_SMALL + 2048;
+constexpr uint32_t PS_GST = PS_SMALL + 2048;  // next value head's gates g, beta (2 x 64 fp32), cp.async
+constexpr uint32_t PS_BYTES = PS_GST + 512;
 constexpr uint32_t PS_TT = PS_A, PS_WBAR = PS_A, PS_W = PS_T;
 static_assert(PS_A % 1024 == 0 && PS_T % 1024 == 0 && PS_P % 1024 == 0, "align");
 static_assert(PS_A + 64 * LDA * 4 <= PS_T && PS_T + 64 * LDA * 4 <= PS_P, "fp32 tiles");
@@ -60,6 +61,7 @@ __global__ void __launch_bounds__(256, 2)
     float* fw = rho + 128;   // beta Gamma rho_k     (columns of Tw)
     float* fb = fw + 64;     // exp(gamma_C - gamma) rho_k   (rows of Kbar, Wbar)
     float* fq = fb + 64;     // scale Gamma rho_q     (rows of Qc)
+    float* gst = reinterpret_cast<float*>(sm + PS_GST);
     float* Am = reinterpret_cast<float*>(sm + PS_A);
     float* Tm = reinterpret_cast<float*>(sm + PS_T);
     float* Xs = reinterpret_cast<float*>(sm + PS_SCR);
@@ -83,7 +85,19 @@ __global__ void __launch_bounds__(256, 2)
         tma_load_4d(sm + PS_V + 8192, &mv, 64, hk * G + hh, c * kChunk, b, &bar_v);
         v_pend = true;
     };
+    // threads 0-63 stage token tid's g and beta of (group g, value head hh); each thread later
+    // reads only the slots it staged itself. Tokens past T are zero-filled (g = 0, beta = 0).
+    auto stage_gb = [&](int g, int hh) {
+        const int c = g % P.NC, hk = (g / P.NC) % P.Hk, b = g / (P.NC * P.Hk);
+        const int t = c * kChunk + tid;
+        const bool in = t < P.T;
+        const size_t bt = in ? ((size_t)b * P.T + t) * P.Hv + hk * G + hh : 0;
+        cp_async4(gst + tid, a.g + bt, in);
+        cp_async4(gst + 64 + tid, a.beta + bt, in);
+        cp_async_commit();
+    };
 
+    if (tid < 64 && (int)blockIdx.x < ngroups) stage_gb(blockIdx.x, 0);
     if (tid == 0) {
         abort_sh = 0;
         mbar_init(&bar_kq, 1);
@@ -106,7 +120,6 @@ __global__ void __launch_bounds__(256, 2)
 
     for (int grp = blockIdx.x; grp < ngroups; grp += gridDim.x) {
         const int c = grp % P.NC, hk = (grp / P.NC) % P.Hk, b = grp / (P.NC * P.Hk);
-        const int t0 = c * kChunk;
         const int next = grp + (int)gridDim.x;
         ok = mbar_wait(&bar_kq, kq_ph, &abort_sh, a.status, 10);
         kq_ph ^= 1;
@@ -130,13 +143,9 @@ __global__ void __launch_bounds__(256, 2)
             }
             // gates of the chunk; tokens past T act as g = 0, beta = 0 (state passes unchanged)
             if (tid < 64) {
-                const int t = t0 + tid;
-                float gv = 0.f, bv = 0.f;
-                if (t < P.T) {
-                    const size_t bt = ((size_t)b * P.T + t) * P.Hv + hv;
-                    gv = a.g[bt];
-                    bv = a.beta[bt];
-                }
+                cp_async_wait_all();
+                float gv = gst[tid];
+                const float bv = gst[64 + tid];
 #pragma unroll
                 for (int o = 1; o < 32; o <<= 1) {
                     const float y = __shfl_up_sync(0xffffffffu, gv, o);
@@ -272,6 +281,10 @@ __global__ void __launch_bounds__(256, 2)
                 if (hh + 1 < G) issue_v(grp, hh + 1);
                 else if (next < ngroups) issue_v(next, 0);
             }
+            if (tid < 64) {  // and its gates
+                if (hh + 1 < G) stage_gb(grp, hh + 1);
+                else if (next < ngroups) stage_gb(next, 0);
+            }
             tc_fence_after();
             {
                 const int lg = warp & 3, h = warp >> 2;
@@ -396,6 +409,7 @@ __global__ void __launch_bounds__(256, 2)
         if (tid == 0 && next < ngroups) issue_kq(next);  // k, q are no longer read
     }  // groups
 teardown:
+    cp_async_wait_all();
     tc_fence_before();
     __syncthreads();
     if (abort_sh && tid == 0) {  // let copies still in flight land before the CTA exits

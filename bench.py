@@ -521,14 +521,17 @@ def main():
             wsc = torch.empty(nwc, dtype=torch.uint8, device=dev)
             ins = [P(dc[n]) for n in ("q", "k", "v", "g", "beta", "h0")] + [P(oc), P(hc)]
             calls = {"chunked": lambda: raise_on(L.gdr_fwd_chunked(ctypes.byref(pc), *ins, P(wsc), nwc, sp))}
+            # the chunked VJP (recomputing the chunk operators and states) of <do, o>
+            dco = torch.randn(dc["v"].shape, device=dev).to(torch.bfloat16)
+            gout = [torch.empty(dc[n].shape, **f32) for n in ("q", "k", "v", "g", "beta", "h0")]
+            bins = [P(dc[n]) for n in ("q", "k", "v", "g", "beta", "h0")] + [P(dco), None] + [P(t) for t in gout]
+            nbc = gdr.bwd_workspace_bytes(pc)
+            wbc = torch.empty(nbc, dtype=torch.uint8, device=dev)
+            calls["bwd_chunked"] = lambda: raise_on(L.gdr_bwd_chunked(ctypes.byref(pc), *bins, P(wbc), nbc, sp))
             if gate == "channel":
                 calls["sequential"] = lambda: raise_on(L.gdr_fwd_sequential(ctypes.byref(pc), *ins, sp))
-                # its backward (the sequential VJP: the chunked VJP covers the scalar gate)
-                dco = torch.randn(dc["v"].shape, device=dev).to(torch.bfloat16)
-                gout = [torch.empty(dc[n].shape, **f32) for n in ("q", "k", "v", "g", "beta", "h0")]
                 nbw = int(L.gdr_bwd_sequential_workspace(ctypes.byref(pc)))
                 wbw = torch.empty(nbw, dtype=torch.uint8, device=dev)
-                bins = [P(dc[n]) for n in ("q", "k", "v", "g", "beta", "h0")] + [P(dco), None] + [P(t) for t in gout]
                 calls["bwd_sequential"] = lambda: raise_on(L.gdr_bwd_sequential(ctypes.byref(pc), *bins, P(wbw), nbw, sp))
             for name, fn in calls.items():
                 for _ in range(3):
@@ -546,7 +549,11 @@ def main():
                     calls["chunked"]()
                     torch.cuda.synchronize(dev)
                 res["channel_kernels_us"] = {n: round(1e3 * t, 1) for n, t in trc.records}
-            del dc, oc, hc, wsc
+                with gdr.trace() as trc:
+                    calls["bwd_chunked"]()
+                    torch.cuda.synchronize(dev)
+                res["channel_bwd_kernels_us"] = {n: round(1e3 * t, 1) for n, t in trc.records}
+            del dc, oc, hc, wsc, wbc
         toks = PREFILL.B * PREFILL.T
         chan = {"config": "B=1, T=4096, Hk=16, Hv=32, Dk=Dv=128, bf16, h0 ~ N(0,0.02), L2 flushed, median of 5",
                 "tokens_per_s_channel_chunked": toks / (res["channel_chunked_us"] * 1e-6), **res}

@@ -33,14 +33,21 @@ constexpr uint32_t REC_P = 65536;        // P     [64 tok x 64 tok]   8 KB
 constexpr uint32_t REC_U = 73728;        // U~    4 x [64 tok x 32] SW64 slices, 4 KB each
 constexpr uint32_t REC_BYTES = 90112;
 constexpr uint32_t STATE_IMG = 32768;    // one bf16 [128 d x 128 v] SW128 state image
-// Extra per-chunk record kept for the backward: T = (I + A)^-1 [64 x 64] and W [64 x 128].
+// Extra per-chunk record kept for the backward: T = (I + A)^-1 [64 x 64] and W [64 x 128];
+// with a per-channel gate also K^ .* Gamma [64 x 128] (the operand of dT's second term).
 constexpr uint32_t REC2_T = 0, REC2_W = 8192, REC2_BYTES = 24576;
+constexpr uint32_t REC2_KG = 24576, REC2_BYTES_CH = 40960;
+// Per-channel backward: the tensor-core pass exports, per (b, hv, chunk), fp32 [64][128]
+// X = dO H0^T, Y = U dH1^T, Z = T^T dW; fp32 [64][64] dPs = scale tril(dO U^T) and
+// dA = -strict_lower(T^T dT T^T); per state row d <dH1, H0>_d; per token V . (T^T dU).
+constexpr uint32_t CHX_X = 0, CHX_Y = 32768, CHX_Z = 65536, CHX_DP = 98304, CHX_DA = 114688;
+constexpr uint32_t CHX_HDH = 131072, CHX_DB = 131584, CHX_BYTES = 131840;
 
 struct ChunkProblem {
     int B, T, Hk, Hv, NC;
     float scale;
     int use_norm;
-    int channel;  // per-channel gate g [B,T,Hv,Dk] (forward only); else one gate per head
+    int channel;  // per-channel gate g [B,T,Hv,Dk]; else one gate per head
 };
 
 struct WsLayout {
@@ -49,6 +56,8 @@ struct WsLayout {
     size_t rec2;     // bwd: T and W per chunk [B*Hv][NC]
     size_t hs;       // bwd: chunk-start states [B*Hv][NC] images
     size_t dhs;      // bwd: chunk-end state gradients [B*Hv][NC] images
+    size_t chx;      // bwd, per-channel gate: tensor-core exports [B*Hv][NC]
+    size_t dqh, dkh; // bwd, per-channel gate: dq^, dk^ per value head, fp32 [B][T][Hv][Dk]
     size_t total;
     int ncpad;
 };
@@ -64,14 +73,22 @@ inline WsLayout ws_layout(const ChunkProblem& p, bool bwd, bool bwd_states = fal
     const size_t ngam = p.channel ? (size_t)p.NC * kD : (size_t)w.ncpad;
     w.rec = round_up(w.gam + nh * ngam * sizeof(float), 1024);
     size_t end = w.rec + nh * p.NC * (size_t)REC_BYTES;
-    w.rec2 = w.hs = w.dhs = 0;
+    w.rec2 = w.hs = w.dhs = w.chx = w.dqh = w.dkh = 0;
     if (bwd) {
         w.rec2 = end;
-        end = w.rec2 + nh * p.NC * (size_t)REC2_BYTES;
+        end = w.rec2 + nh * p.NC * (size_t)(p.channel ? REC2_BYTES_CH : REC2_BYTES);
         w.hs = end;
         if (!bwd_states) end += nh * p.NC * (size_t)STATE_IMG;
         w.dhs = end;
         end = w.dhs + nh * p.NC * (size_t)STATE_IMG;
+        if (p.channel) {
+            w.chx = end;
+            end = w.chx + nh * p.NC * (size_t)CHX_BYTES;
+            const size_t plane = round_up((size_t)p.B * p.T * p.Hv * kD * sizeof(float), 1024);
+            w.dqh = end;
+            w.dkh = end + plane;
+            end += 2 * plane;
+        }
     }
     w.total = end;
     return w;
@@ -147,6 +164,19 @@ cudaError_t launch_prep(const PrepArgs& a, const CUtensorMap& mq, const CUtensor
 // Per-channel gate (chunk_fwd_ch.cu): same record, Gamma_C as [B*Hv][NC][Dk].
 cudaError_t launch_prep_ch(const PrepArgs& a, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                            cudaStream_t s);
+// Per-channel gate backward after the scans (chunk_bwd_ch.cu): the tensor-core pass, the
+// CUDA-core pass and the value-head sum with the norm backward.
+struct GradChArgs {
+    ChunkProblem p;
+    const void *q, *k;
+    const float *g, *beta;
+    const uint8_t *rec, *rec2, *hs, *dhs;
+    uint8_t* chx;
+    float *dqh, *dkh;
+    float *dq, *dk, *dv, *dg, *dbeta;
+    int* status;
+};
+cudaError_t launch_grad_ch(const GradChArgs& a, const CUtensorMap& mv, const CUtensorMap& mdo, cudaStream_t s);
 
 enum ScanMode : int { SCAN_FWD_OUT = 0, SCAN_FWD_STATES = 1, SCAN_BWD = 2 };
 struct ScanArgs {

@@ -837,7 +837,8 @@ cudaError_t launch_chunk_bwd(const ChunkBwdArgs& a, cudaStream_t s) {
         pa.rec = ws + w.rec;
         pa.rec2 = ws + w.rec2;
         pa.ncpad = w.ncpad;
-        if ((e = launch_prep(pa, mq, mk, mv, s)) != cudaSuccess) return e;
+        if ((e = p.channel ? launch_prep_ch(pa, mq, mk, mv, s) : launch_prep(pa, mq, mk, mv, s)) != cudaSuccess)
+            return e;
     }
     uint8_t* dhs = keep ? ws + kSavedBwdDhs : ws + w.dhs;
     ScanArgs sa;
@@ -856,6 +857,28 @@ cudaError_t launch_chunk_bwd(const ChunkBwdArgs& a, cudaStream_t s) {
     sa.hfinal = a.dh0;
     sa.states = dhs;
     if ((e = launch_scan(sa, SCAN_BWD, &mdo32, s)) != cudaSuccess) return e;
+    if (p.channel) {
+        GradChArgs ca;
+        ca.p = p;
+        ca.q = a.q;
+        ca.k = a.k;
+        ca.g = a.g;
+        ca.beta = a.beta;
+        ca.rec = pa.rec;
+        ca.rec2 = pa.rec2;
+        ca.hs = hs;
+        ca.dhs = dhs;
+        ca.chx = ws + w.chx;
+        ca.dqh = reinterpret_cast<float*>(ws + w.dqh);
+        ca.dkh = reinterpret_cast<float*>(ws + w.dkh);
+        ca.dq = a.dq;
+        ca.dk = a.dk;
+        ca.dv = a.dv;
+        ca.dg = a.dg;
+        ca.dbeta = a.dbeta;
+        ca.status = status;
+        return launch_grad_ch(ca, mv, mdo64, s);
+    }
     GradArgs ga;
     ga.p = p;
     ga.g = a.g;

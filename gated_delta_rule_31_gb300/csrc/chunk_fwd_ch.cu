@@ -59,6 +59,7 @@ __global__ void __launch_bounds__(256, 1)
     const int t0 = c * kChunk;
     const size_t bh = (size_t)b * P.Hv + hv;
     uint8_t* rec = a.rec + (bh * P.NC + c) * REC_BYTES;
+    uint8_t* rec2 = a.rec2 ? a.rec2 + (bh * P.NC + c) * REC2_BYTES_CH : nullptr;  // backward: T, W, K^ .* Gamma
     float* al = reinterpret_cast<float*>(sm + CS_AL);
     float* gp = reinterpret_cast<float*>(sm + CS_GP);
     float* Am = reinterpret_cast<float*>(sm + CS_A);
@@ -214,7 +215,7 @@ __global__ void __launch_bounds__(256, 1)
         const int i = row & 63;
         const bool isw = row < 64;
         const float* trow = Tm + i * LDA + 32 * half;
-        float x[32];
+        float t[32], x[32];
 #pragma unroll
         for (int q = 0; q < 8; q++) {
             const float4 f = *reinterpret_cast<const float4*>(trow + 4 * q);
@@ -222,12 +223,16 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
             for (int e = 0; e < 4; e++) {
                 const int j = 32 * half + 4 * q + e;
-                const float t = (j >> 4) <= (i >> 4) ? tv[e] : 0.f;
-                x[4 * q + e] = t * bet[j] * (isw ? rho[j] : 1.f);
+                t[4 * q + e] = (j >> 4) <= (i >> 4) ? tv[e] : 0.f;
+                x[4 * q + e] = t[4 * q + e] * bet[j] * (isw ? rho[j] : 1.f);
             }
         }
 #pragma unroll
-        for (int q = 0; q < 4; q++) st_chunk(sb + CS_A + sw128_chunk(row, 4 * half + q, 128), x + 8 * q, 1.f);
+        for (int q = 0; q < 4; q++) {
+            st_chunk(sb + CS_A + sw128_chunk(row, 4 * half + q, 128), x + 8 * q, 1.f);
+            if (isw && rec2)  // T itself for the backward
+                st_global16(rec2 + REC2_T + sw128_chunk(i, 4 * half + q, 64), pack8(t + 8 * q, 1.f));
+        }
     }
     {  // K .* Gamma and Kbar = diag(rho_k) K .* prod_{t>r} a_t, row r = tid >> 2, 32 channels each
         const int r = tid >> 2, q4 = tid & 3;
@@ -249,6 +254,7 @@ __global__ void __launch_bounds__(256, 1)
             }
             const uint32_t off = sw128_chunk(r, j, 64);
             st_chunk(sb + CS_KG + off, yg, 1.f);
+            if (rec2) st_global16(rec2 + REC2_KG + off, pack8(yg, rk));  // K^ .* Gamma
             const uint4 ub = pack8(yb, 1.f);
             st_shared_v4(sb + CS_KB + off, ub.x, ub.y, ub.z, ub.w);
             st_global16(rec + REC_K + off, ub);
@@ -281,7 +287,10 @@ __global__ void __launch_bounds__(256, 1)
             tmem_ld32(tmem_at(tm, 32 * lg, 64 * h + 32), w + 32);
             tmem_wait_ld();
 #pragma unroll
-            for (int q = 0; q < 8; q++) st_chunk(sb + CS_T + sw128_chunk(i, 8 * h + q, 64), w + 8 * q, 1.f);
+            for (int q = 0; q < 8; q++) {
+                st_chunk(sb + CS_T + sw128_chunk(i, 8 * h + q, 64), w + 8 * q, 1.f);
+                if (rec2) st_global16(rec2 + REC2_W + sw128_chunk(i, 8 * h + q, 64), pack8(w + 8 * q, 1.f));
+            }
         } else {  // U~ rows i = 32 lg + lane - 64 -> record slices
             const int i = 32 * lg + lane - 64;
             float u[64];

@@ -30,6 +30,9 @@ struct SeqBwdArgs {
 };
 size_t seq_bwd_workspace(int B, int T, int Hv, int Dk, int Dv);
 cudaError_t launch_seq_bwd(SeqBwdArgs a, void* ws, cudaStream_t s);
+// dq, dk from per-value-head dq^, dk^ (fp32 [B][T][Hv][Dk] in dqh / dkh): the sum over the
+// value heads of each key head, then the L2-norm backward (bf16 q, k; Dk = 128; dg untouched).
+cudaError_t launch_qk_norm_backward(const SeqBwdArgs& a, cudaStream_t s);
 
 // Launch tracing (api.cu): no-ops unless gdr_trace_enable(1) was called.
 void trace_begin(const char* name, cudaStream_t s);

@@ -335,6 +335,14 @@ cudaError_t launch_seq_bwd_d(const SeqBwdArgs& a, cudaStream_t s) {
 
 }  // namespace
 
+cudaError_t launch_qk_norm_backward(const SeqBwdArgs& a, cudaStream_t s) {
+    if (a.Dk != 128 || !a.bf16 || !a.channel) return cudaErrorInvalidValue;
+    trace_begin("qk_norm_backward", s);
+    seq_bwd_finish_kernel<128, __nv_bfloat16><<<a.B * a.T * a.Hk, 128, 0, s>>>(a);
+    trace_end(s);
+    return cudaGetLastError();
+}
+
 size_t seq_bwd_workspace(int B, int T, int Hv, int Dk, int Dv) {
     const size_t nh = (size_t)B * Hv, plane = (size_t)Dv * Dk * sizeof(float);
     const size_t nseg = (T + kSeg - 1) / kSeg;

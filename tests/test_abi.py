@@ -89,14 +89,20 @@ def test_chunked_support_matrix_and_workspace(L):
         assert L.gdr_fwd_chunked_workspace(ctypes.byref(p)) == 0
         assert L.gdr_fwd_chunked(ctypes.byref(p), *[FAKE] * 8, FAKE, 1 << 30, None) == UNSUPPORTED
         assert L.gdr_bwd_chunked(ctypes.byref(p), *[FAKE] * 14, FAKE, 1 << 30, None) == UNSUPPORTED
-    # per-channel gate: chunked forward only (Gamma_C kept per key channel: a larger workspace)
-    pc = prob(gate=1)
-    assert L.gdr_fwd_chunked_workspace(ctypes.byref(pc)) > L.gdr_fwd_chunked_workspace(ctypes.byref(prob()))
-    assert L.gdr_bwd_chunked_workspace(ctypes.byref(pc)) == 0
-    assert L.gdr_bwd_chunked(ctypes.byref(pc), *[FAKE] * 14, FAKE, 1 << 30, None) == UNSUPPORTED
-    assert L.gdr_chunk_states_bytes(ctypes.byref(pc)) == 0 and L.gdr_chunk_saved_bytes(ctypes.byref(pc)) == 0
-    assert L.gdr_fwd_chunked_states(ctypes.byref(pc), *[FAKE] * 8, FAKE, 1 << 30, FAKE, 1 << 30, None) == UNSUPPORTED
+    # per-channel gate: chunked forward, state handoff and VJP (Gamma_C per key channel, 16 KB more
+    # of T/W/K.*Gamma per chunk and the backward's per-channel exports: larger workspaces); the
+    # operator handoff stays scalar-only
+    pc, ps = prob(gate=1), prob()
+    assert L.gdr_fwd_chunked_workspace(ctypes.byref(pc)) > L.gdr_fwd_chunked_workspace(ctypes.byref(ps))
+    assert L.gdr_bwd_chunked_workspace(ctypes.byref(pc)) > L.gdr_bwd_chunked_workspace(ctypes.byref(ps))
+    assert L.gdr_bwd_chunked_states_workspace(ctypes.byref(pc)) > L.gdr_bwd_chunked_states_workspace(ctypes.byref(ps))
+    assert L.gdr_chunk_states_bytes(ctypes.byref(pc)) == L.gdr_chunk_states_bytes(ctypes.byref(ps)) > 0
+    assert L.gdr_chunk_saved_bytes(ctypes.byref(pc)) == 0
     assert L.gdr_fwd_chunked_saved(ctypes.byref(pc), *[FAKE] * 8, FAKE, 1 << 30, FAKE, 1 << 30, None) == UNSUPPORTED
+    args = [FAKE] * 5 + [FAKE, 1 << 30] + [FAKE] * 8
+    assert L.gdr_bwd_chunked_saved(ctypes.byref(pc), *args, FAKE, 1 << 30, None) == UNSUPPORTED
+    nb = L.gdr_bwd_chunked_workspace(ctypes.byref(pc))
+    assert L.gdr_bwd_chunked(ctypes.byref(pc), *[FAKE] * 14, FAKE, nb - 1, None) == WORKSPACE
     p = prob()
     need = L.gdr_fwd_chunked_workspace(ctypes.byref(p))
     need_b = L.gdr_bwd_chunked_workspace(ctypes.byref(p))

@@ -91,11 +91,3 @@ def test_equal_channels_match_the_scalar_gate():
     o3, h3 = gdr.fwd_chunked(d["q"], d["k"], d["v"], gch, d["beta"], d["h0"])
     assert rel_err(o2, o1) <= BF16_TOL and rel_err(h2, h1) <= BF16_TOL
     assert torch.equal(o2, o3) and torch.equal(h2, h3)
-
-
-def test_channel_gate_backward_is_unsupported():
-    dev = cuda_device()
-    x = make_inputs(Shape(1, 64, 1, 2, 128, 128), dtype=torch.bfloat16, seed=1, gate="channel", grads=True)
-    d = to_dev(x, dev)
-    with pytest.raises(gdr.GdrError):
-        gdr.bwd_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], d["do"], d["dht"])

@@ -394,30 +394,58 @@ __global__ void __launch_bounds__(CH_THREADS, 1) grad_ch_simt_kernel(GradChArgs 
     const __nv_bfloat16* kg = static_cast<const __nv_bfloat16*>(a.k);
     const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(a.q);
 
-    // raw k, q (zero past T), g (0 past T: a = 1, beta = 0), dPs and dA
-    for (int i = tid; i < kChunk * kD; i += CH_THREADS) {
-        const int rr = i >> 7, dd = i & 127, t = t0 + rr;
-        float kv = 0.f, qv = 0.f, gv = 0.f;
-        if (t < P.T) {
-            const size_t xi = (((size_t)b * P.T + t) * P.Hk + hk) * kD + dd;
-            kv = __bfloat162float(kg[xi]);
-            qv = __bfloat162float(qg[xi]);
-            gv = a.g[(((size_t)b * P.T + t) * P.Hv + hv) * kD + dd];
+    // raw k, q (zero past T), g (0 past T: a = 1, beta = 0), dPs and dA: every global load of
+    // the thread is issued before the first shared-memory store
+    {
+        uint4 kr[2], qr[2];
+        float4 gr[4], dp[2], da[2];
+#pragma unroll
+        for (int n = 0; n < 2; n++) {
+            const int u = tid + CH_THREADS * n, rr = u >> 4, t = t0 + rr;
+            const size_t xi = (((size_t)b * P.T + t) * P.Hk + hk) * kD + 8 * (u & 15);
+            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+            kr[n] = t < P.T ? *reinterpret_cast<const uint4*>(kg + xi) : z;
+            qr[n] = t < P.T ? *reinterpret_cast<const uint4*>(qg + xi) : z;
+            dp[n] = reinterpret_cast<const float4*>(chx + CHX_DP / 4)[u];
+            da[n] = reinterpret_cast<const float4*>(chx + CHX_DA / 4)[u];
         }
-        KH[i] = kv;
-        QH[i] = qv;
-        GM[i] = gv;
-        AL[i] = __expf(gv);
+#pragma unroll
+        for (int n = 0; n < 4; n++) {
+            const int u = tid + CH_THREADS * n, rr = u >> 5, t = t0 + rr;
+            gr[n] = t < P.T ? *reinterpret_cast<const float4*>(a.g + (((size_t)b * P.T + t) * P.Hv + hv) * kD +
+                                                                4 * (u & 31))
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        const float bv = (tid < 64 && t0 + tid < P.T) ? a.beta[((size_t)b * P.T + t0 + tid) * P.Hv + hv] : 0.f;
+#pragma unroll
+        for (int n = 0; n < 2; n++) {
+            const int u = tid + CH_THREADS * n;
+            float x[8];
+            unpack8c(kr[n], x);
+#pragma unroll
+            for (int e = 0; e < 8; e++) KH[8 * u + e] = x[e];
+            unpack8c(qr[n], x);
+#pragma unroll
+            for (int e = 0; e < 8; e++) QH[8 * u + e] = x[e];
+            const int rr = u >> 4, j0 = 4 * (u & 15);
+            reinterpret_cast<float4*>(DPR)[u] = dp[n];
+            reinterpret_cast<float4*>(DAR)[u] = da[n];
+            const float pv[4] = {dp[n].x, dp[n].y, dp[n].z, dp[n].w}, av[4] = {da[n].x, da[n].y, da[n].z, da[n].w};
+#pragma unroll
+            for (int e = 0; e < 4; e++) {
+                DPT[(j0 + e) * LDT + rr] = pv[e];
+                DAT[(j0 + e) * LDT + rr] = av[e];
+            }
+        }
+#pragma unroll
+        for (int n = 0; n < 4; n++) {
+            const int u = tid + CH_THREADS * n;
+            reinterpret_cast<float4*>(GM)[u] = gr[n];
+            reinterpret_cast<float4*>(AL)[u] =
+                make_float4(__expf(gr[n].x), __expf(gr[n].y), __expf(gr[n].z), __expf(gr[n].w));
+        }
+        if (tid < 64) bet[tid] = bv;
     }
-    for (int i = tid; i < kChunk * kChunk; i += CH_THREADS) {
-        const int rr = i >> 6, j = i & 63;
-        const float dp = chx[CHX_DP / 4 + i], da = chx[CHX_DA / 4 + i];
-        DPR[i] = dp;
-        DAR[i] = da;
-        DPT[j * LDT + rr] = dp;
-        DAT[j * LDT + rr] = da;
-    }
-    if (tid < 64) bet[tid] = (t0 + tid < P.T) ? a.beta[((size_t)b * P.T + t0 + tid) * P.Hv + hv] : 0.f;
     __syncthreads();
     {  // L2 norm factors: warp w takes rows 4w .. 4w + 3 of k and of q
 #pragma unroll
@@ -462,6 +490,13 @@ __global__ void __launch_bounds__(CH_THREADS, 1) grad_ch_simt_kernel(GradChArgs 
 #pragma unroll
     for (int h = 0; h < 2; h++) {
         const int ra = r0 + 8 * h;
+        float xs[8], ys[8], zs[8];  // fetched now, used after the contraction
+#pragma unroll
+        for (int e = 0; e < 8; e++) {
+            xs[e] = chx[CHX_X / 4 + (ra + e) * kD + d];
+            ys[e] = chx[CHX_Y / 4 + (ra + e) * kD + d];
+            zs[e] = chx[CHX_Z / 4 + (ra + e) * kD + d];
+        }
         float E[8], X1[8], Y1[8];
 #pragma unroll
         for (int e = 0; e < 8; e++) {
@@ -469,7 +504,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1) grad_ch_simt_kernel(GradChArgs 
             X1[e] = 0.f;
             Y1[e] = 0.f;
         }
-        for (int j = ra + 7; j >= 0; j--) {
+        auto row_step = [&](int j, bool diag) {
             const float kj = KH[j * kD + d];
             const float an = j + 1 < kChunk ? AL[(j + 1) * kD + d] : 1.f;
             const float4 p0 = *reinterpret_cast<const float4*>(DPT + j * LDT + ra);
@@ -480,19 +515,21 @@ __global__ void __launch_bounds__(CH_THREADS, 1) grad_ch_simt_kernel(GradChArgs 
             const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
             for (int e = 0; e < 8; e++) {
-                E[e] = (j < ra + e) ? E[e] * an : 1.f;
+                if (diag) E[e] = (j < ra + e) ? E[e] * an : 1.f;
+                else E[e] *= an;
                 const float w = kj * E[e];
                 X1[e] += pv[e] * w;
                 Y1[e] += av[e] * w;
             }
-        }
+        };
+        for (int j = ra + 7; j >= ra; j--) row_step(j, true);  // the diagonal block
+        for (int j = ra - 1; j >= 0; j--) row_step(j, false);  // every row of the half is past j
 #pragma unroll
         for (int e = 0; e < 8; e++) {
             const int i = 8 * h + e, rr = ra + e;
             const float gm = GM[rr * kD + d];
             const float Gm = __expf(gm), bb = __expf(gC - gm);
-            const float x = chx[CHX_X / 4 + rr * kD + d], y = chx[CHX_Y / 4 + rr * kD + d],
-                        z = chx[CHX_Z / 4 + rr * kD + d];
+            const float x = xs[e], y = ys[e], z = zs[e];
             const float kh = KH[rr * kD + d], qh = QH[rr * kD + d], br = bet[rr];
             const float dqv = P.scale * Gm * x + X1[e];
             dk[i] = bb * y + br * Gm * z + br * Y1[e];
@@ -513,7 +550,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1) grad_ch_simt_kernel(GradChArgs 
             E[e] = 1.f;
             X2[e] = 0.f;
         }
-        for (int i = ja; i < kChunk; i++) {
+        auto col_step = [&](int i, bool diag) {
             const float ai = AL[i * kD + d], qi = QH[i * kD + d], kbi = bet[i] * KH[i * kD + d];
             const float4 p0 = *reinterpret_cast<const float4*>(DPR + i * kChunk + ja);
             const float4 p1 = *reinterpret_cast<const float4*>(DPR + i * kChunk + ja + 4);
@@ -523,10 +560,13 @@ __global__ void __launch_bounds__(CH_THREADS, 1) grad_ch_simt_kernel(GradChArgs 
             const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
             for (int e = 0; e < 8; e++) {
-                E[e] = (i > ja + e) ? E[e] * ai : 1.f;
+                if (diag) E[e] = (i > ja + e) ? E[e] * ai : 1.f;
+                else E[e] *= ai;
                 X2[e] += (pv[e] * qi + av[e] * kbi) * E[e];
             }
-        }
+        };
+        for (int i = ja; i < ja + 8; i++) col_step(i, true);  // the diagonal block
+        for (int i = ja + 8; i < kChunk; i++) col_step(i, false);
 #pragma unroll
         for (int e = 0; e < 8; e++) {
             const int i = 8 * h + e, jj = ja + e;

@@ -504,26 +504,49 @@ __global__ void __launch_bounds__(CH_THREADS, 1) grad_ch_simt_kernel(GradChArgs 
             X1[e] = 0.f;
             Y1[e] = 0.f;
         }
-        auto row_step = [&](int j, bool diag) {
+        // the diagonal block (j = ra+7 .. ra) with per-row running products E_rj
+        for (int j = ra + 7; j >= ra; j--) {
             const float kj = KH[j * kD + d];
             const float an = j + 1 < kChunk ? AL[(j + 1) * kD + d] : 1.f;
-            const float4 p0 = *reinterpret_cast<const float4*>(DPT + j * LDT + ra);
-            const float4 p1 = *reinterpret_cast<const float4*>(DPT + j * LDT + ra + 4);
-            const float4 a0 = *reinterpret_cast<const float4*>(DAT + j * LDT + ra);
-            const float4 a1 = *reinterpret_cast<const float4*>(DAT + j * LDT + ra + 4);
-            const float pv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
             for (int e = 0; e < 8; e++) {
-                if (diag) E[e] = (j < ra + e) ? E[e] * an : 1.f;
-                else E[e] *= an;
+                E[e] = (j < ra + e) ? E[e] * an : 1.f;
                 const float w = kj * E[e];
-                X1[e] += pv[e] * w;
-                Y1[e] += av[e] * w;
+                X1[e] += DPT[j * LDT + ra + e] * w;
+                Y1[e] += DAT[j * LDT + ra + e] * w;
             }
-        };
-        for (int j = ra + 7; j >= ra; j--) row_step(j, true);  // the diagonal block
-        for (int j = ra - 1; j >= 0; j--) row_step(j, false);  // every row of the half is past j
+        }
+        // j < ra: E_rj = E_r,ra * F_j with F_j = prod_{j<t<=ra} a_t shared by the 8 rows, so
+        // the rows accumulate sum_j M_rj k^_j F_j and take their own factor E_r,ra at the end
+        {
+            float X1f[8], Y1f[8];
+#pragma unroll
+            for (int e = 0; e < 8; e++) {
+                X1f[e] = 0.f;
+                Y1f[e] = 0.f;
+            }
+            float F = 1.f;
+            for (int j = ra - 1; j >= 0; j--) {
+                F *= AL[(j + 1) * kD + d];
+                const float w = KH[j * kD + d] * F;
+                const float4 p0 = *reinterpret_cast<const float4*>(DPT + j * LDT + ra);
+                const float4 p1 = *reinterpret_cast<const float4*>(DPT + j * LDT + ra + 4);
+                const float4 a0 = *reinterpret_cast<const float4*>(DAT + j * LDT + ra);
+                const float4 a1 = *reinterpret_cast<const float4*>(DAT + j * LDT + ra + 4);
+                const float pv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+                const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+                for (int e = 0; e < 8; e++) {
+                    X1f[e] += pv[e] * w;
+                    Y1f[e] += av[e] * w;
+                }
+            }
+#pragma unroll
+            for (int e = 0; e < 8; e++) {
+                X1[e] += E[e] * X1f[e];
+                Y1[e] += E[e] * Y1f[e];
+            }
+        }
 #pragma unroll
         for (int e = 0; e < 8; e++) {
             const int i = 8 * h + e, rr = ra + e;
@@ -550,23 +573,36 @@ __global__ void __launch_bounds__(CH_THREADS, 1) grad_ch_simt_kernel(GradChArgs 
             E[e] = 1.f;
             X2[e] = 0.f;
         }
-        auto col_step = [&](int i, bool diag) {
+        // the diagonal block (i = ja .. ja+7) with per-column running products E_ij
+        for (int i = ja; i < ja + 8; i++) {
             const float ai = AL[i * kD + d], qi = QH[i * kD + d], kbi = bet[i] * KH[i * kD + d];
-            const float4 p0 = *reinterpret_cast<const float4*>(DPR + i * kChunk + ja);
-            const float4 p1 = *reinterpret_cast<const float4*>(DPR + i * kChunk + ja + 4);
-            const float4 a0 = *reinterpret_cast<const float4*>(DAR + i * kChunk + ja);
-            const float4 a1 = *reinterpret_cast<const float4*>(DAR + i * kChunk + ja + 4);
-            const float pv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
 #pragma unroll
             for (int e = 0; e < 8; e++) {
-                if (diag) E[e] = (i > ja + e) ? E[e] * ai : 1.f;
-                else E[e] *= ai;
-                X2[e] += (pv[e] * qi + av[e] * kbi) * E[e];
+                E[e] = (i > ja + e) ? E[e] * ai : 1.f;
+                X2[e] += (DPR[i * kChunk + ja + e] * qi + DAR[i * kChunk + ja + e] * kbi) * E[e];
             }
-        };
-        for (int i = ja; i < ja + 8; i++) col_step(i, true);  // the diagonal block
-        for (int i = ja + 8; i < kChunk; i++) col_step(i, false);
+        }
+        // i > ja+7: E_ij = E_ja+7,j * F_i with F_i = prod_{ja+7<t<=i} a_t shared by the 8 columns
+        {
+            float X2f[8];
+#pragma unroll
+            for (int e = 0; e < 8; e++) X2f[e] = 0.f;
+            float F = 1.f;
+            for (int i = ja + 8; i < kChunk; i++) {
+                F *= AL[i * kD + d];
+                const float wq = QH[i * kD + d] * F, wk = bet[i] * KH[i * kD + d] * F;
+                const float4 p0 = *reinterpret_cast<const float4*>(DPR + i * kChunk + ja);
+                const float4 p1 = *reinterpret_cast<const float4*>(DPR + i * kChunk + ja + 4);
+                const float4 a0 = *reinterpret_cast<const float4*>(DAR + i * kChunk + ja);
+                const float4 a1 = *reinterpret_cast<const float4*>(DAR + i * kChunk + ja + 4);
+                const float pv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+                const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+                for (int e = 0; e < 8; e++) X2f[e] += pv[e] * wq + av[e] * wk;
+            }
+#pragma unroll
+            for (int e = 0; e < 8; e++) X2[e] += E[e] * X2f[e];
+        }
 #pragma unroll
         for (int e = 0; e < 8; e++) {
             const int i = 8 * h + e, jj = ja + e;

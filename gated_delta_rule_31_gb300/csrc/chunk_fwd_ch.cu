@@ -37,13 +37,18 @@ constexpr uint32_t CS_KG = 157696;    // K .* Gamma image [64 x 128]
 constexpr uint32_t CS_KB = 174080;    // Kbar image [64 x 128]
 constexpr uint32_t CS_SCR = 190464;   // solve scratch [6][16][LDY] fp32
 constexpr uint32_t CS_SMALL = CS_SCR + SOLVE_SCRATCH_BYTES;  // bet[64], rho[128]
+// while A and P are formed: the scaled [k; q] operand L over the K .* Gamma and Kbar images,
+// R_1 / R_2 over T, R_3 over v (which is fetched afterwards)
+constexpr uint32_t CS_L = CS_KG, CS_R2 = CS_T, CS_R1 = CS_T + 8192, CS_R3 = CS_V;
 constexpr uint32_t CS_BYTES = CS_SMALL + 1024;
 static_assert(CS_A % 1024 == 0 && CS_T % 1024 == 0 && CS_P % 1024 == 0 && CS_KG % 1024 == 0 &&
                   CS_KB % 1024 == 0, "operand images need 1024-byte alignment");
 static_assert(CS_A + 64 * LDA * 4 <= CS_T && CS_T + 64 * LDA * 4 <= CS_P, "fp32 tiles");
 static_assert(CS_BYTES + 1024 <= 232448, "prep_ch smem");
 
-__global__ void __launch_bounds__(256, 1)
+constexpr int PCH_THREADS = 512;  // 16 warps: the A/P loop is latency-bound
+
+__global__ void __launch_bounds__(PCH_THREADS, 1)
     prep_ch_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                    const __grid_constant__ CUtensorMap mv, PrepArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -68,6 +73,8 @@ __global__ void __launch_bounds__(256, 1)
     float* bet = reinterpret_cast<float*>(sm + CS_SMALL);
     float* rho = bet + 64;  // [128] rows 0-63: k norm factors, 64-127: q norm factors
     bool ok;
+    uint32_t mph = 0;                        // bar_mma phase
+    bool mma_pend = false, v_pend = false;   // (thread 0) products / v copy not yet waited for
 
     if (tid == 0) {
         abort_sh = 0;
@@ -84,25 +91,23 @@ __global__ void __launch_bounds__(256, 1)
     tc_fence_after();
     const uint32_t tm = tmem_sh;
     if (tid == 0) {
-        mbar_expect_tx(&bar_tma, 6 * 8192);
+        mbar_expect_tx(&bar_tma, 4 * 8192);  // v follows once its region has served as R_3
         tma_load_4d(sm + CS_KQ + 0, &mk, 0, hk, t0, b, &bar_tma);
         tma_load_4d(sm + CS_KQ + 16384, &mk, 64, hk, t0, b, &bar_tma);
         tma_load_4d(sm + CS_KQ + 8192, &mq, 0, hk, t0, b, &bar_tma);
         tma_load_4d(sm + CS_KQ + 24576, &mq, 64, hk, t0, b, &bar_tma);
-        tma_load_4d(sm + CS_V + 0, &mv, 0, hv, t0, b, &bar_tma);
-        tma_load_4d(sm + CS_V + 8192, &mv, 64, hv, t0, b, &bar_tma);
     }
     {  // a_t = exp(g_t) per channel (tokens past T: g = 0, beta = 0: the state passes unchanged)
-        const int t = tid >> 2, q4 = tid & 3;
+        const int t = tid >> 3, q8 = tid & 7;
         const bool valid = t0 + t < P.T;
         const float4* src =
-            reinterpret_cast<const float4*>(a.g + (((size_t)b * P.T + t0 + t) * P.Hv + hv) * kD + 32 * q4);
-        float4* dst = reinterpret_cast<float4*>(al + t * kD + 32 * q4);
-        float4 gv[8];
+            reinterpret_cast<const float4*>(a.g + (((size_t)b * P.T + t0 + t) * P.Hv + hv) * kD + 16 * q8);
+        float4* dst = reinterpret_cast<float4*>(al + t * kD + 16 * q8);
+        float4 gv[4];
 #pragma unroll
-        for (int n = 0; n < 8; n++) gv[n] = valid ? src[n] : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int n = 0; n < 4; n++) gv[n] = valid ? src[n] : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int n = 0; n < 8; n++)
+        for (int n = 0; n < 4; n++)
             dst[n] = make_float4(__expf(gv[n].x), __expf(gv[n].y), __expf(gv[n].z), __expf(gv[n].w));
         if (tid < 64) bet[tid] = (t0 + tid < P.T) ? a.beta[((size_t)b * P.T + t0 + tid) * P.Hv + hv] : 0.f;
     }
@@ -114,7 +119,7 @@ __global__ void __launch_bounds__(256, 1)
             p *= al[t * kD + tid];
             gp[t * kD + tid] = p;
         }
-    } else {  // L2 norm factors: row tid-128 of the [k; q] tile (read order rotated by the row)
+    } else if (tid < 256) {  // L2 norm factors: row tid-128 of the [k; q] tile (read order rotated by the row)
         const int row = tid - 128;
         float ss = 0.f;
 #pragma unroll
@@ -127,72 +132,157 @@ __global__ void __launch_bounds__(256, 1)
         }
         rho[row] = P.use_norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
     }
-    {  // P image starts at zero (its upper triangle is never written)
+    if (tid < 256) {  // P image starts at zero (its upper triangle is never written)
         const uint4 z = make_uint4(0u, 0u, 0u, 0u);
         st_shared_v4(sb + CS_P + tid * 32, z.x, z.y, z.z, z.w);
         st_shared_v4(sb + CS_P + tid * 32 + 16, z.x, z.y, z.z, z.w);
     }
     __syncthreads();
 
-    // A and P on the CUDA cores. Lane = (j group jsel = lane >> 3, channel group cg = lane & 7);
-    // channel group cg owns channels 32 m + 4 cg + x (m, x < 4), so the 8 lanes of a group read
-    // 8 consecutive 16-byte words of a row (no bank conflict) with compile-time register
-    // indices. A thread owns column j1 = 4 warp + jsel and then j2 = 63 - j1, walking rows
-    // r = j .. 63 with the running decay E_rj of its channels (65 steps for every thread, so
-    // control flow stays uniform for the shuffles that sum the 8 channel groups).
+    // A and P by 16-row blocks I (rows 16I .. 16I + 15). For r in block I and j < 16I the decay
+    // factors through s = 16I - 1 into two products of per-token factors, each <= 1:
+    //   E_rj = [prod_{s<t<=r} a_t] [prod_{j<t<=s} a_t]
+    // so the blocks below the block diagonal are tcgen05 products D_I = L R_I^T of scaled
+    // operands: L = [k; q] with row r scaled by prod_{16I<=t<=r} a_t (rows of block 0 zero), R_I =
+    // rows j < 16I of k scaled by prod_{j<t<16I} a_t. The diagonal blocks keep the running decay
+    // on the CUDA cores.
     {
-        const int jsel = lane >> 3, cg = lane & 7;
-        const int j1 = 4 * warp + jsel, j2 = 63 - j1;
-        const int n1 = kChunk - j1;  // steps spent on j1
-        float kj[16], e[16];
-        // 16 channels of row `row` of the [k; q] tile: 4 bf16 (8 bytes) per m
-        auto load_row16 = [&](int row, float* x) {
-#pragma unroll
-            for (int m = 0; m < 4; m++) {
-                const uint32_t off = CS_KQ + sw128_chunk(row, 4 * m + (cg >> 1), 128) + 8 * (cg & 1);
-                const uint2 u = *reinterpret_cast<const uint2*>(sm + off);
-                x[4 * m] = bf16lo(u.x);
-                x[4 * m + 1] = bf16hi(u.x);
-                x[4 * m + 2] = bf16lo(u.y);
-                x[4 * m + 3] = bf16hi(u.y);
-            }
-        };
-        for (int s = 0; s <= kChunk; s++) {
-            const bool first = s < n1;
-            const int j = first ? j1 : j2;
-            const int r = first ? j1 + s : j2 + (s - n1);
-            if (s == 0 || s == n1) {  // start of a column: its k row, decay 1
-                load_row16(j, kj);
-#pragma unroll
-                for (int x = 0; x < 16; x++) e[x] = 1.f;
-            } else {  // E_rj = E_(r-1)j * a_r
-#pragma unroll
-                for (int m = 0; m < 4; m++) {
-                    const float4 f = *reinterpret_cast<const float4*>(al + r * kD + 32 * m + 4 * cg);
-                    e[4 * m] *= f.x; e[4 * m + 1] *= f.y; e[4 * m + 2] *= f.z; e[4 * m + 3] *= f.w;
-                }
-            }
-            float kr[16], qr[16];
-            load_row16(r, kr);
-            load_row16(64 + r, qr);
-            float pa = 0.f, pp = 0.f;
-#pragma unroll
-            for (int x = 0; x < 16; x++) {
-                const float w = kj[x] * e[x];
-                pa += kr[x] * w;
-                pp += qr[x] * w;
-            }
-#pragma unroll
-            for (int o = 1; o < 8; o <<= 1) {
-                pa += __shfl_xor_sync(0xffffffffu, pa, o);
-                pp += __shfl_xor_sync(0xffffffffu, pp, o);
-            }
-            if (cg == 0) {
-                if (r > j) Am[r * LDA + j] = bet[r] * rho[r] * rho[j] * pa;
-                const __nv_bfloat16 pv = __float2bfloat16_rn(P.scale * rho[64 + r] * rho[j] * pp);
-                *reinterpret_cast<__nv_bfloat16*>(sm + CS_P + sw128_off(r, j, 64)) = pv;
+        const int d = tid & 127, blk = tid >> 7;  // channel d, block blk
+        const __nv_bfloat16* kqs = reinterpret_cast<const __nv_bfloat16*>(sm + CS_KQ);
+        float p = blk ? 1.f : 0.f;
+        for (int i = 0; i < 16; i++) {  // L rows of block blk (k rows r, q rows 64 + r)
+            const int r = 16 * blk + i;
+            p *= al[r * kD + d];
+            const float kv = __bfloat162float(kqs[sw128_off(r, d, 128) >> 1]);
+            const float qv = __bfloat162float(kqs[sw128_off(64 + r, d, 128) >> 1]);
+            *reinterpret_cast<__nv_bfloat16*>(sm + CS_L + sw128_off(r, d, 128)) = __float2bfloat16_rn(kv * p);
+            *reinterpret_cast<__nv_bfloat16*>(sm + CS_L + sw128_off(64 + r, d, 128)) = __float2bfloat16_rn(qv * p);
+        }
+        if (blk) {  // R_blk: rows j = 16 blk - 1 .. 0
+            const uint32_t rb = blk == 1 ? CS_R1 : blk == 2 ? CS_R2 : CS_R3;
+            float sfx = 1.f;
+            for (int j = 16 * blk - 1; j >= 0; j--) {
+                const float kv = __bfloat162float(kqs[sw128_off(j, d, 128) >> 1]);
+                *reinterpret_cast<__nv_bfloat16*>(sm + rb + sw128_off(j, d, 16 * blk)) = __float2bfloat16_rn(kv * sfx);
+                sfx *= al[j * kD + d];
             }
         }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {  // D_I (M=128, N=16 I) into TMEM columns 0, 16, 48
+        tc_fence_after();
+#pragma unroll
+        for (int I = 1; I <= 3; I++) {
+            const uint32_t rb = I == 1 ? CS_R1 : I == 2 ? CS_R2 : CS_R3;
+            const uint32_t id = idesc_bf16(128, 16 * I, 0, 0);
+            for (int k0 = 0; k0 < kD; k0 += 16)
+                mma_bf16(tm + 8 * I * (I - 1), desc_kmajor(sb + CS_L, 128, 0, k0), desc_kmajor(sb + rb, 16 * I, 0, k0),
+                         id, k0 > 0);
+        }
+        mma_commit(&bar_mma);
+        mma_pend = true;
+    }
+    // diagonal blocks on the CUDA cores. Lane = (column jsel = lane >> 4, channel group
+    // cg = lane & 15); channel group cg owns channels 32 m + 4 (cg & 7) + x for m = (cg >> 3) +
+    // {0, 2}, x < 4 (the 8 lanes sharing m read 8 consecutive 8-byte words of a row). Warp w
+    // takes block I = w >> 2 and, with c = w & 3, the column pairs (16I + 2c, +1) and then
+    // (16I + 14 - 2c, +1): both halves of the warp walk the same rows jb .. 16I + 15, so every
+    // row load serves two columns, and every warp makes 18 steps.
+    {
+        const int jsel = lane >> 4, cg = lane & 15, mq = cg >> 3, c8 = cg & 7;
+        const int I = warp >> 2, c = warp & 3, rend = 16 * I + 16;
+        float kj[8], e[8];
+        auto load_row8 = [&](int row, float* x) {
+#pragma unroll
+            for (int mm = 0; mm < 2; mm++) {
+                const int m = mq + 2 * mm;
+                const uint32_t off = CS_KQ + sw128_chunk(row, 4 * m + (c8 >> 1), 128) + 8 * (c8 & 1);
+                const uint2 u = *reinterpret_cast<const uint2*>(sm + off);
+                x[4 * mm] = bf16lo(u.x);
+                x[4 * mm + 1] = bf16hi(u.x);
+                x[4 * mm + 2] = bf16lo(u.y);
+                x[4 * mm + 3] = bf16hi(u.y);
+            }
+        };
+#pragma unroll 1
+        for (int ph = 0; ph < 2; ph++) {
+            const int jb = 16 * I + (ph == 0 ? 2 * c : 14 - 2 * c);
+            const int j = jb + jsel;
+            load_row8(j, kj);
+#pragma unroll
+            for (int x = 0; x < 8; x++) e[x] = 1.f;
+            for (int r = jb; r < rend; r++) {
+                const bool past = r > j;  // E_rj = E_(r-1)j * a_r past the column's own row
+#pragma unroll
+                for (int mm = 0; mm < 2; mm++) {
+                    const float4 f = *reinterpret_cast<const float4*>(al + r * kD + 32 * (mq + 2 * mm) + 4 * c8);
+                    e[4 * mm] *= past ? f.x : 1.f;
+                    e[4 * mm + 1] *= past ? f.y : 1.f;
+                    e[4 * mm + 2] *= past ? f.z : 1.f;
+                    e[4 * mm + 3] *= past ? f.w : 1.f;
+                }
+                float kr[8], qr[8];
+                load_row8(r, kr);
+                load_row8(64 + r, qr);
+                float pa = 0.f, pp = 0.f;
+#pragma unroll
+                for (int x = 0; x < 8; x++) {
+                    const float w = kj[x] * e[x];
+                    pa += kr[x] * w;
+                    pp += qr[x] * w;
+                }
+#pragma unroll
+                for (int o = 1; o < 16; o <<= 1) {
+                    pa += __shfl_xor_sync(0xffffffffu, pa, o);
+                    pp += __shfl_xor_sync(0xffffffffu, pp, o);
+                }
+                if (cg == 0 && r >= j) {
+                    if (r > j) Am[r * LDA + j] = bet[r] * rho[r] * rho[j] * pa;
+                    const __nv_bfloat16 pv = __float2bfloat16_rn(P.scale * rho[64 + r] * rho[j] * pp);
+                    *reinterpret_cast<__nv_bfloat16*>(sm + CS_P + sw128_off(r, j, 64)) = pv;
+                }
+            }
+        }
+    }
+    ok = mbar_wait(&bar_mma, mph, &abort_sh, a.status, 18);
+    mph ^= 1;
+    if (__syncthreads_or(!ok)) goto teardown;
+    if (tid == 0) mma_pend = false;
+    tc_fence_after();
+    if (warp < 4) {  // below the block diagonal: row = 32 warp + lane of D (k rows, then q rows)
+        const int row = 32 * warp + lane, rr = row & 63, rI = rr >> 4;
+#pragma unroll
+        for (int I = 1; I <= 3; I++) {
+#pragma unroll
+            for (int pc = 0; pc < I; pc++) {
+                float v[16];
+                tmem_ld16(tmem_at(tm, 32 * warp, 8 * I * (I - 1) + 16 * pc), v);
+                tmem_wait_ld();
+                if (rI == I) {
+                    if (row < 64) {
+                        const float f = bet[rr] * rho[rr];
+#pragma unroll
+                        for (int e2 = 0; e2 < 16; e2++) Am[rr * LDA + 16 * pc + e2] = f * rho[16 * pc + e2] * v[e2];
+                    } else {
+                        const float f = P.scale * rho[64 + rr];
+#pragma unroll
+                        for (int e2 = 0; e2 < 16; e2++)
+                            *reinterpret_cast<__nv_bfloat16*>(sm + CS_P + sw128_off(rr, 16 * pc + e2, 64)) =
+                                __float2bfloat16_rn(f * rho[16 * pc + e2] * v[e2]);
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {  // v into its region (R_3 is no longer read)
+        mbar_expect_tx(&bar_tma, 2 * 8192);
+        tma_load_4d(sm + CS_V + 0, &mv, 0, hv, t0, b, &bar_tma);
+        tma_load_4d(sm + CS_V + 8192, &mv, 64, hv, t0, b, &bar_tma);
+        v_pend = true;
     }
     __syncthreads();
     if (tid < 128) {  // prod_{t>r} a_t, channel d = tid, in place of a_t (read before written)
@@ -204,42 +294,42 @@ __global__ void __launch_bounds__(256, 1)
         }
         a.gam[(bh * P.NC + c) * kD + tid] = gp[(kChunk - 1) * kD + tid];  // Gamma_C per channel
     }
-    {  // P to the record
+    if (tid < 256) {  // P to the record
         const uint4 u = ld_shared_v4(sb + CS_P + tid * 32), w = ld_shared_v4(sb + CS_P + tid * 32 + 16);
         st_global16(rec + REC_P + tid * 32, u);
         st_global16(rec + REC_P + tid * 32 + 16, w);
     }
     ut_solve(Am, Tm, Xs, tid);  // T = (I + A)^-1 (ends with a barrier; suffix products done)
     {  // [Tw; Tu]: Tw = T diag(beta rho_k), Tu = T diag(beta) (K-major A operand, over A)
-        const int row = tid >> 1, half = tid & 1;
+        const int row = tid >> 2, qtr = tid & 3;  // 16 columns per thread
         const int i = row & 63;
         const bool isw = row < 64;
-        const float* trow = Tm + i * LDA + 32 * half;
-        float t[32], x[32];
+        const float* trow = Tm + i * LDA + 16 * qtr;
+        float t[16], x[16];
 #pragma unroll
-        for (int q = 0; q < 8; q++) {
+        for (int q = 0; q < 4; q++) {
             const float4 f = *reinterpret_cast<const float4*>(trow + 4 * q);
             const float tv[4] = {f.x, f.y, f.z, f.w};
 #pragma unroll
             for (int e = 0; e < 4; e++) {
-                const int j = 32 * half + 4 * q + e;
+                const int j = 16 * qtr + 4 * q + e;
                 t[4 * q + e] = (j >> 4) <= (i >> 4) ? tv[e] : 0.f;
                 x[4 * q + e] = t[4 * q + e] * bet[j] * (isw ? rho[j] : 1.f);
             }
         }
 #pragma unroll
-        for (int q = 0; q < 4; q++) {
-            st_chunk(sb + CS_A + sw128_chunk(row, 4 * half + q, 128), x + 8 * q, 1.f);
+        for (int q = 0; q < 2; q++) {
+            st_chunk(sb + CS_A + sw128_chunk(row, 2 * qtr + q, 128), x + 8 * q, 1.f);
             if (isw && rec2)  // T itself for the backward
-                st_global16(rec2 + REC2_T + sw128_chunk(i, 4 * half + q, 64), pack8(t + 8 * q, 1.f));
+                st_global16(rec2 + REC2_T + sw128_chunk(i, 2 * qtr + q, 64), pack8(t + 8 * q, 1.f));
         }
     }
-    {  // K .* Gamma and Kbar = diag(rho_k) K .* prod_{t>r} a_t, row r = tid >> 2, 32 channels each
-        const int r = tid >> 2, q4 = tid & 3;
+    {  // K .* Gamma and Kbar = diag(rho_k) K .* prod_{t>r} a_t, row r = tid >> 3, 16 channels each
+        const int r = tid >> 3, q8 = tid & 7;
         const float rk = rho[r];
 #pragma unroll
-        for (int q = 0; q < 4; q++) {
-            const int j = 4 * q4 + q;  // 8-channel chunk of the row
+        for (int q = 0; q < 2; q++) {
+            const int j = 2 * q8 + q;  // 8-channel chunk of the row
             float x[8], yg[8], yb[8];
             unpack8(ld_shared_v4(sb + CS_KQ + sw128_chunk(r, j, 128)), x);
             const float4* g4 = reinterpret_cast<const float4*>(gp + r * kD + 8 * j);
@@ -266,7 +356,10 @@ __global__ void __launch_bounds__(256, 1)
 
     // W = Tw (K .* Gamma) and U~ = Tu V as two M=128 products of [Tw; Tu] (rows 0-63 of the
     // first, rows 64-127 of the second are the wanted ones); B operands MN-major
+    ok = mbar_wait(&bar_tma, 1, &abort_sh, a.status, 19);
+    if (__syncthreads_or(!ok)) goto teardown;
     if (tid == 0) {
+        v_pend = false;
         tc_fence_after();
         const uint32_t id = idesc_bf16(128, 128, 0, 1);
         for (int k0 = 0; k0 < kChunk; k0 += 16) {
@@ -274,11 +367,14 @@ __global__ void __launch_bounds__(256, 1)
             mma_bf16(tm + 128, desc_kmajor(sb + CS_A, 128, 0, k0), desc_mnmajor(sb + CS_V, 64, 0, k0), id, k0 > 0);
         }
         mma_commit(&bar_mma);
+        mma_pend = true;
     }
-    ok = mbar_wait(&bar_mma, 0, &abort_sh, a.status, 16);
+    ok = mbar_wait(&bar_mma, mph, &abort_sh, a.status, 16);
+    mph ^= 1;
     if (__syncthreads_or(!ok)) goto teardown;
+    if (tid == 0) mma_pend = false;
     tc_fence_after();
-    {
+    if (warp < 8) {
         const int lg = warp & 3, h = warp >> 2;
         if (lg < 2) {  // W rows i = 32 lg + lane -> W image (over T)
             const int i = 32 * lg + lane;
@@ -318,11 +414,14 @@ __global__ void __launch_bounds__(256, 1)
         for (int k0 = 0; k0 < kChunk; k0 += 16)
             mma_bf16(tm + 128, desc_kmajor(sb + CS_P, 64, 0, k0), desc_mnmajor(sb + CS_T, 64, 0, k0), idp, k0 > 0);
         mma_commit(&bar_mma);
+        mma_pend = true;
     }
-    ok = mbar_wait(&bar_mma, 1, &abort_sh, a.status, 17);
+    ok = mbar_wait(&bar_mma, mph, &abort_sh, a.status, 17);
+    mph ^= 1;
     if (__syncthreads_or(!ok)) goto teardown;
+    if (tid == 0) mma_pend = false;
     tc_fence_after();
-    {
+    if (warp < 8) {
         const int lg = warp & 3, h = warp >> 2;
         {  // Mneg rows d = 32 lg + lane
             const int d = 32 * lg + lane;
@@ -363,9 +462,11 @@ __global__ void __launch_bounds__(256, 1)
 teardown:
     tc_fence_before();
     __syncthreads();
-    if (abort_sh && tid == 0) {  // let copies still in flight land before the CTA exits
+    if (abort_sh && tid == 0) {  // let copies and products still in flight finish before the CTA exits
         volatile int never = 0;
         mbar_wait(&bar_tma, 0, &never, nullptr, 0);
+        if (v_pend) mbar_wait(&bar_tma, 1, &never, nullptr, 0);
+        if (mma_pend) mbar_wait(&bar_mma, mph, &never, nullptr, 0);
     }
     __syncthreads();
     if (warp == 0) tmem_dealloc(tm, 256);
@@ -378,7 +479,7 @@ cudaError_t launch_prep_ch(const PrepArgs& a, const CUtensorMap& mq, const CUten
     if (e != cudaSuccess) return e;
     dim3 grid(a.p.NC, a.p.Hv, a.p.B);
     trace_begin("chunk_prep_channel", s);
-    prep_ch_kernel<<<grid, 256, smem, s>>>(mq, mk, mv, a);
+    prep_ch_kernel<<<grid, PCH_THREADS, smem, s>>>(mq, mk, mv, a);
     trace_end(s);
     return cudaGetLastError();
 }

@@ -101,8 +101,10 @@ gdr_status gdr_fwd_sequential(const gdr_problem* p, const void* q, const void* k
 /* Chunked backward (VJP) of gdr_fwd_chunked for the loss <do, o> + <dht, ht>: writes dq, dk,
  * dv, dg, dbeta and, if dh0 != NULL, dh0. h0 and dht may be NULL (zero). Recomputes the
  * chunk-local terms and the chunk-start states instead of reading saved activations;
- * the normalisation backward is done inside. Same support matrix as gdr_fwd_chunked, except
- * that the per-channel gate is forward only (GDR_ERR_UNSUPPORTED here).
+ * the normalisation backward is done inside. Same support matrix as gdr_fwd_chunked; with the
+ * per-channel gate dg is [B,T,Hv,Dk] (one gradient per key channel) and the decay-weighted
+ * intra-chunk contractions run on the CUDA cores with running products of the per-token
+ * factors (no decay can overflow), the dense products on the tensor cores.
  * Deterministic: no floating-point atomics. */
 gdr_status gdr_bwd_chunked(const gdr_problem* p, const void* q, const void* k, const void* v,
                            const float* g, const float* beta, const float* h0, const void* do_,
@@ -112,8 +114,8 @@ gdr_status gdr_bwd_chunked(const gdr_problem* p, const void* q, const void* k, c
 
 /* Sequential (token-by-token) VJP of gdr_fwd_sequential for the loss <do, o> + <dht, ht>:
  * the "sequential case" of "Adding VJP for gated delta net" (MLX PR #4565). Every dtype, gate
- * (scalar or per channel) and Dk, Dv in {32, 64, 128}; the reference backward for problems
- * the chunked VJP does not cover (fp32, other head sizes, the per-channel gate). Arguments,
+ * (scalar or per channel) and Dk, Dv in {32, 64, 128}; the backward for problems the chunked
+ * VJP does not cover (fp32, other head sizes). Arguments,
  * layouts and outputs as gdr_bwd_chunked (gradients fp32; dg has g's shape). The forward is
  * re-run with a checkpoint every 64 tokens (B*Hv*ceil(T/64) fp32 states in the workspace)
  * and each 64-token segment is recomputed in reverse. Deterministic (fixed-order sums, no
@@ -129,7 +131,8 @@ gdr_status gdr_bwd_sequential(const gdr_problem* p, const void* q, const void* k
  * entering every chunk (bf16, opaque layout, gdr_chunk_states_bytes() bytes:
  * B*Hv*ceil(T/64)*32 KB, caller-owned, 256-byte aligned); the backward then reads them
  * instead of re-running the forward scan. Chunk-local operators are still recomputed by
- * the backward. Same support matrix as gdr_bwd_chunked; 0 if the problem is invalid. */
+ * the backward. Same support matrix as gdr_bwd_chunked (scalar or per-channel gate); 0 if
+ * the problem is invalid. */
 size_t gdr_chunk_states_bytes(const gdr_problem* p);
 size_t gdr_bwd_chunked_states_workspace(const gdr_problem* p);
 
@@ -157,8 +160,9 @@ gdr_status gdr_bwd_chunked_states(const gdr_problem* p, const void* q, const voi
  * bitwise identical to gdr_fwd_chunked / gdr_bwd_chunked. The buffer must not be modified
  * between the two calls, and the backward must get the same q, k, v, g, beta and problem.
  * Workspaces: gdr_fwd_chunked_saved_workspace() (the status word only) and
- * gdr_bwd_chunked_saved_workspace(). Same support matrix as gdr_bwd_chunked; the size
- * queries return 0 for an invalid or unsupported problem. Errors as gdr_fwd_chunked, plus
+ * gdr_bwd_chunked_saved_workspace(). Same support matrix as gdr_bwd_chunked but for the
+ * scalar gate only (GDR_ERR_UNSUPPORTED for the per-channel gate); the size queries return 0
+ * for an invalid or unsupported problem. Errors as gdr_fwd_chunked, plus
  * GDR_ERR_WORKSPACE if `saved` is NULL or smaller than required. */
 size_t gdr_chunk_saved_bytes(const gdr_problem* p);
 size_t gdr_fwd_chunked_saved_workspace(const gdr_problem* p);

@@ -468,16 +468,6 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
             tmem_wait_st();
         }
         sync_for_mma();
-        if (tid < 256) {  // column sums of Z: dgamma_j -= sum_r Z_rj (4 threads per column)
-            const int j = tid & 63, part4 = tid >> 6;
-            float s = 0.f;
-#pragma unroll
-            for (int i = 16 * part4; i < 16 * part4 + 16; i++) s += ZS[fsw(i, j)];
-            red[16 + tid] = s;
-        }
-        __syncthreads();
-        if (tid < 64) dgc[tid] -= red[16 + tid] + red[80 + tid] + red[144 + tid] + red[208 + tid];
-
         // ------------------------------------------------------------ M3
         if (tid == 0) {
             tc_fence_after();
@@ -495,6 +485,15 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
             }
             mma_commit(&bar_mma);
         }
+        if (tid < 256) {  // column sums of Z (while M3 runs): dgamma_j -= sum_r Z_rj (4 threads per column)
+            const int j = tid & 63, part4 = tid >> 6;
+            float s = 0.f;
+#pragma unroll
+            for (int i = 16 * part4; i < 16 * part4 + 16; i++) s += ZS[fsw(i, j)];
+            red[16 + tid] = s;
+        }
+        __syncthreads();
+        if (tid < 64) dgc[tid] -= red[16 + tid] + red[80 + tid] + red[144 + tid] + red[208 + tid];
         if (!wait_mma(45)) goto teardown;
         if (more && tid == 0) prefetch(0);
         {
@@ -682,13 +681,6 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
             }
         }
         __syncthreads();
-        if (tid < 256) {
-            const int j = tid & 63, part4 = tid >> 6;
-            float s = 0.f;
-#pragma unroll
-            for (int i = 16 * part4; i < 16 * part4 + 16; i++) s += ZS[fsw(i, j)];
-            red[16 + tid] = s;
-        }
         {  // N_rj = rk_j (M_rj + M_jr) -> image (G_DH + 16K); 8 columns per lane
             const int jc = 2 * qt + (lane >> 4);
             float nrow[8];
@@ -710,6 +702,14 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
             mma_commit(&bar_mma);
             if (more) prefetch(4);  // v: its buffer held M, read before the sync above
         }
+        if (tid < 256) {  // column sums of dA-Z (while M7 runs)
+            const int j = tid & 63, part4 = tid >> 6;
+            float s = 0.f;
+#pragma unroll
+            for (int i = 16 * part4; i < 16 * part4 + 16; i++) s += ZS[fsw(i, j)];
+            red[16 + tid] = s;
+        }
+        __syncthreads();
         // per-head scalars: dgamma -> dg (reverse cumsum within the chunk), dbeta
         if (tid < 64) {  // two warps; row r = tid
             float s3 = 0.f, dgr = dgc[tid] - (red[16 + tid] + red[80 + tid] + red[144 + tid] + red[208 + tid]);

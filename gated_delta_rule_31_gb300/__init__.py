@@ -22,7 +22,7 @@ from ._build import LIB as _LIB_PATH
 from ._build import build
 
 __all__ = ["build", "fwd_chunked", "bwd_chunked", "fwd_sequential", "bwd_sequential", "decode_step", "GdrError",
-           "fwd_workspace_bytes", "bwd_workspace_bytes", "lib", "Problem", "workspace_status", "trace"]
+           "fwd_workspace_bytes", "bwd_workspace_bytes", "lib", "Problem", "workspace_status", "selftest_wait_expiry", "trace"]
 
 GDR_F32, GDR_BF16 = 0, 1
 GDR_GATE_SCALAR, GDR_GATE_CHANNEL = 0, 1
@@ -86,6 +86,8 @@ def lib():
         L.gdr_bwd_chunked_saved.restype = ctypes.c_int
         L.gdr_workspace_status.argtypes = [P, sz, st]
         L.gdr_workspace_status.restype = ctypes.c_int
+        L.gdr_selftest_wait_expiry.argtypes = [P, sz, st]
+        L.gdr_selftest_wait_expiry.restype = ctypes.c_int
         L.gdr_trace_enable.argtypes = [ctypes.c_int]
         L.gdr_trace_enable.restype = ctypes.c_int
         L.gdr_trace_collect.argtypes = [ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_float),
@@ -315,6 +317,13 @@ def decode_step(q, k, v, g, beta, state, scale=None, use_qk_l2norm=True, out=Non
 def workspace_status(ws) -> int:
     """Reads and clears the status word of a chunked workspace (0 = ok, 5 = a wait expired)."""
     return int(lib().gdr_workspace_status(_ptr(ws), ctypes.c_size_t(ws.numel()), _stream(ws.device)))
+
+
+def selftest_wait_expiry(ws) -> None:
+    """gdr_selftest_wait_expiry: one CTA's bounded wait on a phase that nothing completes gives up
+    after about a second and records GDR_ERR_TIMEOUT in the status word of ``ws`` (uint8, >= 256
+    bytes, on the GPU); read it back with workspace_status."""
+    _check(lib().gdr_selftest_wait_expiry(_ptr(ws), ctypes.c_size_t(ws.numel()), _stream(ws.device)))
 
 
 class trace:

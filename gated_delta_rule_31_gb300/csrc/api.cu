@@ -9,6 +9,7 @@
 
 #include "gdr.h"
 #include "chunk.h"
+#include "common.cuh"
 #include "kernels.h"
 
 using namespace gdr;
@@ -16,6 +17,21 @@ using namespace gdr;
 namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// One CTA waits on an mbarrier phase that nothing completes: the bounded wait gives up after
+// about a second, records the expiry in the status word and the kernel returns.
+__global__ void wait_expiry_kernel(int* status) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_sh;
+    if (threadIdx.x == 0) {
+        abort_sh = 0;
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
+    mbar_wait(&bar, 0, &abort_sh, status, 99);
+    __syncthreads();
+}
 bool dim_ok(int d) { return d == 32 || d == 64 || d == 128; }
 
 gdr_status check_problem(const gdr_problem* p, bool decode) {
@@ -387,6 +403,14 @@ gdr_status gdr_workspace_status(void* ws, size_t ws_bytes, gdr_stream_t stream) 
     if (cudaMemsetAsync(ws, 0, 256, st) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess)
         return GDR_ERR_CUDA;
     return word[0] == GDR_ERR_TIMEOUT ? GDR_ERR_TIMEOUT : GDR_ERR_CUDA;
+}
+
+gdr_status gdr_selftest_wait_expiry(void* ws, size_t ws_bytes, gdr_stream_t stream) {
+    if (!ws || ws_bytes < 256 || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return GDR_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cudaMemsetAsync(ws, 0, 256, st) != cudaSuccess) return GDR_ERR_CUDA;
+    wait_expiry_kernel<<<1, 32, 0, st>>>(static_cast<int*>(ws));
+    return cudaGetLastError() == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -193,6 +193,13 @@ gdr_status gdr_decode_step(const gdr_problem* p, const void* q, const void* k, c
  * chunked kernels: GDR_OK, or GDR_ERR_TIMEOUT if a bounded wait expired. */
 gdr_status gdr_workspace_status(void* ws, size_t ws_bytes, gdr_stream_t stream);
 
+/* Check of the library's own failure handling (not an operation of the gated delta rule):
+ * launches one CTA whose wait on an mbarrier phase that nothing completes gives up after
+ * about one second, records GDR_ERR_TIMEOUT in the status word of `ws` (first 256 bytes,
+ * 256-byte aligned) and returns, so the context stays usable. Asynchronous on `stream`;
+ * gdr_workspace_status then reports GDR_ERR_TIMEOUT. */
+gdr_status gdr_selftest_wait_expiry(void* ws, size_t ws_bytes, gdr_stream_t stream);
+
 /* Bytes of the scratch array built into the library for gdr_fwd_chunked_noalloc. */
 #define GDR_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
 

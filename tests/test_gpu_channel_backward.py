@@ -129,7 +129,7 @@ def test_channel_autograd_runs_the_chunked_vjp():
         ((o.float() * x["do"].to(dev).float()).sum() + (ht * x["dht"].to(dev)).sum()).backward()
         torch.cuda.synchronize()
     names = {n for n, _ in tr.records}
-    assert "chunk_grad_channel_mma" in names and "chunk_grad_channel_simt" in names, names
+    assert "chunk_grad_channel_mma" in names and "chunk_grad_channel_contract" in names, names
     ref = oracle.backward(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"], x["do"], x["dht"])
     for n in ("q", "k", "v", "g", "beta", "h0"):
         assert rel_err(t[n].grad, ref["d" + n]) <= BF16_TOL, n

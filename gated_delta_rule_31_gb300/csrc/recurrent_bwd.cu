@@ -333,12 +333,64 @@ cudaError_t launch_seq_bwd_d(const SeqBwdArgs& a, cudaStream_t s) {
     }
 }
 
+// The same sum and norm backward for bf16 q, k with Dk = 128, one warp per (b, t, key head):
+// lane l owns channels 4l .. 4l + 3 (128-bit loads of dq^, dk^, 64-bit loads of q, k), and the
+// four sums are warp reductions, so a block of 8 warps handles 8 rows without a barrier.
+__global__ void __launch_bounds__(256) qk_norm_bwd_warp_kernel(SeqBwdArgs A) {
+    const int lane = threadIdx.x & 31;
+    const size_t row = (size_t)blockIdx.x * 8 + (threadIdx.x >> 5);  // (b * T + t) * Hk + hk
+    if (row >= (size_t)A.B * A.T * A.Hk) return;
+    const int G = A.Hv / A.Hk;
+    const size_t bt = row / A.Hk;
+    const int hk = (int)(row % A.Hk);
+    float4 dq = make_float4(0.f, 0.f, 0.f, 0.f), dk = dq;
+    for (int h = 0; h < G; h++) {
+        const size_t i = (bt * A.Hv + (size_t)hk * G + h) * 128 + 4 * lane;
+        const float4 x = *reinterpret_cast<const float4*>(A.dqh + i), y = *reinterpret_cast<const float4*>(A.dkh + i);
+        dq.x += x.x; dq.y += x.y; dq.z += x.z; dq.w += x.w;
+        dk.x += y.x; dk.y += y.y; dk.z += y.z; dk.w += y.w;
+    }
+    const size_t xi = row * 128 + 4 * lane;
+    const uint2 qu = *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(A.q) + xi);
+    const uint2 ku = *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(A.k) + xi);
+    const float q[4] = {bf16lo(qu.x), bf16hi(qu.x), bf16lo(qu.y), bf16hi(qu.y)};
+    const float k[4] = {bf16lo(ku.x), bf16hi(ku.x), bf16lo(ku.y), bf16hi(ku.y)};
+    float oq[4] = {dq.x, dq.y, dq.z, dq.w}, ok[4] = {dk.x, dk.y, dk.z, dk.w};
+    if (A.use_norm) {
+        float sq = 0.f, sk = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            sq += q[e] * q[e];
+            sk += k[e] * k[e];
+        }
+        sq = warp_sum(sq);
+        sk = warp_sum(sk);
+        const float rq = 1.0f / sqrtf(sq + 1e-6f), rk = 1.0f / sqrtf(sk + 1e-6f);
+        float tq = 0.f, tk = 0.f;  // q^ . dq^, k^ . dk^
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            tq += rq * q[e] * oq[e];
+            tk += rk * k[e] * ok[e];
+        }
+        tq = warp_sum(tq);
+        tk = warp_sum(tk);
+#pragma unroll
+        for (int e = 0; e < 4; e++) {
+            oq[e] = rq * (oq[e] - rq * q[e] * tq);
+            ok[e] = rk * (ok[e] - rk * k[e] * tk);
+        }
+    }
+    *reinterpret_cast<float4*>(A.dq + xi) = make_float4(oq[0], oq[1], oq[2], oq[3]);
+    *reinterpret_cast<float4*>(A.dk + xi) = make_float4(ok[0], ok[1], ok[2], ok[3]);
+}
+
 }  // namespace
 
 cudaError_t launch_qk_norm_backward(const SeqBwdArgs& a, cudaStream_t s) {
     if (a.Dk != 128 || !a.bf16 || !a.channel) return cudaErrorInvalidValue;
+    const size_t rows = (size_t)a.B * a.T * a.Hk;
     trace_begin("qk_norm_backward", s);
-    seq_bwd_finish_kernel<128, __nv_bfloat16><<<a.B * a.T * a.Hk, 128, 0, s>>>(a);
+    qk_norm_bwd_warp_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(a);
     trace_end(s);
     return cudaGetLastError();
 }

@@ -206,11 +206,12 @@ def chunk_ops_channel(K, Q, V, g, beta, scale, rk, rq):
     Kbar = Kh * suf
     Mneg = -Kbar.T @ W
     Qc = scale * Qh * Gam - P @ W
-    return dict(GamC=Gam[-1], W=W, Ut=Ut, P=P, Kbar=Kbar, Mneg=Mneg, Qc=Qc)
+    return dict(GamC=Gam[-1], W=W, Ut=Ut, P=P, Kbar=Kbar, Mneg=Mneg, Qc=Qc, T=T, a=a, Gam=Gam, suf=suf)
 
 
-def forward_channel(q, k, v, g, beta, h0, scale, norm=True, C=64):
-    """Per-channel gate: o, ht with H1 = diag(Gamma_C) H0 + Mneg H0 + Kbar^T U~ per chunk."""
+def forward_channel(q, k, v, g, beta, h0, scale, norm=True, C=64, states=None):
+    """Per-channel gate: o, ht with H1 = diag(Gamma_C) H0 + Mneg H0 + Kbar^T U~ per chunk
+    (chunk-start states into `states[(b, hv, chunk)]` when a dict is given)."""
     B, T, Hk, Dk = q.shape
     Hv, Dv = v.shape[2:]
     grp = Hv // Hk
@@ -225,8 +226,141 @@ def forward_channel(q, k, v, g, beta, h0, scale, norm=True, C=64):
                 Q = _pad(q[b_, s:e, hk], C)
                 ops = chunk_ops_channel(K, Q, _pad(v[b_, s:e, hv], C), _pad(g[b_, s:e, hv], C),
                                         _pad(beta[b_, s:e, hv], C), scale, _norm_factor(K, norm), _norm_factor(Q, norm))
+                if states is not None:
+                    states[(b_, hv, s // C)] = H.copy()
                 O = ops["Qc"] @ H + ops["P"] @ ops["Ut"]
                 H = ops["GamC"][:, None] * H + ops["Mneg"] @ H + ops["Kbar"].T @ ops["Ut"]
                 o[b_, s:e, hv] = O[: e - s]
             ht[b_, hv] = H.T
     return o, ht
+
+
+def _blocked_contractions(dPs, dA, Kh, Qh, beta, a, bs):
+    """The four decay-weighted contractions of the per-channel VJP, organised as the kernel
+    does: by bs-row blocks, the parts below the block diagonal as products of operands scaled
+    by products of per-token factors (the decay factored through the block boundary), the
+    diagonal blocks with running products. Returns X1, Y1 (row side) and X2 (column side):
+        X1[r] = sum_{j<=r} dPs_rj k^_j E_rj,   Y1[r] = sum_{j<r} dA_rj k^_j E_rj
+        X2[j] = sum_{i>=j} dPs_ij q^_i E_ij + sum_{i>j} dA_ij beta_i k^_i E_ij"""
+    C, Dk = Kh.shape
+    X1, Y1, X2 = np.zeros((C, Dk)), np.zeros((C, Dk)), np.zeros((C, Dk))
+    nb = C // bs
+    for I in range(nb):
+        rows = range(bs * I, bs * I + bs)
+        # row side, j in earlier blocks: E_rj = [prod_{bs I<=t<=r} a_t] [prod_{j<t<bs I} a_t]
+        if I > 0:
+            R = np.zeros((bs * I, Dk))
+            sfx = np.ones(Dk)
+            for j in range(bs * I - 1, -1, -1):
+                R[j] = Kh[j] * sfx
+                sfx = sfx * a[j]
+            DX = dPs[bs * I:bs * I + bs, :bs * I] @ R
+            DY = dA[bs * I:bs * I + bs, :bs * I] @ R
+            c = np.ones(Dk)
+            for i, r in enumerate(rows):
+                c = c * a[r]
+                X1[r] += c * DX[i]
+                Y1[r] += c * DY[i]
+        # row side inside the diagonal block: running decay
+        for r in rows:
+            e = np.ones(Dk)
+            for j in range(r, bs * I - 1, -1):
+                if j < r:
+                    e = e * a[j + 1]
+                X1[r] += dPs[r, j] * Kh[j] * e
+                Y1[r] += dA[r, j] * Kh[j] * e
+        # column side, i in later blocks: E_ij = [prod_{j<t<=bs I+bs-1} a_t] [prod_{bs I+bs<=t<=i} a_t]
+        if I < nb - 1:
+            i0 = bs * I + bs
+            Qs = np.zeros((C - i0, Dk))
+            Ks = np.zeros((C - i0, Dk))
+            pr = np.ones(Dk)
+            for i in range(i0, C):
+                pr = pr * a[i]
+                Qs[i - i0] = Qh[i] * pr
+                Ks[i - i0] = beta[i] * Kh[i] * pr
+            DC = dPs[i0:, bs * I:bs * I + bs].T @ Qs + dA[i0:, bs * I:bs * I + bs].T @ Ks
+            f = np.ones(Dk)
+            for jj in range(bs - 1, -1, -1):
+                j = bs * I + jj
+                X2[j] += f * DC[jj]
+                f = f * a[j]
+        # column side inside the diagonal block
+        for j in rows:
+            e = np.ones(Dk)
+            for i in range(j, bs * I + bs):
+                if i > j:
+                    e = e * a[i]
+                X2[j] += (dPs[i, j] * Qh[i] + dA[i, j] * beta[i] * Kh[i]) * e
+    return X1, Y1, X2
+
+
+def backward_channel(q, k, v, g, beta, h0, do, dht, scale, norm=True, C=64, bs=16):
+    """Per-channel gate VJP of <do, o> + <dht, ht> as the chunked kernels organise it: the
+    forward states, the reverse scan dH0 = diag(Gamma_C) dH1 + Mneg^T dH1 + Qc^T dO, the dense
+    products X = dO H0^T, Y = U dH1^T, Z = T^T dW, dP, dT, dA, and the decay-weighted
+    contractions by bs-row blocks (_blocked_contractions); dgamma per key channel, dg its
+    in-chunk reverse cumulative sum plus the Gamma_C terms on every token."""
+    B, T, Hk, Dk = q.shape
+    Hv, Dv = v.shape[2:]
+    grp = Hv // Hk
+    states = {}
+    forward_channel(q, k, v, g, beta, h0, scale, norm, C, states=states)
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    dg, dbeta = np.zeros_like(g), np.zeros_like(beta)
+    dh0 = np.zeros((B, Hv, Dv, Dk))
+    chunks = _chunks(T, C)
+    for b_ in range(B):
+        for hk in range(Hk):
+            dQh = {ci: np.zeros((C, Dk)) for ci in range(len(chunks))}
+            dKh = {ci: np.zeros((C, Dk)) for ci in range(len(chunks))}
+            for hv in range(hk * grp, (hk + 1) * grp):
+                dH = np.zeros((Dk, Dv)) if dht is None else dht[b_, hv].T.copy()
+                for ci in reversed(range(len(chunks))):
+                    s, e = chunks[ci]
+                    K, Q = _pad(k[b_, s:e, hk], C), _pad(q[b_, s:e, hk], C)
+                    V, gg = _pad(v[b_, s:e, hv], C), _pad(g[b_, s:e, hv], C)
+                    bb, dO = _pad(beta[b_, s:e, hv], C), _pad(do[b_, s:e, hv], C)
+                    rk, rq = _norm_factor(K, norm), _norm_factor(Q, norm)
+                    ops = chunk_ops_channel(K, Q, V, gg, bb, scale, rk, rq)
+                    Kh, Qh = rk[:, None] * K, rq[:, None] * Q
+                    H0, dH1 = states[(b_, hv, ci)], dH
+                    Tm, W, Ut, P, Kbar = ops["T"], ops["W"], ops["Ut"], ops["P"], ops["Kbar"]
+                    a, Gam, bdec, GamC = ops["a"], ops["Gam"], ops["suf"], ops["GamC"]
+                    U = Ut - W @ H0
+                    dU = P.T @ dO + Kbar @ dH1
+                    dPs = scale * np.tril(dO @ U.T)
+                    X, Y = dO @ H0.T, U @ dH1.T
+                    dW = -dU @ H0.T
+                    Z = Tm.T @ dW
+                    dT = dU @ (bb[:, None] * V).T + dW @ (bb[:, None] * Kh * Gam).T
+                    TdU = Tm.T @ dU
+                    dA = np.tril(-Tm.T @ dT @ Tm.T, -1)
+                    X1, Y1, X2 = _blocked_contractions(dPs, dA, Kh, Qh, bb, a, bs)
+                    dQ = scale * Gam * X + X1
+                    dK = bdec * Y + bb[:, None] * Gam * Z + bb[:, None] * Y1 + X2
+                    dgam = (scale * Gam * Qh * X - bdec * Kh * Y + bb[:, None] * Gam * Kh * Z
+                            + Qh * X1 + bb[:, None] * Kh * Y1 - Kh * X2)
+                    dgamC = np.sum(bdec * Kh * Y, axis=0) + GamC * np.sum(dH1 * H0, axis=1)
+                    dgg = np.cumsum(dgam[::-1], axis=0)[::-1] + dgamC[None, :]
+                    n = e - s
+                    dv[b_, s:e, hv] = (bb[:, None] * TdU)[:n]
+                    dbeta[b_, s:e, hv] = (np.sum(V * TdU, axis=1) + np.sum(Gam * Kh * Z, axis=1)
+                                          + np.sum(Kh * Y1, axis=1))[:n]
+                    dg[b_, s:e, hv] = dgg[:n]
+                    dQh[ci] += dQ
+                    dKh[ci] += dK
+                    dH = GamC[:, None] * dH1 + ops["Mneg"].T @ dH1 + ops["Qc"].T @ dO
+                dh0[b_, hv] = dH.T
+            for ci, (s, e) in enumerate(chunks):
+                n = e - s
+                for X_, Dst, raw in ((dQh[ci], dq, q), (dKh[ci], dk, k)):
+                    x = raw[b_, s:e, hk]
+                    r = _norm_factor(x, norm)
+                    xh = r[:, None] * x
+                    Xn = X_[:n]
+                    if norm:
+                        Dst[b_, s:e, hk] = r[:, None] * (Xn - xh * np.sum(xh * Xn, axis=1, keepdims=True))
+                    else:
+                        Dst[b_, s:e, hk] = Xn
+    return dict(dq=dq, dk=dk, dv=dv, dg=dg, dbeta=dbeta, dh0=dh0)

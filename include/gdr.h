@@ -102,9 +102,10 @@ gdr_status gdr_fwd_sequential(const gdr_problem* p, const void* q, const void* k
  * dv, dg, dbeta and, if dh0 != NULL, dh0. h0 and dht may be NULL (zero). Recomputes the
  * chunk-local terms and the chunk-start states instead of reading saved activations;
  * the normalisation backward is done inside. Same support matrix as gdr_fwd_chunked; with the
- * per-channel gate dg is [B,T,Hv,Dk] (one gradient per key channel) and the decay-weighted
- * intra-chunk contractions run on the CUDA cores with running products of the per-token
- * factors (no decay can overflow), the dense products on the tensor cores.
+ * per-channel gate dg is [B,T,Hv,Dk] (one gradient per key channel); its decay-weighted
+ * intra-chunk contractions run by 16-token blocks, below the block diagonal on the tensor
+ * cores with operands scaled by products of per-token factors, inside the diagonal blocks
+ * with running products on the CUDA cores (no decay can overflow).
  * Deterministic: no floating-point atomics. */
 gdr_status gdr_bwd_chunked(const gdr_problem* p, const void* q, const void* k, const void* v,
                            const float* g, const float* beta, const float* h0, const void* do_,

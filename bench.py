@@ -58,6 +58,14 @@ KERNEL_TRAFFIC = {"chunk_prep": 1917, "chunk_scan_fwd": 2054, "chunk_scan_bwd": 
 STEP_FLOPS, STEP_BYTES = 655360 * UNITS, 2584 * UNITS
 
 
+def job_throughput(ms_local, tokens_per_rank, world, reduce_max=None):
+    """Whole-job tokens/s: every rank processes tokens_per_rank, the job runs at the pace of the
+    slowest rank (its step time, the max over ranks through reduce_max when world > 1).
+    Returns (tokens/s, the step time in ms)."""
+    ms = reduce_max(ms_local) if world > 1 else ms_local
+    return world * tokens_per_rank / (ms / 1e3), ms
+
+
 def set_tokens(n):
     global T, UNITS, STEP_FLOPS, STEP_BYTES
     T = n
@@ -299,11 +307,13 @@ def main():
     barrier()
     ms = e0.elapsed_time(e1) / args.steps
     clocks = clk.stop()
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
+
+    def max_over_ranks(v):
+        t = torch.tensor([v], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * B * T / (ms / 1e3)
+        return float(t.item())
+
+    value, ms = job_throughput(ms, B * T, world, max_over_ranks)
 
     # the full-recompute variant of the same step (context, not the headline)
     for _ in range(2):

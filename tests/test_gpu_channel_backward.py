@@ -133,3 +133,20 @@ def test_channel_autograd_runs_the_chunked_vjp():
     ref = oracle.backward(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"], x["do"], x["dht"])
     for n in ("q", "k", "v", "g", "beta", "h0"):
         assert rel_err(t[n].grad, ref["d" + n]) <= BF16_TOL, n
+
+
+def test_channel_autograd_keep_operators_uses_the_state_handoff():
+    """keep_operators=True asks for the operator handoff, which the per-channel gate does not
+    have: the function keeps the chunk-start states instead and the gradients are the same."""
+    dev = cuda_device()
+    x = make_inputs(Shape(1, 90, 1, 2, 128, 128), dtype=torch.bfloat16, seed=43, gate="channel", grads=True,
+                    gate_scale=0.3)
+    grads = []
+    for keep in (False, True):
+        t = {n: (None if v is None else v.to(dev).requires_grad_(True))
+             for n, v in x.items() if n not in ("do", "dht")}
+        o, ht = gated_delta_rule(t["q"], t["k"], t["v"], t["g"], t["beta"], t["h0"], keep_operators=keep)
+        ((o.float() * x["do"].to(dev).float()).sum() + (ht * x["dht"].to(dev)).sum()).backward()
+        grads.append({n: t[n].grad for n in ("q", "k", "v", "g", "beta", "h0")})
+    for n in grads[0]:
+        assert torch.equal(grads[0][n], grads[1][n]), n

@@ -576,7 +576,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1) grad_ch_contract_kernel(GradChA
                 Y1[8 * h + e] += av[e] * w;
             }
         }
-        if (h == 1) {  // j = r0 + 7 .. r0: E_rj = E_r,ra * prod_{j<t<=ra-1}... shared by the 8 rows
+        if (h == 1) {  // j = r0 + 7 .. r0: E_rj = E_r,ra * prod_{j<t<=ra} a_t, the second factor shared by the 8 rows
             float X1f[8], Y1f[8];
 #pragma unroll
             for (int e = 0; e < 8; e++) {
@@ -778,7 +778,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1) grad_ch_contract_kernel(GradChA
                 X2[8 * h + e] += (pv[e] * qi + av[e] * kbi) * E[e];
             }
         }
-        if (h == 0) {  // i = r0 + 8 .. r0 + 15: E_ij = E_ja+7,j * prod_{ja+7<t<=i} a_t shared by the 8 columns
+        if (h == 0) {  // i = r0 + 8 .. r0 + 15: E_ij = E_ja+7,j * prod_{ja+7<t<=i} a_t, the second factor shared by the 8 columns
             float X2f[8];
 #pragma unroll
             for (int e = 0; e < 8; e++) X2f[e] = 0.f;

@@ -193,3 +193,10 @@ def test_sequential_backward_validation(L):
     ptrs[6] = None  # do required
     assert L.gdr_bwd_sequential(ctypes.byref(p), *ptrs, FAKE, need, None) == INVALID
     assert L.gdr_bwd_sequential_workspace(ctypes.byref(prob(Dk=96))) == 0
+
+
+def test_wait_expiry_selftest_validation(L):
+    """The expiry self-test checks its workspace before any launch (null, too small, misaligned)."""
+    for ptr, n in ((None, 256), (FAKE, 255), (MISALIGNED, 256)):
+        assert L.gdr_selftest_wait_expiry(ptr, n, None) == INVALID
+    assert L.gdr_workspace_status(None, 256, None) == INVALID

@@ -12,7 +12,7 @@ kept for the backward — the point of "fold q/k L2-norm into the gated_delta_ru
 gated delta net" (MLX PR #4565).
 
 bf16 q/k/v with Dk = Dv = 128 run the chunked forward and the chunked VJP (scalar or
-per-channel gate; the operator handoff of ``keep_operators`` is for the scalar gate only);
+per-channel gate);
 every other problem (fp32, other head sizes) uses the token-by-token kernels
 (gdr_fwd_sequential / gdr_bwd_sequential), keeping h0 for the backward. The only torch operations here
 are argument marshalling: a zero ``do`` when the output is unused, contiguity, and casting
@@ -37,7 +37,7 @@ class GatedDeltaRuleFunction(torch.autograd.Function):
         ctx.scale, ctx.norm, ctx.has_h0 = scale, bool(use_qk_l2norm), h0 is not None
         fwd_chunk = _chunked_ok(q, v)
         ctx.bwd_chunk = fwd_chunk
-        ctx.keep_operators = bool(keep_operators) and ctx.bwd_chunk and g.dim() == 3
+        ctx.keep_operators = bool(keep_operators) and ctx.bwd_chunk
         kw = dict(scale=scale, use_qk_l2norm=use_qk_l2norm)
         fwd = fwd_chunked if fwd_chunk else fwd_sequential
         if any(ctx.needs_input_grad[:6]) and ctx.bwd_chunk:

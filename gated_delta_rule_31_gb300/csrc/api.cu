@@ -62,11 +62,9 @@ gdr_status check_ptrs(const gdr_problem* p, std::initializer_list<const void*> r
     return GDR_OK;
 }
 
-// The tensor-core chunked path: bf16, Dk = Dv = 128; the per-channel gate everywhere except
-// the saved-operator handoff.
-gdr_status check_chunked_support(const gdr_problem* p, bool channel_ok = false) {
+// The tensor-core chunked path: bf16, Dk = Dv = 128; scalar or per-channel gate.
+gdr_status check_chunked_support(const gdr_problem* p) {
     if (p->dtype != GDR_BF16 || p->Dk != 128 || p->Dv != 128) return GDR_ERR_UNSUPPORTED;
-    if (p->gate != GDR_GATE_SCALAR && !(channel_ok && p->gate == GDR_GATE_CHANNEL)) return GDR_ERR_UNSUPPORTED;
     return GDR_OK;
 }
 
@@ -165,12 +163,12 @@ const char* gdr_status_string(gdr_status s) {
 }
 
 size_t gdr_fwd_chunked_workspace(const gdr_problem* p) {
-    if (check_problem(p, false) != GDR_OK || check_chunked_support(p, true) != GDR_OK) return 0;
+    if (check_problem(p, false) != GDR_OK || check_chunked_support(p) != GDR_OK) return 0;
     return chunk_fwd_workspace(chunk_problem(p));
 }
 
 size_t gdr_bwd_chunked_workspace(const gdr_problem* p) {
-    if (check_problem(p, false) != GDR_OK || check_chunked_support(p, true) != GDR_OK) return 0;
+    if (check_problem(p, false) != GDR_OK || check_chunked_support(p) != GDR_OK) return 0;
     return chunk_bwd_workspace(chunk_problem(p));
 }
 
@@ -195,12 +193,12 @@ gdr_status gdr_decode_step(const gdr_problem* p, const void* q, const void* k, c
 }
 
 size_t gdr_chunk_states_bytes(const gdr_problem* p) {
-    if (check_problem(p, false) != GDR_OK || check_chunked_support(p, true) != GDR_OK) return 0;
+    if (check_problem(p, false) != GDR_OK || check_chunked_support(p) != GDR_OK) return 0;
     return chunk_states_bytes(chunk_problem(p));
 }
 
 size_t gdr_bwd_chunked_states_workspace(const gdr_problem* p) {
-    if (check_problem(p, false) != GDR_OK || check_chunked_support(p, true) != GDR_OK) return 0;
+    if (check_problem(p, false) != GDR_OK || check_chunked_support(p) != GDR_OK) return 0;
     return chunk_bwd_states_workspace(chunk_problem(p));
 }
 
@@ -214,7 +212,7 @@ gdr_status gdr_fwd_chunked_states(const gdr_problem* p, const void* q, const voi
                                   gdr_stream_t stream) {
     gdr_status s = check_problem(p, false);
     if (s != GDR_OK) return s;
-    if ((s = check_chunked_support(p, true)) != GDR_OK) return s;
+    if ((s = check_chunked_support(p)) != GDR_OK) return s;
     const size_t need = chunk_states_bytes(chunk_problem(p));
     if (need && (!states || states_bytes < need)) return GDR_ERR_WORKSPACE;
     if (states && (reinterpret_cast<uintptr_t>(states) & 255u) != 0) return GDR_ERR_INVALID_ARG;
@@ -260,7 +258,7 @@ static gdr_status fwd_chunked_impl(const gdr_problem* p, const void* q, const vo
     gdr_status s = check_problem(p, false);
     if (s != GDR_OK) return s;
     if ((s = check_ptrs(p, {q, k, v, g, beta, o}, {h0, ht})) != GDR_OK) return s;
-    if ((s = check_chunked_support(p, !saved)) != GDR_OK) return s;
+    if ((s = check_chunked_support(p)) != GDR_OK) return s;
     const size_t need = saved ? kSavedFwdWorkspace : chunk_fwd_workspace(chunk_problem(p));
     if (!ws || ws_bytes < need) return GDR_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return GDR_ERR_INVALID_ARG;
@@ -301,7 +299,7 @@ gdr_status gdr_bwd_chunked_states(const gdr_problem* p, const void* q, const voi
                                   float* dbeta, float* dh0, void* ws, size_t ws_bytes, gdr_stream_t stream) {
     gdr_status s = check_problem(p, false);
     if (s != GDR_OK) return s;
-    if ((s = check_chunked_support(p, true)) != GDR_OK) return s;
+    if ((s = check_chunked_support(p)) != GDR_OK) return s;
     const size_t need = chunk_states_bytes(chunk_problem(p));
     if (need && (!states || states_bytes < need)) return GDR_ERR_WORKSPACE;
     if (states && (reinterpret_cast<uintptr_t>(states) & 255u) != 0) return GDR_ERR_INVALID_ARG;
@@ -331,7 +329,7 @@ static gdr_status bwd_chunked_impl(const gdr_problem* p, const void* q, const vo
     gdr_status s = check_problem(p, false);
     if (s != GDR_OK) return s;
     if ((s = check_ptrs(p, {q, k, v, g, beta, do_, dq, dk, dv, dg, dbeta}, {h0, dht, dh0})) != GDR_OK) return s;
-    if ((s = check_chunked_support(p, !saved)) != GDR_OK) return s;
+    if ((s = check_chunked_support(p)) != GDR_OK) return s;
     const ChunkProblem cp = chunk_problem(p);
     const size_t need = saved    ? chunk_bwd_saved_workspace(cp)
                         : states ? chunk_bwd_states_workspace(cp)

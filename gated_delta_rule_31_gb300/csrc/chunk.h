@@ -110,19 +110,37 @@ inline SavedLayout saved_layout(const ChunkProblem& p) {
     SavedLayout l;
     l.ncpad = (int)round_up((size_t)p.NC, 4);
     const size_t nh = (size_t)p.B * p.Hv;
+    const size_t ngam = p.channel ? (size_t)p.NC * kD : (size_t)l.ncpad;  // Gamma_C per chunk (per channel)
     l.gam = 0;
-    l.rec = round_up(nh * l.ncpad * sizeof(float), 1024);
+    l.rec = round_up(nh * ngam * sizeof(float), 1024);
     l.rec2 = l.rec + nh * p.NC * (size_t)REC_BYTES;
-    l.hs = l.rec2 + nh * p.NC * (size_t)REC2_BYTES;
+    l.hs = l.rec2 + nh * p.NC * (size_t)(p.channel ? REC2_BYTES_CH : REC2_BYTES);
     l.total = l.hs + nh * p.NC * (size_t)STATE_IMG;
     return l;
 }
 inline size_t chunk_saved_bytes(const ChunkProblem& p) { return saved_layout(p).total; }
 constexpr size_t kSavedFwdWorkspace = 256;  // status word only
-constexpr size_t kSavedBwdDhs = 1024;       // offset of the state gradients in the backward workspace
-inline size_t chunk_bwd_saved_workspace(const ChunkProblem& p) {
-    return kSavedBwdDhs + (size_t)p.B * p.Hv * p.NC * STATE_IMG;
+// The backward's own workspace next to a saved buffer: the status word, the chunk-end state
+// gradients and, with a per-channel gate, the exports and per-value-head dq^, dk^.
+struct SavedBwdLayout {
+    size_t dhs, chx, dqh, dkh, total;
+};
+inline SavedBwdLayout saved_bwd_layout(const ChunkProblem& p) {
+    SavedBwdLayout l;
+    const size_t nh = (size_t)p.B * p.Hv;
+    l.dhs = 1024;
+    l.total = l.dhs + nh * p.NC * (size_t)STATE_IMG;
+    l.chx = l.dqh = l.dkh = 0;
+    if (p.channel) {
+        const size_t plane = round_up((size_t)p.B * p.T * p.Hv * kD * sizeof(float), 1024);
+        l.chx = l.total;
+        l.dqh = l.chx + nh * p.NC * (size_t)CHX_BYTES;
+        l.dkh = l.dqh + plane;
+        l.total = l.dkh + plane;
+    }
+    return l;
 }
+inline size_t chunk_bwd_saved_workspace(const ChunkProblem& p) { return saved_bwd_layout(p).total; }
 
 struct ChunkFwdArgs {
     ChunkProblem p;

@@ -840,7 +840,8 @@ cudaError_t launch_chunk_bwd(const ChunkBwdArgs& a, cudaStream_t s) {
         if ((e = p.channel ? launch_prep_ch(pa, mq, mk, mv, s) : launch_prep(pa, mq, mk, mv, s)) != cudaSuccess)
             return e;
     }
-    uint8_t* dhs = keep ? ws + kSavedBwdDhs : ws + w.dhs;
+    const SavedBwdLayout sl = saved_bwd_layout(p);
+    uint8_t* dhs = keep ? ws + sl.dhs : ws + w.dhs;
     ScanArgs sa;
     sa.p = p;
     sa.gam = pa.gam;
@@ -868,9 +869,9 @@ cudaError_t launch_chunk_bwd(const ChunkBwdArgs& a, cudaStream_t s) {
         ca.rec2 = pa.rec2;
         ca.hs = hs;
         ca.dhs = dhs;
-        ca.chx = ws + w.chx;
-        ca.dqh = reinterpret_cast<float*>(ws + w.dqh);
-        ca.dkh = reinterpret_cast<float*>(ws + w.dkh);
+        ca.chx = ws + (keep ? sl.chx : w.chx);
+        ca.dqh = reinterpret_cast<float*>(ws + (keep ? sl.dqh : w.dqh));
+        ca.dkh = reinterpret_cast<float*>(ws + (keep ? sl.dkh : w.dkh));
         ca.dq = a.dq;
         ca.dk = a.dk;
         ca.dv = a.dv;

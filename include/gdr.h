@@ -161,9 +161,9 @@ gdr_status gdr_bwd_chunked_states(const gdr_problem* p, const void* q, const voi
  * bitwise identical to gdr_fwd_chunked / gdr_bwd_chunked. The buffer must not be modified
  * between the two calls, and the backward must get the same q, k, v, g, beta and problem.
  * Workspaces: gdr_fwd_chunked_saved_workspace() (the status word only) and
- * gdr_bwd_chunked_saved_workspace(). Same support matrix as gdr_bwd_chunked but for the
- * scalar gate only (GDR_ERR_UNSUPPORTED for the per-channel gate); the size queries return 0
- * for an invalid or unsupported problem. Errors as gdr_fwd_chunked, plus
+ * gdr_bwd_chunked_saved_workspace(). Same support matrix as gdr_bwd_chunked (with the
+ * per-channel gate the saved T/W record also holds K^ .* Gamma, 160 KB per (b, hv, chunk));
+ * the size queries return 0 for an invalid or unsupported problem. Errors as gdr_fwd_chunked, plus
  * GDR_ERR_WORKSPACE if `saved` is NULL or smaller than required. */
 size_t gdr_chunk_saved_bytes(const gdr_problem* p);
 size_t gdr_fwd_chunked_saved_workspace(const gdr_problem* p);

@@ -89,18 +89,18 @@ def test_chunked_support_matrix_and_workspace(L):
         assert L.gdr_fwd_chunked_workspace(ctypes.byref(p)) == 0
         assert L.gdr_fwd_chunked(ctypes.byref(p), *[FAKE] * 8, FAKE, 1 << 30, None) == UNSUPPORTED
         assert L.gdr_bwd_chunked(ctypes.byref(p), *[FAKE] * 14, FAKE, 1 << 30, None) == UNSUPPORTED
-    # per-channel gate: chunked forward, state handoff and VJP (Gamma_C per key channel, 16 KB more
-    # of T/W/K.*Gamma per chunk and the backward's per-channel exports: larger workspaces); the
-    # operator handoff stays scalar-only
+    # per-channel gate: chunked forward, both handoffs and the VJP (Gamma_C per key channel, 16 KB
+    # more of T/W/K.*Gamma per chunk and the backward's per-channel exports: larger buffers)
     pc, ps = prob(gate=1), prob()
     assert L.gdr_fwd_chunked_workspace(ctypes.byref(pc)) > L.gdr_fwd_chunked_workspace(ctypes.byref(ps))
     assert L.gdr_bwd_chunked_workspace(ctypes.byref(pc)) > L.gdr_bwd_chunked_workspace(ctypes.byref(ps))
     assert L.gdr_bwd_chunked_states_workspace(ctypes.byref(pc)) > L.gdr_bwd_chunked_states_workspace(ctypes.byref(ps))
     assert L.gdr_chunk_states_bytes(ctypes.byref(pc)) == L.gdr_chunk_states_bytes(ctypes.byref(ps)) > 0
-    assert L.gdr_chunk_saved_bytes(ctypes.byref(pc)) == 0
-    assert L.gdr_fwd_chunked_saved(ctypes.byref(pc), *[FAKE] * 8, FAKE, 1 << 30, FAKE, 1 << 30, None) == UNSUPPORTED
-    args = [FAKE] * 5 + [FAKE, 1 << 30] + [FAKE] * 8
-    assert L.gdr_bwd_chunked_saved(ctypes.byref(pc), *args, FAKE, 1 << 30, None) == UNSUPPORTED
+    sbc, sbs = L.gdr_chunk_saved_bytes(ctypes.byref(pc)), L.gdr_chunk_saved_bytes(ctypes.byref(ps))
+    # header (Gamma_C per chunk and key channel) + (88 KB record + 40 KB T/W/K.*Gamma + 32 KB state)
+    assert sbc == 2048 + 4 * (90112 + 40960 + 32768) and sbs == 1024 + 4 * (90112 + 24576 + 32768)
+    assert L.gdr_bwd_chunked_saved_workspace(ctypes.byref(pc)) > L.gdr_bwd_chunked_saved_workspace(ctypes.byref(ps))
+    assert L.gdr_fwd_chunked_saved(ctypes.byref(pc), *[FAKE] * 8, FAKE, sbc - 1, FAKE, 256, None) == WORKSPACE
     nb = L.gdr_bwd_chunked_workspace(ctypes.byref(pc))
     assert L.gdr_bwd_chunked(ctypes.byref(pc), *[FAKE] * 14, FAKE, nb - 1, None) == WORKSPACE
     p = prob()

@@ -108,12 +108,21 @@ def test_channel_state_handoff_matches_recompute(shape):
     check(gb, x)
 
 
-def test_channel_saved_operator_handoff_is_unsupported():
+@pytest.mark.parametrize("shape", [Shape(1, 300, 2, 4, 128, 128), Shape(2, 129, 1, 2, 128, 128)])
+def test_channel_saved_operator_handoff_matches_recompute(shape):
+    """The forward can keep every chunk operator (with K^ .* Gamma for dT) and state: outputs and all
+    gradients are bitwise those of the recompute path."""
     dev = cuda_device()
-    x = make_inputs(Shape(1, 64, 1, 2, 128, 128), dtype=torch.bfloat16, seed=1, gate="channel")
+    x = make_inputs(shape, dtype=torch.bfloat16, seed=shape.T + 1, gate="channel", grads=True, gate_scale=0.5)
     d = to_dev(x, dev)
-    with pytest.raises(gdr.GdrError):
-        gdr.fwd_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], save_all=True)
+    o1, h1 = gdr.fwd_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"])
+    o2, h2, saved = gdr.fwd_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], save_all=True)
+    assert torch.equal(o1, o2) and torch.equal(h1, h2)
+    ga = gdr.bwd_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], d["do"], d["dht"])
+    gb = gdr.bwd_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], None, d["do"], d["dht"], saved=saved)
+    for n in NAMES:
+        assert torch.equal(ga[n], gb[n]), n
+    check(gb, x)
 
 
 def test_channel_autograd_runs_the_chunked_vjp():
@@ -135,9 +144,9 @@ def test_channel_autograd_runs_the_chunked_vjp():
         assert rel_err(t[n].grad, ref["d" + n]) <= BF16_TOL, n
 
 
-def test_channel_autograd_keep_operators_uses_the_state_handoff():
-    """keep_operators=True asks for the operator handoff, which the per-channel gate does not
-    have: the function keeps the chunk-start states instead and the gradients are the same."""
+def test_channel_autograd_keep_operators_matches_the_state_handoff():
+    """keep_operators=True (the operator handoff) and the default state handoff give the same
+    gradients with a per-channel gate."""
     dev = cuda_device()
     x = make_inputs(Shape(1, 90, 1, 2, 128, 128), dtype=torch.bfloat16, seed=43, gate="channel", grads=True,
                     gate_scale=0.3)

@@ -520,13 +520,23 @@ __global__ void __launch_bounds__(CH_THREADS, 1) grad_ch_contract_kernel(GradChA
             st_chunk(sb + X_AR + sw128_chunk(row, ch, 128), x, 1.f);
         }
         const int d2 = tid & 127, I = tid >> 7;  // R_I rows j = 16 I - 1 .. 0 of channel d2
-        if (I >= 1) {
+        if (I >= 1) {  // 16 rows' inputs loaded before their stores
             const uint32_t rb = I == 1 ? X_R1 : I == 2 ? X_R2 : X_R3;
             float sfx = 1.f;
-            for (int j = 16 * I - 1; j >= 0; j--) {
-                *reinterpret_cast<__nv_bfloat16*>(sm + rb + sw128_off(j, d2, 16 * I)) =
-                    __float2bfloat16_rn(KH[j * kD + d2] * sfx);
-                sfx *= AL[j * kD + d2];
+#pragma unroll 1
+            for (int jb = 16 * I - 16; jb >= 0; jb -= 16) {
+                float av[16], kv[16];
+#pragma unroll
+                for (int i = 0; i < 16; i++) {
+                    av[i] = AL[(jb + i) * kD + d2];
+                    kv[i] = KH[(jb + i) * kD + d2];
+                }
+#pragma unroll
+                for (int i = 15; i >= 0; i--) {
+                    *reinterpret_cast<__nv_bfloat16*>(sm + rb + sw128_off(jb + i, d2, 16 * I)) =
+                        __float2bfloat16_rn(kv[i] * sfx);
+                    sfx *= av[i];
+                }
             }
         }
     }
@@ -725,13 +735,24 @@ __global__ void __launch_bounds__(CH_THREADS, 1) grad_ch_contract_kernel(GradChA
             const int n = 48 - 16 * J;
             const uint32_t bb = J == 0 ? X_B0 : J == 1 ? X_B1 : X_B2;
             float pr = 1.f;
-            for (int i = 16 * J + 16; i < kChunk; i++) {
-                pr *= AL[i * kD + d2];
-                const int row = i - 16 * J - 16;
-                *reinterpret_cast<__nv_bfloat16*>(sm + bb + sw128_off(row, d2, 2 * n)) =
-                    __float2bfloat16_rn(QH[i * kD + d2] * pr);
-                *reinterpret_cast<__nv_bfloat16*>(sm + bb + sw128_off(n + row, d2, 2 * n)) =
-                    __float2bfloat16_rn(bet[i] * KH[i * kD + d2] * pr);
+#pragma unroll 1
+            for (int ib = 16 * J + 16; ib < kChunk; ib += 16) {  // 16 rows' inputs loaded before their stores
+                float av[16], qv[16], kv[16];
+#pragma unroll
+                for (int e = 0; e < 16; e++) {
+                    av[e] = AL[(ib + e) * kD + d2];
+                    qv[e] = QH[(ib + e) * kD + d2];
+                    kv[e] = bet[ib + e] * KH[(ib + e) * kD + d2];
+                }
+#pragma unroll
+                for (int e = 0; e < 16; e++) {
+                    pr *= av[e];
+                    const int row = ib + e - 16 * J - 16;
+                    *reinterpret_cast<__nv_bfloat16*>(sm + bb + sw128_off(row, d2, 2 * n)) =
+                        __float2bfloat16_rn(qv[e] * pr);
+                    *reinterpret_cast<__nv_bfloat16*>(sm + bb + sw128_off(n + row, d2, 2 * n)) =
+                        __float2bfloat16_rn(kv[e] * pr);
+                }
             }
         }
     }

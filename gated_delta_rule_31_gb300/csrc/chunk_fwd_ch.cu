@@ -113,11 +113,18 @@ __global__ void __launch_bounds__(PCH_THREADS, 1)
     }
     ok = mbar_wait(&bar_tma, 0, &abort_sh, a.status, 15);
     if (__syncthreads_or(!ok)) goto teardown;
-    if (tid < 128) {  // Gamma_r, channel d = tid: running product over the chunk's tokens
-        float p = 1.f;
-        for (int t = 0; t < kChunk; t++) {
-            p *= al[t * kD + tid];
-            gp[t * kD + tid] = p;
+    if (tid < 128) {  // Gamma_r, channel d = tid: running product over the chunk's tokens,
+        float p = 1.f;  // 16 tokens' factors loaded before their products are stored
+#pragma unroll 1
+        for (int t0b = 0; t0b < kChunk; t0b += 16) {
+            float x[16];
+#pragma unroll
+            for (int i = 0; i < 16; i++) x[i] = al[(t0b + i) * kD + tid];
+#pragma unroll
+            for (int i = 0; i < 16; i++) {
+                p *= x[i];
+                gp[(t0b + i) * kD + tid] = p;
+            }
         }
     } else if (tid < 256) {  // L2 norm factors: row tid-128 of the [k; q] tile (read order rotated by the row)
         const int row = tid - 128;
@@ -149,22 +156,42 @@ __global__ void __launch_bounds__(PCH_THREADS, 1)
     {
         const int d = tid & 127, blk = tid >> 7;  // channel d, block blk
         const __nv_bfloat16* kqs = reinterpret_cast<const __nv_bfloat16*>(sm + CS_KQ);
-        float p = blk ? 1.f : 0.f;
-        for (int i = 0; i < 16; i++) {  // L rows of block blk (k rows r, q rows 64 + r)
-            const int r = 16 * blk + i;
-            p *= al[r * kD + d];
-            const float kv = __bfloat162float(kqs[sw128_off(r, d, 128) >> 1]);
-            const float qv = __bfloat162float(kqs[sw128_off(64 + r, d, 128) >> 1]);
-            *reinterpret_cast<__nv_bfloat16*>(sm + CS_L + sw128_off(r, d, 128)) = __float2bfloat16_rn(kv * p);
-            *reinterpret_cast<__nv_bfloat16*>(sm + CS_L + sw128_off(64 + r, d, 128)) = __float2bfloat16_rn(qv * p);
+        {  // L rows of block blk (k rows r, q rows 64 + r); all loads before the stores
+            float av[16], kv[16], qv[16];
+#pragma unroll
+            for (int i = 0; i < 16; i++) {
+                const int r = 16 * blk + i;
+                av[i] = al[r * kD + d];
+                kv[i] = __bfloat162float(kqs[sw128_off(r, d, 128) >> 1]);
+                qv[i] = __bfloat162float(kqs[sw128_off(64 + r, d, 128) >> 1]);
+            }
+            float p = blk ? 1.f : 0.f;
+#pragma unroll
+            for (int i = 0; i < 16; i++) {
+                const int r = 16 * blk + i;
+                p *= av[i];
+                *reinterpret_cast<__nv_bfloat16*>(sm + CS_L + sw128_off(r, d, 128)) = __float2bfloat16_rn(kv[i] * p);
+                *reinterpret_cast<__nv_bfloat16*>(sm + CS_L + sw128_off(64 + r, d, 128)) =
+                    __float2bfloat16_rn(qv[i] * p);
+            }
         }
-        if (blk) {  // R_blk: rows j = 16 blk - 1 .. 0
+        if (blk) {  // R_blk: rows j = 16 blk - 1 .. 0, 16 rows' inputs loaded before their stores
             const uint32_t rb = blk == 1 ? CS_R1 : blk == 2 ? CS_R2 : CS_R3;
             float sfx = 1.f;
-            for (int j = 16 * blk - 1; j >= 0; j--) {
-                const float kv = __bfloat162float(kqs[sw128_off(j, d, 128) >> 1]);
-                *reinterpret_cast<__nv_bfloat16*>(sm + rb + sw128_off(j, d, 16 * blk)) = __float2bfloat16_rn(kv * sfx);
-                sfx *= al[j * kD + d];
+#pragma unroll 1
+            for (int jb = 16 * blk - 16; jb >= 0; jb -= 16) {
+                float av[16], kv[16];
+#pragma unroll
+                for (int i = 0; i < 16; i++) {
+                    av[i] = al[(jb + i) * kD + d];
+                    kv[i] = __bfloat162float(kqs[sw128_off(jb + i, d, 128) >> 1]);
+                }
+#pragma unroll
+                for (int i = 15; i >= 0; i--) {
+                    *reinterpret_cast<__nv_bfloat16*>(sm + rb + sw128_off(jb + i, d, 16 * blk)) =
+                        __float2bfloat16_rn(kv[i] * sfx);
+                    sfx *= av[i];
+                }
             }
         }
     }
@@ -285,12 +312,18 @@ __global__ void __launch_bounds__(PCH_THREADS, 1)
         v_pend = true;
     }
     __syncthreads();
-    if (tid < 128) {  // prod_{t>r} a_t, channel d = tid, in place of a_t (read before written)
+    if (tid < 128) {  // prod_{t>r} a_t, channel d = tid, in place of a_t (16 tokens read before written)
         float p = 1.f;
-        for (int t = kChunk - 1; t >= 0; t--) {
-            const float at = al[t * kD + tid];
-            al[t * kD + tid] = p;
-            p *= at;
+#pragma unroll 1
+        for (int t0b = kChunk - 16; t0b >= 0; t0b -= 16) {
+            float x[16];
+#pragma unroll
+            for (int i = 0; i < 16; i++) x[i] = al[(t0b + i) * kD + tid];
+#pragma unroll
+            for (int i = 15; i >= 0; i--) {
+                al[(t0b + i) * kD + tid] = p;
+                p *= x[i];
+            }
         }
         a.gam[(bh * P.NC + c) * kD + tid] = gp[(kChunk - 1) * kD + tid];  // Gamma_C per channel
     }

@@ -448,6 +448,14 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
                 const int jc = 2 * qt + (lane >> 4);  // this lane's 8-column chunk of the row
                 float pr[8];
                 ldrow8(G_P, r, jc, 64, pr);
+                // gam, rk of the chunk's 8 columns before the first store (see the prep epilogues)
+                const float4 ga0 = *reinterpret_cast<const float4*>(gam + 8 * jc);
+                const float4 ga1 = *reinterpret_cast<const float4*>(gam + 8 * jc + 4);
+                const float4 rk0 = *reinterpret_cast<const float4*>(rk + 8 * jc);
+                const float4 rk1 = *reinterpret_cast<const float4*>(rk + 8 * jc + 4);
+                const float gj[8] = {ga0.x, ga0.y, ga0.z, ga0.w, ga1.x, ga1.y, ga1.z, ga1.w};
+                const float rkj[8] = {rk0.x, rk0.y, rk0.z, rk0.w, rk1.x, rk1.y, rk1.z, rk1.w};
+                const float rqr = rq[r];
                 float zs = 0.f;
                 float sk[8], sq[8];
 #pragma unroll
@@ -456,9 +464,9 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
                     const float z = w[e] * pr[e];
                     zs += z;
                     ZS[fsw(r, j)] = z;
-                    const float ds = (j <= r) ? P.scale * __expf(gr - gam[j]) * w[e] : 0.f;
-                    sk[e] = ds * rk[j];
-                    sq[e] = ds * rq[r];
+                    const float ds = (j <= r) ? P.scale * __expf(gr - gj[e]) * w[e] : 0.f;
+                    sk[e] = ds * rkj[e];
+                    sq[e] = ds * rqr;
                 }
                 zs += __shfl_xor_sync(0xffffffffu, zs, 16);
                 if (act) dgp[qt * 64 + r] += zs;
@@ -655,6 +663,16 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
             {
                 const int jc = 2 * qt + (lane >> 4);
                 const float gr = gam[r], br = bet[r], rkr = rk[r];
+                // every shared-memory input of the 8 columns before the first store
+                const float4 ga0 = *reinterpret_cast<const float4*>(gam + 8 * jc);
+                const float4 ga1 = *reinterpret_cast<const float4*>(gam + 8 * jc + 4);
+                const float4 rk0 = *reinterpret_cast<const float4*>(rk + 8 * jc);
+                const float4 rk1 = *reinterpret_cast<const float4*>(rk + 8 * jc + 4);
+                const float gj[8] = {ga0.x, ga0.y, ga0.z, ga0.w, ga1.x, ga1.y, ga1.z, ga1.w};
+                const float rkj[8] = {rk0.x, rk0.y, rk0.z, rk0.w, rk1.x, rk1.y, rk1.z, rk1.w};
+                float gf[8];
+#pragma unroll
+                for (int e = 0; e < 8; e++) gf[e] = GF[fsw(r, 8 * jc + e)];
                 float db = 0.f, zs = 0.f;
 #pragma unroll
                 for (int e = 0; e < 8; e++) {
@@ -662,8 +680,8 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
                     float m = 0.f, z = 0.f;
                     if (j < r) {
                         const float dA = -w[e];
-                        const float E = __expf(gr - gam[j]);
-                        const float kk = rkr * rk[j] * GF[fsw(r, j)];
+                        const float E = __expf(gr - gj[e]);
+                        const float kk = rkr * rkj[e] * gf[e];
                         db += dA * E * kk;
                         z = dA * br * E * kk;
                         m = dA * br * E;

@@ -321,17 +321,19 @@ __global__ void __launch_bounds__(256, 2)
                 // Kbar = diag(exp(gamma_C - gamma) rho_k) K, straight to the record
                 {
                     uint4 kv[4];
+                    float fr[4];
 #pragma unroll
                     for (int n = 0; n < 4; n++) {
                         const int idx = tid + 256 * n, r = idx >> 4, j = idx & 15;
                         kv[n] = ld_shared_v4(sb + PS_KQ + sw128_chunk(r, j, 128));
+                        fr[n] = fb[r];
                     }
 #pragma unroll
                     for (int n = 0; n < 4; n++) {
                         const int idx = tid + 256 * n, r = idx >> 4, j = idx & 15;
                         float x[8];
                         unpack8(kv[n], x);
-                        st_global16(rec + REC_K + sw128_chunk(r, j, 64), pack8(x, fb[r]));
+                        st_global16(rec + REC_K + sw128_chunk(r, j, 64), pack8(x, fr[n]));
                     }
                 }
             }

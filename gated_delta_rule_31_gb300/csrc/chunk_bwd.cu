@@ -23,6 +23,7 @@
 #include <string.h>
 
 #include "chunk.h"
+#include "chunk_dev.cuh"
 #include "common.cuh"
 #include "kernels.h"
 #include "tma_host.h"
@@ -59,39 +60,9 @@ struct GradArgs {
     int* status;
 };
 
-__device__ __forceinline__ void unpack8b(const uint4& u, float* x) {
-    x[0] = bf16lo(u.x); x[1] = bf16hi(u.x); x[2] = bf16lo(u.y); x[3] = bf16hi(u.y);
-    x[4] = bf16lo(u.z); x[5] = bf16hi(u.z); x[6] = bf16lo(u.w); x[7] = bf16hi(u.w);
-}
-__device__ __forceinline__ void st_chunk8(uint32_t addr, const float* x, float s) {
-    st_shared_v4(addr, pack_bf16(s * x[0], s * x[1]), pack_bf16(s * x[2], s * x[3]), pack_bf16(s * x[4], s * x[5]),
-                 pack_bf16(s * x[6], s * x[7]));
-}
 // fp32 [64][64] scratch element (r, j), columns XOR-swizzled by the row so that a warp
 // touching one column across rows (or one row across columns) hits distinct banks
 __device__ __forceinline__ int fsw(int r, int j) { return r * 64 + (j ^ (r & 31)); }
-// An M=64 accumulator row lives in lane l < 16 of its warp; lanes l and l + 16 split its 16
-// columns: lane l keeps columns 0-7, lane l + 16 takes 8-15 (returned in w[0..7]).
-__device__ __forceinline__ void split16(const float* v, float* w, int lane) {
-#pragma unroll
-    for (int e = 0; e < 8; e++) {
-        const float hi = __shfl_sync(0xffffffffu, v[8 + e], lane & 15);
-        w[e] = (lane >> 4) ? hi : v[e];
-    }
-}
-// The same for 32 columns: lane l keeps 0-15, lane l + 16 takes 16-31 (returned in w[0..15]).
-__device__ __forceinline__ void split32(const float* v, float* w, int lane) {
-#pragma unroll
-    for (int e = 0; e < 16; e++) {
-        const float hi = __shfl_sync(0xffffffffu, v[16 + e], lane & 15);
-        w[e] = (lane >> 4) ? hi : v[e];
-    }
-}
-// 64 consecutive fp32 columns of this warp's 32 TMEM lanes
-__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
-    tmem_ld32(taddr, v);
-    tmem_ld32(taddr + 32, v + 32);
-}
 
 // 16 warps: warp w reads TMEM lane group (w & 3) (M=64 accumulator rows 16*(w&3) .. +15 in
 // lanes 0-15) and column quarter (w >> 2) of every product.
@@ -178,7 +149,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
     };
     // 8 bf16 of row `row` of a panelised tile, logical chunk j
     auto ldrow8 = [&](uint32_t tile, int row, int j, int R, float* x) {
-        unpack8b(ld_shared_v4(sb + tile + sw128_chunk(row, j, R)), x);
+        unpack8(ld_shared_v4(sb + tile + sw128_chunk(row, j, R)), x);
     };
     const uint32_t id64x128_kk = idesc_bf16(64, 128, 0, 0), id64x128_km = idesc_bf16(64, 128, 0, 1),
                    id64x128_mm = idesc_bf16(64, 128, 1, 1), id64x64_kk = idesc_bf16(64, 64, 0, 0),
@@ -367,8 +338,8 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
 #pragma unroll
             for (int i = tid; i < 2048; i += GRAD_THREADS) {
                 float x[8], y[8];
-                unpack8b(ld_shared_v4(sb + G_H0 + i * 16), x);
-                unpack8b(ld_shared_v4(sb + G_DH + i * 16), y);
+                unpack8(ld_shared_v4(sb + G_H0 + i * 16), x);
+                unpack8(ld_shared_v4(sb + G_DH + i * 16), y);
 #pragma unroll
                 for (int e = 0; e < 8; e++) s += x[e] * y[e];
             }
@@ -390,20 +361,20 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
             const int q0 = 4 * qt + 2 * (lane >> 4);  // this lane's two 8-column chunks
             tmem_ld32(tl + TM_T1 + c32, x);
             tmem_wait_ld();
-            split32(x, w, lane);
+            split_cols<32>(x, w, lane);
 #pragma unroll
             for (int q = 0; q < 2; q++) {
                 float ut[8];
-                unpack8b(utv[q], ut);
+                unpack8(utv[q], ut);
 #pragma unroll
                 for (int e = 0; e < 8; e++) ut[e] -= w[8 * q + e];
-                st_chunk8(sb + G_W + sw128_chunk(r, q0 + q, 64), ut, 1.f);
+                st_chunk(sb + G_W + sw128_chunk(r, q0 + q, 64), ut, 1.f);
             }
             tmem_ld32(tl + TM_T2 + c32, x);
             tmem_wait_ld();
-            split32(x, w, lane);
+            split_cols<32>(x, w, lane);
 #pragma unroll
-            for (int q = 0; q < 2; q++) st_chunk8(sb + G_KB + sw128_chunk(r, q0 + q, 64), w + 8 * q, 1.f);
+            for (int q = 0; q < 2; q++) st_chunk(sb + G_KB + sw128_chunk(r, q0 + q, 64), w + 8 * q, 1.f);
         }
         sync_for_mma();
 
@@ -444,7 +415,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
                 float v[16], w[8];
                 tmem_ld16(tl + TM_T2 + c16, v);
                 tmem_wait_ld();
-                split16(v, w, lane);
+                split_cols<16>(v, w, lane);
                 const int jc = 2 * qt + (lane >> 4);  // this lane's 8-column chunk of the row
                 float pr[8];
                 ldrow8(G_P, r, jc, 64, pr);
@@ -470,8 +441,8 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
                 }
                 zs += __shfl_xor_sync(0xffffffffu, zs, 16);
                 if (act) dgp[qt * 64 + r] += zs;
-                st_chunk8(sb + G_P + sw128_chunk(r, jc, 64), sk, 1.f);
-                st_chunk8(sb + G_DO + sw128_chunk(r, jc, 64), sq, 1.f);
+                st_chunk(sb + G_P + sw128_chunk(r, jc, 64), sk, 1.f);
+                st_chunk(sb + G_DO + sw128_chunk(r, jc, 64), sq, 1.f);
             }
             tmem_wait_st();
         }
@@ -531,7 +502,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
                 tmem_wait_ld();
                 if (act) {
 #pragma unroll
-                    for (int q = 0; q < 4; q++) st_chunk8(sb + G_H0 + sw128_chunk(r, 4 * qt + q, 64), x + 8 * q, -1.f);
+                    for (int q = 0; q < 4; q++) st_chunk(sb + G_H0 + sw128_chunk(r, 4 * qt + q, 64), x + 8 * q, -1.f);
                 }
             }
             tmem_wait_st();
@@ -558,21 +529,21 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
                 tmem_ld16(tl + TM_T1 + c16, d1);
                 tmem_ld16(tl + TM_T1 + 64 + c16, d2);
                 tmem_wait_ld();
-                split16(d1, w1, lane);
-                split16(d2, w2, lane);
+                split_cols<16>(d1, w1, lane);
+                split_cols<16>(d2, w2, lane);
                 const int jc = 2 * qt + (lane >> 4);
 #pragma unroll
                 for (int e = 0; e < 8; e++) {
                     const int j = 8 * jc + e;
                     w1[e] = bet[j] * (w1[e] + __expf(gam[j]) * rk[j] * w2[e]);
                 }
-                st_chunk8(sb + G_DH + sw128_chunk(r, jc, 64), w1, 1.f);
+                st_chunk(sb + G_DH + sw128_chunk(r, jc, 64), w1, 1.f);
             }
             {  // T^T dU: dv = beta T^T dU; dbeta_r += sum_v V_rv (T^T dU)_rv
                 float x[32], w[16];
                 tmem_ld32(tl + TM_T2 + c32, x);
                 tmem_wait_ld();
-                split32(x, w, lane);
+                split_cols<32>(x, w, lane);
                 const int hf = lane >> 4;  // this lane's 16 columns: c32 + 16 hf ..
                 float dot = 0.f;
 #pragma unroll
@@ -638,7 +609,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
                 if (act) {
 #pragma unroll
                     for (int q = 0; q < 2; q++)
-                        st_chunk8(sb + G_DH + 8192 + sw128_chunk(r, 2 * qt + q, 64), v + 8 * q, 1.f);
+                        st_chunk(sb + G_DH + 8192 + sw128_chunk(r, 2 * qt + q, 64), v + 8 * q, 1.f);
                 }
             }
             tmem_wait_st();
@@ -659,7 +630,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
             float v[16], w[8];
             tmem_ld16(tl + TM_T1 + c16, v);
             tmem_wait_ld();
-            split16(v, w, lane);
+            split_cols<16>(v, w, lane);
             {
                 const int jc = 2 * qt + (lane >> 4);
                 const float gr = gam[r], br = bet[r], rkr = rk[r];
@@ -707,7 +678,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
                 const int j = 8 * jc + e;
                 nrow[e] = rk[j] * (MF[fsw(r, j)] + MF[fsw(j, r)]);
             }
-            st_chunk8(sb + G_DH + 16384 + sw128_chunk(r, jc, 64), nrow, 1.f);
+            st_chunk(sb + G_DH + 16384 + sw128_chunk(r, jc, 64), nrow, 1.f);
         }
         sync_for_mma();
 

@@ -52,20 +52,6 @@ constexpr uint32_t C_BYTES = C_SM + 2048;
 constexpr uint32_t TM1 = 0, TM2 = 128;  // TMEM columns of the two accumulators
 constexpr int CH_THREADS = 512;
 
-__device__ __forceinline__ void unpack8c(const uint4& u, float* x) {
-    x[0] = bf16lo(u.x); x[1] = bf16hi(u.x); x[2] = bf16lo(u.y); x[3] = bf16hi(u.y);
-    x[4] = bf16lo(u.z); x[5] = bf16hi(u.z); x[6] = bf16lo(u.w); x[7] = bf16hi(u.w);
-}
-// An M=64 accumulator row lives in lane l < 16 of its warp; lane l + 16 takes the upper half
-// of the columns read: n = 16 -> w[0..7], n = 32 -> w[0..15].
-template <int N>
-__device__ __forceinline__ void split_cols(const float* v, float* w, int lane) {
-#pragma unroll
-    for (int e = 0; e < N / 2; e++) {
-        const float hi = __shfl_sync(0xffffffffu, v[N / 2 + e], lane & 15);
-        w[e] = (lane >> 4) ? hi : v[e];
-    }
-}
 __device__ __forceinline__ void st_f4x(float* dst, const float* x, int n4) {
     for (int q = 0; q < n4; q++)
         reinterpret_cast<float4*>(dst)[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
@@ -166,8 +152,8 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
 #pragma unroll
         for (int q = 0; q < 4; q++) {
             float x[8], y[8];
-            unpack8c(ld_shared_v4(sb + C_H0 + sw128_chunk(d, 4 * pp + q, 128)), x);
-            unpack8c(ld_shared_v4(sb + C_DH + sw128_chunk(d, 4 * pp + q, 128)), y);
+            unpack8(ld_shared_v4(sb + C_H0 + sw128_chunk(d, 4 * pp + q, 128)), x);
+            unpack8(ld_shared_v4(sb + C_DH + sw128_chunk(d, 4 * pp + q, 128)), y);
 #pragma unroll
             for (int e = 0; e < 8; e++) s += x[e] * y[e];
         }
@@ -189,7 +175,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
 #pragma unroll
         for (int q = 0; q < 2; q++) {
             float ut[8];
-            unpack8c(utv[q], ut);
+            unpack8(utv[q], ut);
 #pragma unroll
             for (int e = 0; e < 8; e++) ut[e] -= w[8 * q + e];
             st_chunk(sb + C_W + sw128_chunk(r, q0 + q, 64), ut, 1.f);
@@ -287,7 +273,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
 #pragma unroll
             for (int q = 0; q < 2; q++) {
                 float vv[8];
-                unpack8c(ld_shared_v4(sb + C_V + sw128_chunk(r, 4 * qt + 2 * hf + q, 64)), vv);
+                unpack8(ld_shared_v4(sb + C_V + sw128_chunk(r, 4 * qt + 2 * hf + q, 64)), vv);
 #pragma unroll
                 for (int e = 0; e < 8; e++) dot += vv[e] * w[8 * q + e];
             }
@@ -458,8 +444,8 @@ __global__ void __launch_bounds__(CH_THREADS, 1) grad_ch_contract_kernel(GradChA
         for (int n = 0; n < 2; n++) {
             const int u = tid + CH_THREADS * n;
             float x[8], y[8];
-            unpack8c(kr[n], x);
-            unpack8c(qr[n], y);
+            unpack8(kr[n], x);
+            unpack8(qr[n], y);
             float sk = 0.f, sq = 0.f;
 #pragma unroll
             for (int e = 0; e < 8; e++) {

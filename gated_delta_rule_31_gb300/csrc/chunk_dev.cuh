@@ -1,5 +1,5 @@
-// chunk_dev.cuh - device helpers shared by the chunk kernels (prep for scalar and per-channel
-// gates): bf16 packing, shared / global 16-byte stores, and the UT solve T = (I + A)^-1.
+// chunk_dev.cuh - device helpers shared by the chunk kernels: bf16 packing, shared / global
+// 16-byte stores, the lane split of M=64 accumulator rows, and the UT solve T = (I + A)^-1.
 #pragma once
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -27,6 +27,17 @@ __device__ __forceinline__ void st_chunk(uint32_t addr, const float* x, float s)
     st_shared_v4(addr, u.x, u.y, u.z, u.w);
 }
 __device__ __forceinline__ void st_global16(uint8_t* p, const uint4& u) { *reinterpret_cast<uint4*>(p) = u; }
+
+// An M=64 accumulator row lives in lane l < 16 of its warp; lane l + 16 takes the upper half of
+// the N columns read from TMEM: N = 16 -> w[0..7], N = 32 -> w[0..15].
+template <int N>
+__device__ __forceinline__ void split_cols(const float* v, float* w, int lane) {
+#pragma unroll
+    for (int e = 0; e < N / 2; e++) {
+        const float hi = __shfl_sync(0xffffffffu, v[N / 2 + e], lane & 15);
+        w[e] = (lane >> 4) ? hi : v[e];
+    }
+}
 
 // T = (I + A)^-1 for the strictly lower triangular fp32 A [64 x 64] (row stride LDA), by 16 x 16
 // blocks. Phase 1 (160 threads, one column each): forward substitution with L_II = I + A_II

@@ -26,6 +26,7 @@ __all__ = ["build", "fwd_chunked", "bwd_chunked", "fwd_sequential", "bwd_sequent
 
 GDR_F32, GDR_BF16 = 0, 1
 GDR_GATE_SCALAR, GDR_GATE_CHANNEL = 0, 1
+GDR_ERR_INVALID_ARG, GDR_ERR_UNSUPPORTED = 1, 2
 
 
 class Problem(ctypes.Structure):
@@ -143,7 +144,7 @@ def _problem(q, v, g, scale, use_qk_l2norm, T=None):
                    GDR_GATE_CHANNEL if channel else GDR_GATE_SCALAR, float(scale), int(bool(use_qk_l2norm)))
 
 
-def _check_inputs(q, k, v, g, beta, h0=None, decode=False):
+def _check_inputs(q, k, v, g, beta, h0=None):
     dev = q.device
     _need(q, "q", device=dev)
     _need(k, "k", dtype=q.dtype, device=dev, shape=q.shape)
@@ -170,12 +171,19 @@ def bwd_workspace_bytes(p: Problem) -> int:
     return int(lib().gdr_bwd_chunked_workspace(ctypes.byref(p)))
 
 
-def _workspace(nbytes, device, workspace):
+def _workspace(query, p, device, workspace, missing=GDR_ERR_UNSUPPORTED):
+    """(workspace, bytes) for the call whose size query is `query`: the caller's tensor after
+    checking it, else a new uint8 buffer. A zero size means the call does not take this problem
+    and raises as the status `missing` would."""
+    nbytes = int(query(ctypes.byref(p)))
+    if nbytes == 0:
+        _check(missing)
     if workspace is not None:
+        _need(workspace, "workspace", device=device)
         if workspace.numel() * workspace.element_size() < nbytes:
-            raise ValueError("workspace too small")
-        return workspace
-    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+            raise ValueError(f"workspace too small: {workspace.numel() * workspace.element_size()} < {nbytes} bytes")
+        return workspace, nbytes
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device), nbytes
 
 
 def fwd_sequential(q, k, v, g, beta, h0=None, scale=None, use_qk_l2norm=True, output_final_state=True):
@@ -201,20 +209,14 @@ def fwd_chunked(q, k, v, g, beta, h0=None, scale=None, use_qk_l2norm=True, outpu
     ht = torch.empty((p.B, p.Hv, p.Dv, p.Dk), dtype=torch.float32, device=v.device) if output_final_state else None
     if save_all:
         L = lib()
-        nbytes = int(L.gdr_fwd_chunked_saved_workspace(ctypes.byref(p)))
-        if nbytes == 0:
-            _check(2)
-        ws = _workspace(nbytes, q.device, workspace)
+        ws, nbytes = _workspace(L.gdr_fwd_chunked_saved_workspace, p, q.device, workspace)
         sb = int(L.gdr_chunk_saved_bytes(ctypes.byref(p)))
         saved = torch.empty(max(sb, 256), dtype=torch.uint8, device=q.device)
         _check(L.gdr_fwd_chunked_saved(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
                                        _ptr(o), _ptr(ht), _ptr(saved), ctypes.c_size_t(sb), _ptr(ws),
                                        ctypes.c_size_t(nbytes), _stream(q.device)))
         return o, ht, saved
-    nbytes = fwd_workspace_bytes(p)
-    if nbytes == 0:
-        _check(2)  # unsupported combination
-    ws = _workspace(nbytes, q.device, workspace)
+    ws, nbytes = _workspace(lib().gdr_fwd_chunked_workspace, p, q.device, workspace)
     if not save_states:
         _check(lib().gdr_fwd_chunked(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
                                      _ptr(o), _ptr(ht), _ptr(ws), ctypes.c_size_t(nbytes), _stream(q.device)))
@@ -246,10 +248,7 @@ def bwd_chunked(q, k, v, g, beta, h0, do, dht=None, scale=None, use_qk_l2norm=Tr
     if saved is not None:
         _need(saved, "saved", dtype=torch.uint8, device=q.device)
         L = lib()
-        nbytes = int(L.gdr_bwd_chunked_saved_workspace(ctypes.byref(p)))
-        if nbytes == 0:
-            _check(2)
-        ws = _workspace(nbytes, q.device, workspace)
+        ws, nbytes = _workspace(L.gdr_bwd_chunked_saved_workspace, p, q.device, workspace)
         _check(L.gdr_bwd_chunked_saved(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
                                        _ptr(saved), ctypes.c_size_t(saved.numel()), _ptr(do), _ptr(dht),
                                        _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dg"]),
@@ -257,20 +256,14 @@ def bwd_chunked(q, k, v, g, beta, h0, do, dht=None, scale=None, use_qk_l2norm=Tr
                                        _stream(q.device)))
         return out
     if states is None:
-        nbytes = bwd_workspace_bytes(p)
-        if nbytes == 0:
-            _check(2)
-        ws = _workspace(nbytes, q.device, workspace)
+        ws, nbytes = _workspace(lib().gdr_bwd_chunked_workspace, p, q.device, workspace)
         _check(lib().gdr_bwd_chunked(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
                                      _ptr(do), _ptr(dht), _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]),
                                      _ptr(out["dg"]), _ptr(out["dbeta"]), _ptr(out["dh0"]), _ptr(ws),
                                      ctypes.c_size_t(nbytes), _stream(q.device)))
         return out
     _need(states, "states", dtype=torch.uint8, device=q.device)
-    nbytes = int(lib().gdr_bwd_chunked_states_workspace(ctypes.byref(p)))
-    if nbytes == 0:
-        _check(2)
-    ws = _workspace(nbytes, q.device, workspace)
+    ws, nbytes = _workspace(lib().gdr_bwd_chunked_states_workspace, p, q.device, workspace)
     _check(lib().gdr_bwd_chunked_states(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
                                         _ptr(states), ctypes.c_size_t(states.numel()), _ptr(do), _ptr(dht),
                                         _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dg"]),
@@ -291,10 +284,7 @@ def bwd_sequential(q, k, v, g, beta, h0, do, dht=None, scale=None, use_qk_l2norm
     out = dict(dq=torch.empty(q.shape, **f32), dk=torch.empty(k.shape, **f32), dv=torch.empty(v.shape, **f32),
                dg=torch.empty(g.shape, **f32), dbeta=torch.empty(beta.shape, **f32),
                dh0=torch.empty((p.B, p.Hv, p.Dv, p.Dk), **f32))
-    nbytes = int(lib().gdr_bwd_sequential_workspace(ctypes.byref(p)))
-    if nbytes == 0:
-        _check(1)
-    ws = _workspace(nbytes, q.device, workspace)
+    ws, nbytes = _workspace(lib().gdr_bwd_sequential_workspace, p, q.device, workspace, missing=GDR_ERR_INVALID_ARG)
     _check(lib().gdr_bwd_sequential(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(h0),
                                     _ptr(do), _ptr(dht), _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]),
                                     _ptr(out["dg"]), _ptr(out["dbeta"]), _ptr(out["dh0"]), _ptr(ws),
@@ -305,7 +295,7 @@ def bwd_sequential(q, k, v, g, beta, h0, do, dht=None, scale=None, use_qk_l2norm
 def decode_step(q, k, v, g, beta, state, scale=None, use_qk_l2norm=True, out=None):
     """One decode step (gdr_decode_step): q,k [B,Hk,Dk]; v [B,Hv,Dv]; g [B,Hv] or [B,Hv,Dk];
     beta [B,Hv]; state [B,Hv,Dv,Dk] fp32 updated in place. Returns o [B,Hv,Dv]."""
-    _check_inputs(q, k, v, g, beta, decode=True)
+    _check_inputs(q, k, v, g, beta)
     p = _problem(q, v, g, scale, use_qk_l2norm)
     _need(state, "state", dtype=torch.float32, device=q.device, shape=(p.B, p.Hv, p.Dv, p.Dk))
     o = out if out is not None else torch.empty(v.shape, dtype=v.dtype, device=v.device)

@@ -200,3 +200,18 @@ def test_wait_expiry_selftest_validation(L):
     for ptr, n in ((None, 256), (FAKE, 255), (MISALIGNED, 256)):
         assert L.gdr_selftest_wait_expiry(ptr, n, None) == INVALID
     assert L.gdr_workspace_status(None, 256, None) == INVALID
+
+
+def test_binding_workspace_checks(L):
+    """The binding's workspace step: a size query of 0 raises the given status, and a caller's
+    workspace must be a CUDA tensor on the problem's device, contiguous and large enough (all
+    checked on the host before any launch)."""
+    from gated_delta_rule_31_gb300 import _workspace
+    with pytest.raises(gdr.GdrError) as e:
+        _workspace(L.gdr_fwd_chunked_workspace, prob(Dk=96), torch.device("cuda", 0), None)
+    assert e.value.code == UNSUPPORTED
+    with pytest.raises(gdr.GdrError) as e:
+        _workspace(L.gdr_bwd_sequential_workspace, prob(Dk=96), torch.device("cuda", 0), None, missing=INVALID)
+    assert e.value.code == INVALID
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        _workspace(L.gdr_fwd_chunked_workspace, prob(), torch.device("cuda", 0), torch.empty(1 << 20, dtype=torch.uint8))

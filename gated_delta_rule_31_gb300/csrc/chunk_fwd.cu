@@ -445,7 +445,9 @@ cudaError_t launch_prep(const PrepArgs& a, const CUtensorMap& mq, const CUtensor
 // ================================================================== scan kernel
 // One ring stage per chunk. Forward with outputs (2 stages): Mneg 32 KB | Kbar 16 KB | Qc 16 KB |
 // P 8 KB | U~ slice 4 KB. States / backward (3 stages): Mneg 32 KB | Kbar or Qc 16 KB | U~ or dO
-// slice 4 KB. The third stage lets the next chunk's operators arrive a step earlier.
+// slice 4 KB. The third stage lets the next chunk's operators arrive a step earlier. A sequence
+// with fewer chunks than stages never wraps the ring: the state tiles follow the stages it uses
+// and it launches with that much shared memory (one chunk: 2 CTAs per SM instead of 1).
 template <int MODE>
 struct ScanLayout {
     static constexpr int NS = MODE == SCAN_FWD_OUT ? 2 : 3;
@@ -453,8 +455,9 @@ struct ScanLayout {
     static constexpr uint32_t ST_Q = 49152, ST_P = 65536;  // forward outputs only
     static constexpr uint32_t ST_U = MODE == SCAN_FWD_OUT ? 73728 : 49152;
     static constexpr uint32_t STG = MODE == SCAN_FWD_OUT ? 78848 : 53248;
-    static constexpr uint32_t SS_H = NS * STG;  // two bf16 [128 x 32] SW64 state tiles (8 KB each)
-    static constexpr uint32_t BYTES = SS_H + 16384;
+    static constexpr uint32_t BYTES = NS * STG + 16384;  // + two bf16 [128 x 32] SW64 state tiles
+    // offset of the state tiles for NC chunks (the stages that NC chunks occupy)
+    __host__ __device__ static constexpr uint32_t ss_h(int NC) { return (NC < 1 ? 1 : NC < NS ? NC : NS) * STG; }
     static_assert(BYTES + 1024 <= 232448, "scan smem");
     static_assert(STG % 1024 == 0, "stage alignment");
 };
@@ -471,7 +474,7 @@ __global__ void __launch_bounds__(192, 1) scan_kernel(const __grid_constant__ CU
     using LY = ScanLayout<MODE>;
     constexpr int NS = LY::NS;
     constexpr uint32_t ST_M = LY::ST_M, ST_K = LY::ST_K, ST_Q = LY::ST_Q, ST_P = LY::ST_P, ST_U = LY::ST_U;
-    constexpr uint32_t STG = LY::STG, SS_H = LY::SS_H;
+    constexpr uint32_t STG = LY::STG;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
     const uint32_t sb = smem_u32(sm);
@@ -482,6 +485,7 @@ __global__ void __launch_bounds__(192, 1) scan_kernel(const __grid_constant__ CU
     const int j = blockIdx.x, hv = blockIdx.y, b = blockIdx.z;
     const ChunkProblem& P = a.p;
     const int NC = P.NC;
+    const uint32_t SS_H = LY::ss_h(NC);
     const size_t bh = (size_t)b * P.Hv + hv;
     auto chunk_of = [&](int i) { return MODE == SCAN_BWD ? NC - 1 - i : i; };
 
@@ -681,7 +685,10 @@ __global__ void __launch_bounds__(192, 1) scan_kernel(const __grid_constant__ CU
 }
 
 cudaError_t launch_scan(const ScanArgs& a, int mode, const CUtensorMap* mdo, cudaStream_t s) {
-    const int smem = (mode == SCAN_FWD_OUT ? ScanLayout<SCAN_FWD_OUT>::BYTES : ScanLayout<SCAN_BWD>::BYTES) + 1024;
+    // the attribute always allows the full ring; a launch asks for what its chunk count uses
+    const int smem_max = (mode == SCAN_FWD_OUT ? ScanLayout<SCAN_FWD_OUT>::BYTES : ScanLayout<SCAN_BWD>::BYTES) + 1024;
+    const int smem = (mode == SCAN_FWD_OUT ? ScanLayout<SCAN_FWD_OUT>::ss_h(a.p.NC) : ScanLayout<SCAN_BWD>::ss_h(a.p.NC)) +
+                     16384 + 1024;
     dim3 grid(kSlices, a.p.Hv, a.p.B);
     CUtensorMap dummy;
     memset(&dummy, 0, sizeof(dummy));
@@ -689,7 +696,7 @@ cudaError_t launch_scan(const ScanArgs& a, int mode, const CUtensorMap* mdo, cud
     cudaError_t e;
     switch (mode) {
         case SCAN_FWD_OUT:
-            e = cudaFuncSetAttribute(scan_kernel<SCAN_FWD_OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            e = cudaFuncSetAttribute(scan_kernel<SCAN_FWD_OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
             if (e != cudaSuccess) return e;
             trace_begin("chunk_scan_fwd", s);
             scan_kernel<SCAN_FWD_OUT><<<grid, 192, smem, s>>>(m, a);
@@ -697,14 +704,14 @@ cudaError_t launch_scan(const ScanArgs& a, int mode, const CUtensorMap* mdo, cud
             break;
         case SCAN_FWD_STATES:
             e = cudaFuncSetAttribute(scan_kernel<SCAN_FWD_STATES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     smem);
+                                     smem_max);
             if (e != cudaSuccess) return e;
             trace_begin("chunk_scan_states", s);
             scan_kernel<SCAN_FWD_STATES><<<grid, 192, smem, s>>>(m, a);
             trace_end(s);
             break;
         default:
-            e = cudaFuncSetAttribute(scan_kernel<SCAN_BWD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            e = cudaFuncSetAttribute(scan_kernel<SCAN_BWD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
             if (e != cudaSuccess) return e;
             trace_begin("chunk_scan_bwd", s);
             scan_kernel<SCAN_BWD><<<grid, 192, smem, s>>>(m, a);

@@ -69,6 +69,7 @@ BWD_CASES = [
     (1, 130, 1, 2, True, True, False, 0.01),
     (1, 300, 2, 4, False, False, True, 0.01),
     (2, 512, 2, 4, True, True, True, 1.0),
+    (3, 64, 4, 16, True, True, True, 1.0),  # one chunk, 192 scan CTAs: two or three share an SM
 ]
 
 

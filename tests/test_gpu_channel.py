@@ -33,6 +33,7 @@ CASES = [
     (1, 130, 1, 2, True, False, 0.01),
     (1, 300, 2, 4, True, True, 5.0),     # strong decay: per-token factors down to ~e^-20
     (2, 512, 2, 4, True, True, 0.01),    # mild decay: the state lives across many chunks
+    (3, 50, 4, 16, True, True, 1.0),     # one chunk, 192 scan CTAs: two share an SM
 ]
 
 

@@ -26,6 +26,7 @@ CASES = [
     (1, 300, 2, 4, True, True, 5.0),     # strong decay: per-token factors down to ~e^-20
     (1, 257, 1, 4, True, True, 0.01),    # mild decay: the state lives across many chunks
     (3, 65, 1, 8, True, True, 1.0),      # eight value heads per key head, odd batch
+    (2, 40, 2, 32, True, True, 1.0),     # one chunk, 256 scan CTAs: two or three share an SM
 ]
 
 

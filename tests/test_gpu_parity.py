@@ -99,6 +99,7 @@ CHUNK_CASES = [
     (1, 129, 1, 2, True, False, 0.01),
     (1, 300, 2, 4, False, True, 0.01),
     (2, 512, 2, 4, True, True, 1.0),
+    (3, 50, 4, 16, True, True, 1.0),     # one chunk, 192 scan CTAs: two share an SM
 ]
 
 

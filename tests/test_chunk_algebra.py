@@ -29,7 +29,8 @@ def test_chunk_forward_and_backward_equal_oracle(C, T, Hk, Hv, norm, h0):
 
 
 @pytest.mark.parametrize("C,T,Hk,Hv,norm,h0,gs", [(4, 11, 1, 2, True, True, 1.0), (8, 16, 2, 4, True, False, 1.0),
-                                                  (5, 5, 1, 2, False, True, 1.0), (16, 21, 1, 1, True, True, 8.0)])
+                                                  (5, 5, 1, 2, False, True, 1.0), (16, 21, 1, 1, True, True, 8.0),
+                                              (64, 150, 1, 2, True, True, 8.0)])
 def test_channel_chunk_forward_equals_oracle(C, T, Hk, Hv, norm, h0, gs):
     """The per-channel chunk algebra (decays as products of per-token factors, diag(Gamma_C)
     in the state update) equals the sequential oracle; gs = 8 makes per-token factors as small
@@ -43,7 +44,9 @@ def test_channel_chunk_forward_equals_oracle(C, T, Hk, Hv, norm, h0, gs):
 
 
 @pytest.mark.parametrize("C,bs,T,Hk,Hv,norm,h0,gs", [(8, 2, 19, 1, 2, True, True, 1.0), (16, 4, 16, 2, 4, True, False, 1.0),
-                                                     (8, 4, 5, 1, 1, False, True, 1.0), (16, 4, 37, 1, 2, True, True, 8.0)])
+                                                     (8, 4, 5, 1, 1, False, True, 1.0), (16, 4, 37, 1, 2, True, True, 8.0),
+                                                     (64, 16, 150, 1, 2, True, True, 8.0),   # the kernels' blocking
+                                                     (64, 16, 64, 2, 4, True, False, 0.3)])
 def test_channel_chunk_backward_equals_oracle(C, bs, T, Hk, Hv, norm, h0, gs):
     """The per-channel VJP as the chunked kernels organise it (dense products; the decay-weighted
     contractions by blocks, factored through the block boundaries below the block diagonal;

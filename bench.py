@@ -108,22 +108,30 @@ class Clocks:
             self.p.kill()
         self.f.flush()
         self.f.seek(0)
-        rows = [l.strip().split(",") for l in self.f.read().splitlines() if l.strip()]
+        text = self.f.read()
         os.unlink(self.f.name)
-        sm, mx, reasons = [], None, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
-            try:
-                sm.append(float(r[1]))
-                mx = float(r[2])
-            except (ValueError, IndexError):
-                continue
-            for n, v in zip(names, r[5:9]):
-                if v.strip().lower() == "active":
-                    reasons.add(n)
-        if not sm:
-            return dict(sm_mhz=None, sm_max_mhz=mx, reasons=sorted(reasons), samples=0)
-        return dict(sm_mhz=statistics.median(sm), sm_max_mhz=mx, reasons=sorted(reasons), samples=len(sm))
+        return parse_clocks(text)
+
+
+def parse_clocks(text):
+    """Summary of nvidia-smi rows (index, clocks.sm, clocks.max.sm, power, active mask, then
+    hw_slowdown, hw_thermal_slowdown, sw_thermal_slowdown, sw_power_cap as Active / Not
+    Active): median SM MHz, max MHz, the throttle reasons seen in any row, and the row count."""
+    rows = [l.strip().split(",") for l in text.splitlines() if l.strip()]
+    sm, mx, reasons = [], None, set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for r in rows:
+        try:
+            sm.append(float(r[1]))
+            mx = float(r[2])
+        except (ValueError, IndexError):
+            continue
+        for n, v in zip(names, r[5:9]):
+            if v.strip().lower() == "active":
+                reasons.add(n)
+    if not sm:
+        return dict(sm_mhz=None, sm_max_mhz=mx, reasons=sorted(reasons), samples=0)
+    return dict(sm_mhz=statistics.median(sm), sm_max_mhz=mx, reasons=sorted(reasons), samples=len(sm))
 
 
 def oracle_sample(target_s=15.0, max_tokens=T):

@@ -215,3 +215,24 @@ def test_binding_workspace_checks(L):
     assert e.value.code == INVALID
     with pytest.raises(ValueError, match="CUDA tensor"):
         _workspace(L.gdr_fwd_chunked_workspace, prob(), torch.device("cuda", 0), torch.empty(1 << 20, dtype=torch.uint8))
+
+
+def test_noalloc_forward_validation(L):
+    """gdr_fwd_chunked_noalloc reports invalid and unsupported problems as gdr_fwd_chunked does,
+    and problems beyond its built-in 64 MiB scratch as GDR_ERR_WORKSPACE, all before any launch."""
+    P = ctypes.c_void_p
+    L.gdr_fwd_chunked_noalloc.argtypes = [ctypes.POINTER(Problem)] + [P] * 8 + [P]
+    L.gdr_fwd_chunked_noalloc.restype = ctypes.c_int
+    for kw, code in ((dict(Hv=3), INVALID), (dict(dtype=0), UNSUPPORTED), (dict(Dk=64), UNSUPPORTED),
+                     (dict(T=4096, Hk=16, Hv=32), WORKSPACE)):
+        assert L.gdr_fwd_chunked_noalloc(ctypes.byref(prob(**kw)), *[FAKE] * 8, None) == code, kw
+    assert L.gdr_fwd_chunked_workspace(ctypes.byref(prob(T=4096, Hk=16, Hv=32))) > 64 * 1024 * 1024
+    assert L.gdr_fwd_chunked_noalloc(None, *[FAKE] * 8, None) == INVALID
+
+
+def test_trace_with_nothing_launched(L):
+    """Tracing on and off with no launch in between records nothing (no CUDA call is made)."""
+    assert L.gdr_trace_enable(1) == OK
+    assert L.gdr_trace_collect(None, None, 0) == 0
+    assert L.gdr_trace_enable(0) == OK
+    assert L.gdr_trace_collect(None, None, 0) == 0

@@ -163,6 +163,10 @@ def run_reference(args, rank, world):
     """The oracle as the reference arm: each step is one bounded sample of the workload."""
     if rank != 0:
         return
+    if world > 1:
+        # the launcher sets OMP_NUM_THREADS=1 for every rank; this arm runs on rank 0 alone, so it
+        # takes the host's cores as a one-process run does (before the oracle's OpenMP starts)
+        os.environ["OMP_NUM_THREADS"] = str(len(os.sched_getaffinity(0)))
     import oracle
     from gated_delta_rule_31_gb300.synth import Shape, make_inputs
 

@@ -36,22 +36,27 @@ def build(force: bool = False) -> str:
     return _LIB_PATH
 
 
+def _bind(lib):
+    """Declares the C signatures on a loaded oracle library (also used by the mutation tests,
+    which load deliberately altered copies of oracle.c)."""
+    i, d, p = ctypes.c_int, ctypes.c_double, ctypes.c_void_p
+    lib.oracle_forward.argtypes = [i] * 7 + [d, i] + [p] * 8
+    lib.oracle_forward.restype = i
+    lib.oracle_backward.argtypes = [i] * 7 + [d, i] + [p] * 14
+    lib.oracle_backward.restype = i
+    lib.oracle_decode_step.argtypes = [i] * 6 + [d, i] + [p] * 7
+    lib.oracle_decode_step.restype = i
+    lib.oracle_num_threads.argtypes = []
+    lib.oracle_num_threads.restype = i
+    return lib
+
+
 def _load():
     global _lib
     with _lock:
         if _lib is None:
             build()
-            lib = ctypes.CDLL(_LIB_PATH)
-            i, d, p = ctypes.c_int, ctypes.c_double, ctypes.c_void_p
-            lib.oracle_forward.argtypes = [i] * 7 + [d, i] + [p] * 8
-            lib.oracle_forward.restype = i
-            lib.oracle_backward.argtypes = [i] * 7 + [d, i] + [p] * 14
-            lib.oracle_backward.restype = i
-            lib.oracle_decode_step.argtypes = [i] * 6 + [d, i] + [p] * 7
-            lib.oracle_decode_step.restype = i
-            lib.oracle_num_threads.argtypes = []
-            lib.oracle_num_threads.restype = i
-            _lib = lib
+            _lib = _bind(ctypes.CDLL(_LIB_PATH))
     return _lib
 
 

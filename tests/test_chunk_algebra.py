@@ -62,3 +62,38 @@ def test_channel_chunk_backward_equals_oracle(C, bs, T, Hk, Hv, norm, h0, gs):
     for name in ("dq", "dk", "dv", "dg", "dbeta", "dh0"):
         err = np.max(np.abs(ref[name] - got[name])) / max(1.0, np.max(np.abs(ref[name])))
         assert err < 1e-10, (name, err)
+
+
+@pytest.mark.parametrize("channel", [False, True])
+def test_degenerate_tokens_forward_and_backward_equal_oracle(channel):
+    """Tokens with beta = 0 (no write), g = 0 (no decay), beta = 1 (full replacement), and zero
+    key or query vectors under the in-kernel norm (k^ = 0 writes nothing, q^ = 0 reads nothing,
+    and the norm backward scales by 1/sqrt(eps) = 1000) inside a sequence of several chunks: the
+    chunk algebra as the kernels organise it still equals the oracle."""
+    q, k, v, g, beta, hh = rand_inputs(B=1, T=40, Hk=1, Hv=2, Dk=6, Dv=5, channel=channel, seed=21)
+    beta[0, 3:6] = 0.0
+    beta[0, 20] = 1.0
+    g[0, 8:12] = 0.0
+    g[0, 30:] = 0.0
+    k[0, 7] = 0.0
+    k[0, 17] = 0.0
+    q[0, 9] = 0.0
+    q[0, 33] = 0.0
+    r = np.random.default_rng(22)
+    do = r.standard_normal(v.shape)
+    dht = r.standard_normal((1, 2, 5, 6))
+    o, ht = oracle.forward(q, k, v, g, beta, hh, scale=0.7, use_qk_l2norm=True)
+    assert np.all(o[0, 9] == 0.0) and np.all(o[0, 33] == 0.0)
+    if channel:
+        o2, ht2 = ca.forward_channel(q, k, v, g, beta, hh, 0.7, True, 16)
+        got = ca.backward_channel(q, k, v, g, beta, hh, do, dht, 0.7, True, 16, 4)
+    else:
+        o2, ht2, _ = ca.forward(q, k, v, g, beta, hh, 0.7, True, 16)
+        got = ca.backward(q, k, v, g, beta, hh, do, dht, 0.7, True, 16)
+    assert np.max(np.abs(o - o2)) < 1e-11 and np.max(np.abs(ht - ht2)) < 1e-11
+    ref = oracle.backward(q, k, v, g, beta, hh, do, dht, scale=0.7, use_qk_l2norm=True)
+    for name in ("dq", "dk", "dv", "dg", "dbeta", "dh0"):
+        err = np.max(np.abs(ref[name] - got[name])) / max(1.0, np.max(np.abs(ref[name])))
+        assert err < 1e-10, (name, err)
+    # a zero key still receives a gradient, scaled by 1/sqrt(eps) through the norm backward
+    assert np.max(np.abs(ref["dk"][0, 7])) > 10 * np.max(np.abs(ref["dk"][0, [6, 8]]))

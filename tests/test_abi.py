@@ -4,6 +4,7 @@ launched (so these run without a GPU: invalid calls never reach the CUDA runtime
 import ctypes
 import os
 import re
+import subprocess
 
 import pytest
 import torch
@@ -236,3 +237,32 @@ def test_trace_with_nothing_launched(L):
     assert L.gdr_trace_collect(None, None, 0) == 0
     assert L.gdr_trace_enable(0) == OK
     assert L.gdr_trace_collect(None, None, 0) == 0
+
+
+def test_plain_c_program_links_and_calls_the_library(L, tmp_path):
+    """include/gdr.h compiles as C99 and a C program links libgdr.so and calls the host-side
+    entry points (workspace query, argument validation, status strings): no C++ or Python
+    is needed to use the library."""
+    src = tmp_path / "use_gdr.c"
+    src.write_text(r'''
+#include <stdio.h>
+#include <string.h>
+#include "gdr.h"
+int main(void) {
+    gdr_problem p;
+    memset(&p, 0, sizeof p);
+    p.B = 1; p.T = 64; p.Hk = 1; p.Hv = 2; p.Dk = 128; p.Dv = 128;
+    p.dtype = GDR_BF16; p.gate = GDR_GATE_SCALAR; p.scale = 0.088f; p.use_qk_l2norm = 1;
+    size_t ws = gdr_fwd_chunked_workspace(&p);
+    gdr_status s = gdr_fwd_chunked(&p, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0);
+    printf("%zu %d %s\n", ws, (int)s, gdr_status_string(s));
+    return (ws > 0 && s == GDR_ERR_INVALID_ARG) ? 0 : 1;
+}
+''')
+    exe = tmp_path / "use_gdr"
+    libdir = os.path.dirname(gdr.lib()._name)
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), str(src),
+                    "-L", libdir, "-lgdr", "-Wl,-rpath," + libdir, "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0, out.stdout + out.stderr
+    assert "GDR_ERR_INVALID_ARG" in out.stdout

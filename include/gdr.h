@@ -209,18 +209,28 @@ gdr_status gdr_selftest_wait_expiry(void* ws, size_t ws_bytes, gdr_stream_t stre
  * another allocator, or a deployment that forbids device allocation once it has started.
  * (The pages on the gated delta rule have no counterpart to this call.) Instead of a
  * caller workspace it uses a scratch array of GDR_NOALLOC_SCRATCH_BYTES (64 MiB) that the
- * library keeps on every GPU where it is loaded, for the life of the process. It allocates
- * nothing. Problems whose gdr_fwd_chunked_workspace() exceeds that size return
- * GDR_ERR_WORKSPACE with nothing launched (about 740 chunk records: for example B=1, Hv=32,
- * T <= 1472). Inputs, outputs and the support matrix are those of gdr_fwd_chunked.
- * The first call on a device looks up the scratch address on that device (so make the
- * first call on each device before any stream capture). All calls share the one array and
- * it keeps the last call's contents (the call clears the status word it needs at zero):
- * calls that can overlap on the GPU (different streams, or different host threads) race
- * on it, so serialise them. */
+ * library keeps on every GPU where it is loaded, for the life of the process. The call
+ * itself allocates nothing, but with lazy module loading (the CUDA default) the driver
+ * reserves that 64 MiB on a device when the first call on it looks up the scratch address:
+ * make the first call on each device at start-up (a problem with B = 0 is enough), and
+ * before any stream capture. Problems whose gdr_fwd_chunked_workspace() exceeds the
+ * scratch return GDR_ERR_WORKSPACE with nothing launched (about 740 chunk records: for
+ * example B=1, Hv=32, T <= 1472). `stream` must belong to the current device
+ * (GDR_ERR_INVALID_ARG otherwise). Inputs, outputs and the support matrix are those of
+ * gdr_fwd_chunked. All calls share the one array and it keeps the last call's contents
+ * (the call clears the status word it needs at zero): calls that can overlap on the GPU
+ * (different streams, or different host threads) race on it, so serialise them. A
+ * bounded-wait expiry is recorded in the scratch's status word: read it with
+ * gdr_noalloc_status before the next call clears it. */
 gdr_status gdr_fwd_chunked_noalloc(const gdr_problem* p, const void* q, const void* k, const void* v,
                                    const float* g, const float* beta, const float* h0, void* o, float* ht,
                                    gdr_stream_t stream);
+
+/* gdr_workspace_status for the scratch of gdr_fwd_chunked_noalloc on the current device:
+ * synchronises on `stream` (which must belong to the current device), then returns GDR_OK,
+ * or GDR_ERR_TIMEOUT if a wait of the last call expired, and clears the word. GDR_OK if no
+ * call has run on this device. */
+gdr_status gdr_noalloc_status(gdr_stream_t stream);
 
 /* Launch tracing for profiling. While enabled, every kernel the library launches is
  * bracketed by two CUDA events recorded on its own stream (host-side events only; no

@@ -87,9 +87,9 @@ def test_chunked_backward_small(case):
     check(gr, x, norm)
 
 
-@pytest.mark.parametrize("idx", [0, 2, 3, 6, 8, 11])
+@pytest.mark.parametrize("idx", range(12))
 def test_vjp_sweep_point(idx):
-    """Points of the B in {1,4,8} x T in {8,64,512,4096} sweep (Hk=16, Hv=32, D=128), with
+    """Every point of the B in {1,4,8} x T in {8,64,512,4096} sweep (Hk=16, Hv=32, D=128), with
     do ~ N(0,1) bf16 and dht ~ N(0, 0.01); groups (b, hk) = (0, 0) and (B-1, 15) checked."""
     dev = cuda_device()
     shape = VJP_SWEEP[idx]
@@ -99,12 +99,33 @@ def test_vjp_sweep_point(idx):
         check(sliced_out(gr, b, hk, 2), sliced(x, b, hk, 2))
 
 
+def sliced_heads(x, heads, G):
+    """Inputs of the key heads `heads` (and their value heads) of batch 0."""
+    vh = [hk * G + j for hk in heads for j in range(G)]
+    s = {}
+    for n, t in x.items():
+        if t is None:
+            s[n] = None
+        elif n in ("q", "k"):
+            s[n] = t[:1, :, heads].contiguous()
+        elif n in ("h0", "dht"):
+            s[n] = t[:1, vh].contiguous()
+        else:
+            s[n] = t[:1, :, vh].contiguous()
+    return s, vh
+
+
 def test_long_context_training_step_backward():
-    """B=1, T=32768, h0 = 0, dht = 0, do ~ N(0,1): key head 5 (value heads 10, 11) checked."""
+    """B=1, T=32768, h0 = 0, dht = 0, do ~ N(0,1): four key heads spread over the 16 (0, 5, 10,
+    15, i.e. value heads 0-1, 10-11, 20-21, 30-31) checked against the oracle."""
     dev = cuda_device()
     x = make_inputs(LONG_TRAIN, dtype=torch.bfloat16, seed=1004, grads=True, h0_std=None, dht_std=None)
     gr = {k: v.cpu() for k, v in gpu_bwd(x, dev).items()}
-    check(sliced_out(gr, 0, 5, 2), sliced(x, 0, 5, 2))
+    heads = [0, 5, 10, 15]
+    xs, vh = sliced_heads(x, heads, 2)
+    out = {n: (t[:1, :, heads] if n in ("dq", "dk") else t[:1, vh] if n == "dh0" else t[:1, :, vh])
+           for n, t in gr.items()}
+    check(out, xs)
 
 
 def test_backward_mild_decay_long_range():

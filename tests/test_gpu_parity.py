@@ -57,18 +57,22 @@ def test_sequential_no_final_state_and_empty():
 
 # ------------------------------------------------------------------ decode
 def test_decode_config_steps():
-    """B=32, Hk=16, Hv=32, Dk=Dv=128, channel gate, fp32: three consecutive steps."""
+    """B=32, Hk=16, Hv=32, Dk=Dv=128, channel gate, fp32: all 256 consecutive steps of the
+    decode workload, each step's output against the oracle's decode step on the oracle's own
+    state trajectory, and the state every 16 steps and at the end."""
     dev = cuda_device()
     cfg = DECODE
-    x = make_decode_inputs(cfg["B"], cfg["Hk"], cfg["Hv"], cfg["Dk"], cfg["Dv"], steps=3, seed=1003)
+    steps = cfg["steps"]
+    x = make_decode_inputs(cfg["B"], cfg["Hk"], cfg["Hv"], cfg["Dk"], cfg["Dv"], steps=steps, seed=1003)
     st = x["state0"].to(dev).clone()
     ref = x["state0"].double().numpy()
-    for t in range(3):
+    for t in range(steps):
         o = gdr.decode_step(x["q"][t].to(dev), x["k"][t].to(dev), x["v"][t].to(dev), x["g"][t].to(dev),
                             x["beta"][t].to(dev), st)
         ro, ref = oracle.decode_step(x["q"][t], x["k"][t], x["v"][t], x["g"][t], x["beta"][t], ref)
-        assert rel_err(o, ro) <= F32_TOL
-        assert rel_err(st, ref) <= F32_TOL
+        assert rel_err(o, ro) <= F32_TOL, t
+        if t % 16 == 15 or t == steps - 1:
+            assert rel_err(st, ref) <= F32_TOL, t
 
 
 @pytest.mark.parametrize("gate", ["scalar", "channel"])

@@ -21,8 +21,6 @@ namespace gdr {
 
 constexpr int kChunk = 64;
 constexpr int kD = 128;        // Dk = Dv handled by the tensor-core path
-constexpr int kSlice = 32;     // Dv columns of the state owned by one scan CTA
-constexpr int kSlices = kD / kSlice;
 
 // Per-(b, hv, chunk) record written by the prep kernel, as shared-memory images
 // (panelised SW128 tiles unless noted) so the scans fetch them with plain bulk copies.
@@ -30,7 +28,8 @@ constexpr uint32_t REC_M = 0;            // Mneg  [128 d  x 128 d']  32 KB
 constexpr uint32_t REC_K = 32768;        // Kbar  [64 tok x 128 d]   16 KB
 constexpr uint32_t REC_Q = 49152;        // Qc    [64 tok x 128 d]   16 KB
 constexpr uint32_t REC_P = 65536;        // P     [64 tok x 64 tok]   8 KB
-constexpr uint32_t REC_U = 73728;        // U~    4 x [64 tok x 32] SW64 slices, 4 KB each
+constexpr uint32_t REC_U = 73728;        // U~    4 x [64 tok x 32] SW64 slices, 4 KB each (a 64-column
+                                         //       half is two consecutive slices: N=64 operand, LBO 4 KB)
 constexpr uint32_t REC_BYTES = 90112;
 constexpr uint32_t STATE_IMG = 32768;    // one bf16 [128 d x 128 v] SW128 state image
 // Extra per-chunk record kept for the backward: T = (I + A)^-1 [64 x 64] and W [64 x 128];

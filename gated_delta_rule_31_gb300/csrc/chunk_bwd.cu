@@ -35,8 +35,8 @@ constexpr uint32_t G_KQ = 0;        // k rows 0-63, q rows 64-127 (panels 16 KB)
 constexpr uint32_t G_V = 32768;     // v [64 x 128]; later M fp32 [64][64]
 constexpr uint32_t G_DO = 49152;    // dO [64 x 128]; later dSq image [64 x 64]
 constexpr uint32_t G_H0 = 65536;    // H0 image [128 d x 128 v]; later dW image [64 x 128]
-constexpr uint32_t G_DH = 98304;    // dH1 image; later dT (+0), Yt (+8K), N (+16K) images
-constexpr uint32_t G_T = 131072;    // T image [64 x 64]
+constexpr uint32_t G_DH = 98304;    // dH1 image (free after M3: the next head's dH1 lands here early)
+constexpr uint32_t G_T = 131072;    // T image [64 x 64]; after M6 the N image
 constexpr uint32_t G_W = 139264;    // W image [64 x 128]; later U image
 constexpr uint32_t G_P = 155648;    // P image [64 x 64]; later dSk image
 constexpr uint32_t G_KB = 163840;   // Kbar image [64 x 128]; later dU image
@@ -109,6 +109,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
 
     uint32_t ld_phase = 0, mma_phase = 0, h_phase = 0;
     bool pend_ld = false, pend_h = false;  // copies issued and not yet waited for (thread 0)
+    bool h_open = false;  // pieces of the next head issued before its arriving piece (thread 0)
     if (tid == 0) {
         abort_sh = 0;
         mbar_init(&bar_ld, 1);
@@ -156,13 +157,14 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
                    id64x64_mm = idesc_bf16(64, 64, 1, 1);
 
     // Inputs of value head hv, issued in pieces as their buffers free up (thread 0 only):
-    // piece 0: P, W, dO   1: Kbar   2: H0   3: T   4: v   5: dH1 (the arrival)
+    // piece 0: P, W, dO   1: Kbar   2: H0   3: T (the arrival, always issued last)   4: v   5: dH1
     auto load_piece = [&](int bb, int cc, int hv, int piece) {
         const size_t bh = (size_t)bb * P.Hv + hv;
         const size_t idx = bh * P.NC + cc;
         const int tt = cc * kChunk;
         const uint8_t* rec = a.rec + idx * REC_BYTES;
         const uint8_t* rec2 = a.rec2 + idx * REC2_BYTES;
+        h_open = piece != 3;
         switch (piece) {
             case 0:
                 mbar_add_tx(&bar_h, 8192 + 16384 + 2 * 8192);
@@ -179,9 +181,10 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
                 mbar_add_tx(&bar_h, 32768);
                 bulk_load(sm + G_H0, a.hs + idx * STATE_IMG, 32768, &bar_h);
                 break;
-            case 3:
-                mbar_add_tx(&bar_h, 8192);
+            case 3:  // issued last: arrives, so the head's phase completes when every piece has landed
+                mbar_expect_tx(&bar_h, 8192);
                 bulk_load(sm + G_T, rec2 + REC2_T, 8192, &bar_h);
+                pend_h = true;
                 break;
             case 4:
                 mbar_add_tx(&bar_h, 2 * 8192);
@@ -189,9 +192,8 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
                 tma_load_4d(sm + G_V + 8192, &mv, 64, hv, tt, bb, &bar_h);
                 break;
             default:
-                mbar_expect_tx(&bar_h, 32768);  // arrives: the head's phase completes when all landed
+                mbar_add_tx(&bar_h, 32768);
                 bulk_load(sm + G_DH, a.dhs + idx * STATE_IMG, 32768, &bar_h);
-                pend_h = true;
                 break;
         }
     };
@@ -223,7 +225,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
         const int t = blockIdx.x;
         const int cc = t % P.NC, hh = (t / P.NC) % P.Hk, bb = t / (P.NC * P.Hk);
         issue_kq(bb, cc, hh, kq);
-        for (int piece = 0; piece < 6; piece++) load_piece(bb, cc, hh * G, piece);  // first value head
+        for (int piece : {0, 1, 2, 4, 5, 3}) load_piece(bb, cc, hh * G, piece);  // first value head (T last)
     }
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
     c = tile % P.NC;
@@ -474,7 +476,10 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
         __syncthreads();
         if (tid < 64) dgc[tid] -= red[16 + tid] + red[80 + tid] + red[144 + tid] + red[208 + tid];
         if (!wait_mma(45)) goto teardown;
-        if (more && tid == 0) prefetch(0);
+        if (more && tid == 0) {  // P, W, dO and dH1 of the next head: their buffers are free after M3
+            prefetch(0);
+            prefetch(5);
+        }
         {
             const float br = __expf(gC - gam[r]);
             {  // Y: db_r = rk_r sum_d K_rd Y_rd; dK^ += b_r Y_r
@@ -524,7 +529,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
         if (!wait_mma(46)) goto teardown;
         if (more && tid == 0) prefetch(1);
         {
-            {  // dT_rj = beta_j (dU V^T + Gamma_j rk_j dW K^T)_rj -> dT image (G_DH)
+            {  // dT_rj = beta_j (dU V^T + Gamma_j rk_j dW K^T)_rj -> dT image (ZS, free until M6's epilogue)
                 float d1[16], d2[16], w1[8], w2[8];
                 tmem_ld16(tl + TM_T1 + c16, d1);
                 tmem_ld16(tl + TM_T1 + 64 + c16, d2);
@@ -537,7 +542,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
                     const int j = 8 * jc + e;
                     w1[e] = bet[j] * (w1[e] + __expf(gam[j]) * rk[j] * w2[e]);
                 }
-                st_chunk(sb + G_DH + sw128_chunk(r, jc, 64), w1, 1.f);
+                st_chunk(sb + gfz + 16384 + sw128_chunk(r, jc, 64), w1, 1.f);
             }
             {  // T^T dU: dv = beta T^T dU; dbeta_r += sum_v V_rv (T^T dU)_rv
                 float x[32], w[16];
@@ -572,7 +577,8 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
             tc_fence_after();
             for (int k0 = 0; k0 < kChunk; k0 += 16) {
                 mma(TM_T2, desc_mnmajor(sb + G_T, 64, 0, k0), desc_mnmajor(sb + G_H0, 64, 0, k0), id64x128_mm, k0 > 0);
-                mma(TM_T1, desc_kmajor(sb + G_DH, 64, 0, k0), desc_kmajor(sb + G_T, 64, 0, k0), id64x64_kk, k0 > 0);
+                mma(TM_T1, desc_kmajor(sb + gfz + 16384, 64, 0, k0), desc_kmajor(sb + G_T, 64, 0, k0), id64x64_kk,
+                    k0 > 0);
             }
             mma_commit(&bar_mma);
         }
@@ -602,14 +608,14 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
                     dgp[qt * 64 + r] += bgr * rk[r] * dot;
                 }
             }
-            {  // Yt -> image (G_DH + 8K)
+            {  // Yt -> image (ZS + 8K)
                 float v[16];
                 tmem_ld16(tl + TM_T1 + c16, v);
                 tmem_wait_ld();
                 if (act) {
 #pragma unroll
                     for (int q = 0; q < 2; q++)
-                        st_chunk(sb + G_DH + 8192 + sw128_chunk(r, 2 * qt + q, 64), v + 8 * q, 1.f);
+                        st_chunk(sb + gfz + 16384 + 8192 + sw128_chunk(r, 2 * qt + q, 64), v + 8 * q, 1.f);
                 }
             }
             tmem_wait_st();
@@ -620,12 +626,12 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
         if (tid == 0) {
             tc_fence_after();
             for (int k0 = 0; k0 < kChunk; k0 += 16)
-                mma(TM_T1, desc_mnmajor(sb + G_T, 64, 0, k0), desc_mnmajor(sb + G_DH + 8192, 64, 0, k0), id64x64_mm,
+                mma(TM_T1, desc_mnmajor(sb + G_T, 64, 0, k0), desc_mnmajor(sb + gfz + 16384 + 8192, 64, 0, k0), id64x64_mm,
                     k0 > 0);
             mma_commit(&bar_mma);
         }
         if (!wait_mma(48)) goto teardown;
-        if (more && tid == 0) prefetch(3);
+
         {  // dA = strict_lower(-T^T Yt); terms of A_rj = beta_r rk_r rk_j E_rj G_rj
             float v[16], w[8];
             tmem_ld16(tl + TM_T1 + c16, v);
@@ -670,7 +676,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
             }
         }
         __syncthreads();
-        {  // N_rj = rk_j (M_rj + M_jr) -> image (G_DH + 16K); 8 columns per lane
+        {  // N_rj = rk_j (M_rj + M_jr) -> image (G_T: T is no longer read); 8 columns per lane
             const int jc = 2 * qt + (lane >> 4);
             float nrow[8];
 #pragma unroll
@@ -678,7 +684,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
                 const int j = 8 * jc + e;
                 nrow[e] = rk[j] * (MF[fsw(r, j)] + MF[fsw(j, r)]);
             }
-            st_chunk(sb + G_DH + 16384 + sw128_chunk(r, jc, 64), nrow, 1.f);
+            st_chunk(sb + G_T + sw128_chunk(r, jc, 64), nrow, 1.f);
         }
         sync_for_mma();
 
@@ -686,7 +692,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
         if (tid == 0) {
             tc_fence_after();
             for (int k0 = 0; k0 < kChunk; k0 += 16)
-                mma(TM_DK, desc_kmajor(sb + G_DH + 16384, 64, 0, k0), desc_mnmajor(sb + kq, 128, 0, k0), id64x128_km,
+                mma(TM_DK, desc_kmajor(sb + G_T, 64, 0, k0), desc_mnmajor(sb + kq, 128, 0, k0), id64x128_km,
                     true);
             mma_commit(&bar_mma);
             if (more) prefetch(4);  // v: its buffer held M, read before the sync above
@@ -732,7 +738,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
             }
         }
         if (!wait_mma(49)) goto teardown;
-        if (more && tid == 0) prefetch(5);
+        if (more && tid == 0) prefetch(3);  // T: its buffer held N, read by M7
         if (last_head && tid == 0 && ntile < ntiles) issue_kq(nb, nc, nhk, gfz);  // GF / ZS are free now
     }
 
@@ -790,6 +796,10 @@ teardown:
     if (abort_sh && tid == 0) {  // let copies still in flight land before the CTA exits
         volatile int never = 0;
         if (pend_ld) mbar_wait(&bar_ld, ld_phase, &never, nullptr, 0);
+        if (h_open) {  // pieces in flight without their arrival: arrive, so the phase ends when they land
+            mbar_arrive(&bar_h);
+            pend_h = true;
+        }
         if (pend_h) mbar_wait(&bar_h, h_phase, &never, nullptr, 0);
         mbar_wait(&bar_mma, mma_phase, &never, nullptr, 0);
     }
@@ -806,7 +816,7 @@ cudaError_t launch_chunk_bwd(const ChunkBwdArgs& a, cudaStream_t s) {
     uint8_t* ws = static_cast<uint8_t*>(a.ws);
     CUtensorMap mq, mk, mv, mdo32, mdo64;
     if (!make_qkv_maps(p, a.q, a.k, a.v, &mq, &mk, &mv)) return cudaErrorInvalidValue;
-    if (!make_map_4d_bf16(&mdo32, a.do_, kD, p.Hv, p.T, p.B, kSlice, kChunk, CU_TENSOR_MAP_SWIZZLE_64B) ||
+    if (!make_map_4d_bf16(&mdo32, a.do_, kD, p.Hv, p.T, p.B, 32, kChunk, CU_TENSOR_MAP_SWIZZLE_64B) ||
         !make_map_4d_bf16(&mdo64, a.do_, kD, p.Hv, p.T, p.B, 64, kChunk, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     int* status = reinterpret_cast<int*>(ws);

@@ -6,9 +6,7 @@
 //                 (UT/WY transform of the k k^T beta block, output and state operators) on
 //                 tcgen05 with TMEM accumulators and writes them as ready-to-use
 //                 shared-memory images.
-//   scan_kernel : one CTA per (b, v-head, 32-column slice of the state). Runs the chunks
-//                 in order (or in reverse for the backward) with the fp32 state slice in
-//                 registers; per chunk one dependent tensor-core product.
+// The chunk-to-chunk scans that consume these operators are in scan.cu.
 // The algebra is stated in chunk.h. The chunked prefill and its backward are the
 // "chunked case" of "Adding VJP for gated delta net" (MLX PR #4565); the q/k L2 norm is
 // applied inside ("fold q/k L2-norm into the gated_delta_rule kernel", eps 1e-6) as an
@@ -439,285 +437,6 @@ cudaError_t launch_prep(const PrepArgs& a, const CUtensorMap& mq, const CUtensor
     trace_begin("chunk_prep", s);
     prep_kernel<<<grid, 256, smem, s>>>(mq, mk, mv, a);
     trace_end(s);
-    return cudaGetLastError();
-}
-
-// ================================================================== scan kernel
-// One ring stage per chunk. Forward with outputs (2 stages): Mneg 32 KB | Kbar 16 KB | Qc 16 KB |
-// P 8 KB | U~ slice 4 KB. States / backward (3 stages): Mneg 32 KB | Kbar or Qc 16 KB | U~ or dO
-// slice 4 KB. The third stage lets the next chunk's operators arrive a step earlier. A sequence
-// with fewer chunks than stages never wraps the ring: the state tiles follow the stages it uses
-// and it launches with that much shared memory (one chunk: 2 CTAs per SM instead of 1).
-template <int MODE>
-struct ScanLayout {
-    static constexpr int NS = MODE == SCAN_FWD_OUT ? 2 : 3;
-    static constexpr uint32_t ST_M = 0, ST_K = 32768;  // ST_K: Kbar (forward) or Qc (backward)
-    static constexpr uint32_t ST_Q = 49152, ST_P = 65536;  // forward outputs only
-    static constexpr uint32_t ST_U = MODE == SCAN_FWD_OUT ? 73728 : 49152;
-    static constexpr uint32_t STG = MODE == SCAN_FWD_OUT ? 78848 : 53248;
-    static constexpr uint32_t BYTES = NS * STG + 16384;  // + two bf16 [128 x 32] SW64 state tiles
-    // offset of the state tiles for NC chunks (the stages that NC chunks occupy)
-    __host__ __device__ static constexpr uint32_t ss_h(int NC) { return (NC < 1 ? 1 : NC < NS ? NC : NS) * STG; }
-    static_assert(BYTES + 1024 <= 232448, "scan smem");
-    static_assert(STG % 1024 == 0, "stage alignment");
-};
-
-__device__ __forceinline__ void write_state_tile(uint32_t tile, int d, const float* H) {
-#pragma unroll
-    for (int q = 0; q < 4; q++)
-        st_shared_v4(tile + sw64_chunk(d, q), pack_bf16(H[8 * q], H[8 * q + 1]), pack_bf16(H[8 * q + 2], H[8 * q + 3]),
-                     pack_bf16(H[8 * q + 4], H[8 * q + 5]), pack_bf16(H[8 * q + 6], H[8 * q + 7]));
-}
-
-template <int MODE>
-__global__ void __launch_bounds__(192, 1) scan_kernel(const __grid_constant__ CUtensorMap mdo, ScanArgs a) {
-    using LY = ScanLayout<MODE>;
-    constexpr int NS = LY::NS;
-    constexpr uint32_t ST_M = LY::ST_M, ST_K = LY::ST_K, ST_Q = LY::ST_Q, ST_P = LY::ST_P, ST_U = LY::ST_U;
-    constexpr uint32_t STG = LY::STG;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = align1024(smem_raw);
-    const uint32_t sb = smem_u32(sm);
-    __shared__ uint64_t full[3], empty[3], hready, sfull, ofull[2], drain;
-    __shared__ uint32_t tmem_sh;
-    __shared__ int abort_sh;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int j = blockIdx.x, hv = blockIdx.y, b = blockIdx.z;
-    const ChunkProblem& P = a.p;
-    const int NC = P.NC;
-    const uint32_t SS_H = LY::ss_h(NC);
-    const size_t bh = (size_t)b * P.Hv + hv;
-    auto chunk_of = [&](int i) { return MODE == SCAN_BWD ? NC - 1 - i : i; };
-
-    if (tid == 0) {
-        abort_sh = 0;
-        for (int s = 0; s < NS; s++) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
-        }
-        mbar_init(&ofull[0], 1);
-        mbar_init(&ofull[1], 1);
-        mbar_init(&hready, 1);
-        mbar_init(&sfull, 1);
-        mbar_init(&drain, 1);
-        fence_barrier_init();
-    }
-    if (warp == 0) {
-        tmem_alloc(&tmem_sh, 128);  // Ds[0..1] cols 0-63, Do[0..1] cols 64-127
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tm = tmem_sh;
-    int last_loaded = -1;
-
-    if (warp == 0) {
-        if (lane == 0) {  // producer: bulk copies of the chunk records (+ dO slice via TMA)
-            for (int i = 0; i < NC; i++) {
-                const int c = chunk_of(i), s = i % NS;
-                if (i >= NS && !mbar_wait(&empty[s], ((i / NS) + 1) & 1, &abort_sh, a.status, 20)) break;
-                uint8_t* st = sm + s * STG;
-                const uint8_t* rec = a.rec + (bh * NC + c) * REC_BYTES;
-                uint32_t bytes = 32768 + 4096 + 16384;
-                if (MODE == SCAN_FWD_OUT) bytes += 16384 + 8192;
-                mbar_expect_tx(&full[s], bytes);
-                bulk_load(st + ST_M, rec + REC_M, 32768, &full[s]);
-                if (MODE != SCAN_BWD) {
-                    bulk_load(st + ST_K, rec + REC_K, 16384, &full[s]);
-                    bulk_load(st + ST_U, rec + REC_U + j * 4096, 4096, &full[s]);
-                }
-                if (MODE == SCAN_FWD_OUT) {
-                    bulk_load(st + ST_Q, rec + REC_Q, 16384, &full[s]);
-                    bulk_load(st + ST_P, rec + REC_P, 8192, &full[s]);
-                }
-                if (MODE == SCAN_BWD) {
-                    bulk_load(st + ST_K, rec + REC_Q, 16384, &full[s]);
-                    tma_load_4d(st + ST_U, &mdo, kSlice * j, hv, kChunk * c, b, &full[s]);
-                }
-                last_loaded = i;
-            }
-        }
-    } else if (warp == 1) {
-        if (lane == 0) {  // MMA issuer
-            const uint32_t id_state = MODE == SCAN_BWD ? idesc_bf16(128, 32, 1, 1) : idesc_bf16(128, 32, 0, 1);
-            const uint32_t id_pre = idesc_bf16(128, 32, 1, 1);
-            const uint32_t id_out = idesc_bf16(64, 32, 0, 1);
-            auto issue_pre = [&](int i) {  // state-independent term into Ds[i & 1]
-                const uint32_t st = sb + (i % NS) * STG;
-                const uint32_t src = st + ST_K;  // Qc^T dO (backward)  or  Kbar^T U~ (forward)
-                for (int k0 = 0; k0 < kChunk; k0 += 16)
-                    mma_bf16(tm + 32 * (i & 1), desc_mnmajor(src, 64, 0, k0), desc_mnmajor_sw64(st + ST_U, 64, k0),
-                             id_pre, k0 > 0);
-            };
-            for (int i = 0; i < NC; i++) {
-                const int s = i % NS, sd = i & 1;  // ring stage, double-buffer index
-                const uint32_t st = sb + s * STG;
-                if (i == 0) {
-                    if (!mbar_wait(&full[0], 0, &abort_sh, a.status, 21)) break;
-                    tc_fence_after();
-                    issue_pre(0);
-                }
-                if (!mbar_wait(&hready, i & 1, &abort_sh, a.status, 22)) break;
-                tc_fence_after();
-                const uint32_t ht = sb + SS_H + (i & 1) * 8192;
-                for (int k0 = 0; k0 < kD; k0 += 16) {
-                    const uint64_t ad =
-                        MODE == SCAN_BWD ? desc_mnmajor(st + ST_M, 128, 0, k0) : desc_kmajor(st + ST_M, 128, 0, k0);
-                    mma_bf16(tm + 32 * sd, ad, desc_mnmajor_sw64(ht, 128, k0), id_state, 1);
-                }
-                mma_commit(&sfull);
-                if (MODE == SCAN_FWD_OUT) {
-                    for (int k0 = 0; k0 < kD; k0 += 16)
-                        mma_bf16(tm + 64 + 32 * sd, desc_kmajor(st + ST_Q, 64, 0, k0), desc_mnmajor_sw64(ht, 128, k0),
-                                 id_out, k0 > 0);
-                    for (int k0 = 0; k0 < kChunk; k0 += 16)
-                        mma_bf16(tm + 64 + 32 * sd, desc_kmajor(st + ST_P, 64, 0, k0),
-                                 desc_mnmajor_sw64(st + ST_U, 64, k0), id_out, 1);
-                    mma_commit(&ofull[sd]);
-                }
-                mma_commit(&empty[s]);
-                if (i + 1 < NC) {
-                    if (!mbar_wait(&full[(i + 1) % NS], ((i + 1) / NS) & 1, &abort_sh, a.status, 23)) break;
-                    tc_fence_after();
-                    issue_pre(i + 1);
-                }
-            }
-            // every product issued so far has completed before TMEM is released
-            mma_commit(&drain);
-            volatile int never = 0;
-            mbar_wait(&drain, 0, &never, nullptr, 0);
-        }
-    } else {  // epilogue: 4 warps, thread <-> TMEM lane d = state row (key channel)
-        const int et = tid - 64;
-        const int lg = warp & 3;
-        const int d = 32 * lg + lane;
-        float H[32];
-#pragma unroll
-        for (int n = 0; n < 32; n++)
-            H[n] = a.hinit ? a.hinit[(bh * kD + kSlice * j + n) * kD + d] : 0.f;
-        write_state_tile(sb + SS_H, d, H);
-        fence_proxy_async_smem();
-        bool bad = bar_sync_or(1, 128, false);
-        if (et == 0) mbar_arrive(&hready);
-        // Gamma_C of each chunk: one per head, or one per key channel (this thread's row d)
-        const float* gam = P.channel ? a.gam + bh * NC * kD + d : a.gam + bh * a.ncpad;
-        const int gstride = P.channel ? kD : 1;
-        float gnext = gam[chunk_of(0) * gstride];
-        int i = 0;
-        for (; i < NC && !bad; i++) {
-            const int c = chunk_of(i), s = i & 1;
-            const float gC = gnext;
-            if (i + 1 < NC) gnext = gam[chunk_of(i + 1) * gstride];
-            if (MODE != SCAN_FWD_OUT || a.states) {  // state entering this step, SW128 [128 x 128] image
-                uint8_t* img = a.states + (bh * NC + c) * (size_t)STATE_IMG;
-#pragma unroll
-                for (int q = 0; q < 4; q++) {
-                    uint4 v = make_uint4(pack_bf16(H[8 * q], H[8 * q + 1]), pack_bf16(H[8 * q + 2], H[8 * q + 3]),
-                                         pack_bf16(H[8 * q + 4], H[8 * q + 5]), pack_bf16(H[8 * q + 6], H[8 * q + 7]));
-                    *reinterpret_cast<uint4*>(img + sw128_chunk(d, 4 * j + q, 128)) = v;
-                }
-            }
-            bool ok = __all_sync(0xffffffffu, mbar_wait(&sfull, i & 1, &abort_sh, a.status, 30));
-            tc_fence_after();
-            float D[32], O[32];
-            if (ok) tmem_ld32(tmem_at(tm, 32 * lg, 32 * s), D);
-            if (MODE == SCAN_FWD_OUT && i > 0 && ok) {
-                ok = __all_sync(0xffffffffu,
-                                mbar_wait(&ofull[(i - 1) & 1], ((i - 1) >> 1) & 1, &abort_sh, a.status, 31));
-                tc_fence_after();
-                if (ok) tmem_ld32(tmem_at(tm, 32 * lg, 64 + 32 * ((i - 1) & 1)), O);
-            }
-            tmem_wait_ld();
-#pragma unroll
-            for (int n = 0; n < 32; n++) H[n] = gC * H[n] + D[n];
-            if (i + 1 < NC) {
-                write_state_tile(sb + SS_H + ((i + 1) & 1) * 8192, d, H);
-                fence_proxy_async_smem();
-            }
-            tc_fence_before();
-            bad = bar_sync_or(1, 128, !ok || abort_sh);
-            if (bad) break;
-            if (i + 1 < NC && et == 0) mbar_arrive(&hready);
-            if (MODE == SCAN_FWD_OUT && i > 0 && lane < 16) {  // output rows of chunk c-1
-                const int r = 16 * lg + lane, t = kChunk * (c - 1) + r;
-                uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.o) +
-                                                      (((size_t)b * P.T + t) * P.Hv + hv) * kD + kSlice * j);
-#pragma unroll
-                for (int q = 0; q < 4; q++)
-                    dst[q] = make_uint4(pack_bf16(O[8 * q], O[8 * q + 1]), pack_bf16(O[8 * q + 2], O[8 * q + 3]),
-                                        pack_bf16(O[8 * q + 4], O[8 * q + 5]), pack_bf16(O[8 * q + 6], O[8 * q + 7]));
-            }
-        }
-        if (!bad && MODE == SCAN_FWD_OUT) {  // outputs of the last chunk
-            const int i_last = NC - 1;
-            bool ok = __all_sync(0xffffffffu,
-                                 mbar_wait(&ofull[i_last & 1], (i_last >> 1) & 1, &abort_sh, a.status, 32));
-            tc_fence_after();
-            float O[32];
-            if (ok) tmem_ld32(tmem_at(tm, 32 * lg, 64 + 32 * (i_last & 1)), O);
-            tmem_wait_ld();
-            const int r = 16 * lg + lane, t = kChunk * i_last + r;
-            if (ok && lane < 16 && t < P.T) {
-                uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(a.o) +
-                                                      (((size_t)b * P.T + t) * P.Hv + hv) * kD + kSlice * j);
-#pragma unroll
-                for (int q = 0; q < 4; q++)
-                    dst[q] = make_uint4(pack_bf16(O[8 * q], O[8 * q + 1]), pack_bf16(O[8 * q + 2], O[8 * q + 3]),
-                                        pack_bf16(O[8 * q + 4], O[8 * q + 5]), pack_bf16(O[8 * q + 6], O[8 * q + 7]));
-            }
-            bad = !ok;
-        }
-        if (!bad && a.hfinal) {
-#pragma unroll
-            for (int n = 0; n < 32; n++) a.hfinal[(bh * kD + kSlice * j + n) * kD + d] = H[n];
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (abort_sh && tid == 0 && last_loaded >= 0) {  // copies still in flight must land first
-        volatile int never = 0;
-        for (int i = last_loaded >= NS - 1 ? last_loaded - (NS - 1) : 0; i <= last_loaded; i++)
-            mbar_wait(&full[i % NS], (i / NS) & 1, &never, nullptr, 0);
-    }
-    __syncthreads();
-    if (warp == 0) tmem_dealloc(tm, 128);
-}
-
-cudaError_t launch_scan(const ScanArgs& a, int mode, const CUtensorMap* mdo, cudaStream_t s) {
-    // the attribute always allows the full ring; a launch asks for what its chunk count uses
-    const int smem_max = (mode == SCAN_FWD_OUT ? ScanLayout<SCAN_FWD_OUT>::BYTES : ScanLayout<SCAN_BWD>::BYTES) + 1024;
-    const int smem = (mode == SCAN_FWD_OUT ? ScanLayout<SCAN_FWD_OUT>::ss_h(a.p.NC) : ScanLayout<SCAN_BWD>::ss_h(a.p.NC)) +
-                     16384 + 1024;
-    dim3 grid(kSlices, a.p.Hv, a.p.B);
-    CUtensorMap dummy;
-    memset(&dummy, 0, sizeof(dummy));
-    const CUtensorMap& m = mdo ? *mdo : dummy;
-    cudaError_t e;
-    switch (mode) {
-        case SCAN_FWD_OUT:
-            e = cudaFuncSetAttribute(scan_kernel<SCAN_FWD_OUT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
-            if (e != cudaSuccess) return e;
-            trace_begin("chunk_scan_fwd", s);
-            scan_kernel<SCAN_FWD_OUT><<<grid, 192, smem, s>>>(m, a);
-            trace_end(s);
-            break;
-        case SCAN_FWD_STATES:
-            e = cudaFuncSetAttribute(scan_kernel<SCAN_FWD_STATES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     smem_max);
-            if (e != cudaSuccess) return e;
-            trace_begin("chunk_scan_states", s);
-            scan_kernel<SCAN_FWD_STATES><<<grid, 192, smem, s>>>(m, a);
-            trace_end(s);
-            break;
-        default:
-            e = cudaFuncSetAttribute(scan_kernel<SCAN_BWD>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
-            if (e != cudaSuccess) return e;
-            trace_begin("chunk_scan_bwd", s);
-            scan_kernel<SCAN_BWD><<<grid, 192, smem, s>>>(m, a);
-            trace_end(s);
-            break;
-    }
     return cudaGetLastError();
 }
 

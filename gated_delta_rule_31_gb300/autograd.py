@@ -11,9 +11,9 @@ kept for the backward — the point of "fold q/k L2-norm into the gated_delta_ru
 (Megatron-LM PR #5396, "What" / "Why"). The VJP is the chunked backward of "Adding VJP for
 gated delta net" (MLX PR #4565).
 
-bf16 q/k/v with Dk = Dv = 128 run the chunked forward and the chunked VJP (scalar or
+bf16 q/k/v (Dk, Dv in {32, 64, 128}) run the chunked forward and the chunked VJP (scalar or
 per-channel gate);
-every other problem (fp32, other head sizes) uses the token-by-token kernels
+fp32 problems use the token-by-token kernels
 (gdr_fwd_sequential / gdr_bwd_sequential), keeping h0 for the backward. The only torch operations here
 are argument marshalling: a zero ``do`` when the output is unused, contiguity, and casting
 the fp32 gradients of q/k/v to their bf16 dtype.
@@ -28,7 +28,7 @@ __all__ = ["gated_delta_rule", "GatedDeltaRuleFunction"]
 
 
 def _chunked_ok(q, v):
-    return q.dtype == torch.bfloat16 and q.shape[-1] == 128 and v.shape[-1] == 128
+    return q.dtype == torch.bfloat16 and q.shape[-1] in (32, 64, 128) and v.shape[-1] in (32, 64, 128)
 
 
 class GatedDeltaRuleFunction(torch.autograd.Function):

@@ -62,10 +62,56 @@ gdr_status check_ptrs(const gdr_problem* p, std::initializer_list<const void*> r
     return GDR_OK;
 }
 
-// The tensor-core chunked path: bf16, Dk = Dv = 128; scalar or per-channel gate.
+// The tensor-core chunked path: bf16 q/k/v, Dk and Dv in {32, 64, 128}; scalar or per-channel gate.
 gdr_status check_chunked_support(const gdr_problem* p) {
-    if (p->dtype != GDR_BF16 || p->Dk != 128 || p->Dv != 128) return GDR_ERR_UNSUPPORTED;
+    if (p->dtype != GDR_BF16) return GDR_ERR_UNSUPPORTED;
     return GDR_OK;
+}
+
+// Head sizes below 128 on the chunked path: the kernels work on 128 key and value channels, so
+// the inputs are copied into zero-padded 128-wide buffers in the workspace (after the padded
+// problem's own workspace) and the results cropped back into the caller's tensors. Zero channels
+// and zero state rows / columns contribute nothing, so the original channels are exact.
+bool narrow(const gdr_problem* p) { return p->Dk != 128 || p->Dv != 128; }
+
+struct Staging {
+    size_t q, k, v, g, h0, o, ht, do_, dht, dq, dk, dv, dg, dh0, total;
+};
+Staging staging(const gdr_problem* p, bool bwd, size_t base) {
+    Staging s;
+    memset(&s, 0, sizeof(s));
+    const size_t tk = (size_t)p->B * p->T * p->Hk * 128, tv = (size_t)p->B * p->T * p->Hv * 128;
+    const size_t st = (size_t)p->B * p->Hv * 128 * 128;
+    const bool ch = p->gate == GDR_GATE_CHANNEL;
+    size_t off = round_up(base, 256);
+    auto take = [&](size_t bytes) {
+        const size_t r = off;
+        off = round_up(off + bytes, 256);
+        return r;
+    };
+    s.q = take(tk * 2);
+    s.k = take(tk * 2);
+    s.v = take(tv * 2);
+    if (ch) s.g = take(tv * 4);
+    s.h0 = take(st * 4);
+    if (bwd) {
+        s.do_ = take(tv * 2);
+        s.dht = take(st * 4);
+        s.dq = take(tk * 4);
+        s.dk = take(tk * 4);
+        s.dv = take(tv * 4);
+        if (ch) s.dg = take(tv * 4);
+        s.dh0 = take(st * 4);
+    } else {
+        s.o = take(tv * 2);
+        s.ht = take(st * 4);
+    }
+    s.total = off;
+    return s;
+}
+// Workspace bytes of a chunked call whose padded problem needs `core`.
+size_t with_staging(const gdr_problem* p, bool bwd, size_t core) {
+    return narrow(p) ? staging(p, bwd, core).total : core;
 }
 
 RecurrentArgs recurrent_args(const gdr_problem* p, const void* q, const void* k, const void* v, const float* g,
@@ -164,12 +210,12 @@ const char* gdr_status_string(gdr_status s) {
 
 size_t gdr_fwd_chunked_workspace(const gdr_problem* p) {
     if (check_problem(p, false) != GDR_OK || check_chunked_support(p) != GDR_OK) return 0;
-    return chunk_fwd_workspace(chunk_problem(p));
+    return with_staging(p, false, chunk_fwd_workspace(chunk_problem(p)));
 }
 
 size_t gdr_bwd_chunked_workspace(const gdr_problem* p) {
     if (check_problem(p, false) != GDR_OK || check_chunked_support(p) != GDR_OK) return 0;
-    return chunk_bwd_workspace(chunk_problem(p));
+    return with_staging(p, true, chunk_bwd_workspace(chunk_problem(p)));
 }
 
 gdr_status gdr_fwd_sequential(const gdr_problem* p, const void* q, const void* k, const void* v, const float* g,
@@ -199,7 +245,7 @@ size_t gdr_chunk_states_bytes(const gdr_problem* p) {
 
 size_t gdr_bwd_chunked_states_workspace(const gdr_problem* p) {
     if (check_problem(p, false) != GDR_OK || check_chunked_support(p) != GDR_OK) return 0;
-    return chunk_bwd_states_workspace(chunk_problem(p));
+    return with_staging(p, true, chunk_bwd_states_workspace(chunk_problem(p)));
 }
 
 static gdr_status fwd_chunked_impl(const gdr_problem* p, const void* q, const void* k, const void* v,
@@ -232,12 +278,12 @@ size_t gdr_chunk_saved_bytes(const gdr_problem* p) {
 
 size_t gdr_fwd_chunked_saved_workspace(const gdr_problem* p) {
     if (check_problem(p, false) != GDR_OK || check_chunked_support(p) != GDR_OK) return 0;
-    return kSavedFwdWorkspace;
+    return with_staging(p, false, kSavedFwdWorkspace);
 }
 
 size_t gdr_bwd_chunked_saved_workspace(const gdr_problem* p) {
     if (check_problem(p, false) != GDR_OK || check_chunked_support(p) != GDR_OK) return 0;
-    return chunk_bwd_saved_workspace(chunk_problem(p));
+    return with_staging(p, true, chunk_bwd_saved_workspace(chunk_problem(p)));
 }
 
 gdr_status gdr_fwd_chunked_saved(const gdr_problem* p, const void* q, const void* k, const void* v,
@@ -259,7 +305,8 @@ static gdr_status fwd_chunked_impl(const gdr_problem* p, const void* q, const vo
     if (s != GDR_OK) return s;
     if ((s = check_ptrs(p, {q, k, v, g, beta, o}, {h0, ht})) != GDR_OK) return s;
     if ((s = check_chunked_support(p)) != GDR_OK) return s;
-    const size_t need = saved ? kSavedFwdWorkspace : chunk_fwd_workspace(chunk_problem(p));
+    const size_t core = saved ? kSavedFwdWorkspace : chunk_fwd_workspace(chunk_problem(p));
+    const size_t need = with_staging(p, false, core);
     if (!ws || ws_bytes < need) return GDR_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return GDR_ERR_INVALID_ARG;
     if (p->B == 0) return GDR_OK;
@@ -276,7 +323,29 @@ static gdr_status fwd_chunked_impl(const gdr_problem* p, const void* q, const vo
     a.states = states;
     a.saved = saved;
     a.ws = ws;
-    return launch_chunk_fwd(a, st) == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+    if (!narrow(p)) return launch_chunk_fwd(a, st) == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+    // head sizes below 128: zero-padded copies in, cropped results out
+    const Staging sg = staging(p, false, core);
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    const size_t tk = (size_t)p->B * p->T * p->Hk, tv = (size_t)p->B * p->T * p->Hv, bh = (size_t)p->B * p->Hv;
+    const bool ch = p->gate == GDR_GATE_CHANNEL;
+    cudaError_t e = cudaSuccess;
+    auto ok = [&](cudaError_t r) { if (e == cudaSuccess) e = r; };
+    ok(launch_pad(q, w + sg.q, 2, tk, 1, p->Dk, 1, 128, st));
+    ok(launch_pad(k, w + sg.k, 2, tk, 1, p->Dk, 1, 128, st));
+    ok(launch_pad(v, w + sg.v, 2, tv, 1, p->Dv, 1, 128, st));
+    if (ch) ok(launch_pad(g, w + sg.g, 4, tv, 1, p->Dk, 1, 128, st));
+    if (h0) ok(launch_pad(h0, w + sg.h0, 4, bh, p->Dv, p->Dk, 128, 128, st));
+    if (e != cudaSuccess) return GDR_ERR_CUDA;
+    a.q = w + sg.q; a.k = w + sg.k; a.v = w + sg.v;
+    a.g = ch ? reinterpret_cast<const float*>(w + sg.g) : g;
+    a.h0 = h0 ? reinterpret_cast<const float*>(w + sg.h0) : nullptr;
+    a.o = w + sg.o;
+    a.ht = ht ? reinterpret_cast<float*>(w + sg.ht) : nullptr;
+    if (launch_chunk_fwd(a, st) != cudaSuccess) return GDR_ERR_CUDA;
+    ok(launch_crop(w + sg.o, o, 2, tv, 1, 128, 1, p->Dv, st));
+    if (ht) ok(launch_crop(w + sg.ht, ht, 4, bh, 128, 128, p->Dv, p->Dk, st));
+    return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
 }
 
 static gdr_status bwd_chunked_impl(const gdr_problem* p, const void* q, const void* k, const void* v,
@@ -331,9 +400,10 @@ static gdr_status bwd_chunked_impl(const gdr_problem* p, const void* q, const vo
     if ((s = check_ptrs(p, {q, k, v, g, beta, do_, dq, dk, dv, dg, dbeta}, {h0, dht, dh0})) != GDR_OK) return s;
     if ((s = check_chunked_support(p)) != GDR_OK) return s;
     const ChunkProblem cp = chunk_problem(p);
-    const size_t need = saved    ? chunk_bwd_saved_workspace(cp)
+    const size_t core = saved    ? chunk_bwd_saved_workspace(cp)
                         : states ? chunk_bwd_states_workspace(cp)
                                  : chunk_bwd_workspace(cp);
+    const size_t need = with_staging(p, true, core);
     if (!ws || ws_bytes < need) return GDR_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return GDR_ERR_INVALID_ARG;
     if (p->B == 0) return GDR_OK;
@@ -353,7 +423,38 @@ static gdr_status bwd_chunked_impl(const gdr_problem* p, const void* q, const vo
     a.states = states;
     a.saved = saved;
     a.ws = ws;
-    return launch_chunk_bwd(a, st) == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+    if (!narrow(p)) return launch_chunk_bwd(a, st) == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+    // head sizes below 128: zero-padded copies in, cropped gradients out
+    const Staging sg = staging(p, true, core);
+    uint8_t* w = static_cast<uint8_t*>(ws);
+    const size_t tk = (size_t)p->B * p->T * p->Hk, tv = (size_t)p->B * p->T * p->Hv, bh = (size_t)p->B * p->Hv;
+    const bool ch = p->gate == GDR_GATE_CHANNEL;
+    cudaError_t e = cudaSuccess;
+    auto ok = [&](cudaError_t r) { if (e == cudaSuccess) e = r; };
+    ok(launch_pad(q, w + sg.q, 2, tk, 1, p->Dk, 1, 128, st));
+    ok(launch_pad(k, w + sg.k, 2, tk, 1, p->Dk, 1, 128, st));
+    ok(launch_pad(v, w + sg.v, 2, tv, 1, p->Dv, 1, 128, st));
+    ok(launch_pad(do_, w + sg.do_, 2, tv, 1, p->Dv, 1, 128, st));
+    if (ch) ok(launch_pad(g, w + sg.g, 4, tv, 1, p->Dk, 1, 128, st));
+    if (h0) ok(launch_pad(h0, w + sg.h0, 4, bh, p->Dv, p->Dk, 128, 128, st));
+    if (dht) ok(launch_pad(dht, w + sg.dht, 4, bh, p->Dv, p->Dk, 128, 128, st));
+    if (e != cudaSuccess) return GDR_ERR_CUDA;
+    a.q = w + sg.q; a.k = w + sg.k; a.v = w + sg.v; a.do_ = w + sg.do_;
+    a.g = ch ? reinterpret_cast<const float*>(w + sg.g) : g;
+    a.h0 = h0 ? reinterpret_cast<const float*>(w + sg.h0) : nullptr;
+    a.dht = dht ? reinterpret_cast<const float*>(w + sg.dht) : nullptr;
+    a.dq = reinterpret_cast<float*>(w + sg.dq);
+    a.dk = reinterpret_cast<float*>(w + sg.dk);
+    a.dv = reinterpret_cast<float*>(w + sg.dv);
+    a.dg = ch ? reinterpret_cast<float*>(w + sg.dg) : dg;
+    a.dh0 = dh0 ? reinterpret_cast<float*>(w + sg.dh0) : nullptr;
+    if (launch_chunk_bwd(a, st) != cudaSuccess) return GDR_ERR_CUDA;
+    ok(launch_crop(w + sg.dq, dq, 4, tk, 1, 128, 1, p->Dk, st));
+    ok(launch_crop(w + sg.dk, dk, 4, tk, 1, 128, 1, p->Dk, st));
+    ok(launch_crop(w + sg.dv, dv, 4, tv, 1, 128, 1, p->Dv, st));
+    if (ch) ok(launch_crop(w + sg.dg, dg, 4, tv, 1, 128, 1, p->Dk, st));
+    if (dh0) ok(launch_crop(w + sg.dh0, dh0, 4, bh, 128, 128, p->Dv, p->Dk, st));
+    return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
 }
 
 size_t gdr_bwd_sequential_workspace(const gdr_problem* p) {

@@ -74,7 +74,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
     const uint32_t sb = smem_u32(sm);
-    __shared__ uint64_t bar_ld, bar_mma, bar_h;
+    __shared__ uint64_t bar_ld, bar_mma, bar_h, bar_h2;
     __shared__ uint32_t tmem_sh;
     __shared__ int abort_sh;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -85,7 +85,6 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
     const int r = 16 * lg + (lane & 15);
     const bool act = lane < 16;
     int c = 0, hk = 0, b = 0, t0 = 0;  // the current tile
-    bool rowvalid = false;
     const int c32 = 32 * qt, c16 = 16 * qt;  // this thread's columns of N=128 / N=64 products
 
     // k/q and the GF / ZS scratch swap their two 32 KB regions from tile to tile, so the next
@@ -107,14 +106,15 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
     float* hdh = red + 272;                             // <dH1, H0>
     float* gst = hdh + 4;                               // [2][64] the next value head's g, beta (cp.async)
 
-    uint32_t ld_phase = 0, mma_phase = 0, h_phase = 0;
-    bool pend_ld = false, pend_h = false;  // copies issued and not yet waited for (thread 0)
-    bool h_open = false;  // pieces of the next head issued before its arriving piece (thread 0)
+    uint32_t ld_phase = 0, mma_phase = 0, h_phase = 0, h2_phase = 0;
+    bool pend_ld = false, pend_h = false, pend_h2 = false;  // copies issued and not yet waited for (thread 0)
+    bool h_open = false, h2_open = false;  // pieces issued before the arriving piece of their barrier (thread 0)
     if (tid == 0) {
         abort_sh = 0;
         mbar_init(&bar_ld, 1);
         mbar_init(&bar_mma, 1);
         mbar_init(&bar_h, 1);
+        mbar_init(&bar_h2, 1);
         fence_barrier_init();
     }
     if (warp == 0) {
@@ -156,17 +156,19 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
                    id64x128_mm = idesc_bf16(64, 128, 1, 1), id64x64_kk = idesc_bf16(64, 64, 0, 0),
                    id64x64_mm = idesc_bf16(64, 64, 1, 1);
 
-    // Inputs of value head hv, issued in pieces as their buffers free up (thread 0 only):
-    // piece 0: P, W, dO   1: Kbar   2: H0   3: T (the arrival, always issued last)   4: v   5: dH1
+    // Inputs of value head hv, issued in pieces as their buffers free up (thread 0 only). Those of the
+    // first products complete bar_h: piece 0: P, W, dO   5: dH1   1: Kbar   2: H0 (issued last: it
+    // arrives, so the phase ends when all four have landed). T and v, first read by M4, complete
+    // bar_h2: piece 4: v   3: T (issued last, arrives); their latency stays off the head's start.
     auto load_piece = [&](int bb, int cc, int hv, int piece) {
         const size_t bh = (size_t)bb * P.Hv + hv;
         const size_t idx = bh * P.NC + cc;
         const int tt = cc * kChunk;
         const uint8_t* rec = a.rec + idx * REC_BYTES;
         const uint8_t* rec2 = a.rec2 + idx * REC2_BYTES;
-        h_open = piece != 3;
         switch (piece) {
             case 0:
+                h_open = true;
                 mbar_add_tx(&bar_h, 8192 + 16384 + 2 * 8192);
                 bulk_load(sm + G_P, rec + REC_P, 8192, &bar_h);
                 bulk_load(sm + G_W, rec2 + REC2_W, 16384, &bar_h);
@@ -174,24 +176,30 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
                 tma_load_4d(sm + G_DO + 8192, &mdo, 64, hv, tt, bb, &bar_h);
                 break;
             case 1:
+                h_open = true;
                 mbar_add_tx(&bar_h, 16384);
                 bulk_load(sm + G_KB, rec + REC_K, 16384, &bar_h);
                 break;
             case 2:
-                mbar_add_tx(&bar_h, 32768);
+                h_open = false;
+                pend_h = true;
+                mbar_expect_tx(&bar_h, 32768);
                 bulk_load(sm + G_H0, a.hs + idx * STATE_IMG, 32768, &bar_h);
                 break;
-            case 3:  // issued last: arrives, so the head's phase completes when every piece has landed
-                mbar_expect_tx(&bar_h, 8192);
-                bulk_load(sm + G_T, rec2 + REC2_T, 8192, &bar_h);
-                pend_h = true;
+            case 3:
+                h2_open = false;
+                pend_h2 = true;
+                mbar_expect_tx(&bar_h2, 8192);
+                bulk_load(sm + G_T, rec2 + REC2_T, 8192, &bar_h2);
                 break;
             case 4:
-                mbar_add_tx(&bar_h, 2 * 8192);
-                tma_load_4d(sm + G_V + 0, &mv, 0, hv, tt, bb, &bar_h);
-                tma_load_4d(sm + G_V + 8192, &mv, 64, hv, tt, bb, &bar_h);
+                h2_open = true;
+                mbar_add_tx(&bar_h2, 2 * 8192);
+                tma_load_4d(sm + G_V + 0, &mv, 0, hv, tt, bb, &bar_h2);
+                tma_load_4d(sm + G_V + 8192, &mv, 64, hv, tt, bb, &bar_h2);
                 break;
             default:
+                h_open = true;
                 mbar_add_tx(&bar_h, 32768);
                 bulk_load(sm + G_DH, a.dhs + idx * STATE_IMG, 32768, &bar_h);
                 break;
@@ -225,14 +233,13 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
         const int t = blockIdx.x;
         const int cc = t % P.NC, hh = (t / P.NC) % P.Hk, bb = t / (P.NC * P.Hk);
         issue_kq(bb, cc, hh, kq);
-        for (int piece : {0, 1, 2, 4, 5, 3}) load_piece(bb, cc, hh * G, piece);  // first value head (T last)
+        for (int piece : {0, 5, 1, 2, 4, 3}) load_piece(bb, cc, hh * G, piece);  // first value head
     }
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
     c = tile % P.NC;
     hk = (tile / P.NC) % P.Hk;
     b = tile / (P.NC * P.Hk);
     t0 = c * kChunk;
-    rowvalid = act && (t0 + r < P.T);
     const int ntile = tile + (int)gridDim.x;  // the next tile of this CTA
     const int nc = ntile % P.NC, nhk = (ntile / P.NC) % P.Hk, nb = ntile / (P.NC * P.Hk);
     if (!wait_ld(40)) goto teardown;
@@ -515,6 +522,12 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
         sync_for_mma();
 
         // ------------------------------------------------------------ M4: dT parts, T^T dU
+        {  // T and v of this head
+            bool okh = mbar_wait(&bar_h2, h2_phase, &abort_sh, a.status, 50);
+            h2_phase ^= 1;
+            if (okh) pend_h2 = false;
+            if (__syncthreads_or(!okh)) goto teardown;
+        }
         if (tid == 0) {
             tc_fence_after();
             for (int k0 = 0; k0 < kD; k0 += 16) {
@@ -743,35 +756,39 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
     }
 
     // ---------------------------------------------------------------- dq, dk: norm backward
-    {
-        float x[32], xx[32];
+    {  // lane l < 16 takes columns c32 .. c32 + 15 of row r, lane l + 16 the next 16 (64 bytes each)
+        const int hf = lane >> 4;
+        const bool rv = t0 + r < P.T;
+        float x[32], w[16], xx[16];
 #pragma unroll 1
         for (int which = 0; which < 2; which++) {  // 0: q, 1: k
             const float* rho = which == 0 ? rq : rk;
             const int krow = which == 0 ? 64 + r : r;
             tmem_ld32(tl + (which == 0 ? TM_DQ : TM_DK) + c32, x);
             tmem_wait_ld();
+            split_cols<32>(x, w, lane);
             float dot = 0.f;
 #pragma unroll
-            for (int q = 0; q < 4; q++) {
-                ldrow8(kq, krow, 4 * qt + q, 128, xx + 8 * q);
+            for (int q = 0; q < 2; q++) {
+                ldrow8(kq, krow, 4 * qt + 2 * hf + q, 128, xx + 8 * q);
 #pragma unroll
-                for (int e = 0; e < 8; e++) dot += xx[8 * q + e] * x[8 * q + e];
+                for (int e = 0; e < 8; e++) dot += xx[8 * q + e] * w[8 * q + e];
             }
+            dot += __shfl_xor_sync(0xffffffffu, dot, 16);
             if (act) part[qt * 64 + r] = dot;
             __syncthreads();
-            if (rowvalid) {
+            if (rv) {
                 const float rr = rho[r];
                 const float full = part[r] + part[64 + r] + part[128 + r] + part[192 + r];
-                float* dst = (which == 0 ? a.dq : a.dk) + (((size_t)b * P.T + t0 + r) * P.Hk + hk) * kD + c32;
+                float* dst = (which == 0 ? a.dq : a.dk) + (((size_t)b * P.T + t0 + r) * P.Hk + hk) * kD + c32 + 16 * hf;
                 float4* d4 = reinterpret_cast<float4*>(dst);
 #pragma unroll
-                for (int q = 0; q < 8; q++) {
+                for (int q = 0; q < 4; q++) {
                     float o4[4];
 #pragma unroll
                     for (int e = 0; e < 4; e++) {
                         const int i = 4 * q + e;
-                        o4[e] = P.use_norm ? rr * (x[i] - rr * xx[i] * rr * full) : x[i];
+                        o4[e] = P.use_norm ? rr * (w[i] - rr * xx[i] * rr * full) : w[i];
                     }
                     d4[q] = make_float4(o4[0], o4[1], o4[2], o4[3]);
                 }
@@ -800,7 +817,12 @@ teardown:
             mbar_arrive(&bar_h);
             pend_h = true;
         }
+        if (h2_open) {
+            mbar_arrive(&bar_h2);
+            pend_h2 = true;
+        }
         if (pend_h) mbar_wait(&bar_h, h_phase, &never, nullptr, 0);
+        if (pend_h2) mbar_wait(&bar_h2, h2_phase, &never, nullptr, 0);
         mbar_wait(&bar_mma, mma_phase, &never, nullptr, 0);
     }
     __syncthreads();

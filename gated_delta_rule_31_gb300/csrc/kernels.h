@@ -34,6 +34,13 @@ cudaError_t launch_seq_bwd(SeqBwdArgs a, void* ws, cudaStream_t s);
 // value heads of each key head, then the L2-norm backward (bf16 q, k; Dk = 128; dg untouched).
 cudaError_t launch_qk_norm_backward(const SeqBwdArgs& a, cudaStream_t s);
 
+// Staging copies (pad.cu): [outer][rs][cs] -> [outer][rd][cd] with zero fill (pad), or the
+// [outer][rd][cd] corner of an [outer][rs][cs] tensor (crop); elements of 2 or 4 bytes.
+cudaError_t launch_pad(const void* src, void* dst, int elem_bytes, size_t outer, int rs, int cs, int rd, int cd,
+                       cudaStream_t s);
+cudaError_t launch_crop(const void* src, void* dst, int elem_bytes, size_t outer, int rs, int cs, int rd, int cd,
+                        cudaStream_t s);
+
 // Launch tracing (api.cu): no-ops unless gdr_trace_enable(1) was called.
 void trace_begin(const char* name, cudaStream_t s);
 void trace_end(cudaStream_t s);

@@ -85,11 +85,26 @@ def test_decode_requires_single_token(L):
 
 
 def test_chunked_support_matrix_and_workspace(L):
-    for kw in (dict(dtype=0), dict(Dk=64, Dv=64)):
+    # fp32 q/k/v: not on the tensor-core chunked path (the token-by-token calls take them)
+    for kw in (dict(dtype=0), dict(dtype=0, Dk=64, Dv=64)):
         p = prob(**kw)
         assert L.gdr_fwd_chunked_workspace(ctypes.byref(p)) == 0
+        assert L.gdr_bwd_chunked_workspace(ctypes.byref(p)) == 0
         assert L.gdr_fwd_chunked(ctypes.byref(p), *[FAKE] * 8, FAKE, 1 << 30, None) == UNSUPPORTED
         assert L.gdr_bwd_chunked(ctypes.byref(p), *[FAKE] * 14, FAKE, 1 << 30, None) == UNSUPPORTED
+    # bf16 head sizes 32 and 64: the workspace adds the zero-padded 128-wide copies of the inputs and
+    # outputs; the saved-state and saved-operator buffers keep the 128-wide layout
+    wide = prob()
+    for dk, dv in ((32, 32), (64, 64), (64, 128), (128, 32)):
+        p = prob(Dk=dk, Dv=dv)
+        for q in ("gdr_fwd_chunked_workspace", "gdr_bwd_chunked_workspace", "gdr_bwd_chunked_states_workspace",
+                  "gdr_fwd_chunked_saved_workspace", "gdr_bwd_chunked_saved_workspace"):
+            assert getattr(L, q)(ctypes.byref(p)) > getattr(L, q)(ctypes.byref(wide)), (dk, dv, q)
+        assert L.gdr_chunk_states_bytes(ctypes.byref(p)) == L.gdr_chunk_states_bytes(ctypes.byref(wide))
+        assert L.gdr_chunk_saved_bytes(ctypes.byref(p)) == L.gdr_chunk_saved_bytes(ctypes.byref(wide))
+        # a workspace one byte short is refused before any launch
+        need = L.gdr_fwd_chunked_workspace(ctypes.byref(p))
+        assert L.gdr_fwd_chunked(ctypes.byref(p), *[FAKE] * 8, FAKE, need - 1, None) == WORKSPACE
     # per-channel gate: chunked forward, both handoffs and the VJP (Gamma_C per key channel, 16 KB
     # more of T/W/K.*Gamma per chunk and the backward's per-channel exports: larger buffers)
     pc, ps = prob(gate=1), prob()
@@ -224,8 +239,8 @@ def test_noalloc_forward_validation(L):
     P = ctypes.c_void_p
     L.gdr_fwd_chunked_noalloc.argtypes = [ctypes.POINTER(Problem)] + [P] * 8 + [P]
     L.gdr_fwd_chunked_noalloc.restype = ctypes.c_int
-    for kw, code in ((dict(Hv=3), INVALID), (dict(dtype=0), UNSUPPORTED), (dict(Dk=64), UNSUPPORTED),
-                     (dict(T=4096, Hk=16, Hv=32), WORKSPACE)):
+    for kw, code in ((dict(Hv=3), INVALID), (dict(dtype=0), UNSUPPORTED), (dict(Dk=64, dtype=0), UNSUPPORTED),
+                     (dict(T=4096, Hk=16, Hv=32), WORKSPACE), (dict(T=2048, Hk=16, Hv=32, Dk=64), WORKSPACE)):
         assert L.gdr_fwd_chunked_noalloc(ctypes.byref(prob(**kw)), *[FAKE] * 8, None) == code, kw
     assert L.gdr_fwd_chunked_workspace(ctypes.byref(prob(T=4096, Hk=16, Hv=32))) > 64 * 1024 * 1024
     assert L.gdr_fwd_chunked_noalloc(None, *[FAKE] * 8, None) == INVALID

@@ -36,6 +36,11 @@ constexpr uint32_t PS_SMALL = PS_SCR + SOLVE_SCRATCH_BYTES;  // per-token factor
 constexpr uint32_t PS_GST = PS_SMALL + 2048;  // next value head's gates g, beta (2 x 64 fp32), cp.async
 constexpr uint32_t PS_BYTES = PS_GST + 512;
 constexpr uint32_t PS_TT = PS_A, PS_WBAR = PS_A, PS_W = PS_T;
+// After the last products of a value head, A, T, P and the solve scratch are dead: the Mneg and Qc
+// images are staged there and leave by two bulk copies (a thread's 16-byte stores into the record
+// would touch one 128-byte line each).
+constexpr uint32_t PS_STAGE = PS_A, PS_STAGE_Q = PS_STAGE + 32768;
+static_assert(PS_STAGE_Q + 16384 <= PS_SMALL, "staging below the small arrays");
 static_assert(PS_A % 1024 == 0 && PS_T % 1024 == 0 && PS_P % 1024 == 0, "align");
 static_assert(PS_A + 64 * LDA * 4 <= PS_T && PS_T + 64 * LDA * 4 <= PS_P, "fp32 tiles");
 static_assert(2 * (PS_BYTES + 1024) <= 228 * 1024, "two prep CTAs per SM");
@@ -178,6 +183,7 @@ __global__ void __launch_bounds__(256, 2)
 
             ok = mbar_wait(&bar_mma, mph, &abort_sh, a.status, 11);
             mph ^= 1;
+            if (tid == 0) bulk_wait_read_all();  // the previous head's staged images are read
             if (__syncthreads_or(!ok)) goto teardown;
             tc_fence_after();
             {  // A = strict_lower(beta_i rho_i rho_j E_ij G_ij) in fp32;  P = scale tril(rho rho E S) in bf16
@@ -215,12 +221,16 @@ __global__ void __launch_bounds__(256, 2)
                         const uint4 u = pack8(v + 8 * q, 1.f);
                         const uint32_t off = sw128_chunk(i, 4 * h + q, 64);
                         st_shared_v4(sb + PS_P + off, u.x, u.y, u.z, u.w);
-                        st_global16(rec + REC_P + off, u);
                     }
+                    fence_proxy_async_smem();  // the P image leaves by a bulk copy
                 }
             }
             tc_fence_before();
             __syncthreads();
+            if (tid == 0) {
+                bulk_store(rec + REC_P, sm + PS_P, 8192);
+                bulk_commit();
+            }
 
             ut_solve(Am, Tm, Xs, tid);  // T = (I + A)^-1
             {  // [Tw; Tu] with Tw = T diag(beta Gamma rho_k), Tu = T diag(beta): K-major A operand (over A).
@@ -299,7 +309,6 @@ __global__ void __launch_bounds__(256, 2)
                             const uint4 u = pack8(w + 8 * q, 1.f);
                             const uint32_t off = sw128_chunk(i, 8 * h + 4 * hh2 + q, 64);
                             st_shared_v4(sb + PS_W + off, u.x, u.y, u.z, u.w);
-                            if (rec2) st_global16(rec2 + REC2_W + off, u);
                             st_chunk(sb + PS_WBAR + off, w + 8 * q, sbar);
                         }
                     }
@@ -341,6 +350,10 @@ __global__ void __launch_bounds__(256, 2)
 
             // Mneg = -K^T Wbar (M=128: A = k tile read MN-major) and P W (M=64)
             if (tid == 0) {
+                if (rec2) {  // W for the backward, from its image
+                    bulk_store(rec2 + REC2_W, sm + PS_W, 16384);
+                    bulk_commit();
+                }
                 tc_fence_after();
                 const uint32_t idm = idesc_bf16(128, 128, 1, 1);
                 for (int k0 = 0; k0 < kChunk; k0 += 16)
@@ -354,6 +367,7 @@ __global__ void __launch_bounds__(256, 2)
             }
             ok = mbar_wait(&bar_mma, mph, &abort_sh, a.status, 13);
             mph ^= 1;
+            if (tid == 0) bulk_wait_read_all();  // the P and W images are read: the staging may overwrite them
             if (__syncthreads_or(!ok)) goto teardown;
             tc_fence_after();
             {
@@ -367,7 +381,10 @@ __global__ void __launch_bounds__(256, 2)
                         tmem_wait_ld();
 #pragma unroll
                         for (int q = 0; q < 4; q++)
-                            st_global16(rec + REC_M + sw128_chunk(d, 8 * h + 4 * hh2 + q, 128), pack8(m + 8 * q, -1.f));
+                        {
+                            const uint4 u = pack8(m + 8 * q, -1.f);
+                            st_shared_v4(sb + PS_STAGE + sw128_chunk(d, 8 * h + 4 * hh2 + q, 128), u.x, u.y, u.z, u.w);
+                        }
                     }
                 }
                 {  // Qc = scale diag(Gamma rho_q) Q - P W, rows i = 16 lg + lane
@@ -397,19 +414,27 @@ __global__ void __launch_bounds__(256, 2)
                         unpack8(qv[q], x);
 #pragma unroll
                         for (int e = 0; e < 8; e++) x[e] = f * x[e] - pw[8 * q + e];
-                        st_global16(rec + REC_Q + sw128_chunk(i, 8 * h + 4 * hf + q, 64), pack8(x, 1.f));
+                        const uint4 u = pack8(x, 1.f);
+                        st_shared_v4(sb + PS_STAGE_Q + sw128_chunk(i, 8 * h + 4 * hf + q, 64), u.x, u.y, u.z, u.w);
                     }
                 }
             }
             if (tid == 0) a.gam[bh * a.ncpad + c] = expf(gam[63]);
+            fence_proxy_async_smem();  // the staged images leave by bulk copies
             tc_fence_before();
             __syncthreads();  // every buffer of this value head is free again
             tc_fence_after();
+            if (tid == 0) {
+                bulk_store(rec + REC_M, sm + PS_STAGE, 32768);
+                bulk_store(rec + REC_Q, sm + PS_STAGE_Q, 16384);
+                bulk_commit();
+            }
         }  // value heads of the group
         if (tid == 0 && next < ngroups) issue_kq(next);  // k, q are no longer read
     }  // groups
 teardown:
     cp_async_wait_all();
+    if (tid == 0) bulk_wait_all();  // record stores complete
     tc_fence_before();
     __syncthreads();
     if (abort_sh && tid == 0) {  // let copies still in flight land before the CTA exits

@@ -285,11 +285,7 @@ __global__ void __launch_bounds__(256, 2)
             ok = mbar_wait(&bar_mma, mph, &abort_sh, a.status, 12);
             mph ^= 1;
             if (__syncthreads_or(!ok)) goto teardown;
-            if (tid == 0) {  // v is consumed: fetch the next value head's (or the next group's first)
-                if (hh + 1 < G) issue_v(grp, hh + 1);
-                else if (next < ngroups) issue_v(next, 0);
-            }
-            if (tid < 64) {  // and its gates
+            if (tid < 64) {  // the next value head's gates (or the next group's first)
                 if (hh + 1 < G) stage_gb(grp, hh + 1);
                 else if (next < ngroups) stage_gb(next, 0);
             }
@@ -321,8 +317,8 @@ __global__ void __launch_bounds__(256, 2)
                         tmem_wait_ld();
                         const int col = 64 * h + 32 * hh2;  // one 32-column U~ slice
 #pragma unroll
-                        for (int q = 0; q < 4; q++)
-                            st_global16(rec + REC_U + (col >> 5) * 4096 + sw64_chunk(i, q), pack8(u + 8 * q, 1.f));
+                        for (int q = 0; q < 4; q++)  // the record's slice image, staged over v (read)
+                            st_chunk(sb + PS_V + (col >> 5) * 4096 + sw64_chunk(i, q), u + 8 * q, 1.f);
                     }
                 }
                 // Kbar = diag(exp(gamma_C - gamma) rho_k) K, straight to the record
@@ -349,11 +345,10 @@ __global__ void __launch_bounds__(256, 2)
             __syncthreads();
 
             // Mneg = -K^T Wbar (M=128: A = k tile read MN-major) and P W (M=64)
-            if (tid == 0) {
-                if (rec2) {  // W for the backward, from its image
-                    bulk_store(rec2 + REC2_W, sm + PS_W, 16384);
-                    bulk_commit();
-                }
+            if (tid == 0) {  // U~ (and W for the backward) to the record, from their images
+                bulk_store(rec + REC_U, sm + PS_V, 16384);
+                if (rec2) bulk_store(rec2 + REC2_W, sm + PS_W, 16384);
+                bulk_commit();
                 tc_fence_after();
                 const uint32_t idm = idesc_bf16(128, 128, 1, 1);
                 for (int k0 = 0; k0 < kChunk; k0 += 16)
@@ -367,7 +362,11 @@ __global__ void __launch_bounds__(256, 2)
             }
             ok = mbar_wait(&bar_mma, mph, &abort_sh, a.status, 13);
             mph ^= 1;
-            if (tid == 0) bulk_wait_read_all();  // the P and W images are read: the staging may overwrite them
+            if (tid == 0) {
+                bulk_wait_read_all();  // the P, U~ and W images are read: the staging may overwrite them,
+                if (hh + 1 < G) issue_v(grp, hh + 1);  // and the next value head's v (or the next
+                else if (next < ngroups) issue_v(next, 0);  // group's first) may land over U~
+            }
             if (__syncthreads_or(!ok)) goto teardown;
             tc_fence_after();
             {

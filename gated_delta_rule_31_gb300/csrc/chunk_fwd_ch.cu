@@ -303,6 +303,7 @@ __global__ void __launch_bounds__(PCH_THREADS, 1)
             }
         }
     }
+    fence_proxy_async_smem();  // the P image leaves by a bulk copy
     tc_fence_before();
     __syncthreads();
     if (tid == 0) {  // v into its region (R_3 is no longer read)
@@ -327,10 +328,9 @@ __global__ void __launch_bounds__(PCH_THREADS, 1)
         }
         a.gam[(bh * P.NC + c) * kD + tid] = gp[(kChunk - 1) * kD + tid];  // Gamma_C per channel
     }
-    if (tid < 256) {  // P to the record
-        const uint4 u = ld_shared_v4(sb + CS_P + tid * 32), w = ld_shared_v4(sb + CS_P + tid * 32 + 16);
-        st_global16(rec + REC_P + tid * 32, u);
-        st_global16(rec + REC_P + tid * 32 + 16, w);
+    if (tid == 0) {  // P to the record
+        bulk_store(rec + REC_P, sm + CS_P, 8192);
+        bulk_commit();
     }
     ut_solve(Am, Tm, Xs, tid);  // T = (I + A)^-1 (ends with a barrier; suffix products done)
     {  // [Tw; Tu]: Tw = T diag(beta rho_k), Tu = T diag(beta) (K-major A operand, over A)
@@ -380,12 +380,15 @@ __global__ void __launch_bounds__(PCH_THREADS, 1)
             if (rec2) st_global16(rec2 + REC2_KG + off, pack8(yg, rk));  // K^ .* Gamma
             const uint4 ub = pack8(yb, 1.f);
             st_shared_v4(sb + CS_KB + off, ub.x, ub.y, ub.z, ub.w);
-            st_global16(rec + REC_K + off, ub);
         }
     }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
+    if (tid == 0) {  // Kbar to the record, from its image
+        bulk_store(rec + REC_K, sm + CS_KB, 16384);
+        bulk_commit();
+    }
 
     // W = Tw (K .* Gamma) and U~ = Tu V as two M=128 products of [Tw; Tu] (rows 0-63 of the
     // first, rows 64-127 of the second are the wanted ones); B operands MN-major
@@ -416,11 +419,8 @@ __global__ void __launch_bounds__(PCH_THREADS, 1)
             tmem_ld32(tmem_at(tm, 32 * lg, 64 * h + 32), w + 32);
             tmem_wait_ld();
 #pragma unroll
-            for (int q = 0; q < 8; q++) {
-                st_chunk(sb + CS_T + sw128_chunk(i, 8 * h + q, 64), w + 8 * q, 1.f);
-                if (rec2) st_global16(rec2 + REC2_W + sw128_chunk(i, 8 * h + q, 64), pack8(w + 8 * q, 1.f));
-            }
-        } else {  // U~ rows i = 32 lg + lane - 64 -> record slices
+            for (int q = 0; q < 8; q++) st_chunk(sb + CS_T + sw128_chunk(i, 8 * h + q, 64), w + 8 * q, 1.f);
+        } else {  // U~ rows i = 32 lg + lane - 64 -> the record's slice images, staged over v (read)
             const int i = 32 * lg + lane - 64;
             float u[64];
             tmem_ld32(tmem_at(tm, 32 * lg, 128 + 64 * h), u);
@@ -429,13 +429,18 @@ __global__ void __launch_bounds__(PCH_THREADS, 1)
 #pragma unroll
             for (int q = 0; q < 8; q++) {
                 const int col = 64 * h + 8 * q;
-                st_global16(rec + REC_U + (col >> 5) * 4096 + sw64_chunk(i, q & 3), pack8(u + 8 * q, 1.f));
+                st_chunk(sb + CS_V + (col >> 5) * 4096 + sw64_chunk(i, q & 3), u + 8 * q, 1.f);
             }
         }
     }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
+    if (tid == 0) {  // U~ (and W for the backward) to the record, from their images
+        bulk_store(rec + REC_U, sm + CS_V, 16384);
+        if (rec2) bulk_store(rec2 + REC2_W, sm + CS_T, 16384);
+        bulk_commit();
+    }
 
     // Mneg = -Kbar^T W (M=128: A = Kbar image read MN-major) and P W (M=64)
     if (tid == 0) {
@@ -463,8 +468,7 @@ __global__ void __launch_bounds__(PCH_THREADS, 1)
             tmem_ld32(tmem_at(tm, 32 * lg, 64 * h + 32), m + 32);
             tmem_wait_ld();
 #pragma unroll
-            for (int q = 0; q < 8; q++)
-                st_global16(rec + REC_M + sw128_chunk(d, 8 * h + q, 128), pack8(m + 8 * q, -1.f));
+            for (int q = 0; q < 8; q++) st_chunk(sb + CS_AL + sw128_chunk(d, 8 * h + q, 128), m + 8 * q, -1.f);
         }
         {  // Qc = scale diag(rho_q) Q .* Gamma - P W, rows i = 16 lg + lane (M=64 layout)
             const int i = 16 * lg + (lane & 15);
@@ -487,12 +491,21 @@ __global__ void __launch_bounds__(PCH_THREADS, 1)
                     const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 #pragma unroll
                     for (int e = 0; e < 8; e++) x[e] = f * x[e] * gg[e] - pw[8 * q + e];
-                    st_global16(rec + REC_Q + sw128_chunk(i, 8 * h + q, 64), pack8(x, 1.f));
+                    st_chunk(sb + CS_A + sw128_chunk(i, 8 * h + q, 64), x, 1.f);
                 }
             }
         }
     }
+    // Mneg (over the decay products) and Qc (over [Tw; Tu]) to the record, from their images
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+        bulk_store(rec + REC_M, sm + CS_AL, 32768);
+        bulk_store(rec + REC_Q, sm + CS_A, 16384);
+        bulk_commit();
+    }
 teardown:
+    if (tid == 0) bulk_wait_all();  // record stores complete before the CTA exits
     tc_fence_before();
     __syncthreads();
     if (abort_sh && tid == 0) {  // let copies and products still in flight finish before the CTA exits

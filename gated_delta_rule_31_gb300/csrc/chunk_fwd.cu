@@ -40,6 +40,14 @@ constexpr uint32_t PS_TT = PS_A, PS_WBAR = PS_A, PS_W = PS_T;
 // images are staged there and leave by two bulk copies (a thread's 16-byte stores into the record
 // would touch one 128-byte line each).
 constexpr uint32_t PS_STAGE = PS_A, PS_STAGE_Q = PS_STAGE + 32768;
+// The intra-chunk decays E_ij = exp(gamma_i - gamma_j) (j <= i) of A and P, kept in the solve scratch
+// until the solve: inside the 16 x 16 diagonal blocks directly, ED [4][16][EDS] fp32; below them
+// factored through the start s = 16 (i / 16) of row i's block, E_ij = exp(gamma_i - gamma_s) x
+// exp(gamma_s - gamma_j), both factors at most 1 for a decay (EA [64] and EB [4][64] fp32). This
+// takes 1024 + 160 exponentials per value head instead of 8192.
+constexpr int EDS = 20;  // row stride (floats): 16-byte rows, conflict-free float4 reads
+constexpr uint32_t PS_ED = PS_SCR, PS_EA = PS_ED + 4 * 16 * EDS * 4, PS_EB = PS_EA + 64 * 4;
+static_assert(PS_EB + 4 * 64 * 4 <= PS_SCR + SOLVE_SCRATCH_BYTES, "decay tables in the solve scratch");
 static_assert(PS_STAGE_Q + 16384 <= PS_SMALL, "staging below the small arrays");
 static_assert(PS_A % 1024 == 0 && PS_T % 1024 == 0 && PS_P % 1024 == 0, "align");
 static_assert(PS_A + 64 * LDA * 4 <= PS_T && PS_T + 64 * LDA * 4 <= PS_P, "fp32 tiles");
@@ -65,6 +73,9 @@ __global__ void __launch_bounds__(256, 2)
     float* fb = fw + 64;     // exp(gamma_C - gamma) rho_k   (rows of Kbar, Wbar)
     float* fq = fb + 64;     // scale Gamma rho_q     (rows of Qc)
     float* gst = reinterpret_cast<float*>(sm + PS_GST);
+    float* ed = reinterpret_cast<float*>(sm + PS_ED);
+    float* ea = reinterpret_cast<float*>(sm + PS_EA);
+    float* eb = reinterpret_cast<float*>(sm + PS_EB);
     float* Am = reinterpret_cast<float*>(sm + PS_A);
     float* Tm = reinterpret_cast<float*>(sm + PS_T);
     float* Xs = reinterpret_cast<float*>(sm + PS_SCR);
@@ -171,7 +182,8 @@ __global__ void __launch_bounds__(256, 2)
                 ss += __shfl_xor_sync(0xffffffffu, ss, 1);
                 if (half == 0) rho[row] = P.use_norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.0f;
             }
-            __syncthreads();
+            if (tid == 0) bulk_wait_read_all();  // the previous head's staged images are read (the decay
+            __syncthreads();                     // tables below and A / P are written over them)
             if (tid >= 32 && tid < 64) gam[tid] += gam[31];
             __syncthreads();
             if (tid < 64) {
@@ -179,11 +191,20 @@ __global__ void __launch_bounds__(256, 2)
                 fw[tid] = bet[tid] * G * rho[tid];
                 fb[tid] = expf(gam[63] - gam[tid]) * rho[tid];
                 fq[tid] = P.scale * G * rho[64 + tid];
+                ea[tid] = __expf(gam[tid] - gam[tid & ~15]);
+            } else if (tid < 160) {  // exp(gamma_s - gamma_j), block starts s = 16, 32, 48 and j < s
+                const int u = tid - 64;
+                const int kb = u < 16 ? 1 : u < 48 ? 2 : 3, jj = u < 16 ? u : u < 48 ? u - 16 : u - 48;
+                eb[kb * 64 + jj] = __expf(gam[16 * kb] - gam[jj]);
+            }
+#pragma unroll
+            for (int e = 0; e < 4; e++) {  // diagonal blocks: entry (block, r, c) = exp(gamma_r - gamma_c), c <= r
+                const int idx = tid + 256 * e, bk = idx >> 8, r = (idx >> 4) & 15, cc = idx & 15;
+                ed[(bk * 16 + r) * EDS + cc] = cc <= r ? __expf(gam[16 * bk + r] - gam[16 * bk + cc]) : 0.f;
             }
 
             ok = mbar_wait(&bar_mma, mph, &abort_sh, a.status, 11);
             mph ^= 1;
-            if (tid == 0) bulk_wait_read_all();  // the previous head's staged images are read
             if (__syncthreads_or(!ok)) goto teardown;
             tc_fence_after();
             {  // A = strict_lower(beta_i rho_i rho_j E_ij G_ij) in fp32;  P = scale tril(rho rho E S) in bf16
@@ -197,17 +218,27 @@ __global__ void __launch_bounds__(256, 2)
                 const bool arow = r < 64;  // warp-uniform
                 const int i = r & 63;
                 const int lim = arow ? i : i + 1;  // A: j < i (strict), P: j <= i
-                const float gi = gam[i], ci = arow ? bet[i] * rho[i] : P.scale * rho[64 + i];
-                const float4* g4 = reinterpret_cast<const float4*>(gam + 32 * h);
+                const int bi = i >> 4;
+                const float ai = ea[i], ci = arow ? bet[i] * rho[i] : P.scale * rho[64 + i];
                 const float4* r4 = reinterpret_cast<const float4*>(rho + 32 * h);
+                const float4* b4 = reinterpret_cast<const float4*>(eb + bi * 64 + 32 * h);
+                const float4* d4 = reinterpret_cast<const float4*>(ed + (bi * 16 + (i & 15)) * EDS);
 #pragma unroll
                 for (int q = 0; q < 8; q++) {
-                    const float4 gg = g4[q], rr = r4[q];
-                    const float gj[4] = {gg.x, gg.y, gg.z, gg.w}, rj[4] = {rr.x, rr.y, rr.z, rr.w};
+                    const int j0 = 32 * h + 4 * q, bj = j0 >> 4;  // the 4 columns share a block
+                    const float4 rr = r4[q];
+                    float4 ee = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (bj < bi) {
+                        const float4 bb = b4[q];
+                        ee = make_float4(ai * bb.x, ai * bb.y, ai * bb.z, ai * bb.w);
+                    } else if (bj == bi) {
+                        ee = d4[(j0 & 15) >> 2];
+                    }
+                    const float rj[4] = {rr.x, rr.y, rr.z, rr.w}, ej[4] = {ee.x, ee.y, ee.z, ee.w};
 #pragma unroll
                     for (int e = 0; e < 4; e++) {
                         const int jj = 4 * q + e;
-                        v[jj] = (32 * h + jj < lim) ? ci * rj[e] * __expf(gi - gj[e]) * v[jj] : 0.f;
+                        v[jj] = (32 * h + jj < lim) ? ci * rj[e] * ej[e] * v[jj] : 0.f;
                     }
                 }
                 if (arow) {

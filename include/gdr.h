@@ -80,10 +80,15 @@ size_t gdr_fwd_chunked_workspace(const gdr_problem* p);
 size_t gdr_bwd_chunked_workspace(const gdr_problem* p);
 
 /* Chunked prefill forward (chunks of 64 tokens): o and, if ht != NULL, the final state.
- * h0 may be NULL (zero initial state). Implemented for dtype BF16, Dk = Dv = 128, with the
- * scalar gate or the per-channel gate (g [B,T,Hv,Dk], the channelwise variant of
- * "Two-pass optimization for channelwise gated delta rule kernel", ExecuTorch PR #21020);
- * other combinations return GDR_ERR_UNSUPPORTED. Pointers 16-byte aligned.
+ * h0 may be NULL (zero initial state). Implemented for dtype BF16 with Dk, Dv in {32, 64, 128},
+ * with the scalar gate or the per-channel gate (g [B,T,Hv,Dk], the channelwise variant of
+ * "Two-pass optimization for channelwise gated delta rule kernel", ExecuTorch PR #21020). The
+ * kernels work on 128 key and value channels: for Dk or Dv below 128 the call stages zero-padded
+ * 128-wide copies of its inputs in the workspace (which the size query includes) and crops the
+ * results; the zero channels contribute nothing, so results are those of the original sizes.
+ * dtype F32 returns GDR_ERR_UNSUPPORTED (the tensor-core path computes with bf16 operands, which
+ * cannot meet fp32 accuracy): gdr_fwd_sequential / gdr_bwd_sequential take fp32 problems.
+ * Pointers 16-byte aligned.
  * Work: per chunk a 64x64 unit-lower-triangular (UT/WY) transform of the k k^T beta
  * block on the tensor cores, then one sequential scan over chunks per (b, hv, Dv slice)
  * with the fp32 state held on chip. Clears and then sets the workspace status word. */

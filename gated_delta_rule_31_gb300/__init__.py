@@ -199,7 +199,8 @@ def fwd_sequential(q, k, v, g, beta, h0=None, scale=None, use_qk_l2norm=True, ou
 
 def fwd_chunked(q, k, v, g, beta, h0=None, scale=None, use_qk_l2norm=True, output_final_state=True,
                 workspace=None, save_states=False, save_all=False):
-    """Chunked prefill forward on the tensor cores (gdr_fwd_chunked). Returns (o, ht or None),
+    """Chunked prefill forward (gdr_fwd_chunked: bf16 on the tensor cores, fp32 on the CUDA-core
+    fp32 kernels). Returns (o, ht or None),
     or (o, ht, states) with save_states=True (gdr_fwd_chunked_states: the chunk-start states
     kept for bwd_chunked(..., states=states)), or (o, ht, saved) with save_all=True
     (gdr_fwd_chunked_saved: states and chunk operators kept for bwd_chunked(..., saved=saved))."""

@@ -12,7 +12,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libgdr.so")
-SOURCES = ["api.cu", "recurrent.cu", "recurrent_bwd.cu", "chunk_fwd.cu", "chunk_fwd_ch.cu", "chunk_bwd.cu", "chunk_bwd_ch.cu", "scan.cu", "pad.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "recurrent.cu", "recurrent_bwd.cu", "chunk_fwd.cu", "chunk_fwd_ch.cu", "chunk_bwd.cu", "chunk_bwd_ch.cu", "scan.cu", "pad.cu", "noalloc.cu", "chunk_f32.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
                 "-I", INCLUDE, "-I", CSRC]

@@ -11,43 +11,34 @@ kept for the backward — the point of "fold q/k L2-norm into the gated_delta_ru
 (Megatron-LM PR #5396, "What" / "Why"). The VJP is the chunked backward of "Adding VJP for
 gated delta net" (MLX PR #4565).
 
-bf16 q/k/v (Dk, Dv in {32, 64, 128}) run the chunked forward and the chunked VJP (scalar or
-per-channel gate);
-fp32 problems use the token-by-token kernels
-(gdr_fwd_sequential / gdr_bwd_sequential), keeping h0 for the backward. The only torch operations here
-are argument marshalling: a zero ``do`` when the output is unused, contiguity, and casting
-the fp32 gradients of q/k/v to their bf16 dtype.
+Every problem the C ABI accepts runs the chunked forward and the chunked VJP (scalar or
+per-channel gate, Dk and Dv in {32, 64, 128}): bf16 q/k/v on the tensor cores, fp32 q/k/v on
+the CUDA-core fp32 kernels of the same chunk algebra (fp32 chunk-start states, 64 KB per
+chunk and value head at D = 128). The only torch operations here are argument marshalling: a
+zero ``do`` when the output is unused, contiguity, and casting the fp32 gradients of q/k/v to
+their dtype.
 """
 from __future__ import annotations
 
 import torch
 
-from . import bwd_chunked, bwd_sequential, fwd_chunked, fwd_sequential
+from . import bwd_chunked, fwd_chunked
 
 __all__ = ["gated_delta_rule", "GatedDeltaRuleFunction"]
-
-
-def _chunked_ok(q, v):
-    return q.dtype == torch.bfloat16 and q.shape[-1] in (32, 64, 128) and v.shape[-1] in (32, 64, 128)
 
 
 class GatedDeltaRuleFunction(torch.autograd.Function):
     @staticmethod
     def forward(ctx, q, k, v, g, beta, h0, scale, use_qk_l2norm, keep_operators):
         ctx.scale, ctx.norm, ctx.has_h0 = scale, bool(use_qk_l2norm), h0 is not None
-        fwd_chunk = _chunked_ok(q, v)
-        ctx.bwd_chunk = fwd_chunk
-        ctx.keep_operators = bool(keep_operators) and ctx.bwd_chunk
+        ctx.keep_operators = bool(keep_operators)
         kw = dict(scale=scale, use_qk_l2norm=use_qk_l2norm)
-        fwd = fwd_chunked if fwd_chunk else fwd_sequential
-        if any(ctx.needs_input_grad[:6]) and ctx.bwd_chunk:
+        if any(ctx.needs_input_grad[:6]):
             o, ht, kept = fwd_chunked(q, k, v, g, beta, h0, save_states=not ctx.keep_operators,
                                       save_all=ctx.keep_operators, **kw)
             ctx.save_for_backward(q, k, v, g, beta, kept)
         else:
-            o, ht = fwd(q, k, v, g, beta, h0, **kw)
-            if any(ctx.needs_input_grad[:6]):
-                ctx.save_for_backward(q, k, v, g, beta, h0)
+            o, ht = fwd_chunked(q, k, v, g, beta, h0, **kw)
         return o, ht
 
     @staticmethod
@@ -57,23 +48,21 @@ class GatedDeltaRuleFunction(torch.autograd.Function):
         do = torch.zeros_like(v) if do is None else do.to(v.dtype).contiguous()
         dht = None if dht is None else dht.to(torch.float32).contiguous()
         kw = dict(scale=ctx.scale, use_qk_l2norm=ctx.norm)
-        if ctx.bwd_chunk:
-            handoff = {"saved": kept} if ctx.keep_operators else {"states": kept}
-            gr = bwd_chunked(q, k, v, g, beta, None, do, dht, **handoff, **kw)
-        else:  # kept is h0 here
-            gr = bwd_sequential(q, k, v, g, beta, kept, do, dht, **kw)
+        handoff = {"saved": kept} if ctx.keep_operators else {"states": kept}
+        gr = bwd_chunked(q, k, v, g, beta, None, do, dht, **handoff, **kw)
         return (gr["dq"].to(q.dtype), gr["dk"].to(k.dtype), gr["dv"].to(v.dtype), gr["dg"], gr["dbeta"],
                 gr["dh0"] if ctx.has_h0 else None, None, None, None)
 
 
 def gated_delta_rule(q, k, v, g, beta, h0=None, scale=None, use_qk_l2norm=True, keep_operators=False):
-    """Differentiable chunked gated delta rule: (o [B,T,Hv,Dv] bf16, ht [B,Hv,Dv,Dk] fp32).
+    """Differentiable chunked gated delta rule: (o [B,T,Hv,Dv] in v's dtype, ht [B,Hv,Dv,Dk] fp32).
 
-    q, k [B,T,Hk,Dk] bf16; v [B,T,Hv,Dv] bf16; g [B,T,Hv] fp32 log-decay; beta [B,T,Hv]
-    fp32; h0 [B,Hv,Dv,Dk] fp32 or None (zero). scale defaults to Dk^-1/2. The forward keeps
-    the chunk-start states (32 KB per chunk and value head) for the backward; with
-    keep_operators=True it keeps the chunk operators too (144 KB per chunk and value head)
-    and the backward then skips all recomputation. Both give bitwise the same results."""
+    q, k [B,T,Hk,Dk] and v [B,T,Hv,Dv] bf16 or fp32; g [B,T,Hv] (or [B,T,Hv,Dk] per key
+    channel) fp32 log-decay; beta [B,T,Hv] fp32; h0 [B,Hv,Dv,Dk] fp32 or None (zero). scale
+    defaults to Dk^-1/2. The forward keeps the chunk-start states (bf16: 32 KB per chunk and
+    value head) for the backward; with keep_operators=True it keeps the chunk operators too
+    (bf16: 144 KB per chunk and value head) and the backward then skips all recomputation.
+    Both give bitwise the same results."""
     if scale is None:
         scale = q.shape[-1] ** -0.5
     return GatedDeltaRuleFunction.apply(q, k, v, g, beta, h0, float(scale), bool(use_qk_l2norm),

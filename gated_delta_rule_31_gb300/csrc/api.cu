@@ -62,17 +62,19 @@ gdr_status check_ptrs(const gdr_problem* p, std::initializer_list<const void*> r
     return GDR_OK;
 }
 
-// The tensor-core chunked path: bf16 q/k/v, Dk and Dv in {32, 64, 128}; scalar or per-channel gate.
-gdr_status check_chunked_support(const gdr_problem* p) {
-    if (p->dtype != GDR_BF16) return GDR_ERR_UNSUPPORTED;
-    return GDR_OK;
+// The chunked calls take every problem check_problem accepts: bf16 q/k/v run on the tensor
+// cores, fp32 q/k/v on the CUDA-core fp32 path (chunk_f32.cu).
+bool f32(const gdr_problem* p) { return p->dtype == GDR_F32; }
+
+Chunk32Layout layout32(const gdr_problem* p, bool bwd, bool own_rec, bool own_states) {
+    return chunk32_layout(p->B, p->T, p->Hv, p->Dk, p->Dv, bwd, own_rec, own_states);
 }
 
 // Head sizes below 128 on the chunked path: the kernels work on 128 key and value channels, so
 // the inputs are copied into zero-padded 128-wide buffers in the workspace (after the padded
 // problem's own workspace) and the results cropped back into the caller's tensors. Zero channels
 // and zero state rows / columns contribute nothing, so the original channels are exact.
-bool narrow(const gdr_problem* p) { return p->Dk != 128 || p->Dv != 128; }
+bool narrow(const gdr_problem* p) { return !f32(p) && (p->Dk != 128 || p->Dv != 128); }
 
 struct Staging {
     size_t q, k, v, g, h0, o, ht, do_, dht, dq, dk, dv, dg, dh0, total;
@@ -134,6 +136,28 @@ ChunkProblem chunk_problem(const gdr_problem* p) {
     c.use_norm = p->use_qk_l2norm;
     c.channel = p->gate == GDR_GATE_CHANNEL;
     return c;
+}
+
+Chunk32Args args32(const gdr_problem* p, const void* q, const void* k, const void* v, const float* g,
+                   const float* beta, const float* h0) {
+    Chunk32Args a;
+    memset(&a, 0, sizeof(a));
+    a.B = p->B; a.T = p->T; a.Hk = p->Hk; a.Hv = p->Hv; a.Dk = p->Dk; a.Dv = p->Dv;
+    a.NC = (p->T + kChunk - 1) / kChunk;
+    a.channel = p->gate == GDR_GATE_CHANNEL;
+    a.use_norm = p->use_qk_l2norm;
+    a.scale = p->scale;
+    a.q = static_cast<const float*>(q); a.k = static_cast<const float*>(k); a.v = static_cast<const float*>(v);
+    a.g = g; a.beta = beta; a.h0 = h0;
+    return a;
+}
+
+// Bytes of the caller's chunk-start states / saved buffer for this problem.
+size_t states_bytes(const gdr_problem* p) {
+    return f32(p) ? chunk32_states_bytes(p->B, p->T, p->Hv, p->Dk, p->Dv) : chunk_states_bytes(chunk_problem(p));
+}
+size_t saved_bytes(const gdr_problem* p) {
+    return f32(p) ? chunk32_saved_bytes(p->B, p->T, p->Hv, p->Dk, p->Dv) : chunk_saved_bytes(chunk_problem(p));
 }
 
 struct TraceRec {
@@ -209,12 +233,14 @@ const char* gdr_status_string(gdr_status s) {
 }
 
 size_t gdr_fwd_chunked_workspace(const gdr_problem* p) {
-    if (check_problem(p, false) != GDR_OK || check_chunked_support(p) != GDR_OK) return 0;
+    if (check_problem(p, false) != GDR_OK) return 0;
+    if (f32(p)) return layout32(p, false, true, false).total;
     return with_staging(p, false, chunk_fwd_workspace(chunk_problem(p)));
 }
 
 size_t gdr_bwd_chunked_workspace(const gdr_problem* p) {
-    if (check_problem(p, false) != GDR_OK || check_chunked_support(p) != GDR_OK) return 0;
+    if (check_problem(p, false) != GDR_OK) return 0;
+    if (f32(p)) return layout32(p, true, true, true).total;
     return with_staging(p, true, chunk_bwd_workspace(chunk_problem(p)));
 }
 
@@ -239,12 +265,14 @@ gdr_status gdr_decode_step(const gdr_problem* p, const void* q, const void* k, c
 }
 
 size_t gdr_chunk_states_bytes(const gdr_problem* p) {
-    if (check_problem(p, false) != GDR_OK || check_chunked_support(p) != GDR_OK) return 0;
+    if (check_problem(p, false) != GDR_OK) return 0;
+    if (f32(p)) return states_bytes(p);
     return chunk_states_bytes(chunk_problem(p));
 }
 
 size_t gdr_bwd_chunked_states_workspace(const gdr_problem* p) {
-    if (check_problem(p, false) != GDR_OK || check_chunked_support(p) != GDR_OK) return 0;
+    if (check_problem(p, false) != GDR_OK) return 0;
+    if (f32(p)) return layout32(p, true, true, false).total;
     return with_staging(p, true, chunk_bwd_states_workspace(chunk_problem(p)));
 }
 
@@ -258,8 +286,7 @@ gdr_status gdr_fwd_chunked_states(const gdr_problem* p, const void* q, const voi
                                   gdr_stream_t stream) {
     gdr_status s = check_problem(p, false);
     if (s != GDR_OK) return s;
-    if ((s = check_chunked_support(p)) != GDR_OK) return s;
-    const size_t need = chunk_states_bytes(chunk_problem(p));
+    const size_t need = ::states_bytes(p);
     if (need && (!states || states_bytes < need)) return GDR_ERR_WORKSPACE;
     if (states && (reinterpret_cast<uintptr_t>(states) & 255u) != 0) return GDR_ERR_INVALID_ARG;
     return fwd_chunked_impl(p, q, k, v, g, beta, h0, o, ht, states, nullptr, ws, ws_bytes, stream);
@@ -272,17 +299,19 @@ gdr_status gdr_fwd_chunked(const gdr_problem* p, const void* q, const void* k, c
 }
 
 size_t gdr_chunk_saved_bytes(const gdr_problem* p) {
-    if (check_problem(p, false) != GDR_OK || check_chunked_support(p) != GDR_OK) return 0;
-    return chunk_saved_bytes(chunk_problem(p));
+    if (check_problem(p, false) != GDR_OK) return 0;
+    return saved_bytes(p);
 }
 
 size_t gdr_fwd_chunked_saved_workspace(const gdr_problem* p) {
-    if (check_problem(p, false) != GDR_OK || check_chunked_support(p) != GDR_OK) return 0;
+    if (check_problem(p, false) != GDR_OK) return 0;
+    if (f32(p)) return layout32(p, false, false, false).total;
     return with_staging(p, false, kSavedFwdWorkspace);
 }
 
 size_t gdr_bwd_chunked_saved_workspace(const gdr_problem* p) {
-    if (check_problem(p, false) != GDR_OK || check_chunked_support(p) != GDR_OK) return 0;
+    if (check_problem(p, false) != GDR_OK) return 0;
+    if (f32(p)) return layout32(p, true, false, false).total;
     return with_staging(p, true, chunk_bwd_saved_workspace(chunk_problem(p)));
 }
 
@@ -291,8 +320,7 @@ gdr_status gdr_fwd_chunked_saved(const gdr_problem* p, const void* q, const void
                                  void* saved, size_t saved_bytes, void* ws, size_t ws_bytes, gdr_stream_t stream) {
     gdr_status s = check_problem(p, false);
     if (s != GDR_OK) return s;
-    if ((s = check_chunked_support(p)) != GDR_OK) return s;
-    const size_t need = chunk_saved_bytes(chunk_problem(p));
+    const size_t need = ::saved_bytes(p);
     if (need && (!saved || saved_bytes < need)) return GDR_ERR_WORKSPACE;
     if (saved && (reinterpret_cast<uintptr_t>(saved) & 255u) != 0) return GDR_ERR_INVALID_ARG;
     return fwd_chunked_impl(p, q, k, v, g, beta, h0, o, ht, nullptr, saved, ws, ws_bytes, stream);
@@ -304,8 +332,9 @@ static gdr_status fwd_chunked_impl(const gdr_problem* p, const void* q, const vo
     gdr_status s = check_problem(p, false);
     if (s != GDR_OK) return s;
     if ((s = check_ptrs(p, {q, k, v, g, beta, o}, {h0, ht})) != GDR_OK) return s;
-    if ((s = check_chunked_support(p)) != GDR_OK) return s;
-    const size_t core = saved ? kSavedFwdWorkspace : chunk_fwd_workspace(chunk_problem(p));
+    const size_t core = f32(p)  ? layout32(p, false, !saved, false).total
+                        : saved ? kSavedFwdWorkspace
+                                : chunk_fwd_workspace(chunk_problem(p));
     const size_t need = with_staging(p, false, core);
     if (!ws || ws_bytes < need) return GDR_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return GDR_ERR_INVALID_ARG;
@@ -316,6 +345,18 @@ static gdr_status fwd_chunked_impl(const gdr_problem* p, const void* q, const vo
         if (!ht) return GDR_OK;
         RecurrentArgs a = recurrent_args(p, q, k, v, g, beta, h0, o, ht);
         return launch_recurrent(a, false, st) == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+    }
+    if (f32(p)) {
+        Chunk32Args a = args32(p, q, k, v, g, beta, h0);
+        a.o = static_cast<float*>(o);
+        a.ht = ht;
+        uint8_t* w = static_cast<uint8_t*>(ws);
+        const Chunk32Layout l = layout32(p, false, !saved, false);
+        uint8_t* sv = static_cast<uint8_t*>(saved);
+        a.rec = reinterpret_cast<float*>(saved ? sv : w + l.rec);
+        a.states = reinterpret_cast<float*>(
+            saved ? sv + chunk32_saved_states_offset(p->B, p->T, p->Hv, p->Dk, p->Dv) : states);
+        return launch_chunk32_fwd(a, true, st) == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
     }
     ChunkFwdArgs a;
     a.p = chunk_problem(p);
@@ -368,8 +409,7 @@ gdr_status gdr_bwd_chunked_states(const gdr_problem* p, const void* q, const voi
                                   float* dbeta, float* dh0, void* ws, size_t ws_bytes, gdr_stream_t stream) {
     gdr_status s = check_problem(p, false);
     if (s != GDR_OK) return s;
-    if ((s = check_chunked_support(p)) != GDR_OK) return s;
-    const size_t need = chunk_states_bytes(chunk_problem(p));
+    const size_t need = ::states_bytes(p);
     if (need && (!states || states_bytes < need)) return GDR_ERR_WORKSPACE;
     if (states && (reinterpret_cast<uintptr_t>(states) & 255u) != 0) return GDR_ERR_INVALID_ARG;
     return bwd_chunked_impl(p, q, k, v, g, beta, nullptr, states, nullptr, do_, dht, dq, dk, dv, dg, dbeta,
@@ -382,8 +422,7 @@ gdr_status gdr_bwd_chunked_saved(const gdr_problem* p, const void* q, const void
                                  float* dbeta, float* dh0, void* ws, size_t ws_bytes, gdr_stream_t stream) {
     gdr_status s = check_problem(p, false);
     if (s != GDR_OK) return s;
-    if ((s = check_chunked_support(p)) != GDR_OK) return s;
-    const size_t need = chunk_saved_bytes(chunk_problem(p));
+    const size_t need = ::saved_bytes(p);
     if (need && (!saved || saved_bytes < need)) return GDR_ERR_WORKSPACE;
     if (saved && (reinterpret_cast<uintptr_t>(saved) & 255u) != 0) return GDR_ERR_INVALID_ARG;
     return bwd_chunked_impl(p, q, k, v, g, beta, nullptr, nullptr, saved, do_, dht, dq, dk, dv, dg, dbeta, dh0,
@@ -398,9 +437,9 @@ static gdr_status bwd_chunked_impl(const gdr_problem* p, const void* q, const vo
     gdr_status s = check_problem(p, false);
     if (s != GDR_OK) return s;
     if ((s = check_ptrs(p, {q, k, v, g, beta, do_, dq, dk, dv, dg, dbeta}, {h0, dht, dh0})) != GDR_OK) return s;
-    if ((s = check_chunked_support(p)) != GDR_OK) return s;
     const ChunkProblem cp = chunk_problem(p);
-    const size_t core = saved    ? chunk_bwd_saved_workspace(cp)
+    const size_t core = f32(p)   ? layout32(p, true, !saved, !saved && !states).total
+                        : saved  ? chunk_bwd_saved_workspace(cp)
                         : states ? chunk_bwd_states_workspace(cp)
                                  : chunk_bwd_workspace(cp);
     const size_t need = with_staging(p, true, core);
@@ -415,6 +454,27 @@ static gdr_status bwd_chunked_impl(const gdr_problem* p, const void* q, const vo
         cudaError_t e = dht ? cudaMemcpyAsync(dh0, dht, bytes, cudaMemcpyDeviceToDevice, st)
                             : cudaMemsetAsync(dh0, 0, bytes, st);
         return e == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
+    }
+    if (f32(p)) {
+        Chunk32Args a = args32(p, q, k, v, g, beta, h0);
+        a.do_ = static_cast<const float*>(do_);
+        a.dht = dht;
+        a.dq = dq; a.dk = dk; a.dv = dv; a.dg = dg; a.dbeta = dbeta; a.dh0 = dh0;
+        uint8_t* w = static_cast<uint8_t*>(ws);
+        const Chunk32Layout l = layout32(p, true, !saved, !saved && !states);
+        const uint8_t* sv = static_cast<const uint8_t*>(saved);
+        const float* hs = saved  ? reinterpret_cast<const float*>(
+                                       sv + chunk32_saved_states_offset(p->B, p->T, p->Hv, p->Dk, p->Dv))
+                          : states ? static_cast<const float*>(states)
+                                   : reinterpret_cast<const float*>(w + l.states);
+        a.rec = saved ? reinterpret_cast<float*>(const_cast<uint8_t*>(sv)) : reinterpret_cast<float*>(w + l.rec);
+        a.states = const_cast<float*>(hs);
+        a.dstates = reinterpret_cast<float*>(w + l.dstates);
+        a.dqh = reinterpret_cast<float*>(w + l.dqh);
+        a.dkh = reinterpret_cast<float*>(w + l.dkh);
+        a.scratch = reinterpret_cast<float*>(w + l.scratch);
+        a.nscratch = l.nscratch;
+        return launch_chunk32_bwd(a, !saved, !saved && !states, st) == cudaSuccess ? GDR_OK : GDR_ERR_CUDA;
     }
     ChunkBwdArgs a;
     a.p = chunk_problem(p);

@@ -395,6 +395,23 @@ cudaError_t launch_qk_norm_backward(const SeqBwdArgs& a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+cudaError_t launch_head_sum_norm_backward(SeqBwdArgs a, cudaStream_t s) {
+    a.channel = 1;  // the finish kernel's scalar-gate dg step is the sequential VJP's own
+    const unsigned blocks = (unsigned)((size_t)a.B * a.T * a.Hk);
+    trace_begin("head_sum_norm_backward", s);
+    switch (a.Dk * 2 + a.bf16) {
+        case 64: seq_bwd_finish_kernel<32, float><<<blocks, 32, 0, s>>>(a); break;
+        case 65: seq_bwd_finish_kernel<32, __nv_bfloat16><<<blocks, 32, 0, s>>>(a); break;
+        case 128: seq_bwd_finish_kernel<64, float><<<blocks, 64, 0, s>>>(a); break;
+        case 129: seq_bwd_finish_kernel<64, __nv_bfloat16><<<blocks, 64, 0, s>>>(a); break;
+        case 256: seq_bwd_finish_kernel<128, float><<<blocks, 128, 0, s>>>(a); break;
+        case 257: seq_bwd_finish_kernel<128, __nv_bfloat16><<<blocks, 128, 0, s>>>(a); break;
+        default: trace_end(s); return cudaErrorInvalidValue;
+    }
+    trace_end(s);
+    return cudaGetLastError();
+}
+
 size_t seq_bwd_workspace(int B, int T, int Hv, int Dk, int Dv) {
     const size_t nh = (size_t)B * Hv, plane = (size_t)Dv * Dk * sizeof(float);
     const size_t nseg = (T + kSeg - 1) / kSeg;

@@ -80,25 +80,24 @@ size_t gdr_fwd_chunked_workspace(const gdr_problem* p);
 size_t gdr_bwd_chunked_workspace(const gdr_problem* p);
 
 /* Chunked prefill forward (chunks of 64 tokens): o and, if ht != NULL, the final state.
- * h0 may be NULL (zero initial state). Implemented for dtype BF16 with Dk, Dv in {32, 64, 128},
+ * h0 may be NULL (zero initial state). Implemented for both dtypes with Dk, Dv in {32, 64, 128},
  * with the scalar gate or the per-channel gate (g [B,T,Hv,Dk], the channelwise variant of
- * "Two-pass optimization for channelwise gated delta rule kernel", ExecuTorch PR #21020). The
- * kernels work on 128 key and value channels: for Dk or Dv below 128 the call stages zero-padded
- * 128-wide copies of its inputs in the workspace (which the size query includes) and crops the
- * results; the zero channels contribute nothing, so results are those of the original sizes.
- * dtype F32 returns GDR_ERR_UNSUPPORTED (the tensor-core path computes with bf16 operands, which
- * cannot meet fp32 accuracy): gdr_fwd_sequential / gdr_bwd_sequential take fp32 problems.
+ * "Two-pass optimization for channelwise gated delta rule kernel", ExecuTorch PR #21020).
+ * BF16: tensor-core kernels on 128 key and value channels; for Dk or Dv below 128 the call
+ * stages zero-padded 128-wide copies of its inputs in the workspace (which the size query
+ * includes) and crops the results; the zero channels contribute nothing, so results are those
+ * of the original sizes. F32: the same chunk algebra with fp32 FMA on the CUDA cores (bf16
+ * tensor-core operands cannot meet fp32 accuracy), every head size in place; o is fp32.
  * Pointers 16-byte aligned.
  * Work: per chunk a 64x64 unit-lower-triangular (UT/WY) transform of the k k^T beta
- * block on the tensor cores, then one sequential scan over chunks per (b, hv, Dv slice)
- * with the fp32 state held on chip. Clears and then sets the workspace status word. */
+ * block, then one sequential scan over chunks per (b, hv, Dv slice) with the fp32 state held
+ * on chip. Clears and then sets the workspace status word. */
 gdr_status gdr_fwd_chunked(const gdr_problem* p, const void* q, const void* k, const void* v,
                            const float* g, const float* beta, const float* h0, void* o, float* ht,
                            void* ws, size_t ws_bytes, gdr_stream_t stream);
 
 /* Token-by-token forward (no workspace): o and, if ht != NULL, the final state. For every
- * dtype, gate and Dk, Dv in {32, 64, 128}; the reference path for small problems and
- * fp32 inputs. */
+ * dtype, gate and Dk, Dv in {32, 64, 128}. */
 gdr_status gdr_fwd_sequential(const gdr_problem* p, const void* q, const void* k, const void* v,
                               const float* g, const float* beta, const float* h0, void* o,
                               float* ht, gdr_stream_t stream);
@@ -120,9 +119,7 @@ gdr_status gdr_bwd_chunked(const gdr_problem* p, const void* q, const void* k, c
 
 /* Sequential (token-by-token) VJP of gdr_fwd_sequential for the loss <do, o> + <dht, ht>:
  * the "sequential case" of "Adding VJP for gated delta net" (MLX PR #4565). Every dtype, gate
- * (scalar or per channel) and Dk, Dv in {32, 64, 128}; the backward for problems the chunked
- * VJP does not cover (fp32, other head sizes). Arguments,
- * layouts and outputs as gdr_bwd_chunked (gradients fp32; dg has g's shape). The forward is
+ * (scalar or per channel) and Dk, Dv in {32, 64, 128}. Arguments, layouts and outputs as gdr_bwd_chunked (gradients fp32; dg has g's shape). The forward is
  * re-run with a checkpoint every 64 tokens (B*Hv*ceil(T/64) fp32 states in the workspace)
  * and each 64-token segment is recomputed in reverse. Deterministic (fixed-order sums, no
  * atomics). Workspace: gdr_bwd_sequential_workspace() bytes, 256-byte aligned. */
@@ -134,8 +131,9 @@ gdr_status gdr_bwd_sequential(const gdr_problem* p, const void* q, const void* k
                               gdr_stream_t stream);
 
 /* Saved-state handoff from the forward to the backward. The forward can keep the state
- * entering every chunk (bf16, opaque layout, gdr_chunk_states_bytes() bytes:
- * B*Hv*ceil(T/64)*32 KB, caller-owned, 256-byte aligned); the backward then reads them
+ * entering every chunk (opaque layout, gdr_chunk_states_bytes() bytes: B*Hv*ceil(T/64)*32 KB
+ * of bf16 images for BF16, B*Hv*ceil(T/64)*Dv*Dk*4 of fp32 states for F32; caller-owned,
+ * 256-byte aligned); the backward then reads them
  * instead of re-running the forward scan. Chunk-local operators are still recomputed by
  * the backward. Same support matrix as gdr_bwd_chunked (scalar or per-channel gate); 0 if
  * the problem is invalid. */
@@ -167,7 +165,9 @@ gdr_status gdr_bwd_chunked_states(const gdr_problem* p, const void* q, const voi
  * between the two calls, and the backward must get the same q, k, v, g, beta and problem.
  * Workspaces: gdr_fwd_chunked_saved_workspace() (the status word only) and
  * gdr_bwd_chunked_saved_workspace(). Same support matrix as gdr_bwd_chunked (with the
- * per-channel gate the saved T/W record also holds K^ .* Gamma, 160 KB per (b, hv, chunk));
+ * per-channel gate the saved T/W record also holds K^ .* Gamma, 160 KB per (b, hv, chunk);
+ * for F32 the buffer holds fp32 records of W, Kbar, scale Gamma Q^, gamma, U~, P and T, then
+ * the fp32 chunk-start states: 256 KB per (b, hv, chunk) at Dk = Dv = 128);
  * the size queries return 0 for an invalid or unsupported problem. Errors as gdr_fwd_chunked, plus
  * GDR_ERR_WORKSPACE if `saved` is NULL or smaller than required. */
 size_t gdr_chunk_saved_bytes(const gdr_problem* p);

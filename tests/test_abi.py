@@ -85,13 +85,24 @@ def test_decode_requires_single_token(L):
 
 
 def test_chunked_support_matrix_and_workspace(L):
-    # fp32 q/k/v: not on the tensor-core chunked path (the token-by-token calls take them)
-    for kw in (dict(dtype=0), dict(dtype=0, Dk=64, Dv=64)):
-        p = prob(**kw)
-        assert L.gdr_fwd_chunked_workspace(ctypes.byref(p)) == 0
-        assert L.gdr_bwd_chunked_workspace(ctypes.byref(p)) == 0
-        assert L.gdr_fwd_chunked(ctypes.byref(p), *[FAKE] * 8, FAKE, 1 << 30, None) == UNSUPPORTED
-        assert L.gdr_bwd_chunked(ctypes.byref(p), *[FAKE] * 14, FAKE, 1 << 30, None) == UNSUPPORTED
+    # fp32 q/k/v: the CUDA-core fp32 chunked path, every head size in place (no staging). Its
+    # forward workspace is the status word and one fp32 record per (b, hv, chunk): W, Kbar, Qg,
+    # gamma [64 x Dk] each, U~ [64 x Dv], P and T [64 x 64], padded to 64 floats
+    for dk, dv in ((128, 128), (64, 64), (32, 128), (128, 32)):
+        p = prob(dtype=0, Dk=dk, Dv=dv)
+        rec = (4 * 64 * dk + 64 * dv + 2 * 4096 + 63) // 64 * 64 * 4
+        need = L.gdr_fwd_chunked_workspace(ctypes.byref(p))
+        assert need == 256 + 4 * rec, (dk, dv)
+        need_b = L.gdr_bwd_chunked_workspace(ctypes.byref(p))
+        assert need_b > need
+        assert L.gdr_fwd_chunked(ctypes.byref(p), *[FAKE] * 8, FAKE, need - 1, None) == WORKSPACE
+        assert L.gdr_bwd_chunked(ctypes.byref(p), *[FAKE] * 14, FAKE, need_b - 1, None) == WORKSPACE
+        states = 4 * dv * dk * 4  # B * Hv * chunks fp32 Dv x Dk chunk-start states
+        assert L.gdr_chunk_states_bytes(ctypes.byref(p)) == states
+        assert L.gdr_chunk_saved_bytes(ctypes.byref(p)) == 4 * rec + states
+        assert L.gdr_fwd_chunked_saved_workspace(ctypes.byref(p)) == 256
+        assert 0 < L.gdr_bwd_chunked_saved_workspace(ctypes.byref(p)) < L.gdr_bwd_chunked_states_workspace(
+            ctypes.byref(p)) < need_b
     # bf16 head sizes 32 and 64: the workspace adds the zero-padded 128-wide copies of the inputs and
     # outputs; the saved-state and saved-operator buffers keep the 128-wide layout
     wide = prob()
@@ -159,9 +170,11 @@ def test_saved_state_handoff_validation(L):
     assert L.gdr_bwd_chunked_states(ctypes.byref(p), *args, FAKE, wsb - 1, None) == WORKSPACE
     args = [FAKE] * 5 + [FAKE, sb - 16] + [FAKE] * 8
     assert L.gdr_bwd_chunked_states(ctypes.byref(p), *args, FAKE, wsb, None) == WORKSPACE
+    # fp32 keeps fp32 states (64 KB per chunk and value head here), so the bf16 size is short
     q = prob(dtype=0)
-    assert L.gdr_chunk_states_bytes(ctypes.byref(q)) == 0
-    assert L.gdr_fwd_chunked_states(ctypes.byref(q), *[FAKE] * 8, FAKE, sb, FAKE, need_f, None) == UNSUPPORTED
+    assert L.gdr_chunk_states_bytes(ctypes.byref(q)) == 2 * sb
+    need_q = L.gdr_fwd_chunked_workspace(ctypes.byref(q))
+    assert L.gdr_fwd_chunked_states(ctypes.byref(q), *[FAKE] * 8, FAKE, sb, FAKE, need_q, None) == WORKSPACE
 
 
 def test_autograd_function_has_no_cpu_path():
@@ -191,8 +204,9 @@ def test_saved_operator_handoff_validation(L):
     args = [FAKE] * 5 + [FAKE, sb - 16] + [FAKE] * 8
     assert L.gdr_bwd_chunked_saved(ctypes.byref(p), *args, FAKE, bw, None) == WORKSPACE
     q = prob(dtype=0)
-    assert L.gdr_chunk_saved_bytes(ctypes.byref(q)) == 0
-    assert L.gdr_fwd_chunked_saved(ctypes.byref(q), *[FAKE] * 8, FAKE, sb, FAKE, fw, None) == UNSUPPORTED
+    sq = L.gdr_chunk_saved_bytes(ctypes.byref(q))
+    assert sq > sb
+    assert L.gdr_fwd_chunked_saved(ctypes.byref(q), *[FAKE] * 8, FAKE, sq - 1, FAKE, fw, None) == WORKSPACE
 
 
 def test_sequential_backward_validation(L):
@@ -239,7 +253,7 @@ def test_noalloc_forward_validation(L):
     P = ctypes.c_void_p
     L.gdr_fwd_chunked_noalloc.argtypes = [ctypes.POINTER(Problem)] + [P] * 8 + [P]
     L.gdr_fwd_chunked_noalloc.restype = ctypes.c_int
-    for kw, code in ((dict(Hv=3), INVALID), (dict(dtype=0), UNSUPPORTED), (dict(Dk=64, dtype=0), UNSUPPORTED),
+    for kw, code in ((dict(Hv=3), INVALID), (dict(Dk=96), UNSUPPORTED), (dict(dtype=0, T=4096, Hk=16, Hv=32), WORKSPACE),
                      (dict(T=4096, Hk=16, Hv=32), WORKSPACE), (dict(T=2048, Hk=16, Hv=32, Dk=64), WORKSPACE)):
         assert L.gdr_fwd_chunked_noalloc(ctypes.byref(prob(**kw)), *[FAKE] * 8, None) == code, kw
     assert L.gdr_fwd_chunked_workspace(ctypes.byref(prob(T=4096, Hk=16, Hv=32))) > 64 * 1024 * 1024

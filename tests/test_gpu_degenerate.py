@@ -6,8 +6,8 @@ and erases nothing), beta = 1 (the key's old value is replaced exactly), g = 0 (
 a = 1), and all-zero keys and/or queries under the in-kernel L2 norm (k^ = 0, q^ = 0; the
 norm factor (0 + 1e-6)^(-1/2) = 1000 of "fold q/k L2-norm into the gated_delta_rule kernel",
 What/Why, multiplies their gradients). The chunked forward and VJP (scalar and per-channel
-gate), the token-by-token forward and VJP (fp32 and bf16) and the decode step are compared
-with the fp64 oracle on the same inputs. Rows of dq / dk at zero queries / keys carry the
+gate; bf16 on the tensor cores, fp32 on the CUDA cores), the token-by-token forward and VJP
+(fp32 and bf16) and the decode step are compared with the fp64 oracle on the same inputs. Rows of dq / dk at zero queries / keys carry the
 1000x factor, so they are checked apart from the other rows (one shared maximum would hide
 errors in either group).
 """
@@ -68,21 +68,23 @@ def oracle_bwd(x):
     return oracle.backward(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"], x["do"], x["dht"])
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("gate", ["scalar", "channel"])
-def test_chunked_forward_and_vjp_degenerate_tokens(gate):
+def test_chunked_forward_and_vjp_degenerate_tokens(gate, dtype):
     dev = cuda_device()
-    x, zk, zq = make_degenerate(Shape(2, 200, 2, 4, 128, 128), torch.bfloat16, seed=501, gate=gate, grads=True)
+    x, zk, zq = make_degenerate(Shape(2, 200, 2, 4, 128, 128), dtype, seed=501, gate=gate, grads=True)
     d = to_dev(x, dev)
+    tol = F32_TOL if dtype == torch.float32 else BF16_TOL
     o, ht = gdr.fwd_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"])
     ro, rht = oracle.forward(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"])
     assert torch.isfinite(o.float()).all() and torch.isfinite(ht).all()
-    assert rel_err(o, ro) <= BF16_TOL and rel_err(ht, rht) <= BF16_TOL
+    assert rel_err(o, ro) <= tol and rel_err(ht, rht) <= tol
     # a zero query reads nothing: its outputs are exactly zero on the GPU too
     assert torch.count_nonzero(o[:, zq].float()) == 0
     gr = gdr.bwd_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], d["do"], d["dht"])
     for n in NAMES:
         assert torch.isfinite(gr[n]).all(), n
-    check_grads(gr, oracle_bwd(x), zk, zq, BF16_TOL)
+    check_grads(gr, oracle_bwd(x), zk, zq, tol)
     # the saved-state handoff sees the same tokens
     o2, h2, states = gdr.fwd_chunked(d["q"], d["k"], d["v"], d["g"], d["beta"], d["h0"], save_states=True)
     assert torch.equal(o, o2) and torch.equal(ht, h2)

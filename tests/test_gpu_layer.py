@@ -104,13 +104,18 @@ def test_unused_outputs_and_no_grad():
 @pytest.mark.parametrize("dtype,D,gate,tol", [(torch.float32, 64, "scalar", 1e-4),
                                               (torch.float32, 32, "channel", 1e-4)],
                          ids=["fp32-D64-scalar", "fp32-D32-channel"])
-def test_autograd_outside_the_chunked_vjp(dtype, D, gate, tol):
-    """Problems the chunked VJP does not cover run the sequential kernels under autograd."""
+@pytest.mark.parametrize("keep_operators", [False, True])
+def test_autograd_fp32_runs_the_fp32_chunked_path(dtype, D, gate, tol, keep_operators):
+    """fp32 problems run the CUDA-core fp32 chunked kernels under autograd, both handoffs."""
     dev = cuda_device()
     x = make_inputs(Shape(1, 100, 1, 2, D, D), dtype=dtype, seed=41, gate=gate, grads=True, gate_scale=0.3)
     t = leaves(x, dev)
-    o, ht = gated_delta_rule(t["q"], t["k"], t["v"], t["g"], t["beta"], t["h0"])
-    ((o.float() * x["do"].to(dev).float()).sum() + (ht * x["dht"].to(dev)).sum()).backward()
+    with gdr.trace() as tr:
+        o, ht = gated_delta_rule(t["q"], t["k"], t["v"], t["g"], t["beta"], t["h0"], keep_operators=keep_operators)
+        ((o.float() * x["do"].to(dev).float()).sum() + (ht * x["dht"].to(dev)).sum()).backward()
+        torch.cuda.synchronize()
+    names = {n for n, _ in tr.records}
+    assert {"chunk32_scan_fwd", "chunk32_scan_bwd", "chunk32_grad"} <= names, names
     ro, rht = oracle.forward(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"])
     ref = oracle.backward(x["q"], x["k"], x["v"], x["g"], x["beta"], x["h0"], x["do"], x["dht"])
     assert rel_err(o.detach(), ro) <= tol and rel_err(ht.detach(), rht) <= tol

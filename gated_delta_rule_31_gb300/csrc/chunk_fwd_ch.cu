@@ -36,11 +36,18 @@ constexpr uint32_t CS_P = 149504;     // P image [64 x 64]
 constexpr uint32_t CS_KG = 157696;    // K .* Gamma image [64 x 128]
 constexpr uint32_t CS_KB = 174080;    // Kbar image [64 x 128]
 constexpr uint32_t CS_SCR = 190464;   // solve scratch [6][16][LDY] fp32
-constexpr uint32_t CS_SMALL = CS_SCR + SOLVE_SCRATCH_BYTES;  // bet[64], rho[128]
+constexpr uint32_t CS_SMALL = CS_SCR + SOLVE_SCRATCH_BYTES;  // bet[64], rho[128], safe[4]
+constexpr uint32_t CS_R01 = 199680;   // R_1 [32 x 128] and R_0 [16 x 128] images (12 KB)
 // while A and P are formed: the scaled [k; q] operand L over the K .* Gamma and Kbar images,
-// R_1 / R_2 over T, R_3 over v (which is fetched afterwards)
-constexpr uint32_t CS_L = CS_KG, CS_R2 = CS_T, CS_R1 = CS_T + 8192, CS_R3 = CS_V;
-constexpr uint32_t CS_BYTES = CS_SMALL + 1024;
+// R_2 over T, R_3 over v (which is fetched afterwards), R_1 and R_0 in their own region
+constexpr uint32_t CS_L = CS_KG, CS_R2 = CS_T, CS_R3 = CS_V, CS_R1 = CS_R01, CS_R0 = CS_R01 + 8192;
+constexpr uint32_t CS_BYTES = CS_R01 + 12288;
+static_assert(CS_SMALL + 1024 <= CS_R01 && CS_R01 % 1024 == 0, "R_0 / R_1 region");
+static_assert(CS_T + 12288 <= CS_P, "R_2 over T");
+// A diagonal block's decays come from the tensor-core product when, on every key channel, the
+// product of its 16 per-token factors is at least this (the largest B-side scale is then below
+// 1e34, far inside the bf16 range); otherwise the running decay on the CUDA cores forms them.
+constexpr float kDiagMinDecay = 1e-34f;
 static_assert(CS_A % 1024 == 0 && CS_T % 1024 == 0 && CS_P % 1024 == 0 && CS_KG % 1024 == 0 &&
                   CS_KB % 1024 == 0, "operand images need 1024-byte alignment");
 static_assert(CS_A + 64 * LDA * 4 <= CS_T && CS_T + 64 * LDA * 4 <= CS_P, "fp32 tiles");
@@ -72,6 +79,7 @@ __global__ void __launch_bounds__(PCH_THREADS, 1)
     float* Xs = reinterpret_cast<float*>(sm + CS_SCR);
     float* bet = reinterpret_cast<float*>(sm + CS_SMALL);
     float* rho = bet + 64;  // [128] rows 0-63: k norm factors, 64-127: q norm factors
+    int* safe = reinterpret_cast<int*>(rho + 128);  // [4][4]: per block and warp, diagonal block by MMA
     bool ok;
     uint32_t mph = 0;                        // bar_mma phase
     bool mma_pend = false, v_pend = false;   // (thread 0) products / v copy not yet waited for
@@ -150,9 +158,12 @@ __global__ void __launch_bounds__(PCH_THREADS, 1)
     // factors through s = 16I - 1 into two products of per-token factors, each <= 1:
     //   E_rj = [prod_{s<t<=r} a_t] [prod_{j<t<=s} a_t]
     // so the blocks below the block diagonal are tcgen05 products D_I = L R_I^T of scaled
-    // operands: L = [k; q] with row r scaled by prod_{16I<=t<=r} a_t (rows of block 0 zero), R_I =
-    // rows j < 16I of k scaled by prod_{j<t<16I} a_t. The diagonal blocks keep the running decay
-    // on the CUDA cores.
+    // operands: L = [k; q] with row r scaled by p_r = prod_{16I<=t<=r} a_t, R_I = rows j < 16I of
+    // k scaled by prod_{j<t<16I} a_t. Inside the diagonal block (16I <= j <= r) E_rj = p_r / p_j,
+    // so R_I continues with the block's own rows k_j / p_j (>= 1): N = 16 (I + 1). That factor is
+    // bounded only while p_j stays in range, so a block whose 16-token product falls below
+    // kDiagMinDecay on some channel takes its diagonal decays from the running product on the
+    // CUDA cores instead (exact for any decay).
     {
         const int d = tid & 127, blk = tid >> 7;  // channel d, block blk
         const __nv_bfloat16* kqs = reinterpret_cast<const __nv_bfloat16*>(sm + CS_KQ);
@@ -165,7 +176,9 @@ __global__ void __launch_bounds__(PCH_THREADS, 1)
                 kv[i] = __bfloat162float(kqs[sw128_off(r, d, 128) >> 1]);
                 qv[i] = __bfloat162float(kqs[sw128_off(64 + r, d, 128) >> 1]);
             }
-            float p = blk ? 1.f : 0.f;
+            const uint32_t rb = blk == 0 ? CS_R0 : blk == 1 ? CS_R1 : blk == 2 ? CS_R2 : CS_R3;
+            const int nr = 16 * blk + 16;  // rows of R_blk
+            float p = 1.f;
 #pragma unroll
             for (int i = 0; i < 16; i++) {
                 const int r = 16 * blk + i;
@@ -173,10 +186,17 @@ __global__ void __launch_bounds__(PCH_THREADS, 1)
                 *reinterpret_cast<__nv_bfloat16*>(sm + CS_L + sw128_off(r, d, 128)) = __float2bfloat16_rn(kv[i] * p);
                 *reinterpret_cast<__nv_bfloat16*>(sm + CS_L + sw128_off(64 + r, d, 128)) =
                     __float2bfloat16_rn(qv[i] * p);
+                // the diagonal block's B-side row k_j / p_j (zero where the block falls back)
+                *reinterpret_cast<__nv_bfloat16*>(sm + rb + sw128_off(r, d, nr)) =
+                    __float2bfloat16_rn(p >= kDiagMinDecay ? kv[i] / p : 0.f);
             }
+            const bool ok_d = p >= kDiagMinDecay;  // p: the block's 16-token product on channel d
+            const unsigned all_ok = __all_sync(0xffffffffu, ok_d);
+            if (lane == 0) safe[4 * blk + (warp & 3)] = all_ok ? 1 : 0;
         }
         if (blk) {  // R_blk: rows j = 16 blk - 1 .. 0, 16 rows' inputs loaded before their stores
             const uint32_t rb = blk == 1 ? CS_R1 : blk == 2 ? CS_R2 : CS_R3;
+            const int nr = 16 * blk + 16;
             float sfx = 1.f;
 #pragma unroll 1
             for (int jb = 16 * blk - 16; jb >= 0; jb -= 16) {
@@ -188,7 +208,7 @@ __global__ void __launch_bounds__(PCH_THREADS, 1)
                 }
 #pragma unroll
                 for (int i = 15; i >= 0; i--) {
-                    *reinterpret_cast<__nv_bfloat16*>(sm + rb + sw128_off(jb + i, d, 16 * blk)) =
+                    *reinterpret_cast<__nv_bfloat16*>(sm + rb + sw128_off(jb + i, d, nr)) =
                         __float2bfloat16_rn(kv[i] * sfx);
                     sfx *= av[i];
                 }
@@ -198,15 +218,15 @@ __global__ void __launch_bounds__(PCH_THREADS, 1)
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
-    if (tid == 0) {  // D_I (M=128, N=16 I) into TMEM columns 0, 16, 48
+    if (tid == 0) {  // D_I (M=128, N=16 (I + 1)) into TMEM columns 0, 16, 48, 96
         tc_fence_after();
 #pragma unroll
-        for (int I = 1; I <= 3; I++) {
-            const uint32_t rb = I == 1 ? CS_R1 : I == 2 ? CS_R2 : CS_R3;
-            const uint32_t id = idesc_bf16(128, 16 * I, 0, 0);
+        for (int I = 0; I <= 3; I++) {
+            const uint32_t rb = I == 0 ? CS_R0 : I == 1 ? CS_R1 : I == 2 ? CS_R2 : CS_R3;
+            const uint32_t id = idesc_bf16(128, 16 * I + 16, 0, 0);
             for (int k0 = 0; k0 < kD; k0 += 16)
-                mma_bf16(tm + 8 * I * (I - 1), desc_kmajor(sb + CS_L, 128, 0, k0), desc_kmajor(sb + rb, 16 * I, 0, k0),
-                         id, k0 > 0);
+                mma_bf16(tm + 8 * I * (I + 1), desc_kmajor(sb + CS_L, 128, 0, k0),
+                         desc_kmajor(sb + rb, 16 * I + 16, 0, k0), id, k0 > 0);
         }
         mma_commit(&bar_mma);
         mma_pend = true;
@@ -220,6 +240,7 @@ __global__ void __launch_bounds__(PCH_THREADS, 1)
     {
         const int jsel = lane >> 4, cg = lane & 15, mq = cg >> 3, c8 = cg & 7;
         const int I = warp >> 2, c = warp & 3, rend = 16 * I + 16;
+        const bool by_mma = safe[4 * I] & safe[4 * I + 1] & safe[4 * I + 2] & safe[4 * I + 3];
         float kj[8], e[8];
         auto load_row8 = [&](int row, float* x) {
 #pragma unroll
@@ -234,7 +255,7 @@ __global__ void __launch_bounds__(PCH_THREADS, 1)
             }
         };
 #pragma unroll 1
-        for (int ph = 0; ph < 2; ph++) {
+        for (int ph = 0; ph < (by_mma ? 0 : 2); ph++) {
             const int jb = 16 * I + (ph == 0 ? 2 * c : 14 - 2 * c);
             const int j = jb + jsel;
             load_row8(j, kj);
@@ -278,27 +299,39 @@ __global__ void __launch_bounds__(PCH_THREADS, 1)
     if (__syncthreads_or(!ok)) goto teardown;
     if (tid == 0) mma_pend = false;
     tc_fence_after();
-    if (warp < 4) {  // below the block diagonal: row = 32 warp + lane of D (k rows, then q rows)
-        const int row = 32 * warp + lane, rr = row & 63, rI = rr >> 4;
+    {  // D row 32 lg + lane (k rows, then q rows) into A / P: below the block diagonal, and the
+       // diagonal blocks formed by the product. The lane group's rows lie in blocks I0 (lanes
+       // 0-15) and I0 + 1; their 16-column panels (I, pc <= I) are shared out over the group's 4 warps.
+        const int lg = warp & 3, sub = warp >> 2;
+        const int row = 32 * lg + lane, rr = row & 63, rI = rr >> 4;
+        const int I0 = 2 * (lg & 1), npan = 2 * I0 + 3;  // panels of blocks I0 and I0 + 1
+        for (int n = sub; n < npan; n += 4) {
+            const int I = n < I0 + 1 ? I0 : I0 + 1, pc = n < I0 + 1 ? n : n - I0 - 1;
+            float v[16];
+            tmem_ld16(tmem_at(tm, 32 * lg, 8 * I * (I + 1) + 16 * pc), v);
+            tmem_wait_ld();
+            const bool diag_mma = safe[4 * I] & safe[4 * I + 1] & safe[4 * I + 2] & safe[4 * I + 3];
+            if (rI == I && (pc < I || diag_mma)) {
+                const float4 r0 = *reinterpret_cast<const float4*>(rho + 16 * pc);
+                const float4 r1 = *reinterpret_cast<const float4*>(rho + 16 * pc + 4);
+                const float4 r2 = *reinterpret_cast<const float4*>(rho + 16 * pc + 8);
+                const float4 r3 = *reinterpret_cast<const float4*>(rho + 16 * pc + 12);
+                const float rj[16] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w,
+                                      r2.x, r2.y, r2.z, r2.w, r3.x, r3.y, r3.z, r3.w};
+                float x[16];
+                if (row < 64) {  // A (strictly lower; zeros above are not read)
+                    const float f = bet[rr] * rho[rr];
 #pragma unroll
-        for (int I = 1; I <= 3; I++) {
+                    for (int e2 = 0; e2 < 16; e2++) x[e2] = 16 * pc + e2 < rr ? f * rj[e2] * v[e2] : 0.f;
+                    float4* dst = reinterpret_cast<float4*>(Am + rr * LDA + 16 * pc);
 #pragma unroll
-            for (int pc = 0; pc < I; pc++) {
-                float v[16];
-                tmem_ld16(tmem_at(tm, 32 * warp, 8 * I * (I - 1) + 16 * pc), v);
-                tmem_wait_ld();
-                if (rI == I) {
-                    if (row < 64) {
-                        const float f = bet[rr] * rho[rr];
+                    for (int q = 0; q < 4; q++) dst[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+                } else {  // P (lower with the diagonal; zeros above)
+                    const float f = P.scale * rho[64 + rr];
 #pragma unroll
-                        for (int e2 = 0; e2 < 16; e2++) Am[rr * LDA + 16 * pc + e2] = f * rho[16 * pc + e2] * v[e2];
-                    } else {
-                        const float f = P.scale * rho[64 + rr];
-#pragma unroll
-                        for (int e2 = 0; e2 < 16; e2++)
-                            *reinterpret_cast<__nv_bfloat16*>(sm + CS_P + sw128_off(rr, 16 * pc + e2, 64)) =
-                                __float2bfloat16_rn(f * rho[16 * pc + e2] * v[e2]);
-                    }
+                    for (int e2 = 0; e2 < 16; e2++) x[e2] = 16 * pc + e2 <= rr ? f * rj[e2] * v[e2] : 0.f;
+                    st_chunk(sb + CS_P + sw128_chunk(rr, 2 * pc, 64), x, 1.f);
+                    st_chunk(sb + CS_P + sw128_chunk(rr, 2 * pc + 1, 64), x + 8, 1.f);
                 }
             }
         }
@@ -313,20 +346,21 @@ __global__ void __launch_bounds__(PCH_THREADS, 1)
         v_pend = true;
     }
     __syncthreads();
-    if (tid < 128) {  // prod_{t>r} a_t, channel d = tid, in place of a_t (16 tokens read before written)
+    if (tid >= 256 && tid < 384) {  // prod_{t>r} a_t, channel d, in place of a_t (16 tokens read
+        const int d = tid - 256;       // before written), by threads the solve's first phase leaves idle
         float p = 1.f;
 #pragma unroll 1
         for (int t0b = kChunk - 16; t0b >= 0; t0b -= 16) {
             float x[16];
 #pragma unroll
-            for (int i = 0; i < 16; i++) x[i] = al[(t0b + i) * kD + tid];
+            for (int i = 0; i < 16; i++) x[i] = al[(t0b + i) * kD + d];
 #pragma unroll
             for (int i = 15; i >= 0; i--) {
-                al[(t0b + i) * kD + tid] = p;
+                al[(t0b + i) * kD + d] = p;
                 p *= x[i];
             }
         }
-        a.gam[(bh * P.NC + c) * kD + tid] = gp[(kChunk - 1) * kD + tid];  // Gamma_C per channel
+        a.gam[(bh * P.NC + c) * kD + d] = gp[(kChunk - 1) * kD + d];  // Gamma_C per channel
     }
     if (tid == 0) {  // P to the record
         bulk_store(rec + REC_P, sm + CS_P, 8192);
@@ -459,39 +493,37 @@ __global__ void __launch_bounds__(PCH_THREADS, 1)
     if (__syncthreads_or(!ok)) goto teardown;
     if (tid == 0) mma_pend = false;
     tc_fence_after();
-    if (warp < 8) {
+    {  // 16 warps: lane group lg, column quarter h (32 columns)
         const int lg = warp & 3, h = warp >> 2;
         {  // Mneg rows d = 32 lg + lane
             const int d = 32 * lg + lane;
-            float m[64];
-            tmem_ld32(tmem_at(tm, 32 * lg, 64 * h), m);
-            tmem_ld32(tmem_at(tm, 32 * lg, 64 * h + 32), m + 32);
+            float m[32];
+            tmem_ld32(tmem_at(tm, 32 * lg, 32 * h), m);
             tmem_wait_ld();
 #pragma unroll
-            for (int q = 0; q < 8; q++) st_chunk(sb + CS_AL + sw128_chunk(d, 8 * h + q, 128), m + 8 * q, -1.f);
+            for (int q = 0; q < 4; q++) st_chunk(sb + CS_AL + sw128_chunk(d, 4 * h + q, 128), m + 8 * q, -1.f);
         }
         {  // Qc = scale diag(rho_q) Q .* Gamma - P W, rows i = 16 lg + lane (M=64 layout)
             const int i = 16 * lg + (lane & 15);
-            float pw[64];
-            tmem_ld32(tmem_at(tm, 32 * lg, 128 + 64 * h), pw);
-            tmem_ld32(tmem_at(tm, 32 * lg, 128 + 64 * h + 32), pw + 32);
+            float pw[32];
+            tmem_ld32(tmem_at(tm, 32 * lg, 128 + 32 * h), pw);
             tmem_wait_ld();
             if (lane < 16) {
                 const float f = P.scale * rho[64 + i];
-                uint4 qv[8];
+                uint4 qv[4];
 #pragma unroll
-                for (int q = 0; q < 8; q++)
-                    qv[q] = ld_shared_v4(sb + CS_KQ + sw128_chunk(64 + i, 8 * h + q, 128));
+                for (int q = 0; q < 4; q++)
+                    qv[q] = ld_shared_v4(sb + CS_KQ + sw128_chunk(64 + i, 4 * h + q, 128));
 #pragma unroll
-                for (int q = 0; q < 8; q++) {
+                for (int q = 0; q < 4; q++) {
                     float x[8];
                     unpack8(qv[q], x);
-                    const float4* g4 = reinterpret_cast<const float4*>(gp + i * kD + 64 * h + 8 * q);
+                    const float4* g4 = reinterpret_cast<const float4*>(gp + i * kD + 32 * h + 8 * q);
                     const float4 g0 = g4[0], g1 = g4[1];
                     const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 #pragma unroll
                     for (int e = 0; e < 8; e++) x[e] = f * x[e] * gg[e] - pw[8 * q + e];
-                    st_chunk(sb + CS_A + sw128_chunk(i, 8 * h + q, 64), x, 1.f);
+                    st_chunk(sb + CS_A + sw128_chunk(i, 4 * h + q, 64), x, 1.f);
                 }
             }
         }

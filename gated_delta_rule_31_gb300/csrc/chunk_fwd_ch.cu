@@ -55,6 +55,11 @@ static_assert(CS_BYTES + 1024 <= 232448, "prep_ch smem");
 
 constexpr int PCH_THREADS = 512;  // 16 warps: the A/P loop is latency-bound
 
+// Element (r, d) of the fp32 [64][128] per-token decay arrays (a_t, then prod_{t>r} a_t; Gamma_r).
+// The 4-float group is XOR-ed with the row's low 3 bits, so 8 rows read at the same channels
+// hit 8 different bank groups, while a row's float4 groups stay contiguous.
+__device__ __forceinline__ int dix(int r, int d) { return r * kD + (d ^ ((r & 7) << 2)); }
+
 __global__ void __launch_bounds__(PCH_THREADS, 1)
     prep_ch_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                    const __grid_constant__ CUtensorMap mv, PrepArgs a) {
@@ -110,13 +115,13 @@ __global__ void __launch_bounds__(PCH_THREADS, 1)
         const bool valid = t0 + t < P.T;
         const float4* src =
             reinterpret_cast<const float4*>(a.g + (((size_t)b * P.T + t0 + t) * P.Hv + hv) * kD + 16 * q8);
-        float4* dst = reinterpret_cast<float4*>(al + t * kD + 16 * q8);
         float4 gv[4];
 #pragma unroll
         for (int n = 0; n < 4; n++) gv[n] = valid ? src[n] : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int n = 0; n < 4; n++)
-            dst[n] = make_float4(__expf(gv[n].x), __expf(gv[n].y), __expf(gv[n].z), __expf(gv[n].w));
+            *reinterpret_cast<float4*>(al + dix(t, 16 * q8 + 4 * n)) =
+                make_float4(__expf(gv[n].x), __expf(gv[n].y), __expf(gv[n].z), __expf(gv[n].w));
         if (tid < 64) bet[tid] = (t0 + tid < P.T) ? a.beta[((size_t)b * P.T + t0 + tid) * P.Hv + hv] : 0.f;
     }
     ok = mbar_wait(&bar_tma, 0, &abort_sh, a.status, 15);
@@ -127,11 +132,11 @@ __global__ void __launch_bounds__(PCH_THREADS, 1)
         for (int t0b = 0; t0b < kChunk; t0b += 16) {
             float x[16];
 #pragma unroll
-            for (int i = 0; i < 16; i++) x[i] = al[(t0b + i) * kD + tid];
+            for (int i = 0; i < 16; i++) x[i] = al[dix(t0b + i, tid)];
 #pragma unroll
             for (int i = 0; i < 16; i++) {
                 p *= x[i];
-                gp[(t0b + i) * kD + tid] = p;
+                gp[dix(t0b + i, tid)] = p;
             }
         }
     } else if (tid < 256) {  // L2 norm factors: row tid-128 of the [k; q] tile (read order rotated by the row)
@@ -172,7 +177,7 @@ __global__ void __launch_bounds__(PCH_THREADS, 1)
 #pragma unroll
             for (int i = 0; i < 16; i++) {
                 const int r = 16 * blk + i;
-                av[i] = al[r * kD + d];
+                av[i] = al[dix(r, d)];
                 kv[i] = __bfloat162float(kqs[sw128_off(r, d, 128) >> 1]);
                 qv[i] = __bfloat162float(kqs[sw128_off(64 + r, d, 128) >> 1]);
             }
@@ -203,7 +208,7 @@ __global__ void __launch_bounds__(PCH_THREADS, 1)
                 float av[16], kv[16];
 #pragma unroll
                 for (int i = 0; i < 16; i++) {
-                    av[i] = al[(jb + i) * kD + d];
+                    av[i] = al[dix(jb + i, d)];
                     kv[i] = __bfloat162float(kqs[sw128_off(jb + i, d, 128) >> 1]);
                 }
 #pragma unroll
@@ -265,7 +270,7 @@ __global__ void __launch_bounds__(PCH_THREADS, 1)
                 const bool past = r > j;  // E_rj = E_(r-1)j * a_r past the column's own row
 #pragma unroll
                 for (int mm = 0; mm < 2; mm++) {
-                    const float4 f = *reinterpret_cast<const float4*>(al + r * kD + 32 * (mq + 2 * mm) + 4 * c8);
+                    const float4 f = *reinterpret_cast<const float4*>(al + dix(r, 32 * (mq + 2 * mm) + 4 * c8));
                     e[4 * mm] *= past ? f.x : 1.f;
                     e[4 * mm + 1] *= past ? f.y : 1.f;
                     e[4 * mm + 2] *= past ? f.z : 1.f;
@@ -353,14 +358,14 @@ __global__ void __launch_bounds__(PCH_THREADS, 1)
         for (int t0b = kChunk - 16; t0b >= 0; t0b -= 16) {
             float x[16];
 #pragma unroll
-            for (int i = 0; i < 16; i++) x[i] = al[(t0b + i) * kD + d];
+            for (int i = 0; i < 16; i++) x[i] = al[dix(t0b + i, d)];
 #pragma unroll
             for (int i = 15; i >= 0; i--) {
-                al[(t0b + i) * kD + d] = p;
+                al[dix(t0b + i, d)] = p;
                 p *= x[i];
             }
         }
-        a.gam[(bh * P.NC + c) * kD + d] = gp[(kChunk - 1) * kD + d];  // Gamma_C per channel
+        a.gam[(bh * P.NC + c) * kD + d] = gp[dix(kChunk - 1, d)];  // Gamma_C per channel
     }
     if (tid == 0) {  // P to the record
         bulk_store(rec + REC_P, sm + CS_P, 8192);
@@ -391,17 +396,19 @@ __global__ void __launch_bounds__(PCH_THREADS, 1)
                 st_global16(rec2 + REC2_T + sw128_chunk(i, 2 * qtr + q, 64), pack8(t + 8 * q, 1.f));
         }
     }
-    {  // K .* Gamma and Kbar = diag(rho_k) K .* prod_{t>r} a_t, row r = tid >> 3, 16 channels each
-        const int r = tid >> 3, q8 = tid & 7;
+    {  // K .* Gamma and Kbar = diag(rho_k) K .* prod_{t>r} a_t, 16 channels of row r each (a quarter
+       // warp takes 8 rows at the same channels)
+        const int r = (tid & 7) + 8 * (tid >> 6), q8 = (tid >> 3) & 7;
         const float rk = rho[r];
 #pragma unroll
         for (int q = 0; q < 2; q++) {
             const int j = 2 * q8 + q;  // 8-channel chunk of the row
             float x[8], yg[8], yb[8];
             unpack8(ld_shared_v4(sb + CS_KQ + sw128_chunk(r, j, 128)), x);
-            const float4* g4 = reinterpret_cast<const float4*>(gp + r * kD + 8 * j);
-            const float4* b4 = reinterpret_cast<const float4*>(al + r * kD + 8 * j);
-            const float4 g0 = g4[0], g1 = g4[1], b0 = b4[0], b1 = b4[1];
+            const float4 g0 = *reinterpret_cast<const float4*>(gp + dix(r, 8 * j));
+            const float4 g1 = *reinterpret_cast<const float4*>(gp + dix(r, 8 * j + 4));
+            const float4 b0 = *reinterpret_cast<const float4*>(al + dix(r, 8 * j));
+            const float4 b1 = *reinterpret_cast<const float4*>(al + dix(r, 8 * j + 4));
             const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
             const float bb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
@@ -518,8 +525,8 @@ __global__ void __launch_bounds__(PCH_THREADS, 1)
                 for (int q = 0; q < 4; q++) {
                     float x[8];
                     unpack8(qv[q], x);
-                    const float4* g4 = reinterpret_cast<const float4*>(gp + i * kD + 32 * h + 8 * q);
-                    const float4 g0 = g4[0], g1 = g4[1];
+                    const float4 g0 = *reinterpret_cast<const float4*>(gp + dix(i, 32 * h + 8 * q));
+                    const float4 g1 = *reinterpret_cast<const float4*>(gp + dix(i, 32 * h + 8 * q + 4));
                     const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 #pragma unroll
                     for (int e = 0; e < 8; e++) x[e] = f * x[e] * gg[e] - pw[8 * q + e];

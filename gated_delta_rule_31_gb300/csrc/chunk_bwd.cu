@@ -242,6 +242,12 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
     t0 = c * kChunk;
     const int ntile = tile + (int)gridDim.x;  // the next tile of this CTA
     const int nc = ntile % P.NC, nhk = (ntile / P.NC) % P.Hk, nb = ntile / (P.NC * P.Hk);
+    if (tid == 0 && ntile < ntiles) {  // its k, q into L2 now: their copy into shared memory, issued at
+        for (int h = 0; h < 2; h++) {  // this tile's end, is then served from L2
+            tma_prefetch_4d(&mk, 64 * h, nhk, nc * kChunk, nb);
+            tma_prefetch_4d(&mq, 64 * h, nhk, nc * kChunk, nb);
+        }
+    }
     if (!wait_ld(40)) goto teardown;
     {  // norm factors: 4 threads per row, 32 elements each
         const int row = tid >> 2, pp = tid & 3;
@@ -541,6 +547,8 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
         }
         if (!wait_mma(46)) goto teardown;
         if (more && tid == 0) prefetch(1);
+        float dvv[16];  // this lane's 16 values of dv: stored once M5 is issued, because the proxy
+                        // fence before M5 would otherwise wait for the global stores to complete
         {
             {  // dT_rj = beta_j (dU V^T + Gamma_j rk_j dW K^T)_rj -> dT image (ZS, free until M6's epilogue)
                 float d1[16], d2[16], w1[8], w2[8];
@@ -561,26 +569,21 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
                 float x[32], w[16];
                 tmem_ld32(tl + TM_T2 + c32, x);
                 tmem_wait_ld();
-                split_cols<32>(x, w, lane);
-                const int hf = lane >> 4;  // this lane's 16 columns: c32 + 16 hf ..
+                split_cols_sector(x, w, lane);
+                const int hf = lane >> 4;  // this lane's columns: c32 + 8 q + 4 hf + 0..3
                 float dot = 0.f;
 #pragma unroll
-                for (int q = 0; q < 2; q++) {
+                for (int q = 0; q < 4; q++) {
                     float vv[8];
-                    ldrow8(G_V, r, 4 * qt + 2 * hf + q, 64, vv);
+                    ldrow8(G_V, r, 4 * qt + q, 64, vv);
 #pragma unroll
-                    for (int e = 0; e < 8; e++) dot += vv[e] * w[8 * q + e];
+                    for (int i = 0; i < 4; i++) dot += (hf ? vv[4 + i] : vv[i]) * w[4 * q + i];
                 }
                 dot += __shfl_xor_sync(0xffffffffu, dot, 16);
                 if (act) dbp[qt * 64 + r] += dot;
-                if (t0 + r < P.T) {
-                    const float bb = bet[r];
-                    float4* dst = reinterpret_cast<float4*>(a.dv + (((size_t)b * P.T + t0 + r) * P.Hv + hv) * kD +
-                                                            c32 + 16 * hf);
+                const float bb = bet[r];
 #pragma unroll
-                    for (int q = 0; q < 4; q++)
-                        dst[q] = make_float4(bb * w[4 * q], bb * w[4 * q + 1], bb * w[4 * q + 2], bb * w[4 * q + 3]);
-                }
+                for (int e = 0; e < 16; e++) dvv[e] = bb * w[e];
             }
         }
         sync_for_mma();
@@ -594,6 +597,13 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
                     k0 > 0);
             }
             mma_commit(&bar_mma);
+        }
+        if (t0 + r < P.T) {  // dv = beta T^T dU (column groups c32 + 8 q + 4 (lane >> 4))
+            float* dst = a.dv + (((size_t)b * P.T + t0 + r) * P.Hv + hv) * kD + c32 + 4 * (lane >> 4);
+#pragma unroll
+            for (int q = 0; q < 4; q++)
+                *reinterpret_cast<float4*>(dst + 8 * q) =
+                    make_float4(dvv[4 * q], dvv[4 * q + 1], dvv[4 * q + 2], dvv[4 * q + 3]);
         }
         if (!wait_mma(47)) goto teardown;
         if (more && tid == 0) prefetch(2);
@@ -756,7 +766,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
     }
 
     // ---------------------------------------------------------------- dq, dk: norm backward
-    {  // lane l < 16 takes columns c32 .. c32 + 15 of row r, lane l + 16 the next 16 (64 bytes each)
+    {  // row r, columns c32 + 8 q + 4 hf + 0..3 (q < 4): lanes l and l + 16 fill 32-byte sectors
         const int hf = lane >> 4;
         const bool rv = t0 + r < P.T;
         float x[32], w[16], xx[16];
@@ -766,13 +776,17 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
             const int krow = which == 0 ? 64 + r : r;
             tmem_ld32(tl + (which == 0 ? TM_DQ : TM_DK) + c32, x);
             tmem_wait_ld();
-            split_cols<32>(x, w, lane);
+            split_cols_sector(x, w, lane);
             float dot = 0.f;
 #pragma unroll
-            for (int q = 0; q < 2; q++) {
-                ldrow8(kq, krow, 4 * qt + 2 * hf + q, 128, xx + 8 * q);
+            for (int q = 0; q < 4; q++) {
+                float x8[8];
+                ldrow8(kq, krow, 4 * qt + q, 128, x8);
 #pragma unroll
-                for (int e = 0; e < 8; e++) dot += xx[8 * q + e] * w[8 * q + e];
+                for (int i = 0; i < 4; i++) {
+                    xx[4 * q + i] = hf ? x8[4 + i] : x8[i];
+                    dot += xx[4 * q + i] * w[4 * q + i];
+                }
             }
             dot += __shfl_xor_sync(0xffffffffu, dot, 16);
             if (act) part[qt * 64 + r] = dot;
@@ -780,8 +794,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
             if (rv) {
                 const float rr = rho[r];
                 const float full = part[r] + part[64 + r] + part[128 + r] + part[192 + r];
-                float* dst = (which == 0 ? a.dq : a.dk) + (((size_t)b * P.T + t0 + r) * P.Hk + hk) * kD + c32 + 16 * hf;
-                float4* d4 = reinterpret_cast<float4*>(dst);
+                float* dst = (which == 0 ? a.dq : a.dk) + (((size_t)b * P.T + t0 + r) * P.Hk + hk) * kD + c32 + 4 * hf;
 #pragma unroll
                 for (int q = 0; q < 4; q++) {
                     float o4[4];
@@ -790,7 +803,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
                         const int i = 4 * q + e;
                         o4[e] = P.use_norm ? rr * (w[i] - rr * xx[i] * rr * full) : w[i];
                     }
-                    d4[q] = make_float4(o4[0], o4[1], o4[2], o4[3]);
+                    *reinterpret_cast<float4*>(dst + 8 * q) = make_float4(o4[0], o4[1], o4[2], o4[3]);
                 }
             }
             tc_fence_before();

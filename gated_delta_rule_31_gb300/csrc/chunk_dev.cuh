@@ -39,6 +39,19 @@ __device__ __forceinline__ void split_cols(const float* v, float* w, int lane) {
     }
 }
 
+// The same split of N = 32 columns with the 4-column groups interleaved: lane l < 16 takes columns
+// 8 q + 0..3 and lane l + 16 columns 8 q + 4..7 (q < 4), w[4 q + i]. A 16-byte store of group q by
+// both lanes then fills one 32-byte sector of the row.
+__device__ __forceinline__ void split_cols_sector(const float* v, float* w, int lane) {
+#pragma unroll
+    for (int q = 0; q < 4; q++)
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            const float hi = __shfl_sync(0xffffffffu, v[8 * q + 4 + i], lane & 15);
+            w[4 * q + i] = (lane >> 4) ? hi : v[8 * q + i];
+        }
+}
+
 // T = (I + A)^-1 for the strictly lower triangular fp32 A [64 x 64] (row stride LDA), by 16 x 16
 // blocks. Phase 1 (160 threads, one column each): forward substitution with L_II = I + A_II
 // gives the diagonal inverses T_II (right-hand side e_c) and Y_IK = T_II A_IK for I > K

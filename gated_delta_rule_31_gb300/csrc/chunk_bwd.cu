@@ -44,7 +44,8 @@ constexpr uint32_t G_GF = 180224;   // G = K K^T fp32 [64][64]                  
 constexpr uint32_t G_ZS = 196608;   // fp32 [64][64] scratch (column sums)
 constexpr uint32_t G_SM = 212992;   // small arrays
 constexpr uint32_t G_SM_FLOATS = 64 * 4 + 256 * 4 + 64 + 272 + 4 + 128;  // see the carve-up in grad_kernel
-constexpr uint32_t G_BYTES = G_SM + 7168;
+constexpr uint32_t G_STG = G_SM + 7168;  // per warp 4 rows x 40 fp32: staging of the fp32 row stores
+constexpr uint32_t G_BYTES = G_STG + 16 * 4 * 40 * 4;
 static_assert(G_SM_FLOATS * 4 <= 7168, "small arrays");
 static_assert(G_BYTES + 1024 <= 232448, "grad smem");
 
@@ -105,6 +106,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
     float* red = dgc + 64;                              // [16 + 256] reductions
     float* hdh = red + 272;                             // <dH1, H0>
     float* gst = hdh + 4;                               // [2][64] the next value head's g, beta (cp.async)
+    float* stg = reinterpret_cast<float*>(sm + G_STG) + warp * 160;  // this warp's row-store staging
 
     uint32_t ld_phase = 0, mma_phase = 0, h_phase = 0, h2_phase = 0;
     bool pend_ld = false, pend_h = false, pend_h2 = false;  // copies issued and not yet waited for (thread 0)
@@ -151,6 +153,29 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
     // 8 bf16 of row `row` of a panelised tile, logical chunk j
     auto ldrow8 = [&](uint32_t tile, int row, int j, int R, float* x) {
         unpack8(ld_shared_v4(sb + tile + sw128_chunk(row, j, R)), x);
+    };
+    // fp32 rows of a [64 x 128] result tile to global memory: this warp holds rows 16 lg .. + 15 of
+    // column quarter qt, lane l (l & 15: the row) the groups c32 + 8 q + 4 (l >> 4) .. + 3 (q < 4).
+    // Four rows at a time go through the warp's staging so that each store instruction writes four
+    // whole 128-byte row segments (8 lanes each) instead of one 32-byte sector in each of 16 rows,
+    // which stalled the warps on the store queue. g0: row 0 of the tile at column c32; rs: floats
+    // per row. Rows past the sequence end are not written.
+    auto store_rows = [&](float* g0, size_t rs, const float* v) {
+        const int hf = lane >> 4, rl = lane & 15, m = lane >> 3, cg = lane & 7;
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            if ((rl >> 2) == i) {
+#pragma unroll
+                for (int q = 0; q < 4; q++)
+                    *reinterpret_cast<float4*>(stg + (rl & 3) * 40 + 8 * q + 4 * hf) =
+                        make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            }
+            __syncwarp();
+            const int row = 16 * lg + 4 * i + m;
+            const float4 x = *reinterpret_cast<const float4*>(stg + m * 40 + 4 * cg);
+            if (t0 + row < P.T) *reinterpret_cast<float4*>(g0 + (size_t)row * rs + 4 * cg) = x;
+            __syncwarp();
+        }
     };
     const uint32_t id64x128_kk = idesc_bf16(64, 128, 0, 0), id64x128_km = idesc_bf16(64, 128, 0, 1),
                    id64x128_mm = idesc_bf16(64, 128, 1, 1), id64x64_kk = idesc_bf16(64, 64, 0, 0),
@@ -598,13 +623,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
             }
             mma_commit(&bar_mma);
         }
-        if (t0 + r < P.T) {  // dv = beta T^T dU (column groups c32 + 8 q + 4 (lane >> 4))
-            float* dst = a.dv + (((size_t)b * P.T + t0 + r) * P.Hv + hv) * kD + c32 + 4 * (lane >> 4);
-#pragma unroll
-            for (int q = 0; q < 4; q++)
-                *reinterpret_cast<float4*>(dst + 8 * q) =
-                    make_float4(dvv[4 * q], dvv[4 * q + 1], dvv[4 * q + 2], dvv[4 * q + 3]);
-        }
+        store_rows(a.dv + (((size_t)b * P.T + t0) * P.Hv + hv) * kD + c32, (size_t)P.Hv * kD, dvv);  // dv
         if (!wait_mma(47)) goto teardown;
         if (more && tid == 0) prefetch(2);
         {
@@ -768,7 +787,6 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
     // ---------------------------------------------------------------- dq, dk: norm backward
     {  // row r, columns c32 + 8 q + 4 hf + 0..3 (q < 4): lanes l and l + 16 fill 32-byte sectors
         const int hf = lane >> 4;
-        const bool rv = t0 + r < P.T;
         float x[32], w[16], xx[16];
 #pragma unroll 1
         for (int which = 0; which < 2; which++) {  // 0: q, 1: k
@@ -791,20 +809,14 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
             dot += __shfl_xor_sync(0xffffffffu, dot, 16);
             if (act) part[qt * 64 + r] = dot;
             __syncthreads();
-            if (rv) {
+            {
                 const float rr = rho[r];
                 const float full = part[r] + part[64 + r] + part[128 + r] + part[192 + r];
-                float* dst = (which == 0 ? a.dq : a.dk) + (((size_t)b * P.T + t0 + r) * P.Hk + hk) * kD + c32 + 4 * hf;
+                float o[16];
 #pragma unroll
-                for (int q = 0; q < 4; q++) {
-                    float o4[4];
-#pragma unroll
-                    for (int e = 0; e < 4; e++) {
-                        const int i = 4 * q + e;
-                        o4[e] = P.use_norm ? rr * (w[i] - rr * xx[i] * rr * full) : w[i];
-                    }
-                    *reinterpret_cast<float4*>(dst + 8 * q) = make_float4(o4[0], o4[1], o4[2], o4[3]);
-                }
+                for (int i = 0; i < 16; i++) o[i] = P.use_norm ? rr * (w[i] - rr * xx[i] * rr * full) : w[i];
+                store_rows((which == 0 ? a.dq : a.dk) + (((size_t)b * P.T + t0) * P.Hk + hk) * kD + c32,
+                           (size_t)P.Hk * kD, o);
             }
             tc_fence_before();
             __syncthreads();

@@ -48,7 +48,8 @@ constexpr uint32_t C_KG = 131072;   // K^ .* Gamma image [64 x 128]
 constexpr uint32_t C_P = 147456;    // P image [64 x 64]
 constexpr uint32_t C_T = 155648;    // T image [64 x 64]
 constexpr uint32_t C_SM = 163840;   // bet[64], dbp[4][64]
-constexpr uint32_t C_BYTES = C_SM + 2048;
+constexpr uint32_t C_STG = C_SM + 2048;  // per warp 4 rows x 36 fp32: staging of the fp32 row stores
+constexpr uint32_t C_BYTES = C_STG + 16 * 4 * 36 * 4;
 constexpr uint32_t TM1 = 0, TM2 = 128;  // TMEM columns of the two accumulators
 constexpr int CH_THREADS = 512;
 
@@ -80,6 +81,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
     const int c32 = 32 * qt, c16 = 16 * qt;
     float* bet = reinterpret_cast<float*>(sm + C_SM);
     float* dbp = bet + 64;  // [4][64] V . (T^T dU) partials by column quarter
+    float* stg = reinterpret_cast<float*>(sm + C_STG) + warp * 144;  // this warp's row-store staging
     uint32_t mph = 0;
     bool ok = true;
 
@@ -128,6 +130,29 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
     };
     auto mma = [&](uint32_t col, uint64_t ad, uint64_t bd, uint32_t id, bool acc) {
         mma_bf16(tm + col, ad, bd, id, acc ? 1u : 0u);
+    };
+    // fp32 rows of a [64 x 128] result tile to global memory: this warp holds rows 16 lg .. + 15 of
+    // column quarter qt, lane l (l & 15: the row) columns c32 + 16 (l >> 4) .. + 15. Four rows at
+    // a time go through the warp's staging so that each store instruction writes four whole 128-byte
+    // row segments (8 lanes each) instead of 64 bytes in each of 16 rows. The stores are issued after
+    // the next products, because the proxy fence before those would otherwise wait for them.
+    // g0: row 0 at column c32; rs: floats per row; rows at or past `rows` are not written.
+    auto store_rows = [&](float* g0, size_t rs, const float* v, int rows) {
+        const int rl = lane & 15, m = lane >> 3, cg = lane & 7;
+#pragma unroll
+        for (int i = 0; i < 4; i++) {
+            if ((rl >> 2) == i) {
+#pragma unroll
+                for (int q = 0; q < 4; q++)
+                    *reinterpret_cast<float4*>(stg + (rl & 3) * 36 + 16 * hf + 4 * q) =
+                        make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            }
+            __syncwarp();
+            const int row = 16 * lg + 4 * i + m;
+            const float4 x = *reinterpret_cast<const float4*>(stg + m * 36 + 4 * cg);
+            if (row < rows) *reinterpret_cast<float4*>(g0 + (size_t)row * rs + 4 * cg) = x;
+            __syncwarp();
+        }
     };
     const uint32_t id64x128_kk = idesc_bf16(64, 128, 0, 0), id64x128_km = idesc_bf16(64, 128, 0, 1),
                    id64x128_mm = idesc_bf16(64, 128, 1, 1), id64x64_kk = idesc_bf16(64, 64, 0, 0),
@@ -198,20 +223,19 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
         mma_commit(&bar_mma);
     }
     if (!wait_mma(62)) goto teardown;
+    float wx[16], up[8];  // X and dPs, exported once M3 is issued
     {
-        float x[32], w[16];
+        float x[32];
         tmem_ld32(tl + TM1 + c32, x);
         tmem_wait_ld();
-        split_cols<32>(x, w, lane);
-        st_f4x(chx + CHX_X / 4 + r * kD + c32 + 16 * hf, w, 4);
-        float v[16], u[8];
+        split_cols<32>(x, wx, lane);
+        float v[16];
         tmem_ld16(tl + TM2 + c16, v);
         tmem_wait_ld();
-        split_cols<16>(v, u, lane);
+        split_cols<16>(v, up, lane);
         const int j0 = c16 + 8 * hf;
 #pragma unroll
-        for (int e = 0; e < 8; e++) u[e] = (j0 + e <= r) ? P.scale * u[e] : 0.f;
-        st_f4x(chx + CHX_DP / 4 + r * kChunk + j0, u, 2);
+        for (int e = 0; e < 8; e++) up[e] = (j0 + e <= r) ? P.scale * up[e] : 0.f;
     }
     sync_for_mma();
 
@@ -224,13 +248,15 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
         }
         mma_commit(&bar_mma);
     }
+    store_rows(chx + CHX_X / 4 + c32, kD, wx, kChunk);
+    st_f4x(chx + CHX_DP / 4 + r * kChunk + c16 + 8 * hf, up, 2);
     if (!wait_mma(63)) goto teardown;
+    float wy[16];  // Y, exported once M4 is issued
     {
         float x[32], w[16];
         tmem_ld32(tl + TM1 + c32, x);
         tmem_wait_ld();
-        split_cols<32>(x, w, lane);
-        st_f4x(chx + CHX_Y / 4 + r * kD + c32 + 16 * hf, w, 4);
+        split_cols<32>(x, wy, lane);
         tmem_ld32(tl + TM2 + c32, x);  // dW = -dWn -> dW image (over H0, which is no longer read)
         tmem_wait_ld();
         split_cols<32>(x, w, lane);
@@ -250,7 +276,9 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
             mma(TM2, desc_mnmajor(sb + C_T, 64, 0, k0), desc_mnmajor(sb + C_KB, 64, 0, k0), id64x128_mm, k0 > 0);
         mma_commit(&bar_mma);
     }
+    store_rows(chx + CHX_Y / 4 + c32, kD, wy, kChunk);
     if (!wait_mma(64)) goto teardown;
+    float wv[16];  // dv, stored once M5 is issued
     {
         {  // dT_rj = beta_j (dU V^T + dW (K^ .* Gamma)^T)_rj -> dT image (C_DH)
             float d1[16], d2[16], w1[8], w2[8];
@@ -279,12 +307,9 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
             }
             dot += __shfl_xor_sync(0xffffffffu, dot, 16);
             if (act) dbp[qt * 64 + r] = dot;
-            if (t0 + r < P.T) {
-                const float bb = bet[r];
+            const float bb = bet[r];
 #pragma unroll
-                for (int e = 0; e < 16; e++) w[e] *= bb;
-                st_f4x(a.dv + (((size_t)b * P.T + t0 + r) * P.Hv + hv) * kD + c32 + 16 * hf, w, 4);
-            }
+            for (int e = 0; e < 16; e++) wv[e] = bb * w[e];
         }
     }
     sync_for_mma();
@@ -298,13 +323,14 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
         }
         mma_commit(&bar_mma);
     }
+    store_rows(a.dv + (((size_t)b * P.T + t0) * P.Hv + hv) * kD + c32, (size_t)P.Hv * kD, wv, P.T - t0);
     if (!wait_mma(65)) goto teardown;
+    float wz[16];  // Z, exported once M6 is issued
     {
-        float x[32], w[16];
+        float x[32];
         tmem_ld32(tl + TM2 + c32, x);
         tmem_wait_ld();
-        split_cols<32>(x, w, lane);
-        st_f4x(chx + CHX_Z / 4 + r * kD + c32 + 16 * hf, w, 4);
+        split_cols<32>(x, wz, lane);
         float v[16], u[8];
         tmem_ld16(tl + TM1 + c16, v);
         tmem_wait_ld();
@@ -321,6 +347,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
                 k0 > 0);
         mma_commit(&bar_mma);
     }
+    store_rows(chx + CHX_Z / 4 + c32, kD, wz, kChunk);
     if (!wait_mma(66)) goto teardown;
     {
         float v[16], u[8];

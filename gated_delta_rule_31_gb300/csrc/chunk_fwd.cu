@@ -285,11 +285,7 @@ __global__ void __launch_bounds__(256, 2)
                     }
                 }
 #pragma unroll
-                for (int q = 0; q < 4; q++) {
-                    st_chunk(sb + PS_TT + sw128_chunk(row, 4 * half + q, 128), x + 8 * q, 1.f);
-                    if (isw && rec2)  // T itself for the backward
-                        st_global16(rec2 + REC2_T + sw128_chunk(i, 4 * half + q, 64), pack8(t + 8 * q, 1.f));
-                }
+                for (int q = 0; q < 4; q++) st_chunk(sb + PS_TT + sw128_chunk(row, 4 * half + q, 128), x + 8 * q, 1.f);
             }
             fence_proxy_async_smem();
             __syncthreads();
@@ -311,6 +307,22 @@ __global__ void __launch_bounds__(256, 2)
                     }
                     mma_commit(&bar_mma);
                     v_ph ^= 1;
+                }
+            }
+            if (rec2 && tid < 128) {  // T itself for the backward, from the fp32 tile (intact until the
+                // W/U~ epilogue), stored once the products are issued: the proxy fence before them
+                // would otherwise wait for these global stores
+                const int i = tid >> 1, half = tid & 1;
+                const float* trow = Tm + i * LDA + 32 * half;
+#pragma unroll
+                for (int q = 0; q < 4; q++) {
+                    float t[8];
+#pragma unroll
+                    for (int e = 0; e < 8; e++) {
+                        const int j = 32 * half + 8 * q + e;
+                        t[e] = (j >> 4) <= (i >> 4) ? trow[8 * q + e] : 0.f;
+                    }
+                    st_global16(rec2 + REC2_T + sw128_chunk(i, 4 * half + q, 64), pack8(t, 1.f));
                 }
             }
             ok = mbar_wait(&bar_mma, mph, &abort_sh, a.status, 12);

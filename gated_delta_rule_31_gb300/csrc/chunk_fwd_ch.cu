@@ -390,11 +390,7 @@ __global__ void __launch_bounds__(PCH_THREADS, 1)
             }
         }
 #pragma unroll
-        for (int q = 0; q < 2; q++) {
-            st_chunk(sb + CS_A + sw128_chunk(row, 2 * qtr + q, 128), x + 8 * q, 1.f);
-            if (isw && rec2)  // T itself for the backward
-                st_global16(rec2 + REC2_T + sw128_chunk(i, 2 * qtr + q, 64), pack8(t + 8 * q, 1.f));
-        }
+        for (int q = 0; q < 2; q++) st_chunk(sb + CS_A + sw128_chunk(row, 2 * qtr + q, 128), x + 8 * q, 1.f);
     }
     {  // K .* Gamma and Kbar = diag(rho_k) K .* prod_{t>r} a_t, 16 channels of row r each (a quarter
        // warp takes 8 rows at the same channels)
@@ -418,7 +414,6 @@ __global__ void __launch_bounds__(PCH_THREADS, 1)
             }
             const uint32_t off = sw128_chunk(r, j, 64);
             st_chunk(sb + CS_KG + off, yg, 1.f);
-            if (rec2) st_global16(rec2 + REC2_KG + off, pack8(yg, rk));  // K^ .* Gamma
             const uint4 ub = pack8(yb, 1.f);
             st_shared_v4(sb + CS_KB + off, ub.x, ub.y, ub.z, ub.w);
         }
@@ -445,6 +440,37 @@ __global__ void __launch_bounds__(PCH_THREADS, 1)
         }
         mma_commit(&bar_mma);
         mma_pend = true;
+    }
+    if (rec2) {  // T and K^ .* Gamma for the backward, from tiles still intact, stored once the
+                 // products are issued: the proxy fence before them would wait for these stores
+        if (tid < 256) {
+            const int i = tid >> 2, qtr = tid & 3;
+            const float* trow = Tm + i * LDA + 16 * qtr;
+#pragma unroll
+            for (int q = 0; q < 2; q++) {
+                float t[8];
+#pragma unroll
+                for (int e = 0; e < 8; e++) {
+                    const int j = 16 * qtr + 8 * q + e;
+                    t[e] = (j >> 4) <= (i >> 4) ? trow[8 * q + e] : 0.f;
+                }
+                st_global16(rec2 + REC2_T + sw128_chunk(i, 2 * qtr + q, 64), pack8(t, 1.f));
+            }
+        }
+        const int r = (tid & 7) + 8 * (tid >> 6), q8 = (tid >> 3) & 7;
+        const float rk = rho[r];
+#pragma unroll
+        for (int q = 0; q < 2; q++) {
+            const int j = 2 * q8 + q;
+            float x[8];
+            unpack8(ld_shared_v4(sb + CS_KQ + sw128_chunk(r, j, 128)), x);
+            const float4 g0 = *reinterpret_cast<const float4*>(gp + dix(r, 8 * j));
+            const float4 g1 = *reinterpret_cast<const float4*>(gp + dix(r, 8 * j + 4));
+            const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+            for (int e = 0; e < 8; e++) x[e] *= gg[e];
+            st_global16(rec2 + REC2_KG + sw128_chunk(r, j, 64), pack8(x, rk));
+        }
     }
     ok = mbar_wait(&bar_mma, mph, &abort_sh, a.status, 16);
     mph ^= 1;

@@ -364,24 +364,6 @@ __global__ void __launch_bounds__(256, 2)
                             st_chunk(sb + PS_V + (col >> 5) * 4096 + sw64_chunk(i, q), u + 8 * q, 1.f);
                     }
                 }
-                // Kbar = diag(exp(gamma_C - gamma) rho_k) K, straight to the record
-                {
-                    uint4 kv[4];
-                    float fr[4];
-#pragma unroll
-                    for (int n = 0; n < 4; n++) {
-                        const int idx = tid + 256 * n, r = idx >> 4, j = idx & 15;
-                        kv[n] = ld_shared_v4(sb + PS_KQ + sw128_chunk(r, j, 128));
-                        fr[n] = fb[r];
-                    }
-#pragma unroll
-                    for (int n = 0; n < 4; n++) {
-                        const int idx = tid + 256 * n, r = idx >> 4, j = idx & 15;
-                        float x[8];
-                        unpack8(kv[n], x);
-                        st_global16(rec + REC_K + sw128_chunk(r, j, 64), pack8(x, fr[n]));
-                    }
-                }
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -402,6 +384,24 @@ __global__ void __launch_bounds__(256, 2)
                     mma_bf16(tm + 128, desc_kmajor(sb + PS_P, 64, 0, k0), desc_mnmajor(sb + PS_W, 64, 0, k0), idp,
                              k0 > 0);
                 mma_commit(&bar_mma);
+            }
+            {  // Kbar = diag(exp(gamma_C - gamma) rho_k) K, straight to the record once the products are
+               // issued (the proxy fence before them would otherwise wait for these global stores)
+                uint4 kv[4];
+                float fr[4];
+#pragma unroll
+                for (int n = 0; n < 4; n++) {
+                    const int idx = tid + 256 * n, r = idx >> 4, j = idx & 15;
+                    kv[n] = ld_shared_v4(sb + PS_KQ + sw128_chunk(r, j, 128));
+                    fr[n] = fb[r];
+                }
+#pragma unroll
+                for (int n = 0; n < 4; n++) {
+                    const int idx = tid + 256 * n, r = idx >> 4, j = idx & 15;
+                    float x[8];
+                    unpack8(kv[n], x);
+                    st_global16(rec + REC_K + sw128_chunk(r, j, 64), pack8(x, fr[n]));
+                }
             }
             ok = mbar_wait(&bar_mma, mph, &abort_sh, a.status, 13);
             mph ^= 1;

@@ -2,7 +2,8 @@
 //   prep_kernel : persistent, two CTAs per SM; a CTA takes (b, key head, chunk) groups in
 //                 turn and, for each, the value heads sharing that key head one after the
 //                 other (k, q and their norms loaded once per group; the next head's v is
-//                 fetched while the current head finishes). Builds each chunk's operators
+//                 fetched while the current head finishes). When there are too few groups to
+//                 give every SM a CTA, each value head is a unit of its own (prep_kernel<true>). Builds each chunk's operators
 //                 (UT/WY transform of the k k^T beta block, output and state operators) on
 //                 tcgen05 with TMEM accumulators and writes them as ready-to-use
 //                 shared-memory images.
@@ -53,6 +54,7 @@ static_assert(PS_A % 1024 == 0 && PS_T % 1024 == 0 && PS_P % 1024 == 0, "align")
 static_assert(PS_A + 64 * LDA * 4 <= PS_T && PS_T + 64 * LDA * 4 <= PS_P, "fp32 tiles");
 static_assert(2 * (PS_BYTES + 1024) <= 228 * 1024, "two prep CTAs per SM");
 
+template <bool kSplit>
 __global__ void __launch_bounds__(256, 2)
     prep_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                 const __grid_constant__ CUtensorMap mv, PrepArgs a) {
@@ -66,6 +68,9 @@ __global__ void __launch_bounds__(256, 2)
     const ChunkProblem& P = a.p;
     const int G = P.Hv / P.Hk;
     const int ngroups = P.B * P.Hk * P.NC;  // (b, key head, chunk); its G value heads run in turn
+    // A work unit is a group's value heads, or (kSplit, when the groups alone would leave SMs idle)
+    // one of them, each unit then loading the group's k and q itself.
+    const int parts = kSplit ? G : 1, hpp = kSplit ? 1 : G, nunits = ngroups * parts;
     float* gam = reinterpret_cast<float*>(sm + PS_SMALL);  // in-chunk cumulative log-decay
     float* bet = gam + 64;
     float* rho = bet + 64;   // [128] rows 0-63: k norm factors, 64-127: q norm factors
@@ -111,7 +116,7 @@ __global__ void __launch_bounds__(256, 2)
         cp_async_commit();
     };
 
-    if (tid < 64 && (int)blockIdx.x < ngroups) stage_gb(blockIdx.x, 0);
+    if (tid < 64 && (int)blockIdx.x < nunits) stage_gb(blockIdx.x / parts, (blockIdx.x % parts) * hpp);
     if (tid == 0) {
         abort_sh = 0;
         mbar_init(&bar_kq, 1);
@@ -127,20 +132,22 @@ __global__ void __launch_bounds__(256, 2)
     __syncthreads();
     tc_fence_after();
     const uint32_t tm = tmem_sh;
-    if (tid == 0 && (int)blockIdx.x < ngroups) {
-        issue_kq(blockIdx.x);
-        issue_v(blockIdx.x, 0);
+    if (tid == 0 && (int)blockIdx.x < nunits) {
+        issue_kq(blockIdx.x / parts);
+        issue_v(blockIdx.x / parts, (blockIdx.x % parts) * hpp);
     }
 
-    for (int grp = blockIdx.x; grp < ngroups; grp += gridDim.x) {
+    for (int unit = blockIdx.x; unit < nunits; unit += gridDim.x) {
+        const int grp = unit / parts, hb = (unit % parts) * hpp, he = hb + hpp;  // heads hb .. he - 1
         const int c = grp % P.NC, hk = (grp / P.NC) % P.Hk, b = grp / (P.NC * P.Hk);
-        const int next = grp + (int)gridDim.x;
+        const int nunit = unit + (int)gridDim.x;  // this CTA's next unit: its group and first head
+        const int next = nunit < nunits ? nunit / parts : ngroups, nh0 = (nunit % parts) * hpp;
         ok = mbar_wait(&bar_kq, kq_ph, &abort_sh, a.status, 10);
         kq_ph ^= 1;
         if (tid == 0) kq_pend = false;
         if (__syncthreads_or(!ok)) goto teardown;
 
-        for (int hh = 0; hh < G; hh++) {
+        for (int hh = hb; hh < he; hh++) {
             const int hv = hk * G + hh;
             const size_t bh = (size_t)b * P.Hv + hv;
             uint8_t* rec = a.rec + (bh * P.NC + c) * REC_BYTES;
@@ -168,7 +175,7 @@ __global__ void __launch_bounds__(256, 2)
                 gam[tid] = gv;
                 bet[tid] = bv;
             }
-            if (hh == 0) {  // L2 norm factors of the 64 keys (rows 0-63) and 64 queries (rows 64-127)
+            if (hh == hb) {  // L2 norm factors of the 64 keys (rows 0-63) and 64 queries (rows 64-127)
                 const int row = tid >> 1, half = tid & 1;
                 const uint32_t base = sb + PS_KQ + half * 16384 + row * 128;
                 float ss = 0.f;
@@ -329,8 +336,8 @@ __global__ void __launch_bounds__(256, 2)
             mph ^= 1;
             if (__syncthreads_or(!ok)) goto teardown;
             if (tid < 64) {  // the next value head's gates (or the next group's first)
-                if (hh + 1 < G) stage_gb(grp, hh + 1);
-                else if (next < ngroups) stage_gb(next, 0);
+                if (hh + 1 < he) stage_gb(grp, hh + 1);
+                else if (next < ngroups) stage_gb(next, nh0);
             }
             tc_fence_after();
             {
@@ -407,8 +414,8 @@ __global__ void __launch_bounds__(256, 2)
             mph ^= 1;
             if (tid == 0) {
                 bulk_wait_read_all();  // the P, U~ and W images are read: the staging may overwrite them,
-                if (hh + 1 < G) issue_v(grp, hh + 1);  // and the next value head's v (or the next
-                else if (next < ngroups) issue_v(next, 0);  // group's first) may land over U~
+                if (hh + 1 < he) issue_v(grp, hh + 1);  // and the next value head's v (or the next
+                else if (next < ngroups) issue_v(next, nh0);  // unit's first) may land over U~
             }
             if (__syncthreads_or(!ok)) goto teardown;
             tc_fence_after();
@@ -471,9 +478,9 @@ __global__ void __launch_bounds__(256, 2)
                 bulk_store(rec + REC_Q, sm + PS_STAGE_Q, 16384);
                 bulk_commit();
             }
-        }  // value heads of the group
+        }  // value heads of the unit
         if (tid == 0 && next < ngroups) issue_kq(next);  // k, q are no longer read
-    }  // groups
+    }  // units
 teardown:
     cp_async_wait_all();
     if (tid == 0) bulk_wait_all();  // record stores complete
@@ -491,7 +498,9 @@ teardown:
 cudaError_t launch_prep(const PrepArgs& a, const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
                         cudaStream_t s) {
     const int smem = PS_BYTES + 1024;
-    cudaError_t e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e = cudaFuncSetAttribute(prep_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(prep_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     static int nsm = 0;  // 2 CTAs fit an SM (smem, TMEM, registers): a persistent grid of 2 per SM
     if (nsm == 0) {
@@ -499,10 +508,15 @@ cudaError_t launch_prep(const PrepArgs& a, const CUtensorMap& mq, const CUtensor
         if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
         if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     }
-    const int ngroups = a.p.B * a.p.Hk * a.p.NC;
-    dim3 grid(ngroups < 2 * nsm ? ngroups : 2 * nsm);
+    const int ngroups = a.p.B * a.p.Hk * a.p.NC, G = a.p.Hv / a.p.Hk;
+    const bool split = (long)ngroups * G <= nsm;  // one value head per unit when each still gets an SM
+    const int nunits = split ? ngroups * G : ngroups;
+    dim3 grid(nunits < 2 * nsm ? nunits : 2 * nsm);
     trace_begin("chunk_prep", s);
-    prep_kernel<<<grid, 256, smem, s>>>(mq, mk, mv, a);
+    if (split)
+        prep_kernel<true><<<grid, 256, smem, s>>>(mq, mk, mv, a);
+    else
+        prep_kernel<false><<<grid, 256, smem, s>>>(mq, mk, mv, a);
     trace_end(s);
     return cudaGetLastError();
 }

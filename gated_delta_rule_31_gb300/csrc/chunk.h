@@ -56,12 +56,21 @@ struct WsLayout {
     size_t hs;       // bwd: chunk-start states [B*Hv][NC] images
     size_t dhs;      // bwd: chunk-end state gradients [B*Hv][NC] images
     size_t chx;      // bwd, per-channel gate: tensor-core exports [B*Hv][NC]
-    size_t dqh, dkh; // bwd, per-channel gate: dq^, dk^ per value head, fp32 [B][T][Hv][Dk]
+    size_t dqh, dkh; // bwd, per-channel gate or split gradient: dq^, dk^ per value head, fp32 [B][T][Hv][Dk]
     size_t total;
     int ncpad;
 };
 
 inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Scalar-gate backward of a small problem: when its (b, key head, chunk) tiles times the value heads
+// per key head number at most this, the gradient kernel takes one value head per CTA (so every head
+// has an SM) and writes dq^, dk^ per value head; a second kernel sums them over the key head's
+// value heads and applies the norm backward. The workspace then holds those two planes.
+constexpr int kGradSplitUnits = 128;
+inline bool grad_split(const ChunkProblem& p) {
+    return !p.channel && (long)p.B * p.Hk * p.NC * (p.Hv / p.Hk) <= kGradSplitUnits;
+}
 
 // bwd_states: a backward that reads saved chunk-start states (no states region of its own).
 inline WsLayout ws_layout(const ChunkProblem& p, bool bwd, bool bwd_states = false) {
@@ -83,6 +92,8 @@ inline WsLayout ws_layout(const ChunkProblem& p, bool bwd, bool bwd_states = fal
         if (p.channel) {
             w.chx = end;
             end = w.chx + nh * p.NC * (size_t)CHX_BYTES;
+        }
+        if (p.channel || grad_split(p)) {
             const size_t plane = round_up((size_t)p.B * p.T * p.Hv * kD * sizeof(float), 1024);
             w.dqh = end;
             w.dkh = end + plane;
@@ -120,7 +131,8 @@ inline SavedLayout saved_layout(const ChunkProblem& p) {
 inline size_t chunk_saved_bytes(const ChunkProblem& p) { return saved_layout(p).total; }
 constexpr size_t kSavedFwdWorkspace = 256;  // status word only
 // The backward's own workspace next to a saved buffer: the status word, the chunk-end state
-// gradients and, with a per-channel gate, the exports and per-value-head dq^, dk^.
+// gradients and, with a per-channel gate, the exports and per-value-head dq^, dk^ (also for a
+// split gradient).
 struct SavedBwdLayout {
     size_t dhs, chx, dqh, dkh, total;
 };
@@ -131,9 +143,12 @@ inline SavedBwdLayout saved_bwd_layout(const ChunkProblem& p) {
     l.total = l.dhs + nh * p.NC * (size_t)STATE_IMG;
     l.chx = l.dqh = l.dkh = 0;
     if (p.channel) {
-        const size_t plane = round_up((size_t)p.B * p.T * p.Hv * kD * sizeof(float), 1024);
         l.chx = l.total;
-        l.dqh = l.chx + nh * p.NC * (size_t)CHX_BYTES;
+        l.total = l.chx + nh * p.NC * (size_t)CHX_BYTES;
+    }
+    if (p.channel || grad_split(p)) {
+        const size_t plane = round_up((size_t)p.B * p.T * p.Hv * kD * sizeof(float), 1024);
+        l.dqh = l.total;
         l.dkh = l.dqh + plane;
         l.total = l.dkh + plane;
     }

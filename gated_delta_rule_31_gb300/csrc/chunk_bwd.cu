@@ -58,6 +58,7 @@ struct GradArgs {
     const uint8_t *rec, *rec2, *hs, *dhs;
     const float* gam;  // Gamma_C per chunk (unused here: recomputed)
     float *dq, *dk, *dv, *dg, *dbeta;
+    float *dqh, *dkh;  // split gradient (kSplit): dq^, dk^ per value head, fp32 [B][T][Hv][Dk]
     int* status;
 };
 
@@ -69,6 +70,9 @@ __device__ __forceinline__ int fsw(int r, int j) { return r * 64 + (j ^ (r & 31)
 // lanes 0-15) and column quarter (w >> 2) of every product.
 constexpr int GRAD_THREADS = 512;
 
+// kSplit: a work unit is one value head of a (b, key head, chunk) tile (small problems; see
+// grad_split): dq^, dk^ of that head leave raw, and a second kernel sums and normalises them.
+template <bool kSplit>
 __global__ void __launch_bounds__(GRAD_THREADS, 1)
     grad_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
                 const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo, GradArgs a) {
@@ -82,6 +86,8 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
     const ChunkProblem& P = a.p;
     const int G = P.Hv / P.Hk;
     const int ntiles = P.B * P.Hk * P.NC;  // (b, key head, chunk), chunk fastest
+    const int GU = kSplit ? G : 1;         // work units per tile
+    const int nunits = ntiles * GU;
     const int lg = warp & 3, qt = warp >> 2;
     const int r = 16 * lg + (lane & 15);
     const bool act = lane < 16;
@@ -250,24 +256,28 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
         }
     };
     // ---------------------------------------------------------------- persistent loop over tiles
-    if ((int)blockIdx.x < ntiles) {
-        const int t = blockIdx.x;
-        stage_gb(t / (P.NC * P.Hk), t % P.NC, ((t / P.NC) % P.Hk) * G);
+    if ((int)blockIdx.x < nunits) {
+        const int t = blockIdx.x / GU;
+        stage_gb(t / (P.NC * P.Hk), t % P.NC, ((t / P.NC) % P.Hk) * G + (int)blockIdx.x % GU);
     }
-    if (tid == 0 && (int)blockIdx.x < ntiles) {
-        const int t = blockIdx.x;
+    if (tid == 0 && (int)blockIdx.x < nunits) {
+        const int t = blockIdx.x / GU;
         const int cc = t % P.NC, hh = (t / P.NC) % P.Hk, bb = t / (P.NC * P.Hk);
         issue_kq(bb, cc, hh, kq);
-        for (int piece : {0, 5, 1, 2, 4, 3}) load_piece(bb, cc, hh * G, piece);  // first value head
+        for (int piece : {0, 5, 1, 2, 4, 3}) load_piece(bb, cc, hh * G + (int)blockIdx.x % GU, piece);  // first head
     }
-    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    for (int unit = blockIdx.x; unit < nunits; unit += gridDim.x) {
+    const int tile = unit / GU;
     c = tile % P.NC;
     hk = (tile / P.NC) % P.Hk;
     b = tile / (P.NC * P.Hk);
     t0 = c * kChunk;
-    const int ntile = tile + (int)gridDim.x;  // the next tile of this CTA
+    const int nunit = unit + (int)gridDim.x;  // the next unit of this CTA: its tile and first value head
+    const int ntile = nunit / GU;
     const int nc = ntile % P.NC, nhk = (ntile / P.NC) % P.Hk, nb = ntile / (P.NC * P.Hk);
-    if (tid == 0 && ntile < ntiles) {  // its k, q into L2 now: their copy into shared memory, issued at
+    const int nh0 = nhk * G + nunit % GU;
+    const int hv_lo = hk * G + unit % GU, hv_hi = kSplit ? hv_lo + 1 : (hk + 1) * G;  // this unit's heads
+    if (tid == 0 && nunit < nunits) {  // its k, q into L2 now: their copy into shared memory, issued at
         for (int h = 0; h < 2; h++) {  // this tile's end, is then served from L2
             tma_prefetch_4d(&mk, 64 * h, nhk, nc * kChunk, nb);
             tma_prefetch_4d(&mq, 64 * h, nhk, nc * kChunk, nb);
@@ -316,17 +326,17 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
     }
     sync_for_mma();
 
-    for (int hv = hk * G; hv < (hk + 1) * G; hv++) {
+    for (int hv = hv_lo; hv < hv_hi; hv++) {
         const size_t bh = (size_t)b * P.Hv + hv;
         const size_t idx = bh * P.NC + c;
         const uint8_t* rec = a.rec + idx * REC_BYTES;
         // the next value head's inputs (the next tile's first head after the last one), fetched
         // piece by piece as their buffers free up
-        const bool last_head = hv + 1 == (hk + 1) * G;
-        const bool more = !last_head || ntile < ntiles;
+        const bool last_head = hv + 1 == hv_hi;
+        const bool more = !last_head || nunit < nunits;
         auto prefetch = [&](int piece) {
             if (!last_head) load_piece(b, c, hv + 1, piece);
-            else load_piece(nb, nc, nhk * G, piece);
+            else load_piece(nb, nc, nh0, piece);
         };
         if (tid < 64) {  // gates of this head, staged during the previous one (thread tid: token tid)
             cp_async_wait_all();
@@ -349,7 +359,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
         if (tid >= 32 && tid < 64) gam[tid] += gam[31];
         if (more) {  // the next head's gates into gst (read by the same threads above)
             if (!last_head) stage_gb(b, c, hv + 1);
-            else stage_gb(nb, nc, nhk * G);
+            else stage_gb(nb, nc, nh0);
         }
         {
             bool okh = mbar_wait(&bar_h, h_phase, &abort_sh, a.status, 42);
@@ -781,11 +791,23 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
         }
         if (!wait_mma(49)) goto teardown;
         if (more && tid == 0) prefetch(3);  // T: its buffer held N, read by M7
-        if (last_head && tid == 0 && ntile < ntiles) issue_kq(nb, nc, nhk, gfz);  // GF / ZS are free now
+        if (last_head && tid == 0 && nunit < nunits) issue_kq(nb, nc, nhk, gfz);  // GF / ZS are free now
     }
 
     // ---------------------------------------------------------------- dq, dk: norm backward
-    {  // row r, columns c32 + 8 q + 4 hf + 0..3 (q < 4): lanes l and l + 16 fill 32-byte sectors
+    if (kSplit) {  // this value head's dq^, dk^ as they are (summed and normalised by the next kernel)
+        float x[32], w[16];
+#pragma unroll 1
+        for (int which = 0; which < 2; which++) {
+            tmem_ld32(tl + (which == 0 ? TM_DQ : TM_DK) + c32, x);
+            tmem_wait_ld();
+            split_cols_sector(x, w, lane);
+            store_rows((which == 0 ? a.dqh : a.dkh) + (((size_t)b * P.T + t0) * P.Hv + hv_lo) * kD + c32,
+                       (size_t)P.Hv * kD, w);
+        }
+        tc_fence_before();
+        __syncthreads();
+    } else {  // row r, columns c32 + 8 q + 4 hf + 0..3 (q < 4): lanes l and l + 16 fill 32-byte sectors
         const int hf = lane >> 4;
         float x[32], w[16], xx[16];
 #pragma unroll 1
@@ -829,7 +851,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
         GF = reinterpret_cast<float*>(sm + gfz);
         ZS = reinterpret_cast<float*>(sm + gfz + 16384);
     }
-    }  // tiles
+    }  // units
 
 teardown:
     cp_async_wait_all();  // staged gates still in flight
@@ -941,8 +963,14 @@ cudaError_t launch_chunk_bwd(const ChunkBwdArgs& a, cudaStream_t s) {
     ga.dg = a.dg;
     ga.dbeta = a.dbeta;
     ga.status = status;
+    const bool split = grad_split(p);
+    ga.dqh = split ? reinterpret_cast<float*>(ws + (keep ? sl.dqh : w.dqh)) : nullptr;
+    ga.dkh = split ? reinterpret_cast<float*>(ws + (keep ? sl.dkh : w.dkh)) : nullptr;
     const int smem = G_BYTES + 1024;
-    if ((e = cudaFuncSetAttribute(grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+    if ((e = cudaFuncSetAttribute(grad_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
+            cudaSuccess ||
+        (e = cudaFuncSetAttribute(grad_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) !=
+            cudaSuccess)
         return e;
     static int nsm = 0;  // one 222 KB CTA per SM: a persistent grid of one per SM
     if (nsm == 0) {
@@ -950,12 +978,24 @@ cudaError_t launch_chunk_bwd(const ChunkBwdArgs& a, cudaStream_t s) {
         if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
         if ((e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     }
-    const int ntiles = p.B * p.Hk * p.NC;
-    dim3 grid(ntiles < nsm ? ntiles : nsm);
+    const int nunits = p.B * p.Hk * p.NC * (split ? p.Hv / p.Hk : 1);
+    dim3 grid(nunits < nsm ? nunits : nsm);
     trace_begin("chunk_grad", s);
-    grad_kernel<<<grid, GRAD_THREADS, smem, s>>>(mq, mk, mv, mdo64, ga);
+    if (split)
+        grad_kernel<true><<<grid, GRAD_THREADS, smem, s>>>(mq, mk, mv, mdo64, ga);
+    else
+        grad_kernel<false><<<grid, GRAD_THREADS, smem, s>>>(mq, mk, mv, mdo64, ga);
     trace_end(s);
-    return cudaGetLastError();
+    if ((e = cudaGetLastError()) != cudaSuccess || !split) return e;
+    // the value-head sum and the norm backward of the split gradient
+    SeqBwdArgs f{};
+    f.B = p.B; f.T = p.T; f.Hk = p.Hk; f.Hv = p.Hv; f.Dk = kD; f.Dv = kD;
+    f.use_norm = p.use_norm;
+    f.bf16 = 1;
+    f.q = a.q; f.k = a.k;
+    f.dq = a.dq; f.dk = a.dk;
+    f.dqh = ga.dqh; f.dkh = ga.dkh;
+    return launch_qk_norm_backward(f, s);
 }
 
 }  // namespace gdr

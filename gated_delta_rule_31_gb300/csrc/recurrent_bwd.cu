@@ -387,7 +387,7 @@ __global__ void __launch_bounds__(256) qk_norm_bwd_warp_kernel(SeqBwdArgs A) {
 }  // namespace
 
 cudaError_t launch_qk_norm_backward(const SeqBwdArgs& a, cudaStream_t s) {
-    if (a.Dk != 128 || !a.bf16 || !a.channel) return cudaErrorInvalidValue;
+    if (a.Dk != 128 || !a.bf16) return cudaErrorInvalidValue;
     const size_t rows = (size_t)a.B * a.T * a.Hk;
     trace_begin("qk_norm_backward", s);
     qk_norm_bwd_warp_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(a);

@@ -194,7 +194,11 @@ def test_saved_operator_handoff_validation(L):
     assert sb == 1024 + 4 * 1 * (90112 + 24576 + 32768)
     fw = L.gdr_fwd_chunked_saved_workspace(ctypes.byref(p))
     bw = L.gdr_bwd_chunked_saved_workspace(ctypes.byref(p))
-    assert fw == 256 and bw == 1024 + 4 * 32768
+    # status word + chunk-end state gradients; a problem this small (4 value-head units) also gets
+    # the split gradient's dq^ and dk^ per value head (fp32 [B][T][Hv][128] each)
+    assert fw == 256 and bw == 1024 + 4 * 32768 + 2 * (64 * 4 * 128 * 4)
+    big = prob(T=32768, Hk=16, Hv=32)  # 16384 units: one CTA per key-head tile, no such planes
+    assert L.gdr_bwd_chunked_saved_workspace(ctypes.byref(big)) == 1024 + 32 * 512 * 32768
     assert L.gdr_fwd_chunked_saved(ctypes.byref(p), *[FAKE] * 8, FAKE, sb - 1, FAKE, fw, None) == WORKSPACE
     assert L.gdr_fwd_chunked_saved(ctypes.byref(p), *[FAKE] * 8, None, sb, FAKE, fw, None) == WORKSPACE
     assert L.gdr_fwd_chunked_saved(ctypes.byref(p), *[FAKE] * 8, FAKE, sb, FAKE, fw - 1, None) == WORKSPACE

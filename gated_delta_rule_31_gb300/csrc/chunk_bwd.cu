@@ -14,7 +14,9 @@
 //   Y   = U dH1^T -> dK^ += diag(b) Y, db = rk .* rowsum(K .* Y)
 //   dW  = -dU H0^T;  dT = dU V^T diag(beta) + dW K^T diag(beta Gamma rk)
 //   dV  = diag(beta) T^T dU;  T^T dW -> dK^ += diag(beta Gamma) T^T dW
-//   dA  = strict_lower(-T^T (dT T^T));  dK^ += N K with N_rj = rk_j (M_rj + M_jr), M = beta_r E .* dA
+//   dA  = strict_lower(-T^T dT T^T) = strict_lower(-(T^T dU) U~^T - (T^T dW) W^T)   (U~ = T diag(beta) V
+//         and W = T diag(beta Gamma rk) K, so dT itself is never formed)
+//   dK^ += N K with N_rj = rk_j (M_rj + M_jr), M = beta_r E .* dA
 //   dgamma from every Gamma, E, b, Gamma_C term;  dg = reverse cumsum of dgamma in the chunk
 //   dq = rq (dQ^ - q^ (q^ . dQ^)), likewise dk (after the group sum).
 #include <cuda_bf16.h>
@@ -32,14 +34,14 @@ namespace gdr {
 
 // shared memory (offsets from a 1024-aligned base)
 constexpr uint32_t G_KQ = 0;        // k rows 0-63, q rows 64-127 (panels 16 KB)      [whole CTA]
-constexpr uint32_t G_V = 32768;     // v [64 x 128]; later M fp32 [64][64]
+constexpr uint32_t G_V = 32768;     // U image [64 x 128]; then v; later M fp32 [64][64]
 constexpr uint32_t G_DO = 49152;    // dO [64 x 128]; later dSq image [64 x 64]
-constexpr uint32_t G_H0 = 65536;    // H0 image [128 d x 128 v]; later dW image [64 x 128]
-constexpr uint32_t G_DH = 98304;    // dH1 image (free after M3: the next head's dH1 lands here early)
+constexpr uint32_t G_H0 = 65536;    // H0 image [128 d x 128 v]; later dW, then T^T dW images [64 x 128]
+constexpr uint32_t G_DH = 98304;    // dH1 image; after M3 U~ as four SW64 slices [64 x 32] (the record's)
 constexpr uint32_t G_T = 131072;    // T image [64 x 64]; after M6 the N image
-constexpr uint32_t G_W = 139264;    // W image [64 x 128]; later U image
+constexpr uint32_t G_W = 139264;    // W image [64 x 128] (read again by M5)
 constexpr uint32_t G_P = 155648;    // P image [64 x 64]; later dSk image
-constexpr uint32_t G_KB = 163840;   // Kbar image [64 x 128]; later dU image
+constexpr uint32_t G_KB = 163840;   // Kbar image [64 x 128]; later dU, then T^T dU images
 constexpr uint32_t G_GF = 180224;   // G = K K^T fp32 [64][64]                            [whole CTA]
 constexpr uint32_t G_ZS = 196608;   // fp32 [64][64] scratch (column sums)
 constexpr uint32_t G_SM = 212992;   // small arrays
@@ -79,7 +81,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
     const uint32_t sb = smem_u32(sm);
-    __shared__ uint64_t bar_ld, bar_mma, bar_h, bar_h2;
+    __shared__ uint64_t bar_ld, bar_mma, bar_h, bar_h2, bar_h3;
     __shared__ uint32_t tmem_sh;
     __shared__ int abort_sh;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -114,8 +116,8 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
     float* gst = hdh + 4;                               // [2][64] the next value head's g, beta (cp.async)
     float* stg = reinterpret_cast<float*>(sm + G_STG) + warp * 160;  // this warp's row-store staging
 
-    uint32_t ld_phase = 0, mma_phase = 0, h_phase = 0, h2_phase = 0;
-    bool pend_ld = false, pend_h = false, pend_h2 = false;  // copies issued and not yet waited for (thread 0)
+    uint32_t ld_phase = 0, mma_phase = 0, h_phase = 0, h2_phase = 0, h3_phase = 0;
+    bool pend_ld = false, pend_h = false, pend_h2 = false, pend_h3 = false;  // issued, not yet waited for (thread 0)
     bool h_open = false, h2_open = false;  // pieces issued before the arriving piece of their barrier (thread 0)
     if (tid == 0) {
         abort_sh = 0;
@@ -123,6 +125,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
         mbar_init(&bar_mma, 1);
         mbar_init(&bar_h, 1);
         mbar_init(&bar_h2, 1);
+        mbar_init(&bar_h3, 1);
         fence_barrier_init();
     }
     if (warp == 0) {
@@ -184,13 +187,13 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
         }
     };
     const uint32_t id64x128_kk = idesc_bf16(64, 128, 0, 0), id64x128_km = idesc_bf16(64, 128, 0, 1),
-                   id64x128_mm = idesc_bf16(64, 128, 1, 1), id64x64_kk = idesc_bf16(64, 64, 0, 0),
-                   id64x64_mm = idesc_bf16(64, 64, 1, 1);
+                   id64x128_mm = idesc_bf16(64, 128, 1, 1), id64x64_kk = idesc_bf16(64, 64, 0, 0);
 
     // Inputs of value head hv, issued in pieces as their buffers free up (thread 0 only). Those of the
-    // first products complete bar_h: piece 0: P, W, dO   5: dH1   1: Kbar   2: H0 (issued last: it
-    // arrives, so the phase ends when all four have landed). T and v, first read by M4, complete
-    // bar_h2: piece 4: v   3: T (issued last, arrives); their latency stays off the head's start.
+    // first products complete bar_h: piece 0: P, dO   6: W   5: dH1   1: Kbar   2: H0 (issued last:
+    // it arrives, so the phase ends when all have landed). T, first read by M4, completes bar_h2
+    // (piece 3); its latency stays off the head's start. v and U~ of the head itself follow its M3
+    // (load_vu, bar_h3), over the U image and dH1.
     auto load_piece = [&](int bb, int cc, int hv, int piece) {
         const size_t bh = (size_t)bb * P.Hv + hv;
         const size_t idx = bh * P.NC + cc;
@@ -200,11 +203,15 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
         switch (piece) {
             case 0:
                 h_open = true;
-                mbar_add_tx(&bar_h, 8192 + 16384 + 2 * 8192);
+                mbar_add_tx(&bar_h, 8192 + 2 * 8192);
                 bulk_load(sm + G_P, rec + REC_P, 8192, &bar_h);
-                bulk_load(sm + G_W, rec2 + REC2_W, 16384, &bar_h);
                 tma_load_4d(sm + G_DO + 0, &mdo, 0, hv, tt, bb, &bar_h);
                 tma_load_4d(sm + G_DO + 8192, &mdo, 64, hv, tt, bb, &bar_h);
+                break;
+            case 6:
+                h_open = true;
+                mbar_add_tx(&bar_h, 16384);
+                bulk_load(sm + G_W, rec2 + REC2_W, 16384, &bar_h);
                 break;
             case 1:
                 h_open = true;
@@ -223,12 +230,6 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
                 mbar_expect_tx(&bar_h2, 8192);
                 bulk_load(sm + G_T, rec2 + REC2_T, 8192, &bar_h2);
                 break;
-            case 4:
-                h2_open = true;
-                mbar_add_tx(&bar_h2, 2 * 8192);
-                tma_load_4d(sm + G_V + 0, &mv, 0, hv, tt, bb, &bar_h2);
-                tma_load_4d(sm + G_V + 8192, &mv, 64, hv, tt, bb, &bar_h2);
-                break;
             default:
                 h_open = true;
                 mbar_add_tx(&bar_h, 32768);
@@ -237,6 +238,14 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
         }
     };
 
+    auto load_vu = [&](int bb, int cc, int hv) {  // v and U~ of value head hv (thread 0)
+        const size_t idx = ((size_t)bb * P.Hv + hv) * P.NC + cc;
+        mbar_expect_tx(&bar_h3, 2 * 8192 + 16384);
+        tma_load_4d(sm + G_V + 0, &mv, 0, hv, cc * kChunk, bb, &bar_h3);
+        tma_load_4d(sm + G_V + 8192, &mv, 64, hv, cc * kChunk, bb, &bar_h3);
+        bulk_load(sm + G_DH, a.rec + idx * REC_BYTES + REC_U, 16384, &bar_h3);
+        pend_h3 = true;
+    };
     auto issue_kq = [&](int bb, int cc, int hh, uint32_t dst) {  // k, q of a tile (thread 0)
         mbar_expect_tx(&bar_ld, 4 * 8192);
         tma_load_4d(sm + dst + 0, &mk, 0, hh, cc * kChunk, bb, &bar_ld);
@@ -264,7 +273,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
         const int t = blockIdx.x / GU;
         const int cc = t % P.NC, hh = (t / P.NC) % P.Hk, bb = t / (P.NC * P.Hk);
         issue_kq(bb, cc, hh, kq);
-        for (int piece : {0, 5, 1, 2, 4, 3}) load_piece(bb, cc, hh * G + (int)blockIdx.x % GU, piece);  // first head
+        for (int piece : {0, 6, 5, 1, 2, 3}) load_piece(bb, cc, hh * G + (int)blockIdx.x % GU, piece);  // first head
     }
     for (int unit = blockIdx.x; unit < nunits; unit += gridDim.x) {
     const int tile = unit / GU;
@@ -406,7 +415,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
             for (int w = 0; w < 16; w++) s += red[w];
             *hdh = s;
         }
-        {  // U = U~ - W H0 -> U image (G_W);  dU -> dU image (G_KB)
+        {  // U = U~ - W H0 -> U image (G_V);  dU -> dU image (G_KB)
             float x[32], w[16];
             const int q0 = 4 * qt + 2 * (lane >> 4);  // this lane's two 8-column chunks
             tmem_ld32(tl + TM_T1 + c32, x);
@@ -418,7 +427,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
                 unpack8(utv[q], ut);
 #pragma unroll
                 for (int e = 0; e < 8; e++) ut[e] -= w[8 * q + e];
-                st_chunk(sb + G_W + sw128_chunk(r, q0 + q, 64), ut, 1.f);
+                st_chunk(sb + G_V + sw128_chunk(r, q0 + q, 64), ut, 1.f);
             }
             tmem_ld32(tl + TM_T2 + c32, x);
             tmem_wait_ld();
@@ -432,7 +441,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
         if (tid == 0) {
             tc_fence_after();
             for (int k0 = 0; k0 < kD; k0 += 16) {
-                mma(TM_T2, desc_kmajor(sb + G_DO, 64, 0, k0), desc_kmajor(sb + G_W, 64, 0, k0), id64x64_kk, k0 > 0);
+                mma(TM_T2, desc_kmajor(sb + G_DO, 64, 0, k0), desc_kmajor(sb + G_V, 64, 0, k0), id64x64_kk, k0 > 0);
                 mma(TM_T1, desc_kmajor(sb + G_DO, 64, 0, k0), desc_kmajor(sb + G_H0, 128, 0, k0), id64x128_kk,
                     k0 > 0);
             }
@@ -508,7 +517,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
             }
             for (int k0 = 0; k0 < kD; k0 += 16) {
                 // Y = U dH1^T ;  dWn = dU H0^T
-                mma(TM_T1, desc_kmajor(sb + G_W, 64, 0, k0), desc_kmajor(sb + G_DH, 128, 0, k0), id64x128_kk, k0 > 0);
+                mma(TM_T1, desc_kmajor(sb + G_V, 64, 0, k0), desc_kmajor(sb + G_DH, 128, 0, k0), id64x128_kk, k0 > 0);
                 mma(TM_T2, desc_kmajor(sb + G_KB, 64, 0, k0), desc_kmajor(sb + G_H0, 128, 0, k0), id64x128_kk,
                     k0 > 0);
             }
@@ -524,9 +533,9 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
         __syncthreads();
         if (tid < 64) dgc[tid] -= red[16 + tid] + red[80 + tid] + red[144 + tid] + red[208 + tid];
         if (!wait_mma(45)) goto teardown;
-        if (more && tid == 0) {  // P, W, dO and dH1 of the next head: their buffers are free after M3
-            prefetch(0);
-            prefetch(5);
+        if (tid == 0) {  // P and dO of the next head (their buffers are free after M3); v and U~ of this
+            if (more) prefetch(0);  // head over the U image and dH1, which M3 was the last to read
+            load_vu(b, c, hv);
         }
         {
             const float br = __expf(gC - gam[r]);
@@ -562,8 +571,8 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
         }
         sync_for_mma();
 
-        // ------------------------------------------------------------ M4: dT parts, T^T dU
-        {  // T and v of this head
+        // ------------------------------------------------------------ M4: T^T dU, T^T dW
+        {  // T of this head
             bool okh = mbar_wait(&bar_h2, h2_phase, &abort_sh, a.status, 50);
             h2_phase ^= 1;
             if (okh) pend_h2 = false;
@@ -571,41 +580,28 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
         }
         if (tid == 0) {
             tc_fence_after();
-            for (int k0 = 0; k0 < kD; k0 += 16) {
-                mma(TM_T1, desc_kmajor(sb + G_KB, 64, 0, k0), desc_kmajor(sb + G_V, 64, 0, k0), id64x64_kk, k0 > 0);
-                mma(TM_T1 + 64, desc_kmajor(sb + G_H0, 64, 0, k0), desc_kmajor(sb + kq, 128, 0, k0), id64x64_kk,
-                    k0 > 0);
-            }
-            for (int k0 = 0; k0 < kChunk; k0 += 16)
+            for (int k0 = 0; k0 < kChunk; k0 += 16) {
                 mma(TM_T2, desc_mnmajor(sb + G_T, 64, 0, k0), desc_mnmajor(sb + G_KB, 64, 0, k0), id64x128_mm, k0 > 0);
+                mma(TM_T1, desc_mnmajor(sb + G_T, 64, 0, k0), desc_mnmajor(sb + G_H0, 64, 0, k0), id64x128_mm, k0 > 0);
+            }
             mma_commit(&bar_mma);
         }
         if (!wait_mma(46)) goto teardown;
-        if (more && tid == 0) prefetch(1);
+        {  // v and U~ of this head
+            bool okh = mbar_wait(&bar_h3, h3_phase, &abort_sh, a.status, 51);
+            h3_phase ^= 1;
+            if (okh) pend_h3 = false;
+            if (__syncthreads_or(!okh)) goto teardown;
+        }
         float dvv[16];  // this lane's 16 values of dv: stored once M5 is issued, because the proxy
                         // fence before M5 would otherwise wait for the global stores to complete
         {
-            {  // dT_rj = beta_j (dU V^T + Gamma_j rk_j dW K^T)_rj -> dT image (ZS, free until M6's epilogue)
-                float d1[16], d2[16], w1[8], w2[8];
-                tmem_ld16(tl + TM_T1 + c16, d1);
-                tmem_ld16(tl + TM_T1 + 64 + c16, d2);
-                tmem_wait_ld();
-                split_cols<16>(d1, w1, lane);
-                split_cols<16>(d2, w2, lane);
-                const int jc = 2 * qt + (lane >> 4);
-#pragma unroll
-                for (int e = 0; e < 8; e++) {
-                    const int j = 8 * jc + e;
-                    w1[e] = bet[j] * (w1[e] + __expf(gam[j]) * rk[j] * w2[e]);
-                }
-                st_chunk(sb + gfz + 16384 + sw128_chunk(r, jc, 64), w1, 1.f);
-            }
-            {  // T^T dU: dv = beta T^T dU; dbeta_r += sum_v V_rv (T^T dU)_rv
+            const int hf = lane >> 4;  // this lane's columns of T^T dU: c32 + 8 q + 4 hf + 0..3
+            {  // T^T dU: dv = beta T^T dU; dbeta_r += sum_v V_rv (T^T dU)_rv; its image over dU (G_KB)
                 float x[32], w[16];
                 tmem_ld32(tl + TM_T2 + c32, x);
                 tmem_wait_ld();
                 split_cols_sector(x, w, lane);
-                const int hf = lane >> 4;  // this lane's columns: c32 + 8 q + 4 hf + 0..3
                 float dot = 0.f;
 #pragma unroll
                 for (int q = 0; q < 4; q++) {
@@ -613,6 +609,10 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
                     ldrow8(G_V, r, 4 * qt + q, 64, vv);
 #pragma unroll
                     for (int i = 0; i < 4; i++) dot += (hf ? vv[4 + i] : vv[i]) * w[4 * q + i];
+                    const uint32_t addr = sb + G_KB + sw128_chunk(r, 4 * qt + q, 64) + 8 * hf;
+                    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr),
+                                 "r"(pack_bf16(w[4 * q], w[4 * q + 1])), "r"(pack_bf16(w[4 * q + 2], w[4 * q + 3]))
+                                 : "memory");
                 }
                 dot += __shfl_xor_sync(0xffffffffu, dot, 16);
                 if (act) dbp[qt * 64 + r] += dot;
@@ -620,26 +620,9 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
 #pragma unroll
                 for (int e = 0; e < 16; e++) dvv[e] = bb * w[e];
             }
-        }
-        sync_for_mma();
-
-        // ------------------------------------------------------------ M5: T^T dW, Yt = dT T^T
-        if (tid == 0) {
-            tc_fence_after();
-            for (int k0 = 0; k0 < kChunk; k0 += 16) {
-                mma(TM_T2, desc_mnmajor(sb + G_T, 64, 0, k0), desc_mnmajor(sb + G_H0, 64, 0, k0), id64x128_mm, k0 > 0);
-                mma(TM_T1, desc_kmajor(sb + gfz + 16384, 64, 0, k0), desc_kmajor(sb + G_T, 64, 0, k0), id64x64_kk,
-                    k0 > 0);
-            }
-            mma_commit(&bar_mma);
-        }
-        store_rows(a.dv + (((size_t)b * P.T + t0) * P.Hv + hv) * kD + c32, (size_t)P.Hv * kD, dvv);  // dv
-        if (!wait_mma(47)) goto teardown;
-        if (more && tid == 0) prefetch(2);
-        {
-            {  // T^T dW: dK^ += beta Gamma (T^T dW); dbeta, dgamma from k^ . (T^T dW)
+            {  // T^T dW: dK^ += beta Gamma (T^T dW); dbeta, dgamma from k^ . (T^T dW); its image over dW (G_H0)
                 float x[32], dk[32];
-                tmem_ld32(tl + TM_T2 + c32, x);
+                tmem_ld32(tl + TM_T1 + c32, x);
                 tmem_ld32(tl + TM_DK + c32, dk);
                 tmem_wait_ld();
                 const float Gr = __expf(gam[r]), bgr = bet[r] * Gr;
@@ -658,33 +641,33 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
                 if (act) {
                     dbp[qt * 64 + r] += Gr * rk[r] * dot;
                     dgp[qt * 64 + r] += bgr * rk[r] * dot;
-                }
-            }
-            {  // Yt -> image (ZS + 8K)
-                float v[16];
-                tmem_ld16(tl + TM_T1 + c16, v);
-                tmem_wait_ld();
-                if (act) {
 #pragma unroll
-                    for (int q = 0; q < 2; q++)
-                        st_chunk(sb + gfz + 16384 + 8192 + sw128_chunk(r, 2 * qt + q, 64), v + 8 * q, 1.f);
+                    for (int q = 0; q < 4; q++) st_chunk(sb + G_H0 + sw128_chunk(r, 4 * qt + q, 64), x + 8 * q, 1.f);
                 }
             }
             tmem_wait_st();
         }
         sync_for_mma();
 
-        // ------------------------------------------------------------ M6: T^T Yt
+        // ------------------------------------------------------------ M5: T^T dT T^T = (T^T dU) U~^T + (T^T dW) W^T
         if (tid == 0) {
             tc_fence_after();
-            for (int k0 = 0; k0 < kChunk; k0 += 16)
-                mma(TM_T1, desc_mnmajor(sb + G_T, 64, 0, k0), desc_mnmajor(sb + gfz + 16384 + 8192, 64, 0, k0), id64x64_mm,
-                    k0 > 0);
+            for (int k0 = 0; k0 < kD; k0 += 16)
+                mma(TM_T1, desc_kmajor(sb + G_KB, 64, 0, k0), desc_kmajor_sw64(sb + G_DH, 64, k0), id64x64_kk, k0 > 0);
+            for (int k0 = 0; k0 < kD; k0 += 16)
+                mma(TM_T1, desc_kmajor(sb + G_H0, 64, 0, k0), desc_kmajor(sb + G_W, 64, 0, k0), id64x64_kk, true);
             mma_commit(&bar_mma);
         }
+        store_rows(a.dv + (((size_t)b * P.T + t0) * P.Hv + hv) * kD + c32, (size_t)P.Hv * kD, dvv);  // dv
         if (!wait_mma(48)) goto teardown;
+        if (more && tid == 0) {  // W, dH1, Kbar and H0 of the next head: M5 was the last to read their buffers
+            prefetch(6);
+            prefetch(5);
+            prefetch(1);
+            prefetch(2);
+        }
 
-        {  // dA = strict_lower(-T^T Yt); terms of A_rj = beta_r rk_r rk_j E_rj G_rj
+        {  // dA = strict_lower(-T^T dT T^T); terms of A_rj = beta_r rk_r rk_j E_rj G_rj
             float v[16], w[8];
             tmem_ld16(tl + TM_T1 + c16, v);
             tmem_wait_ld();
@@ -747,7 +730,6 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
                 mma(TM_DK, desc_kmajor(sb + G_T, 64, 0, k0), desc_mnmajor(sb + kq, 128, 0, k0), id64x128_km,
                     true);
             mma_commit(&bar_mma);
-            if (more) prefetch(4);  // v: its buffer held M, read before the sync above
         }
         if (tid < 256) {  // column sums of dA-Z (while M7 runs)
             const int j = tid & 63, part4 = tid >> 6;
@@ -870,6 +852,7 @@ teardown:
         }
         if (pend_h) mbar_wait(&bar_h, h_phase, &never, nullptr, 0);
         if (pend_h2) mbar_wait(&bar_h2, h2_phase, &never, nullptr, 0);
+        if (pend_h3) mbar_wait(&bar_h3, h3_phase, &never, nullptr, 0);
         mbar_wait(&bar_mma, mma_phase, &never, nullptr, 0);
     }
     __syncthreads();

@@ -316,6 +316,11 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile, int R, int c0, i
     uint32_t a = tile + uint32_t(c0 >> 6) * uint32_t(R * 128) + uint32_t(k0 * 128);
     return sdesc(a, uint32_t(R * 128), 1024, SWZ_128);
 }
+//  K-major over consecutive 32-column SW64 slices (R rows of 64 bytes each, slice s holding
+//           columns 32 s .. 32 s + 31): the contraction runs along the slices' columns.
+__device__ __forceinline__ uint64_t desc_kmajor_sw64(uint32_t tile, int R, int k0) {
+    return sdesc(tile + uint32_t(k0 >> 5) * uint32_t(R * 64) + uint32_t((k0 & 31) * 2), 16, 512, SWZ_64);
+}
 //  MN-major over a 32-column SW64 tile (64-byte rows): N = 32.
 __device__ __forceinline__ uint64_t desc_mnmajor_sw64(uint32_t tile, int R, int k0) {
     return sdesc(tile + uint32_t(k0 * 64), uint32_t(R * 64), 512, SWZ_64);

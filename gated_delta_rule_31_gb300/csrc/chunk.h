@@ -32,10 +32,8 @@ constexpr uint32_t REC_U = 73728;        // U~    4 x [64 tok x 32] SW64 slices,
                                          //       half is two consecutive slices: N=64 operand, LBO 4 KB)
 constexpr uint32_t REC_BYTES = 90112;
 constexpr uint32_t STATE_IMG = 32768;    // one bf16 [128 d x 128 v] SW128 state image
-// Extra per-chunk record kept for the backward: T = (I + A)^-1 [64 x 64] and W [64 x 128];
-// with a per-channel gate also K^ .* Gamma [64 x 128] (the operand of dT's second term).
+// Extra per-chunk record kept for the backward: T = (I + A)^-1 [64 x 64] and W [64 x 128].
 constexpr uint32_t REC2_T = 0, REC2_W = 8192, REC2_BYTES = 24576;
-constexpr uint32_t REC2_KG = 24576, REC2_BYTES_CH = 40960;
 // Per-channel backward: the tensor-core pass exports, per (b, hv, chunk), fp32 [64][128]
 // X = dO H0^T, Y = U dH1^T, Z = T^T dW; fp32 [64][64] dPs = scale tril(dO U^T) and
 // dA = -strict_lower(T^T dT T^T); per state row d <dH1, H0>_d; per token V . (T^T dU).
@@ -84,7 +82,7 @@ inline WsLayout ws_layout(const ChunkProblem& p, bool bwd, bool bwd_states = fal
     w.rec2 = w.hs = w.dhs = w.chx = w.dqh = w.dkh = 0;
     if (bwd) {
         w.rec2 = end;
-        end = w.rec2 + nh * p.NC * (size_t)(p.channel ? REC2_BYTES_CH : REC2_BYTES);
+        end = w.rec2 + nh * p.NC * (size_t)REC2_BYTES;
         w.hs = end;
         if (!bwd_states) end += nh * p.NC * (size_t)STATE_IMG;
         w.dhs = end;
@@ -124,7 +122,7 @@ inline SavedLayout saved_layout(const ChunkProblem& p) {
     l.gam = 0;
     l.rec = round_up(nh * ngam * sizeof(float), 1024);
     l.rec2 = l.rec + nh * p.NC * (size_t)REC_BYTES;
-    l.hs = l.rec2 + nh * p.NC * (size_t)(p.channel ? REC2_BYTES_CH : REC2_BYTES);
+    l.hs = l.rec2 + nh * p.NC * (size_t)REC2_BYTES;
     l.total = l.hs + nh * p.NC * (size_t)STATE_IMG;
     return l;
 }

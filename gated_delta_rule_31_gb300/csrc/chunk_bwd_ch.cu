@@ -3,7 +3,7 @@
 // optimization for channelwise gated delta rule kernel" (ExecuTorch PR #21020) in the chunked
 // reverse mode of "Adding VJP for gated delta net" (MLX PR #4565, chunked case).
 //
-// Launch sequence: prep_ch (also keeps T, W and K^ .* Gamma per chunk) -> forward states scan
+// Launch sequence: prep_ch (also keeps T and W per chunk) -> forward states scan
 // -> reverse scan (chunk-end state gradients, dh0) -> grad_ch_mma -> grad_ch_contract -> the
 // value-head sum with the norm backward.
 //
@@ -13,6 +13,9 @@
 //   X  = dO H0^T          Y  = U dH1^T                     Z  = T^T dW
 //   dPs = scale tril(dO U^T)        dT = dU (diag(beta) V)^T + dW (diag(beta) K^ .* Gamma)^T
 //   dA = -strict_lower(T^T dT T^T)  dv = diag(beta) T^T dU
+// Since U~ = T diag(beta) V and W = T diag(beta) (K^ .* Gamma), T^T dT T^T equals
+// (T^T dU) U~^T + (T^T dW) W^T: dA comes from T^T dU and Z = T^T dW, which are needed anyway,
+// and the kept U~ and W, so dT is never formed.
 // (the dense products, on tcgen05: grad_ch_mma). Then per element (r, d) (grad_ch_contract):
 //   dq^ = scale Gamma X + sum_{j<=r} dPs_rj k^_j E_rj
 //   dk^ = b Y + beta Gamma Z + beta_r sum_{j<r} dA_rj k^_j E_rj
@@ -38,13 +41,13 @@ namespace {
 
 // ---------------------------------------------------------------- tensor-core pass
 // shared memory (offsets from a 1024-aligned base)
-constexpr uint32_t C_DO = 0;        // dO [64 x 128] (TMA, panels 8 KB)
-constexpr uint32_t C_W = 16384;     // W image; then U image
-constexpr uint32_t C_KB = 32768;    // Kbar image; then dU image
-constexpr uint32_t C_H0 = 49152;    // H0 image [128 d x 128 v]; then dW image [64 x 128]
-constexpr uint32_t C_DH = 81920;    // dH1 image; then dT (+0) and Yt (+8 KB) images [64 x 64]
+constexpr uint32_t C_DO = 0;        // dO [64 x 128] (TMA, panels 8 KB); then U~ (4 SW64 slices)
+constexpr uint32_t C_W = 16384;     // W image [64 x 128]
+constexpr uint32_t C_KB = 32768;    // Kbar image; then dU image; then T^T dU image
+constexpr uint32_t C_H0 = 49152;    // H0 image [128 d x 128 v]; then dW, then T^T dW images [64 x 128]
+constexpr uint32_t C_DH = 81920;    // dH1 image [128 d x 128 v]
 constexpr uint32_t C_V = 114688;    // v [64 x 128] (TMA)
-constexpr uint32_t C_KG = 131072;   // K^ .* Gamma image [64 x 128]
+constexpr uint32_t C_U = 131072;    // U image [64 x 128]
 constexpr uint32_t C_P = 147456;    // P image [64 x 64]
 constexpr uint32_t C_T = 155648;    // T image [64 x 64]
 constexpr uint32_t C_SM = 163840;   // bet[64], dbp[4][64]
@@ -73,7 +76,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
     const int t0 = c * kChunk;
     const size_t idx = ((size_t)b * P.Hv + hv) * P.NC + c;
     const uint8_t* rec = a.rec + idx * REC_BYTES;
-    const uint8_t* rec2 = a.rec2 + idx * REC2_BYTES_CH;
+    const uint8_t* rec2 = a.rec2 + idx * REC2_BYTES;
     float* chx = reinterpret_cast<float*>(a.chx + idx * CHX_BYTES);
     const int lg = warp & 3, qt = warp >> 2, hf = lane >> 4;
     const int r = 16 * lg + (lane & 15);
@@ -101,7 +104,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
     const uint32_t tm = tmem_sh;
     const uint32_t tl = tmem_at(tm, 32 * lg, 0);
     if (tid == 0) {
-        mbar_expect_tx(&bar_ld, 163840);
+        mbar_expect_tx(&bar_ld, 147456);
         tma_load_4d(sm + C_DO + 0, &mdo, 0, hv, t0, b, &bar_ld);
         tma_load_4d(sm + C_DO + 8192, &mdo, 64, hv, t0, b, &bar_ld);
         tma_load_4d(sm + C_V + 0, &mv, 0, hv, t0, b, &bar_ld);
@@ -110,7 +113,6 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
         bulk_load(sm + C_KB, rec + REC_K, 16384, &bar_ld);
         bulk_load(sm + C_H0, a.hs + idx * STATE_IMG, 32768, &bar_ld);
         bulk_load(sm + C_DH, a.dhs + idx * STATE_IMG, 32768, &bar_ld);
-        bulk_load(sm + C_KG, rec2 + REC2_KG, 16384, &bar_ld);
         bulk_load(sm + C_P, rec + REC_P, 8192, &bar_ld);
         bulk_load(sm + C_T, rec2 + REC2_T, 8192, &bar_ld);
     }
@@ -155,8 +157,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
         }
     };
     const uint32_t id64x128_kk = idesc_bf16(64, 128, 0, 0), id64x128_km = idesc_bf16(64, 128, 0, 1),
-                   id64x128_mm = idesc_bf16(64, 128, 1, 1), id64x64_kk = idesc_bf16(64, 64, 0, 0),
-                   id64x64_mm = idesc_bf16(64, 64, 1, 1);
+                   id64x128_mm = idesc_bf16(64, 128, 1, 1), id64x64_kk = idesc_bf16(64, 64, 0, 0);
     ok = mbar_wait(&bar_ld, 0, &abort_sh, a.status, 60);
     if (__syncthreads_or(!ok)) goto teardown;
 
@@ -186,12 +187,12 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
         s += __shfl_xor_sync(0xffffffffu, s, 2);
         if (pp == 0) chx[CHX_HDH / 4 + d] = s;
     }
-    uint4 utv[2];  // this lane's half of U~ slice qt (columns c32 + 16 hf ..)
+    uint4 utv[2];  // this lane's half of U~ slice qt (columns c32 + 16 hf ..), kept for its image
 #pragma unroll
     for (int q = 0; q < 2; q++)
         utv[q] = *reinterpret_cast<const uint4*>(rec + REC_U + qt * 4096 + sw64_chunk(r, 2 * hf + q));
     if (!wait_mma(61)) goto teardown;
-    {  // U = U~ - W H0 -> U image (C_W);  dU -> dU image (C_KB)
+    {  // U = U~ - W H0 -> U image (C_U);  dU -> dU image (C_KB)
         float x[32], w[16];
         const int q0 = 4 * qt + 2 * hf;
         tmem_ld32(tl + TM1 + c32, x);
@@ -203,7 +204,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
             unpack8(utv[q], ut);
 #pragma unroll
             for (int e = 0; e < 8; e++) ut[e] -= w[8 * q + e];
-            st_chunk(sb + C_W + sw128_chunk(r, q0 + q, 64), ut, 1.f);
+            st_chunk(sb + C_U + sw128_chunk(r, q0 + q, 64), ut, 1.f);
         }
         tmem_ld32(tl + TM2 + c32, x);
         tmem_wait_ld();
@@ -217,7 +218,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
     if (tid == 0) {
         tc_fence_after();
         for (int k0 = 0; k0 < kD; k0 += 16) {
-            mma(TM2, desc_kmajor(sb + C_DO, 64, 0, k0), desc_kmajor(sb + C_W, 64, 0, k0), id64x64_kk, k0 > 0);
+            mma(TM2, desc_kmajor(sb + C_DO, 64, 0, k0), desc_kmajor(sb + C_U, 64, 0, k0), id64x64_kk, k0 > 0);
             mma(TM1, desc_kmajor(sb + C_DO, 64, 0, k0), desc_kmajor(sb + C_H0, 128, 0, k0), id64x128_kk, k0 > 0);
         }
         mma_commit(&bar_mma);
@@ -225,6 +226,9 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
     if (!wait_mma(62)) goto teardown;
     float wx[16], up[8];  // X and dPs, exported once M3 is issued
     {
+#pragma unroll
+        for (int q = 0; q < 2; q++)  // U~ slice images over dO, which M2 was the last to read
+            *reinterpret_cast<uint4*>(sm + C_DO + qt * 4096 + sw64_chunk(r, 2 * hf + q)) = utv[q];
         float x[32];
         tmem_ld32(tl + TM1 + c32, x);
         tmem_wait_ld();
@@ -243,7 +247,7 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
     if (tid == 0) {
         tc_fence_after();
         for (int k0 = 0; k0 < kD; k0 += 16) {
-            mma(TM1, desc_kmajor(sb + C_W, 64, 0, k0), desc_kmajor(sb + C_DH, 128, 0, k0), id64x128_kk, k0 > 0);
+            mma(TM1, desc_kmajor(sb + C_U, 64, 0, k0), desc_kmajor(sb + C_DH, 128, 0, k0), id64x128_kk, k0 > 0);
             mma(TM2, desc_kmajor(sb + C_KB, 64, 0, k0), desc_kmajor(sb + C_H0, 128, 0, k0), id64x128_kk, k0 > 0);
         }
         mma_commit(&bar_mma);
@@ -265,90 +269,58 @@ __global__ void __launch_bounds__(CH_THREADS, 1)
     }
     sync_for_mma();
 
-    // ---------------------------------------------------------------- M4: dU V^T, dW (K^ .* Gamma)^T, T^T dU
+    // ---------------------------------------------------------------- M4: T^T dU, Z = T^T dW
     if (tid == 0) {
         tc_fence_after();
-        for (int k0 = 0; k0 < kD; k0 += 16) {
-            mma(TM1, desc_kmajor(sb + C_KB, 64, 0, k0), desc_kmajor(sb + C_V, 64, 0, k0), id64x64_kk, k0 > 0);
-            mma(TM1 + 64, desc_kmajor(sb + C_H0, 64, 0, k0), desc_kmajor(sb + C_KG, 64, 0, k0), id64x64_kk, k0 > 0);
-        }
-        for (int k0 = 0; k0 < kChunk; k0 += 16)
+        for (int k0 = 0; k0 < kChunk; k0 += 16) {
             mma(TM2, desc_mnmajor(sb + C_T, 64, 0, k0), desc_mnmajor(sb + C_KB, 64, 0, k0), id64x128_mm, k0 > 0);
+            mma(TM1, desc_mnmajor(sb + C_T, 64, 0, k0), desc_mnmajor(sb + C_H0, 64, 0, k0), id64x128_mm, k0 > 0);
+        }
         mma_commit(&bar_mma);
     }
     store_rows(chx + CHX_Y / 4 + c32, kD, wy, kChunk);
     if (!wait_mma(64)) goto teardown;
-    float wv[16];  // dv, stored once M5 is issued
+    float wv[16], wz[16];  // dv and Z, stored once M5 is issued
     {
-        {  // dT_rj = beta_j (dU V^T + dW (K^ .* Gamma)^T)_rj -> dT image (C_DH)
-            float d1[16], d2[16], w1[8], w2[8];
-            tmem_ld16(tl + TM1 + c16, d1);
-            tmem_ld16(tl + TM1 + 64 + c16, d2);
-            tmem_wait_ld();
-            split_cols<16>(d1, w1, lane);
-            split_cols<16>(d2, w2, lane);
-            const int jc = 2 * qt + hf;
+        const int q0 = 4 * qt + 2 * hf;
+        float x[32], w[16];
+        tmem_ld32(tl + TM2 + c32, x);  // T^T dU: dv = beta T^T dU;  V . (T^T dU) per row; its image
+        tmem_wait_ld();
+        split_cols<32>(x, w, lane);
+        float dot = 0.f;
 #pragma unroll
-            for (int e = 0; e < 8; e++) w1[e] = bet[8 * jc + e] * (w1[e] + w2[e]);
-            st_chunk(sb + C_DH + sw128_chunk(r, jc, 64), w1, 1.f);
+        for (int q = 0; q < 2; q++) {
+            float vv[8];
+            unpack8(ld_shared_v4(sb + C_V + sw128_chunk(r, q0 + q, 64)), vv);
+#pragma unroll
+            for (int e = 0; e < 8; e++) dot += vv[e] * w[8 * q + e];
+            st_chunk(sb + C_KB + sw128_chunk(r, q0 + q, 64), w + 8 * q, 1.f);
         }
-        {  // T^T dU: dv = beta T^T dU;  V . (T^T dU) per row
-            float x[32], w[16];
-            tmem_ld32(tl + TM2 + c32, x);
-            tmem_wait_ld();
-            split_cols<32>(x, w, lane);
-            float dot = 0.f;
+        dot += __shfl_xor_sync(0xffffffffu, dot, 16);
+        if (act) dbp[qt * 64 + r] = dot;
+        const float bb = bet[r];
 #pragma unroll
-            for (int q = 0; q < 2; q++) {
-                float vv[8];
-                unpack8(ld_shared_v4(sb + C_V + sw128_chunk(r, 4 * qt + 2 * hf + q, 64)), vv);
+        for (int e = 0; e < 16; e++) wv[e] = bb * w[e];
+        tmem_ld32(tl + TM1 + c32, x);  // Z and its image
+        tmem_wait_ld();
+        split_cols<32>(x, wz, lane);
 #pragma unroll
-                for (int e = 0; e < 8; e++) dot += vv[e] * w[8 * q + e];
-            }
-            dot += __shfl_xor_sync(0xffffffffu, dot, 16);
-            if (act) dbp[qt * 64 + r] = dot;
-            const float bb = bet[r];
-#pragma unroll
-            for (int e = 0; e < 16; e++) wv[e] = bb * w[e];
-        }
+        for (int q = 0; q < 2; q++) st_chunk(sb + C_H0 + sw128_chunk(r, q0 + q, 64), wz + 8 * q, 1.f);
     }
     sync_for_mma();
 
-    // ---------------------------------------------------------------- M5: Z = T^T dW, Yt = dT T^T
+    // ---------------------------------------------------------------- M5: (T^T dU) U~^T + Z W^T -> dA
     if (tid == 0) {
         tc_fence_after();
-        for (int k0 = 0; k0 < kChunk; k0 += 16) {
-            mma(TM2, desc_mnmajor(sb + C_T, 64, 0, k0), desc_mnmajor(sb + C_H0, 64, 0, k0), id64x128_mm, k0 > 0);
-            mma(TM1, desc_kmajor(sb + C_DH, 64, 0, k0), desc_kmajor(sb + C_T, 64, 0, k0), id64x64_kk, k0 > 0);
-        }
+        for (int k0 = 0; k0 < kD; k0 += 16)
+            mma(TM1, desc_kmajor(sb + C_KB, 64, 0, k0), desc_kmajor_sw64(sb + C_DO, 64, k0), id64x64_kk, k0 > 0);
+        for (int k0 = 0; k0 < kD; k0 += 16)
+            mma(TM1, desc_kmajor(sb + C_H0, 64, 0, k0), desc_kmajor(sb + C_W, 64, 0, k0), id64x64_kk, true);
         mma_commit(&bar_mma);
     }
     store_rows(a.dv + (((size_t)b * P.T + t0) * P.Hv + hv) * kD + c32, (size_t)P.Hv * kD, wv, P.T - t0);
-    if (!wait_mma(65)) goto teardown;
-    float wz[16];  // Z, exported once M6 is issued
-    {
-        float x[32];
-        tmem_ld32(tl + TM2 + c32, x);
-        tmem_wait_ld();
-        split_cols<32>(x, wz, lane);
-        float v[16], u[8];
-        tmem_ld16(tl + TM1 + c16, v);
-        tmem_wait_ld();
-        split_cols<16>(v, u, lane);
-        st_chunk(sb + C_DH + 8192 + sw128_chunk(r, 2 * qt + hf, 64), u, 1.f);
-    }
-    sync_for_mma();
-
-    // ---------------------------------------------------------------- M6: T^T Yt -> dA
-    if (tid == 0) {
-        tc_fence_after();
-        for (int k0 = 0; k0 < kChunk; k0 += 16)
-            mma(TM1, desc_mnmajor(sb + C_T, 64, 0, k0), desc_mnmajor(sb + C_DH + 8192, 64, 0, k0), id64x64_mm,
-                k0 > 0);
-        mma_commit(&bar_mma);
-    }
     store_rows(chx + CHX_Z / 4 + c32, kD, wz, kChunk);
-    if (!wait_mma(66)) goto teardown;
+    if (!wait_mma(65)) goto teardown;
     {
         float v[16], u[8];
         tmem_ld16(tl + TM1 + c16, v);

@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(PCH_THREADS, 1)
     const int t0 = c * kChunk;
     const size_t bh = (size_t)b * P.Hv + hv;
     uint8_t* rec = a.rec + (bh * P.NC + c) * REC_BYTES;
-    uint8_t* rec2 = a.rec2 ? a.rec2 + (bh * P.NC + c) * REC2_BYTES_CH : nullptr;  // backward: T, W, K^ .* Gamma
+    uint8_t* rec2 = a.rec2 ? a.rec2 + (bh * P.NC + c) * REC2_BYTES : nullptr;  // backward: T, W
     float* al = reinterpret_cast<float*>(sm + CS_AL);
     float* gp = reinterpret_cast<float*>(sm + CS_GP);
     float* Am = reinterpret_cast<float*>(sm + CS_A);
@@ -441,35 +441,19 @@ __global__ void __launch_bounds__(PCH_THREADS, 1)
         mma_commit(&bar_mma);
         mma_pend = true;
     }
-    if (rec2) {  // T and K^ .* Gamma for the backward, from tiles still intact, stored once the
-                 // products are issued: the proxy fence before them would wait for these stores
-        if (tid < 256) {
-            const int i = tid >> 2, qtr = tid & 3;
-            const float* trow = Tm + i * LDA + 16 * qtr;
-#pragma unroll
-            for (int q = 0; q < 2; q++) {
-                float t[8];
-#pragma unroll
-                for (int e = 0; e < 8; e++) {
-                    const int j = 16 * qtr + 8 * q + e;
-                    t[e] = (j >> 4) <= (i >> 4) ? trow[8 * q + e] : 0.f;
-                }
-                st_global16(rec2 + REC2_T + sw128_chunk(i, 2 * qtr + q, 64), pack8(t, 1.f));
-            }
-        }
-        const int r = (tid & 7) + 8 * (tid >> 6), q8 = (tid >> 3) & 7;
-        const float rk = rho[r];
+    if (rec2 && tid < 256) {  // T for the backward, from the tile still intact, stored once the
+                              // products are issued: the proxy fence before them would wait for it
+        const int i = tid >> 2, qtr = tid & 3;
+        const float* trow = Tm + i * LDA + 16 * qtr;
 #pragma unroll
         for (int q = 0; q < 2; q++) {
-            const int j = 2 * q8 + q;
-            float x[8];
-            unpack8(ld_shared_v4(sb + CS_KQ + sw128_chunk(r, j, 128)), x);
-            const float4 g0 = *reinterpret_cast<const float4*>(gp + dix(r, 8 * j));
-            const float4 g1 = *reinterpret_cast<const float4*>(gp + dix(r, 8 * j + 4));
-            const float gg[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+            float t[8];
 #pragma unroll
-            for (int e = 0; e < 8; e++) x[e] *= gg[e];
-            st_global16(rec2 + REC2_KG + sw128_chunk(r, j, 64), pack8(x, rk));
+            for (int e = 0; e < 8; e++) {
+                const int j = 16 * qtr + 8 * q + e;
+                t[e] = (j >> 4) <= (i >> 4) ? trow[8 * q + e] : 0.f;
+            }
+            st_global16(rec2 + REC2_T + sw128_chunk(i, 2 * qtr + q, 64), pack8(t, 1.f));
         }
     }
     ok = mbar_wait(&bar_mma, mph, &abort_sh, a.status, 16);

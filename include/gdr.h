@@ -164,9 +164,8 @@ gdr_status gdr_bwd_chunked_states(const gdr_problem* p, const void* q, const voi
  * bitwise identical to gdr_fwd_chunked / gdr_bwd_chunked. The buffer must not be modified
  * between the two calls, and the backward must get the same q, k, v, g, beta and problem.
  * Workspaces: gdr_fwd_chunked_saved_workspace() (the status word only) and
- * gdr_bwd_chunked_saved_workspace(). Same support matrix as gdr_bwd_chunked (with the
- * per-channel gate the saved T/W record also holds K^ .* Gamma, 160 KB per (b, hv, chunk);
- * for F32 the buffer holds fp32 records of W, Kbar, scale Gamma Q^, gamma, U~, P and T, then
+ * gdr_bwd_chunked_saved_workspace(). Same support matrix as gdr_bwd_chunked (bf16: 144 KB per
+ * (b, hv, chunk) with either gate, plus the per-chunk Gamma_C header; for F32 the buffer holds fp32 records of W, Kbar, scale Gamma Q^, gamma, U~, P and T, then
  * the fp32 chunk-start states: 256 KB per (b, hv, chunk) at Dk = Dv = 128);
  * the size queries return 0 for an invalid or unsupported problem. Errors as gdr_fwd_chunked, plus
  * GDR_ERR_WORKSPACE if `saved` is NULL or smaller than required. */

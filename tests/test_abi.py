@@ -116,16 +116,16 @@ def test_chunked_support_matrix_and_workspace(L):
         # a workspace one byte short is refused before any launch
         need = L.gdr_fwd_chunked_workspace(ctypes.byref(p))
         assert L.gdr_fwd_chunked(ctypes.byref(p), *[FAKE] * 8, FAKE, need - 1, None) == WORKSPACE
-    # per-channel gate: chunked forward, both handoffs and the VJP (Gamma_C per key channel, 16 KB
-    # more of T/W/K.*Gamma per chunk and the backward's per-channel exports: larger buffers)
+    # per-channel gate: chunked forward, both handoffs and the VJP (Gamma_C per key channel and the
+    # backward's per-channel exports: larger buffers; the same T/W record per chunk)
     pc, ps = prob(gate=1), prob()
     assert L.gdr_fwd_chunked_workspace(ctypes.byref(pc)) > L.gdr_fwd_chunked_workspace(ctypes.byref(ps))
     assert L.gdr_bwd_chunked_workspace(ctypes.byref(pc)) > L.gdr_bwd_chunked_workspace(ctypes.byref(ps))
     assert L.gdr_bwd_chunked_states_workspace(ctypes.byref(pc)) > L.gdr_bwd_chunked_states_workspace(ctypes.byref(ps))
     assert L.gdr_chunk_states_bytes(ctypes.byref(pc)) == L.gdr_chunk_states_bytes(ctypes.byref(ps)) > 0
     sbc, sbs = L.gdr_chunk_saved_bytes(ctypes.byref(pc)), L.gdr_chunk_saved_bytes(ctypes.byref(ps))
-    # header (Gamma_C per chunk and key channel) + (88 KB record + 40 KB T/W/K.*Gamma + 32 KB state)
-    assert sbc == 2048 + 4 * (90112 + 40960 + 32768) and sbs == 1024 + 4 * (90112 + 24576 + 32768)
+    # header (Gamma_C per chunk and key channel) + (88 KB record + 24 KB T/W + 32 KB state)
+    assert sbc == 2048 + 4 * (90112 + 24576 + 32768) and sbs == 1024 + 4 * (90112 + 24576 + 32768)
     assert L.gdr_bwd_chunked_saved_workspace(ctypes.byref(pc)) > L.gdr_bwd_chunked_saved_workspace(ctypes.byref(ps))
     assert L.gdr_fwd_chunked_saved(ctypes.byref(pc), *[FAKE] * 8, FAKE, sbc - 1, FAKE, 256, None) == WORKSPACE
     nb = L.gdr_bwd_chunked_workspace(ctypes.byref(pc))

@@ -77,7 +77,8 @@ constexpr int GRAD_THREADS = 512;
 template <bool kSplit>
 __global__ void __launch_bounds__(GRAD_THREADS, 1)
     grad_kernel(const __grid_constant__ CUtensorMap mq, const __grid_constant__ CUtensorMap mk,
-                const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo, GradArgs a) {
+                const __grid_constant__ CUtensorMap mv, const __grid_constant__ CUtensorMap mdo,
+                const __grid_constant__ CUtensorMap mdq, const __grid_constant__ CUtensorMap mdk, GradArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
     const uint32_t sb = smem_u32(sm);
@@ -664,7 +665,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
             prefetch(6);
             prefetch(5);
             prefetch(1);
-            prefetch(2);
+            if (kSplit || !last_head) prefetch(2);  // else H0's buffer first stages the tile's dk
         }
 
         {  // dA = strict_lower(-T^T dT T^T); terms of A_rj = beta_r rk_r rk_j E_rj G_rj
@@ -789,41 +790,69 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
         }
         tc_fence_before();
         __syncthreads();
-    } else {  // row r, columns c32 + 8 q + 4 hf + 0..3 (q < 4): lanes l and l + 16 fill 32-byte sectors
+    } else {  // row r, columns c32 + 8 q + 4 hf + 0..3 (q < 4)
+        // dq = rq (dq^ - rq^2 (q . dq^) q), dk likewise, leave by tensor-map stores of four [64 x 32]
+        // fp32 boxes each (128-byte swizzle), staged over k/q (dq) and H0's buffer (dk), so no warp
+        // waits on its global stores. H0 of the next tile's first head is copied in once they are read.
         const int hf = lane >> 4;
-        float x[32], w[16], xx[16];
-#pragma unroll 1
+        float w[2][16];
+#pragma unroll
         for (int which = 0; which < 2; which++) {  // 0: q, 1: k
-            const float* rho = which == 0 ? rq : rk;
-            const int krow = which == 0 ? 64 + r : r;
+            float x[32];
             tmem_ld32(tl + (which == 0 ? TM_DQ : TM_DK) + c32, x);
             tmem_wait_ld();
-            split_cols_sector(x, w, lane);
+            split_cols_sector(x, w[which], lane);
+            const int krow = which == 0 ? 64 + r : r;
             float dot = 0.f;
 #pragma unroll
             for (int q = 0; q < 4; q++) {
                 float x8[8];
                 ldrow8(kq, krow, 4 * qt + q, 128, x8);
 #pragma unroll
-                for (int i = 0; i < 4; i++) {
-                    xx[4 * q + i] = hf ? x8[4 + i] : x8[i];
-                    dot += xx[4 * q + i] * w[4 * q + i];
-                }
+                for (int i = 0; i < 4; i++) dot += (hf ? x8[4 + i] : x8[i]) * w[which][4 * q + i];
             }
             dot += __shfl_xor_sync(0xffffffffu, dot, 16);
-            if (act) part[qt * 64 + r] = dot;
-            __syncthreads();
-            {
-                const float rr = rho[r];
-                const float full = part[r] + part[64 + r] + part[128 + r] + part[192 + r];
-                float o[16];
+            if (act) (which == 0 ? part : red + 16)[qt * 64 + r] = dot;
+        }
+        tc_fence_before();
+        __syncthreads();
 #pragma unroll
-                for (int i = 0; i < 16; i++) o[i] = P.use_norm ? rr * (w[i] - rr * xx[i] * rr * full) : w[i];
-                store_rows((which == 0 ? a.dq : a.dk) + (((size_t)b * P.T + t0) * P.Hk + hk) * kD + c32,
-                           (size_t)P.Hk * kD, o);
+        for (int which = 0; which < 2; which++) {
+            const float* pw = which == 0 ? part : red + 16;
+            const float rr = (which == 0 ? rq : rk)[r];
+            const float full = pw[r] + pw[64 + r] + pw[128 + r] + pw[192 + r];
+            const int krow = which == 0 ? 64 + r : r;
+#pragma unroll
+            for (int q = 0; q < 4; q++) {
+                float x8[8];
+                ldrow8(kq, krow, 4 * qt + q, 128, x8);
+#pragma unroll
+                for (int i = 0; i < 4; i++) {
+                    const float xv = hf ? x8[4 + i] : x8[i];
+                    float& o = w[which][4 * q + i];
+                    if (P.use_norm) o = rr * (o - rr * xv * rr * full);
+                }
             }
-            tc_fence_before();
-            __syncthreads();
+        }
+        __syncthreads();  // k/q read: its region and H0's buffer take the staging
+#pragma unroll
+        for (int which = 0; which < 2; which++) {
+            uint8_t* box = sm + (which == 0 ? kq : G_H0) + qt * 8192;
+#pragma unroll
+            for (int q = 0; q < 4; q++)
+                *reinterpret_cast<float4*>(box + sw128_chunk(r, 2 * q + hf, 64)) =
+                    make_float4(w[which][4 * q], w[which][4 * q + 1], w[which][4 * q + 2], w[which][4 * q + 3]);
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            for (int qq = 0; qq < 4; qq++) {
+                tma_store_4d(&mdq, sm + kq + qq * 8192, 32 * qq, hk, t0, b);
+                tma_store_4d(&mdk, sm + G_H0 + qq * 8192, 32 * qq, hk, t0, b);
+            }
+            bulk_commit();
+            bulk_wait_read_all();  // the staging is read: both regions may be rewritten
+            if (nunit < nunits) load_piece(nb, nc, nh0, 2);
         }
     }
     {  // swap the k/q and scratch regions for the next tile
@@ -837,6 +866,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
 
 teardown:
     cp_async_wait_all();  // staged gates still in flight
+    if (tid == 0) bulk_wait_all();  // dq, dk stores
     tc_fence_before();
     __syncthreads();
     if (abort_sh && tid == 0) {  // let copies still in flight land before the CTA exits
@@ -963,11 +993,17 @@ cudaError_t launch_chunk_bwd(const ChunkBwdArgs& a, cudaStream_t s) {
     }
     const int nunits = p.B * p.Hk * p.NC * (split ? p.Hv / p.Hk : 1);
     dim3 grid(nunits < nsm ? nunits : nsm);
+    CUtensorMap mdq, mdk;  // fp32 [B][T][Hk][Dk] stores of [64 x 32] boxes
+    if (!make_map_4d(&mdq, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.dq, kD, p.Hk, p.T, p.B, 32, kChunk,
+                     CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map_4d(&mdk, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, a.dk, kD, p.Hk, p.T, p.B, 32, kChunk,
+                     CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
     trace_begin("chunk_grad", s);
     if (split)
-        grad_kernel<true><<<grid, GRAD_THREADS, smem, s>>>(mq, mk, mv, mdo64, ga);
+        grad_kernel<true><<<grid, GRAD_THREADS, smem, s>>>(mq, mk, mv, mdo64, mdq, mdk, ga);
     else
-        grad_kernel<false><<<grid, GRAD_THREADS, smem, s>>>(mq, mk, mv, mdo64, ga);
+        grad_kernel<false><<<grid, GRAD_THREADS, smem, s>>>(mq, mk, mv, mdo64, mdq, mdk, ga);
     trace_end(s);
     if ((e = cudaGetLastError()) != cudaSuccess || !split) return e;
     // the value-head sum and the norm backward of the split gradient

@@ -53,7 +53,7 @@ KERNEL_MODEL = {
 # DRAM traffic per unit (dram__bytes_read.sum + dram__bytes_write.sum) of the current kernel
 # versions, from one ncu capture of the T=8192 training step, scaled to a launch by its units
 # (traffic grows with the units): prep averaged over its forward and backward launches.
-KERNEL_TRAFFIC = {"chunk_prep": 1900, "chunk_scan_fwd": 2055, "chunk_scan_bwd": 1422, "chunk_grad": 3813}
+KERNEL_TRAFFIC = {"chunk_prep": 1900, "chunk_scan_fwd": 2055, "chunk_scan_bwd": 1422, "chunk_grad": 3808}
 # Whole-step algorithmic roofline (forward + VJP): 655,360 flops and 2,584 bytes per unit.
 STEP_FLOPS, STEP_BYTES = 655360 * UNITS, 2584 * UNITS
 

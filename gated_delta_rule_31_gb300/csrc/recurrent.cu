@@ -178,7 +178,11 @@ __global__ void __launch_bounds__(WARPS * 32) recurrent_rows_kernel(RecurrentArg
 // Decode: one CTA of 4 warps per (b, hv); warp w streams state rows [w*Dv/4, (w+1)*Dv/4) in
 // groups of 4 rows, loading group g+1 while it reduces and writes group g, so each lane
 // keeps four to eight 128-bit loads in flight for the whole CTA life. With one wave of
-// CTAs (B*Hv of them) the grid has no tail.
+// CTAs (B*Hv of them) the grid has no tail. The step is launched as a programmatic dependent
+// of the kernel before it on the stream: it lets the next launch begin at once
+// (griddepcontrol.launch_dependents), loads q, k, v, g, beta and forms the norms, and only then
+// waits for the previous kernel to complete (griddepcontrol.wait) before it reads the state or
+// writes anything. Back-to-back steps so overlap one step's start with the previous one's end.
 #ifndef GDR_DECODE_GROUP
 #define GDR_DECODE_GROUP 4
 #endif
@@ -186,6 +190,7 @@ template <int DK, typename TIn>
 __global__ void __launch_bounds__(128) decode_kernel(RecurrentArgs a) {
     constexpr int EL = DK / 32;
     constexpr int G = GDR_DECODE_GROUP;  // rows per group
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int hv = blockIdx.x, b = blockIdx.y;
     const int hk = hv / (a.Hv / a.Hk);
@@ -198,8 +203,6 @@ __global__ void __launch_bounds__(128) decode_kernel(RecurrentArgs a) {
     float* Sout = a.ht + bh * (size_t)a.Dv * DK;
 
     float cur[G][EL], nxt[G][EL];
-#pragma unroll
-    for (int i = 0; i < G; i++) ld_row<EL>(Sin + (size_t)(r0 + i) * DK + c0, cur[i]);
 
     const TIn* q = reinterpret_cast<const TIn*>(a.q);
     const TIn* k = reinterpret_cast<const TIn*>(a.k);
@@ -238,6 +241,9 @@ __global__ void __launch_bounds__(128) decode_kernel(RecurrentArgs a) {
     for (int e = 0; e < EL; e++) ak[e] = dec[e] * kh[e];
     const float beta = a.beta[bh];
     const size_t vo = bh * (size_t)a.Dv;
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // the previous kernel's writes are complete
+#pragma unroll
+    for (int i = 0; i < G; i++) ld_row<EL>(Sin + (size_t)(r0 + i) * DK + c0, cur[i]);
 
     for (int gi = 0; gi < ngroups; gi++) {
         const int rg = r0 + gi * G;
@@ -288,11 +294,20 @@ __global__ void __launch_bounds__(128) decode_kernel(RecurrentArgs a) {
 
 template <int DK, typename TIn>
 static cudaError_t launch_decode(const RecurrentArgs& a, cudaStream_t s) {
-    dim3 grid(a.Hv, a.B);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.Hv, a.B);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see decode_kernel
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
     trace_begin("decode_step", s);
-    decode_kernel<DK, TIn><<<grid, 128, 0, s>>>(a);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, decode_kernel<DK, TIn>, a);
     trace_end(s);
-    return cudaGetLastError();
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int DK, typename TIn, int ROWS, int WARPS>

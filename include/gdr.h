@@ -189,7 +189,11 @@ gdr_status gdr_bwd_chunked_saved(const gdr_problem* p, const void* q, const void
 /* One decode step (p->T must be 1) on the state in place: per state row, one pass forms
  * the prediction with the decay folded in, a second applies decay plus the rank-one
  * update while accumulating the output, so the state is read once and written once.
- * Layouts as above without the T axis. Every dtype, gate and Dk, Dv in {32, 64, 128}. */
+ * Layouts as above without the T axis. Every dtype, gate and Dk, Dv in {32, 64, 128}.
+ * The step is launched as a programmatic dependent launch: it may read q, k, v, g and beta
+ * while the kernel enqueued before it on `stream` is still running if that kernel is itself a
+ * decode step, and reads the state and writes `o` only once that kernel has completed. So the
+ * `o` of one step must not alias the q, k, v, g or beta of the step enqueued right after it. */
 gdr_status gdr_decode_step(const gdr_problem* p, const void* q, const void* k, const void* v,
                            const float* g, const float* beta, float* state, void* o,
                            gdr_stream_t stream);

@@ -474,12 +474,14 @@ __global__ void __launch_bounds__(256, 2)
             __syncthreads();  // every buffer of this value head is free again
             tc_fence_after();
             if (tid == 0) {
+                // after the unit's last head k, q are no longer read: the next unit's copy goes into
+                // the copy engine ahead of this head's record stores
+                if (hh + 1 == he && next < ngroups) issue_kq(next);
                 bulk_store(rec + REC_M, sm + PS_STAGE, 32768);
                 bulk_store(rec + REC_Q, sm + PS_STAGE_Q, 16384);
                 bulk_commit();
             }
         }  // value heads of the unit
-        if (tid == 0 && next < ngroups) issue_kq(next);  // k, q are no longer read
     }  // units
 teardown:
     cp_async_wait_all();

@@ -135,6 +135,18 @@ def test_backward_mild_decay_long_range():
     check(gpu_bwd(x, dev), x)
 
 
+def test_backward_ragged_many_tiles():
+    """A ragged last chunk on the per-tile grad path (more than 128 value-head units: every tile's
+    value heads in one CTA, dq / dk / dv leaving by tensor-map stores that must skip the rows past
+    T), also run twice for bitwise determinism."""
+    dev = cuda_device()
+    x = make_inputs(Shape(1, 2000, 4, 8, 128, 128), dtype=torch.bfloat16, seed=41, grads=True, gate_scale=0.05)
+    a, b = gpu_bwd(x, dev), gpu_bwd(x, dev)
+    for n in NAMES:
+        assert torch.equal(a[n], b[n]), n
+    check(a, x)
+
+
 def test_backward_deterministic():
     dev = cuda_device()
     x = make_inputs(Shape(1, 333, 2, 4, 128, 128), dtype=torch.bfloat16, seed=5, grads=True)

@@ -38,7 +38,7 @@ constexpr uint32_t G_V = 32768;     // U image [64 x 128]; then v; later M fp32 
 constexpr uint32_t G_DO = 49152;    // dO [64 x 128]; later dSq image [64 x 64]
 constexpr uint32_t G_H0 = 65536;    // H0 image [128 d x 128 v]; later dW, then T^T dW images [64 x 128]
 constexpr uint32_t G_DH = 98304;    // dH1 image; after M3 U~ as four SW64 slices [64 x 32] (the record's)
-constexpr uint32_t G_T = 131072;    // T image [64 x 64]; after M6 the N image
+constexpr uint32_t G_T = 131072;    // T image [64 x 64]; after M5 (dA) the N image
 constexpr uint32_t G_W = 139264;    // W image [64 x 128] (read again by M5)
 constexpr uint32_t G_P = 155648;    // P image [64 x 64]; later dSk image
 constexpr uint32_t G_KB = 163840;   // Kbar image [64 x 128]; later dU, then T^T dU images
@@ -724,7 +724,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
         }
         sync_for_mma();
 
-        // ------------------------------------------------------------ M7: dK^ += N K
+        // ------------------------------------------------------------ M6: dK^ += N K
         if (tid == 0) {
             tc_fence_after();
             for (int k0 = 0; k0 < kChunk; k0 += 16)
@@ -732,7 +732,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
                     true);
             mma_commit(&bar_mma);
         }
-        if (tid < 256) {  // column sums of dA-Z (while M7 runs)
+        if (tid < 256) {  // column sums of dA-Z (while M6 runs)
             const int j = tid & 63, part4 = tid >> 6;
             float s = 0.f;
 #pragma unroll
@@ -773,7 +773,7 @@ __global__ void __launch_bounds__(GRAD_THREADS, 1)
             }
         }
         if (!wait_mma(49)) goto teardown;
-        if (more && tid == 0) prefetch(3);  // T: its buffer held N, read by M7
+        if (more && tid == 0) prefetch(3);  // T: its buffer held N, read by M6
         if (last_head && tid == 0 && nunit < nunits) issue_kq(nb, nc, nhk, gfz);  // GF / ZS are free now
     }
 

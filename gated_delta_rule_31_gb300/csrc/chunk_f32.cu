@@ -235,14 +235,35 @@ __global__ void __launch_bounds__(kScanThreads) scan32_kernel(Chunk32Args A) {
         const int c = MODE == 2 ? A.NC - 1 - step : step;
         const int t0 = c * C, n = min(C, A.T - t0);
         const float* rec = A.rec + (bh * A.NC + c) * ro.n;
-        for (int i = tid; i < C * K; i += kScanThreads) {
-            const int r = i / K, d = i % K;
-            sW[r * KS + d] = rec[ro.W + i];
-            sKb[r * KS + d] = rec[ro.Kb + i];
-            if (MODE != 1) sQg[r * KS + d] = rec[ro.Qg + i];
+        if (tid == 0 && step + 1 < A.NC) {  // the next step's record into L2 while this one is read
+            const int cn = MODE == 2 ? c - 1 : c + 1;
+            const float* nrec = A.rec + (bh * A.NC + cn) * ro.n;
+            for (int o = 0; o < 3 * C * K; o += 8192)  // W, Kbar, Qg
+                bulk_prefetch_l2(nrec + o, (uint32_t)min(8192, 3 * C * K - o) * 4);
+            bulk_prefetch_l2(nrec + ro.Gm + (C - 1) * K, K * 4);
+            bulk_prefetch_l2(nrec + ro.Ut, (C * V + C * C) * 4);  // U~ and P
+        }
+        for (int i4 = tid; i4 < C * K / 4; i4 += kScanThreads) {  // 16-byte loads, padded rows in smem
+            const int i = 4 * i4, r = i / K, d = i % K;
+            const float4 w = *reinterpret_cast<const float4*>(rec + ro.W + i);
+            const float4 kb = *reinterpret_cast<const float4*>(rec + ro.Kb + i);
+            float* pw = sW + r * KS + d;
+            float* pk = sKb + r * KS + d;
+            pw[0] = w.x; pw[1] = w.y; pw[2] = w.z; pw[3] = w.w;
+            pk[0] = kb.x; pk[1] = kb.y; pk[2] = kb.z; pk[3] = kb.w;
+            if (MODE != 1) {
+                const float4 q = *reinterpret_cast<const float4*>(rec + ro.Qg + i);
+                float* pq = sQg + r * KS + d;
+                pq[0] = q.x; pq[1] = q.y; pq[2] = q.z; pq[3] = q.w;
+            }
         }
         if (MODE != 1)
-            for (int i = tid; i < C * C; i += kScanThreads) sP[(i / C) * CS + i % C] = rec[ro.P + i];
+            for (int i4 = tid; i4 < C * C / 4; i4 += kScanThreads) {
+                const int i = 4 * i4;
+                const float4 x = *reinterpret_cast<const float4*>(rec + ro.P + i);
+                float* pp = sP + (i / C) * CS + i % C;
+                pp[0] = x.x; pp[1] = x.y; pp[2] = x.z; pp[3] = x.w;
+            }
         for (int d = tid; d < K; d += kScanThreads) sGc[d] = expf(rec[ro.Gm + (C - 1) * K + d]);
         for (int i = tid; i < C * R; i += kScanThreads) {
             const int r = i / R, w = i % R;

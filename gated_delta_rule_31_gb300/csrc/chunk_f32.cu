@@ -214,15 +214,16 @@ __global__ void __launch_bounds__(kScanThreads) scan32_kernel(Chunk32Args A) {
     const int hv = blockIdx.y, b = blockIdx.z, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int v0 = blockIdx.x * R, v = v0 + warp;
     const size_t bh = (size_t)b * A.Hv + hv;
-    float* sW = sm;               // [C][KS]
-    float* sKb = sW + C * KS;     // [C][KS]
-    float* sQg = sKb + C * KS;    // [C][KS]
-    float* sP = sQg + C * KS;     // [C][CS]
-    float* sGc = sP + C * CS;     // [K] Gamma_C
-    float* sX = sGc + K;          // [C][R] U~ (forward) or dO (reverse) columns of the CTA's rows
+    // What a mode does not use takes no room: the reverse scan reads P from the record (L2) and
+    // keeps no outputs, so two of its CTAs share an SM and its grid is one wave.
+    float* sW = sm;                                // [C][KS]
+    float* sKb = sW + C * KS;                      // [C][KS]
+    float* sQg = sKb + C * KS;                     // [C][KS] (forward with outputs, reverse)
+    float* sP = sQg + (MODE != 1 ? C * KS : 0);    // [C][CS] (forward with outputs)
+    float* sX = sP + (MODE == 0 ? C * CS : 0);    // [C][R] U~ (forward) or dO (reverse) columns of the rows
     float* sS = sX + C * R;       // [R][K] state (gradient) rows
     float* sU = sS + R * K;       // [R][C] u or du per row
-    float* sO = sU + R * C;       // [C][R] outputs
+    float* sO = sU + R * C;       // [C][R] outputs (forward with outputs)
     const RecOff ro = rec_off(K, V);
     const int M = K / 32;
     float s[4];
@@ -257,14 +258,15 @@ __global__ void __launch_bounds__(kScanThreads) scan32_kernel(Chunk32Args A) {
                 pq[0] = q.x; pq[1] = q.y; pq[2] = q.z; pq[3] = q.w;
             }
         }
-        if (MODE != 1)
+        if (MODE == 0)
             for (int i4 = tid; i4 < C * C / 4; i4 += kScanThreads) {
                 const int i = 4 * i4;
                 const float4 x = *reinterpret_cast<const float4*>(rec + ro.P + i);
                 float* pp = sP + (i / C) * CS + i % C;
                 pp[0] = x.x; pp[1] = x.y; pp[2] = x.z; pp[3] = x.w;
             }
-        for (int d = tid; d < K; d += kScanThreads) sGc[d] = expf(rec[ro.Gm + (C - 1) * K + d]);
+        float gc[4];  // Gamma_C of this lane's state columns
+        for (int m = 0; m < M; m++) gc[m] = expf(rec[ro.Gm + (C - 1) * K + lane + 32 * m]);
         for (int i = tid; i < C * R; i += kScanThreads) {
             const int r = i / R, w = i % R;
             if (MODE == 2)
@@ -296,12 +298,13 @@ __global__ void __launch_bounds__(kScanThreads) scan32_kernel(Chunk32Args A) {
                 const int d = lane + 32 * m;
                 float acc = 0.f;
                 for (int i = 0; i < C; i++) acc += sKb[i * KS + d] * urow[i];
-                s[m] = sGc[d] * s[m] + acc;
+                s[m] = gc[m] * s[m] + acc;
             }
         } else {
+            const float* prec = rec + ro.P;  // P [C][C] row-major: lanes read a row's consecutive entries
             for (int i = lane; i < C; i += 32) {  // du = P^T do + Kbar ds
                 float acc = 0.f;
-                for (int j = i; j < C; j++) acc += sP[j * CS + i] * sX[j * R + warp];
+                for (int j = i; j < C; j++) acc += prec[j * C + i] * sX[j * R + warp];
                 for (int d = 0; d < K; d++) acc += sKb[i * KS + d] * srow[d];
                 urow[i] = acc;
             }
@@ -310,7 +313,7 @@ __global__ void __launch_bounds__(kScanThreads) scan32_kernel(Chunk32Args A) {
                 const int d = lane + 32 * m;
                 float acc = 0.f;
                 for (int i = 0; i < C; i++) acc += sQg[i * KS + d] * sX[i * R + warp] - sW[i * KS + d] * urow[i];
-                s[m] = sGc[d] * s[m] + acc;
+                s[m] = gc[m] * s[m] + acc;
             }
         }
         __syncthreads();
@@ -582,9 +585,10 @@ size_t chunk32_saved_bytes(int B, int T, int Hv, int Dk, int Dv) {
 
 namespace {
 size_t prep_smem(int K, int V) { return (size_t)(3 * C * (K + 1) + C * (V + 1) + 2 * C * (C + 1) + 3 * C) * 4; }
-size_t scan_smem(int K) {
+size_t scan_smem(int K, int mode) {  // the carve-up of scan32_kernel<mode>
     const int R = kRowsPerCta;
-    return (size_t)(3 * C * (K + 1) + C * (C + 1) + K + C * R + R * K + R * C + C * R) * 4;
+    const int ops = (mode == 1 ? 2 : 3) * C * (K + 1) + (mode == 0 ? C * (C + 1) : 0);
+    return (size_t)(ops + C * R + R * K + R * C + (mode == 0 ? C * R : 0)) * 4;
 }
 cudaError_t run_prep(const Chunk32Args& a, cudaStream_t s) {
     const size_t smem = prep_smem(a.Dk, a.Dv);
@@ -597,7 +601,7 @@ cudaError_t run_prep(const Chunk32Args& a, cudaStream_t s) {
 }
 template <int MODE>
 cudaError_t run_scan(const Chunk32Args& a, cudaStream_t s) {
-    const size_t smem = scan_smem(a.Dk);
+    const size_t smem = scan_smem(a.Dk, MODE);
     cudaError_t e = cudaFuncSetAttribute(scan32_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     trace_begin(MODE == 0 ? "chunk32_scan_fwd" : MODE == 1 ? "chunk32_scan_states" : "chunk32_scan_bwd", s);

@@ -40,7 +40,7 @@ namespace {
 
 constexpr int C = kChunk;
 constexpr int kThreads = 256;
-constexpr int kGradCtas = 256;  // persistent grad CTAs, one scratch slot each
+constexpr int kGradCtas = 304;  // persistent grad CTAs, one scratch slot each: two per SM of a GB300
 
 // Record of one (b, value head, chunk), fp32, row-major; offsets in floats.
 struct RecOff {
